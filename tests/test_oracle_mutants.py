@@ -1,0 +1,44 @@
+"""Plant plausible mistakes in a copy of the oracle; the pins must catch every one.
+
+Each mutant is the oracle's C source with one edit (an off-by-one mask, a
+dropped scale, a flipped sign, a wrong index...).  It is compiled on the CPU
+into a temporary library and run against every pin; at least one pin must
+fail.  The committed oracle itself is never modified.
+"""
+import os
+
+import pytest
+
+import oracle
+import oracle_pins
+
+MUTANTS = {
+    "causal_includes_diagonal": ("j > i) return 0", "j >= i) return 0"),
+    "padding_off_by_one": ("j >= len_b) return 0", "j > len_b) return 0"),
+    "scale_dropped": ("w[j] = scale * dot;", "w[j] = dot;"),
+    "exponent_sign_flipped": ("w[j] = exp(w[j] - mu);", "w[j] = exp(mu - w[j]);"),
+    "not_normalised": ("double p = w[j] / Z;", "double p = w[j];"),
+    "keys_reversed": ("dot += q[c] * Kh[j * d + c];", "dot += q[c] * Kh[(n - 1 - j) * d + c];"),
+    "values_reversed": ("o[c] += p * Vh[j * d + c];", "o[c] += p * Vh[(n - 1 - j) * d + c];"),
+    "query_row_of_first_position": ("const double *q = Q + r * d;", "const double *q = Q + bh * m * d;"),
+    "length_of_wrong_batch": ("int64_t b = bh / h;", "int64_t b = (bh / h + 1) % B;"),
+    "length_not_clamped": ("if (len > n) len = n;", "if (len > n) len = n - 1;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(oracle.SOURCE).read()
+    assert src.count(old) == 1, f"mutation anchor {old!r} not found exactly once"
+    path = tmp_path / "mutant.c"
+    path.write_text(src.replace(old, new))
+    lib = oracle.compile_oracle(str(path), str(tmp_path / "libmutant.so"), openmp=False)
+    mutant = oracle.load(lib)
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(mutant)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"mutant {name} passed every pin"
