@@ -1,0 +1,404 @@
+#!/usr/bin/env python
+"""Benchmark: masked multi-head attention forward TFLOPS on GB300.
+
+Default workload: long causal self-attention, bf16, B=4 h=16 n=m=8192 d_k=64
+(the workload the throughput target is stated on).  One step = one attn_fwd
+call over the whole batch (every step of the hot path runs in that one
+kernel launch).  Inputs: 3 x 64 MiB + 64 MiB output = 268 MB, larger than the
+126 MB L2, so consecutive steps cannot serve each other from L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  Under torchrun each rank runs its own full
+batch (independent (batch, head) work, no collective on the data path) and
+the time is the max over ranks: weak scaling.
+
+--impl reference times the fp64 CPU oracle on the host cores instead, on a
+bounded sample of query rows of the same workload per step (the pages have no
+GPU implementation to compare against).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from workloads import WORKLOADS, draw  # noqa: E402
+
+METRIC = "masked MHA fwd TFLOPS on 1 GB300 (and % of bf16 tensor peak / HBM GB/s)"
+UNIT = "TFLOPS"
+
+
+def nominal_flops(w) -> float:
+    """4 * B * h * m * n * d_k, halved for a causal mask (the headline formula)."""
+    f = 4.0 * w.B * w.h * w.m * w.n * w.d
+    return f / 2 if w.causal else f
+
+
+def allowed_pairs(w, lengths) -> float:
+    """Number of (query, key) pairs the mask allows, summed over batch and heads."""
+    total = 0.0
+    for b in range(w.B):
+        L = w.n if not w.padded else max(0, min(int(lengths[b]), w.n))
+        if w.causal:
+            # keys j <= i and j < L, for i in [0, m)
+            total += sum(min(i + 1, L) for i in range(w.m))
+        else:
+            total += w.m * L
+    return total * w.h
+
+
+def useful_flops(w, lengths) -> float:
+    """4 * d_k per allowed pair (2 d_k for Q K^T, 2 d_k for P V)."""
+    return 4.0 * w.d * allowed_pairs(w, lengths)
+
+
+def algorithmic_bytes(w, lengths) -> float:
+    """Q and O once, K and V once up to the allowed length per (batch)."""
+    esz = 2 if w.dtype == "bf16" else 4
+    kv_rows = 0
+    for b in range(w.B):
+        L = w.n if not w.padded else max(0, min(int(lengths[b]), w.n))
+        kv_rows += L
+    return esz * w.d * (2 * w.B * w.h * w.m + 2 * w.h * kv_rows)
+
+
+def row_pairs(w, lengths, rows) -> float:
+    """Allowed (query, key) pairs of the given linear output rows ((b*h + head)*m + i)."""
+    rows = np.asarray(rows, dtype=np.int64)
+    i = rows % w.m
+    b = (rows // w.m) // w.h
+    L = np.clip(np.asarray(lengths, dtype=np.int64)[b], 0, w.n) if w.padded else np.full(rows.shape, w.n)
+    return float((np.minimum(i + 1, L) if w.causal else L).sum())
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 1900.0, 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for _, _, flags in rows for k, f in enumerate(flags) if f.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def to_device(x, dtype, torch, device):
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(np.ascontiguousarray(x)).to(device)
+
+
+def time_launches(fn, steps, torch, stream):
+    """Average device time of `steps` calls of fn on `stream`, CUDA events on that stream."""
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / steps
+
+
+def short_workloads(torch, attn, device, peak_hbm):
+    """Per-launch time of the memory-bound workloads (and the fp32 one) with
+    input sets rotated so their total exceeds twice the L2 size; launches are
+    captured in a CUDA graph so the figure is device time, not launch latency."""
+    props = torch.cuda.get_device_properties(device)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
+    res = {}
+    for cfg in (1, 2, 3, 4):
+        w = WORKLOADS[cfg]
+        inp = draw(w)
+        esz = 2 if w.dtype == "bf16" else 4
+        set_bytes = esz * w.d * (2 * w.B * w.h * w.m + 2 * w.B * w.h * w.n)
+        copies = max(1, min(64, int(np.ceil(2 * l2 / set_bytes))))
+        sets = []
+        for _ in range(copies):
+            q, k, v = (to_device(x, w.dtype, torch, device) for x in (inp.q, inp.k, inp.v))
+            lens = torch.from_numpy(inp.key_lengths).to(device)
+            sets.append((q, k, v, lens, torch.empty_like(q)))
+        kern = attn.select_kernel(w.B, w.h, w.m, w.n, w.d, 0 if w.dtype == "bf16" else 1, w.mask)
+        stream = torch.cuda.Stream(device)
+        with torch.cuda.stream(stream):
+            for s in sets:
+                attn.attn_fwd(s[0], s[1], s[2], s[3], w.mask, w.scale, out=s[4], stream=stream)
+            stream.synchronize()
+            reps = max(1, 200 // copies)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(reps):
+                    for s in sets:
+                        attn.attn_fwd(s[0], s[1], s[2], s[3], w.mask, w.scale, out=s[4], stream=stream)
+            g.replay()
+            stream.synchronize()
+            times = []
+            for _ in range(5):
+                t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                t0.record(stream)
+                g.replay()
+                t1.record(stream)
+                t1.synchronize()
+                times.append(t0.elapsed_time(t1) / (reps * copies))
+        ms = statistics.median(times)
+        nb = algorithmic_bytes(w, inp.key_lengths)
+        res[w.name] = {
+            "kernel": attn._native.KERNEL_NAMES[kern], "us_per_launch": ms * 1e3,
+            "tflops_nominal": nominal_flops(w) / (ms * 1e-3) / 1e12,
+            "tflops_useful": useful_flops(w, inp.key_lengths) / (ms * 1e-3) / 1e12,
+            "hbm_gbs_algorithmic": nb / (ms * 1e-3) / 1e9,
+            "hbm_frac": nb / (ms * 1e-3) / 1e9 / peak_hbm,
+            "input_sets": copies, "launches_timed": reps * copies * 5,
+        }
+        del sets, g
+        torch.cuda.empty_cache()
+    return res
+
+
+def cpu_oracle_sample(w, inp, target_s, seed=3):
+    """Time the fp64 oracle on random query rows of w for about target_s seconds."""
+    import oracle
+    orc = oracle.load()
+    qd, kd, vd = orc.widen(inp.q), orc.widen(inp.k), orc.widen(inp.v)
+    rng = np.random.default_rng(seed)
+    total_rows = w.B * w.h * w.m
+
+    probe = rng.integers(0, total_rows, size=16)
+    t0 = time.perf_counter()
+    orc.attn_rows(qd, kd, vd, inp.key_lengths, w.mask, w.scale, probe, widened=True)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    count = int(np.clip(16 * target_s / dt, 16, total_rows))
+    rows = rng.integers(0, total_rows, size=count)
+    t0 = time.perf_counter()
+    orc.attn_rows(qd, kd, vd, inp.key_lengths, w.mask, w.scale, rows, widened=True)
+    el = time.perf_counter() - t0
+    flops = 4.0 * w.d * row_pairs(w, inp.key_lengths, rows)
+    return {"value": flops / el / 1e12, "unit": UNIT, "cores": orc.num_threads(), "kind": "oracle",
+            "sample": f"{count} random query rows of {w.description} ({el:.1f} s, fp64, "
+                      f"{flops / 1e9:.1f} GFLOP useful)", "seconds": el}, (orc, qd, kd, vd)
+
+
+def run_reference(args, w):
+    """--impl reference: the fp64 CPU oracle, one bounded row sample per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    inp = draw(w)
+    orc = oracle.load()
+    qd, kd, vd = orc.widen(inp.q), orc.widen(inp.k), orc.widen(inp.v)
+    rng = np.random.default_rng(11)
+    total_rows = w.B * w.h * w.m
+    # size each step so the whole run stays within about two minutes
+    probe = rng.integers(0, total_rows, size=8)
+    t0 = time.perf_counter()
+    orc.attn_rows(qd, kd, vd, inp.key_lengths, w.mask, w.scale, probe, widened=True)
+    per_row = max((time.perf_counter() - t0) / 8, 1e-6)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    rows_per_step = int(np.clip(budget / per_row, 1, 4096))
+    for _ in range(args.warmup):
+        orc.attn_rows(qd, kd, vd, inp.key_lengths, w.mask, w.scale,
+                      rng.integers(0, total_rows, size=rows_per_step), widened=True)
+    flops = 0.0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        rows = rng.integers(0, total_rows, size=rows_per_step)
+        orc.attn_rows(qd, kd, vd, inp.key_lengths, w.mask, w.scale, rows, widened=True)
+        flops += 4.0 * w.d * row_pairs(w, inp.key_lengths, rows)
+    el = time.perf_counter() - t0
+    value = flops / el / 1e12
+    sample = f"{rows_per_step} random query rows per step of {w.description}"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.description, "B": w.B, "h": w.h, "m": w.m, "n": w.n,
+                                        "d_k": w.d, "mask": w.mask},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": orc.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=5, choices=sorted(WORKLOADS))
+    ap.add_argument("--kernel-only", action="store_true",
+                    help="time only the main kernel loop (for profiler runs)")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    w = WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import torch
+    import transformer_scaled_dot_masked_gb300 as attn
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    inp = draw(w)  # every rank processes a full batch of its own (weak scaling)
+    q, k, v = (to_device(x, w.dtype, torch, device) for x in (inp.q, inp.k, inp.v))
+    lens = torch.from_numpy(inp.key_lengths).to(device)
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream(device)
+    kern = attn.select_kernel(w.B, w.h, w.m, w.n, w.d, 0 if w.dtype == "bf16" else 1, w.mask)
+
+    def step():
+        attn.attn_fwd(q, k, v, lens, w.mask, w.scale, out=out, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        ms = time_launches(step, args.steps, torch, stream)
+    torch.cuda.synchronize()
+    if dist:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+    st, info = attn.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} (info {info}) after the timed loop")
+
+    peak_tf, peak_hbm, peak_src = load_peaks()
+    flops_nom = nominal_flops(w)
+    value = flops_nom * world / (ms * 1e-3) / 1e12
+    flops_use = useful_flops(w, inp.key_lengths)
+    achieved = flops_use / (ms * 1e-3) / 1e12
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.description, "B": w.B, "h": w.h, "m": w.m, "n": w.n, "d_k": w.d,
+                   "mask": "causal" if w.causal else ("key_padding" if w.padded else "none"),
+                   "kernel": attn._native.KERNEL_NAMES[kern],
+                   "l2": "inputs+output 268 MB > L2, no flush between steps",
+                   "parallelism": f"replicas x{world} ((batch, head) work is independent)"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tf, "traffic": None,
+                     "peak_source": f"{peak_src} bf16 dense burst",
+                     "algorithmic": "4*d_k FLOPs per allowed (query, key) pair per launch"},
+        "gpu_launches": args.steps,
+    }
+    result["clocks"] = clk.summary()
+
+    if not args.kernel_only:
+        # end to end through the public API: pinned host inputs in, host output back, every step
+        hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
+        hl = lens.cpu().pin_memory()
+        ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        dq, dk, dv, dl, do = (torch.empty_like(x) for x in (q, k, v, lens, out))
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            dl.copy_(hl, non_blocking=True)
+            attn.attn_fwd(dq, dk, dv, dl, w.mask, w.scale, out=do, stream=stream)
+            ho.copy_(do, non_blocking=True)
+
+        e2e_steps = max(3, min(args.steps, 50))
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        ems = time_launches(e2e_step, e2e_steps, torch, stream)
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hl))
+        result["e2e"] = {"value": flops_nom * world / (ems * 1e-3) / 1e12, "unit": UNIT,
+                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": ho.numel() * ho.element_size(),
+                         "ms_per_step": ems, "steps": e2e_steps}
+        result["gpu_launches"] = args.steps  # e2e launches are outside the device-timed region
+        result["other_workloads"] = short_workloads(torch, attn, device, peak_hbm)
+        if rank == 0:
+            cb, _ = cpu_oracle_sample(w, inp, args.cpu_seconds)
+            cb.pop("seconds", None)
+            result["cpu_baseline"] = cb
+
+    if rank == 0:
+        print(json.dumps(result))
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

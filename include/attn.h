@@ -1,0 +1,160 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) masked scaled dot-product attention library.
+ *
+ * The library computes, for every batch b, head h and query row i,
+ *
+ *     out[b,h,i,:] = softmax_j( scale * Q[b,h,i,:] . K[b,h,j,:] + M[b,i,j] ) V[b,h,j,:]
+ *
+ * which is the attention equation of "Paper Deep Reading: Attention Is All
+ * You Need", §04 Attention mechanics (softmax(Q K^T / sqrt(d_k) + M) V), run
+ * for every head of multi-head attention at once (the head_i terms of the
+ * same section's MultiHead equation, and the slide deck's "Multi-Head
+ * Attention" slide).  The additive mask M is 0 where attention is allowed and
+ * -inf where it is not:
+ *   - ATTN_MASK_KEY_PADDING: key j of batch b is masked iff j >= key_lengths[b]
+ *     ("the encoder mainly masks padding", §04);
+ *   - ATTN_MASK_CAUSAL: key j is masked for query i iff j > i (the decoder's
+ *     masked self-attention; §03 "Decoder layer" sets illegal future
+ *     connections to -inf before the softmax);
+ *   - both flags together: the union of both masked sets.
+ * A query row with no allowed key is written as 0.
+ *
+ * The three uses named on the slide deck ("Three Applications of Attention")
+ * map to: encoder self-attention (m == n, key padding), decoder
+ * self-attention (m == n, causal) and encoder-decoder attention (m queries
+ * from the decoder, n keys/values from the encoder, key padding).
+ *
+ * Layout: Q is [B][h][m][d_k], K and V are [B][h][n][d_k], out is
+ * [B][h][m][d_k], all dense row-major with d_k fastest (d_v == d_k), in
+ * device memory of the current CUDA device.  key_lengths is int32 [B] in
+ * device memory.
+ *
+ * Ownership: the caller allocates and owns every buffer.  The library keeps
+ * no per-call state and allocates no device memory; the only global state is
+ * a small device status word that records a kernel giving up a bounded wait.
+ *
+ * Asynchrony: every compute entry point only enqueues work on the given
+ * stream (a cudaStream_t; NULL is the legacy default stream) and returns.  A
+ * status other than ATTN_OK means nothing was enqueued.  Buffers must stay
+ * valid until the stream has executed the work.  `out` must not overlap Q, K,
+ * V or key_lengths.  Calls that overlap on the GPU may share inputs freely.
+ *
+ * Errors are reported through the return value; no function aborts, prints
+ * or throws.
+ */
+#ifndef ATTN_GB300_ATTN_H
+#define ATTN_GB300_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_NULL = 1,           /* a required pointer is NULL */
+    ATTN_ERR_SHAPE = 2,          /* B, h, m, n out of range, or causal with m != n */
+    ATTN_ERR_DTYPE = 3,          /* unknown dtype, or d_k not supported for that dtype */
+    ATTN_ERR_MASK = 4,           /* mask_kind has bits other than KEY_PADDING | CAUSAL */
+    ATTN_ERR_ALIGN = 5,          /* a tensor pointer is not 16-byte aligned */
+    ATTN_ERR_UNSUPPORTED = 6,    /* the kernel asked for cannot run this call */
+    ATTN_ERR_CUDA = 7,           /* a CUDA runtime call failed (device query, launch) */
+    ATTN_ERR_DEVICE_TIMEOUT = 8, /* a kernel gave up a bounded wait (see attn_device_status) */
+    ATTN_ERR_VALUE = 9,          /* scale is negative or not finite */
+    ATTN_ERR_ALIAS = 10          /* out overlaps Q, K, V or key_lengths */
+} attn_status;
+
+typedef enum {
+    ATTN_MASK_NONE = 0,
+    ATTN_MASK_KEY_PADDING = 1,
+    ATTN_MASK_CAUSAL = 2
+} attn_mask_kind; /* bit flags: 3 = key padding and causal */
+
+typedef enum {
+    ATTN_BF16 = 0, /* bf16 in and out; fp32 accumulation and softmax state */
+    ATTN_FP32 = 1  /* fp32 in and out; fp32 arithmetic throughout (no TF32) */
+} attn_dtype;
+
+typedef enum {
+    ATTN_KERNEL_AUTO = 0,  /* let the library choose (what attn_fwd does) */
+    ATTN_KERNEL_FLASH = 1, /* tcgen05/TMA flash kernel, 256 query rows per CTA tile (bf16, d_k == 64) */
+    ATTN_KERNEL_SHORT = 2, /* same machinery, two heads per CTA tile, whole head resident (bf16, d_k == 64, m <= 128) */
+    ATTN_KERNEL_SIMT = 3   /* CUDA-core fp32 kernel (fp32 or bf16, d_k <= 64) */
+} attn_kernel;
+
+typedef struct {
+    int32_t B;     /* batch size, >= 1 */
+    int32_t h;     /* heads, >= 1 */
+    int32_t m;     /* query rows per (batch, head), >= 1 */
+    int32_t n;     /* key/value rows per (batch, head), >= 1 */
+    int32_t d_k;   /* head width (d_v == d_k), 1..64; the tensor-core kernels need 64 */
+    int32_t dtype; /* attn_dtype */
+} attn_dims;
+
+/*
+ * Masked scaled dot-product attention over all heads (see the top of this
+ * file for the formula, layout, ownership and asynchrony).
+ *
+ *   Q, K, V      device tensors, layout above, element type dims->dtype; 16-byte aligned
+ *   key_lengths  device int32 [B], 4-byte aligned; read only when mask_kind has
+ *                KEY_PADDING (may be NULL otherwise).  Values are clamped to [0, n]
+ *                on the device.
+ *   mask_kind    attn_mask_kind bits
+ *   scale        multiplies Q K^T; 1/sqrt(d_k) in the formula.  Must be finite and >= 0.
+ *   out          device tensor [B][h][m][d_k] of dims->dtype; 16-byte aligned
+ *   dims         shapes and dtype (host pointer)
+ *   stream       cudaStream_t to enqueue on (NULL = legacy default stream)
+ *
+ * Returns ATTN_OK once the work is enqueued.  Rejects (nothing enqueued):
+ * NULL pointers (ATTN_ERR_NULL), non-positive sizes or causal with m != n or
+ * sizes whose element counts overflow int64 (ATTN_ERR_SHAPE), unsupported
+ * dtype/d_k (ATTN_ERR_DTYPE), unknown mask bits (ATTN_ERR_MASK), unaligned
+ * pointers (ATTN_ERR_ALIGN), bad scale (ATTN_ERR_VALUE), `out` overlapping
+ * an input (ATTN_ERR_ALIAS), CUDA failures (ATTN_ERR_CUDA).  Inputs must be
+ * finite: non-finite values propagate through the arithmetic as IEEE rules
+ * dictate.  Kernel choice: bf16 with d_k == 64 runs on tensor cores
+ * (ATTN_KERNEL_SHORT when m <= 128, else ATTN_KERNEL_FLASH); everything else
+ * runs ATTN_KERNEL_SIMT.
+ */
+attn_status attn_fwd(const void *Q, const void *K, const void *V,
+                     const int32_t *key_lengths, int mask_kind, float scale,
+                     void *out, const attn_dims *dims, void *stream);
+
+/*
+ * attn_fwd with an explicit kernel choice (attn_kernel).  Same arguments,
+ * rules and errors as attn_fwd; additionally returns ATTN_ERR_UNSUPPORTED when
+ * the kernel asked for cannot run the call (for example ATTN_KERNEL_SHORT with
+ * m > 128, or a tensor-core kernel with fp32).  Lets tests and benchmarks run
+ * each kernel on the same inputs.
+ */
+attn_status attn_fwd_kernel(const void *Q, const void *K, const void *V,
+                            const int32_t *key_lengths, int mask_kind, float scale,
+                            void *out, const attn_dims *dims, void *stream,
+                            int kernel);
+
+/* The kernel attn_fwd would run for these dims and mask (host only, no CUDA call);
+ * ATTN_KERNEL_AUTO (0) if the call would be rejected. */
+int attn_select_kernel(const attn_dims *dims, int mask_kind);
+
+/*
+ * Synchronises `stream`, then reports whether any kernel of this library on
+ * the current device gave up a bounded wait since the previous call
+ * (ATTN_ERR_DEVICE_TIMEOUT; *info, if not NULL, receives a code naming the
+ * wait) or not (ATTN_OK).  Clears the record.  ATTN_ERR_CUDA if the
+ * synchronisation itself fails.  A kernel that gives up a wait stops early and
+ * leaves its output incomplete, but leaves the CUDA context usable.
+ */
+attn_status attn_device_status(void *stream, int32_t *info);
+
+/* Static description of a status code (never NULL). */
+const char *attn_status_string(int status);
+
+/* ABI version: (major << 16) | minor. */
+int32_t attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_ATTN_H */

@@ -1,0 +1,98 @@
+"""The C-ABI library on the host: it loads, exports what include/attn.h declares,
+and rejects bad arguments before touching the GPU (no compute calls here)."""
+import ctypes
+import re
+import subprocess
+
+import pytest
+
+import transformer_scaled_dot_masked_gb300 as attn
+from transformer_scaled_dot_masked_gb300 import _native as N
+
+HEADER_TEXT = open(N.HEADER).read()
+
+
+def _enum(name):
+    return int(re.search(rf"\b{name}\s*=\s*(\d+)", HEADER_TEXT).group(1))
+
+
+def test_library_exports_every_declared_function():
+    declared = N.header_exports()
+    assert set(declared) >= {"attn_fwd", "attn_fwd_kernel", "attn_select_kernel", "attn_device_status",
+                             "attn_status_string", "attn_version"}
+    out = subprocess.run(["nm", "-D", "--defined-only", N.LIBRARY], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT\s+(\w+)$", out, re.M))
+    missing = [f for f in declared if f not in exported]
+    assert not missing, f"declared in attn.h but not exported: {missing}"
+    for f in declared:
+        assert hasattr(N.lib, f)
+
+
+def test_python_constants_match_header():
+    assert N.ATTN_OK == _enum("ATTN_OK")
+    assert N.ATTN_ERR_DEVICE_TIMEOUT == _enum("ATTN_ERR_DEVICE_TIMEOUT")
+    assert (N.MASK_KEY_PADDING, N.MASK_CAUSAL) == (_enum("ATTN_MASK_KEY_PADDING"), _enum("ATTN_MASK_CAUSAL"))
+    assert (N.DTYPE_BF16, N.DTYPE_FP32) == (_enum("ATTN_BF16"), _enum("ATTN_FP32"))
+    assert (N.KERNEL_FLASH, N.KERNEL_SHORT, N.KERNEL_SIMT) == (
+        _enum("ATTN_KERNEL_FLASH"), _enum("ATTN_KERNEL_SHORT"), _enum("ATTN_KERNEL_SIMT"))
+    # the dims struct is six int32 fields in this order
+    fields = re.search(r"typedef struct \{(.*?)\} attn_dims;", HEADER_TEXT, re.S).group(1)
+    assert re.findall(r"int32_t (\w+);", fields) == [f for f, _ in N.AttnDims._fields_]
+
+
+def test_status_strings_and_version():
+    for code in range(0, 11):
+        s = N.status_string(code)
+        assert s and s != "unknown status"
+    assert N.status_string(99) == "unknown status"
+    assert N.lib.attn_version() >> 16 == 1
+
+
+def test_kernel_selection():
+    bf, f32 = N.DTYPE_BF16, N.DTYPE_FP32
+    assert attn.select_kernel(64, 8, 100, 100, 64, bf, 1) == N.KERNEL_SHORT
+    assert attn.select_kernel(32, 16, 128, 160, 64, bf, 1) == N.KERNEL_SHORT
+    assert attn.select_kernel(4, 16, 8192, 8192, 64, bf, 2) == N.KERNEL_FLASH
+    assert attn.select_kernel(1, 1, 16, 16, 64, f32, 0) == N.KERNEL_SIMT
+    assert attn.select_kernel(1, 1, 16, 16, 32, bf, 0) == N.KERNEL_SIMT
+    assert attn.select_kernel(1, 1, 16, 17, 64, bf, 2) == N.KERNEL_AUTO   # causal needs m == n
+    assert attn.select_kernel(1, 1, 16, 16, 65, bf, 0) == N.KERNEL_AUTO   # d_k > 64
+    assert attn.select_kernel(1, 1, 16, 16, 64, bf, 4) == N.KERNEL_AUTO   # unknown mask bit
+    assert attn.select_kernel(0, 1, 16, 16, 64, bf, 0) == N.KERNEL_AUTO
+
+
+# Fake 16-byte-aligned "device" addresses: validation rejects these calls before
+# any CUDA call is made, so nothing is ever dereferenced.
+A, B_, C, O, L = 0x1000000, 0x2000000, 0x3000000, 0x4000000, 0x5000000
+
+
+def _call(q=A, k=B_, v=C, lens=L, mask=0, scale=0.125, out=O, dims=(2, 2, 8, 8, 64, 0), kernel=0):
+    d = N.make_dims(*dims)
+    return N.fwd_raw(q, k, v, lens, mask, scale, out, d, None, kernel)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(q=None), 1), (dict(out=None), 1), (dict(lens=None, mask=1), 1),
+    (dict(dims=(0, 2, 8, 8, 64, 0)), 2), (dict(dims=(2, 2, 8, 0, 64, 0)), 2),
+    (dict(dims=(2, 2, 8, 9, 64, 0), mask=2), 2), (dict(dims=(70000, 1, 8, 8, 64, 0)), 2),
+    (dict(dims=(2, 2, 8, 8, 65, 0)), 3), (dict(dims=(2, 2, 8, 8, 0, 0)), 3), (dict(dims=(2, 2, 8, 8, 64, 7)), 3),
+    (dict(mask=4), 4), (dict(mask=-1), 4),
+    (dict(q=A + 8), 5), (dict(out=O + 4), 5), (dict(lens=L + 2, mask=1), 5),
+    (dict(scale=float("nan")), 9), (dict(scale=float("inf")), 9), (dict(scale=-0.5), 9),
+    (dict(out=A), 10), (dict(out=B_ + 64), 10), (dict(out=L - 16, mask=1), 10),
+])
+def test_rejects_bad_arguments(kwargs, status):
+    assert _call(**kwargs) == status
+
+
+def test_rejects_unsupported_kernel_choice():
+    # fp32 on a tensor-core kernel, SHORT with m > 128, unknown kernel id
+    assert _call(dims=(2, 2, 8, 8, 64, 1), kernel=N.KERNEL_FLASH) == 6
+    assert _call(dims=(2, 2, 200, 200, 64, 0), kernel=N.KERNEL_SHORT) == 6
+    assert _call(dims=(2, 2, 8, 8, 32, 0), kernel=N.KERNEL_SHORT) == 6
+    assert _call(kernel=17) == 6
+
+
+def test_null_dims():
+    assert N.lib.attn_fwd(A, B_, C, None, 0, ctypes.c_float(0.125), O, None, None) == 1

@@ -1,0 +1,203 @@
+"""GPU kernels against the fp64 oracle, element by element, on seeded inputs.
+
+Tolerances: max abs error <= 1e-2 for bf16 inputs/outputs, <= 1e-4 for the
+fp32 path.  Every kernel that can run a case is run on it.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import transformer_scaled_dot_masked_gb300 as attn
+from workloads import WORKLOADS, MASK_CAUSAL, MASK_KEY_PADDING, MASK_NONE, Workload, draw, sample_rows
+
+from gpu_helpers import as_f64, report, run, to_device, tol_for
+
+pytestmark = pytest.mark.gpu
+
+K_FLASH, K_SHORT, K_SIMT, K_AUTO = attn.KERNEL_FLASH, attn.KERNEL_SHORT, attn.KERNEL_SIMT, attn.KERNEL_AUTO
+
+
+def kernels_for(w: Workload):
+    ks = [K_SIMT]
+    if w.dtype == "bf16" and w.d == 64:
+        ks.append(K_FLASH)
+        if w.m <= 128:
+            ks.append(K_SHORT)
+    return ks
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.load()
+
+
+def check_full(orc, w, kernel, inp=None, scale=None):
+    inp = inp if inp is not None else draw(w)
+    got = as_f64(run(inp, kernel, scale=scale))
+    ref = orc.attn_fwd(inp.q, inp.k, inp.v, inp.key_lengths, w.mask, w.scale if scale is None else scale)
+    tol = tol_for(w)
+    assert np.abs(got - ref).max() <= tol, report(got, ref, tol)
+    return got, ref
+
+
+# ---------------------------------------------------------------- the reference workloads
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4])
+def test_workload_full(orc, cfg):
+    w = WORKLOADS[cfg]
+    inp = draw(w)
+    ref = orc.attn_fwd(inp.q, inp.k, inp.v, inp.key_lengths, w.mask, w.scale)
+    for kern in [K_AUTO] + kernels_for(w):
+        got = as_f64(run(inp, kern))
+        assert np.abs(got - ref).max() <= tol_for(w), f"kernel {kern}: " + report(got, ref, tol_for(w))
+
+
+def test_long_causal_sampled_rows(orc):
+    """n = m = 8192 causal at full size, in the launch configuration the benchmark times;
+    checked on sampled rows (tile edges of the first and last head plus random rows)."""
+    w = WORKLOADS[5]
+    inp = draw(w)
+    assert attn.select_kernel(w.B, w.h, w.m, w.n, w.d, 0, w.mask) == K_FLASH
+    got = as_f64(run(inp, K_AUTO)).reshape(-1, w.d)
+    rows = sample_rows(w, 1536)
+    ref = orc.attn_rows(inp.q, inp.k, inp.v, inp.key_lengths, w.mask, w.scale, rows)
+    assert np.abs(got[rows] - ref).max() <= 1e-2, report(got[rows], ref, 1e-2)
+    assert np.isfinite(got).all()
+    # every row of a softmax-weighted mean lies inside the hull of the value rows it averages
+    assert np.abs(got).max() <= 5.5
+
+
+# ---------------------------------------------------------------- ragged and edge shapes
+EDGE = [
+    # name, B, h, m, n, mask, lengths
+    ("causal_ragged_3tiles", 2, 3, 300, 300, MASK_CAUSAL, None),
+    ("causal_one_tile_pair_tail", 1, 2, 129, 129, MASK_CAUSAL, None),
+    ("cross_ragged", 2, 2, 200, 333, MASK_NONE, None),
+    ("cross_padding_long", 3, 2, 190, 700, MASK_KEY_PADDING, (0, 700)),
+    ("self_padding_causal", 3, 2, 260, 260, MASK_KEY_PADDING | MASK_CAUSAL, (1, 260)),
+    ("short_padding_odd_heads", 3, 3, 77, 150, MASK_KEY_PADDING, (0, 150)),
+    ("single_key", 2, 2, 50, 1, MASK_NONE, None),
+    ("single_query", 2, 2, 1, 500, MASK_KEY_PADDING, (1, 500)),
+    ("one_by_one_causal", 1, 1, 1, 1, MASK_CAUSAL, None),
+    ("exact_tiles_no_mask", 1, 2, 256, 256, MASK_NONE, None),
+]
+
+
+@pytest.mark.parametrize("name,B,h,m,n,mask,lengths", EDGE, ids=[e[0] for e in EDGE])
+def test_edge_shapes(orc, name, B, h, m, n, mask, lengths):
+    w = Workload(name, "bf16", B, h, m, n, 64, mask, 0.125, 4242, lengths)
+    inp = draw(w)
+    ref = orc.attn_fwd(inp.q, inp.k, inp.v, inp.key_lengths, w.mask, w.scale)
+    for kern in kernels_for(w):
+        got = as_f64(run(inp, kern))
+        assert np.abs(got - ref).max() <= 1e-2, f"kernel {kern}: " + report(got, ref, 1e-2)
+
+
+def test_zero_and_full_lengths(orc):
+    """len_b = 0 (no allowed key: output 0), 1 (output = V[0]), n, and out-of-range lengths."""
+    w = Workload("lengths", "bf16", 6, 2, 100, 140, 64, MASK_KEY_PADDING, 0.125, 77)
+    inp = draw(w)
+    inp.key_lengths[:] = [0, 1, 140, 129, -5, 1000]
+    ref = orc.attn_fwd(inp.q, inp.k, inp.v, inp.key_lengths, w.mask, w.scale)
+    for kern in kernels_for(w):
+        got = as_f64(run(inp, kern))
+        assert np.abs(got - ref).max() <= 1e-2, f"kernel {kern}: " + report(got, ref, 1e-2)
+        assert (got[0] == 0).all() and (got[4] == 0).all()
+        v0 = as_f64(to_device(inp.v, "bf16"))[1, :, :1]
+        np.testing.assert_array_equal(got[1], np.broadcast_to(v0, got[1].shape))
+
+
+@pytest.mark.parametrize("scale", [0.0, 1.0, 0.01, 0.35])
+def test_other_scales(orc, scale):
+    w = Workload("scales", "bf16", 2, 2, 160, 160, 64, MASK_CAUSAL, scale, 99)
+    for kern in kernels_for(w):
+        check_full(orc, w, kern)
+
+
+def test_fp32_path_shapes(orc):
+    for (m, n, d, mask) in [(16, 16, 64, 0), (33, 70, 17, 1), (50, 50, 64, 3), (5, 200, 2, 0)]:
+        w = Workload("fp32", "fp32", 2, 2, m, n, d, mask, d ** -0.5, 5, (0, n))
+        check_full(orc, w, K_SIMT)
+
+
+def test_worked_example_on_every_kernel():
+    """The primer's 2x2 example (scale 1) with d_k = 2 zero-padded to 64: zero
+    columns leave every score unchanged.  bf16 holds 1, -1, 5 exactly."""
+    import json, os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "worked_sdpa_2x2.json")))
+    for dtype, kernels in (("bf16", [K_FLASH, K_SHORT, K_SIMT]), ("fp32", [K_SIMT])):
+        tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+        q = torch.zeros(1, 1, 2, 64, dtype=tdt, device="cuda")
+        k, v = torch.zeros_like(q), torch.zeros_like(q)
+        q[0, 0, :, :2] = torch.tensor(g["Q"], dtype=tdt)
+        k[0, 0, :, :2] = torch.tensor(g["K"], dtype=tdt)
+        v[0, 0, :, :2] = torch.tensor(g["V"], dtype=tdt)
+        for kern in kernels:
+            out = attn.attn_fwd(q, k, v, None, 0, 1.0, kernel=kern).float().cpu().numpy()[0, 0]
+            # printed precision 0.005 plus bf16 output rounding of 4.4 (half-ulp 0.0156)
+            tol = 0.005 + (0.016 if dtype == "bf16" else 1e-4)
+            np.testing.assert_allclose(out[:, :2], g["printed"]["output"], atol=tol)
+            assert (out[:, 2:] == 0).all()
+
+
+# ---------------------------------------------------------------- invariants
+@pytest.mark.parametrize("cfg", [2, 3, 4])
+def test_masked_keys_do_not_matter_bitwise(cfg):
+    """Changing K/V rows that the mask hides leaves the output bit-identical."""
+    w = WORKLOADS[cfg].with_(B=8)
+    inp = draw(w)
+    for kern in kernels_for(w):
+        base = run(inp, kern).clone()
+        k2, v2 = inp.k.copy(), inp.v.copy()
+        rng = np.random.default_rng(1)
+        for b in range(w.B):
+            if w.padded:
+                L = inp.key_lengths[b]
+                k2[b, :, L:] = rng.integers(0, 2 ** 14, size=k2[b, :, L:].shape, dtype=np.uint16)
+                v2[b, :, L:] = rng.integers(0, 2 ** 14, size=v2[b, :, L:].shape, dtype=np.uint16)
+        if w.causal:
+            # for causal, perturb keys after a query row: compare rows up to it
+            cut = 37
+            k2[:, :, cut + 1:] ^= 0x0101
+            v2[:, :, cut + 1:] ^= 0x0101
+        inp2 = type(inp)(w, inp.q, k2, v2, inp.key_lengths)
+        got = run(inp2, kern)
+        if w.causal:
+            assert torch.equal(got[:, :, :cut + 1], base[:, :, :cut + 1])
+            assert not torch.equal(got, base)
+        else:
+            assert torch.equal(got, base)
+
+
+def test_rows_sum_to_one_on_gpu():
+    """With V = 1 everywhere every output is 1 (bf16: within 4e-3)."""
+    w = WORKLOADS[3].with_(B=4, m=300, n=300)
+    inp = draw(w)
+    one = np.uint16(0x3F80)  # bf16 1.0
+    inp.v[...] = one
+    for kern in kernels_for(w):
+        got = as_f64(run(inp, kern))
+        assert np.abs(got - 1.0).max() <= 4e-3
+
+
+def test_deterministic_bitwise():
+    for cfg in (3, 4):
+        w = WORKLOADS[cfg]
+        inp = draw(w)
+        for kern in kernels_for(w):
+            a = run(inp, kern).clone()
+            b = run(inp, kern)
+            assert torch.equal(a, b)
+
+
+def test_no_writes_outside_out():
+    """Guard bands around `out` keep their sentinel bytes."""
+    w = WORKLOADS[4].with_(B=3, m=100)
+    inp = draw(w)
+    for kern in kernels_for(w):
+        n_out = w.B * w.h * w.m * w.d
+        guard = 4096
+        buf = torch.full((n_out + 2 * guard,), -7.0, dtype=torch.bfloat16, device="cuda")
+        out = buf[guard:guard + n_out].view(w.B, w.h, w.m, w.d)
+        run(inp, kern, out=out)
+        assert (buf[:guard] == -7.0).all() and (buf[guard + n_out:] == -7.0).all()

@@ -1,0 +1,78 @@
+"""GB300 (sm_103a) masked scaled dot-product multi-head attention.
+
+    out = attn_fwd(q, k, v, key_lengths, mask_kind, scale)
+
+computes softmax(scale * Q K^T + M) V for every (batch, head) on the GPU
+through the C ABI in ``include/attn.h`` ("Paper Deep Reading: Attention Is All
+You Need", §04 attention equation with the additive mask M).  Importing the
+package fails when the CUDA library has not been built.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+from . import _native
+from ._native import (AttnError, KERNEL_AUTO, KERNEL_FLASH, KERNEL_SHORT, KERNEL_SIMT, MASK_CAUSAL,
+                      MASK_KEY_PADDING, MASK_NONE, DTYPE_BF16, DTYPE_FP32)
+
+__all__ = ["attn_fwd", "AttnError", "select_kernel", "device_status", "MASK_NONE", "MASK_KEY_PADDING",
+           "MASK_CAUSAL", "KERNEL_AUTO", "KERNEL_FLASH", "KERNEL_SHORT", "KERNEL_SIMT"]
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if t.dtype == torch.float32:
+        return DTYPE_FP32
+    raise TypeError(f"attn_fwd supports bfloat16 and float32 tensors, got {t.dtype}")
+
+
+def attn_fwd(q, k, v, key_lengths=None, mask_kind: int = MASK_NONE, scale: Optional[float] = None,
+             out=None, kernel: int = KERNEL_AUTO, stream=None):
+    """Masked scaled dot-product attention over [B, h, len, d_k] CUDA tensors.
+
+    q: [B, h, m, d_k]; k, v: [B, h, n, d_k]; same dtype (bf16 or fp32), contiguous,
+    on the current CUDA device.  key_lengths: int32 [B] CUDA tensor (needed for
+    MASK_KEY_PADDING).  scale defaults to 1/sqrt(d_k).  out: optional preallocated
+    [B, h, m, d_k] tensor.  Enqueued on ``stream`` (default: torch's current stream).
+    """
+    import torch
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, h, len, d_k]")
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous CUDA tensors")
+    B, h, m, d = q.shape
+    n = k.shape[2]
+    if k.shape != (B, h, n, d) or v.shape != k.shape or q.dtype != k.dtype or q.dtype != v.dtype:
+        raise ValueError(f"shape/dtype mismatch: q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError("out must be a contiguous CUDA tensor shaped and typed like q")
+    lens_ptr = None
+    if mask_kind & MASK_KEY_PADDING:
+        if key_lengths is None or key_lengths.dtype != torch.int32 or not key_lengths.is_cuda \
+                or key_lengths.numel() != B:
+            raise ValueError("key padding needs key_lengths: int32 CUDA tensor of B elements")
+        lens_ptr = key_lengths.data_ptr()
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    dims = _native.make_dims(B, h, m, n, d, _dtype_code(q))
+    st = _native.fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), lens_ptr, mask_kind, scale,
+                         out.data_ptr(), dims, stream.cuda_stream, kernel)
+    if st != _native.ATTN_OK:
+        raise AttnError(st)
+    return out
+
+
+def select_kernel(B, h, m, n, d, dtype: int, mask_kind: int) -> int:
+    return _native.select_kernel(B, h, m, n, d, dtype, mask_kind)
+
+
+def device_status(stream=None):
+    """(status, info) of the bounded-wait record; synchronises the stream."""
+    return _native.device_status(None if stream is None else stream.cuda_stream)

@@ -1,0 +1,89 @@
+"""ctypes binding of libattn_gb300.so (argument marshalling only).
+
+Every step of the computation runs in the library's CUDA kernels; this module
+turns torch tensors into pointers and shapes, passes the current CUDA stream,
+and turns status codes into exceptions.  It raises at import time when the
+library has not been built: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(_PKG, "libattn_gb300.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "attn.h")
+
+if not os.path.exists(LIBRARY):
+    raise ImportError(
+        f"{LIBRARY} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+
+# Keep these in step with include/attn.h (tests/test_abi.py checks them against the header).
+ATTN_OK = 0
+ATTN_ERR_DEVICE_TIMEOUT = 8
+MASK_NONE, MASK_KEY_PADDING, MASK_CAUSAL = 0, 1, 2
+DTYPE_BF16, DTYPE_FP32 = 0, 1
+KERNEL_AUTO, KERNEL_FLASH, KERNEL_SHORT, KERNEL_SIMT = 0, 1, 2, 3
+KERNEL_NAMES = {KERNEL_AUTO: "auto", KERNEL_FLASH: "flash", KERNEL_SHORT: "short", KERNEL_SIMT: "simt"}
+
+
+class AttnDims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("h", ctypes.c_int32), ("m", ctypes.c_int32),
+                ("n", ctypes.c_int32), ("d_k", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+lib = ctypes.CDLL(LIBRARY)
+_vp = ctypes.c_void_p
+lib.attn_fwd.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_float, _vp,
+                         ctypes.POINTER(AttnDims), _vp]
+lib.attn_fwd.restype = ctypes.c_int
+lib.attn_fwd_kernel.argtypes = lib.attn_fwd.argtypes + [ctypes.c_int]
+lib.attn_fwd_kernel.restype = ctypes.c_int
+lib.attn_select_kernel.argtypes = [ctypes.POINTER(AttnDims), ctypes.c_int]
+lib.attn_select_kernel.restype = ctypes.c_int
+lib.attn_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32)]
+lib.attn_device_status.restype = ctypes.c_int
+lib.attn_status_string.argtypes = [ctypes.c_int]
+lib.attn_status_string.restype = ctypes.c_char_p
+lib.attn_version.argtypes = []
+lib.attn_version.restype = ctypes.c_int32
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int):
+        self.status = status
+        super().__init__(f"attn status {status}: {status_string(status)}")
+
+
+def status_string(status: int) -> str:
+    return lib.attn_status_string(int(status)).decode()
+
+
+def header_exports(path: str = HEADER):
+    """Function names declared in include/attn.h."""
+    text = open(path).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(", text, re.M)))
+
+
+def make_dims(B, h, m, n, d, dtype: int) -> AttnDims:
+    return AttnDims(int(B), int(h), int(m), int(n), int(d), int(dtype))
+
+
+def select_kernel(B, h, m, n, d, dtype: int, mask_kind: int) -> int:
+    dims = make_dims(B, h, m, n, d, dtype)
+    return lib.attn_select_kernel(ctypes.byref(dims), int(mask_kind))
+
+
+def fwd_raw(q_ptr, k_ptr, v_ptr, lens_ptr, mask_kind, scale, out_ptr, dims: AttnDims, stream_ptr,
+            kernel: int = KERNEL_AUTO) -> int:
+    """Direct call with integer device pointers; returns the status code."""
+    return lib.attn_fwd_kernel(q_ptr, k_ptr, v_ptr, lens_ptr, int(mask_kind), float(scale), out_ptr,
+                               ctypes.byref(dims), stream_ptr, int(kernel))
+
+
+def device_status(stream_ptr=None):
+    info = ctypes.c_int32(0)
+    st = lib.attn_device_status(stream_ptr, ctypes.byref(info))
+    return st, info.value

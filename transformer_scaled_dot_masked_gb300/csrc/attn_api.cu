@@ -1,0 +1,151 @@
+// C-ABI layer: argument validation, kernel choice, launch on the caller's stream.
+// The operation and its rules are documented in include/attn.h.
+#include <cmath>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/attn.h"
+#include "kernels.h"
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool overlaps(const void *a, uint64_t abytes, const void *b, uint64_t bbytes)
+{
+    if (a == nullptr || b == nullptr) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+// Which kernel AUTO picks: tensor cores for bf16 with d_k == 64 (two heads per
+// CTA tile when a head has at most 128 queries, two query tiles of one head
+// otherwise); CUDA cores for fp32 and for narrower bf16 heads.
+int auto_kernel(const attn_dims &d)
+{
+    if (d.dtype == ATTN_BF16 && d.d_k == 64) return d.m <= 128 ? ATTN_KERNEL_SHORT : ATTN_KERNEL_FLASH;
+    return ATTN_KERNEL_SIMT;
+}
+
+attn_status validate_dims(const attn_dims *dims, int mask_kind, float scale)
+{
+    if (dims == nullptr) return ATTN_ERR_NULL;
+    if ((mask_kind & ~(ATTN_MASK_KEY_PADDING | ATTN_MASK_CAUSAL)) != 0) return ATTN_ERR_MASK;
+    const attn_dims &d = *dims;
+    if (d.dtype != ATTN_BF16 && d.dtype != ATTN_FP32) return ATTN_ERR_DTYPE;
+    if (d.d_k < 1 || d.d_k > 64) return ATTN_ERR_DTYPE;
+    if (d.B < 1 || d.h < 1 || d.m < 1 || d.n < 1) return ATTN_ERR_SHAPE;
+    if (d.B > 65535 || d.h > 65535) return ATTN_ERR_SHAPE;                  // grid limits
+    if ((mask_kind & ATTN_MASK_CAUSAL) && d.m != d.n) return ATTN_ERR_SHAPE; // queries and keys share positions
+    if (!std::isfinite(scale) || scale < 0.f) return ATTN_ERR_VALUE;
+    return ATTN_OK;
+}
+
+attn_status validate(const void *Q, const void *K, const void *V, const int32_t *key_lengths, int mask_kind,
+                     float scale, void *out, const attn_dims *dims)
+{
+    if (dims == nullptr || Q == nullptr || K == nullptr || V == nullptr || out == nullptr) return ATTN_ERR_NULL;
+    if ((mask_kind & ATTN_MASK_KEY_PADDING) && key_lengths == nullptr) return ATTN_ERR_NULL;
+    const attn_status st = validate_dims(dims, mask_kind, scale);
+    if (st != ATTN_OK) return st;
+    const attn_dims &d = *dims;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(out, 16)) return ATTN_ERR_ALIGN;
+    if ((mask_kind & ATTN_MASK_KEY_PADDING) && !aligned(key_lengths, 4)) return ATTN_ERR_ALIGN;
+    const uint64_t esz = d.dtype == ATTN_BF16 ? 2 : 4;
+    const uint64_t qbytes = static_cast<uint64_t>(d.B) * d.h * d.m * d.d_k * esz;
+    const uint64_t kbytes = static_cast<uint64_t>(d.B) * d.h * d.n * d.d_k * esz;
+    if (overlaps(out, qbytes, Q, qbytes) || overlaps(out, qbytes, K, kbytes) || overlaps(out, qbytes, V, kbytes))
+        return ATTN_ERR_ALIAS;
+    if ((mask_kind & ATTN_MASK_KEY_PADDING) && overlaps(out, qbytes, key_lengths, 4ull * d.B))
+        return ATTN_ERR_ALIAS;
+    return ATTN_OK;
+}
+
+} // namespace
+
+extern "C" {
+
+attn_status attn_fwd_kernel(const void *Q, const void *K, const void *V, const int32_t *key_lengths,
+                            int mask_kind, float scale, void *out, const attn_dims *dims, void *stream,
+                            int kernel)
+{
+    const attn_status st = validate(Q, K, V, key_lengths, mask_kind, scale, out, dims);
+    if (st != ATTN_OK) return st;
+    const attn_dims &d = *dims;
+    if (kernel == ATTN_KERNEL_AUTO) kernel = auto_kernel(d);
+    attn::Problem p;
+    p.q = Q;
+    p.k = K;
+    p.v = V;
+    p.key_lengths = (mask_kind & ATTN_MASK_KEY_PADDING) ? key_lengths : nullptr;
+    p.out = out;
+    p.B = d.B;
+    p.h = d.h;
+    p.m = d.m;
+    p.n = d.n;
+    p.d = d.d_k;
+    p.mask_kind = mask_kind;
+    p.scale = scale;
+    p.bf16 = d.dtype == ATTN_BF16;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    switch (kernel) {
+    case ATTN_KERNEL_SIMT:
+        e = attn::launch_simt(p, s);
+        break;
+    case ATTN_KERNEL_FLASH:
+        if (!p.bf16 || p.d != 64) return ATTN_ERR_UNSUPPORTED;
+        e = attn::launch_flash(p, /*pair_mode=*/true, s);
+        break;
+    case ATTN_KERNEL_SHORT:
+        if (!p.bf16 || p.d != 64 || p.m > 128) return ATTN_ERR_UNSUPPORTED;
+        e = attn::launch_flash(p, /*pair_mode=*/false, s);
+        break;
+    default:
+        return ATTN_ERR_UNSUPPORTED;
+    }
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status attn_fwd(const void *Q, const void *K, const void *V, const int32_t *key_lengths, int mask_kind,
+                     float scale, void *out, const attn_dims *dims, void *stream)
+{
+    return attn_fwd_kernel(Q, K, V, key_lengths, mask_kind, scale, out, dims, stream, ATTN_KERNEL_AUTO);
+}
+
+int attn_select_kernel(const attn_dims *dims, int mask_kind)
+{
+    if (validate_dims(dims, mask_kind, 1.0f) != ATTN_OK) return ATTN_KERNEL_AUTO;
+    return auto_kernel(*dims);
+}
+
+attn_status attn_device_status(void *stream, int32_t *info)
+{
+    uint32_t code = 0, where = 0;
+    if (attn::flash_status_read_and_clear(static_cast<cudaStream_t>(stream), &code, &where) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    if (info != nullptr) *info = static_cast<int32_t>(where);
+    return code != 0 ? ATTN_ERR_DEVICE_TIMEOUT : ATTN_OK;
+}
+
+const char *attn_status_string(int status)
+{
+    switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_NULL: return "a required pointer is NULL";
+    case ATTN_ERR_SHAPE: return "shape out of range (or causal mask with m != n)";
+    case ATTN_ERR_DTYPE: return "unsupported dtype or head width";
+    case ATTN_ERR_MASK: return "unknown mask bits";
+    case ATTN_ERR_ALIGN: return "pointer not aligned (16 bytes for tensors, 4 for key_lengths)";
+    case ATTN_ERR_UNSUPPORTED: return "the requested kernel cannot run this call";
+    case ATTN_ERR_CUDA: return "CUDA runtime error";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait; its output is incomplete";
+    case ATTN_ERR_VALUE: return "scale must be finite and >= 0";
+    case ATTN_ERR_ALIAS: return "out overlaps an input";
+    default: return "unknown status";
+    }
+}
+
+int32_t attn_version(void) { return (1 << 16) | 0; }
+
+} // extern "C"

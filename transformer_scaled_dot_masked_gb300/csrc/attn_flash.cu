@@ -1,0 +1,625 @@
+// Fused masked scaled dot-product attention for sm_103a: TMA + tcgen05 + TMEM.
+//
+// What it computes is softmax(scale * Q K^T + M) V per (batch, head)
+// ("Paper Deep Reading: Attention Is All You Need", §04 attention equation;
+// M from §03 "Decoder layer" and §04), one 128-key tile at a time with an
+// online softmax, so no score matrix larger than one tile ever exists.
+//
+// CTA organisation (persistent: one CTA per SM, CTA tiles strided over the grid)
+//   warps 0-3  softmax group of slot 0 (thread t owns query row t of the slot)
+//   warps 4-7  softmax group of slot 1
+//   warp 8     TMA producer (one lane): Q tiles, then K/V tiles into a 4-stage ring
+//   warp 9     MMA issuer (one lane) + TMEM allocation for the CTA
+// A CTA tile has two slots of 128 query rows each:
+//   pair mode   two consecutive query tiles of one head; each K/V stage feeds both
+//   split mode  query tile 0 of two different heads (m <= 128: the whole head's
+//               queries, keys and values are resident at once)
+//
+// TMEM (512 columns, fp32 unless noted), per slot s at column 256*s:
+//   S [0,128)   scores of the current key tile, Q K^T
+//   P [128,192) exp2 weights as packed bf16 pairs: the A operand of the PV MMA
+//   O [192,256) output accumulator
+//
+// Per key tile j of a slot:
+//   MMA:     S = Q K_j^T                       (4 x tcgen05.mma M128 N128 K16, both K-major)
+//   softmax: read S, mask (boundary tiles only), running max with lazy
+//            rescaling (the max used for the exponentials is only moved when
+//            it grows by more than 2^8, so O and the running sum stay exact
+//            multiples of the true ones and are rescaled rarely),
+//            P = exp2(S * scale * log2 e - max), row sum, write P as bf16
+//   MMA:     O += P V_j                        (8 x tcgen05.mma M128 N64 K16, A from TMEM, V MN-major)
+// Key tiles wholly beyond the causal diagonal or the padded length are never
+// loaded or computed.  The epilogue divides O by the row sum (0 for a row with
+// no allowed key) and stores bf16 rows with 16-byte stores.
+//
+// Every mbarrier wait is bounded (kWaitLimitNs).  A wait that runs out sets a
+// shared abort flag and the device status word; all roles then leave their
+// loops, wait (bounded) for their own asynchronous copies and MMAs, and the
+// CTA frees its TMEM and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+#include <math_constants.h>
+
+#include <mutex>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace attn {
+
+// Device status word: code (bit 0 = a bounded wait gave up) and info (which wait).
+__device__ unsigned int g_flash_status_code;
+__device__ unsigned int g_flash_status_info;
+
+namespace {
+
+constexpr int kBM = 128;   // query rows per slot
+constexpr int kBN = 128;   // keys per key tile
+constexpr int kD = 64;     // head width
+constexpr int kSlots = 2;
+constexpr int kStages = 4; // K/V ring depth
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr uint32_t kTileBytes = kBM * kD * 2; // one 128 x 64 bf16 tile = 16 KiB
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSlotCols = 256;
+constexpr uint32_t kColS = 0, kColP = 128, kColO = 192;
+constexpr float kRescaleThreshold = 8.0f; // log2 units: rescale only when the max grows by > 2^8
+constexpr uint64_t kWaitLimitNs = 2000000000ull; // 2 s
+constexpr uint64_t kDrainLimitNs = 200000000ull; // 0.2 s
+
+constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, 0, 0); // Q (K-major) x K^T (K-major)
+constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kD, 0, 1); // P (TMEM) x V (MN-major)
+
+// Where a wait gave up (reported through the status word's info).
+enum WaitSite : uint32_t {
+    kSiteLoadQEmpty = 1, kSiteLoadKvEmpty, kSiteMmaQFull, kSiteMmaKvFull, kSiteMmaSFree,
+    kSiteMmaPFull, kSiteMmaOFree, kSiteSmSFull, kSiteSmPvDone, kSiteSmPvLast
+};
+
+struct alignas(1024) SharedStorage {
+    uint8_t q[kSlots][kTileBytes];
+    uint8_t k[kStages][kTileBytes];
+    uint8_t v[kStages][kTileBytes];
+    uint64_t q_full[kSlots], q_empty[kSlots];
+    uint64_t kv_full[kStages], kv_empty[kStages];
+    uint64_t s_full[kSlots], s_free[kSlots], p_full[kSlots], pv_done[kSlots], o_free[kSlots];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+struct FlashParams {
+    const int32_t *key_lengths;
+    __nv_bfloat16 *out;
+    int BH, h, m, n, mask_kind;
+    float scale_log2;
+    int pair_mode;
+    int num_tiles;
+    int q_pairs; // pair mode: query-tile pairs per head
+};
+
+struct Tile {
+    int bh[kSlots];
+    int q0[kSlots];
+    int kv_len[kSlots]; // keys allowed by padding (n without padding)
+    int n_kv[kSlots];   // key tiles to process (0: nothing allowed or slot unused)
+    bool active[kSlots];
+    bool shared_kv;
+};
+
+__device__ __forceinline__ Tile decode_tile(const FlashParams &p, int t)
+{
+    Tile T;
+    if (p.pair_mode) {
+        // heaviest pair first: with a causal mask later query tiles see more keys
+        const int pair = p.q_pairs - 1 - t / p.BH;
+        const int bh = t % p.BH;
+        T.bh[0] = T.bh[1] = bh;
+        T.q0[0] = pair * 2 * kBM;
+        T.q0[1] = pair * 2 * kBM + kBM;
+        T.shared_kv = true;
+    } else {
+        T.bh[0] = 2 * t;
+        T.bh[1] = 2 * t + 1;
+        T.q0[0] = T.q0[1] = 0;
+        T.shared_kv = false;
+    }
+    const bool causal = (p.mask_kind & kMaskCausal) != 0;
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s) {
+        T.active[s] = T.bh[s] < p.BH && T.q0[s] < p.m;
+        T.kv_len[s] = 0;
+        T.n_kv[s] = 0;
+        if (!T.active[s]) continue;
+        int len = p.n;
+        if ((p.mask_kind & kMaskKeyPadding) && p.key_lengths != nullptr) {
+            len = __ldg(p.key_lengths + T.bh[s] / p.h);
+            len = len < 0 ? 0 : (len > p.n ? p.n : len);
+        }
+        const int lim = causal ? min(len, T.q0[s] + kBM) : len;
+        T.kv_len[s] = len;
+        T.n_kv[s] = (lim + kBN - 1) / kBN;
+    }
+    return T;
+}
+
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, int *abort_flag, uint32_t site)
+{
+    const uint64_t start = global_timer_ns();
+    while (true) {
+        for (int k = 0; k < 64; ++k)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*reinterpret_cast<volatile int *>(abort_flag)) return false;
+        if (global_timer_ns() - start > kWaitLimitNs) {
+            *reinterpret_cast<volatile int *>(abort_flag) = 1;
+            atomicOr(&g_flash_status_code, 1u);
+            atomicCAS(&g_flash_status_info, 0u, site);
+            return false;
+        }
+    }
+}
+
+// Bounded wait for phase `parity` of `bar` to complete.  false: gave up (or another role did).
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, int *abort_flag, uint32_t site)
+{
+    const uint32_t a = smem_addr(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    return wait_slow(a, parity, abort_flag, site);
+}
+
+// Bounded wait that ignores the abort flag (used to drain in-flight work on the way out).
+__device__ __noinline__ void drain_wait(uint64_t *bar, uint32_t parity)
+{
+    const uint32_t a = smem_addr(bar);
+    const uint64_t start = global_timer_ns();
+    while (!mbar_try_wait(a, parity))
+        if (global_timer_ns() - start > kDrainLimitNs) return;
+}
+
+__device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffffu, ok); }
+
+// ------------------------------------------------------------------ roles
+__device__ __forceinline__ void load_role(SharedStorage &sm, const FlashParams &p, const CUtensorMap *tm_q,
+                                          const CUtensorMap *tm_k, const CUtensorMap *tm_v)
+{
+    tma_prefetch_map(tm_q);
+    tma_prefetch_map(tm_k);
+    tma_prefetch_map(tm_v);
+    uint32_t q_cnt[kSlots] = {0, 0};
+    uint32_t seq = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        const Tile T = decode_tile(p, t);
+#pragma unroll
+        for (int s = 0; s < kSlots; ++s) {
+            if (T.n_kv[s] == 0) continue;
+            if (!(ok = wait_bar(&sm.q_empty[s], (q_cnt[s] & 1) ^ 1, &sm.abort_flag, kSiteLoadQEmpty))) break;
+            mbar_arrive_expect_tx(&sm.q_full[s], kTileBytes);
+            tma_load_3d(sm.q[s], tm_q, &sm.q_full[s], 0, T.q0[s], T.bh[s]);
+            ++q_cnt[s];
+        }
+        const int J = max(T.n_kv[0], T.n_kv[1]);
+        for (int j = 0; j < J && ok; ++j) {
+#pragma unroll
+            for (int s = 0; s < kSlots; ++s) {
+                if (j >= T.n_kv[s]) continue;
+                if (T.shared_kv && s == 1 && j < T.n_kv[0]) continue; // slot 1 reads slot 0's stage
+                const int st = seq % kStages;
+                if (!(ok = wait_bar(&sm.kv_empty[st], ((seq / kStages) & 1) ^ 1, &sm.abort_flag,
+                                    kSiteLoadKvEmpty)))
+                    break;
+                mbar_arrive_expect_tx(&sm.kv_full[st], 2 * kTileBytes);
+                tma_load_3d(sm.k[st], tm_k, &sm.kv_full[st], 0, j * kBN, T.bh[s]);
+                tma_load_3d(sm.v[st], tm_v, &sm.kv_full[st], 0, j * kBN, T.bh[s]);
+                ++seq;
+            }
+        }
+    }
+    // Tail: every stage and Q buffer must be released (its last copy landed and
+    // the MMAs reading it completed) before the CTA may exit.
+    for (int st = 0; st < kStages; ++st) {
+        const uint32_t uses = seq / kStages + (static_cast<uint32_t>(st) < seq % kStages ? 1u : 0u);
+        if (uses == 0) continue;
+        if (ok) {
+            wait_bar(&sm.kv_empty[st], (uses - 1) & 1, &sm.abort_flag, kSiteLoadKvEmpty);
+        } else {
+            drain_wait(&sm.kv_full[st], (uses - 1) & 1);
+        }
+    }
+    for (int s = 0; s < kSlots; ++s) {
+        if (q_cnt[s] == 0) continue;
+        if (ok) {
+            wait_bar(&sm.q_empty[s], (q_cnt[s] - 1) & 1, &sm.abort_flag, kSiteLoadQEmpty);
+        } else {
+            drain_wait(&sm.q_full[s], (q_cnt[s] - 1) & 1);
+        }
+    }
+}
+
+__device__ __forceinline__ void mma_role(SharedStorage &sm, const FlashParams &p, uint32_t tmem)
+{
+    uint32_t q_cnt[kSlots] = {0, 0}, s_cnt[kSlots] = {0, 0}, p_cnt[kSlots] = {0, 0}, o_cnt[kSlots] = {0, 0};
+    uint32_t seq = 0;
+    bool ok = true;
+    int *ab = &sm.abort_flag;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        const Tile T = decode_tile(p, t);
+        for (int s = 0; s < kSlots && ok; ++s) {
+            if (T.n_kv[s] == 0) continue;
+            ok = wait_bar(&sm.q_full[s], q_cnt[s] & 1, ab, kSiteMmaQFull);
+            ++q_cnt[s];
+        }
+        const int J = max(T.n_kv[0], T.n_kv[1]);
+        int prev_stage[kSlots] = {0, 0};
+        for (int j = 0; j <= J && ok; ++j) {
+            int cur_stage[kSlots] = {0, 0};
+            if (j < J) {
+                for (int s = 0; s < kSlots && ok; ++s) {
+                    if (j >= T.n_kv[s]) continue;
+                    if (T.shared_kv && s == 1 && j < T.n_kv[0]) {
+                        cur_stage[1] = cur_stage[0];
+                        continue;
+                    }
+                    const int st = seq % kStages;
+                    ok = wait_bar(&sm.kv_full[st], (seq / kStages) & 1, ab, kSiteMmaKvFull);
+                    ++seq;
+                    cur_stage[s] = st;
+                }
+                for (int s = 0; s < kSlots && ok; ++s) {
+                    if (j >= T.n_kv[s]) continue;
+                    if (!(ok = wait_bar(&sm.s_free[s], (s_cnt[s] & 1) ^ 1, ab, kSiteMmaSFree))) break;
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem + s * kSlotCols + kColS;
+                    const uint32_t qa = smem_addr(sm.q[s]);
+                    const uint32_t ka = smem_addr(sm.k[cur_stage[s]]);
+#pragma unroll
+                    for (int kk = 0; kk < kD / 16; ++kk) {
+                        // 16 bf16 of K per instruction = 32 bytes along the swizzled 128-byte row
+                        mma_ss(d_tmem, smem_desc_sw128(qa + kk * 32, 16, 1024),
+                               smem_desc_sw128(ka + kk * 32, 16, 1024), kIdescS, kk > 0);
+                    }
+                    mma_commit(&sm.s_full[s]);
+                    ++s_cnt[s];
+                    if (j == T.n_kv[s] - 1) mma_commit(&sm.q_empty[s]);
+                }
+            }
+            if (j >= 1) {
+                const int jp = j - 1;
+                for (int s = 0; s < kSlots && ok; ++s) {
+                    if (jp >= T.n_kv[s]) continue;
+                    if (!(ok = wait_bar(&sm.p_full[s], p_cnt[s] & 1, ab, kSiteMmaPFull))) break;
+                    ++p_cnt[s];
+                    tc_fence_after();
+                    if (jp == 0) {
+                        // first PV of this tile overwrites O: the previous epilogue must have read it
+                        if (!(ok = wait_bar(&sm.o_free[s], (o_cnt[s] & 1) ^ 1, ab, kSiteMmaOFree))) break;
+                        ++o_cnt[s];
+                        tc_fence_after();
+                    }
+                    const uint32_t d_tmem = tmem + s * kSlotCols + kColO;
+                    const uint32_t a_tmem = tmem + s * kSlotCols + kColP;
+                    const uint32_t va = smem_addr(sm.v[prev_stage[s]]);
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk) {
+                        // keys 16kk..16kk+15: P columns 8kk.. (two bf16 per column), V rows 16kk..
+                        mma_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128(va + kk * 16 * 128, kTileBytes, 1024),
+                               kIdescPV, (jp > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&sm.pv_done[s]);
+                    const bool last_user = (s == 1) || !(T.shared_kv && jp < T.n_kv[1]);
+                    if (last_user) mma_commit(&sm.kv_empty[prev_stage[s]]);
+                }
+            }
+#pragma unroll
+            for (int s = 0; s < kSlots; ++s) prev_stage[s] = cur_stage[s];
+        }
+    }
+    if (!ok) {
+        // make sure no MMA is still writing TMEM when the CTA frees it
+        mma_commit(&sm.drain);
+        drain_wait(&sm.drain, 0);
+    }
+}
+
+__device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParams &p, uint32_t tmem, int slot)
+{
+    const int warp_in_group = (threadIdx.x / 32) % 4; // TMEM lane quadrant this warp may access
+    const int row = warp_in_group * 32 + (threadIdx.x % 32);
+    const uint32_t lane_base = static_cast<uint32_t>(warp_in_group * 32) << 16;
+    const uint32_t t_s = tmem + lane_base + slot * kSlotCols + kColS;
+    const uint32_t t_p = tmem + lane_base + slot * kSlotCols + kColP;
+    const uint32_t t_o = tmem + lane_base + slot * kSlotCols + kColO;
+    const bool causal = (p.mask_kind & kMaskCausal) != 0;
+    const float sl2 = p.scale_log2;
+    int *ab = &sm.abort_flag;
+    uint32_t s_cnt = 0, pv_cnt = 0;
+    bool ok = true;
+
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        const Tile T = decode_tile(p, t);
+        if (!T.active[slot]) continue;
+        const int i = T.q0[slot] + row;
+        __nv_bfloat16 *orow = p.out + (static_cast<size_t>(T.bh[slot]) * p.m + i) * kD;
+        const int n_kv = T.n_kv[slot];
+        const int kv_len = T.kv_len[slot];
+        if (n_kv == 0) { // no allowed key for any row of this tile: output 0
+            if (i < p.m) {
+                uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int c = 0; c < kD / 8; ++c) reinterpret_cast<uint4 *>(orow)[c] = z;
+            }
+            continue;
+        }
+        float m_run = -CUDART_INF_F; // running max, log2 units, as used for the exponentials
+        float l_run = 0.f;           // running sum of exponentials relative to m_run
+        for (int j = 0; j < n_kv; ++j) {
+            ok = warp_all(wait_bar(&sm.s_full[slot], s_cnt & 1, ab, kSiteSmSFull));
+            if (!ok) break;
+            ++s_cnt;
+            tc_fence_after();
+            uint32_t sr[kBN];
+#pragma unroll
+            for (int c = 0; c < kBN / 32; ++c) tmem_ld32(t_s + c * 32, sr + c * 32);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < kBN / 32; ++c) reg_fence32(sr + c * 32);
+            tc_fence_before();
+            mbar_arrive(&sm.s_free[slot]); // S may be overwritten by the next Q K^T
+
+            const int key0 = j * kBN;
+            const bool boundary = (key0 + kBN > kv_len) || (causal && key0 + kBN - 1 > i - row);
+            float x[kBN];
+            float row_max = -CUDART_INF_F;
+            if (boundary) {
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) {
+                    const int key = key0 + c;
+                    const bool allowed = key < kv_len && !(causal && key > i);
+                    x[c] = allowed ? __uint_as_float(sr[c]) * sl2 : -CUDART_INF_F;
+                    row_max = fmaxf(row_max, x[c]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) {
+                    x[c] = __uint_as_float(sr[c]);
+                    row_max = fmaxf(row_max, x[c]);
+                }
+                row_max *= sl2;
+            }
+            const float m_new = fmaxf(m_run, row_max);
+            const bool grow = m_new > m_run + kRescaleThreshold;
+            const float m_use = grow ? m_new : m_run;
+            const float alpha = grow ? ex2(m_run - m_new) : 1.f; // 0 on the first tile
+            const float m_sub = (m_use == -CUDART_INF_F) ? 0.f : m_use;
+
+            if (j > 0) {
+                // P and O are still in use by the previous P V until it completes
+                ok = warp_all(wait_bar(&sm.pv_done[slot], pv_cnt & 1, ab, kSiteSmPvDone));
+                if (!ok) break;
+                ++pv_cnt;
+                tc_fence_after();
+            }
+            // exponentials, 32 keys at a time, written straight to TMEM as bf16 pairs
+            float sum = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < kBN / 32; ++cc) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int c2 = 0; c2 < 16; ++c2) {
+                    const int c = cc * 32 + 2 * c2;
+                    float e0, e1;
+                    if (boundary) {
+                        e0 = ex2(x[c] - m_sub);
+                        e1 = ex2(x[c + 1] - m_sub);
+                    } else {
+                        e0 = ex2(fmaf(x[c], sl2, -m_sub));
+                        e1 = ex2(fmaf(x[c + 1], sl2, -m_sub));
+                    }
+                    sum += e0 + e1;
+                    pk[c2] = pack_bf16x2(e0, e1);
+                }
+                tmem_st16(t_p + cc * 16, pk);
+            }
+            l_run = l_run * alpha + sum;
+            if (j > 0 && __any_sync(0xffffffffu, grow)) {
+                // move O to the new reference max (rare: only when the max grew by > 2^8)
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    uint32_t orr[32];
+                    tmem_ld32(t_o + 32 * h2, orr);
+                    tmem_wait_ld();
+                    reg_fence32(orr);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) orr[c] = __float_as_uint(__uint_as_float(orr[c]) * alpha);
+                    tmem_st32(t_o + 32 * h2, orr);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&sm.p_full[slot]);
+            m_run = m_use;
+        }
+        if (!ok) break;
+        ok = warp_all(wait_bar(&sm.pv_done[slot], pv_cnt & 1, ab, kSiteSmPvLast));
+        if (!ok) break;
+        ++pv_cnt;
+        tc_fence_after();
+        uint32_t orr[kD];
+        tmem_ld32(t_o, orr);
+        tmem_ld32(t_o + 32, orr + 32);
+        tmem_wait_ld();
+        reg_fence32(orr);
+        reg_fence32(orr + 32);
+        tc_fence_before();
+        mbar_arrive(&sm.o_free[slot]);
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        if (i < p.m) {
+#pragma unroll
+            for (int c = 0; c < kD / 8; ++c) {
+                uint4 v;
+                v.x = pack_bf16x2(__uint_as_float(orr[8 * c + 0]) * inv, __uint_as_float(orr[8 * c + 1]) * inv);
+                v.y = pack_bf16x2(__uint_as_float(orr[8 * c + 2]) * inv, __uint_as_float(orr[8 * c + 3]) * inv);
+                v.z = pack_bf16x2(__uint_as_float(orr[8 * c + 4]) * inv, __uint_as_float(orr[8 * c + 5]) * inv);
+                v.w = pack_bf16x2(__uint_as_float(orr[8 * c + 6]) * inv, __uint_as_float(orr[8 * c + 7]) * inv);
+                reinterpret_cast<uint4 *>(orow)[c] = v;
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+attn_flash_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const FlashParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    SharedStorage &sm = *reinterpret_cast<SharedStorage *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x / 32;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(&sm.q_full[s], 1);
+            mbar_init(&sm.q_empty[s], 1);
+            mbar_init(&sm.s_full[s], 1);
+            mbar_init(&sm.s_free[s], kBM);
+            mbar_init(&sm.p_full[s], kBM);
+            mbar_init(&sm.pv_done[s], 1);
+            mbar_init(&sm.o_free[s], kBM);
+        }
+        for (int st = 0; st < kStages; ++st) {
+            mbar_init(&sm.kv_full[st], 1);
+            mbar_init(&sm.kv_empty[st], 1);
+        }
+        mbar_init(&sm.drain, 1);
+        sm.abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    __syncwarp();
+    if (warp == kMmaWarp) {
+        tmem_alloc(&sm.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+
+    if (warp < 4 * kSlots) {
+        softmax_role(sm, p, tmem, warp / 4);
+    } else if (warp == kLoadWarp) {
+        if (threadIdx.x % 32 == 0) load_role(sm, p, &tm_q, &tm_k, &tm_v);
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        if (threadIdx.x % 32 == 0) mma_role(sm, p, tmem);
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// [BH][rows][64] bf16 viewed as a 3-D tensor; box = 128 rows x 64 columns of one (b, h).
+bool encode_map(CUtensorMap *map, const void *base, int rows, int BH)
+{
+    auto enc = get_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(rows) * kD * 2};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(kD), static_cast<cuuint32_t>(kBM), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct DeviceInfo {
+    int sms = 0;
+    bool configured = false;
+};
+
+constexpr size_t kSmemBytes = sizeof(SharedStorage) + 1024; // + alignment slack
+
+} // namespace
+
+cudaError_t launch_flash(const Problem &pb, bool pair_mode, cudaStream_t stream)
+{
+    static DeviceInfo infos[64];
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        DeviceInfo &di = infos[dev];
+        if (!di.configured) {
+            if ((e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+            if ((e = cudaFuncSetAttribute(attn_flash_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>(kSmemBytes))) != cudaSuccess)
+                return e;
+            di.configured = true;
+        }
+    }
+    const int sms = infos[dev].sms;
+    const int BH = pb.B * pb.h;
+    CUtensorMap tq, tk, tv;
+    if (!encode_map(&tq, pb.q, pb.m, BH) || !encode_map(&tk, pb.k, pb.n, BH) || !encode_map(&tv, pb.v, pb.n, BH))
+        return cudaErrorInvalidValue;
+    FlashParams p;
+    p.key_lengths = (pb.mask_kind & kMaskKeyPadding) ? pb.key_lengths : nullptr;
+    p.out = static_cast<__nv_bfloat16 *>(pb.out);
+    p.BH = BH;
+    p.h = pb.h;
+    p.m = pb.m;
+    p.n = pb.n;
+    p.mask_kind = pb.mask_kind;
+    p.scale_log2 = pb.scale * 1.4426950408889634f;
+    p.pair_mode = pair_mode ? 1 : 0;
+    p.q_pairs = (pb.m + 2 * kBM - 1) / (2 * kBM);
+    p.num_tiles = pair_mode ? BH * p.q_pairs : (BH + 1) / 2;
+    const int grid = p.num_tiles < sms ? p.num_tiles : sms;
+    attn_flash_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+}
+
+cudaError_t flash_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint32_t *info)
+{
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return e;
+    unsigned int c = 0, i = 0, zero = 0;
+    if ((e = cudaMemcpyFromSymbol(&c, g_flash_status_code, sizeof c)) != cudaSuccess) return e;
+    if ((e = cudaMemcpyFromSymbol(&i, g_flash_status_info, sizeof i)) != cudaSuccess) return e;
+    if ((e = cudaMemcpyToSymbol(g_flash_status_code, &zero, sizeof zero)) != cudaSuccess) return e;
+    if ((e = cudaMemcpyToSymbol(g_flash_status_info, &zero, sizeof zero)) != cudaSuccess) return e;
+    *code = c;
+    *info = i;
+    return cudaSuccess;
+}
+
+} // namespace attn

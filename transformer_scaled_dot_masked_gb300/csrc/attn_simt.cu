@@ -1,0 +1,154 @@
+// CUDA-core attention kernel: fp32 arithmetic from fp32 or bf16 inputs.
+//
+// Computes softmax(scale * Q K^T + M) V ("Paper Deep Reading: Attention Is All
+// You Need", §04, attention equation with the additive mask) one key block
+// at a time with a running (online) softmax: per query row it keeps the
+// running maximum and the running sum of exponentials, and rescales the
+// partial output whenever the maximum grows.  This is exact algebra for the
+// row softmax; only rounding differs from the two-pass definition.
+//
+// It serves the fp32 path (true fp32: no tensor cores, so no TF32 rounding)
+// and is a plain baseline for the tensor-core kernel on bf16 inputs.
+//
+// Grid: (ceil(m / kRows), h, B); 128 threads = 4 warps; each warp owns
+// kRowsPerWarp query rows, and lane l owns output columns l and l + 32.
+// Key/value blocks of 32 rows are staged in shared memory as fp32.
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "kernels.h"
+
+namespace attn {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kRowsPerWarp = 4;
+constexpr int kRows = kWarps * kRowsPerWarp;
+constexpr int kKeys = 32;
+constexpr int kDMax = 64;
+constexpr int kStride = kDMax + 1; // padded row stride: lane-per-key reads hit distinct banks
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ void from_f32(float x, float *dst) { *dst = x; }
+__device__ __forceinline__ void from_f32(float x, __nv_bfloat16 *dst) { *dst = __float2bfloat16_rn(x); }
+
+template <typename T>
+__global__ void __launch_bounds__(kWarps * 32)
+attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ K, const T *__restrict__ V,
+                 const int32_t *__restrict__ key_lengths, T *__restrict__ out, int h, int m, int n, int d,
+                 int mask_kind, float scale_log2)
+{
+    __shared__ float sq[kRows][kStride];
+    __shared__ float sk[kKeys][kStride];
+    __shared__ float sv[kKeys][kDMax];
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const int b = blockIdx.z;
+    const int bh = b * h + blockIdx.y;
+    const int q0 = blockIdx.x * kRows;
+    const bool causal = (mask_kind & kMaskCausal) != 0;
+
+    int kv_len = n;
+    if ((mask_kind & kMaskKeyPadding) && key_lengths != nullptr) {
+        kv_len = key_lengths[b];
+        kv_len = kv_len < 0 ? 0 : (kv_len > n ? n : kv_len);
+    }
+    int kv_end = kv_len;
+    if (causal) kv_end = min(kv_end, min(q0 + kRows, m)); // keys beyond the last row are never allowed
+
+    const T *Qh = Q + static_cast<size_t>(bh) * m * d;
+    const T *Kh = K + static_cast<size_t>(bh) * n * d;
+    const T *Vh = V + static_cast<size_t>(bh) * n * d;
+
+    for (int t = threadIdx.x; t < kRows * kDMax; t += blockDim.x) {
+        int r = t / kDMax, c = t % kDMax;
+        sq[r][c] = (q0 + r < m && c < d) ? to_f32(Qh[static_cast<size_t>(q0 + r) * d + c]) : 0.f;
+    }
+
+    float run_max[kRowsPerWarp], run_sum[kRowsPerWarp], acc0[kRowsPerWarp], acc1[kRowsPerWarp];
+#pragma unroll
+    for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+        run_max[rr] = -CUDART_INF_F;
+        run_sum[rr] = 0.f;
+        acc0[rr] = 0.f;
+        acc1[rr] = 0.f;
+    }
+
+    for (int k0 = 0; k0 < kv_end; k0 += kKeys) {
+        __syncthreads();
+        for (int t = threadIdx.x; t < kKeys * kDMax; t += blockDim.x) {
+            int r = t / kDMax, c = t % kDMax;
+            bool in = (k0 + r < n) && (c < d);
+            sk[r][c] = in ? to_f32(Kh[static_cast<size_t>(k0 + r) * d + c]) : 0.f;
+            sv[r][c] = in ? to_f32(Vh[static_cast<size_t>(k0 + r) * d + c]) : 0.f;
+        }
+        __syncthreads();
+
+        const int j = k0 + lane; // this lane's key
+#pragma unroll
+        for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+            const int r = warp * kRowsPerWarp + rr;
+            const int i = q0 + r;
+            float s = 0.f;
+            for (int c = 0; c < d; ++c) s = fmaf(sq[r][c], sk[lane][c], s);
+            const bool allowed = (j < kv_len) && !(causal && j > i);
+            // scale folded with log2(e): exp(x) = exp2(x * log2 e)
+            const float x = allowed ? s * scale_log2 : -CUDART_INF_F;
+            float blk_max = x;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) blk_max = fmaxf(blk_max, __shfl_xor_sync(0xffffffffu, blk_max, off));
+            const float new_max = fmaxf(run_max[rr], blk_max);
+            if (new_max == -CUDART_INF_F) continue; // nothing allowed for this row yet
+            const float p = allowed ? exp2f(x - new_max) : 0.f;
+            const float alpha = exp2f(run_max[rr] - new_max); // 0 when run_max is -inf
+            float blk_sum = p;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) blk_sum += __shfl_xor_sync(0xffffffffu, blk_sum, off);
+            run_sum[rr] = run_sum[rr] * alpha + blk_sum;
+            float a0 = acc0[rr] * alpha, a1 = acc1[rr] * alpha;
+#pragma unroll 8
+            for (int jj = 0; jj < kKeys; ++jj) {
+                const float pj = __shfl_sync(0xffffffffu, p, jj);
+                a0 = fmaf(pj, sv[jj][lane], a0);
+                a1 = fmaf(pj, sv[jj][lane + 32], a1);
+            }
+            acc0[rr] = a0;
+            acc1[rr] = a1;
+            run_max[rr] = new_max;
+        }
+    }
+
+#pragma unroll
+    for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+        const int i = q0 + warp * kRowsPerWarp + rr;
+        if (i >= m) continue;
+        const float inv = run_sum[rr] > 0.f ? 1.f / run_sum[rr] : 0.f; // no allowed key -> 0
+        T *o = out + (static_cast<size_t>(bh) * m + i) * d;
+        if (lane < d) from_f32(acc0[rr] * inv, o + lane);
+        if (lane + 32 < d) from_f32(acc1[rr] * inv, o + lane + 32);
+    }
+}
+
+} // namespace
+
+cudaError_t launch_simt(const Problem &p, cudaStream_t stream)
+{
+    if (p.d > kDMax) return cudaErrorInvalidValue;
+    const float scale_log2 = p.scale * 1.4426950408889634f;
+    dim3 grid((p.m + kRows - 1) / kRows, p.h, p.B);
+    if (p.bf16) {
+        attn_simt_kernel<__nv_bfloat16><<<grid, kWarps * 32, 0, stream>>>(
+            static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.k),
+            static_cast<const __nv_bfloat16 *>(p.v), p.key_lengths, static_cast<__nv_bfloat16 *>(p.out), p.h,
+            p.m, p.n, p.d, p.mask_kind, scale_log2);
+    } else {
+        attn_simt_kernel<float><<<grid, kWarps * 32, 0, stream>>>(
+            static_cast<const float *>(p.q), static_cast<const float *>(p.k), static_cast<const float *>(p.v),
+            p.key_lengths, static_cast<float *>(p.out), p.h, p.m, p.n, p.d, p.mask_kind, scale_log2);
+    }
+    return cudaGetLastError();
+}
+
+} // namespace attn
