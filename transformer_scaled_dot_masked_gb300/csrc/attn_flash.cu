@@ -10,6 +10,8 @@
 //   warps 4-7  softmax group of slot 1
 //   warp 8     TMA producer (one lane): Q tiles, then K/V tiles into a 4-stage ring
 //   warp 9     MMA issuer (one lane) + TMEM allocation for the CTA
+//   warps 10-11 idle: they complete the third warpgroup so that setmaxnreg can
+//              move registers from it to the softmax warpgroups (200 each, vs 104)
 // A CTA tile has two slots of 128 query rows each:
 //   pair mode   two consecutive query tiles of one head; each K/V stage feeds both
 //   split mode  query tile 0 of two different heads (m <= 128: the whole head's
@@ -61,7 +63,10 @@ constexpr int kSlots = 2;
 constexpr int kStages = 4; // K/V ring depth
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;           // three full warpgroups
+constexpr uint32_t kSoftmaxRegs = 200;  // per thread, softmax warpgroups (setmaxnreg; spill-free)
+constexpr uint32_t kControlRegs = 104;  // per thread, producer/MMA warpgroup
+static_assert(2 * kSoftmaxRegs + kControlRegs <= 3 * 168, "register split exceeds the launch allocation");
 constexpr uint32_t kTileBytes = kBM * kD * 2; // one 128 x 64 bf16 tile = 16 KiB
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSlotCols = 256;
@@ -146,7 +151,7 @@ __device__ __forceinline__ Tile decode_tile(const FlashParams &p, int t)
     return T;
 }
 
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, int *abort_flag, uint32_t site)
+__device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, int *abort_flag, uint32_t site)
 {
     const uint64_t start = global_timer_ns();
     while (true) {
@@ -171,7 +176,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, int *ab
 }
 
 // Bounded wait that ignores the abort flag (used to drain in-flight work on the way out).
-__device__ __noinline__ void drain_wait(uint64_t *bar, uint32_t parity)
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity)
 {
     const uint32_t a = smem_addr(bar);
     const uint64_t start = global_timer_ns();
@@ -247,8 +252,9 @@ __device__ __forceinline__ void mma_role(SharedStorage &sm, const FlashParams &p
     int *ab = &sm.abort_flag;
     for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
         const Tile T = decode_tile(p, t);
-        for (int s = 0; s < kSlots && ok; ++s) {
-            if (T.n_kv[s] == 0) continue;
+#pragma unroll
+        for (int s = 0; s < kSlots; ++s) {
+            if (!ok || T.n_kv[s] == 0) continue;
             ok = wait_bar(&sm.q_full[s], q_cnt[s] & 1, ab, kSiteMmaQFull);
             ++q_cnt[s];
         }
@@ -257,8 +263,9 @@ __device__ __forceinline__ void mma_role(SharedStorage &sm, const FlashParams &p
         for (int j = 0; j <= J && ok; ++j) {
             int cur_stage[kSlots] = {0, 0};
             if (j < J) {
-                for (int s = 0; s < kSlots && ok; ++s) {
-                    if (j >= T.n_kv[s]) continue;
+#pragma unroll
+                for (int s = 0; s < kSlots; ++s) {
+                    if (!ok || j >= T.n_kv[s]) continue;
                     if (T.shared_kv && s == 1 && j < T.n_kv[0]) {
                         cur_stage[1] = cur_stage[0];
                         continue;
@@ -268,9 +275,10 @@ __device__ __forceinline__ void mma_role(SharedStorage &sm, const FlashParams &p
                     ++seq;
                     cur_stage[s] = st;
                 }
-                for (int s = 0; s < kSlots && ok; ++s) {
-                    if (j >= T.n_kv[s]) continue;
-                    if (!(ok = wait_bar(&sm.s_free[s], (s_cnt[s] & 1) ^ 1, ab, kSiteMmaSFree))) break;
+#pragma unroll
+                for (int s = 0; s < kSlots; ++s) {
+                    if (!ok || j >= T.n_kv[s]) continue;
+                    if (!(ok = wait_bar(&sm.s_free[s], (s_cnt[s] & 1) ^ 1, ab, kSiteMmaSFree))) continue;
                     tc_fence_after();
                     const uint32_t d_tmem = tmem + s * kSlotCols + kColS;
                     const uint32_t qa = smem_addr(sm.q[s]);
@@ -288,14 +296,15 @@ __device__ __forceinline__ void mma_role(SharedStorage &sm, const FlashParams &p
             }
             if (j >= 1) {
                 const int jp = j - 1;
-                for (int s = 0; s < kSlots && ok; ++s) {
-                    if (jp >= T.n_kv[s]) continue;
-                    if (!(ok = wait_bar(&sm.p_full[s], p_cnt[s] & 1, ab, kSiteMmaPFull))) break;
+#pragma unroll
+                for (int s = 0; s < kSlots; ++s) {
+                    if (!ok || jp >= T.n_kv[s]) continue;
+                    if (!(ok = wait_bar(&sm.p_full[s], p_cnt[s] & 1, ab, kSiteMmaPFull))) continue;
                     ++p_cnt[s];
                     tc_fence_after();
                     if (jp == 0) {
                         // first PV of this tile overwrites O: the previous epilogue must have read it
-                        if (!(ok = wait_bar(&sm.o_free[s], (o_cnt[s] & 1) ^ 1, ab, kSiteMmaOFree))) break;
+                        if (!(ok = wait_bar(&sm.o_free[s], (o_cnt[s] & 1) ^ 1, ab, kSiteMmaOFree))) continue;
                         ++o_cnt[s];
                         tc_fence_after();
                     }
@@ -340,11 +349,15 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
 
     for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
         const Tile T = decode_tile(p, t);
-        if (!T.active[slot]) continue;
-        const int i = T.q0[slot] + row;
-        __nv_bfloat16 *orow = p.out + (static_cast<size_t>(T.bh[slot]) * p.m + i) * kD;
-        const int n_kv = T.n_kv[slot];
-        const int kv_len = T.kv_len[slot];
+        // select this slot's fields without indexing the per-slot arrays at run time
+        const bool active = slot ? T.active[1] : T.active[0];
+        if (!active) continue;
+        const int q0 = slot ? T.q0[1] : T.q0[0];
+        const int bh = slot ? T.bh[1] : T.bh[0];
+        const int n_kv = slot ? T.n_kv[1] : T.n_kv[0];
+        const int kv_len = slot ? T.kv_len[1] : T.kv_len[0];
+        const int i = q0 + row;
+        __nv_bfloat16 *orow = p.out + (static_cast<size_t>(bh) * p.m + i) * kD;
         if (n_kv == 0) { // no allowed key for any row of this tile: output 0
             if (i < p.m) {
                 uint4 z = make_uint4(0, 0, 0, 0);
@@ -370,25 +383,30 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
             mbar_arrive(&sm.s_free[slot]); // S may be overwritten by the next Q K^T
 
             const int key0 = j * kBN;
-            const bool boundary = (key0 + kBN > kv_len) || (causal && key0 + kBN - 1 > i - row);
+            const bool boundary = (key0 + kBN > kv_len) || (causal && key0 + kBN - 1 > q0);
             float x[kBN];
-            float row_max = -CUDART_INF_F;
+#pragma unroll
+            for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(sr[c]);
             if (boundary) {
+                // scale first, then mask: a zero scale must not turn -inf into NaN
 #pragma unroll
                 for (int c = 0; c < kBN; ++c) {
                     const int key = key0 + c;
                     const bool allowed = key < kv_len && !(causal && key > i);
-                    x[c] = allowed ? __uint_as_float(sr[c]) * sl2 : -CUDART_INF_F;
-                    row_max = fmaxf(row_max, x[c]);
+                    x[c] = allowed ? x[c] * sl2 : -CUDART_INF_F;
                 }
-            } else {
-#pragma unroll
-                for (int c = 0; c < kBN; ++c) {
-                    x[c] = __uint_as_float(sr[c]);
-                    row_max = fmaxf(row_max, x[c]);
-                }
-                row_max *= sl2;
             }
+            // row maximum: four independent chains of three-input max
+            float mx[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mx[k] = fmaxf(x[2 * k], x[2 * k + 1]);
+#pragma unroll
+            for (int c = 8; c < kBN; c += 8) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) mx[k] = max3(mx[k], x[c + 2 * k], x[c + 2 * k + 1]);
+            }
+            float row_max = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            if (!boundary) row_max *= sl2;
             const float m_new = fmaxf(m_run, row_max);
             const bool grow = m_new > m_run + kRescaleThreshold;
             const float m_use = grow ? m_new : m_run;
@@ -402,27 +420,29 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
                 ++pv_cnt;
                 tc_fence_after();
             }
-            // exponentials, 32 keys at a time, written straight to TMEM as bf16 pairs
-            float sum = 0.f;
+            // exponentials, 32 keys at a time, written straight to TMEM as bf16 pairs;
+            // the exponent argument and the row sum use packed two-lane fp32 ops
+            const uint64_t mul2 = boundary ? f2(1.f, 1.f) : f2(sl2, sl2);
+            const uint64_t sub2 = f2(-m_sub, -m_sub);
+            uint64_t acc2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
             for (int cc = 0; cc < kBN / 32; ++cc) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int c2 = 0; c2 < 16; ++c2) {
                     const int c = cc * 32 + 2 * c2;
-                    float e0, e1;
-                    if (boundary) {
-                        e0 = ex2(x[c] - m_sub);
-                        e1 = ex2(x[c + 1] - m_sub);
-                    } else {
-                        e0 = ex2(fmaf(x[c], sl2, -m_sub));
-                        e1 = ex2(fmaf(x[c + 1], sl2, -m_sub));
-                    }
-                    sum += e0 + e1;
+                    float a0, a1;
+                    unf2(fma2(f2(x[c], x[c + 1]), mul2, sub2), a0, a1);
+                    const float e0 = ex2(a0), e1 = ex2(a1);
+                    acc2[c2 & 1] = add2(acc2[c2 & 1], f2(e0, e1));
                     pk[c2] = pack_bf16x2(e0, e1);
                 }
                 tmem_st16(t_p + cc * 16, pk);
             }
+            float s0, s1, s2, s3;
+            unf2(acc2[0], s0, s1);
+            unf2(acc2[1], s2, s3);
+            const float sum = (s0 + s1) + (s2 + s3);
             l_run = l_run * alpha + sum;
             if (j > 0 && __any_sync(0xffffffffu, grow)) {
                 // move O to the new reference max (rare: only when the max grew by > 2^8)
@@ -507,20 +527,26 @@ attn_flash_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
 
+    // The two register regions never rejoin: each branch ends with its own
+    // CTA-wide barrier (every thread arrives exactly once) and returns.
     if (warp < 4 * kSlots) {
+        regs_increase<kSoftmaxRegs>();
         softmax_role(sm, p, tmem, warp / 4);
-    } else if (warp == kLoadWarp) {
+        tc_fence_before();
+        __syncthreads();
+        return;
+    }
+    regs_decrease<kControlRegs>();
+    if (warp == kLoadWarp) {
         if (threadIdx.x % 32 == 0) load_role(sm, p, &tm_q, &tm_k, &tm_v);
         __syncwarp();
     } else if (warp == kMmaWarp) {
         if (threadIdx.x % 32 == 0) mma_role(sm, p, tmem);
         __syncwarp();
     }
-
     tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp) {
-        __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
