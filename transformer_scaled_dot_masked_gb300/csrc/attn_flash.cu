@@ -9,8 +9,11 @@
 //   warps 0-3  softmax group of slot 0 (thread t owns query row t of the slot)
 //   warps 4-7  softmax group of slot 1
 //   warp 8     TMA producer (one lane): Q tiles, then K/V tiles into a 4-stage ring
-//   warp 9     MMA issuer (one lane) + TMEM allocation for the CTA
-//   warps 10-11 idle: they complete the third warpgroup so that setmaxnreg can
+//   warp 9     Q K^T MMA issuer (one lane) + TMEM allocation for the CTA
+//   warp 10    P V MMA issuer (one lane): a second issuing thread on another
+//              SM sub-partition, so S for the next key tile is never queued
+//              behind P V of the current one in one thread's program order
+//   warp 11    idle: it completes the third warpgroup so that setmaxnreg can
 //              move registers from it to the softmax warpgroups (200 each, vs 104)
 // A CTA tile has two slots of 128 query rows each:
 //   pair mode   two consecutive query tiles of one head; each K/V stage feeds both
@@ -62,7 +65,8 @@ constexpr int kD = 64;     // head width
 constexpr int kSlots = 2;
 constexpr int kStages = 4; // K/V ring depth
 constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;    // Q K^T issuer; allocates and frees TMEM
+constexpr int kMmaPvWarp = 10; // P V issuer
 constexpr int kThreads = 384;           // three full warpgroups
 constexpr uint32_t kSoftmaxRegs = 200;  // per thread, softmax warpgroups (setmaxnreg; spill-free)
 constexpr uint32_t kControlRegs = 104;  // per thread, producer/MMA warpgroup
@@ -91,7 +95,7 @@ struct alignas(1024) SharedStorage {
     uint64_t q_full[kSlots], q_empty[kSlots];
     uint64_t kv_full[kStages], kv_empty[kStages];
     uint64_t s_full[kSlots], s_free[kSlots], p_full[kSlots], pv_done[kSlots], o_free[kSlots];
-    uint64_t drain;
+    uint64_t drain_s, drain_pv;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -244,12 +248,40 @@ __device__ __forceinline__ void load_role(SharedStorage &sm, const FlashParams &
     }
 }
 
-__device__ __forceinline__ void mma_role(SharedStorage &sm, const FlashParams &p, uint32_t tmem)
-{
-    uint32_t q_cnt[kSlots] = {0, 0}, s_cnt[kSlots] = {0, 0}, p_cnt[kSlots] = {0, 0}, o_cnt[kSlots] = {0, 0};
+// K/V stage used by slot s at key tile j of a CTA tile, in the order the load
+// role fills the ring: pair mode shares one stage per key tile; split mode
+// takes one stage per slot.  `seq` is the ring position of the next new stage.
+struct StageCursor {
     uint32_t seq = 0;
+    // stages of key tile j for both slots (only meaningful where j < n_kv[s])
+    __device__ __forceinline__ void next(const Tile &T, int j, uint32_t (&st)[kSlots], uint32_t (&ph)[kSlots])
+    {
+#pragma unroll
+        for (int s = 0; s < kSlots; ++s) {
+            if (j >= T.n_kv[s]) continue;
+            if (T.shared_kv && s == 1 && j < T.n_kv[0]) {
+                st[1] = st[0];
+                ph[1] = ph[0];
+                continue;
+            }
+            st[s] = seq % kStages;
+            ph[s] = (seq / kStages) & 1;
+            ++seq;
+        }
+    }
+};
+
+// S = Q K^T issuer (one lane of its own warp).
+__device__ __forceinline__ void mma_s_role(SharedStorage &sm, const FlashParams &p, uint32_t tmem)
+{
+    uint32_t q_cnt[kSlots] = {0, 0}, s_cnt[kSlots] = {0, 0};
+    StageCursor cur;
     bool ok = true;
     int *ab = &sm.abort_flag;
+    // descriptors of the tiles this role reads, computed once; k steps add 32 bytes (2 units)
+    const uint64_t q_desc0 = smem_desc_sw128(smem_addr(sm.q[0]), 16, 1024);
+    const uint64_t q_desc1 = smem_desc_sw128(smem_addr(sm.q[1]), 16, 1024);
+    const uint64_t k_desc = smem_desc_sw128(smem_addr(sm.k[0]), 16, 1024);
     for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
         const Tile T = decode_tile(p, t);
 #pragma unroll
@@ -259,77 +291,77 @@ __device__ __forceinline__ void mma_role(SharedStorage &sm, const FlashParams &p
             ++q_cnt[s];
         }
         const int J = max(T.n_kv[0], T.n_kv[1]);
-        int prev_stage[kSlots] = {0, 0};
-        for (int j = 0; j <= J && ok; ++j) {
-            int cur_stage[kSlots] = {0, 0};
-            if (j < J) {
+        for (int j = 0; j < J && ok; ++j) {
+            uint32_t st[kSlots] = {0, 0}, ph[kSlots] = {0, 0};
+            cur.next(T, j, st, ph);
 #pragma unroll
-                for (int s = 0; s < kSlots; ++s) {
-                    if (!ok || j >= T.n_kv[s]) continue;
-                    if (T.shared_kv && s == 1 && j < T.n_kv[0]) {
-                        cur_stage[1] = cur_stage[0];
-                        continue;
-                    }
-                    const int st = seq % kStages;
-                    ok = wait_bar(&sm.kv_full[st], (seq / kStages) & 1, ab, kSiteMmaKvFull);
-                    ++seq;
-                    cur_stage[s] = st;
-                }
+            for (int s = 0; s < kSlots; ++s) {
+                if (!ok || j >= T.n_kv[s]) continue;
+                if (!(s == 1 && T.shared_kv && j < T.n_kv[0]))
+                    if (!(ok = wait_bar(&sm.kv_full[st[s]], ph[s], ab, kSiteMmaKvFull))) continue;
+                if (!(ok = wait_bar(&sm.s_free[s], (s_cnt[s] & 1) ^ 1, ab, kSiteMmaSFree))) continue;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + s * kSlotCols + kColS;
+                const uint64_t qd = s ? q_desc1 : q_desc0;
+                const uint64_t kd = k_desc + static_cast<uint64_t>(st[s] * (kTileBytes >> 4));
 #pragma unroll
-                for (int s = 0; s < kSlots; ++s) {
-                    if (!ok || j >= T.n_kv[s]) continue;
-                    if (!(ok = wait_bar(&sm.s_free[s], (s_cnt[s] & 1) ^ 1, ab, kSiteMmaSFree))) continue;
-                    tc_fence_after();
-                    const uint32_t d_tmem = tmem + s * kSlotCols + kColS;
-                    const uint32_t qa = smem_addr(sm.q[s]);
-                    const uint32_t ka = smem_addr(sm.k[cur_stage[s]]);
-#pragma unroll
-                    for (int kk = 0; kk < kD / 16; ++kk) {
-                        // 16 bf16 of K per instruction = 32 bytes along the swizzled 128-byte row
-                        mma_ss(d_tmem, smem_desc_sw128(qa + kk * 32, 16, 1024),
-                               smem_desc_sw128(ka + kk * 32, 16, 1024), kIdescS, kk > 0);
-                    }
-                    mma_commit(&sm.s_full[s]);
-                    ++s_cnt[s];
-                    if (j == T.n_kv[s] - 1) mma_commit(&sm.q_empty[s]);
-                }
+                for (int kk = 0; kk < kD / 16; ++kk) mma_ss(d_tmem, qd + 2 * kk, kd + 2 * kk, kIdescS, kk > 0);
+                mma_commit(&sm.s_full[s]);
+                ++s_cnt[s];
+                if (j == T.n_kv[s] - 1) mma_commit(&sm.q_empty[s]);
             }
-            if (j >= 1) {
-                const int jp = j - 1;
-#pragma unroll
-                for (int s = 0; s < kSlots; ++s) {
-                    if (!ok || jp >= T.n_kv[s]) continue;
-                    if (!(ok = wait_bar(&sm.p_full[s], p_cnt[s] & 1, ab, kSiteMmaPFull))) continue;
-                    ++p_cnt[s];
-                    tc_fence_after();
-                    if (jp == 0) {
-                        // first PV of this tile overwrites O: the previous epilogue must have read it
-                        if (!(ok = wait_bar(&sm.o_free[s], (o_cnt[s] & 1) ^ 1, ab, kSiteMmaOFree))) continue;
-                        ++o_cnt[s];
-                        tc_fence_after();
-                    }
-                    const uint32_t d_tmem = tmem + s * kSlotCols + kColO;
-                    const uint32_t a_tmem = tmem + s * kSlotCols + kColP;
-                    const uint32_t va = smem_addr(sm.v[prev_stage[s]]);
-#pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk) {
-                        // keys 16kk..16kk+15: P columns 8kk.. (two bf16 per column), V rows 16kk..
-                        mma_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128(va + kk * 16 * 128, kTileBytes, 1024),
-                               kIdescPV, (jp > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    mma_commit(&sm.pv_done[s]);
-                    const bool last_user = (s == 1) || !(T.shared_kv && jp < T.n_kv[1]);
-                    if (last_user) mma_commit(&sm.kv_empty[prev_stage[s]]);
-                }
-            }
-#pragma unroll
-            for (int s = 0; s < kSlots; ++s) prev_stage[s] = cur_stage[s];
         }
     }
     if (!ok) {
-        // make sure no MMA is still writing TMEM when the CTA frees it
-        mma_commit(&sm.drain);
-        drain_wait(&sm.drain, 0);
+        mma_commit(&sm.drain_s);
+        drain_wait(&sm.drain_s, 0);
+    }
+}
+
+// O += P V issuer (one lane of its own warp).  P_j being written implies S_j
+// completed, which implies the stage's K and V landed: no kv_full wait here.
+__device__ __forceinline__ void mma_pv_role(SharedStorage &sm, const FlashParams &p, uint32_t tmem)
+{
+    uint32_t p_cnt[kSlots] = {0, 0}, o_cnt[kSlots] = {0, 0};
+    StageCursor cur;
+    bool ok = true;
+    int *ab = &sm.abort_flag;
+    const uint64_t v_desc = smem_desc_sw128(smem_addr(sm.v[0]), kTileBytes, 1024);
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        const Tile T = decode_tile(p, t);
+        const int J = max(T.n_kv[0], T.n_kv[1]);
+        for (int j = 0; j < J && ok; ++j) {
+            uint32_t st[kSlots] = {0, 0}, ph[kSlots] = {0, 0};
+            cur.next(T, j, st, ph);
+#pragma unroll
+            for (int s = 0; s < kSlots; ++s) {
+                if (!ok || j >= T.n_kv[s]) continue;
+                if (!(ok = wait_bar(&sm.p_full[s], p_cnt[s] & 1, ab, kSiteMmaPFull))) continue;
+                ++p_cnt[s];
+                tc_fence_after();
+                if (j == 0) {
+                    // the first P V of a tile overwrites O: the previous epilogue must have read it
+                    if (!(ok = wait_bar(&sm.o_free[s], (o_cnt[s] & 1) ^ 1, ab, kSiteMmaOFree))) continue;
+                    ++o_cnt[s];
+                    tc_fence_after();
+                }
+                const uint32_t d_tmem = tmem + s * kSlotCols + kColO;
+                const uint32_t a_tmem = tmem + s * kSlotCols + kColP;
+                const uint64_t vd = v_desc + static_cast<uint64_t>(st[s] * (kTileBytes >> 4));
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk) {
+                    // keys 16kk..16kk+15: P columns 8kk.. (two bf16 per column), V rows 16kk.. (2 KiB)
+                    mma_ts(d_tmem, a_tmem + kk * 8, vd + kk * (2048 >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(&sm.pv_done[s]);
+                const bool last_user = (s == 1) || !(T.shared_kv && j < T.n_kv[1]);
+                if (last_user) mma_commit(&sm.kv_empty[st[s]]);
+            }
+        }
+    }
+    if (!ok) {
+        mma_commit(&sm.drain_pv);
+        drain_wait(&sm.drain_pv, 0);
     }
 }
 
@@ -513,7 +545,8 @@ attn_flash_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             mbar_init(&sm.kv_full[st], 1);
             mbar_init(&sm.kv_empty[st], 1);
         }
-        mbar_init(&sm.drain, 1);
+        mbar_init(&sm.drain_s, 1);
+        mbar_init(&sm.drain_pv, 1);
         sm.abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -541,7 +574,10 @@ attn_flash_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (threadIdx.x % 32 == 0) load_role(sm, p, &tm_q, &tm_k, &tm_v);
         __syncwarp();
     } else if (warp == kMmaWarp) {
-        if (threadIdx.x % 32 == 0) mma_role(sm, p, tmem);
+        if (threadIdx.x % 32 == 0) mma_s_role(sm, p, tmem);
+        __syncwarp();
+    } else if (warp == kMmaPvWarp) {
+        if (threadIdx.x % 32 == 0) mma_pv_role(sm, p, tmem);
         __syncwarp();
     }
     tc_fence_before();
