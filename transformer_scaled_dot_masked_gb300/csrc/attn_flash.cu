@@ -9,10 +9,8 @@
 //   warps 0-3  softmax group of slot 0 (thread t owns query row t of the slot)
 //   warps 4-7  softmax group of slot 1
 //   warp 8     TMA producer (one lane): Q tiles, then K/V tiles into a 4-stage ring
-//   warp 9     Q K^T MMA issuer (one lane) + TMEM allocation for the CTA
-//   warp 10    P V MMA issuer (one lane): a second issuing thread on another
-//              SM sub-partition, so S for the next key tile is never queued
-//              behind P V of the current one in one thread's program order
+//   warp 9     MMA issuer of slot 0 (one lane) + TMEM allocation for the CTA
+//   warp 10    MMA issuer of slot 1 (one lane), on another SM sub-partition
 //   warp 11    idle: it completes the third warpgroup so that setmaxnreg can
 //              move registers from it to the softmax warpgroups (200 each, vs 104)
 // A CTA tile has two slots of 128 query rows each:
@@ -65,8 +63,8 @@ constexpr int kD = 64;     // head width
 constexpr int kSlots = 2;
 constexpr int kStages = 4; // K/V ring depth
 constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;    // Q K^T issuer; allocates and frees TMEM
-constexpr int kMmaPvWarp = 10; // P V issuer
+constexpr int kMmaWarp = 9;  // MMA issuer of slot 0; allocates and frees TMEM
+constexpr int kMma1Warp = 10; // MMA issuer of slot 1
 constexpr int kThreads = 384;           // three full warpgroups
 constexpr uint32_t kSoftmaxRegs = 200;  // per thread, softmax warpgroups (setmaxnreg; spill-free)
 constexpr uint32_t kControlRegs = 104;  // per thread, producer/MMA warpgroup
@@ -95,7 +93,7 @@ struct alignas(1024) SharedStorage {
     uint64_t q_full[kSlots], q_empty[kSlots];
     uint64_t kv_full[kStages], kv_empty[kStages];
     uint64_t s_full[kSlots], s_free[kSlots], p_full[kSlots], pv_done[kSlots], o_free[kSlots];
-    uint64_t drain_s, drain_pv;
+    uint64_t drain[kSlots];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -248,120 +246,118 @@ __device__ __forceinline__ void load_role(SharedStorage &sm, const FlashParams &
     }
 }
 
-// K/V stage used by slot s at key tile j of a CTA tile, in the order the load
-// role fills the ring: pair mode shares one stage per key tile; split mode
-// takes one stage per slot.  `seq` is the ring position of the next new stage.
-struct StageCursor {
-    uint32_t seq = 0;
-    // stages of key tile j for both slots (only meaningful where j < n_kv[s])
-    __device__ __forceinline__ void next(const Tile &T, int j, uint32_t (&st)[kSlots], uint32_t (&ph)[kSlots])
-    {
-#pragma unroll
-        for (int s = 0; s < kSlots; ++s) {
-            if (j >= T.n_kv[s]) continue;
-            if (T.shared_kv && s == 1 && j < T.n_kv[0]) {
-                st[1] = st[0];
-                ph[1] = ph[0];
-                continue;
-            }
-            st[s] = seq % kStages;
-            ph[s] = (seq / kStages) & 1;
-            ++seq;
-        }
-    }
-};
-
-// S = Q K^T issuer (one lane of its own warp).
-__device__ __forceinline__ void mma_s_role(SharedStorage &sm, const FlashParams &p, uint32_t tmem)
+// Ring position of the stage holding key tile j for slot s in CTA tile T: the
+// load role fills the ring per CTA tile, key tile by key tile; in pair mode one
+// stage per key tile serves both slots, in split mode each slot takes its own
+// stage (slot 0 first).
+__device__ __forceinline__ uint32_t stage_offset(const Tile &T, int j, int s)
 {
-    uint32_t q_cnt[kSlots] = {0, 0}, s_cnt[kSlots] = {0, 0};
-    StageCursor cur;
-    bool ok = true;
-    int *ab = &sm.abort_flag;
-    // descriptors of the tiles this role reads, computed once; k steps add 32 bytes (2 units)
-    const uint64_t q_desc0 = smem_desc_sw128(smem_addr(sm.q[0]), 16, 1024);
-    const uint64_t q_desc1 = smem_desc_sw128(smem_addr(sm.q[1]), 16, 1024);
-    const uint64_t k_desc = smem_desc_sw128(smem_addr(sm.k[0]), 16, 1024);
-    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-        const Tile T = decode_tile(p, t);
-#pragma unroll
-        for (int s = 0; s < kSlots; ++s) {
-            if (!ok || T.n_kv[s] == 0) continue;
-            ok = wait_bar(&sm.q_full[s], q_cnt[s] & 1, ab, kSiteMmaQFull);
-            ++q_cnt[s];
-        }
-        const int J = max(T.n_kv[0], T.n_kv[1]);
-        for (int j = 0; j < J && ok; ++j) {
-            uint32_t st[kSlots] = {0, 0}, ph[kSlots] = {0, 0};
-            cur.next(T, j, st, ph);
-#pragma unroll
-            for (int s = 0; s < kSlots; ++s) {
-                if (!ok || j >= T.n_kv[s]) continue;
-                if (!(s == 1 && T.shared_kv && j < T.n_kv[0]))
-                    if (!(ok = wait_bar(&sm.kv_full[st[s]], ph[s], ab, kSiteMmaKvFull))) continue;
-                if (!(ok = wait_bar(&sm.s_free[s], (s_cnt[s] & 1) ^ 1, ab, kSiteMmaSFree))) continue;
-                tc_fence_after();
-                const uint32_t d_tmem = tmem + s * kSlotCols + kColS;
-                const uint64_t qd = s ? q_desc1 : q_desc0;
-                const uint64_t kd = k_desc + static_cast<uint64_t>(st[s] * (kTileBytes >> 4));
-#pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk) mma_ss(d_tmem, qd + 2 * kk, kd + 2 * kk, kIdescS, kk > 0);
-                mma_commit(&sm.s_full[s]);
-                ++s_cnt[s];
-                if (j == T.n_kv[s] - 1) mma_commit(&sm.q_empty[s]);
-            }
-        }
-    }
-    if (!ok) {
-        mma_commit(&sm.drain_s);
-        drain_wait(&sm.drain_s, 0);
-    }
+    if (T.shared_kv) return static_cast<uint32_t>(j);
+    return static_cast<uint32_t>(min(j, T.n_kv[0]) + min(j, T.n_kv[1]) + ((s == 1 && j < T.n_kv[0]) ? 1 : 0));
 }
 
-// O += P V issuer (one lane of its own warp).  P_j being written implies S_j
-// completed, which implies the stage's K and V landed: no kv_full wait here.
-__device__ __forceinline__ void mma_pv_role(SharedStorage &sm, const FlashParams &p, uint32_t tmem)
+__device__ __forceinline__ uint32_t stages_of(const Tile &T)
 {
-    uint32_t p_cnt[kSlots] = {0, 0}, o_cnt[kSlots] = {0, 0};
-    StageCursor cur;
+    return T.shared_kv ? static_cast<uint32_t>(max(T.n_kv[0], T.n_kv[1]))
+                       : static_cast<uint32_t>(T.n_kv[0] + T.n_kv[1]);
+}
+
+// MMA issuer of one slot (one lane of its own warp): S_s(j) = Q_s K_j^T as soon
+// as the softmax has read S_s(j-1), and O_s += P_s(j-1) V_(j-1) as soon as P is
+// written.  Each slot has its own issuing thread so that neither slot's P V
+// waits behind the other's in one thread's program order.  A K/V stage shared by
+// both slots (pair mode) is released when both issuers have arrived on its
+// kv_empty barrier (count 2): after their P V completes, or, for a slot that
+// does not read that stage, once the stage is loaded (so the arrival can only
+// count towards the stage's current fill).  Descriptors are computed once.
+__device__ __forceinline__ void mma_role(SharedStorage &sm, const FlashParams &p, uint32_t tmem, int s)
+{
+    uint32_t q_cnt = 0, s_cnt = 0, p_cnt = 0, o_cnt = 0;
+    uint32_t seq_base = 0;
     bool ok = true;
     int *ab = &sm.abort_flag;
-    const uint64_t v_desc = smem_desc_sw128(smem_addr(sm.v[0]), kTileBytes, 1024);
+    uint64_t *q_full = &sm.q_full[s], *q_empty = &sm.q_empty[s], *s_full = &sm.s_full[s];
+    uint64_t *s_free = &sm.s_free[s], *p_full = &sm.p_full[s], *pv_done = &sm.pv_done[s], *o_free = &sm.o_free[s];
+    const uint32_t desc_hi = static_cast<uint32_t>(smem_desc_sw128(0, 0, 1024) >> 32);
+    const uint32_t q_lo = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.q[s]), 16, 1024));
+    const uint32_t k_lo = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.k[0]), 16, 1024));
+    const uint32_t v_lo = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.v[0]), kTileBytes, 1024));
+    const uint32_t s_tmem = tmem + s * kSlotCols + kColS;
+    const uint32_t p_tmem = tmem + s * kSlotCols + kColP;
+    const uint32_t o_tmem = tmem + s * kSlotCols + kColO;
     for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
         const Tile T = decode_tile(p, t);
-        const int J = max(T.n_kv[0], T.n_kv[1]);
-        for (int j = 0; j < J && ok; ++j) {
-            uint32_t st[kSlots] = {0, 0}, ph[kSlots] = {0, 0};
-            cur.next(T, j, st, ph);
-#pragma unroll
-            for (int s = 0; s < kSlots; ++s) {
-                if (!ok || j >= T.n_kv[s]) continue;
-                if (!(ok = wait_bar(&sm.p_full[s], p_cnt[s] & 1, ab, kSiteMmaPFull))) continue;
-                ++p_cnt[s];
+        const int n = s ? T.n_kv[1] : T.n_kv[0];
+        if (n > 0) {
+            ok = wait_bar(q_full, q_cnt & 1, ab, kSiteMmaQFull);
+            ++q_cnt;
+        }
+        for (int j = 0; j <= n && ok; ++j) {
+            if (j < n) {
+                // S(j)
+                const uint32_t seq = seq_base + stage_offset(T, j, s);
+                const uint32_t st = seq % kStages;
+                ok = wait_bar(&sm.kv_full[st], (seq / kStages) & 1, ab, kSiteMmaKvFull);
+                if (ok) ok = wait_bar(s_free, (s_cnt & 1) ^ 1, ab, kSiteMmaSFree);
+                if (!ok) break;
                 tc_fence_after();
-                if (j == 0) {
+                const uint32_t kd = k_lo + st * (kTileBytes >> 4);
+                // 16 bf16 of K per step = 32 bytes (2 descriptor units) along the swizzled rows
+                mma_ss_k<0, 0>(s_tmem, q_lo, kd, desc_hi, kIdescS, 0u);
+                mma_ss_k<2, 2>(s_tmem, q_lo, kd, desc_hi, kIdescS, 1u);
+                mma_ss_k<4, 4>(s_tmem, q_lo, kd, desc_hi, kIdescS, 1u);
+                mma_ss_k<6, 6>(s_tmem, q_lo, kd, desc_hi, kIdescS, 1u);
+                mma_commit(s_full);
+                ++s_cnt;
+                if (j == n - 1) mma_commit(q_empty);
+            }
+            if (j >= 1) {
+                // P V(j - 1)
+                const int jp = j - 1;
+                ok = wait_bar(p_full, p_cnt & 1, ab, kSiteMmaPFull);
+                if (!ok) break;
+                ++p_cnt;
+                tc_fence_after();
+                if (jp == 0) {
                     // the first P V of a tile overwrites O: the previous epilogue must have read it
-                    if (!(ok = wait_bar(&sm.o_free[s], (o_cnt[s] & 1) ^ 1, ab, kSiteMmaOFree))) continue;
-                    ++o_cnt[s];
+                    ok = wait_bar(o_free, (o_cnt & 1) ^ 1, ab, kSiteMmaOFree);
+                    if (!ok) break;
+                    ++o_cnt;
                     tc_fence_after();
                 }
-                const uint32_t d_tmem = tmem + s * kSlotCols + kColO;
-                const uint32_t a_tmem = tmem + s * kSlotCols + kColP;
-                const uint64_t vd = v_desc + static_cast<uint64_t>(st[s] * (kTileBytes >> 4));
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    // keys 16kk..16kk+15: P columns 8kk.. (two bf16 per column), V rows 16kk.. (2 KiB)
-                    mma_ts(d_tmem, a_tmem + kk * 8, vd + kk * (2048 >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-                }
-                mma_commit(&sm.pv_done[s]);
-                const bool last_user = (s == 1) || !(T.shared_kv && j < T.n_kv[1]);
-                if (last_user) mma_commit(&sm.kv_empty[st[s]]);
+                const uint32_t st = (seq_base + stage_offset(T, jp, s)) % kStages;
+                const uint32_t vd = v_lo + st * (kTileBytes >> 4);
+                // keys 16kk..16kk+15 per step: P columns 8kk.. (two bf16 per column), V rows
+                // 16kk.. (2 KiB = 128 descriptor units)
+                const uint32_t acc0 = jp > 0 ? 1u : 0u;
+                mma_ts_k<0, 0>(o_tmem, p_tmem, vd, desc_hi, kIdescPV, acc0);
+                mma_ts_k<8, 128>(o_tmem, p_tmem, vd, desc_hi, kIdescPV, 1u);
+                mma_ts_k<16, 256>(o_tmem, p_tmem, vd, desc_hi, kIdescPV, 1u);
+                mma_ts_k<24, 384>(o_tmem, p_tmem, vd, desc_hi, kIdescPV, 1u);
+                mma_ts_k<32, 512>(o_tmem, p_tmem, vd, desc_hi, kIdescPV, 1u);
+                mma_ts_k<40, 640>(o_tmem, p_tmem, vd, desc_hi, kIdescPV, 1u);
+                mma_ts_k<48, 768>(o_tmem, p_tmem, vd, desc_hi, kIdescPV, 1u);
+                mma_ts_k<56, 896>(o_tmem, p_tmem, vd, desc_hi, kIdescPV, 1u);
+                mma_commit(pv_done);
+                mma_commit(&sm.kv_empty[st]);
             }
         }
+        if (ok && T.shared_kv) {
+            // stages of this CTA tile that only the other slot reads: arrive once each is loaded
+            const int J = max(T.n_kv[0], T.n_kv[1]);
+            for (int j = n; j < J && ok; ++j) {
+                const uint32_t seq = seq_base + static_cast<uint32_t>(j);
+                const uint32_t st = seq % kStages;
+                ok = wait_bar(&sm.kv_full[st], (seq / kStages) & 1, ab, kSiteMmaKvFull);
+                if (ok) mbar_arrive(&sm.kv_empty[st]);
+            }
+        }
+        seq_base += stages_of(T);
     }
     if (!ok) {
-        mma_commit(&sm.drain_pv);
-        drain_wait(&sm.drain_pv, 0);
+        // make sure no MMA is still writing TMEM when the CTA frees it
+        mma_commit(&sm.drain[s]);
+        drain_wait(&sm.drain[s], 0);
     }
 }
 
@@ -445,50 +441,49 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
             const float alpha = grow ? ex2(m_run - m_new) : 1.f; // 0 on the first tile
             const float m_sub = (m_use == -CUDART_INF_F) ? 0.f : m_use;
 
-            if (j > 0) {
-                // P and O are still in use by the previous P V until it completes
-                ok = warp_all(wait_bar(&sm.pv_done[slot], pv_cnt & 1, ab, kSiteSmPvDone));
-                if (!ok) break;
-                ++pv_cnt;
-                tc_fence_after();
-            }
-            // exponentials, 32 keys at a time, written straight to TMEM as bf16 pairs;
-            // the exponent argument and the row sum use packed two-lane fp32 ops
+            // exponentials into registers as bf16 pairs; the exponent argument and
+            // the row sum use packed two-lane fp32 ops
             const uint64_t mul2 = boundary ? f2(1.f, 1.f) : f2(sl2, sl2);
             const uint64_t sub2 = f2(-m_sub, -m_sub);
             uint64_t acc2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
+            uint32_t pk[kBN / 2];
 #pragma unroll
-            for (int cc = 0; cc < kBN / 32; ++cc) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int c2 = 0; c2 < 16; ++c2) {
-                    const int c = cc * 32 + 2 * c2;
-                    float a0, a1;
-                    unf2(fma2(f2(x[c], x[c + 1]), mul2, sub2), a0, a1);
-                    const float e0 = ex2(a0), e1 = ex2(a1);
-                    acc2[c2 & 1] = add2(acc2[c2 & 1], f2(e0, e1));
-                    pk[c2] = pack_bf16x2(e0, e1);
-                }
-                tmem_st16(t_p + cc * 16, pk);
+            for (int c2 = 0; c2 < kBN / 2; ++c2) {
+                const int c = 2 * c2;
+                float a0, a1;
+                unf2(fma2(f2(x[c], x[c + 1]), mul2, sub2), a0, a1);
+                const float e0 = ex2(a0), e1 = ex2(a1);
+                acc2[c2 & 1] = add2(acc2[c2 & 1], f2(e0, e1));
+                pk[c2] = pack_bf16x2(e0, e1);
             }
             float s0, s1, s2, s3;
             unf2(acc2[0], s0, s1);
             unf2(acc2[1], s2, s3);
-            const float sum = (s0 + s1) + (s2 + s3);
-            l_run = l_run * alpha + sum;
-            if (j > 0 && __any_sync(0xffffffffu, grow)) {
-                // move O to the new reference max (rare: only when the max grew by > 2^8)
+            l_run = l_run * alpha + ((s0 + s1) + (s2 + s3));
+
+            if (j > 0) {
+                // P and O are still in use by the previous P V until it completes;
+                // waiting only now lets the exponentials above overlap with it
+                ok = warp_all(wait_bar(&sm.pv_done[slot], pv_cnt & 1, ab, kSiteSmPvDone));
+                if (!ok) break;
+                ++pv_cnt;
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, grow)) {
+                    // move O to the new reference max (rare: only when the max grew by > 2^8)
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    uint32_t orr[32];
-                    tmem_ld32(t_o + 32 * h2, orr);
-                    tmem_wait_ld();
-                    reg_fence32(orr);
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        uint32_t orr[32];
+                        tmem_ld32(t_o + 32 * h2, orr);
+                        tmem_wait_ld();
+                        reg_fence32(orr);
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) orr[c] = __float_as_uint(__uint_as_float(orr[c]) * alpha);
-                    tmem_st32(t_o + 32 * h2, orr);
+                        for (int c = 0; c < 32; ++c) orr[c] = __float_as_uint(__uint_as_float(orr[c]) * alpha);
+                        tmem_st32(t_o + 32 * h2, orr);
+                    }
                 }
             }
+            tmem_st32(t_p, pk);
+            tmem_st32(t_p + 32, pk + 32);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&sm.p_full[slot]);
@@ -543,10 +538,10 @@ attn_flash_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         for (int st = 0; st < kStages; ++st) {
             mbar_init(&sm.kv_full[st], 1);
-            mbar_init(&sm.kv_empty[st], 1);
+            mbar_init(&sm.kv_empty[st], p.pair_mode ? 2 : 1); // pair mode: one arrival per slot issuer
         }
-        mbar_init(&sm.drain_s, 1);
-        mbar_init(&sm.drain_pv, 1);
+        mbar_init(&sm.drain[0], 1);
+        mbar_init(&sm.drain[1], 1);
         sm.abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -573,11 +568,8 @@ attn_flash_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (warp == kLoadWarp) {
         if (threadIdx.x % 32 == 0) load_role(sm, p, &tm_q, &tm_k, &tm_v);
         __syncwarp();
-    } else if (warp == kMmaWarp) {
-        if (threadIdx.x % 32 == 0) mma_s_role(sm, p, tmem);
-        __syncwarp();
-    } else if (warp == kMmaPvWarp) {
-        if (threadIdx.x % 32 == 0) mma_pv_role(sm, p, tmem);
+    } else if (warp == kMmaWarp || warp == kMma1Warp) {
+        if (threadIdx.x % 32 == 0) mma_role(sm, p, tmem, warp == kMmaWarp ? 0 : 1);
         __syncwarp();
     }
     tc_fence_before();
