@@ -83,6 +83,19 @@ def row_pairs(w, lengths, rows) -> float:
     return float((np.minimum(i + 1, L) if w.causal else L).sum())
 
 
+# DRAM bytes (read + write) of one flash-kernel launch on the default workload,
+# from an ncu capture (profiles/attn_flash_long_causal_8192.md), keyed by a hash of
+# the kernel source it was taken on: any later change to the kernel reports null.
+MEASURED_TRAFFIC = {"f53278096ef75adc": 839323904 + 47733760}
+
+
+def measured_traffic():
+    import hashlib
+    path = os.path.join(ROOT, "transformer_scaled_dot_masked_gb300", "csrc", "attn_flash.cu")
+    key = hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+    return MEASURED_TRAFFIC.get(key)
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -150,6 +163,21 @@ def to_device(x, dtype, torch, device):
     if dtype == "bf16":
         return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(device)
     return torch.from_numpy(np.ascontiguousarray(x)).to(device)
+
+
+def max_over_ranks(ms, dist, device):
+    """The slowest rank's time: every rank must be done for the job to be done."""
+    import torch
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(ms)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank, world, ms):
+    """Aggregate throughput: the work of all ranks over the slowest rank's time."""
+    return flops_per_rank * world / (ms * 1e-3) / 1e12
 
 
 def time_launches(fn, steps, torch, stream):
@@ -333,9 +361,7 @@ def main():
         ms = time_launches(step, args.steps, torch, stream)
     torch.cuda.synchronize()
     if dist:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(ms, dist, device)
         dist.barrier()
     st, info = attn.device_status()
     if st != 0:
@@ -343,7 +369,7 @@ def main():
 
     peak_tf, peak_hbm, peak_src = load_peaks()
     flops_nom = nominal_flops(w)
-    value = flops_nom * world / (ms * 1e-3) / 1e12
+    value = whole_job_tflops(flops_nom, world, ms)
     flops_use = useful_flops(w, inp.key_lengths)
     achieved = flops_use / (ms * 1e-3) / 1e12
     result = {
@@ -356,7 +382,8 @@ def main():
                    "l2": "inputs+output 268 MB > L2, no flush between steps",
                    "parallelism": f"replicas x{world} ((batch, head) work is independent)"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": achieved / peak_tf, "traffic": None,
+                     "frac": achieved / peak_tf,
+                     "traffic": measured_traffic() if args.workload == 5 else None,
                      "peak_source": f"{peak_src} bf16 dense burst",
                      "algorithmic": "4*d_k FLOPs per allowed (query, key) pair per launch"},
         "gpu_launches": args.steps,
