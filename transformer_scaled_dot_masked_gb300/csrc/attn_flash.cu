@@ -5,7 +5,7 @@
 // M from §03 "Decoder layer" and §04), one 128-key tile at a time with an
 // online softmax, so no score matrix larger than one tile ever exists.
 //
-// CTA organisation (persistent: one CTA per SM, CTA tiles strided over the grid)
+// CTA organisation (persistent: one CTA per SM; CTA tiles dealt to CTAs in snake order)
 //   warps 0-3  softmax group of slot 0 (thread t owns query row t of the slot)
 //   warps 4-7  softmax group of slot 1
 //   warp 8     TMA producer (one lane): Q tiles, then K/V tiles into a 4-stage ring
@@ -117,6 +117,16 @@ struct Tile {
     bool shared_kv;
 };
 
+// The t-th CTA tile this CTA processes in round r: rounds walk the heaviest-first
+// tile order, alternating direction (CTA c takes position c of even rounds and
+// position G-1-c of odd rounds), which evens out the causal work per CTA (the
+// heaviest and lightest tiles of consecutive rounds land on the same CTA).
+__device__ __forceinline__ int tile_of(int r)
+{
+    const int k = (r & 1) ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
+    return r * static_cast<int>(gridDim.x) + k;
+}
+
 __device__ __forceinline__ Tile decode_tile(const FlashParams &p, int t)
 {
     Tile T;
@@ -198,7 +208,7 @@ __device__ __forceinline__ void load_role(SharedStorage &sm, const FlashParams &
     uint32_t q_cnt[kSlots] = {0, 0};
     uint32_t seq = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+    for (int r = 0, t = tile_of(0); t < p.num_tiles && ok; t = tile_of(++r)) {
         const Tile T = decode_tile(p, t);
 #pragma unroll
         for (int s = 0; s < kSlots; ++s) {
@@ -285,7 +295,7 @@ __device__ __forceinline__ void mma_role(SharedStorage &sm, const FlashParams &p
     const uint32_t s_tmem = tmem + s * kSlotCols + kColS;
     const uint32_t p_tmem = tmem + s * kSlotCols + kColP;
     const uint32_t o_tmem = tmem + s * kSlotCols + kColO;
-    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+    for (int r = 0, t = tile_of(0); t < p.num_tiles && ok; t = tile_of(++r)) {
         const Tile T = decode_tile(p, t);
         const int n = s ? T.n_kv[1] : T.n_kv[0];
         if (n > 0) {
@@ -375,7 +385,7 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
     uint32_t s_cnt = 0, pv_cnt = 0;
     bool ok = true;
 
-    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+    for (int r = 0, t = tile_of(0); t < p.num_tiles && ok; t = tile_of(++r)) {
         const Tile T = decode_tile(p, t);
         // select this slot's fields without indexing the per-slot arrays at run time
         const bool active = slot ? T.active[1] : T.active[0];
