@@ -321,6 +321,8 @@ def main():
     ap.add_argument("--kernel-only", action="store_true",
                     help="time only the main kernel loop (for profiler runs)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-workspace", action="store_true",
+                    help="call attn_fwd (static tile schedule) instead of attn_fwd_ws")
     args = ap.parse_args()
     w = WORKLOADS[args.workload]
 
@@ -347,9 +349,10 @@ def main():
     out = torch.empty_like(q)
     stream = torch.cuda.current_stream(device)
     kern = attn.select_kernel(w.B, w.h, w.m, w.n, w.d, 0 if w.dtype == "bf16" else 1, w.mask)
+    ws = None if args.no_workspace else attn.make_workspace(device)
 
     def step():
-        attn.attn_fwd(q, k, v, lens, w.mask, w.scale, out=out, stream=stream)
+        attn.attn_fwd(q, k, v, lens, w.mask, w.scale, out=out, stream=stream, workspace=ws)
 
     for _ in range(args.warmup):
         step()
@@ -379,6 +382,7 @@ def main():
         "config": {"workload": w.description, "B": w.B, "h": w.h, "m": w.m, "n": w.n, "d_k": w.d,
                    "mask": "causal" if w.causal else ("key_padding" if w.padded else "none"),
                    "kernel": attn._native.KERNEL_NAMES[kern],
+                   "entry_point": "attn_fwd" if ws is None else "attn_fwd_ws (dynamic tile schedule)",
                    "l2": "inputs+output 268 MB > L2, no flush between steps",
                    "parallelism": f"replicas x{world} ((batch, head) work is independent)"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
@@ -402,7 +406,7 @@ def main():
             dk.copy_(hk, non_blocking=True)
             dv.copy_(hv, non_blocking=True)
             dl.copy_(hl, non_blocking=True)
-            attn.attn_fwd(dq, dk, dv, dl, w.mask, w.scale, out=do, stream=stream)
+            attn.attn_fwd(dq, dk, dv, dl, w.mask, w.scale, out=do, stream=stream, workspace=ws)
             ho.copy_(do, non_blocking=True)
 
         e2e_steps = max(3, min(args.steps, 50))

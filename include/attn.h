@@ -32,6 +32,7 @@
  * Ownership: the caller allocates and owns every buffer.  The library keeps
  * no per-call state and allocates no device memory; the only global state is
  * a small device status word that records a kernel giving up a bounded wait.
+ * attn_fwd_ws additionally takes a caller-owned workspace (see there).
  *
  * Asynchrony: every compute entry point only enqueues work on the given
  * stream (a cudaStream_t; NULL is the legacy default stream) and returns.  A
@@ -45,6 +46,7 @@
 #ifndef ATTN_GB300_ATTN_H
 #define ATTN_GB300_ATTN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -132,6 +134,32 @@ attn_status attn_fwd_kernel(const void *Q, const void *K, const void *V,
                             const int32_t *key_lengths, int mask_kind, float scale,
                             void *out, const attn_dims *dims, void *stream,
                             int kernel);
+
+/* Bytes of device workspace attn_fwd_ws needs (host only, no CUDA call). */
+size_t attn_workspace_size(void);
+
+/*
+ * attn_fwd with a caller-owned device workspace of at least
+ * attn_workspace_size() bytes, 16-byte aligned, not overlapping any tensor.
+ * The tensor-core kernels use it for a dynamic tile schedule: CTAs claim
+ * tiles from a counter in the workspace, so faster SMs take more tiles and
+ * the last tiles finish closer together (the schedule of attn_fwd is
+ * static).  Results are identical either way.
+ *
+ * Contract: the workspace must be zero-filled before its first use (for
+ * example with cudaMemsetAsync); every call returns it to zero-filled when
+ * its kernel finishes, also after a bounded wait gave up.  Calls that may
+ * run at the same time on the GPU (different streams) must use different
+ * workspaces; calls ordered on one stream may share one.
+ *
+ * Errors as attn_fwd, plus: workspace NULL (ATTN_ERR_NULL), too small
+ * (ATTN_ERR_SHAPE), unaligned (ATTN_ERR_ALIGN), overlapping a tensor
+ * (ATTN_ERR_ALIAS).
+ */
+attn_status attn_fwd_ws(const void *Q, const void *K, const void *V,
+                        const int32_t *key_lengths, int mask_kind, float scale,
+                        void *out, const attn_dims *dims, void *stream,
+                        void *workspace, size_t workspace_bytes);
 
 /* The kernel attn_fwd would run for these dims and mask (host only, no CUDA call);
  * ATTN_KERNEL_AUTO (0) if the call would be rejected. */

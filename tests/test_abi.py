@@ -96,3 +96,19 @@ def test_rejects_unsupported_kernel_choice():
 
 def test_null_dims():
     assert N.lib.attn_fwd(A, B_, C, None, 0, ctypes.c_float(0.125), O, None, None) == 1
+
+
+def _call_ws(ws=0x6000000, ws_bytes=None, **kw):
+    d = N.make_dims(*(kw.pop("dims", (2, 2, 8, 8, 64, 0))))
+    ws_bytes = N.workspace_size() if ws_bytes is None else ws_bytes
+    return N.fwd_ws_raw(kw.get("q", A), B_, C, L, 0, 0.125, kw.get("out", O), d, None, ws, ws_bytes)
+
+
+def test_workspace_validation():
+    assert N.workspace_size() >= 8
+    assert _call_ws(ws=None) == 1
+    assert _call_ws(ws_bytes=N.workspace_size() - 1) == 2
+    assert _call_ws(ws=0x6000000 + 4) == 5
+    assert _call_ws(ws=O + 64) == 10          # inside out
+    assert _call_ws(ws=A) == 10               # inside Q
+    assert _call_ws(q=A + 8) == 5             # tensor checks still apply

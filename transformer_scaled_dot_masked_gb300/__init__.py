@@ -15,7 +15,7 @@ from . import _native
 from ._native import (AttnError, KERNEL_AUTO, KERNEL_FLASH, KERNEL_SHORT, KERNEL_SIMT, MASK_CAUSAL,
                       MASK_KEY_PADDING, MASK_NONE, DTYPE_BF16, DTYPE_FP32)
 
-__all__ = ["attn_fwd", "AttnError", "select_kernel", "device_status", "MASK_NONE", "MASK_KEY_PADDING",
+__all__ = ["attn_fwd", "AttnError", "select_kernel", "device_status", "make_workspace", "workspace_size", "MASK_NONE", "MASK_KEY_PADDING",
            "MASK_CAUSAL", "KERNEL_AUTO", "KERNEL_FLASH", "KERNEL_SHORT", "KERNEL_SIMT"]
 
 
@@ -28,14 +28,28 @@ def _dtype_code(t) -> int:
     raise TypeError(f"attn_fwd supports bfloat16 and float32 tensors, got {t.dtype}")
 
 
+def workspace_size() -> int:
+    """Bytes of device workspace ``attn_fwd(..., workspace=...)`` needs."""
+    return _native.workspace_size()
+
+
+def make_workspace(device=None):
+    """A zero-filled workspace for ``attn_fwd(..., workspace=...)`` (torch allocation)."""
+    import torch
+    return torch.zeros(workspace_size(), dtype=torch.uint8, device=device or "cuda")
+
+
 def attn_fwd(q, k, v, key_lengths=None, mask_kind: int = MASK_NONE, scale: Optional[float] = None,
-             out=None, kernel: int = KERNEL_AUTO, stream=None):
+             out=None, kernel: int = KERNEL_AUTO, stream=None, workspace=None):
     """Masked scaled dot-product attention over [B, h, len, d_k] CUDA tensors.
 
     q: [B, h, m, d_k]; k, v: [B, h, n, d_k]; same dtype (bf16 or fp32), contiguous,
     on the current CUDA device.  key_lengths: int32 [B] CUDA tensor (needed for
     MASK_KEY_PADDING).  scale defaults to 1/sqrt(d_k).  out: optional preallocated
     [B, h, m, d_k] tensor.  Enqueued on ``stream`` (default: torch's current stream).
+    workspace: optional zero-filled CUDA buffer from ``make_workspace`` (selects the
+    dynamic tile schedule, attn_fwd_ws; not combinable with an explicit kernel).
+    Calls that may overlap on the GPU need different workspaces.
     """
     import torch
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
@@ -62,8 +76,17 @@ def attn_fwd(q, k, v, key_lengths=None, mask_kind: int = MASK_NONE, scale: Optio
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     dims = _native.make_dims(B, h, m, n, d, _dtype_code(q))
-    st = _native.fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), lens_ptr, mask_kind, scale,
-                         out.data_ptr(), dims, stream.cuda_stream, kernel)
+    if workspace is not None:
+        if kernel != KERNEL_AUTO:
+            raise ValueError("a workspace call always uses the automatic kernel choice")
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        st = _native.fwd_ws_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), lens_ptr, mask_kind, scale,
+                                out.data_ptr(), dims, stream.cuda_stream, workspace.data_ptr(),
+                                workspace.numel() * workspace.element_size())
+    else:
+        st = _native.fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), lens_ptr, mask_kind, scale,
+                             out.data_ptr(), dims, stream.cuda_stream, kernel)
     if st != _native.ATTN_OK:
         raise AttnError(st)
     return out

@@ -41,6 +41,10 @@ lib.attn_fwd.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_float, _vp,
 lib.attn_fwd.restype = ctypes.c_int
 lib.attn_fwd_kernel.argtypes = lib.attn_fwd.argtypes + [ctypes.c_int]
 lib.attn_fwd_kernel.restype = ctypes.c_int
+lib.attn_workspace_size.argtypes = []
+lib.attn_workspace_size.restype = ctypes.c_size_t
+lib.attn_fwd_ws.argtypes = lib.attn_fwd.argtypes + [_vp, ctypes.c_size_t]
+lib.attn_fwd_ws.restype = ctypes.c_int
 lib.attn_select_kernel.argtypes = [ctypes.POINTER(AttnDims), ctypes.c_int]
 lib.attn_select_kernel.restype = ctypes.c_int
 lib.attn_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32)]
@@ -81,6 +85,17 @@ def fwd_raw(q_ptr, k_ptr, v_ptr, lens_ptr, mask_kind, scale, out_ptr, dims: Attn
     """Direct call with integer device pointers; returns the status code."""
     return lib.attn_fwd_kernel(q_ptr, k_ptr, v_ptr, lens_ptr, int(mask_kind), float(scale), out_ptr,
                                ctypes.byref(dims), stream_ptr, int(kernel))
+
+
+def workspace_size() -> int:
+    return int(lib.attn_workspace_size())
+
+
+def fwd_ws_raw(q_ptr, k_ptr, v_ptr, lens_ptr, mask_kind, scale, out_ptr, dims: AttnDims, stream_ptr,
+               ws_ptr, ws_bytes) -> int:
+    """attn_fwd_ws with integer device pointers; returns the status code."""
+    return lib.attn_fwd_ws(q_ptr, k_ptr, v_ptr, lens_ptr, int(mask_kind), float(scale), out_ptr,
+                           ctypes.byref(dims), stream_ptr, ws_ptr, int(ws_bytes))
 
 
 def device_status(stream_ptr=None):

@@ -63,11 +63,10 @@ attn_status validate(const void *Q, const void *K, const void *V, const int32_t 
 
 } // namespace
 
-extern "C" {
+namespace {
 
-attn_status attn_fwd_kernel(const void *Q, const void *K, const void *V, const int32_t *key_lengths,
-                            int mask_kind, float scale, void *out, const attn_dims *dims, void *stream,
-                            int kernel)
+attn_status run(const void *Q, const void *K, const void *V, const int32_t *key_lengths, int mask_kind, float scale,
+                void *out, const attn_dims *dims, void *stream, int kernel, int *tile_counter)
 {
     const attn_status st = validate(Q, K, V, key_lengths, mask_kind, scale, out, dims);
     if (st != ATTN_OK) return st;
@@ -95,16 +94,49 @@ attn_status attn_fwd_kernel(const void *Q, const void *K, const void *V, const i
         break;
     case ATTN_KERNEL_FLASH:
         if (!p.bf16 || p.d != 64) return ATTN_ERR_UNSUPPORTED;
-        e = attn::launch_flash(p, /*pair_mode=*/true, s);
+        e = attn::launch_flash(p, /*pair_mode=*/true, tile_counter, s);
         break;
     case ATTN_KERNEL_SHORT:
         if (!p.bf16 || p.d != 64 || p.m > 128) return ATTN_ERR_UNSUPPORTED;
-        e = attn::launch_flash(p, /*pair_mode=*/false, s);
+        e = attn::launch_flash(p, /*pair_mode=*/false, tile_counter, s);
         break;
     default:
         return ATTN_ERR_UNSUPPORTED;
     }
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+} // namespace
+
+extern "C" {
+
+attn_status attn_fwd_kernel(const void *Q, const void *K, const void *V, const int32_t *key_lengths,
+                            int mask_kind, float scale, void *out, const attn_dims *dims, void *stream,
+                            int kernel)
+{
+    return run(Q, K, V, key_lengths, mask_kind, scale, out, dims, stream, kernel, nullptr);
+}
+
+size_t attn_workspace_size(void) { return attn::kWorkspaceBytes; }
+
+attn_status attn_fwd_ws(const void *Q, const void *K, const void *V, const int32_t *key_lengths, int mask_kind,
+                        float scale, void *out, const attn_dims *dims, void *stream, void *workspace,
+                        size_t workspace_bytes)
+{
+    if (workspace == nullptr) return ATTN_ERR_NULL;
+    if (workspace_bytes < attn::kWorkspaceBytes) return ATTN_ERR_SHAPE;
+    if (!aligned(workspace, 16)) return ATTN_ERR_ALIGN;
+    const attn_status st = validate(Q, K, V, key_lengths, mask_kind, scale, out, dims);
+    if (st != ATTN_OK) return st;
+    const attn_dims &d = *dims;
+    const uint64_t esz = d.dtype == ATTN_BF16 ? 2 : 4;
+    const uint64_t qbytes = static_cast<uint64_t>(d.B) * d.h * d.m * d.d_k * esz;
+    const uint64_t kbytes = static_cast<uint64_t>(d.B) * d.h * d.n * d.d_k * esz;
+    if (overlaps(workspace, workspace_bytes, out, qbytes) || overlaps(workspace, workspace_bytes, Q, qbytes) ||
+        overlaps(workspace, workspace_bytes, K, kbytes) || overlaps(workspace, workspace_bytes, V, kbytes))
+        return ATTN_ERR_ALIAS;
+    return run(Q, K, V, key_lengths, mask_kind, scale, out, dims, stream, ATTN_KERNEL_AUTO,
+               static_cast<int *>(workspace));
 }
 
 attn_status attn_fwd(const void *Q, const void *K, const void *V, const int32_t *key_lengths, int mask_kind,

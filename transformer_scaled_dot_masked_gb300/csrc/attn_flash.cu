@@ -73,6 +73,8 @@ constexpr uint32_t kTileBytes = kBM * kD * 2; // one 128 x 64 bf16 tile = 16 KiB
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSlotCols = 256;
 constexpr uint32_t kColS = 0, kColP = 128, kColO = 192;
+constexpr int kTileRing = 4;              // CTA tile indices handed from the loader to the other roles
+constexpr uint32_t kTileConsumers = 2 + 2 * 128; // two MMA issuers, two softmax warpgroups
 constexpr float kRescaleThreshold = 8.0f; // log2 units: rescale only when the max grows by > 2^8
 constexpr uint64_t kWaitLimitNs = 2000000000ull; // 2 s
 constexpr uint64_t kDrainLimitNs = 200000000ull; // 0.2 s
@@ -83,7 +85,7 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kD, 0, 1); // P (TMEM) x V (MN
 // Where a wait gave up (reported through the status word's info).
 enum WaitSite : uint32_t {
     kSiteLoadQEmpty = 1, kSiteLoadKvEmpty, kSiteMmaQFull, kSiteMmaKvFull, kSiteMmaSFree,
-    kSiteMmaPFull, kSiteMmaOFree, kSiteSmSFull, kSiteSmPvDone, kSiteSmPvLast
+    kSiteMmaPFull, kSiteMmaOFree, kSiteSmSFull, kSiteSmPvDone, kSiteSmPvLast, kSiteTileEmpty, kSiteTileFull
 };
 
 struct alignas(1024) SharedStorage {
@@ -94,6 +96,8 @@ struct alignas(1024) SharedStorage {
     uint64_t kv_full[kStages], kv_empty[kStages];
     uint64_t s_full[kSlots], s_free[kSlots], p_full[kSlots], pv_done[kSlots], o_free[kSlots];
     uint64_t drain[kSlots];
+    uint64_t tile_full[kTileRing], tile_empty[kTileRing];
+    int tile_ring[kTileRing];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -105,7 +109,8 @@ struct FlashParams {
     float scale_log2;
     int pair_mode;
     int num_tiles;
-    int q_pairs; // pair mode: query-tile pairs per head
+    int q_pairs;        // pair mode: query-tile pairs per head
+    int *tile_counter;  // [0] next tile to claim, [1] CTAs done; nullptr: static snake schedule
 };
 
 struct Tile {
@@ -126,6 +131,19 @@ __device__ __forceinline__ int tile_of(int r)
     const int k = (r & 1) ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
     return r * static_cast<int>(gridDim.x) + k;
 }
+
+// Sequence of CTA tiles one role of this CTA processes.  Static schedule: the
+// snake order above.  Dynamic schedule (a zeroed counter in global memory): the
+// loader claims the next tile of the heaviest-first order with an atomic add
+// when it is about to load it, and hands the index to the MMA issuers and the
+// softmax warpgroups through a small ring in shared memory, so CTAs on faster
+// SMs simply take more tiles.  -1 ends the sequence.
+struct TileFeed {
+    uint32_t k = 0;
+
+    __device__ __forceinline__ int produce(SharedStorage &sm, const FlashParams &p, bool &ok);
+    __device__ __forceinline__ int consume(SharedStorage &sm, const FlashParams &p, bool &ok, bool warp_wide);
+};
 
 __device__ __forceinline__ Tile decode_tile(const FlashParams &p, int t)
 {
@@ -198,6 +216,42 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity)
 
 __device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffffu, ok); }
 
+// Loader side (one thread): claim the next tile and publish it to the ring.
+__device__ __forceinline__ int TileFeed::produce(SharedStorage &sm, const FlashParams &p, bool &ok)
+{
+    if (p.tile_counter == nullptr) {
+        const int t = tile_of(static_cast<int>(k++));
+        return t < p.num_tiles ? t : -1;
+    }
+    int t = atomicAdd(p.tile_counter, 1);
+    if (t >= p.num_tiles) t = -1;
+    const uint32_t slot = k % kTileRing;
+    ok = wait_bar(&sm.tile_empty[slot], ((k / kTileRing) & 1) ^ 1, &sm.abort_flag, kSiteTileEmpty);
+    if (!ok) return -1;
+    sm.tile_ring[slot] = t;
+    mbar_arrive(&sm.tile_full[slot]); // release: the index is visible to whoever sees the phase
+    ++k;
+    return t;
+}
+
+// Consumer side: every thread of a consuming group reads the index and arrives.
+__device__ __forceinline__ int TileFeed::consume(SharedStorage &sm, const FlashParams &p, bool &ok, bool warp_wide)
+{
+    if (p.tile_counter == nullptr) {
+        const int t = tile_of(static_cast<int>(k++));
+        return t < p.num_tiles ? t : -1;
+    }
+    const uint32_t slot = k % kTileRing;
+    bool got = wait_bar(&sm.tile_full[slot], (k / kTileRing) & 1, &sm.abort_flag, kSiteTileFull);
+    if (warp_wide) got = warp_all(got);
+    ok = got;
+    if (!ok) return -1;
+    const int t = *reinterpret_cast<volatile int *>(&sm.tile_ring[slot]);
+    mbar_arrive(&sm.tile_empty[slot]);
+    ++k;
+    return t;
+}
+
 // ------------------------------------------------------------------ roles
 __device__ __forceinline__ void load_role(SharedStorage &sm, const FlashParams &p, const CUtensorMap *tm_q,
                                           const CUtensorMap *tm_k, const CUtensorMap *tm_v)
@@ -208,7 +262,10 @@ __device__ __forceinline__ void load_role(SharedStorage &sm, const FlashParams &
     uint32_t q_cnt[kSlots] = {0, 0};
     uint32_t seq = 0;
     bool ok = true;
-    for (int r = 0, t = tile_of(0); t < p.num_tiles && ok; t = tile_of(++r)) {
+    TileFeed feed;
+    while (ok) {
+        const int t = feed.produce(sm, p, ok);
+        if (t < 0) break;
         const Tile T = decode_tile(p, t);
 #pragma unroll
         for (int s = 0; s < kSlots; ++s) {
@@ -295,7 +352,10 @@ __device__ __forceinline__ void mma_role(SharedStorage &sm, const FlashParams &p
     const uint32_t s_tmem = tmem + s * kSlotCols + kColS;
     const uint32_t p_tmem = tmem + s * kSlotCols + kColP;
     const uint32_t o_tmem = tmem + s * kSlotCols + kColO;
-    for (int r = 0, t = tile_of(0); t < p.num_tiles && ok; t = tile_of(++r)) {
+    TileFeed feed;
+    while (ok) {
+        const int t = feed.consume(sm, p, ok, false);
+        if (t < 0) break;
         const Tile T = decode_tile(p, t);
         const int n = s ? T.n_kv[1] : T.n_kv[0];
         if (n > 0) {
@@ -385,7 +445,10 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
     uint32_t s_cnt = 0, pv_cnt = 0;
     bool ok = true;
 
-    for (int r = 0, t = tile_of(0); t < p.num_tiles && ok; t = tile_of(++r)) {
+    TileFeed feed;
+    while (ok) {
+        const int t = feed.consume(sm, p, ok, true);
+        if (t < 0) break;
         const Tile T = decode_tile(p, t);
         // select this slot's fields without indexing the per-slot arrays at run time
         const bool active = slot ? T.active[1] : T.active[0];
@@ -550,6 +613,10 @@ attn_flash_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             mbar_init(&sm.kv_full[st], 1);
             mbar_init(&sm.kv_empty[st], p.pair_mode ? 2 : 1); // pair mode: one arrival per slot issuer
         }
+        for (int r = 0; r < kTileRing; ++r) {
+            mbar_init(&sm.tile_full[r], 1);
+            mbar_init(&sm.tile_empty[r], kTileConsumers);
+        }
         mbar_init(&sm.drain[0], 1);
         mbar_init(&sm.drain[1], 1);
         sm.abort_flag = 0;
@@ -587,6 +654,15 @@ attn_flash_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
+    }
+    if (p.tile_counter != nullptr && threadIdx.x == kLoadWarp * 32) {
+        // every claim of this CTA precedes this point; the last CTA to get here
+        // returns the counters to zero for the next call that uses the workspace
+        __threadfence();
+        if (atomicAdd(p.tile_counter + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+            atomicExch(p.tile_counter, 0);
+            atomicExch(p.tile_counter + 1, 0);
+        }
     }
 }
 
@@ -631,7 +707,7 @@ constexpr size_t kSmemBytes = sizeof(SharedStorage) + 1024; // + alignment slack
 
 } // namespace
 
-cudaError_t launch_flash(const Problem &pb, bool pair_mode, cudaStream_t stream)
+cudaError_t launch_flash(const Problem &pb, bool pair_mode, int *tile_counter, cudaStream_t stream)
 {
     static DeviceInfo infos[64];
     static std::mutex mu;
@@ -667,6 +743,7 @@ cudaError_t launch_flash(const Problem &pb, bool pair_mode, cudaStream_t stream)
     p.pair_mode = pair_mode ? 1 : 0;
     p.q_pairs = (pb.m + 2 * kBM - 1) / (2 * kBM);
     p.num_tiles = pair_mode ? BH * p.q_pairs : (BH + 1) / 2;
+    p.tile_counter = tile_counter;
     const int grid = p.num_tiles < sms ? p.num_tiles : sms;
     attn_flash_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();

@@ -27,7 +27,12 @@ cudaError_t launch_simt(const Problem &p, cudaStream_t stream);
 // tcgen05/TMA kernel (bf16, d == 64).  pair_mode: each CTA tile holds two
 // consecutive 128-row query tiles of one head sharing K/V; otherwise each
 // CTA tile holds one 128-row query tile of each of two heads (m <= 128).
-cudaError_t launch_flash(const Problem &p, bool pair_mode, cudaStream_t stream);
+// tile_counter: two zeroed ints in global memory for the dynamic tile
+// schedule (left zeroed on exit), or nullptr for the static schedule.
+cudaError_t launch_flash(const Problem &p, bool pair_mode, int *tile_counter, cudaStream_t stream);
+
+// Bytes of workspace the dynamic tile schedule needs.
+constexpr size_t kWorkspaceBytes = 256;
 
 // Device status word of the flash kernel (bounded waits that gave up).
 cudaError_t flash_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint32_t *info);
