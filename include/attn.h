@@ -64,7 +64,8 @@ typedef enum {
     ATTN_ERR_CUDA = 7,           /* a CUDA runtime call failed (device query, launch) */
     ATTN_ERR_DEVICE_TIMEOUT = 8, /* a kernel gave up a bounded wait (see attn_device_status) */
     ATTN_ERR_VALUE = 9,          /* scale is negative or not finite */
-    ATTN_ERR_ALIAS = 10          /* out overlaps Q, K, V or key_lengths */
+    ATTN_ERR_ALIAS = 10,         /* out overlaps Q, K, V or key_lengths */
+    ATTN_ERR_SCRATCH = 11        /* the call needs more scratch than attn_fwd_noalloc holds */
 } attn_status;
 
 typedef enum {
@@ -160,6 +161,41 @@ attn_status attn_fwd_ws(const void *Q, const void *K, const void *V,
                         const int32_t *key_lengths, int mask_kind, float scale,
                         void *out, const attn_dims *dims, void *stream,
                         void *workspace, size_t workspace_bytes);
+
+/* Size of the device array attn_fwd_noalloc uses as its workspace. */
+#define ATTN_NOALLOC_SCRATCH_BYTES 256
+
+/*
+ * attn_fwd_noalloc: attn_fwd_ws without a caller-supplied workspace, for
+ * callers that cannot allocate device memory when they call.  No page of the
+ * method has a counterpart for this entry point; it is library plumbing.
+ *
+ * Who needs it: code that must not call cudaMalloc (or a framework
+ * allocator) on its hot path -- cudaMalloc can synchronise the whole device
+ * and stall every stream, so serving loops and latency-critical code
+ * allocate everything up front and never again -- and code that runs inside
+ * a host framework that owns all device memory and offers no scratch buffer
+ * to the library.  This entry point calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *
+ * Scratch: instead of a workspace it uses a statically allocated device
+ * array of ATTN_NOALLOC_SCRATCH_BYTES bytes inside the library.  Every GPU
+ * that loads the library holds that array until the process exits.  The
+ * first call on a device looks up the array's device address with that
+ * device current (one-time set-up); make that first call before any stream
+ * capture on that device.  Each call zeroes the counters it needs on
+ * `stream` before its kernel.  All calls on a device share the one array:
+ * calls that may run at the same time on the GPU (different streams) race
+ * on it and must not be made; calls ordered on one stream are safe.
+ *
+ * Arguments, rules and errors as attn_fwd.  A call whose scratch need
+ * (attn_workspace_size()) exceeds ATTN_NOALLOC_SCRATCH_BYTES is rejected
+ * with ATTN_ERR_SCRATCH; ATTN_ERR_CUDA if the one-time address lookup or the
+ * zeroing fails.
+ */
+attn_status attn_fwd_noalloc(const void *Q, const void *K, const void *V,
+                             const int32_t *key_lengths, int mask_kind, float scale,
+                             void *out, const attn_dims *dims, void *stream);
 
 /* The kernel attn_fwd would run for these dims and mask (host only, no CUDA call);
  * ATTN_KERNEL_AUTO (0) if the call would be rejected. */

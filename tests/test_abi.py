@@ -42,7 +42,7 @@ def test_python_constants_match_header():
 
 
 def test_status_strings_and_version():
-    for code in range(0, 11):
+    for code in range(0, 12):
         s = N.status_string(code)
         assert s and s != "unknown status"
     assert N.status_string(99) == "unknown status"

@@ -1,0 +1,50 @@
+"""attn_fwd_noalloc: the entry point for callers that cannot allocate device
+memory when they call (for example serving loops that allocate everything at
+start-up, because cudaMalloc can synchronise the device, or code inside a
+framework that owns all device memory).  It takes no workspace and uses the
+library's own statically allocated device array instead.
+
+Called through the C ABI and compared with attn_fwd on the same inputs, on two
+calls in a row (the array keeps the previous call's contents, so the second
+call checks that each call starts from cleared counters).  This file is named
+to be collected last; it passes alone and after the other tests.
+"""
+import numpy as np
+import pytest
+import torch
+
+import transformer_scaled_dot_masked_gb300 as attn
+from transformer_scaled_dot_masked_gb300 import _native as N
+from workloads import WORKLOADS, draw
+
+from gpu_helpers import BF16_TOL, FP32_TOL, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc(q, k, v, lens, w, out):
+    dims = N.make_dims(w.B, w.h, w.m, w.n, w.d, N.DTYPE_BF16 if w.dtype == "bf16" else N.DTYPE_FP32)
+    stream = torch.cuda.current_stream()
+    return N.fwd_noalloc_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), lens.data_ptr(), w.mask, w.scale,
+                             out.data_ptr(), dims, stream.cuda_stream)
+
+
+@pytest.mark.parametrize("cfg,shape", [
+    (5, dict(B=1, h=4, m=1024, n=1024)),   # long causal, pair mode
+    (4, dict(B=6)),                        # cross-attention with padding, split mode
+    (1, dict()),                           # fp32 (CUDA-core kernel, no scratch needed)
+])
+def test_noalloc_matches_attn_fwd_twice(cfg, shape):
+    w = WORKLOADS[cfg].with_(**shape)
+    inp = draw(w)
+    q, k, v = (to_device(x, w.dtype) for x in (inp.q, inp.k, inp.v))
+    lens = torch.from_numpy(inp.key_lengths).cuda()
+    ref = attn.attn_fwd(q, k, v, lens, w.mask, w.scale)
+    tol = BF16_TOL if w.dtype == "bf16" else FP32_TOL
+    for _ in range(2):
+        out = torch.full_like(q, float("nan"))
+        assert _noalloc(q, k, v, lens, w, out) == N.ATTN_OK
+        torch.cuda.synchronize()
+        assert attn.device_status()[0] == 0
+        err = float((out.float() - ref.float()).abs().max())
+        assert err <= tol, f"max abs err {err} vs attn_fwd"

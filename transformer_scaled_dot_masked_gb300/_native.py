@@ -45,6 +45,8 @@ lib.attn_workspace_size.argtypes = []
 lib.attn_workspace_size.restype = ctypes.c_size_t
 lib.attn_fwd_ws.argtypes = lib.attn_fwd.argtypes + [_vp, ctypes.c_size_t]
 lib.attn_fwd_ws.restype = ctypes.c_int
+lib.attn_fwd_noalloc.argtypes = lib.attn_fwd.argtypes
+lib.attn_fwd_noalloc.restype = ctypes.c_int
 lib.attn_select_kernel.argtypes = [ctypes.POINTER(AttnDims), ctypes.c_int]
 lib.attn_select_kernel.restype = ctypes.c_int
 lib.attn_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32)]
@@ -96,6 +98,13 @@ def fwd_ws_raw(q_ptr, k_ptr, v_ptr, lens_ptr, mask_kind, scale, out_ptr, dims: A
     """attn_fwd_ws with integer device pointers; returns the status code."""
     return lib.attn_fwd_ws(q_ptr, k_ptr, v_ptr, lens_ptr, int(mask_kind), float(scale), out_ptr,
                            ctypes.byref(dims), stream_ptr, ws_ptr, int(ws_bytes))
+
+
+def fwd_noalloc_raw(q_ptr, k_ptr, v_ptr, lens_ptr, mask_kind, scale, out_ptr, dims: AttnDims,
+                    stream_ptr) -> int:
+    """attn_fwd_noalloc with integer device pointers; returns the status code."""
+    return lib.attn_fwd_noalloc(q_ptr, k_ptr, v_ptr, lens_ptr, int(mask_kind), float(scale), out_ptr,
+                                ctypes.byref(dims), stream_ptr)
 
 
 def device_status(stream_ptr=None):

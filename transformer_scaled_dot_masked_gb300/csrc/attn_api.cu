@@ -3,6 +3,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <mutex>
 
 #include "../../include/attn.h"
 #include "kernels.h"
@@ -106,9 +107,53 @@ attn_status run(const void *Q, const void *K, const void *V, const int32_t *key_
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// Scratch of attn_fwd_noalloc: a statically allocated device array (one per
+// device that loads the library, held until the process exits).  Host code
+// cannot use the symbol's name as a device address; its address is looked up
+// once per device with cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
+
+struct NoAllocDevice {
+    std::once_flag once;
+    void *ptr = nullptr;
+    cudaError_t err = cudaSuccess;
+};
+constexpr int kMaxDevices = 64;
+NoAllocDevice g_noalloc_devices[kMaxDevices];
+
+// Device address of g_noalloc_scratch on the current device (set up on first use).
+cudaError_t noalloc_scratch(void **ptr)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    NoAllocDevice &d = g_noalloc_devices[dev];
+    std::call_once(d.once, [&d] { d.err = cudaGetSymbolAddress(&d.ptr, g_noalloc_scratch); });
+    if (d.err != cudaSuccess) return d.err;
+    *ptr = d.ptr;
+    return cudaSuccess;
+}
+
 } // namespace
 
 extern "C" {
+
+attn_status attn_fwd_noalloc(const void *Q, const void *K, const void *V, const int32_t *key_lengths,
+                             int mask_kind, float scale, void *out, const attn_dims *dims, void *stream)
+{
+    const attn_status st = validate(Q, K, V, key_lengths, mask_kind, scale, out, dims);
+    if (st != ATTN_OK) return st;
+    if (attn::kWorkspaceBytes > ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_SCRATCH;
+    void *scratch = nullptr;
+    if (noalloc_scratch(&scratch) != cudaSuccess) return ATTN_ERR_CUDA;
+    // the array keeps the previous call's contents: the tile counters must start at zero
+    if (cudaMemsetAsync(scratch, 0, attn::kWorkspaceBytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return run(Q, K, V, key_lengths, mask_kind, scale, out, dims, stream, ATTN_KERNEL_AUTO,
+               static_cast<int *>(scratch));
+}
+
 
 attn_status attn_fwd_kernel(const void *Q, const void *K, const void *V, const int32_t *key_lengths,
                             int mask_kind, float scale, void *out, const attn_dims *dims, void *stream,
@@ -174,6 +219,7 @@ const char *attn_status_string(int status)
     case ATTN_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait; its output is incomplete";
     case ATTN_ERR_VALUE: return "scale must be finite and >= 0";
     case ATTN_ERR_ALIAS: return "out overlaps an input";
+    case ATTN_ERR_SCRATCH: return "the call needs more scratch than attn_fwd_noalloc holds";
     default: return "unknown status";
     }
 }
