@@ -489,13 +489,12 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
 #pragma unroll
             for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(sr[c]);
             if (boundary) {
-                // scale first, then mask: a zero scale must not turn -inf into NaN
+                // keys allowed for row i are exactly those below one bound (the padded
+                // length, and i + 1 for a causal mask): column c is allowed iff c < cnt.
+                // Scale first, then mask: a zero scale must not turn -inf into NaN.
+                const int cnt = (causal ? min(kv_len, i + 1) : kv_len) - key0;
 #pragma unroll
-                for (int c = 0; c < kBN; ++c) {
-                    const int key = key0 + c;
-                    const bool allowed = key < kv_len && !(causal && key > i);
-                    x[c] = allowed ? x[c] * sl2 : -CUDART_INF_F;
-                }
+                for (int c = 0; c < kBN; ++c) x[c] = c < cnt ? x[c] * sl2 : -CUDART_INF_F;
             }
             // row maximum: four independent chains of three-input max
             float mx[4];
