@@ -76,6 +76,9 @@ EDGE = [
     ("cross_padding_long", 3, 2, 190, 700, MASK_KEY_PADDING, (0, 700)),
     ("self_padding_causal", 3, 2, 260, 260, MASK_KEY_PADDING | MASK_CAUSAL, (1, 260)),
     ("short_padding_odd_heads", 3, 3, 77, 150, MASK_KEY_PADDING, (0, 150)),
+    # h = 1: the two heads of a split-mode CTA tile belong to different sequences, so
+    # their key tile counts differ (0 to 16) and their K/V rings run out of step
+    ("short_single_head_ragged_keys", 9, 1, 128, 2000, MASK_KEY_PADDING, (0, 2000)),
     ("single_key", 2, 2, 50, 1, MASK_NONE, None),
     ("single_query", 2, 2, 1, 500, MASK_KEY_PADDING, (1, 500)),
     ("one_by_one_causal", 1, 1, 1, 1, MASK_CAUSAL, None),

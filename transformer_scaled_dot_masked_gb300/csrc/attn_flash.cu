@@ -252,6 +252,30 @@ __device__ __forceinline__ int TileFeed::consume(SharedStorage &sm, const FlashP
     return t;
 }
 
+// K/V stage rings.  Pair mode: one ring of kStages stages, one fill per key
+// tile, read by both slots.  Split mode: each slot owns a ring of kStages / 2
+// stages holding its own head's key tiles.  Every thread that waits on a
+// stage's kv_full barrier thus sees each of that stage's phases in order, so a
+// parity wait can never be satisfied by a phase two fills away.
+struct StagePos {
+    uint32_t st;    // stage index
+    uint32_t phase; // parity of the fill
+};
+
+__device__ __forceinline__ StagePos ring_pos(bool pair_mode, int ring, uint32_t fill)
+{
+    if (pair_mode) return {fill % kStages, (fill / kStages) & 1u};
+    constexpr uint32_t kHalf = kStages / 2;
+    return {static_cast<uint32_t>(ring) * kHalf + fill % kHalf, (fill / kHalf) & 1u};
+}
+
+// Fills of slot s's ring that CTA tile T takes.
+__device__ __forceinline__ uint32_t fills_of(const Tile &T, int s)
+{
+    // a select, not T.n_kv[s]: a runtime index would put the tile on the stack
+    return static_cast<uint32_t>(T.shared_kv ? max(T.n_kv[0], T.n_kv[1]) : (s ? T.n_kv[1] : T.n_kv[0]));
+}
+
 // ------------------------------------------------------------------ roles
 __device__ __forceinline__ void load_role(SharedStorage &sm, const FlashParams &p, const CUtensorMap *tm_q,
                                           const CUtensorMap *tm_k, const CUtensorMap *tm_v)
@@ -260,7 +284,7 @@ __device__ __forceinline__ void load_role(SharedStorage &sm, const FlashParams &
     tma_prefetch_map(tm_k);
     tma_prefetch_map(tm_v);
     uint32_t q_cnt[kSlots] = {0, 0};
-    uint32_t seq = 0;
+    uint32_t fill0 = 0, fill1 = 0; // fills of ring 0 and ring 1 (pair mode uses ring 0 only)
     bool ok = true;
     TileFeed feed;
     while (ok) {
@@ -281,26 +305,29 @@ __device__ __forceinline__ void load_role(SharedStorage &sm, const FlashParams &
             for (int s = 0; s < kSlots; ++s) {
                 if (j >= T.n_kv[s]) continue;
                 if (T.shared_kv && s == 1 && j < T.n_kv[0]) continue; // slot 1 reads slot 0's stage
-                const int st = seq % kStages;
-                if (!(ok = wait_bar(&sm.kv_empty[st], ((seq / kStages) & 1) ^ 1, &sm.abort_flag,
-                                    kSiteLoadKvEmpty)))
-                    break;
-                mbar_arrive_expect_tx(&sm.kv_full[st], 2 * kTileBytes);
-                tma_load_3d(sm.k[st], tm_k, &sm.kv_full[st], 0, j * kBN, T.bh[s]);
-                tma_load_3d(sm.v[st], tm_v, &sm.kv_full[st], 0, j * kBN, T.bh[s]);
-                ++seq;
+                const int ring = T.shared_kv ? 0 : s;
+                const StagePos sp = ring_pos(p.pair_mode, ring, ring ? fill1 : fill0);
+                if (!(ok = wait_bar(&sm.kv_empty[sp.st], sp.phase ^ 1, &sm.abort_flag, kSiteLoadKvEmpty))) break;
+                mbar_arrive_expect_tx(&sm.kv_full[sp.st], 2 * kTileBytes);
+                tma_load_3d(sm.k[sp.st], tm_k, &sm.kv_full[sp.st], 0, j * kBN, T.bh[s]);
+                tma_load_3d(sm.v[sp.st], tm_v, &sm.kv_full[sp.st], 0, j * kBN, T.bh[s]);
+                if (ring) ++fill1; else ++fill0;
             }
         }
     }
     // Tail: every stage and Q buffer must be released (its last copy landed and
     // the MMAs reading it completed) before the CTA may exit.
-    for (int st = 0; st < kStages; ++st) {
-        const uint32_t uses = seq / kStages + (static_cast<uint32_t>(st) < seq % kStages ? 1u : 0u);
-        if (uses == 0) continue;
-        if (ok) {
-            wait_bar(&sm.kv_empty[st], (uses - 1) & 1, &sm.abort_flag, kSiteLoadKvEmpty);
-        } else {
-            drain_wait(&sm.kv_full[st], (uses - 1) & 1);
+    for (int ring = 0; ring < (p.pair_mode ? 1 : kSlots); ++ring) {
+        // the last fill of each stage that was used at all
+        const uint32_t depth = p.pair_mode ? kStages : kStages / 2;
+        const uint32_t fills = ring ? fill1 : fill0;
+        for (uint32_t f = fills > depth ? fills - depth : 0; f < fills; ++f) {
+            const StagePos sp = ring_pos(p.pair_mode, ring, f);
+            if (ok) {
+                wait_bar(&sm.kv_empty[sp.st], sp.phase, &sm.abort_flag, kSiteLoadKvEmpty);
+            } else {
+                drain_wait(&sm.kv_full[sp.st], sp.phase);
+            }
         }
     }
     for (int s = 0; s < kSlots; ++s) {
@@ -311,22 +338,6 @@ __device__ __forceinline__ void load_role(SharedStorage &sm, const FlashParams &
             drain_wait(&sm.q_full[s], (q_cnt[s] - 1) & 1);
         }
     }
-}
-
-// Ring position of the stage holding key tile j for slot s in CTA tile T: the
-// load role fills the ring per CTA tile, key tile by key tile; in pair mode one
-// stage per key tile serves both slots, in split mode each slot takes its own
-// stage (slot 0 first).
-__device__ __forceinline__ uint32_t stage_offset(const Tile &T, int j, int s)
-{
-    if (T.shared_kv) return static_cast<uint32_t>(j);
-    return static_cast<uint32_t>(min(j, T.n_kv[0]) + min(j, T.n_kv[1]) + ((s == 1 && j < T.n_kv[0]) ? 1 : 0));
-}
-
-__device__ __forceinline__ uint32_t stages_of(const Tile &T)
-{
-    return T.shared_kv ? static_cast<uint32_t>(max(T.n_kv[0], T.n_kv[1]))
-                       : static_cast<uint32_t>(T.n_kv[0] + T.n_kv[1]);
 }
 
 // MMA issuer of one slot (one lane of its own warp): S_s(j) = Q_s K_j^T as soon
@@ -340,7 +351,7 @@ __device__ __forceinline__ uint32_t stages_of(const Tile &T)
 __device__ __forceinline__ void mma_role(SharedStorage &sm, const FlashParams &p, uint32_t tmem, int s)
 {
     uint32_t q_cnt = 0, s_cnt = 0, p_cnt = 0, o_cnt = 0;
-    uint32_t seq_base = 0;
+    uint32_t fill_base = 0; // fills of this slot's ring before the current CTA tile
     bool ok = true;
     int *ab = &sm.abort_flag;
     uint64_t *q_full = &sm.q_full[s], *q_empty = &sm.q_empty[s], *s_full = &sm.s_full[s];
@@ -365,13 +376,12 @@ __device__ __forceinline__ void mma_role(SharedStorage &sm, const FlashParams &p
         for (int j = 0; j <= n && ok; ++j) {
             if (j < n) {
                 // S(j)
-                const uint32_t seq = seq_base + stage_offset(T, j, s);
-                const uint32_t st = seq % kStages;
-                ok = wait_bar(&sm.kv_full[st], (seq / kStages) & 1, ab, kSiteMmaKvFull);
+                const StagePos sp = ring_pos(p.pair_mode, s, fill_base + j);
+                ok = wait_bar(&sm.kv_full[sp.st], sp.phase, ab, kSiteMmaKvFull);
                 if (ok) ok = wait_bar(s_free, (s_cnt & 1) ^ 1, ab, kSiteMmaSFree);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t kd = k_lo + st * (kTileBytes >> 4);
+                const uint32_t kd = k_lo + sp.st * (kTileBytes >> 4);
                 // 16 bf16 of K per step = 32 bytes (2 descriptor units) along the swizzled rows
                 mma_ss_k<0, 0>(s_tmem, q_lo, kd, desc_hi, kIdescS, 0u);
                 mma_ss_k<2, 2>(s_tmem, q_lo, kd, desc_hi, kIdescS, 1u);
@@ -395,7 +405,7 @@ __device__ __forceinline__ void mma_role(SharedStorage &sm, const FlashParams &p
                     ++o_cnt;
                     tc_fence_after();
                 }
-                const uint32_t st = (seq_base + stage_offset(T, jp, s)) % kStages;
+                const uint32_t st = ring_pos(p.pair_mode, s, fill_base + jp).st;
                 const uint32_t vd = v_lo + st * (kTileBytes >> 4);
                 // keys 16kk..16kk+15 per step: P columns 8kk.. (two bf16 per column), V rows
                 // 16kk.. (2 KiB = 128 descriptor units)
@@ -416,13 +426,12 @@ __device__ __forceinline__ void mma_role(SharedStorage &sm, const FlashParams &p
             // stages of this CTA tile that only the other slot reads: arrive once each is loaded
             const int J = max(T.n_kv[0], T.n_kv[1]);
             for (int j = n; j < J && ok; ++j) {
-                const uint32_t seq = seq_base + static_cast<uint32_t>(j);
-                const uint32_t st = seq % kStages;
-                ok = wait_bar(&sm.kv_full[st], (seq / kStages) & 1, ab, kSiteMmaKvFull);
-                if (ok) mbar_arrive(&sm.kv_empty[st]);
+                const StagePos sp = ring_pos(p.pair_mode, s, fill_base + j);
+                ok = wait_bar(&sm.kv_full[sp.st], sp.phase, ab, kSiteMmaKvFull);
+                if (ok) mbar_arrive(&sm.kv_empty[sp.st]);
             }
         }
-        seq_base += stages_of(T);
+        fill_base += fills_of(T, s);
     }
     if (!ok) {
         // make sure no MMA is still writing TMEM when the CTA frees it
