@@ -85,17 +85,20 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kD, 0, 1); // P (TMEM) x V (MN
 // Where a wait gave up (reported through the status word's info).
 enum WaitSite : uint32_t {
     kSiteLoadQEmpty = 1, kSiteLoadKvEmpty, kSiteMmaQFull, kSiteMmaKvFull, kSiteMmaSFree,
-    kSiteMmaPFull, kSiteMmaOFree, kSiteSmSFull, kSiteSmPvDone, kSiteSmPvLast, kSiteTileEmpty, kSiteTileFull
+    kSiteMmaPFull, kSiteMmaOFree, kSiteSmSFull, kSiteSmPvDone, kSiteSmPvLast, kSiteTileEmpty, kSiteTileFull,
+    kSiteSmStageFree, kSiteSmStageFull
 };
 
 struct alignas(1024) SharedStorage {
     uint8_t q[kSlots][kTileBytes];
     uint8_t k[kStages][kTileBytes];
     uint8_t v[kStages][kTileBytes];
+    uint8_t o_stage[kSlots][kTileBytes]; // output tile of each slot, SW128 layout, read by a TMA store
     uint64_t q_full[kSlots], q_empty[kSlots];
     uint64_t kv_full[kStages], kv_empty[kStages];
     uint64_t s_full[kSlots], s_free[kSlots], p_full[kSlots], pv_done[kSlots], o_free[kSlots];
     uint64_t drain[kSlots];
+    uint64_t stage_free[kSlots], stage_full[kSlots]; // o_stage may be written / may be stored
     uint64_t tile_full[kTileRing], tile_empty[kTileRing];
     int tile_ring[kTileRing];
     uint32_t tmem_base;
@@ -440,7 +443,8 @@ __device__ __forceinline__ void mma_role(SharedStorage &sm, const FlashParams &p
     }
 }
 
-__device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParams &p, uint32_t tmem, int slot)
+__device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParams &p, const CUtensorMap *tm_o,
+                                             uint32_t tmem, int slot)
 {
     const int warp_in_group = (threadIdx.x / 32) % 4; // TMEM lane quadrant this warp may access
     const int row = warp_in_group * 32 + (threadIdx.x % 32);
@@ -451,8 +455,10 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
     const bool causal = (p.mask_kind & kMaskCausal) != 0;
     const float sl2 = p.scale_log2;
     int *ab = &sm.abort_flag;
-    uint32_t s_cnt = 0, pv_cnt = 0;
+    uint32_t s_cnt = 0, pv_cnt = 0, epi_cnt = 0;
     bool ok = true;
+    if (row == 0) tma_prefetch_map(tm_o);
+    const uint32_t stage_row = smem_addr(sm.o_stage[slot]) + row * (kD * 2);
 
     TileFeed feed;
     while (ok) {
@@ -584,23 +590,46 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
         tc_fence_before();
         mbar_arrive(&sm.o_free[slot]);
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        if (i < p.m) {
+        // Output: each thread writes its row of O / l into this slot's staging tile in
+        // the 128-byte-swizzled layout (16-byte chunk c of row r at chunk c ^ (r % 8):
+        // conflict-free), then one thread stores the tile with TMA, which clips rows
+        // past m.  The staging tile is rewritten only after the previous store has
+        // read it.
+        if (row == 0) {
+            bulk_wait_read_all();
+            mbar_arrive(&sm.stage_free[slot]);
+        }
+        ok = warp_all(wait_bar(&sm.stage_free[slot], epi_cnt & 1, ab, kSiteSmStageFree));
+        if (!ok) break;
 #pragma unroll
-            for (int c = 0; c < kD / 8; ++c) {
-                uint4 v;
-                v.x = pack_bf16x2(__uint_as_float(orr[8 * c + 0]) * inv, __uint_as_float(orr[8 * c + 1]) * inv);
-                v.y = pack_bf16x2(__uint_as_float(orr[8 * c + 2]) * inv, __uint_as_float(orr[8 * c + 3]) * inv);
-                v.z = pack_bf16x2(__uint_as_float(orr[8 * c + 4]) * inv, __uint_as_float(orr[8 * c + 5]) * inv);
-                v.w = pack_bf16x2(__uint_as_float(orr[8 * c + 6]) * inv, __uint_as_float(orr[8 * c + 7]) * inv);
-                reinterpret_cast<uint4 *>(orow)[c] = v;
+        for (int c = 0; c < kD / 8; ++c) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(orr[8 * c + 0]) * inv, __uint_as_float(orr[8 * c + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(orr[8 * c + 2]) * inv, __uint_as_float(orr[8 * c + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(orr[8 * c + 4]) * inv, __uint_as_float(orr[8 * c + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(orr[8 * c + 6]) * inv, __uint_as_float(orr[8 * c + 7]) * inv);
+            st_shared_v4(stage_row + ((c ^ (row & 7)) << 4), v);
+        }
+        fence_proxy_async_shared();
+        mbar_arrive(&sm.stage_full[slot]);
+        if (row == 0) {
+            ok = wait_bar(&sm.stage_full[slot], epi_cnt & 1, ab, kSiteSmStageFull);
+            if (ok) {
+                tma_store_3d(tm_o, sm.o_stage[slot], 0, q0, bh);
+                bulk_commit_group();
             }
         }
+        ok = warp_all(ok);
+        ++epi_cnt;
     }
+    // the staging tiles must stay valid, and the output written, until the stores complete
+    if (row == 0) bulk_wait_all();
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
 attn_flash_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const FlashParams p)
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  const FlashParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     SharedStorage &sm = *reinterpret_cast<SharedStorage *>(
@@ -616,6 +645,8 @@ attn_flash_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             mbar_init(&sm.p_full[s], kBM);
             mbar_init(&sm.pv_done[s], 1);
             mbar_init(&sm.o_free[s], kBM);
+            mbar_init(&sm.stage_free[s], 1);
+            mbar_init(&sm.stage_full[s], kBM);
         }
         for (int st = 0; st < kStages; ++st) {
             mbar_init(&sm.kv_full[st], 1);
@@ -644,7 +675,7 @@ attn_flash_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // CTA-wide barrier (every thread arrives exactly once) and returns.
     if (warp < 4 * kSlots) {
         regs_increase<kSoftmaxRegs>();
-        softmax_role(sm, p, tmem, warp / 4);
+        softmax_role(sm, p, &tm_o, tmem, warp / 4);
         tc_fence_before();
         __syncthreads();
         return;
@@ -736,8 +767,9 @@ cudaError_t launch_flash(const Problem &pb, bool pair_mode, int *tile_counter, c
     }
     const int sms = infos[dev].sms;
     const int BH = pb.B * pb.h;
-    CUtensorMap tq, tk, tv;
-    if (!encode_map(&tq, pb.q, pb.m, BH) || !encode_map(&tk, pb.k, pb.n, BH) || !encode_map(&tv, pb.v, pb.n, BH))
+    CUtensorMap tq, tk, tv, to;
+    if (!encode_map(&tq, pb.q, pb.m, BH) || !encode_map(&tk, pb.k, pb.n, BH) || !encode_map(&tv, pb.v, pb.n, BH) ||
+        !encode_map(&to, pb.out, pb.m, BH))
         return cudaErrorInvalidValue;
     FlashParams p;
     p.key_lengths = (pb.mask_kind & kMaskKeyPadding) ? pb.key_lengths : nullptr;
@@ -753,7 +785,7 @@ cudaError_t launch_flash(const Problem &pb, bool pair_mode, int *tile_counter, c
     p.num_tiles = pair_mode ? BH * p.q_pairs : (BH + 1) / 2;
     p.tile_counter = tile_counter;
     const int grid = p.num_tiles < sms ? p.num_tiles : sms;
-    attn_flash_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+    attn_flash_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, p);
     return cudaGetLastError();
 }
 
