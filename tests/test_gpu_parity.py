@@ -143,6 +143,63 @@ def test_worked_example_on_every_kernel():
             assert (out[:, 2:] == 0).all()
 
 
+JUMP_CASES = [
+    # name, B, h, m, n, mask, lengths, rows whose scores jump by ~20, by > 128 (log2 units)
+    ("cross_split_mode", 3, 1, 128, 512, MASK_NONE, None, [5, 77, 127], [6, 100]),
+    ("cross_pair_mode", 2, 2, 384, 512, MASK_KEY_PADDING, (380, 512), [5, 200, 383], [6, 301]),
+    ("self_causal", 2, 2, 512, 512, MASK_CAUSAL, None, [300, 450, 511], [420, 509]),
+]
+
+
+def jump_inputs(name, B, h, m, n, mask, lengths, soft, hard):
+    """Seeded inputs in which the listed rows' scores grow sharply after their first
+    key tiles: by ~20 log2 units (exponentials against the running reference stay
+    finite but leave the kept range) and by > 128 (they overflow fp32).  The two
+    large keys also make most other rows peaked."""
+    w = Workload(name, "bf16", B, h, m, n, 64, mask, 0.125, 321, lengths)
+    inp = draw(w)
+    bits = lambda x: np.uint16(np.array(x, dtype=np.float32).view(np.uint32) >> 16)  # exact in bf16
+    inp.q[:, :, soft, :32], inp.q[:, :, soft, 32:] = bits(1.0), bits(0.0)
+    inp.q[:, :, hard, :32], inp.q[:, :, hard, 32:] = bits(0.0), bits(1.0)
+    inp.k[:, :, 260, :32], inp.k[:, :, 260, 32:] = bits(4.0), bits(0.0)   # soft rows: S = 128
+    inp.k[:, :, 400, :32], inp.k[:, :, 400, 32:] = bits(0.0), bits(32.0)  # hard rows: S = 1024
+    return w, inp
+
+
+@pytest.mark.parametrize("name,B,h,m,n,mask,lengths,soft,hard", JUMP_CASES, ids=[c[0] for c in JUMP_CASES])
+def test_score_jumps_between_key_tiles(orc, name, B, h, m, n, mask, lengths, soft, hard):
+    """Tolerance 1e-2 with value rows in [-1, 1].  A row dominated by one key carries
+    that key's bf16 weight rounding (up to 2^-8 relative) into the output, plus the
+    output's own rounding; with |v| <= 1 both together stay below 6e-3, so an error
+    above 1e-2 here means a wrong reference, rescale or recomputation."""
+    w, inp = jump_inputs(name, B, h, m, n, mask, lengths, soft, hard)
+    rng = np.random.default_rng(5)
+    vals = rng.uniform(-1.0, 1.0, size=inp.v.shape).astype(np.float32)
+    inp.v[...] = (vals.view(np.uint32) >> 16).astype(np.uint16)  # truncation keeps |v| <= 1
+    ref = orc.attn_fwd(inp.q, inp.k, inp.v, inp.key_lengths, w.mask, w.scale)
+    for kern in kernels_for(w):
+        got = as_f64(run(inp, kern))
+        assert np.isfinite(got).all()
+        assert np.abs(got - ref).max() <= 1e-2, f"kernel {kern}: " + report(got, ref, 1e-2)
+
+
+@pytest.mark.parametrize("name,B,h,m,n,mask,lengths,soft,hard", JUMP_CASES, ids=[c[0] for c in JUMP_CASES])
+def test_peaked_rows_error_bound(orc, name, B, h, m, n, mask, lengths, soft, hard):
+    """The same peaked rows with standard normal values, against the error bound of
+    bf16 weights: per element |err| <= 2^-8 max|v| (weight rounding) + half an
+    output ulp + 1e-3 (fp32 accumulation)."""
+    w, inp = jump_inputs(name, B, h, m, n, mask, lengths, soft, hard)
+    ref = orc.attn_fwd(inp.q, inp.k, inp.v, inp.key_lengths, w.mask, w.scale)
+    vmax = np.abs(as_f64(to_device(inp.v, "bf16"))).max(axis=(2, 3), keepdims=True)
+    half_ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -126))) - 8)
+    bound = 2.0 ** -8 * vmax + half_ulp + 1e-3
+    for kern in kernels_for(w):
+        got = as_f64(run(inp, kern))
+        assert np.isfinite(got).all()
+        excess = np.abs(got - ref) - bound
+        assert excess.max() <= 0, f"kernel {kern}: " + report(got, ref, float(bound.max()))
+
+
 # ---------------------------------------------------------------- invariants
 @pytest.mark.parametrize("cfg", [2, 3, 4])
 def test_masked_keys_do_not_matter_bitwise(cfg):

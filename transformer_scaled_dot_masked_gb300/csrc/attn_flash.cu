@@ -25,15 +25,18 @@
 //
 // Per key tile j of a slot:
 //   MMA:     S = Q K_j^T                       (4 x tcgen05.mma M128 N128 K16, both K-major)
-//   softmax: read S, mask (boundary tiles only), running max with lazy
-//            rescaling (the max used for the exponentials is only moved when
-//            it grows by more than 2^8, so O and the running sum stay exact
-//            multiples of the true ones and are rescaled rarely),
-//            P = exp2(S * scale * log2 e - max), row sum, write P as bf16
+//   softmax: read S, mask (boundary tiles only), P = exp2(S * scale * log2 e - r)
+//            against a per-row reference r, row sum, write P as bf16.  r is the
+//            row max of the row's first key tile; later tiles keep r and check
+//            the tile's row sum instead of taking a max (sum <= 2^15 bounds
+//            every weight).  A larger sum moves r up by an integer k and scales
+//            the weights by 2^-k exactly; an overflowed one recomputes the row's
+//            scores and takes their max.  O and the running sum stay exact
+//            multiples of the true ones and are rescaled only when r moves.
 //   MMA:     O += P V_j                        (8 x tcgen05.mma M128 N64 K16, A from TMEM, V MN-major)
 // Key tiles wholly beyond the causal diagonal or the padded length are never
 // loaded or computed.  The epilogue divides O by the row sum (0 for a row with
-// no allowed key) and stores bf16 rows with 16-byte stores.
+// no allowed key) and writes the bf16 tile through shared memory with a TMA store.
 //
 // Every mbarrier wait is bounded (kWaitLimitNs).  A wait that runs out sets a
 // shared abort flag and the device status word; all roles then leave their
@@ -75,7 +78,11 @@ constexpr uint32_t kSlotCols = 256;
 constexpr uint32_t kColS = 0, kColP = 128, kColO = 192;
 constexpr int kTileRing = 4;              // CTA tile indices handed from the loader to the other roles
 constexpr uint32_t kTileConsumers = 2 + 2 * 128; // two MMA issuers, two softmax warpgroups
-constexpr float kRescaleThreshold = 8.0f; // log2 units: rescale only when the max grows by > 2^8
+// A key tile's exponentials are taken against the row's running reference max
+// and kept when their sum is at most 2^15 (so is every weight).  A larger finite
+// sum is brought back below 2^8 by an exact power of two; an infinite one (the
+// row's scores grew by 128 or more in log2 units) recomputes that row's scores.
+constexpr float kFastSumLimit = 32768.0f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull; // 2 s
 constexpr uint64_t kDrainLimitNs = 200000000ull; // 0.2 s
 
@@ -106,6 +113,7 @@ struct alignas(1024) SharedStorage {
 };
 
 struct FlashParams {
+    const __nv_bfloat16 *q, *k; // read only by the rare score recomputation
     const int32_t *key_lengths;
     __nv_bfloat16 *out;
     int BH, h, m, n, mask_kind;
@@ -443,6 +451,86 @@ __device__ __forceinline__ void mma_role(SharedStorage &sm, const FlashParams &p
     }
 }
 
+// Row max of one key tile (x holds scores, or scores * scale * log2 e when
+// `prescaled`), in log2 units; moves the reference up to it if it is larger.
+// alpha rescales what was accumulated against the old reference (0 when there
+// was none).
+__device__ __forceinline__ void move_reference(const float (&x)[kBN], bool prescaled, float sl2, float m_run,
+                                               float &m_use, float &alpha, bool &grow)
+{
+    // four independent chains of three-input max
+    float mx[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) mx[k] = fmaxf(x[2 * k], x[2 * k + 1]);
+#pragma unroll
+    for (int c = 8; c < kBN; c += 8) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mx[k] = max3(mx[k], x[c + 2 * k], x[c + 2 * k + 1]);
+    }
+    float row_max = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    if (!prescaled) row_max *= sl2;
+    const float m_new = fmaxf(m_run, row_max);
+    grow = m_new > m_run;
+    m_use = grow ? m_new : m_run;
+    alpha = grow ? ex2(m_run - m_new) : 1.f;
+}
+
+// Weights exp2(x * scale * log2 e - m_use) of one key tile as bf16 pairs (column
+// 2c in the low half of pk[c]); returns their sum (before rounding).  The
+// exponent argument and the sum use packed two-lane fp32 ops.
+__device__ __forceinline__ float weights_bf16(const float (&x)[kBN], bool prescaled, float sl2, float m_use,
+                                              uint32_t (&pk)[kBN / 2])
+{
+    const float m_sub = (m_use == -CUDART_INF_F) ? 0.f : m_use;
+    const uint64_t mul2 = prescaled ? f2(1.f, 1.f) : f2(sl2, sl2);
+    const uint64_t sub2 = f2(-m_sub, -m_sub);
+    uint64_t acc2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
+#pragma unroll
+    for (int c2 = 0; c2 < kBN / 2; ++c2) {
+        const int c = 2 * c2;
+        float a0, a1;
+        unf2(fma2(f2(x[c], x[c + 1]), mul2, sub2), a0, a1);
+        const float e0 = ex2(a0), e1 = ex2(a1);
+        acc2[c2 & 1] = add2(acc2[c2 & 1], f2(e0, e1));
+        pk[c2] = pack_bf16x2(e0, e1);
+    }
+    float s0, s1, s2, s3;
+    unf2(acc2[0], s0, s1);
+    unf2(acc2[1], s2, s3);
+    return (s0 + s1) + (s2 + s3);
+}
+
+// Scores of query row i of head bh against keys key0 .. key0+127, recomputed on
+// the CUDA cores from Q and K in global memory (fp32 sums of exact bf16
+// products), multiplied by scale * log2 e, and -inf where not allowed (column c
+// is allowed iff c < cnt; allowed keys are below n).  Rows past m read as zero
+// queries, as the TMA loads fill them.  Taken only when a tile's exponentials
+// against the running reference overflowed, so it favours size over speed.
+__device__ __forceinline__ void recompute_scores(const FlashParams &p, int bh, int i, int key0, int cnt,
+                                                 float (&x)[kBN])
+{
+    const bool row_in = i < p.m;
+    const __nv_bfloat16 *qr = p.q + (static_cast<size_t>(bh) * p.m + (row_in ? i : 0)) * kD;
+    float q[kD];
+#pragma unroll
+    for (int d = 0; d < kD; ++d) q[d] = row_in ? __bfloat162float(qr[d]) : 0.f;
+    float srow[kBN];
+#pragma unroll 1
+    for (int c = 0; c < kBN; ++c) {
+        float v = -CUDART_INF_F;
+        if (c < cnt) {
+            const __nv_bfloat16 *kr = p.k + (static_cast<size_t>(bh) * p.n + key0 + c) * kD;
+            float a = 0.f;
+#pragma unroll
+            for (int d = 0; d < kD; ++d) a = fmaf(q[d], __bfloat162float(kr[d]), a);
+            v = a * p.scale_log2;
+        }
+        srow[c] = v;
+    }
+#pragma unroll
+    for (int c = 0; c < kBN; ++c) x[c] = srow[c];
+}
+
 __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParams &p, const CUtensorMap *tm_o,
                                              uint32_t tmem, int slot)
 {
@@ -499,55 +587,54 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
             mbar_arrive(&sm.s_free[slot]); // S may be overwritten by the next Q K^T
 
             const int key0 = j * kBN;
+            // keys allowed for row i are exactly those below one bound (the padded
+            // length, and i + 1 for a causal mask): column c is allowed iff c < cnt
+            const int cnt = (causal ? min(kv_len, i + 1) : kv_len) - key0;
             const bool boundary = (key0 + kBN > kv_len) || (causal && key0 + kBN - 1 > q0);
             float x[kBN];
 #pragma unroll
             for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(sr[c]);
+            bool prescaled = boundary; // x already multiplied by scale * log2 e
             if (boundary) {
-                // keys allowed for row i are exactly those below one bound (the padded
-                // length, and i + 1 for a causal mask): column c is allowed iff c < cnt.
-                // Scale first, then mask: a zero scale must not turn -inf into NaN.
-                const int cnt = (causal ? min(kv_len, i + 1) : kv_len) - key0;
+                // scale first, then mask: a zero scale must not turn -inf into NaN
 #pragma unroll
                 for (int c = 0; c < kBN; ++c) x[c] = c < cnt ? x[c] * sl2 : -CUDART_INF_F;
             }
-            // row maximum: four independent chains of three-input max
-            float mx[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) mx[k] = fmaxf(x[2 * k], x[2 * k + 1]);
-#pragma unroll
-            for (int c = 8; c < kBN; c += 8) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) mx[k] = max3(mx[k], x[c + 2 * k], x[c + 2 * k + 1]);
-            }
-            float row_max = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-            if (!boundary) row_max *= sl2;
-            const float m_new = fmaxf(m_run, row_max);
-            const bool grow = m_new > m_run + kRescaleThreshold;
-            const float m_use = grow ? m_new : m_run;
-            const float alpha = grow ? ex2(m_run - m_new) : 1.f; // 0 on the first tile
-            const float m_sub = (m_use == -CUDART_INF_F) ? 0.f : m_use;
 
-            // exponentials into registers as bf16 pairs; the exponent argument and
-            // the row sum use packed two-lane fp32 ops
-            const uint64_t mul2 = boundary ? f2(1.f, 1.f) : f2(sl2, sl2);
-            const uint64_t sub2 = f2(-m_sub, -m_sub);
-            uint64_t acc2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
+            // Reference for the exponentials.  The row max is taken only on the row's
+            // first key tile; later tiles use the running reference and check the
+            // result through the tile's row sum.
+            float m_use = m_run, alpha = 1.f;
+            bool grow = false;
+            const bool first = m_run == -CUDART_INF_F;
+            if (first) move_reference(x, prescaled, sl2, m_run, m_use, alpha, grow);
             uint32_t pk[kBN / 2];
+            float tile_sum = weights_bf16(x, prescaled, sl2, m_use, pk);
+            if (!first && !(tile_sum <= kFastSumLimit)) {
+                if (tile_sum < CUDART_INF_F) {
+                    // Finite but large: scale the weights by 2^-k (k an integer, so the
+                    // bf16 values scale exactly) and move the reference up by k.
+                    const int k = ((__float_as_int(tile_sum) >> 23) & 0xff) - 127 - 7; // 8..120
+                    const float f = __int_as_float((127 - k) << 23);                   // 2^-k
 #pragma unroll
-            for (int c2 = 0; c2 < kBN / 2; ++c2) {
-                const int c = 2 * c2;
-                float a0, a1;
-                unf2(fma2(f2(x[c], x[c + 1]), mul2, sub2), a0, a1);
-                const float e0 = ex2(a0), e1 = ex2(a1);
-                acc2[c2 & 1] = add2(acc2[c2 & 1], f2(e0, e1));
-                pk[c2] = pack_bf16x2(e0, e1);
+                    for (int c2 = 0; c2 < kBN / 2; ++c2) {
+                        const float lo = __uint_as_float(pk[c2] << 16), hi = __uint_as_float(pk[c2] & 0xffff0000u);
+                        pk[c2] = pack_bf16x2(lo * f, hi * f);
+                    }
+                    tile_sum *= f;
+                    alpha = f;
+                    m_use = m_run + static_cast<float>(k);
+                    grow = true;
+                } else {
+                    // Some weight overflowed (the scores grew by 128 or more in log2
+                    // units, or are not finite).  The scores have left the registers:
+                    // recompute this row's from Q and K, already scaled and masked,
+                    // and take their max.
+                    recompute_scores(p, bh, i, key0, cnt, x);
+                    move_reference(x, true, sl2, m_run, m_use, alpha, grow);
+                    tile_sum = weights_bf16(x, true, sl2, m_use, pk);
+                }
             }
-            float s0, s1, s2, s3;
-            unf2(acc2[0], s0, s1);
-            unf2(acc2[1], s2, s3);
-            l_run = l_run * alpha + ((s0 + s1) + (s2 + s3));
-
             if (j > 0) {
                 // P and O are still in use by the previous P V until it completes;
                 // waiting only now lets the exponentials above overlap with it
@@ -555,18 +642,18 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
                 if (!ok) break;
                 ++pv_cnt;
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, grow)) {
-                    // move O to the new reference max (rare: only when the max grew by > 2^8)
+            }
+            if (j > 0 && __any_sync(0xffffffffu, grow)) {
+                // move O to the new reference (rare: a large tile sum or a recomputation)
 #pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        uint32_t orr[32];
-                        tmem_ld32(t_o + 32 * h2, orr);
-                        tmem_wait_ld();
-                        reg_fence32(orr);
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    uint32_t orr[32];
+                    tmem_ld32(t_o + 32 * h2, orr);
+                    tmem_wait_ld();
+                    reg_fence32(orr);
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) orr[c] = __float_as_uint(__uint_as_float(orr[c]) * alpha);
-                        tmem_st32(t_o + 32 * h2, orr);
-                    }
+                    for (int c = 0; c < 32; ++c) orr[c] = __float_as_uint(__uint_as_float(orr[c]) * alpha);
+                    tmem_st32(t_o + 32 * h2, orr);
                 }
             }
             tmem_st32(t_p, pk);
@@ -574,6 +661,7 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&sm.p_full[slot]);
+            l_run = l_run * alpha + tile_sum;
             m_run = m_use;
         }
         if (!ok) break;
@@ -772,6 +860,8 @@ cudaError_t launch_flash(const Problem &pb, bool pair_mode, int *tile_counter, c
         !encode_map(&to, pb.out, pb.m, BH))
         return cudaErrorInvalidValue;
     FlashParams p;
+    p.q = static_cast<const __nv_bfloat16 *>(pb.q);
+    p.k = static_cast<const __nv_bfloat16 *>(pb.k);
     p.key_lengths = (pb.mask_kind & kMaskKeyPadding) ? pb.key_lengths : nullptr;
     p.out = static_cast<__nv_bfloat16 *>(pb.out);
     p.BH = BH;
