@@ -65,6 +65,12 @@ class Oracle:
         lib.oracle_bf16_to_f64.restype = None
         lib.oracle_f32_to_f64.argtypes = [ctypes.POINTER(ctypes.c_float), dp, i64]
         lib.oracle_f32_to_f64.restype = None
+        lib.oracle_attn_lse.argtypes = [dp, dp, i32p, ctypes.c_int, ctypes.c_double,
+                                        i64, i64, i64, i64, i64, dp]
+        lib.oracle_attn_lse.restype = ctypes.c_int
+        lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, i32p, ctypes.c_int, ctypes.c_double,
+                                        i64, i64, i64, i64, i64, i64p, i64, dp, dp, dp]
+        lib.oracle_attn_bwd.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
         self._lib = lib
@@ -134,6 +140,48 @@ class Oracle:
         if rc != 0:
             raise RuntimeError("oracle_attn_rows failed")
         return out
+
+    def attn_lse(self, q, k, key_lengths: Optional[np.ndarray], mask_kind: int, scale: float) -> np.ndarray:
+        """Natural log of each row's softmax normaliser, float64 [B, h, m] (-inf: no allowed key)."""
+        q, k = self.widen(q), self.widen(k)
+        B, h, m, n, d = self._dims(q, k, k)
+        lens = None if key_lengths is None else np.ascontiguousarray(key_lengths, dtype=np.int32)
+        out = np.empty((B, h, m), dtype=np.float64)
+        dp = ctypes.POINTER(ctypes.c_double)
+        rc = self._lib.oracle_attn_lse(
+            q.ctypes.data_as(dp), k.ctypes.data_as(dp),
+            None if lens is None else lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+            int(mask_kind), float(scale), B, h, m, n, d, out.ctypes.data_as(dp))
+        if rc != 0:
+            raise RuntimeError("oracle_attn_lse failed")
+        return out
+
+    def attn_bwd(self, q, k, v, do, key_lengths: Optional[np.ndarray], mask_kind: int, scale: float,
+                 heads: Optional[np.ndarray] = None):
+        """Gradients (dQ, dK, dV) of sum(dO * out), float64, shaped like q, k, v.
+
+        heads: linear (batch * h + head) ids to compute; the others stay NaN.
+        """
+        q, k, v, do = self.widen(q), self.widen(k), self.widen(v), self.widen(do)
+        B, h, m, n, d = self._dims(q, k, v)
+        if do.shape != q.shape:
+            raise ValueError(f"dO{do.shape} must match q{q.shape}")
+        lens = None if key_lengths is None else np.ascontiguousarray(key_lengths, dtype=np.int32)
+        dq = np.full(q.shape, np.nan)
+        dk = np.full(k.shape, np.nan)
+        dv = np.full(v.shape, np.nan)
+        hl = None if heads is None else np.ascontiguousarray(heads, dtype=np.int64)
+        dp = ctypes.POINTER(ctypes.c_double)
+        rc = self._lib.oracle_attn_bwd(
+            q.ctypes.data_as(dp), k.ctypes.data_as(dp), v.ctypes.data_as(dp), do.ctypes.data_as(dp),
+            None if lens is None else lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+            int(mask_kind), float(scale), B, h, m, n, d,
+            None if hl is None else hl.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+            0 if hl is None else hl.size,
+            dq.ctypes.data_as(dp), dk.ctypes.data_as(dp), dv.ctypes.data_as(dp))
+        if rc != 0:
+            raise RuntimeError("oracle_attn_bwd failed")
+        return dq, dk, dv
 
 
 _default: Optional[Oracle] = None

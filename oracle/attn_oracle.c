@@ -181,3 +181,180 @@ int oracle_attn_fwd(const double *Q, const double *K, const double *V,
     free(rows);
     return rc;
 }
+
+/*
+ * Natural log of the softmax normaliser of every row, lse_i = log sum_j exp(s_ij)
+ * over the allowed keys (s_ij the scaled scores above), so that the weights are
+ * exp(s_ij - lse_i); -inf for a row with no allowed key.  lse is [B][h][m].
+ */
+int oracle_attn_lse(const double *Q, const double *K, const int32_t *key_lengths, int mask_kind,
+                    double scale, int64_t B, int64_t h, int64_t m, int64_t n, int64_t d, double *lse)
+{
+    if (!Q || !K || !lse || B < 0 || h < 0 || m < 0 || n < 1 || d < 1) return -1;
+    int64_t total = B * h * m;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 16)
+#endif
+    for (int64_t r = 0; r < total; ++r) {
+        int64_t i = r % m, bh = r / m, b = bh / h;
+        int64_t len_b = clamp_len(key_lengths, mask_kind, b, n);
+        const double *qr = Q + r * d;
+        const double *Kh = K + bh * n * d;
+        double mu = -INFINITY;
+        for (int64_t j = 0; j < n; ++j) {
+            if (!key_allowed(mask_kind, i, j, len_b)) continue;
+            const double *kj = Kh + j * d;
+            double dot = 0.0;
+            for (int64_t c = 0; c < d; ++c) dot += qr[c] * kj[c];
+            if (scale * dot > mu) mu = scale * dot;
+        }
+        if (mu == -INFINITY) {
+            lse[r] = -INFINITY;
+            continue;
+        }
+        double Z = 0.0;
+        for (int64_t j = 0; j < n; ++j) {
+            if (!key_allowed(mask_kind, i, j, len_b)) continue;
+            const double *kj = Kh + j * d;
+            double dot = 0.0;
+            for (int64_t c = 0; c < d; ++c) dot += qr[c] * kj[c];
+            Z += exp(scale * dot - mu);
+        }
+        lse[r] = mu + log(Z);
+    }
+    return 0;
+}
+
+/*
+ * Gradients of sum(dO * O) with respect to Q, K and V, O the attention output
+ * above, dO an upstream gradient [B][h][m][d].  The pages train the model
+ * (slide deck "Training Details"; primer "Training and Implementation Details")
+ * but do not write the backward pass out: it is the chain rule applied to the
+ * attention equation.  With p_ij the softmax weights of row i (0 for masked
+ * keys) and s_ij = scale * q_i . k_j:
+ *
+ *   O_i   = sum_j p_ij v_j                  =>  dV_j  = sum_i p_ij dO_i
+ *   dP_ij = dO_i . v_j
+ *   p_i.  = softmax(s_i.)                   =>  dS_ij = p_ij (dP_ij - sum_k p_ik dP_ik)
+ *   s_ij  = scale q_i . k_j                 =>  dQ_i  = scale sum_j dS_ij k_j,
+ *                                               dK_j  = scale sum_i dS_ij q_i
+ *
+ * A row with no allowed key has output 0 whatever Q, K, V are: it contributes
+ * nothing.  The work runs as two loops over the same definitions: per query row
+ * (weights, dP, the row term D_i = sum_k p_ik dP_ik, dQ_i) and per key row (dV_j,
+ * dK_j, recomputing p_ij and dP_ij from the saved row max, normaliser and D_i).
+ * Only the (batch, head) pairs listed in bh_list are computed (all when
+ * bh_list is NULL); the gradients of other pairs are left untouched.
+ */
+int oracle_attn_bwd(const double *Q, const double *K, const double *V, const double *dO,
+                    const int32_t *key_lengths, int mask_kind, double scale,
+                    int64_t B, int64_t h, int64_t m, int64_t n, int64_t d,
+                    const int64_t *bh_list, int64_t nbh,
+                    double *dQ, double *dK, double *dV)
+{
+    if (!Q || !K || !V || !dO || !dQ || !dK || !dV || B < 0 || h < 0 || m < 0 || n < 1 || d < 1) return -1;
+    if (bh_list == NULL) nbh = B * h;
+    double *mu = (double *)malloc(sizeof(double) * (size_t)(m > 0 ? m : 1));
+    double *Z = (double *)malloc(sizeof(double) * (size_t)(m > 0 ? m : 1));
+    double *D = (double *)malloc(sizeof(double) * (size_t)(m > 0 ? m : 1));
+    if (!mu || !Z || !D) {
+        free(mu);
+        free(Z);
+        free(D);
+        return -1;
+    }
+    for (int64_t t = 0; t < nbh; ++t) {
+        int64_t bh = bh_list ? bh_list[t] : t;
+        int64_t len_b = clamp_len(key_lengths, mask_kind, bh / h, n);
+        const double *Qh = Q + bh * m * d, *Kh = K + bh * n * d, *Vh = V + bh * n * d;
+        const double *dOh = dO + bh * m * d;
+        double *dQh = dQ + bh * m * d, *dKh = dK + bh * n * d, *dVh = dV + bh * n * d;
+
+        /* per query row: softmax statistics, D_i and dQ_i */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 8)
+#endif
+        for (int64_t i = 0; i < m; ++i) {
+            const double *q = Qh + i * d, *g = dOh + i * d;
+            double *dq = dQh + i * d;
+            for (int64_t c = 0; c < d; ++c) dq[c] = 0.0;
+            double mx = -INFINITY;
+            for (int64_t j = 0; j < n; ++j) {
+                if (!key_allowed(mask_kind, i, j, len_b)) continue;
+                const double *kj = Kh + j * d;
+                double dot = 0.0;
+                for (int64_t c = 0; c < d; ++c) dot += q[c] * kj[c];
+                if (scale * dot > mx) mx = scale * dot;
+            }
+            mu[i] = mx;
+            Z[i] = 0.0;
+            D[i] = 0.0;
+            if (mx == -INFINITY) continue; /* no allowed key */
+            double z = 0.0;
+            for (int64_t j = 0; j < n; ++j) {
+                if (!key_allowed(mask_kind, i, j, len_b)) continue;
+                const double *kj = Kh + j * d;
+                double dot = 0.0;
+                for (int64_t c = 0; c < d; ++c) dot += q[c] * kj[c];
+                z += exp(scale * dot - mx);
+            }
+            Z[i] = z;
+            double Di = 0.0;
+            for (int64_t j = 0; j < n; ++j) {
+                if (!key_allowed(mask_kind, i, j, len_b)) continue;
+                const double *kj = Kh + j * d, *vj = Vh + j * d;
+                double dot = 0.0, dp = 0.0;
+                for (int64_t c = 0; c < d; ++c) {
+                    dot += q[c] * kj[c];
+                    dp += g[c] * vj[c];
+                }
+                Di += exp(scale * dot - mx) / z * dp;
+            }
+            D[i] = Di;
+            for (int64_t j = 0; j < n; ++j) {
+                if (!key_allowed(mask_kind, i, j, len_b)) continue;
+                const double *kj = Kh + j * d, *vj = Vh + j * d;
+                double dot = 0.0, dp = 0.0;
+                for (int64_t c = 0; c < d; ++c) {
+                    dot += q[c] * kj[c];
+                    dp += g[c] * vj[c];
+                }
+                double ds = exp(scale * dot - mx) / z * (dp - Di);
+                for (int64_t c = 0; c < d; ++c) dq[c] += scale * ds * kj[c];
+            }
+        }
+
+        /* per key row: dV_j and dK_j */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 8)
+#endif
+        for (int64_t j = 0; j < n; ++j) {
+            const double *k = Kh + j * d, *v = Vh + j * d;
+            double *dk = dKh + j * d, *dv = dVh + j * d;
+            for (int64_t c = 0; c < d; ++c) {
+                dk[c] = 0.0;
+                dv[c] = 0.0;
+            }
+            for (int64_t i = 0; i < m; ++i) {
+                if (mu[i] == -INFINITY || !key_allowed(mask_kind, i, j, len_b)) continue;
+                const double *q = Qh + i * d, *g = dOh + i * d;
+                double dot = 0.0, dp = 0.0;
+                for (int64_t c = 0; c < d; ++c) {
+                    dot += q[c] * k[c];
+                    dp += g[c] * v[c];
+                }
+                double p = exp(scale * dot - mu[i]) / Z[i];
+                double ds = p * (dp - D[i]);
+                for (int64_t c = 0; c < d; ++c) {
+                    dv[c] += p * g[c];
+                    dk[c] += scale * ds * q[c];
+                }
+            }
+        }
+    }
+    free(mu);
+    free(Z);
+    free(D);
+    return 0;
+}
+

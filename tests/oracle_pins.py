@@ -250,6 +250,148 @@ def pin_torch_sdpa(o):
         np.testing.assert_allclose(got[live], ref[live], rtol=0, atol=1e-12)
 
 
+# ---------------------------------------------------------------- backward and lse
+# The gradients are the chain rule of the attention equation (the pages train the
+# model but do not write the backward pass out).  They are pinned by the forward
+# oracle itself through finite differences of sum(dO * out), by exact identities
+# that follow from the softmax, and by torch's fp64 autograd.
+
+def _bwd_case(rng, B, h, m, n, d):
+    return (_rand(rng, B, h, m, d), _rand(rng, B, h, n, d), _rand(rng, B, h, n, d),
+            _rand(rng, B, h, m, d))
+
+
+def _loss(o, Q, K, V, dO, lens, mk, scale):
+    return float((dO * o.attn_fwd(Q, K, V, lens, mk, scale)).sum())
+
+
+def pin_bwd_elementwise_finite_differences(o):
+    """Every element of dQ, dK, dV against a central difference of sum(dO * out)."""
+    rng = np.random.default_rng(31)
+    eps = 1e-6
+    for mk, (m, n), lens in ((0, (3, 4), None), (PAD, (3, 5), [0, 3]), (CAUSAL, (4, 4), None),
+                             (PAD | CAUSAL, (4, 4), [2, 9])):
+        B, h, d = 2, 2, 3
+        Q, K, V, dO = _bwd_case(rng, B, h, m, n, d)
+        lens_a = None if lens is None else np.array(lens, dtype=np.int32)
+        grads = o.attn_bwd(Q, K, V, dO, lens_a, mk, 0.9)
+        for x, g, name in zip((Q, K, V), grads, "QKV"):
+            for idx in np.ndindex(x.shape):
+                keep = x[idx]
+                x[idx] = keep + eps
+                up = _loss(o, Q, K, V, dO, lens_a, mk, 0.9)
+                x[idx] = keep - eps
+                down = _loss(o, Q, K, V, dO, lens_a, mk, 0.9)
+                x[idx] = keep
+                fd = (up - down) / (2 * eps)
+                assert abs(fd - g[idx]) <= 1e-7 * (1 + abs(fd)), (name, mk, idx, fd, g[idx])
+
+
+def pin_bwd_directional_finite_differences(o):
+    """Larger shapes (several heads, ragged lengths): directional derivatives along random
+    directions against central differences."""
+    rng = np.random.default_rng(32)
+    B, h, m, n, d = 3, 2, 19, 19, 8
+    eps = 1e-6
+    lens = np.array([19, 7, 0], dtype=np.int32)
+    for mk in (0, PAD, CAUSAL, PAD | CAUSAL):
+        Q, K, V, dO = _bwd_case(rng, B, h, m, n, d)
+        grads = o.attn_bwd(Q, K, V, dO, lens, mk, 0.35)
+        for which in range(3):
+            xs = [Q, K, V]
+            Dir = rng.standard_normal(xs[which].shape)
+            up = list(xs)
+            up[which] = xs[which] + eps * Dir
+            down = list(xs)
+            down[which] = xs[which] - eps * Dir
+            fd = (_loss(o, *up, dO, lens, mk, 0.35) - _loss(o, *down, dO, lens, mk, 0.35)) / (2 * eps)
+            an = float((grads[which] * Dir).sum())
+            assert abs(fd - an) <= 1e-6 * (1 + abs(fd)), ("QKV"[which], mk, fd, an)
+
+
+def pin_bwd_softmax_identities(o):
+    """Exact consequences of the softmax, per (batch, head):
+    sum_j dK_j = 0 (shifting every key by one vector shifts a row's scores by a constant);
+    sum_j dV_j = sum of dO over rows with an allowed key (each row's weights sum to one);
+    sum_i q_i . dQ_i = sum_j k_j . dK_j (Q and K enter only through their products)."""
+    rng = np.random.default_rng(33)
+    B, h, m, n, d = 2, 3, 9, 12, 5
+    lens = np.array([0, 8], dtype=np.int32)
+    for mk in (0, PAD, PAD | CAUSAL):
+        mm = n if mk & CAUSAL else m
+        Q, K, V, dO = _bwd_case(rng, B, h, mm, n, d)
+        dQ, dK, dV = o.attn_bwd(Q, K, V, dO, lens, mk, 0.6)
+        np.testing.assert_allclose(dK.sum(axis=2), 0.0, atol=1e-12)
+        live = np.ones((B, 1, mm, 1), dtype=bool)
+        if mk & PAD:
+            live[lens == 0] = False
+        np.testing.assert_allclose(dV.sum(axis=2), (dO * live).sum(axis=2), atol=1e-12)
+        np.testing.assert_allclose((Q * dQ).sum(axis=(2, 3)), (K * dK).sum(axis=(2, 3)), atol=1e-12)
+
+
+def pin_bwd_uniform_scores(o):
+    """Q = 0: every allowed key has weight 1/len, so dV_j is the mean of dO over the rows
+    that see key j, and dQ_i = scale * sum_j (1/len)(dP_ij - mean dP_i.) k_j."""
+    rng = np.random.default_rng(34)
+    B, h, n, d = 1, 1, 6, 4
+    Q = np.zeros((B, h, n, d))
+    K, V, dO = _rand(rng, B, h, n, d), _rand(rng, B, h, n, d), _rand(rng, B, h, n, d)
+    dQ, dK, dV = o.attn_bwd(Q, K, V, dO, None, CAUSAL, 0.5)
+    for j in range(n):
+        ref = sum(dO[0, 0, i] / (i + 1) for i in range(j, n))
+        np.testing.assert_allclose(dV[0, 0, j], ref, atol=1e-13)
+    for i in range(n):
+        dp = V[0, 0, :i + 1] @ dO[0, 0, i]
+        ds = (dp - dp.mean()) / (i + 1)
+        np.testing.assert_allclose(dQ[0, 0, i], 0.5 * ds @ K[0, 0, :i + 1], atol=1e-13)
+    np.testing.assert_allclose(dK, 0.0, atol=1e-15)  # dS is multiplied by q_i = 0
+
+
+def pin_lse(o):
+    """lse against the full-matrix formula: exp(scale*QK^T + M - lse) has unit row sums,
+    and uniform scores give log(len)."""
+    rng = np.random.default_rng(35)
+    B, h, m, n, d = 2, 2, 7, 7, 3
+    Q, K = _rand(rng, B, h, m, d), _rand(rng, B, h, n, d)
+    lens = np.array([0, 5], dtype=np.int32)
+    for mk in (0, PAD, CAUSAL, PAD | CAUSAL):
+        lse = o.attn_lse(Q, K, lens, mk, 0.7)
+        for b in range(B):
+            M = brute.additive_mask(m, n, mk, int(lens[b]))
+            for head in range(h):
+                S = Q[b, head] @ K[b, head].T * 0.7 + M
+                for i in range(m):
+                    if np.isfinite(S[i]).any():
+                        assert abs(np.exp(S[i] - lse[b, head, i]).sum() - 1.0) <= 1e-13
+                    else:
+                        assert lse[b, head, i] == -np.inf
+    zero = np.zeros((1, 1, 5, 3))
+    np.testing.assert_allclose(o.attn_lse(zero, K[:1, :1, :5], None, CAUSAL, 1.0)[0, 0],
+                               np.log(np.arange(1, 6)), atol=1e-14)
+
+
+def pin_bwd_torch_autograd(o):
+    """torch fp64 autograd through its scaled_dot_product_attention (rows with an allowed key)."""
+    import torch
+    import torch.nn.functional as F
+
+    rng = np.random.default_rng(36)
+    B, h, m, n, d = 2, 2, 10, 10, 8
+    lens = np.array([4, 10], dtype=np.int32)
+    for mk in (0, PAD, CAUSAL, PAD | CAUSAL):
+        Q, K, V, dO = _bwd_case(rng, B, h, m, n, d)
+        allow = np.ones((B, 1, m, n), dtype=bool)
+        if mk & CAUSAL:
+            allow &= ~(np.arange(n)[None, None, None, :] > np.arange(m)[None, None, :, None])
+        if mk & PAD:
+            allow &= np.arange(n)[None, None, None, :] < lens[:, None, None, None]
+        tq, tk, tv = (torch.from_numpy(x.copy()).requires_grad_(True) for x in (Q, K, V))
+        out = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=torch.from_numpy(allow), scale=0.4)
+        out.backward(torch.from_numpy(dO))
+        for got, ref in zip(o.attn_bwd(Q, K, V, dO, lens, mk, 0.4), (tq.grad, tk.grad, tv.grad)):
+            np.testing.assert_allclose(got, ref.numpy(), rtol=0, atol=1e-12)
+
+
 ALL_PINS = [
     pin_worked_example_printed,
     pin_worked_example_closed_form,
@@ -265,4 +407,10 @@ ALL_PINS = [
     pin_lengths_indexed_by_batch,
     pin_brute_force,
     pin_torch_sdpa,
+    pin_bwd_elementwise_finite_differences,
+    pin_bwd_directional_finite_differences,
+    pin_bwd_softmax_identities,
+    pin_bwd_uniform_scores,
+    pin_lse,
+    pin_bwd_torch_autograd,
 ]

@@ -23,6 +23,21 @@ MUTANTS = {
     "query_row_of_first_position": ("const double *q = Q + r * d;", "const double *q = Q + bh * m * d;"),
     "length_of_wrong_batch": ("int64_t b = bh / h;", "int64_t b = (bh / h + 1) % B;"),
     "length_not_clamped": ("if (len > n) len = n;", "if (len > n) len = n - 1;"),
+    # backward and lse
+    "bwd_dq_drops_row_term": ("double ds = exp(scale * dot - mx) / z * (dp - Di);",
+                              "double ds = exp(scale * dot - mx) / z * dp;"),
+    "bwd_dk_drops_row_term": ("double ds = p * (dp - D[i]);", "double ds = p * dp;"),
+    "bwd_row_term_unweighted": ("Di += exp(scale * dot - mx) / z * dp;", "Di += dp;"),
+    "bwd_dv_uses_score_gradient": ("dv[c] += p * g[c];", "dv[c] += ds * g[c];"),
+    "bwd_dk_missing_scale": ("dk[c] += scale * ds * q[c];", "dk[c] += ds * q[c];"),
+    "bwd_dq_uses_values": ("dq[c] += scale * ds * kj[c];", "dq[c] += scale * ds * vj[c];"),
+    "bwd_key_pass_ignores_mask": ("if (mu[i] == -INFINITY || !key_allowed(mask_kind, i, j, len_b)) continue;",
+                                  "if (mu[i] == -INFINITY) continue;"),
+    "bwd_upstream_of_wrong_head": ("const double *dOh = dO + bh * m * d;",
+                                   "const double *dOh = dO + (bh + 1) % (B * h) * m * d;"),
+    "bwd_normaliser_dropped_in_key_pass": ("double p = exp(scale * dot - mu[i]) / Z[i];",
+                                           "double p = exp(scale * dot - mu[i]);"),
+    "lse_missing_max": ("lse[r] = mu + log(Z);", "lse[r] = log(Z);"),
 }
 
 

@@ -27,3 +27,18 @@ def test_rows_match_full(oracle_lib):
     rows = sample_rows(w, 40)
     part = oracle_lib.attn_rows(inp.q, inp.k, inp.v, inp.key_lengths, w.mask, w.scale, rows)
     np.testing.assert_array_equal(part, full.reshape(-1, w.d)[rows])
+
+
+def test_bwd_heads_subset_matches_full(oracle_lib):
+    import numpy as np
+    rng = np.random.default_rng(8)
+    q, k, v, do = (rng.standard_normal((2, 3, 9, 4)) for _ in range(4))
+    lens = np.array([4, 9], dtype=np.int32)
+    full = oracle_lib.attn_bwd(q, k, v, do, lens, 3, 0.5)
+    heads = np.array([1, 4])
+    part = oracle_lib.attn_bwd(q, k, v, do, lens, 3, 0.5, heads=heads)
+    for f, g in zip(full, part):
+        f, g = f.reshape(6, 9, 4), g.reshape(6, 9, 4)
+        np.testing.assert_array_equal(g[heads], f[heads])
+        assert np.isnan(np.delete(g, heads, axis=0)).all()
+
