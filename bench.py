@@ -34,7 +34,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from workloads import WORKLOADS, draw  # noqa: E402
+from workloads import draw_dout, WORKLOADS, draw  # noqa: E402
 
 METRIC = "masked MHA fwd TFLOPS on 1 GB300 (and % of bf16 tensor peak / HBM GB/s)"
 UNIT = "TFLOPS"
@@ -246,6 +246,44 @@ def short_workloads(torch, attn, device, peak_hbm):
     return res
 
 
+def backward_workload(torch, attn, device, peak_tf, steps=20):
+    """The backward of workload 5 (B4 h16 n=m=8192 causal): attn_bwd from the output and
+    log-sum-exp of attn_fwd_lse, inputs resident; per call three kernels (row pass,
+    tensor-core pass, dQ conversion).  Useful work: 10*d_k FLOPs per allowed pair
+    (S recomputed, dP, dV, dK, dQ)."""
+    w = WORKLOADS[5]
+    inp = draw(w)
+    q, k, v = (to_device(x, w.dtype, torch, device) for x in (inp.q, inp.k, inp.v))
+    do = to_device(draw_dout(w), w.dtype, torch, device)
+    lens = torch.from_numpy(inp.key_lengths).to(device)
+    stream = torch.cuda.current_stream(device)
+    out, lse = attn.attn_fwd_lse(q, k, v, lens, w.mask, w.scale, stream=stream)
+    ws = torch.empty(attn.bwd_workspace_size(w.B, w.h, w.m, w.n, w.d), dtype=torch.uint8, device=device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def bwd():
+        attn.attn_bwd(q, k, v, out, do, lse, lens, w.mask, w.scale, dq, dk, dv, ws, stream=stream)
+
+    def fwd():
+        attn.attn_fwd_lse(q, k, v, lens, w.mask, w.scale, out=out, lse=lse, stream=stream)
+
+    for _ in range(3):
+        bwd()
+    torch.cuda.synchronize()
+    ms_b = time_launches(bwd, steps, torch, stream)
+    ms_f = time_launches(fwd, steps, torch, stream)
+    st, info = attn.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} (info {info}) after the backward loop")
+    flops_b = 2.5 * useful_flops(w, inp.key_lengths)
+    return {"workload": w.description, "entry_point": "attn_bwd (after attn_fwd_lse)",
+            "us_per_call": ms_b * 1e3, "tflops_useful": flops_b / (ms_b * 1e-3) / 1e12,
+            "frac_of_peak": flops_b / (ms_b * 1e-3) / 1e12 / peak_tf,
+            "forward_with_lse_us": ms_f * 1e3,
+            "training_pass_tflops": 3.5 * useful_flops(w, inp.key_lengths) / ((ms_b + ms_f) * 1e-3) / 1e12,
+            "calls_timed": steps, "algorithmic": "10*d_k FLOPs per allowed (query, key) pair"}
+
+
 def cpu_oracle_sample(w, inp, target_s, seed=3):
     """Time the fp64 oracle on random query rows of w for about target_s seconds."""
     import oracle
@@ -420,6 +458,7 @@ def main():
                          "ms_per_step": ems, "steps": e2e_steps}
         result["gpu_launches"] = args.steps  # e2e launches are outside the device-timed region
         result["other_workloads"] = short_workloads(torch, attn, device, peak_hbm)
+        result["backward"] = backward_workload(torch, attn, device, peak_tf)
         if rank == 0:
             cb, _ = cpu_oracle_sample(w, inp, args.cpu_seconds)
             cb.pop("seconds", None)

@@ -197,6 +197,64 @@ attn_status attn_fwd_noalloc(const void *Q, const void *K, const void *V,
                              const int32_t *key_lengths, int mask_kind, float scale,
                              void *out, const attn_dims *dims, void *stream);
 
+/*
+ * attn_fwd that also writes each query row's log-sum-exp,
+ *
+ *     lse[b,h,i] = log sum_j exp( scale * Q[b,h,i,:] . K[b,h,j,:] + M[b,i,j] )
+ *
+ * (natural log; -inf for a row with no allowed key), so that the softmax
+ * weights of the row are exp(s_ij - lse_i).  It is the statistic a backward
+ * pass (attn_bwd) needs to recompute the weights without storing them.
+ *
+ *   lse   device float [B][h][m], 4-byte aligned, owned by the caller; must not
+ *         overlap any other argument.
+ * Other arguments, rules, errors and kernel choice as attn_fwd; lse NULL is
+ * ATTN_ERR_NULL, unaligned ATTN_ERR_ALIGN, overlapping ATTN_ERR_ALIAS.
+ */
+attn_status attn_fwd_lse(const void *Q, const void *K, const void *V,
+                         const int32_t *key_lengths, int mask_kind, float scale,
+                         void *out, float *lse, const attn_dims *dims, void *stream);
+
+/* Bytes of device workspace attn_bwd needs for these dims (host only, no CUDA
+ * call); 0 if attn_bwd would reject the dims. */
+size_t attn_bwd_workspace_size(const attn_dims *dims);
+
+/*
+ * Backward of the attention: with out = attn_fwd(Q, K, V) and an upstream
+ * gradient dout of the same shape, the gradients of sum(dout * out),
+ *
+ *     dV = P^T dout,   dS = P o (dout V^T - D),   D_i = sum_c dout_ic out_ic,
+ *     dQ = scale dS K, dK = scale dS^T Q,
+ *
+ * per (batch, head), P the softmax weights of the forward.  The pages train the
+ * model (slide deck "Training Details") but do not write this pass out: it is
+ * the chain rule of the attention equation.  P is recomputed from Q, K and lse.
+ *
+ *   Q, K, V, out   the forward's inputs and output (out as written by attn_fwd_lse)
+ *   dout           device [B][h][m][d_k], the gradient of the loss w.r.t. out
+ *   lse            device float [B][h][m] written by attn_fwd_lse for the same
+ *                  inputs, mask and scale
+ *   key_lengths, mask_kind, scale   as for the forward
+ *   dQ, dK, dV     device outputs shaped like Q, K, V; every element is written
+ *                  (0 for keys no query may see)
+ *   workspace      device scratch of at least attn_bwd_workspace_size(dims)
+ *                  bytes, 256-byte aligned, any contents; calls that may run at
+ *                  the same time on the GPU need different workspaces
+ *   dims, stream   as for the forward
+ *
+ * Supported: bf16 with d_k == 64 (ATTN_ERR_DTYPE otherwise).  All tensors
+ * 16-byte aligned, lse 4-byte aligned (ATTN_ERR_ALIGN).  dQ, dK, dV and the
+ * workspace must not overlap each other or any input (ATTN_ERR_ALIAS).  A
+ * workspace that is too small is ATTN_ERR_SHAPE.  Other errors as attn_fwd.
+ * Three kernels are enqueued: a row pass (D and the padded per-row table; zeroes
+ * the dQ accumulator), the tensor-core pass, and the dQ conversion.
+ */
+attn_status attn_bwd(const void *Q, const void *K, const void *V, const void *out,
+                     const void *dout, const float *lse, const int32_t *key_lengths,
+                     int mask_kind, float scale, void *dQ, void *dK, void *dV,
+                     void *workspace, size_t workspace_bytes,
+                     const attn_dims *dims, void *stream);
+
 /* The kernel attn_fwd would run for these dims and mask (host only, no CUDA call);
  * ATTN_KERNEL_AUTO (0) if the call would be rejected. */
 int attn_select_kernel(const attn_dims *dims, int mask_kind);

@@ -112,3 +112,44 @@ def test_workspace_validation():
     assert _call_ws(ws=O + 64) == 10          # inside out
     assert _call_ws(ws=A) == 10               # inside Q
     assert _call_ws(q=A + 8) == 5             # tensor checks still apply
+
+
+# ---------------------------------------------------------------- forward with lse, backward
+LSE, DO, OUT2, DQ, DK, DV, WS = 0x7000000, 0x8000000, 0x9000000, 0xA000000, 0xB000000, 0xC000000, 0xD000000
+
+
+def test_fwd_lse_validation():
+    d = N.make_dims(2, 2, 8, 8, 64, 0)
+    assert N.fwd_lse_raw(A, B_, C, None, 0, 0.125, O, None, d, None) == 1      # lse NULL
+    assert N.fwd_lse_raw(A, B_, C, None, 0, 0.125, O, LSE + 2, d, None) == 5   # lse unaligned
+    assert N.fwd_lse_raw(A, B_, C, None, 0, 0.125, O, O + 16, d, None) == 10   # lse inside out
+    assert N.fwd_lse_raw(A, B_, C, None, 0, 0.125, O, A, d, None) == 10        # lse inside Q
+    assert N.fwd_lse_raw(A + 8, B_, C, None, 0, 0.125, O, LSE, d, None) == 5   # forward checks apply
+
+
+def test_bwd_workspace_size():
+    assert N.bwd_workspace_size(N.make_dims(2, 3, 300, 200, 64, 0)) >= 2 * 3 * 300 * 64 * 4
+    assert N.bwd_workspace_size(N.make_dims(2, 3, 300, 200, 64, 1)) == 0   # fp32: no backward
+    assert N.bwd_workspace_size(N.make_dims(2, 3, 300, 200, 32, 0)) == 0   # d_k != 64
+    assert N.bwd_workspace_size(N.make_dims(0, 3, 300, 200, 64, 0)) == 0   # bad dims
+
+
+def _call_bwd(dims=(2, 2, 8, 8, 64, 0), mask=0, lens=None, ws_bytes=None, **kw):
+    d = N.make_dims(*dims)
+    ws_bytes = N.bwd_workspace_size(N.make_dims(2, 2, 8, 8, 64, 0)) if ws_bytes is None else ws_bytes
+    a = dict(q=A, k=B_, v=C, out=OUT2, dout=DO, lse=LSE, dq=DQ, dk=DK, dv=DV, ws=WS)
+    a.update(kw)
+    return N.bwd_raw(a["q"], a["k"], a["v"], a["out"], a["dout"], a["lse"], lens, mask, 0.125, a["dq"],
+                     a["dk"], a["dv"], a["ws"], ws_bytes, d, None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(out=None), 1), (dict(dout=None), 1), (dict(lse=None), 1), (dict(dq=None), 1), (dict(dk=None), 1),
+    (dict(dv=None), 1), (dict(ws=None), 1), (dict(q=None), 1), (dict(mask=1), 1),
+    (dict(dims=(2, 2, 8, 8, 64, 1)), 3), (dict(dims=(2, 2, 8, 8, 32, 0)), 3),
+    (dict(dims=(2, 2, 8, 9, 64, 0), mask=2), 2), (dict(ws_bytes=64), 2),
+    (dict(dout=DO + 8), 5), (dict(dk=DK + 2), 5), (dict(lse=LSE + 1), 5), (dict(ws=WS + 16), 5),
+    (dict(dq=A), 10), (dict(dk=DQ + 32), 10), (dict(dv=DO), 10), (dict(ws=LSE), 10), (dict(dv=OUT2 + 16), 10),
+])
+def test_bwd_rejects_bad_arguments(kwargs, status):
+    assert _call_bwd(**kwargs) == status

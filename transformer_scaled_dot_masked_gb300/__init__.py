@@ -1,8 +1,11 @@
 """GB300 (sm_103a) masked scaled dot-product multi-head attention.
 
     out = attn_fwd(q, k, v, key_lengths, mask_kind, scale)
+    out, lse = attn_fwd_lse(q, k, v, key_lengths, mask_kind, scale)
+    dq, dk, dv = attn_bwd(q, k, v, out, dout, lse, key_lengths, mask_kind, scale)
 
-computes softmax(scale * Q K^T + M) V for every (batch, head) on the GPU
+computes softmax(scale * Q K^T + M) V for every (batch, head) on the GPU, and
+its gradients (the chain rule of that equation),
 through the C ABI in ``include/attn.h`` ("Paper Deep Reading: Attention Is All
 You Need", §04 attention equation with the additive mask M).  Importing the
 package fails when the CUDA library has not been built.
@@ -15,7 +18,7 @@ from . import _native
 from ._native import (AttnError, KERNEL_AUTO, KERNEL_FLASH, KERNEL_SHORT, KERNEL_SIMT, MASK_CAUSAL,
                       MASK_KEY_PADDING, MASK_NONE, DTYPE_BF16, DTYPE_FP32)
 
-__all__ = ["attn_fwd", "AttnError", "select_kernel", "device_status", "make_workspace", "workspace_size", "MASK_NONE", "MASK_KEY_PADDING",
+__all__ = ["attn_fwd", "attn_fwd_lse", "attn_bwd", "bwd_workspace_size", "AttnError", "select_kernel", "device_status", "make_workspace", "workspace_size", "MASK_NONE", "MASK_KEY_PADDING",
            "MASK_CAUSAL", "KERNEL_AUTO", "KERNEL_FLASH", "KERNEL_SHORT", "KERNEL_SIMT"]
 
 
@@ -99,3 +102,98 @@ def select_kernel(B, h, m, n, d, dtype: int, mask_kind: int) -> int:
 def device_status(stream=None):
     """(status, info) of the bounded-wait record; synchronises the stream."""
     return _native.device_status(None if stream is None else stream.cuda_stream)
+
+
+def _check_qkv(q, k, v):
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, h, len, d_k]")
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous CUDA tensors")
+    B, h, m, d = q.shape
+    n = k.shape[2]
+    if k.shape != (B, h, n, d) or v.shape != k.shape or q.dtype != k.dtype or q.dtype != v.dtype:
+        raise ValueError(f"shape/dtype mismatch: q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    return B, h, m, n, d
+
+
+def _lengths_ptr(key_lengths, mask_kind, B):
+    import torch
+    if not mask_kind & MASK_KEY_PADDING:
+        return None
+    if key_lengths is None or key_lengths.dtype != torch.int32 or not key_lengths.is_cuda \
+            or key_lengths.numel() != B:
+        raise ValueError("key padding needs key_lengths: int32 CUDA tensor of B elements")
+    return key_lengths.data_ptr()
+
+
+def _like(t, ref, name):
+    if t.shape != ref.shape or t.dtype != ref.dtype or not t.is_contiguous() or not t.is_cuda:
+        raise ValueError(f"{name} must be a contiguous CUDA tensor shaped and typed like {tuple(ref.shape)}")
+
+
+def attn_fwd_lse(q, k, v, key_lengths=None, mask_kind: int = MASK_NONE, scale: Optional[float] = None,
+                 out=None, lse=None, stream=None):
+    """attn_fwd that also returns each query row's log-sum-exp (float32 [B, h, m], natural log),
+    the statistic ``attn_bwd`` needs.  Returns (out, lse)."""
+    import torch
+    B, h, m, n, d = _check_qkv(q, k, v)
+    scale = d ** -0.5 if scale is None else scale
+    if out is None:
+        out = torch.empty_like(q)
+    _like(out, q, "out")
+    if lse is None:
+        lse = torch.empty((B, h, m), dtype=torch.float32, device=q.device)
+    elif lse.shape != (B, h, m) or lse.dtype != torch.float32 or not lse.is_contiguous() or not lse.is_cuda:
+        raise ValueError("lse must be a contiguous float32 CUDA tensor [B, h, m]")
+    stream = torch.cuda.current_stream(q.device) if stream is None else stream
+    dims = _native.make_dims(B, h, m, n, d, _dtype_code(q))
+    st = _native.fwd_lse_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), _lengths_ptr(key_lengths, mask_kind, B),
+                             mask_kind, scale, out.data_ptr(), lse.data_ptr(), dims, stream.cuda_stream)
+    if st != _native.ATTN_OK:
+        raise AttnError(st)
+    return out, lse
+
+
+def bwd_workspace_size(B, h, m, n, d, dtype: int = DTYPE_BF16) -> int:
+    """Bytes of device workspace ``attn_bwd`` needs (0: those dims are not supported)."""
+    return _native.bwd_workspace_size(_native.make_dims(B, h, m, n, d, dtype))
+
+
+def attn_bwd(q, k, v, out, dout, lse, key_lengths=None, mask_kind: int = MASK_NONE,
+             scale: Optional[float] = None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of sum(dout * out) for out = attention(q, k, v), bf16 with d_k = 64.
+
+    out and lse come from ``attn_fwd_lse`` on the same inputs, mask and scale.
+    workspace: optional CUDA uint8 buffer of at least ``bwd_workspace_size(...)`` bytes
+    (allocated per call otherwise); calls that may overlap on the GPU need different ones.
+    """
+    import torch
+    B, h, m, n, d = _check_qkv(q, k, v)
+    scale = d ** -0.5 if scale is None else scale
+    _like(out, q, "out")
+    _like(dout, q, "dout")
+    if lse.shape != (B, h, m) or lse.dtype != torch.float32 or not lse.is_contiguous() or not lse.is_cuda:
+        raise ValueError("lse must be a contiguous float32 CUDA tensor [B, h, m]")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _like(dq, q, "dq")
+    _like(dk, k, "dk")
+    _like(dv, v, "dv")
+    dims = _native.make_dims(B, h, m, n, d, _dtype_code(q))
+    need = _native.bwd_workspace_size(dims)
+    if need == 0:
+        raise AttnError(3)  # ATTN_ERR_DTYPE: the backward runs bf16 with d_k = 64
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    stream = torch.cuda.current_stream(q.device) if stream is None else stream
+    st = _native.bwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), dout.data_ptr(),
+                         lse.data_ptr(), _lengths_ptr(key_lengths, mask_kind, B), mask_kind, scale,
+                         dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+                         workspace.numel() * workspace.element_size(), dims, stream.cuda_stream)
+    if st != _native.ATTN_OK:
+        raise AttnError(st)
+    return dq, dk, dv

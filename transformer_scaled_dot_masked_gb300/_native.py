@@ -47,6 +47,14 @@ lib.attn_fwd_ws.argtypes = lib.attn_fwd.argtypes + [_vp, ctypes.c_size_t]
 lib.attn_fwd_ws.restype = ctypes.c_int
 lib.attn_fwd_noalloc.argtypes = lib.attn_fwd.argtypes
 lib.attn_fwd_noalloc.restype = ctypes.c_int
+lib.attn_fwd_lse.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_float, _vp, _vp,
+                             ctypes.POINTER(AttnDims), _vp]
+lib.attn_fwd_lse.restype = ctypes.c_int
+lib.attn_bwd_workspace_size.argtypes = [ctypes.POINTER(AttnDims)]
+lib.attn_bwd_workspace_size.restype = ctypes.c_size_t
+lib.attn_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_float, _vp, _vp, _vp,
+                         _vp, ctypes.c_size_t, ctypes.POINTER(AttnDims), _vp]
+lib.attn_bwd.restype = ctypes.c_int
 lib.attn_select_kernel.argtypes = [ctypes.POINTER(AttnDims), ctypes.c_int]
 lib.attn_select_kernel.restype = ctypes.c_int
 lib.attn_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32)]
@@ -105,6 +113,25 @@ def fwd_noalloc_raw(q_ptr, k_ptr, v_ptr, lens_ptr, mask_kind, scale, out_ptr, di
     """attn_fwd_noalloc with integer device pointers; returns the status code."""
     return lib.attn_fwd_noalloc(q_ptr, k_ptr, v_ptr, lens_ptr, int(mask_kind), float(scale), out_ptr,
                                 ctypes.byref(dims), stream_ptr)
+
+
+def fwd_lse_raw(q_ptr, k_ptr, v_ptr, lens_ptr, mask_kind, scale, out_ptr, lse_ptr, dims: AttnDims,
+                stream_ptr) -> int:
+    """attn_fwd_lse with integer device pointers; returns the status code."""
+    return lib.attn_fwd_lse(q_ptr, k_ptr, v_ptr, lens_ptr, int(mask_kind), float(scale), out_ptr, lse_ptr,
+                            ctypes.byref(dims), stream_ptr)
+
+
+def bwd_workspace_size(dims: AttnDims) -> int:
+    return int(lib.attn_bwd_workspace_size(ctypes.byref(dims)))
+
+
+def bwd_raw(q_ptr, k_ptr, v_ptr, out_ptr, dout_ptr, lse_ptr, lens_ptr, mask_kind, scale, dq_ptr, dk_ptr,
+            dv_ptr, ws_ptr, ws_bytes, dims: AttnDims, stream_ptr) -> int:
+    """attn_bwd with integer device pointers; returns the status code."""
+    return lib.attn_bwd(q_ptr, k_ptr, v_ptr, out_ptr, dout_ptr, lse_ptr, lens_ptr, int(mask_kind),
+                        float(scale), dq_ptr, dk_ptr, dv_ptr, ws_ptr, int(ws_bytes), ctypes.byref(dims),
+                        stream_ptr)
 
 
 def device_status(stream_ptr=None):

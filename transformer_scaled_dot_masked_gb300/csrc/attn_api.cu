@@ -67,7 +67,7 @@ attn_status validate(const void *Q, const void *K, const void *V, const int32_t 
 namespace {
 
 attn_status run(const void *Q, const void *K, const void *V, const int32_t *key_lengths, int mask_kind, float scale,
-                void *out, const attn_dims *dims, void *stream, int kernel, int *tile_counter)
+                void *out, const attn_dims *dims, void *stream, int kernel, int *tile_counter, float *lse = nullptr)
 {
     const attn_status st = validate(Q, K, V, key_lengths, mask_kind, scale, out, dims);
     if (st != ATTN_OK) return st;
@@ -79,6 +79,7 @@ attn_status run(const void *Q, const void *K, const void *V, const int32_t *key_
     p.v = V;
     p.key_lengths = (mask_kind & ATTN_MASK_KEY_PADDING) ? key_lengths : nullptr;
     p.out = out;
+    p.lse = lse;
     p.B = d.B;
     p.h = d.h;
     p.m = d.m;
@@ -190,6 +191,87 @@ attn_status attn_fwd(const void *Q, const void *K, const void *V, const int32_t 
     return attn_fwd_kernel(Q, K, V, key_lengths, mask_kind, scale, out, dims, stream, ATTN_KERNEL_AUTO);
 }
 
+attn_status attn_fwd_lse(const void *Q, const void *K, const void *V, const int32_t *key_lengths, int mask_kind,
+                         float scale, void *out, float *lse, const attn_dims *dims, void *stream)
+{
+    if (lse == nullptr) return ATTN_ERR_NULL;
+    const attn_status st = validate(Q, K, V, key_lengths, mask_kind, scale, out, dims);
+    if (st != ATTN_OK) return st;
+    if (!aligned(lse, 4)) return ATTN_ERR_ALIGN;
+    const attn_dims &d = *dims;
+    const uint64_t esz = d.dtype == ATTN_BF16 ? 2 : 4;
+    const uint64_t qbytes = static_cast<uint64_t>(d.B) * d.h * d.m * d.d_k * esz;
+    const uint64_t kbytes = static_cast<uint64_t>(d.B) * d.h * d.n * d.d_k * esz;
+    const uint64_t lbytes = static_cast<uint64_t>(d.B) * d.h * d.m * 4;
+    if (overlaps(lse, lbytes, out, qbytes) || overlaps(lse, lbytes, Q, qbytes) || overlaps(lse, lbytes, K, kbytes) ||
+        overlaps(lse, lbytes, V, kbytes))
+        return ATTN_ERR_ALIAS;
+    if ((mask_kind & ATTN_MASK_KEY_PADDING) && overlaps(lse, lbytes, key_lengths, 4ull * d.B))
+        return ATTN_ERR_ALIAS;
+    return run(Q, K, V, key_lengths, mask_kind, scale, out, dims, stream, ATTN_KERNEL_AUTO, nullptr, lse);
+}
+
+size_t attn_bwd_workspace_size(const attn_dims *dims)
+{
+    if (validate_dims(dims, 0, 1.0f) != ATTN_OK || dims->dtype != ATTN_BF16 || dims->d_k != 64) return 0;
+    return attn::bwd_workspace_bytes(dims->B, dims->h, dims->m);
+}
+
+attn_status attn_bwd(const void *Q, const void *K, const void *V, const void *out, const void *dout, const float *lse,
+                     const int32_t *key_lengths, int mask_kind, float scale, void *dQ, void *dK, void *dV,
+                     void *workspace, size_t workspace_bytes, const attn_dims *dims, void *stream)
+{
+    if (out == nullptr || dout == nullptr || lse == nullptr || dQ == nullptr || dK == nullptr || dV == nullptr ||
+        workspace == nullptr)
+        return ATTN_ERR_NULL;
+    // Q, K, V, key_lengths, mask, scale and dims as for the forward; dQ stands in for out
+    const attn_status st = validate(Q, K, V, key_lengths, mask_kind, scale, dQ, dims);
+    if (st != ATTN_OK) return st;
+    const attn_dims &d = *dims;
+    if (d.dtype != ATTN_BF16 || d.d_k != 64) return ATTN_ERR_DTYPE;
+    if (!aligned(out, 16) || !aligned(dout, 16) || !aligned(dK, 16) || !aligned(dV, 16) || !aligned(lse, 4) ||
+        !aligned(workspace, 256))
+        return ATTN_ERR_ALIGN;
+    const size_t need = attn::bwd_workspace_bytes(d.B, d.h, d.m);
+    if (workspace_bytes < need) return ATTN_ERR_SHAPE;
+    const uint64_t qbytes = static_cast<uint64_t>(d.B) * d.h * d.m * d.d_k * 2;
+    const uint64_t kbytes = static_cast<uint64_t>(d.B) * d.h * d.n * d.d_k * 2;
+    const uint64_t lbytes = static_cast<uint64_t>(d.B) * d.h * d.m * 4;
+    struct Span {
+        const void *p;
+        uint64_t n;
+    };
+    const Span outs[4] = {{dQ, qbytes}, {dK, kbytes}, {dV, kbytes}, {workspace, need}};
+    const Span ins[7] = {{Q, qbytes},   {K, kbytes},   {V, kbytes}, {out, qbytes},
+                         {dout, qbytes}, {lse, lbytes},
+                         {(mask_kind & ATTN_MASK_KEY_PADDING) ? key_lengths : nullptr, 4ull * d.B}};
+    for (int a = 0; a < 4; ++a) {
+        for (int b = a + 1; b < 4; ++b)
+            if (overlaps(outs[a].p, outs[a].n, outs[b].p, outs[b].n)) return ATTN_ERR_ALIAS;
+        for (int b = 0; b < 7; ++b)
+            if (overlaps(outs[a].p, outs[a].n, ins[b].p, ins[b].n)) return ATTN_ERR_ALIAS;
+    }
+    attn::BwdProblem p;
+    p.q = Q;
+    p.k = K;
+    p.v = V;
+    p.out = out;
+    p.dout = dout;
+    p.lse = lse;
+    p.key_lengths = (mask_kind & ATTN_MASK_KEY_PADDING) ? key_lengths : nullptr;
+    p.dq = dQ;
+    p.dk = dK;
+    p.dv = dV;
+    p.workspace = workspace;
+    p.B = d.B;
+    p.h = d.h;
+    p.m = d.m;
+    p.n = d.n;
+    p.mask_kind = mask_kind;
+    p.scale = scale;
+    return attn::launch_bwd(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 int attn_select_kernel(const attn_dims *dims, int mask_kind)
 {
     if (validate_dims(dims, mask_kind, 1.0f) != ATTN_OK) return ATTN_KERNEL_AUTO;
@@ -198,9 +280,15 @@ int attn_select_kernel(const attn_dims *dims, int mask_kind)
 
 attn_status attn_device_status(void *stream, int32_t *info)
 {
-    uint32_t code = 0, where = 0;
+    uint32_t code = 0, where = 0, bcode = 0, bwhere = 0;
     if (attn::flash_status_read_and_clear(static_cast<cudaStream_t>(stream), &code, &where) != cudaSuccess)
         return ATTN_ERR_CUDA;
+    if (attn::bwd_status_read_and_clear(static_cast<cudaStream_t>(stream), &bcode, &bwhere) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    if (code == 0 && bcode != 0) {
+        code = bcode;
+        where = 100 + bwhere; // backward wait sites are reported as 100 + site
+    }
     if (info != nullptr) *info = static_cast<int32_t>(where);
     return code != 0 ? ATTN_ERR_DEVICE_TIMEOUT : ATTN_OK;
 }
@@ -224,6 +312,6 @@ const char *attn_status_string(int status)
     }
 }
 
-int32_t attn_version(void) { return (1 << 16) | 0; }
+int32_t attn_version(void) { return (1 << 16) | 1; }
 
 } // extern "C"

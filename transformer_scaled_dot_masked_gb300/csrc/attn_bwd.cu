@@ -1,0 +1,610 @@
+// Backward of the fused masked scaled dot-product attention for sm_103a:
+// TMA + tcgen05 + TMEM.
+//
+// For each (batch, head), with S = scale * Q K^T + M, P = softmax(S) row-wise,
+// O = P V and an upstream gradient dO (the chain rule of the attention equation,
+// "Paper Deep Reading: Attention Is All You Need", §04 attention equation; the
+// model is trained, slide deck "Training Details"):
+//
+//   dV = P^T dO,  dP = dO V^T,  D_i = sum_c dO_ic O_ic (= sum_j P_ij dP_ij),
+//   dS = P o (dP - D),  dQ = scale dS K,  dK = scale dS^T Q.
+//
+// P is recomputed from Q, K and the forward's per-row log-sum-exp, never stored.
+//
+// Three launches:
+//   attn_bwd_pre_kernel   D_i and (lse_i * log2 e, D_i) per query row, padded to
+//                         whole 128-row tiles (padding rows: (+inf, 0) so their
+//                         weights are 0); zeroes the fp32 dQ accumulator.
+//   attn_bwd_kernel       one CTA per (key tile j of 128 keys, head): K_j, V_j stay
+//                         in shared memory; dV_j and dK_j accumulate in TMEM over
+//                         the query tiles i that can see key tile j (i >= j with a
+//                         causal mask); each step adds its dQ_i part to the fp32
+//                         accumulator with vector reductions.
+//   attn_bwd_post_kernel  dQ = bf16(scale * accumulator).
+//
+// Per step (query tile i) of attn_bwd_kernel, keys as the MMA rows (two groups of
+// four compute warps; thread t of each group owns key row t = TMEM lane t, group g
+// takes the step's queries 64g .. 64g+63):
+//   MMA:      S^T = K_j Q_i^T, dP^T = V_j dO_i^T     (4 + 4 x M128 N128 K16, K-major)
+//   compute:  P^T = exp2(S^T scale log2 e - L_i), dS^T = P^T o (dP^T - D_i), masked;
+//             P^T and dS^T overwrite S^T and dP^T in TMEM as bf16 pairs, and dS is
+//             also written to shared memory as a K-major [query][key] tile
+//   MMA:      dV_j += P^T dO_i, dK_j += dS^T Q_i       (A from TMEM, B MN-major)
+//             dQ_i  = dS K_j                           (A K-major, B MN-major)
+//   compute:  read dQ_i from TMEM (lane = query row), reduce into the accumulator
+// The epilogue writes dV_j and scale * dK_j as bf16.
+//
+// TMEM (512 columns): S^T/P^T [0,128), dP^T/dS^T [128,256), dV [256,320),
+// dK [320,384), dQ [384,448).
+//
+// Every mbarrier wait is bounded; a wait that runs out sets the CTA's abort flag
+// and this file's device status word, and every role leaves its loop.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace attn {
+
+__device__ unsigned int g_bwd_status_code;
+__device__ unsigned int g_bwd_status_info;
+
+namespace {
+
+constexpr int kBM = 128; // keys per CTA (TMEM lanes) and queries per step
+constexpr int kD = 64;
+constexpr int kStages = 2;
+constexpr int kThreads = 320; // warps 0-7 compute (two groups), warp 8 TMA producer, warp 9 MMA issuer
+constexpr int kComputeThreads = 256;
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTileBytes = kBM * kD * 2;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384;
+constexpr uint64_t kWaitLimitNs = 2000000000ull; // 2 s: far beyond any legitimate wait
+constexpr uint32_t kIdescNN = idesc_bf16_f32(kBM, kBM, 0, 0); // both operands K-major, N = 128
+constexpr uint32_t kIdescN64 = idesc_bf16_f32(kBM, kD, 0, 1); // B MN-major, N = 64
+
+enum BwdSite : uint32_t {
+    kSiteLoadQEmpty = 1, kSiteMmaKvFull, kSiteMmaQFull, kSiteMmaDqFull, kSiteMmaPReady, kSiteMmaDqFree,
+    kSiteCmpQFull, kSiteCmpSdpFull, kSiteCmpDqFull, kSiteCmpSLoaded
+};
+
+struct alignas(1024) BwdSmem {
+    uint8_t k[kTileBytes];
+    uint8_t v[kTileBytes];
+    uint8_t q[kStages][kTileBytes];
+    uint8_t dout[kStages][kTileBytes];
+    uint8_t ds[2][kTileBytes]; // dS [query][key] bf16, 128-byte swizzle: keys 0-63, keys 64-127
+    float2 ld[kStages][kBM];    // (lse * log2 e, D) of the step's query rows
+    uint64_t kv_full, q_full[kStages], q_empty[kStages];
+    uint64_t sdp_full, p_ready, dq_full, dq_free;
+    uint64_t s_loaded; // group 0 has read its S^T and dP^T columns out of TMEM
+    uint64_t drain; // abort path only: completion of every MMA this CTA issued
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+struct BwdParams {
+    const float2 *ld;        // [BH][m_pad] (lse * log2 e, D); padding rows (+inf, 0)
+    float *dq_acc;           // [BH][m][64] fp32, zeroed by the pre kernel
+    __nv_bfloat16 *dk, *dv;  // [BH][n][64]
+    const int32_t *key_lengths;
+    int BH, h, m, n, m_pad, mask_kind, q_tiles;
+    float scale_log2;        // scale * log2 e
+    float scale;
+};
+
+__device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, int *abort_flag, uint32_t site)
+{
+    const uint64_t start = global_timer_ns();
+    while (true) {
+        for (int k = 0; k < 64; ++k)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*reinterpret_cast<volatile int *>(abort_flag)) return false;
+        if (global_timer_ns() - start > kWaitLimitNs) {
+            *reinterpret_cast<volatile int *>(abort_flag) = 1;
+            atomicOr(&g_bwd_status_code, 1u);
+            atomicCAS(&g_bwd_status_info, 0u, site);
+            return false;
+        }
+    }
+}
+
+// Bounded wait for phase `parity` of `bar`.  false: gave up (or another role did).
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, int *abort_flag, uint32_t site)
+{
+    const uint32_t a = smem_addr(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    return wait_slow(a, parity, abort_flag, site);
+}
+
+// Wait, bounded and ignoring the abort flag, for copies already in flight to land.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity)
+{
+    const uint32_t a = smem_addr(bar);
+    const uint64_t start = global_timer_ns();
+    while (!mbar_try_wait(a, parity))
+        if (global_timer_ns() - start > kWaitLimitNs) return;
+}
+
+__device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
+
+// Keys of batch b allowed by padding (n without it).
+__device__ __forceinline__ int key_len(const BwdParams &p, int bh)
+{
+    int len = p.n;
+    if ((p.mask_kind & kMaskKeyPadding) && p.key_lengths != nullptr) {
+        len = __ldg(p.key_lengths + bh / p.h);
+        len = len < 0 ? 0 : (len > p.n ? p.n : len);
+    }
+    return len;
+}
+
+// ------------------------------------------------------------------ roles
+__device__ __forceinline__ void load_role(BwdSmem &sm, const BwdParams &p, const CUtensorMap *tm_q,
+                                          const CUtensorMap *tm_k, const CUtensorMap *tm_v,
+                                          const CUtensorMap *tm_do, int bh, int key0, int i_begin, int steps)
+{
+    int *ab = &sm.abort_flag;
+    tma_prefetch_map(tm_q);
+    tma_prefetch_map(tm_do);
+    mbar_arrive_expect_tx(&sm.kv_full, 2 * kTileBytes);
+    tma_load_3d(sm.k, tm_k, &sm.kv_full, 0, key0, bh);
+    tma_load_3d(sm.v, tm_v, &sm.kv_full, 0, key0, bh);
+    int issued = 0;
+    for (int t = 0; t < steps; ++t) {
+        const int s = t % kStages;
+        if (!wait_bar(&sm.q_empty[s], ((t / kStages) & 1) ^ 1, ab, kSiteLoadQEmpty)) break;
+        const int i0 = (i_begin + t) * kBM;
+        mbar_arrive_expect_tx(&sm.q_full[s], 2 * kTileBytes + kBM * sizeof(float2));
+        tma_load_3d(sm.q[s], tm_q, &sm.q_full[s], 0, i0, bh);
+        tma_load_3d(sm.dout[s], tm_do, &sm.q_full[s], 0, i0, bh);
+        bulk_load(sm.ld[s], p.ld + static_cast<size_t>(bh) * p.m_pad + i0, kBM * sizeof(float2), &sm.q_full[s]);
+        ++issued;
+    }
+    // copies still in flight must land before the CTA may exit
+    drain_wait(&sm.kv_full, 0);
+    for (int t = issued > kStages ? issued - kStages : 0; t < issued; ++t)
+        drain_wait(&sm.q_full[t % kStages], (t / kStages) & 1);
+}
+
+__device__ __forceinline__ void mma_role(BwdSmem &sm, uint32_t tmem, int steps)
+{
+    int *ab = &sm.abort_flag;
+    const uint32_t desc_hi = static_cast<uint32_t>(smem_desc_sw128(0, 0, 1024) >> 32);
+    // K-major operands (rows x 64 bf16 = one 128-byte swizzle atom wide)
+    const uint32_t k_km = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.k), 16, 1024));
+    const uint32_t v_km = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.v), 16, 1024));
+    const uint32_t q_km = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.q[0]), 16, 1024));
+    const uint32_t do_km = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.dout[0]), 16, 1024));
+    const uint32_t ds_km = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.ds[0]), 16, 1024));
+    // the same tiles as MN-major B operands (rows are the reduction dimension)
+    const uint32_t k_mn = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.k), kTileBytes, 1024));
+    const uint32_t q_mn = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.q[0]), kTileBytes, 1024));
+    const uint32_t do_mn = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.dout[0]), kTileBytes, 1024));
+    constexpr uint32_t kStageUnits = kTileBytes >> 4; // descriptor units per stage
+
+    bool ok = wait_bar(&sm.kv_full, 0, ab, kSiteMmaKvFull);
+    for (int t = 0; t < steps && ok; ++t) {
+        const int s = t % kStages;
+        const uint32_t su = static_cast<uint32_t>(s) * kStageUnits;
+        if (!(ok = wait_bar(&sm.q_full[s], (t / kStages) & 1, ab, kSiteMmaQFull))) break;
+        if (t > 0) {
+            // every MMA of the previous step has completed: P^T and dS^T were consumed
+            if (!(ok = wait_bar(&sm.dq_full, (t - 1) & 1, ab, kSiteMmaDqFull))) break;
+        }
+        tc_fence_after();
+        // S^T = K Q^T and dP^T = V dO^T: 16 of the 64 columns (32 bytes) per K step
+        const uint32_t ts = tmem + kColS, tdp = tmem + kColDP;
+        mma_ss_k<0, 0>(ts, k_km, q_km + su, desc_hi, kIdescNN, 0u);
+        mma_ss_k<2, 2>(ts, k_km, q_km + su, desc_hi, kIdescNN, 1u);
+        mma_ss_k<4, 4>(ts, k_km, q_km + su, desc_hi, kIdescNN, 1u);
+        mma_ss_k<6, 6>(ts, k_km, q_km + su, desc_hi, kIdescNN, 1u);
+        mma_ss_k<0, 0>(tdp, v_km, do_km + su, desc_hi, kIdescNN, 0u);
+        mma_ss_k<2, 2>(tdp, v_km, do_km + su, desc_hi, kIdescNN, 1u);
+        mma_ss_k<4, 4>(tdp, v_km, do_km + su, desc_hi, kIdescNN, 1u);
+        mma_ss_k<6, 6>(tdp, v_km, do_km + su, desc_hi, kIdescNN, 1u);
+        mma_commit(&sm.sdp_full);
+
+        if (!(ok = wait_bar(&sm.p_ready, t & 1, ab, kSiteMmaPReady))) break;
+        tc_fence_after();
+        // dV += P^T dO, dK += dS^T Q: queries 16kk.. are TMEM columns 8kk.. (bf16
+        // pairs) and MN-major B rows 16kk.. (2 KiB = 128 descriptor units)
+        const uint32_t acc = t > 0 ? 1u : 0u;
+        const uint32_t tdv = tmem + kColDV, tdk = tmem + kColDK;
+        const uint32_t tp = tmem + kColS, tds = tmem + kColDP;
+        const uint32_t dob = do_mn + su, qb = q_mn + su;
+        mma_ts_k<0, 0>(tdv, tp, dob, desc_hi, kIdescN64, acc);
+        mma_ts_k<8, 128>(tdv, tp, dob, desc_hi, kIdescN64, 1u);
+        mma_ts_k<16, 256>(tdv, tp, dob, desc_hi, kIdescN64, 1u);
+        mma_ts_k<24, 384>(tdv, tp, dob, desc_hi, kIdescN64, 1u);
+        mma_ts_k<32, 512>(tdv, tp, dob, desc_hi, kIdescN64, 1u);
+        mma_ts_k<40, 640>(tdv, tp, dob, desc_hi, kIdescN64, 1u);
+        mma_ts_k<48, 768>(tdv, tp, dob, desc_hi, kIdescN64, 1u);
+        mma_ts_k<56, 896>(tdv, tp, dob, desc_hi, kIdescN64, 1u);
+        mma_ts_k<0, 0>(tdk, tds, qb, desc_hi, kIdescN64, acc);
+        mma_ts_k<8, 128>(tdk, tds, qb, desc_hi, kIdescN64, 1u);
+        mma_ts_k<16, 256>(tdk, tds, qb, desc_hi, kIdescN64, 1u);
+        mma_ts_k<24, 384>(tdk, tds, qb, desc_hi, kIdescN64, 1u);
+        mma_ts_k<32, 512>(tdk, tds, qb, desc_hi, kIdescN64, 1u);
+        mma_ts_k<40, 640>(tdk, tds, qb, desc_hi, kIdescN64, 1u);
+        mma_ts_k<48, 768>(tdk, tds, qb, desc_hi, kIdescN64, 1u);
+        mma_ts_k<56, 896>(tdk, tds, qb, desc_hi, kIdescN64, 1u);
+        if (t > 0) {
+            // the compute warps have read the previous dQ out of TMEM
+            if (!(ok = wait_bar(&sm.dq_free, (t - 1) & 1, ab, kSiteMmaDqFree))) break;
+            tc_fence_after();
+        }
+        // dQ = dS K: keys 0-63 in the first dS atom (32 bytes per K step), keys
+        // 64-127 in the second (16 KiB on); K_j rows 16kk.. as MN-major B
+        const uint32_t tdq = tmem + kColDQ;
+        mma_ss_k<0, 0>(tdq, ds_km, k_mn, desc_hi, kIdescN64, 0u);
+        mma_ss_k<2, 128>(tdq, ds_km, k_mn, desc_hi, kIdescN64, 1u);
+        mma_ss_k<4, 256>(tdq, ds_km, k_mn, desc_hi, kIdescN64, 1u);
+        mma_ss_k<6, 384>(tdq, ds_km, k_mn, desc_hi, kIdescN64, 1u);
+        mma_ss_k<1024, 512>(tdq, ds_km, k_mn, desc_hi, kIdescN64, 1u);
+        mma_ss_k<1026, 640>(tdq, ds_km, k_mn, desc_hi, kIdescN64, 1u);
+        mma_ss_k<1028, 768>(tdq, ds_km, k_mn, desc_hi, kIdescN64, 1u);
+        mma_ss_k<1030, 896>(tdq, ds_km, k_mn, desc_hi, kIdescN64, 1u);
+        mma_commit(&sm.q_empty[s]);
+        mma_commit(&sm.dq_full);
+    }
+}
+
+// Two groups of four compute warps.  Thread t of group g: key row t of the CTA's
+// key tile for the score work on queries 64g .. 64g+63 of each step; query row t
+// and output columns 32g .. 32g+31 for the dQ readout; dV (g = 0) or dK (g = 1)
+// of key row t in the epilogue.
+__device__ __forceinline__ void compute_role(BwdSmem &sm, const BwdParams &p, uint32_t tmem, int bh, int key0,
+                                             int len, int i_begin, int steps)
+{
+    const int warp = threadIdx.x / 32;
+    const int g = warp / 4;              // query half of each step
+    const int t = threadIdx.x % 128;     // TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    const uint32_t t_s = tmem + lane_base + kColS, t_dp = tmem + lane_base + kColDP;
+    const uint32_t t_dq = tmem + lane_base + kColDQ + 32 * g;
+    const bool causal = (p.mask_kind & kMaskCausal) != 0;
+    const float sl2 = p.scale_log2;
+    const int k = key0 + t;         // this thread's key
+    const bool key_live = k < len;  // len <= n: keys past n (zero-filled rows) are never live
+    // dS[q][k] goes to row q of the atom holding key k: chunk (k % 64) / 8 of the
+    // row, swizzled with the row's low three bits
+    const uint32_t ds_col = smem_addr(sm.ds[t / 64]) + ((t % 64) % 8) * 2;
+    const uint32_t ds_chunk = (t % 64) / 8;
+    int *ab = &sm.abort_flag;
+    bool ok = true;
+
+    for (int st = 0; st < steps && ok; ++st) {
+        const int s = st % kStages;
+        const int i0 = (i_begin + st) * kBM;
+        ok = warp_all(wait_bar(&sm.q_full[s], (st / kStages) & 1, ab, kSiteCmpQFull));
+        if (ok) ok = warp_all(wait_bar(&sm.sdp_full, st & 1, ab, kSiteCmpSdpFull));
+        if (!ok) break;
+        tc_fence_after();
+        // Only the diagonal tile of a causal mask (i0 == key0: key t is allowed for
+        // query row qq iff t <= qq) and padded key rows need masking; elsewhere the
+        // whole warp takes the unmasked path.
+        const bool diag = causal && i0 == key0;
+        const bool plain = __all_sync(0xffffffffu, key_live) && !diag;
+        const float4 *ldv = reinterpret_cast<const float4 *>(sm.ld[s]);
+        // Both of this group's 32-query chunks come out of TMEM before any weight goes
+        // back in: P^T and dS^T of queries q sit at columns q / 2 (the layout the P V
+        // and dS^T Q products read), so group 1's columns 32..63 are group 0's second
+        // score chunk, which group 1 may overwrite only once group 0 has read it.
+        uint32_t sr[64], dr[64];
+        tmem_ld32(t_s + 64 * g, sr);
+        tmem_ld32(t_s + 64 * g + 32, sr + 32);
+        tmem_ld32(t_dp + 64 * g, dr);
+        tmem_ld32(t_dp + 64 * g + 32, dr + 32);
+        tmem_wait_ld();
+        reg_fence32(sr);
+        reg_fence32(sr + 32);
+        reg_fence32(dr);
+        reg_fence32(dr + 32);
+        if (g == 0) {
+            tc_fence_before();
+            mbar_arrive(&sm.s_loaded);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int c = 2 * g + h; // chunk of 32 queries
+            uint32_t pp[16], pd[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int qq = 32 * c + 2 * u;              // query rows qq, qq + 1 of the tile
+                const float4 ld = ldv[qq / 2];              // (L, D) of both rows
+                float e0 = ex2(fmaf(__uint_as_float(sr[32 * h + 2 * u]), sl2, -ld.x));
+                float e1 = ex2(fmaf(__uint_as_float(sr[32 * h + 2 * u + 1]), sl2, -ld.z));
+                if (!plain) {
+                    e0 = (key_live && !(diag && t > qq)) ? e0 : 0.f;
+                    e1 = (key_live && !(diag && t > qq + 1)) ? e1 : 0.f;
+                }
+                const float d0 = e0 * (__uint_as_float(dr[32 * h + 2 * u]) - ld.y);
+                const float d1 = e1 * (__uint_as_float(dr[32 * h + 2 * u + 1]) - ld.w);
+                pp[u] = pack_bf16x2(e0, e1);
+                pd[u] = pack_bf16x2(d0, d1);
+                // dS into shared memory, one bf16 per query row
+                st_shared_u16(ds_col + qq * 128 + ((ds_chunk ^ (qq & 7)) << 4), static_cast<uint16_t>(pd[u]));
+                st_shared_u16(ds_col + (qq + 1) * 128 + ((ds_chunk ^ ((qq + 1) & 7)) << 4),
+                              static_cast<uint16_t>(pd[u] >> 16));
+            }
+            if (g == 1 && h == 0) {
+                ok = warp_all(wait_bar(&sm.s_loaded, st & 1, ab, kSiteCmpSLoaded));
+                if (!ok) break;
+                tc_fence_after();
+            }
+            tmem_st16(t_s + 16 * c, pp);
+            tmem_st16(t_dp + 16 * c, pd);
+        }
+        if (!ok) break;
+        tmem_wait_st();
+        tc_fence_before();
+        fence_proxy_async_shared();
+        mbar_arrive(&sm.p_ready);
+
+        ok = warp_all(wait_bar(&sm.dq_full, st & 1, ab, kSiteCmpDqFull));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t qr[32];
+        tmem_ld32(t_dq, qr);
+        tmem_wait_ld();
+        reg_fence32(qr);
+        tc_fence_before();
+        mbar_arrive(&sm.dq_free);
+        const int q = i0 + t;
+        if (q < p.m) {
+            float4 *dst = reinterpret_cast<float4 *>(p.dq_acc + (static_cast<size_t>(bh) * p.m + q) * kD + 32 * g);
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4)
+                red_add_v4(dst + c4, __uint_as_float(qr[4 * c4]), __uint_as_float(qr[4 * c4 + 1]),
+                           __uint_as_float(qr[4 * c4 + 2]), __uint_as_float(qr[4 * c4 + 3]));
+        }
+    }
+    if (!ok) return;
+    // dV (group 0) or scale * dK (group 1) of this thread's key row: every MMA
+    // completed with the last dq_full
+    tc_fence_after();
+    uint32_t r[kD];
+    const uint32_t col = g ? kColDK : kColDV;
+    tmem_ld32(tmem + lane_base + col, r);
+    tmem_ld32(tmem + lane_base + col + 32, r + 32);
+    tmem_wait_ld();
+    reg_fence32(r);
+    reg_fence32(r + 32);
+    if (k < p.n) {
+        const float f = g ? p.scale : 1.f;
+        uint4 *dst = reinterpret_cast<uint4 *>((g ? p.dk : p.dv) + (static_cast<size_t>(bh) * p.n + k) * kD);
+#pragma unroll
+        for (int c = 0; c < kD / 8; ++c) {
+            uint4 a;
+            a.x = pack_bf16x2(__uint_as_float(r[8 * c + 0]) * f, __uint_as_float(r[8 * c + 1]) * f);
+            a.y = pack_bf16x2(__uint_as_float(r[8 * c + 2]) * f, __uint_as_float(r[8 * c + 3]) * f);
+            a.z = pack_bf16x2(__uint_as_float(r[8 * c + 4]) * f, __uint_as_float(r[8 * c + 5]) * f);
+            a.w = pack_bf16x2(__uint_as_float(r[8 * c + 6]) * f, __uint_as_float(r[8 * c + 7]) * f);
+            dst[c] = a;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                const BwdParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    BwdSmem &sm = *reinterpret_cast<BwdSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x / 32;
+    // key tile j ascending first: with a causal mask the low key tiles see the most queries
+    const int j = blockIdx.x / p.BH;
+    const int bh = blockIdx.x % p.BH;
+    const int key0 = j * kBM;
+    const int len = key_len(p, bh);
+    const bool causal = (p.mask_kind & kMaskCausal) != 0;
+    const int i_begin = causal ? j : 0; // causal: m == n, query tile i sees key tile j iff i >= j
+    const int steps = key0 < len ? p.q_tiles - i_begin : 0;
+
+    if (steps <= 0) {
+        // no query sees any key of this tile: its gradients are 0
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        for (int r = threadIdx.x; r < kBM * (kD / 8); r += blockDim.x) {
+            const int kk = key0 + r / (kD / 8);
+            if (kk >= p.n) continue;
+            const size_t off = (static_cast<size_t>(bh) * p.n + kk) * kD / 8 + r % (kD / 8);
+            reinterpret_cast<uint4 *>(p.dv)[off] = z;
+            reinterpret_cast<uint4 *>(p.dk)[off] = z;
+        }
+        return;
+    }
+
+    if (threadIdx.x == 0) {
+        mbar_init(&sm.kv_full, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&sm.q_full[s], 1);
+            mbar_init(&sm.q_empty[s], 1);
+        }
+        mbar_init(&sm.sdp_full, 1);
+        mbar_init(&sm.p_ready, kComputeThreads);
+        mbar_init(&sm.dq_full, 1);
+        mbar_init(&sm.dq_free, kComputeThreads);
+        mbar_init(&sm.s_loaded, kBM);
+        mbar_init(&sm.drain, 1);
+        sm.abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    __syncwarp();
+    if (warp == kMmaWarp) {
+        tmem_alloc(&sm.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+
+    if (warp < 8) {
+        compute_role(sm, p, tmem, bh, key0, len, i_begin, steps);
+    } else if (warp == kLoadWarp) {
+        if (threadIdx.x % 32 == 0) load_role(sm, p, &tm_q, &tm_k, &tm_v, &tm_do, bh, key0, i_begin, steps);
+        __syncwarp();
+    } else {
+        if (threadIdx.x % 32 == 0) {
+            mma_role(sm, tmem, steps);
+            if (*reinterpret_cast<volatile int *>(&sm.abort_flag)) {
+                // make sure no MMA is still writing TMEM when the CTA frees it
+                mma_commit(&sm.drain);
+                drain_wait(&sm.drain, 0);
+            }
+        }
+        __syncwarp();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// D_i = sum_c dO_ic O_ic and (lse_i log2 e, D_i) per query row, padded to whole
+// tiles; zeroes the dQ accumulator.  One thread per (head, padded row).
+__global__ void attn_bwd_pre_kernel(const __nv_bfloat16 *__restrict__ out, const __nv_bfloat16 *__restrict__ dout,
+                                    const float *__restrict__ lse, float2 *__restrict__ ld,
+                                    float *__restrict__ dq_acc, int BH, int m, int m_pad)
+{
+    const size_t r = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (r >= static_cast<size_t>(BH) * m_pad) return;
+    const int bh = static_cast<int>(r / m_pad), q = static_cast<int>(r % m_pad);
+    if (q >= m) {
+        ld[r] = make_float2(CUDART_INF_F, 0.f);
+        return;
+    }
+    const size_t row = static_cast<size_t>(bh) * m + q;
+    const uint4 *o = reinterpret_cast<const uint4 *>(out + row * kD);
+    const uint4 *g = reinterpret_cast<const uint4 *>(dout + row * kD);
+    float dsum = 0.f;
+#pragma unroll
+    for (int c = 0; c < kD / 8; ++c) {
+        const uint4 a = o[c], b = g[c];
+        const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            dsum = fmaf(__uint_as_float(av[u] << 16), __uint_as_float(bv[u] << 16), dsum);
+            dsum = fmaf(__uint_as_float(av[u] & 0xffff0000u), __uint_as_float(bv[u] & 0xffff0000u), dsum);
+        }
+    }
+    ld[r] = make_float2(lse[row] * 1.4426950408889634f, dsum);
+    float4 *acc = reinterpret_cast<float4 *>(dq_acc + row * kD);
+#pragma unroll
+    for (int c = 0; c < kD / 4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// dQ = bf16(scale * accumulator), eight elements per thread.
+__global__ void attn_bwd_post_kernel(const float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dq,
+                                     size_t count8, float scale)
+{
+    const size_t r = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (r >= count8) return;
+    const float4 a = reinterpret_cast<const float4 *>(dq_acc)[2 * r];
+    const float4 b = reinterpret_cast<const float4 *>(dq_acc)[2 * r + 1];
+    uint4 o;
+    o.x = pack_bf16x2(a.x * scale, a.y * scale);
+    o.y = pack_bf16x2(a.z * scale, a.w * scale);
+    o.z = pack_bf16x2(b.x * scale, b.y * scale);
+    o.w = pack_bf16x2(b.z * scale, b.w * scale);
+    reinterpret_cast<uint4 *>(dq)[r] = o;
+}
+
+constexpr size_t kSmemBytes = sizeof(BwdSmem) + 1024; // + alignment slack
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+} // namespace
+
+size_t bwd_workspace_bytes(int B, int h, int m)
+{
+    const size_t BH = static_cast<size_t>(B) * h;
+    const size_t m_pad = align_up(static_cast<size_t>(m), kBM);
+    return align_up(BH * m * kD * sizeof(float), 256) + BH * m_pad * sizeof(float2);
+}
+
+cudaError_t launch_bwd(const BwdProblem &pb, cudaStream_t stream)
+{
+    static bool configured[64] = {};
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!configured[dev]) {
+            if ((e = cudaFuncSetAttribute(attn_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>(kSmemBytes))) != cudaSuccess)
+                return e;
+            configured[dev] = true;
+        }
+    }
+    const int BH = pb.B * pb.h;
+    const int m_pad = static_cast<int>(align_up(static_cast<size_t>(pb.m), kBM));
+    float *dq_acc = static_cast<float *>(pb.workspace);
+    float2 *ld = reinterpret_cast<float2 *>(static_cast<uint8_t *>(pb.workspace) +
+                                            align_up(static_cast<size_t>(BH) * pb.m * kD * sizeof(float), 256));
+    CUtensorMap tq, tk, tv, tdo;
+    if (!encode_rows_map(&tq, pb.q, pb.m, BH) || !encode_rows_map(&tk, pb.k, pb.n, BH) ||
+        !encode_rows_map(&tv, pb.v, pb.n, BH) || !encode_rows_map(&tdo, pb.dout, pb.m, BH))
+        return cudaErrorInvalidValue;
+
+    const size_t pre_rows = static_cast<size_t>(BH) * m_pad;
+    attn_bwd_pre_kernel<<<static_cast<unsigned>((pre_rows + 255) / 256), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(pb.out), static_cast<const __nv_bfloat16 *>(pb.dout), pb.lse, ld,
+        dq_acc, BH, pb.m, m_pad);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+    BwdParams p;
+    p.ld = ld;
+    p.dq_acc = dq_acc;
+    p.dk = static_cast<__nv_bfloat16 *>(pb.dk);
+    p.dv = static_cast<__nv_bfloat16 *>(pb.dv);
+    p.key_lengths = (pb.mask_kind & kMaskKeyPadding) ? pb.key_lengths : nullptr;
+    p.BH = BH;
+    p.h = pb.h;
+    p.m = pb.m;
+    p.n = pb.n;
+    p.m_pad = m_pad;
+    p.mask_kind = pb.mask_kind;
+    p.q_tiles = m_pad / kBM;
+    p.scale_log2 = pb.scale * 1.4426950408889634f;
+    p.scale = pb.scale;
+    const int k_tiles = (pb.n + kBM - 1) / kBM;
+    attn_bwd_kernel<<<k_tiles * BH, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+    const size_t count8 = static_cast<size_t>(BH) * pb.m * kD / 8;
+    attn_bwd_post_kernel<<<static_cast<unsigned>((count8 + 255) / 256), 256, 0, stream>>>(
+        dq_acc, static_cast<__nv_bfloat16 *>(pb.dq), count8, pb.scale);
+    return cudaGetLastError();
+}
+
+cudaError_t bwd_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint32_t *info)
+{
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return e;
+    unsigned int c = 0, i = 0, zero = 0;
+    if ((e = cudaMemcpyFromSymbol(&c, g_bwd_status_code, sizeof c)) != cudaSuccess) return e;
+    if ((e = cudaMemcpyFromSymbol(&i, g_bwd_status_info, sizeof i)) != cudaSuccess) return e;
+    if ((e = cudaMemcpyToSymbol(g_bwd_status_code, &zero, sizeof zero)) != cudaSuccess) return e;
+    if ((e = cudaMemcpyToSymbol(g_bwd_status_info, &zero, sizeof zero)) != cudaSuccess) return e;
+    *code = c;
+    *info = i;
+    return cudaSuccess;
+}
+
+} // namespace attn

@@ -116,6 +116,7 @@ struct FlashParams {
     const __nv_bfloat16 *q, *k; // read only by the rare score recomputation
     const int32_t *key_lengths;
     __nv_bfloat16 *out;
+    float *lse; // per-row log-sum-exp of the scaled scores (natural log), or nullptr
     int BH, h, m, n, mask_kind;
     float scale_log2;
     int pair_mode;
@@ -567,6 +568,7 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
                 uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
                 for (int c = 0; c < kD / 8; ++c) reinterpret_cast<uint4 *>(orow)[c] = z;
+                if (p.lse != nullptr) p.lse[static_cast<size_t>(bh) * p.m + i] = -CUDART_INF_F;
             }
             continue;
         }
@@ -678,6 +680,9 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
         tc_fence_before();
         mbar_arrive(&sm.o_free[slot]);
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        if (p.lse != nullptr && i < p.m) // weights are exp2(x - m_run) / l_run: lse = (m_run + log2 l_run) ln 2
+            p.lse[static_cast<size_t>(bh) * p.m + i] =
+                l_run > 0.f ? (m_run + __log2f(l_run)) * 0.6931471805599453f : -CUDART_INF_F;
         // Output: each thread writes its row of O / l into this slot's staging tile in
         // the 128-byte-swizzled layout (16-byte chunk c of row r at chunk c ^ (r % 8):
         // conflict-free), then one thread stores the tile with TMA, which clips rows
@@ -794,37 +799,6 @@ attn_flash_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 }
 
 // ------------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 get_encoder()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
-// [BH][rows][64] bf16 viewed as a 3-D tensor; box = 128 rows x 64 columns of one (b, h).
-bool encode_map(CUtensorMap *map, const void *base, int rows, int BH)
-{
-    auto enc = get_encoder();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows),
-                          static_cast<cuuint64_t>(BH)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(rows) * kD * 2};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(kD), static_cast<cuuint32_t>(kBM), 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 struct DeviceInfo {
     int sms = 0;
     bool configured = false;
@@ -856,14 +830,15 @@ cudaError_t launch_flash(const Problem &pb, bool pair_mode, int *tile_counter, c
     const int sms = infos[dev].sms;
     const int BH = pb.B * pb.h;
     CUtensorMap tq, tk, tv, to;
-    if (!encode_map(&tq, pb.q, pb.m, BH) || !encode_map(&tk, pb.k, pb.n, BH) || !encode_map(&tv, pb.v, pb.n, BH) ||
-        !encode_map(&to, pb.out, pb.m, BH))
+    if (!encode_rows_map(&tq, pb.q, pb.m, BH) || !encode_rows_map(&tk, pb.k, pb.n, BH) ||
+        !encode_rows_map(&tv, pb.v, pb.n, BH) || !encode_rows_map(&to, pb.out, pb.m, BH))
         return cudaErrorInvalidValue;
     FlashParams p;
     p.q = static_cast<const __nv_bfloat16 *>(pb.q);
     p.k = static_cast<const __nv_bfloat16 *>(pb.k);
     p.key_lengths = (pb.mask_kind & kMaskKeyPadding) ? pb.key_lengths : nullptr;
     p.out = static_cast<__nv_bfloat16 *>(pb.out);
+    p.lse = pb.lse;
     p.BH = BH;
     p.h = pb.h;
     p.m = pb.m;

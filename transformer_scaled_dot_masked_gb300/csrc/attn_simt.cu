@@ -36,8 +36,8 @@ __device__ __forceinline__ void from_f32(float x, __nv_bfloat16 *dst) { *dst = _
 template <typename T>
 __global__ void __launch_bounds__(kWarps * 32)
 attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ K, const T *__restrict__ V,
-                 const int32_t *__restrict__ key_lengths, T *__restrict__ out, int h, int m, int n, int d,
-                 int mask_kind, float scale_log2)
+                 const int32_t *__restrict__ key_lengths, T *__restrict__ out, float *__restrict__ lse, int h,
+                 int m, int n, int d, int mask_kind, float scale_log2)
 {
     __shared__ float sq[kRows][kStride];
     __shared__ float sk[kKeys][kStride];
@@ -120,6 +120,15 @@ attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ K, const T *__re
         }
     }
 
+    // lane rr of the warp writes row rr's log-sum-exp (weights are exp2(x - run_max) / run_sum)
+    if (lse != nullptr && lane < kRowsPerWarp) {
+        float mx = run_max[0], sm = run_sum[0];
+#pragma unroll
+        for (int rr = 1; rr < kRowsPerWarp; ++rr)
+            if (lane == rr) mx = run_max[rr], sm = run_sum[rr];
+        const int i = q0 + warp * kRowsPerWarp + lane;
+        if (i < m) lse[static_cast<size_t>(bh) * m + i] = sm > 0.f ? (mx + __log2f(sm)) * 0.6931471805599453f : -CUDART_INF_F;
+    }
 #pragma unroll
     for (int rr = 0; rr < kRowsPerWarp; ++rr) {
         const int i = q0 + warp * kRowsPerWarp + rr;
@@ -141,12 +150,12 @@ cudaError_t launch_simt(const Problem &p, cudaStream_t stream)
     if (p.bf16) {
         attn_simt_kernel<__nv_bfloat16><<<grid, kWarps * 32, 0, stream>>>(
             static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.k),
-            static_cast<const __nv_bfloat16 *>(p.v), p.key_lengths, static_cast<__nv_bfloat16 *>(p.out), p.h,
+            static_cast<const __nv_bfloat16 *>(p.v), p.key_lengths, static_cast<__nv_bfloat16 *>(p.out), p.lse, p.h,
             p.m, p.n, p.d, p.mask_kind, scale_log2);
     } else {
         attn_simt_kernel<float><<<grid, kWarps * 32, 0, stream>>>(
             static_cast<const float *>(p.q), static_cast<const float *>(p.k), static_cast<const float *>(p.v),
-            p.key_lengths, static_cast<float *>(p.out), p.h, p.m, p.n, p.d, p.mask_kind, scale_log2);
+            p.key_lengths, static_cast<float *>(p.out), p.lse, p.h, p.m, p.n, p.d, p.mask_kind, scale_log2);
     }
     return cudaGetLastError();
 }

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace attn {
@@ -13,6 +14,7 @@ struct Problem {
     const void *v;
     const int32_t *key_lengths; // device [B]; nullptr unless key padding
     void *out;
+    float *lse;                 // device [B][h][m] natural log of each row's softmax normaliser, or nullptr
     int B, h, m, n, d;
     int mask_kind;  // bit 0 key padding, bit 1 causal
     float scale;    // >= 0
@@ -33,6 +35,28 @@ cudaError_t launch_flash(const Problem &p, bool pair_mode, int *tile_counter, cu
 
 // Bytes of workspace the dynamic tile schedule needs.
 constexpr size_t kWorkspaceBytes = 256;
+
+// [BH][rows][64] bf16 viewed as a 3-D tensor (64, rows, BH) for TMA; box = 128
+// rows x 64 columns of one (b, h), 128-byte swizzle, rows past `rows` read as 0.
+bool encode_rows_map(CUtensorMap *map, const void *base, int rows, int BH);
+
+// Backward: dQ, dK, dV (bf16, d == 64) from Q, K, V, the forward's output and
+// per-row log-sum-exp, and the output gradient.
+struct BwdProblem {
+    const void *q, *k, *v, *out, *dout; // bf16 [B][h][rows][64]
+    const float *lse;                   // [B][h][m], natural log
+    const int32_t *key_lengths;         // device [B]; nullptr unless key padding
+    void *dq, *dk, *dv;                 // bf16, shaped like q, k, v
+    void *workspace;                    // bwd_workspace_bytes(B, h, m), 256-byte aligned
+    int B, h, m, n;
+    int mask_kind;
+    float scale;
+};
+
+// Workspace of the backward: the fp32 dQ accumulator and the per-row table.
+size_t bwd_workspace_bytes(int B, int h, int m);
+cudaError_t launch_bwd(const BwdProblem &p, cudaStream_t stream);
+cudaError_t bwd_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint32_t *info);
 
 // Device status word of the flash kernel (bounded waits that gave up).
 cudaError_t flash_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint32_t *info);

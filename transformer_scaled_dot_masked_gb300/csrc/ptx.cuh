@@ -91,6 +91,16 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// Contiguous copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// from global to shared memory, completion signalled as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
 // 3-D tiled store of one box from shared memory (bulk-group completion).  Rows
 // outside the tensor are not written.  The shared source must have been made
 // visible to the async proxy (fence_proxy_async_shared) by every thread that
@@ -115,6 +125,17 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 __device__ __forceinline__ void fence_proxy_async_shared()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v)
+{
+    asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+// Four-lane fp32 reduction into global memory (result unused).
+__device__ __forceinline__ void red_add_v4(float4 *dst, float a, float b, float c, float d)
+{
+    atomicAdd(dst, make_float4(a, b, c, d));
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v)

@@ -136,6 +136,14 @@ def draw(w: Workload, seed: Optional[int] = None) -> Inputs:
     return Inputs(w, q, k, v, lens)
 
 
+def draw_dout(w: Workload, seed: Optional[int] = None) -> np.ndarray:
+    """An upstream gradient dO for workload ``w``: standard normal [B, h, m, d] from its
+    own generator (seed 2000 + the workload's seed unless given), rounded like the inputs."""
+    rng = np.random.default_rng(2000 + w.seed if seed is None else seed)
+    g = rng.standard_normal(size=(w.B, w.h, w.m, w.d), dtype=np.float32)
+    return round_to_bf16_bits(g) if w.dtype == "bf16" else g
+
+
 def sample_rows(w: Workload, count: int, seed: int = 7) -> np.ndarray:
     """Linear output-row ids ``((b*h + head)*m + i)`` spread over a workload.
 
