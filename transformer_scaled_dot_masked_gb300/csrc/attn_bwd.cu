@@ -19,7 +19,7 @@
 //                         in shared memory; dV_j and dK_j accumulate in TMEM over
 //                         the query tiles i that can see key tile j (i >= j with a
 //                         causal mask); each step adds its dQ_i part to the fp32
-//                         accumulator with vector reductions.
+//                         accumulator with TMA reductions from shared memory.
 //   attn_bwd_post_kernel  dQ = bf16(scale * accumulator).
 //
 // Per step (query tile i) of attn_bwd_kernel, keys as the MMA rows (two groups of
@@ -31,7 +31,8 @@
 //             also written to shared memory as a K-major [query][key] tile
 //   MMA:      dV_j += P^T dO_i, dK_j += dS^T Q_i       (A from TMEM, B MN-major)
 //             dQ_i  = dS K_j                           (A K-major, B MN-major)
-//   compute:  read dQ_i from TMEM (lane = query row), reduce into the accumulator
+//   compute:  read dQ_i from TMEM (lane = query row), stage it in shared memory
+//             and add it to the accumulator with one TMA reduction per group
 // The epilogue writes dV_j and scale * dK_j as bf16.
 //
 // TMEM (512 columns): S^T/P^T [0,128), dP^T/dS^T [128,256), dV [256,320),
@@ -72,7 +73,7 @@ constexpr uint32_t kIdescN64 = idesc_bf16_f32(kBM, kD, 0, 1); // B MN-major, N =
 
 enum BwdSite : uint32_t {
     kSiteLoadQEmpty = 1, kSiteMmaKvFull, kSiteMmaQFull, kSiteMmaDqFull, kSiteMmaPReady, kSiteMmaDqFree,
-    kSiteCmpQFull, kSiteCmpSdpFull, kSiteCmpDqFull, kSiteCmpSLoaded
+    kSiteCmpQFull, kSiteCmpSdpFull, kSiteCmpDqFull, kSiteCmpSLoaded, kSiteCmpDqsFree, kSiteCmpDqsFull
 };
 
 struct alignas(1024) BwdSmem {
@@ -81,10 +82,12 @@ struct alignas(1024) BwdSmem {
     uint8_t q[kStages][kTileBytes];
     uint8_t dout[kStages][kTileBytes];
     uint8_t ds[2][kTileBytes]; // dS [query][key] bf16, 128-byte swizzle: keys 0-63, keys 64-127
+    uint8_t dq_stage[2][kBM * 32 * 4]; // dQ part of each compute group: 128 rows x 32 fp32, 128-byte swizzle
     float2 ld[kStages][kBM];    // (lse * log2 e, D) of the step's query rows
     uint64_t kv_full, q_full[kStages], q_empty[kStages];
     uint64_t sdp_full, p_ready, dq_full, dq_free;
     uint64_t s_loaded; // group 0 has read its S^T and dP^T columns out of TMEM
+    uint64_t dqs_free[2], dqs_full[2]; // dq_stage[g] may be written / may be reduced into the accumulator
     uint64_t drain; // abort path only: completion of every MMA this CTA issued
     uint32_t tmem_base;
     int abort_flag;
@@ -261,8 +264,8 @@ __device__ __forceinline__ void mma_role(BwdSmem &sm, uint32_t tmem, int steps)
 // key tile for the score work on queries 64g .. 64g+63 of each step; query row t
 // and output columns 32g .. 32g+31 for the dQ readout; dV (g = 0) or dK (g = 1)
 // of key row t in the epilogue.
-__device__ __forceinline__ void compute_role(BwdSmem &sm, const BwdParams &p, uint32_t tmem, int bh, int key0,
-                                             int len, int i_begin, int steps)
+__device__ __forceinline__ void compute_role(BwdSmem &sm, const BwdParams &p, const CUtensorMap *tm_dq,
+                                             uint32_t tmem, int bh, int key0, int len, int i_begin, int steps)
 {
     const int warp = threadIdx.x / 32;
     const int g = warp / 4;              // query half of each step
@@ -278,6 +281,7 @@ __device__ __forceinline__ void compute_role(BwdSmem &sm, const BwdParams &p, ui
     // row, swizzled with the row's low three bits
     const uint32_t ds_col = smem_addr(sm.ds[t / 64]) + ((t % 64) % 8) * 2;
     const uint32_t ds_chunk = (t % 64) / 8;
+    const uint32_t dqs_row = smem_addr(sm.dq_stage[g]) + t * 128; // this thread's staging row
     int *ab = &sm.abort_flag;
     bool ok = true;
 
@@ -293,47 +297,50 @@ __device__ __forceinline__ void compute_role(BwdSmem &sm, const BwdParams &p, ui
         // whole warp takes the unmasked path.
         const bool diag = causal && i0 == key0;
         const bool plain = __all_sync(0xffffffffu, key_live) && !diag;
-        const float4 *ldv = reinterpret_cast<const float4 *>(sm.ld[s]);
-        // Both of this group's 32-query chunks come out of TMEM before any weight goes
-        // back in: P^T and dS^T of queries q sit at columns q / 2 (the layout the P V
-        // and dS^T Q products read), so group 1's columns 32..63 are group 0's second
-        // score chunk, which group 1 may overwrite only once group 0 has read it.
-        uint32_t sr[64], dr[64];
-        tmem_ld32(t_s + 64 * g, sr);
-        tmem_ld32(t_s + 64 * g + 32, sr + 32);
-        tmem_ld32(t_dp + 64 * g, dr);
-        tmem_ld32(t_dp + 64 * g + 32, dr + 32);
-        tmem_wait_ld();
-        reg_fence32(sr);
-        reg_fence32(sr + 32);
-        reg_fence32(dr);
-        reg_fence32(dr + 32);
-        if (g == 0) {
-            tc_fence_before();
-            mbar_arrive(&sm.s_loaded);
-        }
-#pragma unroll
+        const uint32_t ldv = smem_addr(sm.ld[s]); // float2 (L, D) per query row
+        // P^T and dS^T of queries q go back to columns q / 2 (the layout the P V and
+        // dS^T Q products read), over scores already read: group 0 writes into its own
+        // first chunk's columns, group 1 into group 0's second chunk, so group 1 stores
+        // only once group 0 has read that chunk (s_loaded).
+#pragma unroll 1
         for (int h = 0; h < 2; ++h) {
             const int c = 2 * g + h; // chunk of 32 queries
+            uint32_t sr[32], dr[32];
+            tmem_ld32(t_s + 32 * c, sr);
+            tmem_ld32(t_dp + 32 * c, dr);
+            tmem_wait_ld();
+            reg_fence32(sr);
+            reg_fence32(dr);
+            if (g == 0 && h == 1) {
+                tc_fence_before();
+                mbar_arrive(&sm.s_loaded);
+            }
             uint32_t pp[16], pd[16];
+            // (L, D) of rows qq, qq + 1 in one 16-byte load, issued two pairs ahead
+            float4 ldq[3];
+            ldq[0] = ld_shared_f4_ordered(ldv + (32 * c) * 8);
+            ldq[1] = ld_shared_f4_ordered(ldv + (32 * c + 2) * 8);
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
                 const int qq = 32 * c + 2 * u;              // query rows qq, qq + 1 of the tile
-                const float4 ld = ldv[qq / 2];              // (L, D) of both rows
-                float e0 = ex2(fmaf(__uint_as_float(sr[32 * h + 2 * u]), sl2, -ld.x));
-                float e1 = ex2(fmaf(__uint_as_float(sr[32 * h + 2 * u + 1]), sl2, -ld.z));
+                if (u + 2 < 16) ldq[(u + 2) % 3] = ld_shared_f4_ordered(ldv + (qq + 4) * 8);
+                const float4 ld = ldq[u % 3];
+                float e0 = ex2(fmaf(__uint_as_float(sr[2 * u]), sl2, -ld.x));
+                float e1 = ex2(fmaf(__uint_as_float(sr[2 * u + 1]), sl2, -ld.z));
                 if (!plain) {
                     e0 = (key_live && !(diag && t > qq)) ? e0 : 0.f;
                     e1 = (key_live && !(diag && t > qq + 1)) ? e1 : 0.f;
                 }
-                const float d0 = e0 * (__uint_as_float(dr[32 * h + 2 * u]) - ld.y);
-                const float d1 = e1 * (__uint_as_float(dr[32 * h + 2 * u + 1]) - ld.w);
+                const float d0 = e0 * (__uint_as_float(dr[2 * u]) - ld.y);
+                const float d1 = e1 * (__uint_as_float(dr[2 * u + 1]) - ld.w);
                 pp[u] = pack_bf16x2(e0, e1);
                 pd[u] = pack_bf16x2(d0, d1);
-                // dS into shared memory, one bf16 per query row
-                st_shared_u16(ds_col + qq * 128 + ((ds_chunk ^ (qq & 7)) << 4), static_cast<uint16_t>(pd[u]));
-                st_shared_u16(ds_col + (qq + 1) * 128 + ((ds_chunk ^ ((qq + 1) & 7)) << 4),
-                              static_cast<uint16_t>(pd[u] >> 16));
+                // dS into shared memory, one bf16 per query row (ordered after the
+                // loads above but free of them otherwise; fence_proxy_async below
+                // publishes them to the MMA)
+                st_shared_u16_ordered(ds_col + qq * 128 + ((ds_chunk ^ (qq & 7)) << 4), static_cast<uint16_t>(pd[u]));
+                st_shared_u16_ordered(ds_col + (qq + 1) * 128 + ((ds_chunk ^ ((qq + 1) & 7)) << 4),
+                                      static_cast<uint16_t>(pd[u] >> 16));
             }
             if (g == 1 && h == 0) {
                 ok = warp_all(wait_bar(&sm.s_loaded, st & 1, ab, kSiteCmpSLoaded));
@@ -358,15 +365,33 @@ __device__ __forceinline__ void compute_role(BwdSmem &sm, const BwdParams &p, ui
         reg_fence32(qr);
         tc_fence_before();
         mbar_arrive(&sm.dq_free);
-        const int q = i0 + t;
-        if (q < p.m) {
-            float4 *dst = reinterpret_cast<float4 *>(p.dq_acc + (static_cast<size_t>(bh) * p.m + q) * kD + 32 * g);
-#pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4)
-                red_add_v4(dst + c4, __uint_as_float(qr[4 * c4]), __uint_as_float(qr[4 * c4 + 1]),
-                           __uint_as_float(qr[4 * c4 + 2]), __uint_as_float(qr[4 * c4 + 3]));
+        // dQ part into the accumulator: each group stages its 128 x 32 block (row t at
+        // t * 128 bytes, 16-byte chunk c at c ^ (t % 8): conflict-free) and one of
+        // its threads adds it with a TMA reduction, which skips rows past m.  The
+        // staging block is rewritten only after the previous reduction has read it.
+        if (t == 0) {
+            bulk_wait_read_all();
+            mbar_arrive(&sm.dqs_free[g]);
         }
+        ok = warp_all(wait_bar(&sm.dqs_free[g], st & 1, ab, kSiteCmpDqsFree));
+        if (!ok) break;
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4)
+            st_shared_v4(dqs_row + ((c4 ^ (t & 7)) << 4),
+                         make_uint4(qr[4 * c4], qr[4 * c4 + 1], qr[4 * c4 + 2], qr[4 * c4 + 3]));
+        fence_proxy_async_shared();
+        mbar_arrive(&sm.dqs_full[g]);
+        if (t == 0) {
+            ok = wait_bar(&sm.dqs_full[g], st & 1, ab, kSiteCmpDqsFull);
+            if (ok) {
+                tma_reduce_add_3d(tm_dq, sm.dq_stage[g], 32 * g, i0, bh);
+                bulk_commit_group();
+            }
+        }
+        ok = warp_all(ok);
     }
+    // the staging blocks must stay valid, and the sums land, before the CTA exits
+    if (t == 0) bulk_wait_all();
     if (!ok) return;
     // dV (group 0) or scale * dK (group 1) of this thread's key row: every MMA
     // completed with the last dq_full
@@ -396,7 +421,7 @@ __device__ __forceinline__ void compute_role(BwdSmem &sm, const BwdParams &p, ui
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                const BwdParams p)
+                const __grid_constant__ CUtensorMap tm_dq, const BwdParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     BwdSmem &sm = *reinterpret_cast<BwdSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -435,6 +460,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(&sm.dq_full, 1);
         mbar_init(&sm.dq_free, kComputeThreads);
         mbar_init(&sm.s_loaded, kBM);
+        for (int g = 0; g < 2; ++g) {
+            mbar_init(&sm.dqs_free[g], 1);
+            mbar_init(&sm.dqs_full[g], kBM);
+        }
         mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
         fence_mbarrier_init();
@@ -450,7 +479,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t tmem = sm.tmem_base;
 
     if (warp < 8) {
-        compute_role(sm, p, tmem, bh, key0, len, i_begin, steps);
+        compute_role(sm, p, &tm_dq, tmem, bh, key0, len, i_begin, steps);
     } else if (warp == kLoadWarp) {
         if (threadIdx.x % 32 == 0) load_role(sm, p, &tm_q, &tm_k, &tm_v, &tm_do, bh, key0, i_begin, steps);
         __syncwarp();
@@ -557,9 +586,10 @@ cudaError_t launch_bwd(const BwdProblem &pb, cudaStream_t stream)
     float *dq_acc = static_cast<float *>(pb.workspace);
     float2 *ld = reinterpret_cast<float2 *>(static_cast<uint8_t *>(pb.workspace) +
                                             align_up(static_cast<size_t>(BH) * pb.m * kD * sizeof(float), 256));
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdq;
     if (!encode_rows_map(&tq, pb.q, pb.m, BH) || !encode_rows_map(&tk, pb.k, pb.n, BH) ||
-        !encode_rows_map(&tv, pb.v, pb.n, BH) || !encode_rows_map(&tdo, pb.dout, pb.m, BH))
+        !encode_rows_map(&tv, pb.v, pb.n, BH) || !encode_rows_map(&tdo, pb.dout, pb.m, BH) ||
+        !encode_rows_map_f32(&tdq, dq_acc, pb.m, BH))
         return cudaErrorInvalidValue;
 
     const size_t pre_rows = static_cast<size_t>(BH) * m_pad;
@@ -584,7 +614,7 @@ cudaError_t launch_bwd(const BwdProblem &pb, cudaStream_t stream)
     p.scale_log2 = pb.scale * 1.4426950408889634f;
     p.scale = pb.scale;
     const int k_tiles = (pb.n + kBM - 1) / kBM;
-    attn_bwd_kernel<<<k_tiles * BH, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+    attn_bwd_kernel<<<k_tiles * BH, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     const size_t count8 = static_cast<size_t>(BH) * pb.m * kD / 8;

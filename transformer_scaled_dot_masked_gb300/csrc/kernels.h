@@ -40,6 +40,10 @@ constexpr size_t kWorkspaceBytes = 256;
 // rows x 64 columns of one (b, h), 128-byte swizzle, rows past `rows` read as 0.
 bool encode_rows_map(CUtensorMap *map, const void *base, int rows, int BH);
 
+// [BH][rows][64] fp32 as a 3-D tensor for TMA reductions; box = 128 rows x 32
+// columns (one 128-byte swizzle span), 128-byte swizzle.
+bool encode_rows_map_f32(CUtensorMap *map, void *base, int rows, int BH);
+
 // Backward: dQ, dK, dV (bf16, d == 64) from Q, K, V, the forward's output and
 // per-row log-sum-exp, and the output gradient.
 struct BwdProblem {

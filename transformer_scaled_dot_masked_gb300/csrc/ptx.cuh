@@ -113,6 +113,17 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void 
                  : "memory");
 }
 
+// 3-D tiled element-wise add of one box from shared memory into global memory
+// (bulk-group completion; the element type comes from the tensor map).  Rows
+// outside the tensor are not touched.  Same visibility rule as tma_store_3d.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap *map, const void *src, int x, int y, int z)
+{
+    asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_addr(src)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // this thread's committed bulk stores have finished reading shared memory
@@ -130,6 +141,22 @@ __device__ __forceinline__ void fence_proxy_async_shared()
 __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v)
 {
     asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+// Shared-memory load and store that stay in program order with each other but do
+// not order unrelated memory accesses (no memory clobber): for loops that
+// software-pipeline their own loads.  The caller orders them against other
+// accesses to the same bytes (mbarriers, fences).
+__device__ __forceinline__ float4 ld_shared_f4_ordered(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_u16_ordered(uint32_t addr, uint16_t v)
+{
+    asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v));
 }
 
 // Four-lane fp32 reduction into global memory (result unused).

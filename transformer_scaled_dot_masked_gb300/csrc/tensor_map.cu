@@ -46,4 +46,20 @@ bool encode_rows_map(CUtensorMap *map, const void *base, int rows, int BH)
     return r == CUDA_SUCCESS;
 }
 
+bool encode_rows_map_f32(CUtensorMap *map, void *base, int rows, int BH)
+{
+    auto enc = get_encoder();
+    if (!enc) return false;
+    constexpr int kD = 64, kBoxCols = 32, kBox = 128; // 32 fp32 = one 128-byte swizzle span
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 4, static_cast<cuuint64_t>(rows) * kD * 4};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(kBoxCols), static_cast<cuuint32_t>(kBox), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 } // namespace attn
