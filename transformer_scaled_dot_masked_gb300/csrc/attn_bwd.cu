@@ -22,9 +22,9 @@
 //                         accumulator with TMA reductions from shared memory.
 //   attn_bwd_post_kernel  dQ = bf16(scale * accumulator).
 //
-// Per step (query tile i) of attn_bwd_kernel, keys as the MMA rows (two groups of
+// Per step (query tile i) of attn_bwd_kernel, keys as the MMA rows (four groups of
 // four compute warps; thread t of each group owns key row t = TMEM lane t, group g
-// takes the step's queries 64g .. 64g+63):
+// takes the step's queries 32g .. 32g+31):
 //   MMA:      S^T = K_j Q_i^T, dP^T = V_j dO_i^T     (4 + 4 x M128 N128 K16, K-major)
 //   compute:  P^T = exp2(S^T scale log2 e - L_i), dS^T = P^T o (dP^T - D_i), masked;
 //             P^T and dS^T overwrite S^T and dP^T in TMEM as bf16 pairs, and dS is
@@ -60,10 +60,11 @@ namespace {
 constexpr int kBM = 128; // keys per CTA (TMEM lanes) and queries per step
 constexpr int kD = 64;
 constexpr int kStages = 2;
-constexpr int kThreads = 320; // warps 0-7 compute (two groups), warp 8 TMA producer, warp 9 MMA issuer
-constexpr int kComputeThreads = 256;
-constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kGroups = 4;                       // compute groups of four warps, 32 queries each per step
+constexpr int kComputeThreads = kGroups * 128;
+constexpr int kThreads = kComputeThreads + 64;   // + warp 16 TMA producer, warp 17 MMA issuer
+constexpr int kLoadWarp = kGroups * 4;
+constexpr int kMmaWarp = kLoadWarp + 1;
 constexpr uint32_t kTileBytes = kBM * kD * 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384;
@@ -82,11 +83,11 @@ struct alignas(1024) BwdSmem {
     uint8_t q[kStages][kTileBytes];
     uint8_t dout[kStages][kTileBytes];
     uint8_t ds[2][kTileBytes]; // dS [query][key] bf16, 128-byte swizzle: keys 0-63, keys 64-127
-    uint8_t dq_stage[2][kBM * 32 * 4]; // dQ part of each compute group: 128 rows x 32 fp32, 128-byte swizzle
+    uint8_t dq_stage[2][kBM * 32 * 4]; // dQ columns 0-31 / 32-63: 128 rows x 32 fp32, 128-byte swizzle
     float2 ld[kStages][kBM];    // (lse * log2 e, D) of the step's query rows
     uint64_t kv_full, q_full[kStages], q_empty[kStages];
     uint64_t sdp_full, p_ready, dq_full, dq_free;
-    uint64_t s_loaded; // group 0 has read its S^T and dP^T columns out of TMEM
+    uint64_t s_loaded; // every group has read its S^T and dP^T columns out of TMEM
     uint64_t dqs_free[2], dqs_full[2]; // dq_stage[g] may be written / may be reduced into the accumulator
     uint64_t drain; // abort path only: completion of every MMA this CTA issued
     uint32_t tmem_base;
@@ -260,19 +261,20 @@ __device__ __forceinline__ void mma_role(BwdSmem &sm, uint32_t tmem, int steps)
     }
 }
 
-// Two groups of four compute warps.  Thread t of group g: key row t of the CTA's
-// key tile for the score work on queries 64g .. 64g+63 of each step; query row t
-// and output columns 32g .. 32g+31 for the dQ readout; dV (g = 0) or dK (g = 1)
-// of key row t in the epilogue.
+// Four groups of four compute warps.  Thread t of group g: key row t of the CTA's
+// key tile for the score work on queries 32g .. 32g+31 of each step; query row t
+// and dQ columns 16g .. 16g+15 for the dQ readout; in the epilogue, columns
+// 32(g % 2) .. +31 of dV (g < 2) or dK (g >= 2) of key row t.
 __device__ __forceinline__ void compute_role(BwdSmem &sm, const BwdParams &p, const CUtensorMap *tm_dq,
                                              uint32_t tmem, int bh, int key0, int len, int i_begin, int steps)
 {
     const int warp = threadIdx.x / 32;
-    const int g = warp / 4;              // query half of each step
+    const int g = warp / 4;              // query chunk of each step
     const int t = threadIdx.x % 128;     // TMEM lane
+    const int half = g / 2;              // dQ staging block (columns 32 * half ..)
     const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
-    const uint32_t t_s = tmem + lane_base + kColS, t_dp = tmem + lane_base + kColDP;
-    const uint32_t t_dq = tmem + lane_base + kColDQ + 32 * g;
+    const uint32_t t_s = tmem + lane_base + kColS + 32 * g, t_dp = tmem + lane_base + kColDP + 32 * g;
+    const uint32_t t_dq = tmem + lane_base + kColDQ + 16 * g;
     const bool causal = (p.mask_kind & kMaskCausal) != 0;
     const float sl2 = p.scale_log2;
     const int k = key0 + t;         // this thread's key
@@ -281,7 +283,8 @@ __device__ __forceinline__ void compute_role(BwdSmem &sm, const BwdParams &p, co
     // row, swizzled with the row's low three bits
     const uint32_t ds_col = smem_addr(sm.ds[t / 64]) + ((t % 64) % 8) * 2;
     const uint32_t ds_chunk = (t % 64) / 8;
-    const uint32_t dqs_row = smem_addr(sm.dq_stage[g]) + t * 128; // this thread's staging row
+    const uint32_t dqs_row = smem_addr(sm.dq_stage[half]) + t * 128; // this thread's staging row
+    const bool dq_issuer = t == 0 && g % 2 == 0;
     int *ab = &sm.abort_flag;
     bool ok = true;
 
@@ -297,60 +300,58 @@ __device__ __forceinline__ void compute_role(BwdSmem &sm, const BwdParams &p, co
         // whole warp takes the unmasked path.
         const bool diag = causal && i0 == key0;
         const bool plain = __all_sync(0xffffffffu, key_live) && !diag;
-        const uint32_t ldv = smem_addr(sm.ld[s]); // float2 (L, D) per query row
+        const uint32_t ldv = smem_addr(sm.ld[s]) + 32 * g * 8; // float2 (L, D) per query row
         // P^T and dS^T of queries q go back to columns q / 2 (the layout the P V and
-        // dS^T Q products read), over scores already read: group 0 writes into its own
-        // first chunk's columns, group 1 into group 0's second chunk, so group 1 stores
-        // only once group 0 has read that chunk (s_loaded).
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-            const int c = 2 * g + h; // chunk of 32 queries
-            uint32_t sr[32], dr[32];
-            tmem_ld32(t_s + 32 * c, sr);
-            tmem_ld32(t_dp + 32 * c, dr);
+        // dS^T Q products read), over scores another group may not have read yet:
+        // every group reads all its columns (s_loaded) before any group writes.
+        // The chunk is read and processed in two halves of 16 queries.
+        uint32_t pp[16], pd[16];
+        // (L, D) of rows qq, qq + 1 in one 16-byte load, issued two pairs ahead
+        float4 ldq[3];
+        ldq[0] = ld_shared_f4_ordered(ldv);
+        ldq[1] = ld_shared_f4_ordered(ldv + 16);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            uint32_t sr[16], dr[16];
+            tmem_ld16(t_s + 16 * hh, sr);
+            tmem_ld16(t_dp + 16 * hh, dr);
             tmem_wait_ld();
-            reg_fence32(sr);
-            reg_fence32(dr);
-            if (g == 0 && h == 1) {
+            reg_fence16(sr);
+            reg_fence16(dr);
+            if (hh == 1) {
                 tc_fence_before();
                 mbar_arrive(&sm.s_loaded);
             }
-            uint32_t pp[16], pd[16];
-            // (L, D) of rows qq, qq + 1 in one 16-byte load, issued two pairs ahead
-            float4 ldq[3];
-            ldq[0] = ld_shared_f4_ordered(ldv + (32 * c) * 8);
-            ldq[1] = ld_shared_f4_ordered(ldv + (32 * c + 2) * 8);
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int qq = 32 * c + 2 * u;              // query rows qq, qq + 1 of the tile
-                if (u + 2 < 16) ldq[(u + 2) % 3] = ld_shared_f4_ordered(ldv + (qq + 4) * 8);
+            for (int v = 0; v < 8; ++v) {
+                const int u = 8 * hh + v;
+                const int qq = 32 * g + 2 * u;              // query rows qq, qq + 1 of the tile
+                if (u + 2 < 16) ldq[(u + 2) % 3] = ld_shared_f4_ordered(ldv + (2 * u + 4) * 8);
                 const float4 ld = ldq[u % 3];
-                float e0 = ex2(fmaf(__uint_as_float(sr[2 * u]), sl2, -ld.x));
-                float e1 = ex2(fmaf(__uint_as_float(sr[2 * u + 1]), sl2, -ld.z));
+                float e0 = ex2(fmaf(__uint_as_float(sr[2 * v]), sl2, -ld.x));
+                float e1 = ex2(fmaf(__uint_as_float(sr[2 * v + 1]), sl2, -ld.z));
                 if (!plain) {
                     e0 = (key_live && !(diag && t > qq)) ? e0 : 0.f;
                     e1 = (key_live && !(diag && t > qq + 1)) ? e1 : 0.f;
                 }
-                const float d0 = e0 * (__uint_as_float(dr[2 * u]) - ld.y);
-                const float d1 = e1 * (__uint_as_float(dr[2 * u + 1]) - ld.w);
+                const float d0 = e0 * (__uint_as_float(dr[2 * v]) - ld.y);
+                const float d1 = e1 * (__uint_as_float(dr[2 * v + 1]) - ld.w);
                 pp[u] = pack_bf16x2(e0, e1);
                 pd[u] = pack_bf16x2(d0, d1);
                 // dS into shared memory, one bf16 per query row (ordered after the
                 // loads above but free of them otherwise; fence_proxy_async below
-                // publishes them to the MMA)
-                st_shared_u16_ordered(ds_col + qq * 128 + ((ds_chunk ^ (qq & 7)) << 4), static_cast<uint16_t>(pd[u]));
+                // publishes them)
+                st_shared_u16_ordered(ds_col + qq * 128 + ((ds_chunk ^ (qq & 7)) << 4),
+                                      static_cast<uint16_t>(pd[u]));
                 st_shared_u16_ordered(ds_col + (qq + 1) * 128 + ((ds_chunk ^ ((qq + 1) & 7)) << 4),
                                       static_cast<uint16_t>(pd[u] >> 16));
             }
-            if (g == 1 && h == 0) {
-                ok = warp_all(wait_bar(&sm.s_loaded, st & 1, ab, kSiteCmpSLoaded));
-                if (!ok) break;
-                tc_fence_after();
-            }
-            tmem_st16(t_s + 16 * c, pp);
-            tmem_st16(t_dp + 16 * c, pd);
         }
+        ok = warp_all(wait_bar(&sm.s_loaded, st & 1, ab, kSiteCmpSLoaded));
         if (!ok) break;
+        tc_fence_after();
+        tmem_st16(tmem + lane_base + kColS + 16 * g, pp);
+        tmem_st16(tmem + lane_base + kColDP + 16 * g, pd);
         tmem_wait_st();
         tc_fence_before();
         fence_proxy_async_shared();
@@ -359,55 +360,55 @@ __device__ __forceinline__ void compute_role(BwdSmem &sm, const BwdParams &p, co
         ok = warp_all(wait_bar(&sm.dq_full, st & 1, ab, kSiteCmpDqFull));
         if (!ok) break;
         tc_fence_after();
-        uint32_t qr[32];
-        tmem_ld32(t_dq, qr);
+        uint32_t qr[16];
+        tmem_ld16(t_dq, qr);
         tmem_wait_ld();
-        reg_fence32(qr);
+        reg_fence16(qr);
         tc_fence_before();
         mbar_arrive(&sm.dq_free);
-        // dQ part into the accumulator: each group stages its 128 x 32 block (row t at
-        // t * 128 bytes, 16-byte chunk c at c ^ (t % 8): conflict-free) and one of
-        // its threads adds it with a TMA reduction, which skips rows past m.  The
-        // staging block is rewritten only after the previous reduction has read it.
-        if (t == 0) {
+        // dQ part into the accumulator: groups 2h and 2h+1 stage columns 32h .. 32h+31
+        // (row t at t * 128 bytes, 16-byte chunk c at c ^ (t % 8): conflict-free) and
+        // one thread adds the block with a TMA reduction, which skips rows past m.
+        // The block is rewritten only after the previous reduction has read it.
+        if (dq_issuer) {
             bulk_wait_read_all();
-            mbar_arrive(&sm.dqs_free[g]);
+            mbar_arrive(&sm.dqs_free[half]);
         }
-        ok = warp_all(wait_bar(&sm.dqs_free[g], st & 1, ab, kSiteCmpDqsFree));
+        ok = warp_all(wait_bar(&sm.dqs_free[half], st & 1, ab, kSiteCmpDqsFree));
         if (!ok) break;
 #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4)
+        for (int j = 0; j < 4; ++j) {
+            const int c4 = 4 * (g % 2) + j;
             st_shared_v4(dqs_row + ((c4 ^ (t & 7)) << 4),
-                         make_uint4(qr[4 * c4], qr[4 * c4 + 1], qr[4 * c4 + 2], qr[4 * c4 + 3]));
+                         make_uint4(qr[4 * j], qr[4 * j + 1], qr[4 * j + 2], qr[4 * j + 3]));
+        }
         fence_proxy_async_shared();
-        mbar_arrive(&sm.dqs_full[g]);
-        if (t == 0) {
-            ok = wait_bar(&sm.dqs_full[g], st & 1, ab, kSiteCmpDqsFull);
+        mbar_arrive(&sm.dqs_full[half]);
+        if (dq_issuer) {
+            ok = wait_bar(&sm.dqs_full[half], st & 1, ab, kSiteCmpDqsFull);
             if (ok) {
-                tma_reduce_add_3d(tm_dq, sm.dq_stage[g], 32 * g, i0, bh);
+                tma_reduce_add_3d(tm_dq, sm.dq_stage[half], 32 * half, i0, bh);
                 bulk_commit_group();
             }
         }
         ok = warp_all(ok);
     }
     // the staging blocks must stay valid, and the sums land, before the CTA exits
-    if (t == 0) bulk_wait_all();
+    if (dq_issuer) bulk_wait_all();
     if (!ok) return;
-    // dV (group 0) or scale * dK (group 1) of this thread's key row: every MMA
-    // completed with the last dq_full
+    // 32 columns of dV (groups 0, 1) or scale * dK (groups 2, 3) of this thread's
+    // key row: every MMA completed with the last dq_full
     tc_fence_after();
-    uint32_t r[kD];
-    const uint32_t col = g ? kColDK : kColDV;
-    tmem_ld32(tmem + lane_base + col, r);
-    tmem_ld32(tmem + lane_base + col + 32, r + 32);
+    uint32_t r[32];
+    tmem_ld32(tmem + lane_base + (g < 2 ? kColDV : kColDK) + 32 * (g % 2), r);
     tmem_wait_ld();
     reg_fence32(r);
-    reg_fence32(r + 32);
     if (k < p.n) {
-        const float f = g ? p.scale : 1.f;
-        uint4 *dst = reinterpret_cast<uint4 *>((g ? p.dk : p.dv) + (static_cast<size_t>(bh) * p.n + k) * kD);
+        const float f = g < 2 ? 1.f : p.scale;
+        uint4 *dst = reinterpret_cast<uint4 *>((g < 2 ? p.dv : p.dk) + (static_cast<size_t>(bh) * p.n + k) * kD +
+                                               32 * (g % 2));
 #pragma unroll
-        for (int c = 0; c < kD / 8; ++c) {
+        for (int c = 0; c < 4; ++c) {
             uint4 a;
             a.x = pack_bf16x2(__uint_as_float(r[8 * c + 0]) * f, __uint_as_float(r[8 * c + 1]) * f);
             a.y = pack_bf16x2(__uint_as_float(r[8 * c + 2]) * f, __uint_as_float(r[8 * c + 3]) * f);
@@ -459,10 +460,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(&sm.p_ready, kComputeThreads);
         mbar_init(&sm.dq_full, 1);
         mbar_init(&sm.dq_free, kComputeThreads);
-        mbar_init(&sm.s_loaded, kBM);
+        mbar_init(&sm.s_loaded, kComputeThreads);
         for (int g = 0; g < 2; ++g) {
             mbar_init(&sm.dqs_free[g], 1);
-            mbar_init(&sm.dqs_full[g], kBM);
+            mbar_init(&sm.dqs_full[g], 2 * kBM);
         }
         mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
@@ -478,7 +479,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
 
-    if (warp < 8) {
+    if (warp < kGroups * 4) {
         compute_role(sm, p, &tm_dq, tmem, bh, key0, len, i_begin, steps);
     } else if (warp == kLoadWarp) {
         if (threadIdx.x % 32 == 0) load_role(sm, p, &tm_q, &tm_k, &tm_v, &tm_do, bh, key0, i_begin, steps);

@@ -285,6 +285,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r)
         : "r"(taddr));
 }
 
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r)
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : ATTN_R8(0), ATTN_R8(8)
+        : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r)
 {
     asm volatile(
@@ -320,6 +329,8 @@ __device__ __forceinline__ void reg_fence32(uint32_t *r)
 {
     asm volatile("" : ATTN_U8(0), ATTN_U8(8), ATTN_U8(16), ATTN_U8(24)::"memory");
 }
+
+__device__ __forceinline__ void reg_fence16(uint32_t *r) { asm volatile("" : ATTN_U8(0), ATTN_U8(8)::"memory"); }
 
 #undef ATTN_R8
 #undef ATTN_W8
