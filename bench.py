@@ -34,7 +34,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from workloads import draw_dout, WORKLOADS, draw  # noqa: E402
+from workloads import DECODE, draw_dout, WORKLOADS, draw  # noqa: E402
 
 METRIC = "masked MHA fwd TFLOPS on 1 GB300 (and % of bf16 tensor peak / HBM GB/s)"
 UNIT = "TFLOPS"
@@ -284,6 +284,38 @@ def backward_workload(torch, attn, device, peak_tf, steps=20):
             "calls_timed": steps, "algorithmic": "10*d_k FLOPs per allowed (query, key) pair"}
 
 
+def decode_workload(torch, attn, device, peak_hbm, steps=50):
+    """One incremental-decoding step (workloads.DECODE: B64 h16, one new row each, K/V
+    caches of capacity 4096 holding 1024..4096 rows) through attn_decode, caches
+    resident (1.07 GB > L2, so no flush).  Algorithmic bytes: every live cached K and
+    V row once, plus Q and O."""
+    w = DECODE
+    inp = draw(w)
+    q, k, v = (to_device(x, w.dtype, torch, device) for x in (inp.q, inp.k, inp.v))
+    lens = torch.from_numpy(inp.key_lengths).to(device)
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream(device)
+    ws_bytes = attn.decode_workspace_size(w.B, w.h, w.m, w.n)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device)
+
+    def step():
+        attn.attn_decode(q, k, v, lens, w.scale, out=out, workspace=ws, stream=stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    ms = time_launches(step, steps, torch, stream)
+    st, info = attn.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} (info {info}) after the decode loop")
+    live = float(np.clip(inp.key_lengths, 0, w.n).sum()) * w.h
+    nbytes = live * w.d * 2 * 2 + 2 * w.B * w.h * w.m * w.d * 2 + 4 * w.B
+    return {"workload": w.description, "entry_point": "attn_decode (split-KV, CUDA cores)",
+            "us_per_call": ms * 1e3, "hbm_gbs_algorithmic": nbytes / (ms * 1e-3) / 1e9,
+            "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peak_hbm, "calls_timed": steps,
+            "algorithmic": "each live cached K and V row once, plus Q and O (bf16)"}
+
+
 def cpu_oracle_sample(w, inp, target_s, seed=3):
     """Time the fp64 oracle on random query rows of w for about target_s seconds."""
     import oracle
@@ -459,6 +491,7 @@ def main():
         result["gpu_launches"] = args.steps  # e2e launches are outside the device-timed region
         result["other_workloads"] = short_workloads(torch, attn, device, peak_hbm)
         result["backward"] = backward_workload(torch, attn, device, peak_tf)
+        result["decode"] = decode_workload(torch, attn, device, peak_hbm)
         if rank == 0:
             cb, _ = cpu_oracle_sample(w, inp, args.cpu_seconds)
             cb.pop("seconds", None)

@@ -255,6 +255,40 @@ attn_status attn_bwd(const void *Q, const void *K, const void *V, const void *ou
                      void *workspace, size_t workspace_bytes,
                      const attn_dims *dims, void *stream);
 
+/* Bytes of device workspace attn_decode needs for these dims on the current
+ * device (its SM count sets how the keys are split); 0 when no workspace is
+ * needed or when attn_decode would reject the dims. */
+size_t attn_decode_workspace_size(const attn_dims *dims);
+
+/*
+ * Incremental decoding: m (1..8) new query rows per (batch, head) against a
+ * cache of keys and values, as when a decoder produces one position at a time
+ * and attends to the positions produced so far ("Paper Deep Reading", §03
+ * "Decoder layer").  Query i of batch b sees cached keys 0 .. cache_lengths[b]-1:
+ * exactly attn_fwd with ATTN_MASK_KEY_PADDING and key_lengths = cache_lengths
+ * (a row with no cached key is 0).
+ *
+ *   Q              device bf16 [B][h][m][64], 1 <= m <= 8
+ *   K, V           device bf16 [B][h][n][64]: the caches, n = their capacity
+ *   cache_lengths  device int32 [B], clamped to [0, n]; NULL: every row holds n keys
+ *   scale          as for attn_fwd
+ *   out            device bf16 [B][h][m][64]
+ *   lse            NULL, or device float [B][h][m]: each row's log-sum-exp (natural log)
+ *   workspace      attn_decode_workspace_size(dims) bytes, 16-byte aligned, any
+ *                  contents (may be NULL when that size is 0); calls that may run
+ *                  at the same time on the GPU need different workspaces
+ *
+ * The keys of each (batch, head) are split over several CTAs on the CUDA cores
+ * (the work is memory-bound: each cached row is read once per call), then one
+ * pass merges the splits.  Errors as attn_fwd, plus: dtype other than bf16 or
+ * d_k != 64 (ATTN_ERR_DTYPE), m > 8 (ATTN_ERR_SHAPE), workspace NULL or too small
+ * when one is needed (ATTN_ERR_NULL / ATTN_ERR_SHAPE), lse or the workspace
+ * unaligned (ATTN_ERR_ALIGN) or overlapping a tensor (ATTN_ERR_ALIAS).
+ */
+attn_status attn_decode(const void *Q, const void *K, const void *V, const int32_t *cache_lengths,
+                        float scale, void *out, float *lse, const attn_dims *dims,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
 /* The kernel attn_fwd would run for these dims and mask (host only, no CUDA call);
  * ATTN_KERNEL_AUTO (0) if the call would be rejected. */
 int attn_select_kernel(const attn_dims *dims, int mask_kind);

@@ -153,3 +153,25 @@ def _call_bwd(dims=(2, 2, 8, 8, 64, 0), mask=0, lens=None, ws_bytes=None, **kw):
 ])
 def test_bwd_rejects_bad_arguments(kwargs, status):
     assert _call_bwd(**kwargs) == status
+
+
+def _call_dec(dims=(2, 2, 1, 64, 64, 0), lens=L, lse=None, ws=None, ws_bytes=0, **kw):
+    d = N.make_dims(*dims)
+    return N.decode_raw(kw.get("q", A), kw.get("k", B_), kw.get("v", C), lens, kw.get("scale", 0.125),
+                        kw.get("out", O), lse, d, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(q=None), 1), (dict(out=None), 1),
+    (dict(dims=(2, 2, 1, 64, 64, 1)), 3), (dict(dims=(2, 2, 1, 64, 32, 0)), 3),
+    (dict(dims=(2, 2, 9, 64, 64, 0)), 2), (dict(dims=(2, 2, 0, 64, 64, 0)), 2),
+    (dict(q=A + 8), 5), (dict(lens=L + 2), 5), (dict(lse=LSE + 2), 5),
+    (dict(scale=float("nan")), 9), (dict(out=B_ + 64), 10), (dict(lse=O + 16), 10),
+])
+def test_decode_rejects_bad_arguments(kwargs, status):
+    assert _call_dec(**kwargs) == status
+
+
+def test_decode_workspace_size_rejects_bad_dims():
+    assert N.decode_workspace_size(N.make_dims(2, 2, 9, 64, 64, 0)) == 0
+    assert N.decode_workspace_size(N.make_dims(2, 2, 1, 64, 64, 1)) == 0

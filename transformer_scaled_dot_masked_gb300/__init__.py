@@ -3,6 +3,7 @@
     out = attn_fwd(q, k, v, key_lengths, mask_kind, scale)
     out, lse = attn_fwd_lse(q, k, v, key_lengths, mask_kind, scale)
     dq, dk, dv = attn_bwd(q, k, v, out, dout, lse, key_lengths, mask_kind, scale)
+    out = attn_decode(q_new, k_cache, v_cache, cache_lengths, scale)
 
 computes softmax(scale * Q K^T + M) V for every (batch, head) on the GPU, and
 its gradients (the chain rule of that equation),
@@ -18,7 +19,7 @@ from . import _native
 from ._native import (AttnError, KERNEL_AUTO, KERNEL_FLASH, KERNEL_SHORT, KERNEL_SIMT, MASK_CAUSAL,
                       MASK_KEY_PADDING, MASK_NONE, DTYPE_BF16, DTYPE_FP32)
 
-__all__ = ["attn_fwd", "attn_fwd_lse", "attn_bwd", "bwd_workspace_size", "AttnError", "select_kernel", "device_status", "make_workspace", "workspace_size", "MASK_NONE", "MASK_KEY_PADDING",
+__all__ = ["attn_fwd", "attn_fwd_lse", "attn_bwd", "bwd_workspace_size", "attn_decode", "decode_workspace_size", "AttnError", "select_kernel", "device_status", "make_workspace", "workspace_size", "MASK_NONE", "MASK_KEY_PADDING",
            "MASK_CAUSAL", "KERNEL_AUTO", "KERNEL_FLASH", "KERNEL_SHORT", "KERNEL_SIMT"]
 
 
@@ -197,3 +198,44 @@ def attn_bwd(q, k, v, out, dout, lse, key_lengths=None, mask_kind: int = MASK_NO
     if st != _native.ATTN_OK:
         raise AttnError(st)
     return dq, dk, dv
+
+
+def decode_workspace_size(B, h, m, n, d=64, dtype: int = DTYPE_BF16) -> int:
+    """Bytes of device workspace ``attn_decode`` needs on the current device (0: none)."""
+    return _native.decode_workspace_size(_native.make_dims(B, h, m, n, d, dtype))
+
+
+def attn_decode(q, k_cache, v_cache, cache_lengths=None, scale: Optional[float] = None, out=None, lse=None,
+                workspace=None, stream=None):
+    """m (1..8) new query rows per (batch, head) against cached keys/values (bf16, d_k = 64).
+
+    q: [B, h, m, 64]; k_cache, v_cache: [B, h, n, 64] (n = capacity); cache_lengths: int32 [B]
+    CUDA tensor of valid cached rows per batch entry (None: all n).  Same result as
+    ``attn_fwd`` with MASK_KEY_PADDING.  lse: optional float32 [B, h, m] output.
+    """
+    import torch
+    B, h, m, n, d = _check_qkv(q, k_cache, v_cache)
+    scale = d ** -0.5 if scale is None else scale
+    if out is None:
+        out = torch.empty_like(q)
+    _like(out, q, "out")
+    lens_ptr = None
+    if cache_lengths is not None:
+        lens_ptr = _lengths_ptr(cache_lengths, MASK_KEY_PADDING, B)
+    if lse is not None and (lse.shape != (B, h, m) or lse.dtype != torch.float32 or not lse.is_cuda
+                            or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous float32 CUDA tensor [B, h, m]")
+    dims = _native.make_dims(B, h, m, n, d, _dtype_code(q))
+    need = _native.decode_workspace_size(dims)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    stream = torch.cuda.current_stream(q.device) if stream is None else stream
+    st = _native.decode_raw(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), lens_ptr, scale, out.data_ptr(),
+                            None if lse is None else lse.data_ptr(), dims,
+                            None if workspace is None else workspace.data_ptr(),
+                            0 if workspace is None else workspace.numel() * workspace.element_size(),
+                            stream.cuda_stream)
+    if st != _native.ATTN_OK:
+        raise AttnError(st)
+    return out
+

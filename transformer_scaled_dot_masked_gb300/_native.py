@@ -55,6 +55,11 @@ lib.attn_bwd_workspace_size.restype = ctypes.c_size_t
 lib.attn_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_float, _vp, _vp, _vp,
                          _vp, ctypes.c_size_t, ctypes.POINTER(AttnDims), _vp]
 lib.attn_bwd.restype = ctypes.c_int
+lib.attn_decode_workspace_size.argtypes = [ctypes.POINTER(AttnDims)]
+lib.attn_decode_workspace_size.restype = ctypes.c_size_t
+lib.attn_decode.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, ctypes.POINTER(AttnDims), _vp,
+                            ctypes.c_size_t, _vp]
+lib.attn_decode.restype = ctypes.c_int
 lib.attn_select_kernel.argtypes = [ctypes.POINTER(AttnDims), ctypes.c_int]
 lib.attn_select_kernel.restype = ctypes.c_int
 lib.attn_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32)]
@@ -132,6 +137,17 @@ def bwd_raw(q_ptr, k_ptr, v_ptr, out_ptr, dout_ptr, lse_ptr, lens_ptr, mask_kind
     return lib.attn_bwd(q_ptr, k_ptr, v_ptr, out_ptr, dout_ptr, lse_ptr, lens_ptr, int(mask_kind),
                         float(scale), dq_ptr, dk_ptr, dv_ptr, ws_ptr, int(ws_bytes), ctypes.byref(dims),
                         stream_ptr)
+
+
+def decode_workspace_size(dims: AttnDims) -> int:
+    return int(lib.attn_decode_workspace_size(ctypes.byref(dims)))
+
+
+def decode_raw(q_ptr, k_ptr, v_ptr, lens_ptr, scale, out_ptr, lse_ptr, dims: AttnDims, ws_ptr, ws_bytes,
+               stream_ptr) -> int:
+    """attn_decode with integer device pointers; returns the status code."""
+    return lib.attn_decode(q_ptr, k_ptr, v_ptr, lens_ptr, float(scale), out_ptr, lse_ptr, ctypes.byref(dims),
+                           ws_ptr, int(ws_bytes), stream_ptr)
 
 
 def device_status(stream_ptr=None):

@@ -272,6 +272,86 @@ attn_status attn_bwd(const void *Q, const void *K, const void *V, const void *ou
     return attn::launch_bwd(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+namespace {
+// SM count of the current device (the decode kernel's split geometry); 0 on error.
+int current_sms()
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return sms;
+}
+
+attn_status validate_decode_dims(const attn_dims *dims)
+{
+    if (dims == nullptr) return ATTN_ERR_NULL;
+    const attn_status st = validate_dims(dims, ATTN_MASK_KEY_PADDING, 1.0f);
+    if (st != ATTN_OK) return st;
+    if (dims->dtype != ATTN_BF16 || dims->d_k != 64) return ATTN_ERR_DTYPE;
+    if (dims->m > 8) return ATTN_ERR_SHAPE;
+    return ATTN_OK;
+}
+} // namespace
+
+size_t attn_decode_workspace_size(const attn_dims *dims)
+{
+    if (validate_decode_dims(dims) != ATTN_OK) return 0;
+    const int sms = current_sms();
+    if (sms <= 0) return 0;
+    return attn::decode_workspace_bytes(dims->B, dims->h, dims->m, dims->n, sms);
+}
+
+attn_status attn_decode(const void *Q, const void *K, const void *V, const int32_t *cache_lengths, float scale,
+                        void *out, float *lse, const attn_dims *dims, void *workspace, size_t workspace_bytes,
+                        void *stream)
+{
+    attn_status st = validate_decode_dims(dims);
+    if (st != ATTN_OK) return st;
+    const int mask = cache_lengths != nullptr ? ATTN_MASK_KEY_PADDING : ATTN_MASK_NONE;
+    st = validate(Q, K, V, cache_lengths, mask, scale, out, dims);
+    if (st != ATTN_OK) return st;
+    const attn_dims &d = *dims;
+    const uint64_t qbytes = static_cast<uint64_t>(d.B) * d.h * d.m * 64 * 2;
+    const uint64_t kbytes = static_cast<uint64_t>(d.B) * d.h * d.n * 64 * 2;
+    const uint64_t lbytes = static_cast<uint64_t>(d.B) * d.h * d.m * 4;
+    if (lse != nullptr) {
+        if (!aligned(lse, 4)) return ATTN_ERR_ALIGN;
+        if (overlaps(lse, lbytes, out, qbytes) || overlaps(lse, lbytes, Q, qbytes) ||
+            overlaps(lse, lbytes, K, kbytes) || overlaps(lse, lbytes, V, kbytes) ||
+            overlaps(lse, lbytes, cache_lengths, 4ull * d.B))
+            return ATTN_ERR_ALIAS;
+    }
+    const int sms = current_sms();
+    if (sms <= 0) return ATTN_ERR_CUDA;
+    const size_t need = attn::decode_workspace_bytes(d.B, d.h, d.m, d.n, sms);
+    if (need > 0) {
+        if (workspace == nullptr) return ATTN_ERR_NULL;
+        if (workspace_bytes < need) return ATTN_ERR_SHAPE;
+        if (!aligned(workspace, 16)) return ATTN_ERR_ALIGN;
+        if (overlaps(workspace, need, out, qbytes) || overlaps(workspace, need, Q, qbytes) ||
+            overlaps(workspace, need, K, kbytes) || overlaps(workspace, need, V, kbytes) ||
+            overlaps(workspace, need, cache_lengths, 4ull * d.B) || (lse && overlaps(workspace, need, lse, lbytes)))
+            return ATTN_ERR_ALIAS;
+    }
+    attn::Problem p;
+    p.q = Q;
+    p.k = K;
+    p.v = V;
+    p.key_lengths = cache_lengths;
+    p.out = out;
+    p.lse = lse;
+    p.B = d.B;
+    p.h = d.h;
+    p.m = d.m;
+    p.n = d.n;
+    p.d = 64;
+    p.mask_kind = mask;
+    p.scale = scale;
+    p.bf16 = true;
+    return attn::launch_decode(p, workspace, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK
+                                                                                                  : ATTN_ERR_CUDA;
+}
+
 int attn_select_kernel(const attn_dims *dims, int mask_kind)
 {
     if (validate_dims(dims, mask_kind, 1.0f) != ATTN_OK) return ATTN_KERNEL_AUTO;

@@ -1,0 +1,295 @@
+// Incremental decoding: a few new query rows per (batch, head) against a cached
+// K/V prefix, the decoder's per-step attention during generation ("Paper Deep
+// Reading: Attention Is All You Need", §03 "Decoder layer": the decoder produces
+// one position at a time and attends to the positions produced so far; the slide
+// deck's "Training Details" / results slides use beam search).  Every new query
+// sees the cached keys 0 .. len_b - 1 of its batch entry (the key-padding mask of
+// the attention equation with len_b = the cache length), so the result is exactly
+// attn_fwd with ATTN_MASK_KEY_PADDING.
+//
+// The work is memory-bound (each cached K and V row is read once per step and used
+// by m <= 8 queries), so it runs on the CUDA cores and is split over the keys
+// (split-KV): CTA (split, b*h) reads keys [split * chunk, (split + 1) * chunk) of
+// one head.  Eight lanes share a key row (16 bytes each, so a warp load covers
+// four whole rows), each eight-lane group keeps an online softmax over its rows,
+// and the CTA merges its 32 groups.  With one split the CTA writes the output;
+// otherwise it writes (max, sum, unnormalised O) and attn_decode_combine_kernel
+// merges the splits.
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include <cstdint>
+
+#include "kernels.h"
+
+namespace attn {
+
+namespace {
+
+constexpr int kD = 64;
+constexpr int kWarps = 8;
+constexpr int kRowsPerPass = kWarps * 4; // key rows the CTA reads per pass
+constexpr int kPart = kD + 2;            // floats of one partial: O[64], max, sum
+
+__device__ __forceinline__ float ex2f(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void unpack8(uint4 u, float (&f)[8])
+{
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+// Merge softmax state (m2, l2, a2) into (m, l, a): both are sums of exp2(x - m)
+// weights over disjoint key sets.
+template <int M>
+__device__ __forceinline__ void merge(float (&m)[M], float (&l)[M], float (&a)[M][8], const float (&m2)[M],
+                                      const float (&l2)[M], const float (&a2)[M][8])
+{
+#pragma unroll
+    for (int q = 0; q < M; ++q) {
+        const float mn = fmaxf(m[q], m2[q]);
+        const float f1 = mn == -CUDART_INF_F ? 0.f : ex2f(m[q] - mn);
+        const float f2 = mn == -CUDART_INF_F ? 0.f : ex2f(m2[q] - mn);
+        l[q] = l[q] * f1 + l2[q] * f2;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a[q][e] = a[q][e] * f1 + a2[q][e] * f2;
+        m[q] = mn;
+    }
+}
+
+// M: query rows handled per (b, h) (the call's m rounded up to 1, 2, 4 or 8).
+template <int M>
+__global__ void __launch_bounds__(kWarps * 32)
+attn_decode_kernel(const __nv_bfloat16 *__restrict__ Q, const __nv_bfloat16 *__restrict__ K,
+                   const __nv_bfloat16 *__restrict__ V, const int32_t *__restrict__ lengths,
+                   __nv_bfloat16 *__restrict__ out, float *__restrict__ lse, float *__restrict__ part, int h,
+                   int m, int n, int chunk, int splits, float scale_log2)
+{
+    __shared__ float red[kWarps][M][kPart];
+    const int bh = blockIdx.x;
+    const int split = blockIdx.y;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int r = lane / 8;  // key row within the warp's four
+    const int j = lane % 8;  // 16-byte slice of the row: dims 8j .. 8j+7
+    int len = n;
+    if (lengths != nullptr) {
+        len = __ldg(lengths + bh / h);
+        len = len < 0 ? 0 : (len > n ? n : len);
+    }
+    const int k_begin = split * chunk;
+    const int k_end = min(len, k_begin + chunk);
+
+    // this lane's slice of every query row, pre-multiplied by scale * log2 e
+    float q[M][8];
+#pragma unroll
+    for (int qi = 0; qi < M; ++qi) {
+        if (qi < m) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(Q + (static_cast<size_t>(bh) * m + qi) * kD) + j);
+            unpack8(u, q[qi]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) q[qi][e] *= scale_log2;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) q[qi][e] = 0.f;
+        }
+    }
+    float mx[M], sm[M], acc[M][8];
+#pragma unroll
+    for (int qi = 0; qi < M; ++qi) {
+        mx[qi] = -CUDART_INF_F;
+        sm[qi] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[qi][e] = 0.f;
+    }
+
+    const uint4 *Kh = reinterpret_cast<const uint4 *>(K + static_cast<size_t>(bh) * n * kD);
+    const uint4 *Vh = reinterpret_cast<const uint4 *>(V + static_cast<size_t>(bh) * n * kD);
+    // Passes over the warp's rows are warp-uniform (the shuffles below need all 32
+    // lanes); a row past the chunk is loaded as nothing and skipped after them.
+    // The next pass's rows are requested before this pass's arithmetic.
+    int row = k_begin + warp * 4 + r;
+    uint4 ku = make_uint4(0, 0, 0, 0), vu = make_uint4(0, 0, 0, 0);
+    if (row < k_end) {
+        ku = __ldg(Kh + static_cast<size_t>(row) * (kD / 8) + j);
+        vu = __ldg(Vh + static_cast<size_t>(row) * (kD / 8) + j);
+    }
+    for (int base = k_begin + warp * 4; base < k_end; base += kRowsPerPass, row += kRowsPerPass) {
+        const bool valid = row < k_end;
+        const int nrow = row + kRowsPerPass;
+        uint4 kn = make_uint4(0, 0, 0, 0), vn = make_uint4(0, 0, 0, 0);
+        if (nrow < k_end) {
+            kn = __ldg(Kh + static_cast<size_t>(nrow) * (kD / 8) + j);
+            vn = __ldg(Vh + static_cast<size_t>(nrow) * (kD / 8) + j);
+        }
+        float kf[8], vf[8];
+        unpack8(ku, kf);
+        unpack8(vu, vf);
+#pragma unroll
+        for (int qi = 0; qi < M; ++qi) {
+            float x = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x = fmaf(q[qi][e], kf[e], x);
+            // the eight lanes of this row hold the eight partial dot products
+            x += __shfl_xor_sync(0xffffffffu, x, 1);
+            x += __shfl_xor_sync(0xffffffffu, x, 2);
+            x += __shfl_xor_sync(0xffffffffu, x, 4);
+            if (valid) {
+                const float mn = fmaxf(mx[qi], x);
+                const float alpha = ex2f(mx[qi] - mn); // 0 on the group's first row
+                const float pw = ex2f(x - mn);
+                sm[qi] = sm[qi] * alpha + pw;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[qi][e] = fmaf(pw, vf[e], acc[qi][e] * alpha);
+                mx[qi] = mn;
+            }
+        }
+        ku = kn;
+        vu = vn;
+    }
+    // the warp's four row groups (lanes j, j + 8, j + 16, j + 24) into lanes 0-7
+#pragma unroll
+    for (int off = 8; off <= 16; off *= 2) {
+        float m2[M], l2[M], a2[M][8];
+#pragma unroll
+        for (int qi = 0; qi < M; ++qi) {
+            m2[qi] = __shfl_xor_sync(0xffffffffu, mx[qi], off);
+            l2[qi] = __shfl_xor_sync(0xffffffffu, sm[qi], off);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) a2[qi][e] = __shfl_xor_sync(0xffffffffu, acc[qi][e], off);
+        }
+        merge<M>(mx, sm, acc, m2, l2, a2);
+    }
+    if (lane < 8) {
+#pragma unroll
+        for (int qi = 0; qi < M; ++qi) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) red[warp][qi][8 * j + e] = acc[qi][e];
+            if (j == 0) {
+                red[warp][qi][kD] = mx[qi];
+                red[warp][qi][kD + 1] = sm[qi];
+            }
+        }
+    }
+    __syncthreads();
+    // the CTA's warps: thread t < M * 64 merges dimension t % 64 of query t / 64
+    for (int t = threadIdx.x; t < M * kD; t += blockDim.x) {
+        const int qi = t / kD, dim = t % kD;
+        if (qi >= m) continue;
+        float mm = -CUDART_INF_F;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, red[w][qi][kD]);
+        float ll = 0.f, aa = 0.f;
+        if (mm != -CUDART_INF_F) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float f = ex2f(red[w][qi][kD] - mm);
+                ll += red[w][qi][kD + 1] * f;
+                aa += red[w][qi][dim] * f;
+            }
+        }
+        const size_t row = static_cast<size_t>(bh) * m + qi;
+        if (splits == 1) {
+            out[row * kD + dim] = __float2bfloat16_rn(ll > 0.f ? aa / ll : 0.f); // no allowed key -> 0
+            if (lse != nullptr && dim == 0)
+                lse[row] = ll > 0.f ? (mm + __log2f(ll)) * 0.6931471805599453f : -CUDART_INF_F;
+        } else {
+            float *pp = part + (row * splits + split) * kPart;
+            pp[dim] = aa;
+            if (dim == 0) {
+                pp[kD] = mm;
+                pp[kD + 1] = ll;
+            }
+        }
+    }
+}
+
+// One warp per (b, h, query row): merge the splits' (max, sum, O), divide, store.
+__global__ void attn_decode_combine_kernel(const float *__restrict__ part, __nv_bfloat16 *__restrict__ out,
+                                           float *__restrict__ lse, int rows, int splits)
+{
+    const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    if (row >= rows) return;
+    const float *pr = part + static_cast<size_t>(row) * splits * kPart;
+    float mm = -CUDART_INF_F;
+    for (int s = lane; s < splits; s += 32) mm = fmaxf(mm, pr[s * kPart + kD]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, off));
+    float ll = 0.f, a0 = 0.f, a1 = 0.f;
+    if (mm != -CUDART_INF_F) {
+        for (int s = 0; s < splits; ++s) {
+            const float *ps = pr + s * kPart;
+            const float f = ex2f(ps[kD] - mm); // 0 for a split with no key (max -inf)
+            ll += ps[kD + 1] * f;
+            a0 += ps[lane] * f;
+            a1 += ps[lane + 32] * f;
+        }
+    }
+    const float inv = ll > 0.f ? 1.f / ll : 0.f;
+    out[static_cast<size_t>(row) * kD + lane] = __float2bfloat16_rn(a0 * inv);
+    out[static_cast<size_t>(row) * kD + lane + 32] = __float2bfloat16_rn(a1 * inv);
+    if (lse != nullptr && lane == 0) lse[row] = ll > 0.f ? (mm + __log2f(ll)) * 0.6931471805599453f : -CUDART_INF_F;
+}
+
+} // namespace
+
+int decode_splits(int B, int h, int n, int sms)
+{
+    // enough CTAs for about four waves, each reading at least 256 keys
+    const int max_splits = (n + 255) / 256;
+    const long heads = static_cast<long>(B) * h;
+    long want = (4L * sms + heads - 1) / heads;
+    if (want < 1) want = 1;
+    if (want > max_splits) want = max_splits;
+    if (want > 65535) want = 65535;
+    return static_cast<int>(want);
+}
+
+size_t decode_workspace_bytes(int B, int h, int m, int n, int sms)
+{
+    const int splits = decode_splits(B, h, n, sms);
+    if (splits <= 1) return 0;
+    return static_cast<size_t>(B) * h * m * splits * kPart * sizeof(float);
+}
+
+cudaError_t launch_decode(const Problem &p, void *workspace, int sms, cudaStream_t stream)
+{
+    const int splits = decode_splits(p.B, p.h, p.n, sms);
+    int chunk = (p.n + splits - 1) / splits;
+    chunk = (chunk + kRowsPerPass - 1) / kRowsPerPass * kRowsPerPass;
+    const float scale_log2 = p.scale * 1.4426950408889634f;
+    const dim3 grid(p.B * p.h, splits);
+    const auto *q = static_cast<const __nv_bfloat16 *>(p.q);
+    const auto *k = static_cast<const __nv_bfloat16 *>(p.k);
+    const auto *v = static_cast<const __nv_bfloat16 *>(p.v);
+    auto *o = static_cast<__nv_bfloat16 *>(p.out);
+    float *part = static_cast<float *>(workspace);
+    if (p.m <= 1)
+        attn_decode_kernel<1><<<grid, kWarps * 32, 0, stream>>>(q, k, v, p.key_lengths, o, p.lse, part, p.h, p.m,
+                                                               p.n, chunk, splits, scale_log2);
+    else if (p.m <= 2)
+        attn_decode_kernel<2><<<grid, kWarps * 32, 0, stream>>>(q, k, v, p.key_lengths, o, p.lse, part, p.h, p.m,
+                                                               p.n, chunk, splits, scale_log2);
+    else if (p.m <= 4)
+        attn_decode_kernel<4><<<grid, kWarps * 32, 0, stream>>>(q, k, v, p.key_lengths, o, p.lse, part, p.h, p.m,
+                                                               p.n, chunk, splits, scale_log2);
+    else
+        attn_decode_kernel<8><<<grid, kWarps * 32, 0, stream>>>(q, k, v, p.key_lengths, o, p.lse, part, p.h, p.m,
+                                                               p.n, chunk, splits, scale_log2);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || splits == 1) return e;
+    const int rows = p.B * p.h * p.m;
+    attn_decode_combine_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(part, o, p.lse, rows, splits);
+    return cudaGetLastError();
+}
+
+} // namespace attn

@@ -36,6 +36,12 @@ cudaError_t launch_flash(const Problem &p, bool pair_mode, int *tile_counter, cu
 // Bytes of workspace the dynamic tile schedule needs.
 constexpr size_t kWorkspaceBytes = 256;
 
+// Incremental decoding (bf16, d == 64, m <= 8 queries per head, every query sees
+// keys 0 .. len_b - 1): split-KV CUDA-core kernel plus a combine pass.
+int decode_splits(int B, int h, int n, int sms);
+size_t decode_workspace_bytes(int B, int h, int m, int n, int sms);
+cudaError_t launch_decode(const Problem &p, void *workspace, int sms, cudaStream_t stream);
+
 // [BH][rows][64] bf16 viewed as a 3-D tensor (64, rows, BH) for TMA; box = 128
 // rows x 64 columns of one (b, h), 128-byte swizzle, rows past `rows` read as 0.
 bool encode_rows_map(CUtensorMap *map, const void *base, int rows, int BH);

@@ -89,6 +89,15 @@ WORKLOADS = {
 }
 
 
+# One incremental-decoding step against a key/value cache: 16 sentences x beam 4,
+# the big model's 16 heads, one new query row each, caches of capacity 4096 holding
+# 1024..4096 positions.  Same draw order as the others (lengths, then Q, K, V).
+DECODE = Workload("decode_step_kv_cache", "bf16", 64, 16, 1, 4096, 64, MASK_KEY_PADDING, 0.125, 1006,
+                  (1024, 4096),
+                  description="decode step, bf16, B=64 (16 x beam 4) h=16 m=1 against K/V caches of "
+                              "capacity 4096 holding 1024..4096 rows, d_k=64")
+
+
 def round_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """float32 -> bf16 bit patterns (uint16), round to nearest even.
 
