@@ -25,6 +25,7 @@ LIBRARY = os.path.join(_HERE, "liboracle.so")
 
 MASK_KEY_PADDING = 1
 MASK_CAUSAL = 2
+MASK_WINDOW = 4
 
 
 def compile_oracle(source: str = SOURCE, output: str = LIBRARY, openmp: bool = True) -> str:
@@ -65,6 +66,15 @@ class Oracle:
         lib.oracle_bf16_to_f64.restype = None
         lib.oracle_f32_to_f64.argtypes = [ctypes.POINTER(ctypes.c_float), dp, i64]
         lib.oracle_f32_to_f64.restype = None
+        lib.oracle_attn_fwd_w.argtypes = [dp, dp, dp, i32p, ctypes.c_int, i64, ctypes.c_double,
+                                          i64, i64, i64, i64, i64, dp]
+        lib.oracle_attn_fwd_w.restype = ctypes.c_int
+        lib.oracle_attn_rows_w.argtypes = [dp, dp, dp, i32p, ctypes.c_int, i64, ctypes.c_double,
+                                           i64, i64, i64, i64, i64, i64p, i64, dp]
+        lib.oracle_attn_rows_w.restype = ctypes.c_int
+        lib.oracle_attn_lse_w.argtypes = [dp, dp, i32p, ctypes.c_int, i64, ctypes.c_double,
+                                          i64, i64, i64, i64, i64, dp]
+        lib.oracle_attn_lse_w.restype = ctypes.c_int
         lib.oracle_attn_lse.argtypes = [dp, dp, i32p, ctypes.c_int, ctypes.c_double,
                                         i64, i64, i64, i64, i64, dp]
         lib.oracle_attn_lse.restype = ctypes.c_int
@@ -106,23 +116,32 @@ class Oracle:
         return B, h, m, k.shape[2], d
 
     def attn_fwd(self, q, k, v, key_lengths: Optional[np.ndarray], mask_kind: int,
-                 scale: float) -> np.ndarray:
-        """Every output row, float64 [B, h, m, d]."""
+                 scale: float, window: Optional[int] = None) -> np.ndarray:
+        """Every output row, float64 [B, h, m, d].  window: half-width of the restricted-
+        attention window (used when mask_kind has MASK_WINDOW)."""
         q, k, v = self.widen(q), self.widen(k), self.widen(v)
         B, h, m, n, d = self._dims(q, k, v)
         lens = None if key_lengths is None else np.ascontiguousarray(key_lengths, dtype=np.int32)
         out = np.empty((B, h, m, d), dtype=np.float64)
         dp = ctypes.POINTER(ctypes.c_double)
+        lp = None if lens is None else lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+        if window is not None:
+            rc = self._lib.oracle_attn_fwd_w(q.ctypes.data_as(dp), k.ctypes.data_as(dp), v.ctypes.data_as(dp),
+                                             lp, int(mask_kind), int(window), float(scale), B, h, m, n, d,
+                                             out.ctypes.data_as(dp))
+            if rc != 0:
+                raise RuntimeError("oracle_attn_fwd_w failed")
+            return out
         rc = self._lib.oracle_attn_fwd(
-            q.ctypes.data_as(dp), k.ctypes.data_as(dp), v.ctypes.data_as(dp),
-            None if lens is None else lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+            q.ctypes.data_as(dp), k.ctypes.data_as(dp), v.ctypes.data_as(dp), lp,
             int(mask_kind), float(scale), B, h, m, n, d, out.ctypes.data_as(dp))
         if rc != 0:
             raise RuntimeError("oracle_attn_fwd failed")
         return out
 
     def attn_rows(self, q, k, v, key_lengths: Optional[np.ndarray], mask_kind: int,
-                  scale: float, rows: np.ndarray, widened: bool = False) -> np.ndarray:
+                  scale: float, rows: np.ndarray, widened: bool = False,
+                  window: Optional[int] = None) -> np.ndarray:
         """Selected output rows (linear ids ((b*h+head)*m+i)), float64 [len(rows), d]."""
         if not widened:
             q, k, v = self.widen(q), self.widen(k), self.widen(v)
@@ -131,26 +150,37 @@ class Oracle:
         lens = None if key_lengths is None else np.ascontiguousarray(key_lengths, dtype=np.int32)
         out = np.empty((rows.size, d), dtype=np.float64)
         dp = ctypes.POINTER(ctypes.c_double)
-        rc = self._lib.oracle_attn_rows(
-            q.ctypes.data_as(dp), k.ctypes.data_as(dp), v.ctypes.data_as(dp),
-            None if lens is None else lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
-            int(mask_kind), float(scale), B, h, m, n, d,
-            rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), rows.size,
-            out.ctypes.data_as(dp))
+        lp = None if lens is None else lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+        rp = rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+        if window is not None:
+            rc = self._lib.oracle_attn_rows_w(q.ctypes.data_as(dp), k.ctypes.data_as(dp), v.ctypes.data_as(dp),
+                                              lp, int(mask_kind), int(window), float(scale), B, h, m, n, d,
+                                              rp, rows.size, out.ctypes.data_as(dp))
+        else:
+            rc = self._lib.oracle_attn_rows(
+                q.ctypes.data_as(dp), k.ctypes.data_as(dp), v.ctypes.data_as(dp), lp,
+                int(mask_kind), float(scale), B, h, m, n, d, rp, rows.size, out.ctypes.data_as(dp))
         if rc != 0:
             raise RuntimeError("oracle_attn_rows failed")
         return out
 
-    def attn_lse(self, q, k, key_lengths: Optional[np.ndarray], mask_kind: int, scale: float) -> np.ndarray:
+    def attn_lse(self, q, k, key_lengths: Optional[np.ndarray], mask_kind: int, scale: float,
+                 window: Optional[int] = None) -> np.ndarray:
         """Natural log of each row's softmax normaliser, float64 [B, h, m] (-inf: no allowed key)."""
         q, k = self.widen(q), self.widen(k)
         B, h, m, n, d = self._dims(q, k, k)
         lens = None if key_lengths is None else np.ascontiguousarray(key_lengths, dtype=np.int32)
         out = np.empty((B, h, m), dtype=np.float64)
         dp = ctypes.POINTER(ctypes.c_double)
+        lp = None if lens is None else lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+        if window is not None:
+            rc = self._lib.oracle_attn_lse_w(q.ctypes.data_as(dp), k.ctypes.data_as(dp), lp, int(mask_kind),
+                                             int(window), float(scale), B, h, m, n, d, out.ctypes.data_as(dp))
+            if rc != 0:
+                raise RuntimeError("oracle_attn_lse_w failed")
+            return out
         rc = self._lib.oracle_attn_lse(
-            q.ctypes.data_as(dp), k.ctypes.data_as(dp),
-            None if lens is None else lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+            q.ctypes.data_as(dp), k.ctypes.data_as(dp), lp,
             int(mask_kind), float(scale), B, h, m, n, d, out.ctypes.data_as(dp))
         if rc != 0:
             raise RuntimeError("oracle_attn_lse failed")

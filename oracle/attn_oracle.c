@@ -25,7 +25,11 @@
  *    positions; the library rejects causal with m != n);
  *  - a query row with no allowed key has output 0 (the formula gives 0/0);
  *  - the scale is an argument (1/sqrt(d_k) in the formula; the pages' worked
- *    example needs other values).
+ *    example needs other values);
+ *  - restricted self-attention (the deep-reading page's §04 complexity table,
+ *    "Restricted self-attention", O(r n d); the slide deck's "Limitations and
+ *    Future Work") keeps, for query i, the keys j with |i - j| <= w: a
+ *    neighbourhood of r = 2w + 1 positions around the query (w is the argument).
  *
  * Every function is the plain definition: no blocking, no online softmax,
  * no reordering beyond what the definition states.  Rows run in parallel with
@@ -41,6 +45,7 @@
 
 #define ORACLE_MASK_KEY_PADDING 1
 #define ORACLE_MASK_CAUSAL 2
+#define ORACLE_MASK_WINDOW 4
 
 /* bf16 is the upper half of an IEEE binary32: shift the 16 bits into place. */
 void oracle_bf16_to_f64(const uint16_t *src, double *dst, int64_t count)
@@ -67,11 +72,16 @@ int oracle_num_threads(void)
 #endif
 }
 
+/* Half-width of the restricted-attention window for the current call (set by the
+ * _w entry points for the duration of one call; 0 otherwise). */
+static int64_t g_window = 0;
+
 /* M_ij == 0 (allowed) or -inf (masked): deep reading §04, §03 "Decoder layer". */
 static int key_allowed(int mask_kind, int64_t i, int64_t j, int64_t len_b)
 {
     if ((mask_kind & ORACLE_MASK_CAUSAL) && j > i) return 0;
     if ((mask_kind & ORACLE_MASK_KEY_PADDING) && j >= len_b) return 0;
+    if ((mask_kind & ORACLE_MASK_WINDOW) && (i - j > g_window || j - i > g_window)) return 0;
     return 1;
 }
 
@@ -356,5 +366,42 @@ int oracle_attn_bwd(const double *Q, const double *K, const double *V, const dou
     free(Z);
     free(D);
     return 0;
+}
+
+/* The same three functions with a restricted-attention window: keys j with
+ * |i - j| <= window stay for query i when mask_kind has ORACLE_MASK_WINDOW.
+ * Not reentrant (the window is held for the call); the tests call the oracle
+ * from one thread. */
+int oracle_attn_fwd_w(const double *Q, const double *K, const double *V, const int32_t *key_lengths,
+                      int mask_kind, int64_t window, double scale, int64_t B, int64_t h, int64_t m, int64_t n,
+                      int64_t d, double *out)
+{
+    if (window < 0) return -1;
+    g_window = window;
+    int rc = oracle_attn_fwd(Q, K, V, key_lengths, mask_kind, scale, B, h, m, n, d, out);
+    g_window = 0;
+    return rc;
+}
+
+int oracle_attn_rows_w(const double *Q, const double *K, const double *V, const int32_t *key_lengths,
+                       int mask_kind, int64_t window, double scale, int64_t B, int64_t h, int64_t m, int64_t n,
+                       int64_t d, const int64_t *rows, int64_t nrows, double *out)
+{
+    if (window < 0) return -1;
+    g_window = window;
+    int rc = oracle_attn_rows(Q, K, V, key_lengths, mask_kind, scale, B, h, m, n, d, rows, nrows, out);
+    g_window = 0;
+    return rc;
+}
+
+int oracle_attn_lse_w(const double *Q, const double *K, const int32_t *key_lengths, int mask_kind,
+                      int64_t window, double scale, int64_t B, int64_t h, int64_t m, int64_t n, int64_t d,
+                      double *lse)
+{
+    if (window < 0) return -1;
+    g_window = window;
+    int rc = oracle_attn_lse(Q, K, key_lengths, mask_kind, scale, B, h, m, n, d, lse);
+    g_window = 0;
+    return rc;
 }
 

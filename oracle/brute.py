@@ -14,11 +14,16 @@ import numpy as np
 
 MASK_KEY_PADDING = 1
 MASK_CAUSAL = 2
+MASK_WINDOW = 4
 
 
-def additive_mask(m: int, n: int, mask_kind: int, length: int) -> np.ndarray:
-    """M for one (batch, head): -inf for future keys (causal) and padded keys."""
+def additive_mask(m: int, n: int, mask_kind: int, length: int, window: int = 0) -> np.ndarray:
+    """M for one (batch, head): -inf for future keys (causal), padded keys, and keys
+    further than `window` positions from the query (restricted attention)."""
     M = np.zeros((m, n), dtype=np.float64)
+    if mask_kind & MASK_WINDOW:
+        far = np.abs(np.arange(n)[None, :] - np.arange(m)[:, None]) > window
+        M[far] = -np.inf
     if mask_kind & MASK_CAUSAL:
         future = np.arange(n)[None, :] > np.arange(m)[:, None]
         M[future] = -np.inf
@@ -28,14 +33,14 @@ def additive_mask(m: int, n: int, mask_kind: int, length: int) -> np.ndarray:
 
 
 def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, key_lengths, mask_kind: int,
-              scale: float) -> np.ndarray:
+              scale: float, window: int = 0) -> np.ndarray:
     """q [B,h,m,d], k/v [B,h,n,d] float64 -> [B,h,m,d]; rows with no allowed key are 0."""
     B, h, m, d = q.shape
     n = k.shape[2]
     out = np.zeros((B, h, m, d), dtype=np.float64)
     for b in range(B):
         length = n if key_lengths is None else int(key_lengths[b])
-        M = additive_mask(m, n, mask_kind, length)
+        M = additive_mask(m, n, mask_kind, length, window)
         for head in range(h):
             S = (q[b, head] @ k[b, head].T) * scale + M
             top = S.max(axis=1, keepdims=True)

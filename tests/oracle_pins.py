@@ -392,6 +392,83 @@ def pin_bwd_torch_autograd(o):
             np.testing.assert_allclose(got, ref.numpy(), rtol=0, atol=1e-12)
 
 
+# ---------------------------------------------------------------- restricted attention
+# Restricted self-attention: the deep-reading page's §04 complexity table lists it as
+# O(r n d) with path length O(n / r); the slide deck lists local, restricted attention
+# under "Limitations and Future Work".  Reading: keys with |i - j| <= w stay.
+WIN = 4
+
+
+def pin_window_brute_force(o):
+    """The full-matrix formula with the banded mask, every tiny shape, window and mask."""
+    rng = np.random.default_rng(41)
+    for n in range(1, 8):
+        for w in (0, 1, 2, 3, 9):
+            B, h, d = 2, 2, 3
+            Q, K, V = _rand(rng, B, h, n, d), _rand(rng, B, h, n, d), _rand(rng, B, h, n, d)
+            lens = rng.integers(0, n + 1, size=B).astype(np.int32)
+            for mk in (WIN, WIN | PAD, WIN | CAUSAL, WIN | PAD | CAUSAL):
+                got = o.attn_fwd(Q, K, V, lens, mk, 0.7, window=w)
+                ref = brute.attention(Q, K, V, lens, mk, 0.7, window=w)
+                np.testing.assert_allclose(got, ref, rtol=0, atol=1e-13, err_msg=f"n={n} w={w} mask={mk}")
+
+
+def pin_window_zero_copies_values(o):
+    """w = 0: each query sees only its own position, so its output is that value row."""
+    rng = np.random.default_rng(42)
+    Q, K, V = _rand(rng, 2, 3, 9, 5), _rand(rng, 2, 3, 9, 5), _rand(rng, 2, 3, 9, 5)
+    for mk in (WIN, WIN | CAUSAL):
+        np.testing.assert_allclose(o.attn_fwd(Q, K, V, None, mk, 0.9, window=0), V, rtol=0, atol=1e-15)
+
+
+def pin_window_wide_equals_full(o):
+    """A window covering every key changes nothing (bit for bit)."""
+    rng = np.random.default_rng(43)
+    Q, K, V = _rand(rng, 2, 2, 11, 4), _rand(rng, 2, 2, 11, 4), _rand(rng, 2, 2, 11, 4)
+    lens = np.array([5, 11], dtype=np.int32)
+    for mk in (0, PAD, CAUSAL, PAD | CAUSAL):
+        np.testing.assert_array_equal(o.attn_fwd(Q, K, V, lens, mk | WIN, 0.5, window=10),
+                                      o.attn_fwd(Q, K, V, lens, mk, 0.5))
+
+
+def pin_window_locality(o):
+    """Row i is bitwise unchanged when keys and values outside [i - w, i + w] change."""
+    rng = np.random.default_rng(44)
+    n, w, i = 16, 3, 7
+    Q, K, V = _rand(rng, 1, 1, n, 4), _rand(rng, 1, 1, n, 4), _rand(rng, 1, 1, n, 4)
+    base = o.attn_fwd(Q, K, V, None, WIN, 0.8, window=w)
+    K2, V2 = K.copy(), V.copy()
+    far = [j for j in range(n) if abs(j - i) > w]
+    K2[0, 0, far] = rng.standard_normal((len(far), 4)) * 5
+    V2[0, 0, far] = rng.standard_normal((len(far), 4)) * 5
+    moved = o.attn_fwd(Q, K2, V2, None, WIN, 0.8, window=w)
+    np.testing.assert_array_equal(moved[0, 0, i], base[0, 0, i])
+    assert not np.array_equal(moved, base)
+
+
+def pin_window_torch_sdpa(o):
+    """torch's fp64 scaled_dot_product_attention with a banded boolean mask."""
+    import torch
+    import torch.nn.functional as F
+
+    rng = np.random.default_rng(45)
+    B, h, n, d, w = 2, 2, 13, 8, 2
+    Q, K, V = _rand(rng, B, h, n, d), _rand(rng, B, h, n, d), _rand(rng, B, h, n, d)
+    lens = np.array([6, 13], dtype=np.int32)
+    for mk in (WIN, WIN | CAUSAL, WIN | PAD):
+        allow = np.abs(np.arange(n)[None, :] - np.arange(n)[:, None]) <= w
+        allow = np.broadcast_to(allow, (B, 1, n, n)).copy()
+        if mk & CAUSAL:
+            allow &= ~(np.arange(n)[None, None, None, :] > np.arange(n)[None, None, :, None])
+        if mk & PAD:
+            allow &= np.arange(n)[None, None, None, :] < lens[:, None, None, None]
+        ref = F.scaled_dot_product_attention(torch.from_numpy(Q), torch.from_numpy(K), torch.from_numpy(V),
+                                             attn_mask=torch.from_numpy(allow), scale=0.4).numpy()
+        got = o.attn_fwd(Q, K, V, lens, mk, 0.4, window=w)
+        live = np.broadcast_to(allow.any(axis=3, keepdims=True), got.shape)
+        np.testing.assert_allclose(got[live], ref[live], rtol=0, atol=1e-12)
+
+
 ALL_PINS = [
     pin_worked_example_printed,
     pin_worked_example_closed_form,
@@ -413,4 +490,9 @@ ALL_PINS = [
     pin_bwd_uniform_scores,
     pin_lse,
     pin_bwd_torch_autograd,
+    pin_window_brute_force,
+    pin_window_zero_copies_values,
+    pin_window_wide_equals_full,
+    pin_window_locality,
+    pin_window_torch_sdpa,
 ]

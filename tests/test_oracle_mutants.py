@@ -38,6 +38,9 @@ MUTANTS = {
     "bwd_normaliser_dropped_in_key_pass": ("double p = exp(scale * dot - mu[i]) / Z[i];",
                                            "double p = exp(scale * dot - mu[i]);"),
     "lse_missing_max": ("lse[r] = mu + log(Z);", "lse[r] = log(Z);"),
+    # restricted attention
+    "window_off_by_one": ("(i - j > g_window || j - i > g_window)", "(i - j >= g_window || j - i > g_window)"),
+    "window_one_sided": ("(i - j > g_window || j - i > g_window)", "(i - j > g_window)"),
 }
 
 
