@@ -284,6 +284,35 @@ def backward_workload(torch, attn, device, peak_tf, steps=20):
             "calls_timed": steps, "algorithmic": "10*d_k FLOPs per allowed (query, key) pair"}
 
 
+def window_workload(torch, attn, device, peak_tf, steps=50, window=256):
+    """Restricted self-attention on the long sequences of workload 5 without the causal
+    mask: B4 h16 n=m=8192, keys with |i - j| <= 256 (513-position neighbourhoods), through
+    attn_fwd_window.  Useful work: 4*d_k FLOPs per allowed (query, key) pair."""
+    w = WORKLOADS[5]
+    inp = draw(w)
+    q, k, v = (to_device(x, w.dtype, torch, device) for x in (inp.q, inp.k, inp.v))
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        attn.attn_fwd_window(q, k, v, None, attn.MASK_WINDOW, window, w.scale, out=out, stream=stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    ms = time_launches(step, steps, torch, stream)
+    st, info = attn.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} (info {info}) after the window loop")
+    i = np.arange(w.n)
+    pairs = float((np.minimum(i + window, w.n - 1) - np.maximum(i - window, 0) + 1).sum()) * w.B * w.h
+    flops = 4 * w.d * pairs
+    return {"workload": f"restricted self-attention, bf16, B={w.B} h={w.h} n=m={w.n} d_k={w.d}, window {window}",
+            "entry_point": "attn_fwd_window", "us_per_call": ms * 1e3,
+            "tflops_useful": flops / (ms * 1e-3) / 1e12, "frac_of_peak": flops / (ms * 1e-3) / 1e12 / peak_tf,
+            "calls_timed": steps, "algorithmic": "4*d_k FLOPs per allowed (query, key) pair"}
+
+
 def decode_workload(torch, attn, device, peak_hbm, steps=50):
     """One incremental-decoding step (workloads.DECODE: B64 h16, one new row each, K/V
     caches of capacity 4096 holding 1024..4096 rows) through attn_decode, caches
@@ -492,6 +521,7 @@ def main():
         result["other_workloads"] = short_workloads(torch, attn, device, peak_hbm)
         result["backward"] = backward_workload(torch, attn, device, peak_tf)
         result["decode"] = decode_workload(torch, attn, device, peak_hbm)
+        result["window"] = window_workload(torch, attn, device, peak_tf)
         if rank == 0:
             cb, _ = cpu_oracle_sample(w, inp, args.cpu_seconds)
             cb.pop("seconds", None)

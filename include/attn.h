@@ -71,7 +71,8 @@ typedef enum {
 typedef enum {
     ATTN_MASK_NONE = 0,
     ATTN_MASK_KEY_PADDING = 1,
-    ATTN_MASK_CAUSAL = 2
+    ATTN_MASK_CAUSAL = 2,
+    ATTN_MASK_WINDOW = 4 /* restricted self-attention; attn_fwd_window only */
 } attn_mask_kind; /* bit flags: 3 = key padding and causal */
 
 typedef enum {
@@ -214,6 +215,25 @@ attn_status attn_fwd_noalloc(const void *Q, const void *K, const void *V,
 attn_status attn_fwd_lse(const void *Q, const void *K, const void *V,
                          const int32_t *key_lengths, int mask_kind, float scale,
                          void *out, float *lse, const attn_dims *dims, void *stream);
+
+/*
+ * Restricted self-attention: attn_fwd where mask_kind may also hold
+ * ATTN_MASK_WINDOW, which keeps, for query i, only the keys j with
+ * |i - j| <= window (a neighbourhood of r = 2 * window + 1 positions around the
+ * query; the deep-reading page's §04 complexity table lists "restricted
+ * self-attention" at O(r n d), the slide deck's "Limitations and Future Work"
+ * local, restricted attention).  The window combines with the other bits as a
+ * union of masked keys (with CAUSAL: keys i - window .. i).  Key tiles outside
+ * every row's window are never loaded or computed, so the work grows with
+ * n * window, not n * n.
+ *
+ * Requires m == n when ATTN_MASK_WINDOW is set (ATTN_ERR_SHAPE) and window >= 0
+ * (ATTN_ERR_VALUE).  Other arguments, rules, errors and kernel choice as attn_fwd;
+ * without ATTN_MASK_WINDOW the call is attn_fwd.
+ */
+attn_status attn_fwd_window(const void *Q, const void *K, const void *V,
+                            const int32_t *key_lengths, int mask_kind, int window, float scale,
+                            void *out, const attn_dims *dims, void *stream);
 
 /* Bytes of device workspace attn_bwd needs for these dims (host only, no CUDA
  * call); 0 if attn_bwd would reject the dims. */

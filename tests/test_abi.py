@@ -175,3 +175,14 @@ def test_decode_rejects_bad_arguments(kwargs, status):
 def test_decode_workspace_size_rejects_bad_dims():
     assert N.decode_workspace_size(N.make_dims(2, 2, 9, 64, 64, 0)) == 0
     assert N.decode_workspace_size(N.make_dims(2, 2, 1, 64, 64, 1)) == 0
+
+
+def test_window_mask_validation():
+    assert N.MASK_WINDOW == _enum("ATTN_MASK_WINDOW")
+    d = N.make_dims(2, 2, 8, 8, 64, 0)
+    assert N.fwd_raw(A, B_, C, None, N.MASK_WINDOW, 0.125, O, d, None) == 4          # attn_fwd: no window bit
+    assert N.fwd_window_raw(A, B_, C, None, N.MASK_WINDOW, -1, 0.125, O, d, None) == 9  # negative window
+    assert N.fwd_window_raw(A, B_, C, None, 8, 3, 0.125, O, d, None) == 4              # unknown bit
+    d2 = N.make_dims(2, 2, 8, 9, 64, 0)
+    assert N.fwd_window_raw(A, B_, C, None, N.MASK_WINDOW, 3, 0.125, O, d2, None) == 2  # m != n
+    assert N.fwd_window_raw(A + 8, B_, C, None, N.MASK_WINDOW, 3, 0.125, O, d, None) == 5

@@ -1,0 +1,74 @@
+"""Restricted self-attention (ATTN_MASK_WINDOW) on every kernel against the fp64 oracle.
+
+Keys with |i - j| <= window stay for query i; tolerance 1e-2 (bf16) / 1e-4 (fp32),
+as for the forward.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import transformer_scaled_dot_masked_gb300 as attn
+from workloads import MASK_CAUSAL, MASK_KEY_PADDING, Workload, draw
+
+from gpu_helpers import as_f64, report, to_device
+
+pytestmark = pytest.mark.gpu
+
+WIN = attn.MASK_WINDOW
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.load()
+
+
+def run_window(inp, mask, window, kernel_m=None):
+    w = inp.workload
+    q, k, v = (to_device(x, w.dtype) for x in (inp.q, inp.k, inp.v))
+    lens = torch.from_numpy(inp.key_lengths).cuda()
+    out = attn.attn_fwd_window(q, k, v, lens, mask, window, w.scale)
+    torch.cuda.synchronize()
+    st, info = attn.device_status()
+    assert st == 0, f"device status {st} (info {info})"
+    return as_f64(out)
+
+
+CASES = [
+    # name, dtype, B, h, n, extra mask, window, lengths
+    ("pair_mode_w0", "bf16", 2, 2, 300, 0, 0, None),
+    ("pair_mode_w1_causal", "bf16", 2, 2, 300, MASK_CAUSAL, 1, None),
+    ("pair_mode_w127", "bf16", 1, 2, 700, 0, 127, None),
+    ("pair_mode_w128_padding", "bf16", 3, 2, 700, MASK_KEY_PADDING, 128, (0, 700)),
+    ("pair_mode_w200_causal_padding", "bf16", 2, 2, 1000, MASK_CAUSAL | MASK_KEY_PADDING, 200, (100, 1000)),
+    ("pair_mode_long_w300", "bf16", 1, 4, 4096, 0, 300, None),
+    ("pair_mode_covering_window", "bf16", 2, 2, 260, MASK_CAUSAL, 5000, None),
+    ("split_mode_w10", "bf16", 3, 3, 100, MASK_KEY_PADDING, 10, (0, 100)),
+    ("split_mode_w64_causal", "bf16", 4, 2, 128, MASK_CAUSAL, 64, None),
+    ("fp32_w7", "fp32", 2, 2, 150, MASK_KEY_PADDING, 7, (1, 150)),
+    ("narrow_heads_w3", "bf16_d32", 2, 2, 90, MASK_CAUSAL, 3, None),
+]
+
+
+@pytest.mark.parametrize("name,dtype,B,h,n,mask,window,lengths", CASES, ids=[c[0] for c in CASES])
+def test_window_matches_oracle(orc, name, dtype, B, h, n, mask, window, lengths):
+    d = 32 if dtype.endswith("d32") else 64
+    w = Workload(name, dtype.split("_")[0], B, h, n, n, d, mask | WIN, d ** -0.5, 51, lengths)
+    inp = draw(w)
+    got = run_window(inp, mask | WIN, window)
+    ref = orc.attn_fwd(inp.q, inp.k, inp.v, inp.key_lengths, mask | WIN, w.scale, window=window)
+    tol = 1e-4 if w.dtype == "fp32" else 1e-2
+    assert np.abs(got - ref).max() <= tol, report(got, ref, tol)
+
+
+def test_window_locality_bitwise():
+    """Row i is bitwise unchanged when keys and values further than the window from it change."""
+    w = Workload("loc", "bf16", 1, 2, 1024, 1024, 64, WIN, 0.125, 52)
+    inp = draw(w)
+    base = run_window(inp, WIN, 100)
+    k2, v2 = inp.k.copy(), inp.v.copy()
+    k2[:, :, 700:] ^= 0x0101
+    v2[:, :, 700:] ^= 0x0101
+    moved = run_window(type(inp)(w, inp.q, k2, v2, inp.key_lengths), WIN, 100)
+    np.testing.assert_array_equal(moved[:, :, :600], base[:, :, :600])
+    assert not np.array_equal(moved, base)

@@ -17,9 +17,9 @@ from typing import Optional
 
 from . import _native
 from ._native import (AttnError, KERNEL_AUTO, KERNEL_FLASH, KERNEL_SHORT, KERNEL_SIMT, MASK_CAUSAL,
-                      MASK_KEY_PADDING, MASK_NONE, DTYPE_BF16, DTYPE_FP32)
+                      MASK_KEY_PADDING, MASK_NONE, MASK_WINDOW, DTYPE_BF16, DTYPE_FP32)
 
-__all__ = ["attn_fwd", "attn_fwd_lse", "attn_bwd", "bwd_workspace_size", "attn_decode", "decode_workspace_size", "AttnError", "select_kernel", "device_status", "make_workspace", "workspace_size", "MASK_NONE", "MASK_KEY_PADDING",
+__all__ = ["attn_fwd", "attn_fwd_window", "attn_fwd_lse", "MASK_WINDOW", "attn_bwd", "bwd_workspace_size", "attn_decode", "decode_workspace_size", "AttnError", "select_kernel", "device_status", "make_workspace", "workspace_size", "MASK_NONE", "MASK_KEY_PADDING",
            "MASK_CAUSAL", "KERNEL_AUTO", "KERNEL_FLASH", "KERNEL_SHORT", "KERNEL_SIMT"]
 
 
@@ -235,6 +235,25 @@ def attn_decode(q, k_cache, v_cache, cache_lengths=None, scale: Optional[float] 
                             None if workspace is None else workspace.data_ptr(),
                             0 if workspace is None else workspace.numel() * workspace.element_size(),
                             stream.cuda_stream)
+    if st != _native.ATTN_OK:
+        raise AttnError(st)
+    return out
+
+
+def attn_fwd_window(q, k, v, key_lengths=None, mask_kind: int = MASK_WINDOW, window: int = 0,
+                    scale: Optional[float] = None, out=None, stream=None):
+    """Restricted self-attention: attn_fwd where MASK_WINDOW in mask_kind keeps, for query i,
+    the keys j with |i - j| <= window (combinable with MASK_CAUSAL and MASK_KEY_PADDING)."""
+    import torch
+    B, h, m, n, d = _check_qkv(q, k, v)
+    scale = d ** -0.5 if scale is None else scale
+    if out is None:
+        out = torch.empty_like(q)
+    _like(out, q, "out")
+    stream = torch.cuda.current_stream(q.device) if stream is None else stream
+    dims = _native.make_dims(B, h, m, n, d, _dtype_code(q))
+    st = _native.fwd_window_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), _lengths_ptr(key_lengths, mask_kind, B),
+                                mask_kind, window, scale, out.data_ptr(), dims, stream.cuda_stream)
     if st != _native.ATTN_OK:
         raise AttnError(st)
     return out

@@ -23,7 +23,7 @@ if not os.path.exists(LIBRARY):
 # Keep these in step with include/attn.h (tests/test_abi.py checks them against the header).
 ATTN_OK = 0
 ATTN_ERR_DEVICE_TIMEOUT = 8
-MASK_NONE, MASK_KEY_PADDING, MASK_CAUSAL = 0, 1, 2
+MASK_NONE, MASK_KEY_PADDING, MASK_CAUSAL, MASK_WINDOW = 0, 1, 2, 4
 DTYPE_BF16, DTYPE_FP32 = 0, 1
 KERNEL_AUTO, KERNEL_FLASH, KERNEL_SHORT, KERNEL_SIMT = 0, 1, 2, 3
 KERNEL_NAMES = {KERNEL_AUTO: "auto", KERNEL_FLASH: "flash", KERNEL_SHORT: "short", KERNEL_SIMT: "simt"}
@@ -55,6 +55,9 @@ lib.attn_bwd_workspace_size.restype = ctypes.c_size_t
 lib.attn_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_float, _vp, _vp, _vp,
                          _vp, ctypes.c_size_t, ctypes.POINTER(AttnDims), _vp]
 lib.attn_bwd.restype = ctypes.c_int
+lib.attn_fwd_window.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_float, _vp,
+                                ctypes.POINTER(AttnDims), _vp]
+lib.attn_fwd_window.restype = ctypes.c_int
 lib.attn_decode_workspace_size.argtypes = [ctypes.POINTER(AttnDims)]
 lib.attn_decode_workspace_size.restype = ctypes.c_size_t
 lib.attn_decode.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, ctypes.POINTER(AttnDims), _vp,
@@ -137,6 +140,13 @@ def bwd_raw(q_ptr, k_ptr, v_ptr, out_ptr, dout_ptr, lse_ptr, lens_ptr, mask_kind
     return lib.attn_bwd(q_ptr, k_ptr, v_ptr, out_ptr, dout_ptr, lse_ptr, lens_ptr, int(mask_kind),
                         float(scale), dq_ptr, dk_ptr, dv_ptr, ws_ptr, int(ws_bytes), ctypes.byref(dims),
                         stream_ptr)
+
+
+def fwd_window_raw(q_ptr, k_ptr, v_ptr, lens_ptr, mask_kind, window, scale, out_ptr, dims: AttnDims,
+                   stream_ptr) -> int:
+    """attn_fwd_window with integer device pointers; returns the status code."""
+    return lib.attn_fwd_window(q_ptr, k_ptr, v_ptr, lens_ptr, int(mask_kind), int(window), float(scale), out_ptr,
+                               ctypes.byref(dims), stream_ptr)
 
 
 def decode_workspace_size(dims: AttnDims) -> int:

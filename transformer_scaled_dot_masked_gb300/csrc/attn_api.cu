@@ -67,9 +67,12 @@ attn_status validate(const void *Q, const void *K, const void *V, const int32_t 
 namespace {
 
 attn_status run(const void *Q, const void *K, const void *V, const int32_t *key_lengths, int mask_kind, float scale,
-                void *out, const attn_dims *dims, void *stream, int kernel, int *tile_counter, float *lse = nullptr)
+                void *out, const attn_dims *dims, void *stream, int kernel, int *tile_counter, float *lse = nullptr,
+                int window = -1)
 {
-    const attn_status st = validate(Q, K, V, key_lengths, mask_kind, scale, out, dims);
+    // the window bit is accepted only from attn_fwd_window (window >= 0), which checks it
+    const int checked = window >= 0 ? (mask_kind & ~ATTN_MASK_WINDOW) : mask_kind;
+    const attn_status st = validate(Q, K, V, key_lengths, checked, scale, out, dims);
     if (st != ATTN_OK) return st;
     const attn_dims &d = *dims;
     if (kernel == ATTN_KERNEL_AUTO) kernel = auto_kernel(d);
@@ -86,6 +89,7 @@ attn_status run(const void *Q, const void *K, const void *V, const int32_t *key_
     p.n = d.n;
     p.d = d.d_k;
     p.mask_kind = mask_kind;
+    p.window = window;
     p.scale = scale;
     p.bf16 = d.dtype == ATTN_BF16;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -183,6 +187,21 @@ attn_status attn_fwd_ws(const void *Q, const void *K, const void *V, const int32
         return ATTN_ERR_ALIAS;
     return run(Q, K, V, key_lengths, mask_kind, scale, out, dims, stream, ATTN_KERNEL_AUTO,
                static_cast<int *>(workspace));
+}
+
+attn_status attn_fwd_window(const void *Q, const void *K, const void *V, const int32_t *key_lengths, int mask_kind,
+                            int window, float scale, void *out, const attn_dims *dims, void *stream)
+{
+    if (!(mask_kind & ATTN_MASK_WINDOW))
+        return run(Q, K, V, key_lengths, mask_kind, scale, out, dims, stream, ATTN_KERNEL_AUTO, nullptr);
+    if (dims == nullptr) return ATTN_ERR_NULL;
+    if ((mask_kind & ~(ATTN_MASK_KEY_PADDING | ATTN_MASK_CAUSAL | ATTN_MASK_WINDOW)) != 0) return ATTN_ERR_MASK;
+    const attn_status st = validate(Q, K, V, key_lengths, mask_kind & ~ATTN_MASK_WINDOW, scale, out, dims);
+    if (st != ATTN_OK) return st;
+    if (dims->m != dims->n) return ATTN_ERR_SHAPE; // self-attention: queries and keys share positions
+    if (window < 0) return ATTN_ERR_VALUE;
+    return run(Q, K, V, key_lengths, mask_kind, scale, out, dims, stream, ATTN_KERNEL_AUTO, nullptr, nullptr,
+               window);
 }
 
 attn_status attn_fwd(const void *Q, const void *K, const void *V, const int32_t *key_lengths, int mask_kind,

@@ -117,6 +117,7 @@ struct FlashParams {
     const int32_t *key_lengths;
     __nv_bfloat16 *out;
     float *lse; // per-row log-sum-exp of the scaled scores (natural log), or nullptr
+    int window; // restricted attention: keys with |i - j| <= window stay; -1: no window
     int BH, h, m, n, mask_kind;
     float scale_log2;
     int pair_mode;
@@ -129,7 +130,8 @@ struct Tile {
     int bh[kSlots];
     int q0[kSlots];
     int kv_len[kSlots]; // keys allowed by padding (n without padding)
-    int n_kv[kSlots];   // key tiles to process (0: nothing allowed or slot unused)
+    int kv_lo[kSlots];  // first key tile to process (0 without a window)
+    int n_kv[kSlots];   // end of the key tiles to process (n_kv <= kv_lo: nothing allowed or slot unused)
     bool active[kSlots];
     bool shared_kv;
 };
@@ -179,6 +181,7 @@ __device__ __forceinline__ Tile decode_tile(const FlashParams &p, int t)
     for (int s = 0; s < kSlots; ++s) {
         T.active[s] = T.bh[s] < p.BH && T.q0[s] < p.m;
         T.kv_len[s] = 0;
+        T.kv_lo[s] = 0;
         T.n_kv[s] = 0;
         if (!T.active[s]) continue;
         int len = p.n;
@@ -186,9 +189,16 @@ __device__ __forceinline__ Tile decode_tile(const FlashParams &p, int t)
             len = __ldg(p.key_lengths + T.bh[s] / p.h);
             len = len < 0 ? 0 : (len > p.n ? p.n : len);
         }
-        const int lim = causal ? min(len, T.q0[s] + kBM) : len;
+        int lim = causal ? min(len, T.q0[s] + kBM) : len;
+        int lo = 0;
+        if (p.window >= 0) {
+            // keys within `window` of some row q0 .. min(m, q0 + 128) - 1 of the tile
+            lo = max(0, T.q0[s] - p.window) / kBN;
+            lim = min(lim, min(p.m, T.q0[s] + kBM) + p.window);
+        }
         T.kv_len[s] = len;
-        T.n_kv[s] = (lim + kBN - 1) / kBN;
+        T.kv_lo[s] = lo;
+        T.n_kv[s] = max(lo, (lim + kBN - 1) / kBN);
     }
     return T;
 }
@@ -281,11 +291,26 @@ __device__ __forceinline__ StagePos ring_pos(bool pair_mode, int ring, uint32_t 
     return {static_cast<uint32_t>(ring) * kHalf + fill % kHalf, (fill / kHalf) & 1u};
 }
 
+// Pair mode: the key tiles loaded for the CTA tile, [shared_lo, shared_hi): the
+// union of the two slots' ranges (a slot with nothing to do adds nothing).
+__device__ __forceinline__ int shared_lo(const Tile &T)
+{
+    const bool e0 = T.n_kv[0] <= T.kv_lo[0], e1 = T.n_kv[1] <= T.kv_lo[1];
+    return e0 ? (e1 ? 0 : T.kv_lo[1]) : (e1 ? T.kv_lo[0] : min(T.kv_lo[0], T.kv_lo[1]));
+}
+
+__device__ __forceinline__ int shared_hi(const Tile &T)
+{
+    const bool e0 = T.n_kv[0] <= T.kv_lo[0], e1 = T.n_kv[1] <= T.kv_lo[1];
+    return e0 ? (e1 ? 0 : T.n_kv[1]) : (e1 ? T.n_kv[0] : max(T.n_kv[0], T.n_kv[1]));
+}
+
 // Fills of slot s's ring that CTA tile T takes.
 __device__ __forceinline__ uint32_t fills_of(const Tile &T, int s)
 {
-    // a select, not T.n_kv[s]: a runtime index would put the tile on the stack
-    return static_cast<uint32_t>(T.shared_kv ? max(T.n_kv[0], T.n_kv[1]) : (s ? T.n_kv[1] : T.n_kv[0]));
+    // selects, not T.n_kv[s]: a runtime index would put the tile on the stack
+    if (T.shared_kv) return static_cast<uint32_t>(shared_hi(T) - shared_lo(T));
+    return static_cast<uint32_t>(s ? T.n_kv[1] - T.kv_lo[1] : T.n_kv[0] - T.kv_lo[0]);
 }
 
 // ------------------------------------------------------------------ roles
@@ -305,18 +330,20 @@ __device__ __forceinline__ void load_role(SharedStorage &sm, const FlashParams &
         const Tile T = decode_tile(p, t);
 #pragma unroll
         for (int s = 0; s < kSlots; ++s) {
-            if (T.n_kv[s] == 0) continue;
+            if (T.n_kv[s] <= T.kv_lo[s]) continue;
             if (!(ok = wait_bar(&sm.q_empty[s], (q_cnt[s] & 1) ^ 1, &sm.abort_flag, kSiteLoadQEmpty))) break;
             mbar_arrive_expect_tx(&sm.q_full[s], kTileBytes);
             tma_load_3d(sm.q[s], tm_q, &sm.q_full[s], 0, T.q0[s], T.bh[s]);
             ++q_cnt[s];
         }
-        const int J = max(T.n_kv[0], T.n_kv[1]);
-        for (int j = 0; j < J && ok; ++j) {
+        // pair mode: each key tile of the union once (both slots read it); split mode:
+        // each slot's own range into its own ring, the slots interleaved
+        const int J0 = T.shared_kv ? shared_lo(T) : min(T.kv_lo[0], T.kv_lo[1]);
+        const int J = T.shared_kv ? shared_hi(T) : max(T.n_kv[0], T.n_kv[1]);
+        for (int j = J0; j < J && ok; ++j) {
 #pragma unroll
             for (int s = 0; s < kSlots; ++s) {
-                if (j >= T.n_kv[s]) continue;
-                if (T.shared_kv && s == 1 && j < T.n_kv[0]) continue; // slot 1 reads slot 0's stage
+                if (T.shared_kv ? s == 1 : (j < T.kv_lo[s] || j >= T.n_kv[s])) continue;
                 const int ring = T.shared_kv ? 0 : s;
                 const StagePos sp = ring_pos(p.pair_mode, ring, ring ? fill1 : fill0);
                 if (!(ok = wait_bar(&sm.kv_empty[sp.st], sp.phase ^ 1, &sm.abort_flag, kSiteLoadKvEmpty))) break;
@@ -380,15 +407,27 @@ __device__ __forceinline__ void mma_role(SharedStorage &sm, const FlashParams &p
         const int t = feed.consume(sm, p, ok, false);
         if (t < 0) break;
         const Tile T = decode_tile(p, t);
-        const int n = s ? T.n_kv[1] : T.n_kv[0];
+        const int lo = s ? T.kv_lo[1] : T.kv_lo[0];
+        const int n = max(0, (s ? T.n_kv[1] : T.n_kv[0]) - lo);
+        // fill of this slot's first key tile; pair mode: stages of the union that
+        // precede this slot's range are only acknowledged (below)
+        const int J0 = T.shared_kv ? shared_lo(T) : lo;
         if (n > 0) {
             ok = wait_bar(q_full, q_cnt & 1, ab, kSiteMmaQFull);
             ++q_cnt;
         }
+        if (ok && T.shared_kv) {
+            for (int j = J0; j < lo && ok && n > 0; ++j) {
+                const StagePos sp = ring_pos(p.pair_mode, s, fill_base + static_cast<uint32_t>(j - J0));
+                ok = wait_bar(&sm.kv_full[sp.st], sp.phase, ab, kSiteMmaKvFull);
+                if (ok) mbar_arrive(&sm.kv_empty[sp.st]);
+            }
+        }
+        const uint32_t own_base = fill_base + static_cast<uint32_t>(n > 0 ? lo - J0 : 0);
         for (int j = 0; j <= n && ok; ++j) {
             if (j < n) {
                 // S(j)
-                const StagePos sp = ring_pos(p.pair_mode, s, fill_base + j);
+                const StagePos sp = ring_pos(p.pair_mode, s, own_base + j);
                 ok = wait_bar(&sm.kv_full[sp.st], sp.phase, ab, kSiteMmaKvFull);
                 if (ok) ok = wait_bar(s_free, (s_cnt & 1) ^ 1, ab, kSiteMmaSFree);
                 if (!ok) break;
@@ -417,7 +456,7 @@ __device__ __forceinline__ void mma_role(SharedStorage &sm, const FlashParams &p
                     ++o_cnt;
                     tc_fence_after();
                 }
-                const uint32_t st = ring_pos(p.pair_mode, s, fill_base + jp).st;
+                const uint32_t st = ring_pos(p.pair_mode, s, own_base + jp).st;
                 const uint32_t vd = v_lo + st * (kTileBytes >> 4);
                 // keys 16kk..16kk+15 per step: P columns 8kk.. (two bf16 per column), V rows
                 // 16kk.. (2 KiB = 128 descriptor units)
@@ -435,10 +474,12 @@ __device__ __forceinline__ void mma_role(SharedStorage &sm, const FlashParams &p
             }
         }
         if (ok && T.shared_kv) {
-            // stages of this CTA tile that only the other slot reads: arrive once each is loaded
-            const int J = max(T.n_kv[0], T.n_kv[1]);
-            for (int j = n; j < J && ok; ++j) {
-                const StagePos sp = ring_pos(p.pair_mode, s, fill_base + j);
+            // stages of this CTA tile that only the other slot reads: arrive once each
+            // is loaded (in fill order: after this slot's own range, or all of them
+            // when this slot has nothing to do)
+            const int J = shared_hi(T);
+            for (int j = n > 0 ? lo + n : J0; j < J && ok; ++j) {
+                const StagePos sp = ring_pos(p.pair_mode, s, fill_base + static_cast<uint32_t>(j - J0));
                 ok = wait_bar(&sm.kv_full[sp.st], sp.phase, ab, kSiteMmaKvFull);
                 if (ok) mbar_arrive(&sm.kv_empty[sp.st]);
             }
@@ -504,11 +545,11 @@ __device__ __forceinline__ float weights_bf16(const float (&x)[kBN], bool presca
 // Scores of query row i of head bh against keys key0 .. key0+127, recomputed on
 // the CUDA cores from Q and K in global memory (fp32 sums of exact bf16
 // products), multiplied by scale * log2 e, and -inf where not allowed (column c
-// is allowed iff c < cnt; allowed keys are below n).  Rows past m read as zero
+// is allowed iff cnt_lo <= c < cnt; allowed keys are below n).  Rows past m read as zero
 // queries, as the TMA loads fill them.  Taken only when a tile's exponentials
 // against the running reference overflowed, so it favours size over speed.
-__device__ __forceinline__ void recompute_scores(const FlashParams &p, int bh, int i, int key0, int cnt,
-                                                 float (&x)[kBN])
+__device__ __forceinline__ void recompute_scores(const FlashParams &p, int bh, int i, int key0, int cnt_lo,
+                                                 int cnt, float (&x)[kBN])
 {
     const bool row_in = i < p.m;
     const __nv_bfloat16 *qr = p.q + (static_cast<size_t>(bh) * p.m + (row_in ? i : 0)) * kD;
@@ -519,7 +560,7 @@ __device__ __forceinline__ void recompute_scores(const FlashParams &p, int bh, i
 #pragma unroll 1
     for (int c = 0; c < kBN; ++c) {
         float v = -CUDART_INF_F;
-        if (c < cnt) {
+        if (c < cnt && c >= cnt_lo) {
             const __nv_bfloat16 *kr = p.k + (static_cast<size_t>(bh) * p.n + key0 + c) * kD;
             float a = 0.f;
 #pragma unroll
@@ -532,6 +573,9 @@ __device__ __forceinline__ void recompute_scores(const FlashParams &p, int bh, i
     for (int c = 0; c < kBN; ++c) x[c] = srow[c];
 }
 
+// kWindow: the launch has a restricted-attention window (compiled separately so
+// that launches without one run none of its bound arithmetic).
+template <bool kWindow>
 __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParams &p, const CUtensorMap *tm_o,
                                              uint32_t tmem, int slot)
 {
@@ -542,6 +586,7 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
     const uint32_t t_p = tmem + lane_base + slot * kSlotCols + kColP;
     const uint32_t t_o = tmem + lane_base + slot * kSlotCols + kColO;
     const bool causal = (p.mask_kind & kMaskCausal) != 0;
+    const int win = kWindow ? p.window : -1;
     const float sl2 = p.scale_log2;
     int *ab = &sm.abort_flag;
     uint32_t s_cnt = 0, pv_cnt = 0, epi_cnt = 0;
@@ -559,11 +604,12 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
         if (!active) continue;
         const int q0 = slot ? T.q0[1] : T.q0[0];
         const int bh = slot ? T.bh[1] : T.bh[0];
+        const int kv_lo = slot ? T.kv_lo[1] : T.kv_lo[0];
         const int n_kv = slot ? T.n_kv[1] : T.n_kv[0];
         const int kv_len = slot ? T.kv_len[1] : T.kv_len[0];
         const int i = q0 + row;
         __nv_bfloat16 *orow = p.out + (static_cast<size_t>(bh) * p.m + i) * kD;
-        if (n_kv == 0) { // no allowed key for any row of this tile: output 0
+        if (n_kv <= kv_lo) { // no allowed key for any row of this tile: output 0
             if (i < p.m) {
                 uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
@@ -574,7 +620,7 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
         }
         float m_run = -CUDART_INF_F; // running max, log2 units, as used for the exponentials
         float l_run = 0.f;           // running sum of exponentials relative to m_run
-        for (int j = 0; j < n_kv; ++j) {
+        for (int j = kv_lo; j < n_kv; ++j) {
             ok = warp_all(wait_bar(&sm.s_full[slot], s_cnt & 1, ab, kSiteSmSFull));
             if (!ok) break;
             ++s_cnt;
@@ -589,10 +635,18 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
             mbar_arrive(&sm.s_free[slot]); // S may be overwritten by the next Q K^T
 
             const int key0 = j * kBN;
-            // keys allowed for row i are exactly those below one bound (the padded
-            // length, and i + 1 for a causal mask): column c is allowed iff c < cnt
-            const int cnt = (causal ? min(kv_len, i + 1) : kv_len) - key0;
-            const bool boundary = (key0 + kBN > kv_len) || (causal && key0 + kBN - 1 > q0);
+            // keys allowed for row i are exactly those in one range [lo_i, hi_i): below
+            // the padded length (and i + 1 for a causal mask), and within `win` of i
+            // for a window; column c of the tile is allowed iff cnt_lo <= c < cnt
+            int hi_i = causal ? min(kv_len, i + 1) : kv_len;
+            int lo_i = 0;
+            if (kWindow) {
+                hi_i = min(hi_i, i + win + 1);
+                lo_i = i - win;
+            }
+            const int cnt = hi_i - key0, cnt_lo = lo_i - key0;
+            const bool boundary = (key0 + kBN > kv_len) || (causal && key0 + kBN - 1 > q0) ||
+                                  (kWindow && (key0 < q0 + kBM - 1 - win || key0 + kBN - 1 > q0 + win));
             float x[kBN];
 #pragma unroll
             for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(sr[c]);
@@ -600,7 +654,8 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
             if (boundary) {
                 // scale first, then mask: a zero scale must not turn -inf into NaN
 #pragma unroll
-                for (int c = 0; c < kBN; ++c) x[c] = c < cnt ? x[c] * sl2 : -CUDART_INF_F;
+                for (int c = 0; c < kBN; ++c)
+                    x[c] = (c < cnt && (!kWindow || c >= cnt_lo)) ? x[c] * sl2 : -CUDART_INF_F;
             }
 
             // Reference for the exponentials.  The row max is taken only on the row's
@@ -632,12 +687,12 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
                     // units, or are not finite).  The scores have left the registers:
                     // recompute this row's from Q and K, already scaled and masked,
                     // and take their max.
-                    recompute_scores(p, bh, i, key0, cnt, x);
+                    recompute_scores(p, bh, i, key0, cnt_lo, cnt, x);
                     move_reference(x, true, sl2, m_run, m_use, alpha, grow);
                     tile_sum = weights_bf16(x, true, sl2, m_use, pk);
                 }
             }
-            if (j > 0) {
+            if (j > kv_lo) {
                 // P and O are still in use by the previous P V until it completes;
                 // waiting only now lets the exponentials above overlap with it
                 ok = warp_all(wait_bar(&sm.pv_done[slot], pv_cnt & 1, ab, kSiteSmPvDone));
@@ -645,7 +700,7 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
                 ++pv_cnt;
                 tc_fence_after();
             }
-            if (j > 0 && __any_sync(0xffffffffu, grow)) {
+            if (j > kv_lo && __any_sync(0xffffffffu, grow)) {
                 // move O to the new reference (rare: a large tile sum or a recomputation)
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
@@ -768,7 +823,10 @@ attn_flash_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // CTA-wide barrier (every thread arrives exactly once) and returns.
     if (warp < 4 * kSlots) {
         regs_increase<kSoftmaxRegs>();
-        softmax_role(sm, p, &tm_o, tmem, warp / 4);
+        if (p.window >= 0)
+            softmax_role<true>(sm, p, &tm_o, tmem, warp / 4);
+        else
+            softmax_role<false>(sm, p, &tm_o, tmem, warp / 4);
         tc_fence_before();
         __syncthreads();
         return;
@@ -839,6 +897,7 @@ cudaError_t launch_flash(const Problem &pb, bool pair_mode, int *tile_counter, c
     p.key_lengths = (pb.mask_kind & kMaskKeyPadding) ? pb.key_lengths : nullptr;
     p.out = static_cast<__nv_bfloat16 *>(pb.out);
     p.lse = pb.lse;
+    p.window = (pb.mask_kind & kMaskWindow) ? pb.window : -1;
     p.BH = BH;
     p.h = pb.h;
     p.m = pb.m;

@@ -37,7 +37,7 @@ template <typename T>
 __global__ void __launch_bounds__(kWarps * 32)
 attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ K, const T *__restrict__ V,
                  const int32_t *__restrict__ key_lengths, T *__restrict__ out, float *__restrict__ lse, int h,
-                 int m, int n, int d, int mask_kind, float scale_log2)
+                 int m, int n, int d, int mask_kind, int window, float scale_log2)
 {
     __shared__ float sq[kRows][kStride];
     __shared__ float sk[kKeys][kStride];
@@ -57,6 +57,11 @@ attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ K, const T *__re
     }
     int kv_end = kv_len;
     if (causal) kv_end = min(kv_end, min(q0 + kRows, m)); // keys beyond the last row are never allowed
+    int kv_begin = 0;
+    if (window >= 0) { // keys within `window` of some row of this block
+        kv_end = min(kv_end, min(q0 + kRows, m) + window);
+        kv_begin = max(0, q0 - window) / kKeys * kKeys;
+    }
 
     const T *Qh = Q + static_cast<size_t>(bh) * m * d;
     const T *Kh = K + static_cast<size_t>(bh) * n * d;
@@ -76,7 +81,7 @@ attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ K, const T *__re
         acc1[rr] = 0.f;
     }
 
-    for (int k0 = 0; k0 < kv_end; k0 += kKeys) {
+    for (int k0 = kv_begin; k0 < kv_end; k0 += kKeys) {
         __syncthreads();
         for (int t = threadIdx.x; t < kKeys * kDMax; t += blockDim.x) {
             int r = t / kDMax, c = t % kDMax;
@@ -93,7 +98,8 @@ attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ K, const T *__re
             const int i = q0 + r;
             float s = 0.f;
             for (int c = 0; c < d; ++c) s = fmaf(sq[r][c], sk[lane][c], s);
-            const bool allowed = (j < kv_len) && !(causal && j > i);
+            const bool allowed = (j < kv_len) && !(causal && j > i) &&
+                                 !(window >= 0 && (j < i - window || j > i + window));
             // scale folded with log2(e): exp(x) = exp2(x * log2 e)
             const float x = allowed ? s * scale_log2 : -CUDART_INF_F;
             float blk_max = x;
@@ -151,11 +157,12 @@ cudaError_t launch_simt(const Problem &p, cudaStream_t stream)
         attn_simt_kernel<__nv_bfloat16><<<grid, kWarps * 32, 0, stream>>>(
             static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.k),
             static_cast<const __nv_bfloat16 *>(p.v), p.key_lengths, static_cast<__nv_bfloat16 *>(p.out), p.lse, p.h,
-            p.m, p.n, p.d, p.mask_kind, scale_log2);
+            p.m, p.n, p.d, p.mask_kind, (p.mask_kind & kMaskWindow) ? p.window : -1, scale_log2);
     } else {
         attn_simt_kernel<float><<<grid, kWarps * 32, 0, stream>>>(
             static_cast<const float *>(p.q), static_cast<const float *>(p.k), static_cast<const float *>(p.v),
-            p.key_lengths, static_cast<float *>(p.out), p.lse, p.h, p.m, p.n, p.d, p.mask_kind, scale_log2);
+            p.key_lengths, static_cast<float *>(p.out), p.lse, p.h, p.m, p.n, p.d, p.mask_kind,
+            (p.mask_kind & kMaskWindow) ? p.window : -1, scale_log2);
     }
     return cudaGetLastError();
 }

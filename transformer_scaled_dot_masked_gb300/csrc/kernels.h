@@ -16,12 +16,13 @@ struct Problem {
     void *out;
     float *lse;                 // device [B][h][m] natural log of each row's softmax normaliser, or nullptr
     int B, h, m, n, d;
-    int mask_kind;  // bit 0 key padding, bit 1 causal
+    int mask_kind;  // bit 0 key padding, bit 1 causal, bit 2 window
+    int window = -1; // window half-width when bit 2 is set (keys with |i - j| <= window stay)
     float scale;    // >= 0
     bool bf16;      // element type of q, k, v, out (fp32 otherwise)
 };
 
-enum : int { kMaskKeyPadding = 1, kMaskCausal = 2 };
+enum : int { kMaskKeyPadding = 1, kMaskCausal = 2, kMaskWindow = 4 };
 
 // CUDA-core kernel: fp32 arithmetic, d <= 64, any m, n.
 cudaError_t launch_simt(const Problem &p, cudaStream_t stream);
