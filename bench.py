@@ -284,6 +284,33 @@ def backward_workload(torch, attn, device, peak_tf, steps=20):
             "calls_timed": steps, "algorithmic": "10*d_k FLOPs per allowed (query, key) pair"}
 
 
+def head_width_workloads(torch, attn, device, steps=50):
+    """The model variants that trade heads for head width at h * d_k = 512 (h=4 d_k=128,
+    h=16 d_k=32, h=32 d_k=16) on the encoder workload's shape (B64, n=m=100, key padding),
+    next to the base h=8 d_k=64.  Widths other than 64 run on the CUDA-core kernel."""
+    base = WORKLOADS[2]
+    res = {}
+    for h, d in ((8, 64), (4, 128), (16, 32), (32, 16)):
+        w = base.with_(h=h, d=d, scale=d ** -0.5, name=f"encoder_h{h}_d{d}")
+        inp = draw(w)
+        q, k, v = (to_device(x, w.dtype, torch, device) for x in (inp.q, inp.k, inp.v))
+        lens = torch.from_numpy(inp.key_lengths).to(device)
+        out = torch.empty_like(q)
+        stream = torch.cuda.current_stream(device)
+
+        def step():
+            attn.attn_fwd(q, k, v, lens, w.mask, w.scale, out=out, stream=stream)
+
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        ms = time_launches(step, steps, torch, stream)
+        kern = attn.select_kernel(w.B, w.h, w.m, w.n, w.d, 0, w.mask)
+        res[w.name] = {"kernel": attn._native.KERNEL_NAMES[kern], "us_per_launch": ms * 1e3,
+                       "tflops_useful": useful_flops(w, inp.key_lengths) / (ms * 1e-3) / 1e12}
+    return res
+
+
 def window_workload(torch, attn, device, peak_tf, steps=50, window=256):
     """Restricted self-attention on the long sequences of workload 5 without the causal
     mask: B4 h16 n=m=8192, keys with |i - j| <= 256 (513-position neighbourhoods), through
@@ -522,6 +549,7 @@ def main():
         result["backward"] = backward_workload(torch, attn, device, peak_tf)
         result["decode"] = decode_workload(torch, attn, device, peak_hbm)
         result["window"] = window_workload(torch, attn, device, peak_tf)
+        result["head_widths"] = head_width_workloads(torch, attn, device)
         if rank == 0:
             cb, _ = cpu_oracle_sample(w, inp, args.cpu_seconds)
             cb.pop("seconds", None)

@@ -84,7 +84,7 @@ typedef enum {
     ATTN_KERNEL_AUTO = 0,  /* let the library choose (what attn_fwd does) */
     ATTN_KERNEL_FLASH = 1, /* tcgen05/TMA flash kernel, 256 query rows per CTA tile (bf16, d_k == 64) */
     ATTN_KERNEL_SHORT = 2, /* same machinery, two heads per CTA tile, whole head resident (bf16, d_k == 64, m <= 128) */
-    ATTN_KERNEL_SIMT = 3   /* CUDA-core fp32 kernel (fp32 or bf16, d_k <= 64) */
+    ATTN_KERNEL_SIMT = 3   /* CUDA-core fp32 kernel (fp32 or bf16, d_k <= 128) */
 } attn_kernel;
 
 typedef struct {
@@ -92,7 +92,7 @@ typedef struct {
     int32_t h;     /* heads, >= 1 */
     int32_t m;     /* query rows per (batch, head), >= 1 */
     int32_t n;     /* key/value rows per (batch, head), >= 1 */
-    int32_t d_k;   /* head width (d_v == d_k), 1..64; the tensor-core kernels need 64 */
+    int32_t d_k;   /* head width (d_v == d_k), 1..128; the tensor-core kernels need 64 */
     int32_t dtype; /* attn_dtype */
 } attn_dims;
 

@@ -57,7 +57,8 @@ def test_kernel_selection():
     assert attn.select_kernel(1, 1, 16, 16, 64, f32, 0) == N.KERNEL_SIMT
     assert attn.select_kernel(1, 1, 16, 16, 32, bf, 0) == N.KERNEL_SIMT
     assert attn.select_kernel(1, 1, 16, 17, 64, bf, 2) == N.KERNEL_AUTO   # causal needs m == n
-    assert attn.select_kernel(1, 1, 16, 16, 65, bf, 0) == N.KERNEL_AUTO   # d_k > 64
+    assert attn.select_kernel(1, 1, 16, 16, 65, bf, 0) == N.KERNEL_SIMT   # d_k > 64: CUDA cores
+    assert attn.select_kernel(1, 1, 16, 16, 129, bf, 0) == N.KERNEL_AUTO  # d_k > 128
     assert attn.select_kernel(1, 1, 16, 16, 64, bf, 4) == N.KERNEL_AUTO   # unknown mask bit
     assert attn.select_kernel(0, 1, 16, 16, 64, bf, 0) == N.KERNEL_AUTO
 
@@ -76,7 +77,7 @@ def _call(q=A, k=B_, v=C, lens=L, mask=0, scale=0.125, out=O, dims=(2, 2, 8, 8, 
     (dict(q=None), 1), (dict(out=None), 1), (dict(lens=None, mask=1), 1),
     (dict(dims=(0, 2, 8, 8, 64, 0)), 2), (dict(dims=(2, 2, 8, 0, 64, 0)), 2),
     (dict(dims=(2, 2, 8, 9, 64, 0), mask=2), 2), (dict(dims=(70000, 1, 8, 8, 64, 0)), 2),
-    (dict(dims=(2, 2, 8, 8, 65, 0)), 3), (dict(dims=(2, 2, 8, 8, 0, 0)), 3), (dict(dims=(2, 2, 8, 8, 64, 7)), 3),
+    (dict(dims=(2, 2, 8, 8, 129, 0)), 3), (dict(dims=(2, 2, 8, 8, 0, 0)), 3), (dict(dims=(2, 2, 8, 8, 64, 7)), 3),
     (dict(mask=4), 4), (dict(mask=-1), 4),
     (dict(q=A + 8), 5), (dict(out=O + 4), 5), (dict(lens=L + 2, mask=1), 5),
     (dict(scale=float("nan")), 9), (dict(scale=float("inf")), 9), (dict(scale=-0.5), 9),

@@ -261,3 +261,21 @@ def test_no_writes_outside_out():
         out = buf[guard:guard + n_out].view(w.B, w.h, w.m, w.d)
         run(inp, kern, out=out)
         assert (buf[:guard] == -7.0).all() and (buf[guard + n_out:] == -7.0).all()
+
+
+# ---------------------------------------------------------------- other head widths
+WIDTHS = [
+    # the model variants that change d_k (h * d_k = 512): h=4 d_k=128, h=16 d_k=32, h=32 d_k=16
+    ("h4_d128_padding", "bf16", 4, 4, 100, 100, 128, MASK_KEY_PADDING, (10, 100)),
+    ("h16_d32_causal", "bf16", 4, 16, 128, 128, 32, MASK_CAUSAL, None),
+    ("h32_d16_cross", "bf16", 2, 32, 60, 90, 16, MASK_KEY_PADDING, (0, 90)),
+    ("fp32_d128_causal", "fp32", 2, 2, 70, 70, 128, MASK_CAUSAL, None),
+    ("fp32_d100_ragged", "fp32", 2, 3, 33, 47, 100, MASK_KEY_PADDING, (0, 47)),
+]
+
+
+@pytest.mark.parametrize("name,dtype,B,h,m,n,d,mask,lengths", WIDTHS, ids=[c[0] for c in WIDTHS])
+def test_head_widths(orc, name, dtype, B, h, m, n, d, mask, lengths):
+    w = Workload(name, dtype, B, h, m, n, d, mask, d ** -0.5, 61, lengths)
+    assert attn.select_kernel(B, h, m, n, d, 0 if dtype == "bf16" else 1, mask) == K_SIMT
+    check_full(orc, w, K_AUTO)

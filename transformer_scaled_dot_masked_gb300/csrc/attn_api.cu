@@ -34,7 +34,7 @@ attn_status validate_dims(const attn_dims *dims, int mask_kind, float scale)
     if ((mask_kind & ~(ATTN_MASK_KEY_PADDING | ATTN_MASK_CAUSAL)) != 0) return ATTN_ERR_MASK;
     const attn_dims &d = *dims;
     if (d.dtype != ATTN_BF16 && d.dtype != ATTN_FP32) return ATTN_ERR_DTYPE;
-    if (d.d_k < 1 || d.d_k > 64) return ATTN_ERR_DTYPE;
+    if (d.d_k < 1 || d.d_k > 128) return ATTN_ERR_DTYPE;
     if (d.B < 1 || d.h < 1 || d.m < 1 || d.n < 1) return ATTN_ERR_SHAPE;
     if (d.B > 65535 || d.h > 65535) return ATTN_ERR_SHAPE;                  // grid limits
     if ((mask_kind & ATTN_MASK_CAUSAL) && d.m != d.n) return ATTN_ERR_SHAPE; // queries and keys share positions

@@ -11,8 +11,9 @@
 // and is a plain baseline for the tensor-core kernel on bf16 inputs.
 //
 // Grid: (ceil(m / kRows), h, B); 128 threads = 4 warps; each warp owns
-// kRowsPerWarp query rows, and lane l owns output columns l and l + 32.
-// Key/value blocks of 32 rows are staged in shared memory as fp32.
+// kRowsPerWarp query rows, and lane l owns output columns l, l + 32, ... (up to
+// the instantiation's maximum head width, 64 or 128).  Key/value blocks of 32
+// rows are staged in shared memory as fp32.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -25,23 +26,25 @@ constexpr int kWarps = 4;
 constexpr int kRowsPerWarp = 4;
 constexpr int kRows = kWarps * kRowsPerWarp;
 constexpr int kKeys = 32;
-constexpr int kDMax = 64;
-constexpr int kStride = kDMax + 1; // padded row stride: lane-per-key reads hit distinct banks
+constexpr int kDMaxAll = 128; // widest head this kernel takes
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ void from_f32(float x, float *dst) { *dst = x; }
 __device__ __forceinline__ void from_f32(float x, __nv_bfloat16 *dst) { *dst = __float2bfloat16_rn(x); }
 
-template <typename T>
+// DMAX: maximum head width of the instantiation (64 or 128); d <= DMAX.
+template <typename T, int DMAX>
 __global__ void __launch_bounds__(kWarps * 32)
 attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ K, const T *__restrict__ V,
                  const int32_t *__restrict__ key_lengths, T *__restrict__ out, float *__restrict__ lse, int h,
                  int m, int n, int d, int mask_kind, int window, float scale_log2)
 {
+    constexpr int kStride = DMAX + 1; // padded row stride: lane-per-key reads hit distinct banks
+    constexpr int kCols = DMAX / 32;  // output columns per lane
     __shared__ float sq[kRows][kStride];
     __shared__ float sk[kKeys][kStride];
-    __shared__ float sv[kKeys][kDMax];
+    __shared__ float sv[kKeys][DMAX];
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -67,24 +70,24 @@ attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ K, const T *__re
     const T *Kh = K + static_cast<size_t>(bh) * n * d;
     const T *Vh = V + static_cast<size_t>(bh) * n * d;
 
-    for (int t = threadIdx.x; t < kRows * kDMax; t += blockDim.x) {
-        int r = t / kDMax, c = t % kDMax;
+    for (int t = threadIdx.x; t < kRows * DMAX; t += blockDim.x) {
+        int r = t / DMAX, c = t % DMAX;
         sq[r][c] = (q0 + r < m && c < d) ? to_f32(Qh[static_cast<size_t>(q0 + r) * d + c]) : 0.f;
     }
 
-    float run_max[kRowsPerWarp], run_sum[kRowsPerWarp], acc0[kRowsPerWarp], acc1[kRowsPerWarp];
+    float run_max[kRowsPerWarp], run_sum[kRowsPerWarp], acc[kRowsPerWarp][kCols];
 #pragma unroll
     for (int rr = 0; rr < kRowsPerWarp; ++rr) {
         run_max[rr] = -CUDART_INF_F;
         run_sum[rr] = 0.f;
-        acc0[rr] = 0.f;
-        acc1[rr] = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < kCols; ++cc) acc[rr][cc] = 0.f;
     }
 
     for (int k0 = kv_begin; k0 < kv_end; k0 += kKeys) {
         __syncthreads();
-        for (int t = threadIdx.x; t < kKeys * kDMax; t += blockDim.x) {
-            int r = t / kDMax, c = t % kDMax;
+        for (int t = threadIdx.x; t < kKeys * DMAX; t += blockDim.x) {
+            int r = t / DMAX, c = t % DMAX;
             bool in = (k0 + r < n) && (c < d);
             sk[r][c] = in ? to_f32(Kh[static_cast<size_t>(k0 + r) * d + c]) : 0.f;
             sv[r][c] = in ? to_f32(Vh[static_cast<size_t>(k0 + r) * d + c]) : 0.f;
@@ -113,15 +116,17 @@ attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ K, const T *__re
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) blk_sum += __shfl_xor_sync(0xffffffffu, blk_sum, off);
             run_sum[rr] = run_sum[rr] * alpha + blk_sum;
-            float a0 = acc0[rr] * alpha, a1 = acc1[rr] * alpha;
+            float a[kCols];
+#pragma unroll
+            for (int cc = 0; cc < kCols; ++cc) a[cc] = acc[rr][cc] * alpha;
 #pragma unroll 8
             for (int jj = 0; jj < kKeys; ++jj) {
                 const float pj = __shfl_sync(0xffffffffu, p, jj);
-                a0 = fmaf(pj, sv[jj][lane], a0);
-                a1 = fmaf(pj, sv[jj][lane + 32], a1);
+#pragma unroll
+                for (int cc = 0; cc < kCols; ++cc) a[cc] = fmaf(pj, sv[jj][lane + 32 * cc], a[cc]);
             }
-            acc0[rr] = a0;
-            acc1[rr] = a1;
+#pragma unroll
+            for (int cc = 0; cc < kCols; ++cc) acc[rr][cc] = a[cc];
             run_max[rr] = new_max;
         }
     }
@@ -141,30 +146,38 @@ attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ K, const T *__re
         if (i >= m) continue;
         const float inv = run_sum[rr] > 0.f ? 1.f / run_sum[rr] : 0.f; // no allowed key -> 0
         T *o = out + (static_cast<size_t>(bh) * m + i) * d;
-        if (lane < d) from_f32(acc0[rr] * inv, o + lane);
-        if (lane + 32 < d) from_f32(acc1[rr] * inv, o + lane + 32);
+#pragma unroll
+        for (int cc = 0; cc < kCols; ++cc)
+            if (lane + 32 * cc < d) from_f32(acc[rr][cc] * inv, o + lane + 32 * cc);
     }
+}
+
+
+template <int DMAX>
+cudaError_t launch_simt_w(const Problem &p, cudaStream_t stream)
+{
+    const float scale_log2 = p.scale * 1.4426950408889634f;
+    const int win = (p.mask_kind & kMaskWindow) ? p.window : -1;
+    dim3 grid((p.m + kRows - 1) / kRows, p.h, p.B);
+    if (p.bf16) {
+        attn_simt_kernel<__nv_bfloat16, DMAX><<<grid, kWarps * 32, 0, stream>>>(
+            static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.k),
+            static_cast<const __nv_bfloat16 *>(p.v), p.key_lengths, static_cast<__nv_bfloat16 *>(p.out), p.lse, p.h,
+            p.m, p.n, p.d, p.mask_kind, win, scale_log2);
+    } else {
+        attn_simt_kernel<float, DMAX><<<grid, kWarps * 32, 0, stream>>>(
+            static_cast<const float *>(p.q), static_cast<const float *>(p.k), static_cast<const float *>(p.v),
+            p.key_lengths, static_cast<float *>(p.out), p.lse, p.h, p.m, p.n, p.d, p.mask_kind, win, scale_log2);
+    }
+    return cudaGetLastError();
 }
 
 } // namespace
 
 cudaError_t launch_simt(const Problem &p, cudaStream_t stream)
 {
-    if (p.d > kDMax) return cudaErrorInvalidValue;
-    const float scale_log2 = p.scale * 1.4426950408889634f;
-    dim3 grid((p.m + kRows - 1) / kRows, p.h, p.B);
-    if (p.bf16) {
-        attn_simt_kernel<__nv_bfloat16><<<grid, kWarps * 32, 0, stream>>>(
-            static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.k),
-            static_cast<const __nv_bfloat16 *>(p.v), p.key_lengths, static_cast<__nv_bfloat16 *>(p.out), p.lse, p.h,
-            p.m, p.n, p.d, p.mask_kind, (p.mask_kind & kMaskWindow) ? p.window : -1, scale_log2);
-    } else {
-        attn_simt_kernel<float><<<grid, kWarps * 32, 0, stream>>>(
-            static_cast<const float *>(p.q), static_cast<const float *>(p.k), static_cast<const float *>(p.v),
-            p.key_lengths, static_cast<float *>(p.out), p.lse, p.h, p.m, p.n, p.d, p.mask_kind,
-            (p.mask_kind & kMaskWindow) ? p.window : -1, scale_log2);
-    }
-    return cudaGetLastError();
+    if (p.d > kDMaxAll) return cudaErrorInvalidValue;
+    return p.d <= 64 ? launch_simt_w<64>(p, stream) : launch_simt_w<128>(p, stream);
 }
 
 } // namespace attn
