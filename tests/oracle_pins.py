@@ -469,6 +469,69 @@ def pin_window_torch_sdpa(o):
         np.testing.assert_allclose(got[live], ref[live], rtol=0, atol=1e-12)
 
 
+# ---------------------------------------------------------------- multi-head projections
+def pin_mha_two_head_example(o):
+    """The primer's two-head example through the projections: X_q = X_kv = I, head 1's
+    projections give the worked 2x2 example (Q = I, K = [[1,1],[1,-1]], V = [[5,0],[0,5]]),
+    head 2's are the same followed by the feature swap P, W^O = I: the output is the
+    printed concatenation (scale 1, printed precision)."""
+    from oracle import mha
+    g = _golden("worked_mha_2head.json")
+    I2, P = np.eye(2), np.array([[0.0, 1.0], [1.0, 0.0]])
+    K1, V1 = np.array([[1.0, 1.0], [1.0, -1.0]]), np.array([[5.0, 0.0], [0.0, 5.0]])
+    wq = np.hstack([I2, P])
+    wk = np.hstack([K1, K1 @ P])
+    wv = np.hstack([V1, V1 @ P])
+    out = mha.mha_fwd(o, I2[None], I2[None], wq, wk, wv, np.eye(4), 2, None, 0, 1.0)
+    np.testing.assert_allclose(out[0], g["printed"]["concat"], atol=g["printed"]["printed_precision"])
+
+
+def pin_mha_torch(o):
+    """torch's fp64 multi_head_attention_forward (separate projection weights, no biases,
+    boolean mask), against the same inputs."""
+    import torch
+    import torch.nn.functional as F
+    from oracle import mha
+
+    rng = np.random.default_rng(71)
+    B, m, n, h, dk = 2, 7, 9, 3, 4
+    dm = h * dk  # d_k = d_model / h, as on the pages (and as torch requires)
+    xq, xkv = rng.standard_normal((B, m, dm)), rng.standard_normal((B, n, dm))
+    wq, wk, wv = (rng.standard_normal((dm, h * dk)) / np.sqrt(dm) for _ in range(3))
+    wo = rng.standard_normal((h * dk, dm)) / np.sqrt(h * dk)
+    lens = np.array([4, 9], dtype=np.int32)
+    for mk in (0, PAD):
+        allow = np.ones((B, m, n), dtype=bool)
+        if mk & PAD:
+            allow &= np.arange(n)[None, None, :] < lens[:, None, None]
+        got = mha.mha_fwd(o, xq, xkv, wq, wk, wv, wo, h, lens, mk, dk ** -0.5)
+        for b in range(B):
+            t = lambda x: torch.from_numpy(np.ascontiguousarray(x))
+            ref, _ = F.multi_head_attention_forward(
+                t(xq[b][:, None]), t(xkv[b][:, None]), t(xkv[b][:, None]), dm, h,
+                in_proj_weight=None, in_proj_bias=None, bias_k=None, bias_v=None, add_zero_attn=False,
+                dropout_p=0.0, out_proj_weight=t(wo.T), out_proj_bias=None, training=False, need_weights=False,
+                attn_mask=t(~allow[b]), use_separate_proj_weight=True, q_proj_weight=t(wq.T),
+                k_proj_weight=t(wk.T), v_proj_weight=t(wv.T))
+            np.testing.assert_allclose(got[b], ref[:, 0].numpy(), rtol=0, atol=1e-12)
+
+
+def pin_mha_identity_projections(o):
+    """Identity projections and W^O: each head attends over its own column block of the
+    inputs, and the output is those heads side by side."""
+    from oracle import mha
+
+    rng = np.random.default_rng(72)
+    B, n, h, dk = 2, 6, 2, 3
+    x = rng.standard_normal((B, n, h * dk))
+    I = np.eye(h * dk)
+    out = mha.mha_fwd(o, x, x, I, I, I, I, h, None, CAUSAL, 0.6)
+    for head in range(h):
+        xs = x[:, None, :, head * dk:(head + 1) * dk]
+        np.testing.assert_allclose(out[:, :, head * dk:(head + 1) * dk],
+                                   brute.attention(xs, xs, xs, None, CAUSAL, 0.6)[:, 0], atol=1e-13)
+
+
 ALL_PINS = [
     pin_worked_example_printed,
     pin_worked_example_closed_form,
@@ -495,4 +558,7 @@ ALL_PINS = [
     pin_window_wide_equals_full,
     pin_window_locality,
     pin_window_torch_sdpa,
+    pin_mha_two_head_example,
+    pin_mha_torch,
+    pin_mha_identity_projections,
 ]

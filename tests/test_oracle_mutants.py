@@ -60,3 +60,33 @@ def test_mutant_is_caught(name, tmp_path):
         except AssertionError:
             caught.append(pin.__name__)
     assert caught, f"mutant {name} passed every pin"
+
+
+# Mistakes planted in the multi-head oracle (oracle/mha.py): the mutated function
+# replaces oracle.mha.mha_fwd while the multi-head pins run.
+MHA_MUTANTS = {
+    "interleaved_head_split": (".reshape(B, L, h, dk).transpose(0, 2, 1, 3)", ".reshape(B, L, dk, h).transpose(0, 3, 1, 2)"),
+    "output_projection_transposed": ("return concat @ wo", "return concat @ wo.T"),
+    "concat_in_head_order": ("concat = O.transpose(0, 2, 1, 3).reshape(B, m, hd)", "concat = O.reshape(B, m, hd)"),
+    "keys_projected_with_value_weights": ("K, V = heads(xq, wq, m), heads(xkv, wk, n), heads(xkv, wv, n)",
+                                          "K, V = heads(xq, wq, m), heads(xkv, wv, n), heads(xkv, wv, n)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MHA_MUTANTS))
+def test_mha_mutant_is_caught(name, monkeypatch, oracle_lib):
+    import oracle.mha as mha
+    old, new = MHA_MUTANTS[name]
+    src = open(mha.__file__).read()
+    assert src.count(old) == 1, f"mutation anchor {old!r} not found exactly once"
+    ns = {}
+    exec(compile(src.replace(old, new), "mha_mutant", "exec"), ns)
+    monkeypatch.setattr(mha, "mha_fwd", ns["mha_fwd"])
+    caught = []
+    for pin in (oracle_pins.pin_mha_two_head_example, oracle_pins.pin_mha_torch,
+                oracle_pins.pin_mha_identity_projections):
+        try:
+            pin(oracle_lib)
+        except Exception:  # a wrong shape is as much a catch as a wrong value
+            caught.append(pin.__name__)
+    assert caught, f"mutant {name} passed every pin"
