@@ -34,7 +34,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from workloads import DECODE, draw_dout, WORKLOADS, draw  # noqa: E402
+from workloads import DECODE, draw_dout, draw_mha, WORKLOADS, draw  # noqa: E402
 
 METRIC = "masked MHA fwd TFLOPS on 1 GB300 (and % of bf16 tensor peak / HBM GB/s)"
 UNIT = "TFLOPS"
@@ -282,6 +282,43 @@ def backward_workload(torch, attn, device, peak_tf, steps=20):
             "forward_with_lse_us": ms_f * 1e3,
             "training_pass_tflops": 3.5 * useful_flops(w, inp.key_lengths) / ((ms_b + ms_f) * 1e-3) / 1e12,
             "calls_timed": steps, "algorithmic": "10*d_k FLOPs per allowed (query, key) pair"}
+
+
+def mha_workload(torch, attn, device, peak_tf, steps=50):
+    """Multi-head self-attention with its projections for the big model's width (d_model
+    1024, h = 16, d_k = 64): B32 sentences of 256 positions with key padding (lengths in
+    [128, 256]), through attn_mha_fwd (three input projections, attention, output
+    projection).  Useful work: 2*B*L*d_model*h*64 FLOPs per projection (four of them)
+    plus 4*d_k per allowed (query, key) pair."""
+    B, h, L, dm = 32, 16, 256, 1024
+    xq, _, wq, wk, wv, wo = draw_mha(B, h, L, L, dm, seed=1007, self_attention=True)
+    lens_np = np.random.default_rng(1008).integers(128, 257, size=B).astype(np.int32)
+    dev = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+    x, Wq, Wk, Wv, Wo = dev(xq), dev(wq), dev(wk), dev(wv), dev(wo)
+    lens = torch.from_numpy(lens_np).to(device)
+    out = torch.empty_like(x)
+    ws = torch.empty(attn.mha_workspace_size(B, h, L, L, dm), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        attn.attn_mha_fwd(x, x, Wq, Wk, Wv, Wo, h, lens, attn.MASK_KEY_PADDING, 0.125, out=out, workspace=ws,
+                          stream=stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    ms = time_launches(step, steps, torch, stream)
+    st, info = attn.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} (info {info}) after the multi-head loop")
+    proj = 4 * 2.0 * B * L * dm * h * 64
+    att = 4 * 64 * float(np.clip(lens_np, 0, L).sum()) * L * h
+    return {"workload": f"multi-head self-attention with projections, bf16, B={B} L={L} d_model={dm} h={h}, "
+                        "key padding with lengths in [128,256]",
+            "entry_point": "attn_mha_fwd", "us_per_call": ms * 1e3,
+            "tflops_useful": (proj + att) / (ms * 1e-3) / 1e12,
+            "frac_of_peak": (proj + att) / (ms * 1e-3) / 1e12 / peak_tf, "calls_timed": steps,
+            "algorithmic": "4 projections of 2*B*L*d_model*h*64 FLOPs + 4*d_k per allowed pair"}
 
 
 def head_width_workloads(torch, attn, device, steps=50):
@@ -550,6 +587,7 @@ def main():
         result["decode"] = decode_workload(torch, attn, device, peak_hbm)
         result["window"] = window_workload(torch, attn, device, peak_tf)
         result["head_widths"] = head_width_workloads(torch, attn, device)
+        result["mha"] = mha_workload(torch, attn, device, peak_tf)
         if rank == 0:
             cb, _ = cpu_oracle_sample(w, inp, args.cpu_seconds)
             cb.pop("seconds", None)

@@ -309,6 +309,51 @@ attn_status attn_decode(const void *Q, const void *K, const void *V, const int32
                         float scale, void *out, float *lse, const attn_dims *dims,
                         void *workspace, size_t workspace_bytes, void *stream);
 
+/* Shapes of a multi-head attention call with its projections (d_k = d_v = 64). */
+typedef struct {
+    int32_t B;       /* batch */
+    int32_t h;       /* heads; h * 64 must be a multiple of 128 */
+    int32_t m;       /* query positions */
+    int32_t n;       /* key/value positions */
+    int32_t d_model; /* model width, a multiple of 128 */
+} attn_mha_dims;
+
+/* Bytes of device workspace attn_mha_fwd needs (host only, no CUDA call); 0 if
+ * attn_mha_fwd would reject the dims. */
+size_t attn_mha_workspace_size(const attn_mha_dims *dims);
+
+/*
+ * Multi-head attention with its projections ("Paper Deep Reading", §04; the
+ * slide deck's "Multi-Head Attention" slide):
+ *
+ *     head_i = Attention(Xq W_i^Q, Xkv W_i^K, Xkv W_i^V),
+ *     out    = Concat(head_1, ..., head_h) W^O,
+ *
+ * with d_k = d_v = 64 and no bias terms (the formula has none); Attention is
+ * attn_fwd's (mask and scale as there).  All tensors bf16, row-major, in device
+ * memory of the current device, 16-byte aligned:
+ *   Xq   [B][m][d_model], Xkv [B][n][d_model] (pass Xq for self-attention)
+ *   Wq, Wk, Wv  [d_model][h * 64]: head i uses columns 64i .. 64i+63
+ *   Wo   [h * 64][d_model]: head i's output multiplies rows 64i .. 64i+63
+ *   out  [B][m][d_model]
+ *   workspace  attn_mha_workspace_size(dims) bytes (Q, K, V and the heads'
+ *              outputs in [B][h][len][64]), 256-byte aligned, any contents
+ * Five kernels are enqueued: three projections into the head-split layout
+ * (tcgen05 GEMMs whose epilogues write each 64-column block as one head), the
+ * attention, and the output projection, which reads the heads' outputs as its K
+ * dimension directly (the concatenation costs no copy).
+ *
+ * Errors: NULL pointers (ATTN_ERR_NULL), bad shapes or h * 64 or d_model not
+ * multiples of 128, causal with m != n (ATTN_ERR_SHAPE), mask bits other than
+ * KEY_PADDING and CAUSAL (ATTN_ERR_MASK), unaligned pointers (ATTN_ERR_ALIGN),
+ * bad scale (ATTN_ERR_VALUE), a workspace too small (ATTN_ERR_SHAPE), out or the
+ * workspace overlapping an input or each other (ATTN_ERR_ALIAS), CUDA errors.
+ */
+attn_status attn_mha_fwd(const void *Xq, const void *Xkv, const void *Wq, const void *Wk,
+                         const void *Wv, const void *Wo, const int32_t *key_lengths,
+                         int mask_kind, float scale, void *out, const attn_mha_dims *dims,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
 /* The kernel attn_fwd would run for these dims and mask (host only, no CUDA call);
  * ATTN_KERNEL_AUTO (0) if the call would be rejected. */
 int attn_select_kernel(const attn_dims *dims, int mask_kind);

@@ -187,3 +187,21 @@ def test_window_mask_validation():
     d2 = N.make_dims(2, 2, 8, 9, 64, 0)
     assert N.fwd_window_raw(A, B_, C, None, N.MASK_WINDOW, 3, 0.125, O, d2, None) == 2  # m != n
     assert N.fwd_window_raw(A + 8, B_, C, None, N.MASK_WINDOW, 3, 0.125, O, d, None) == 5
+
+
+def _call_mha(dims=(2, 2, 8, 8, 128), mask=0, lens=None, ws=0xE000000, ws_bytes=None, **kw):
+    ws_bytes = N.mha_workspace_size(*dims) if ws_bytes is None else ws_bytes
+    a = dict(xq=A, xkv=B_, wq=C, wk=0x7000000, wv=0x8000000, wo=0x9000000, out=O)
+    a.update(kw)
+    return N.mha_raw(a["xq"], a["xkv"], a["wq"], a["wk"], a["wv"], a["wo"], lens, mask, 0.125, a["out"], *dims,
+                     ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(xq=None), 1), (dict(wo=None), 1), (dict(ws=None), 1), (dict(mask=1), 1),
+    (dict(dims=(2, 3, 8, 8, 128)), 2), (dict(dims=(2, 2, 8, 8, 96)), 2), (dict(dims=(2, 2, 8, 9, 128), mask=2), 2),
+    (dict(ws_bytes=16), 2), (dict(mask=4), 4), (dict(wq=C + 8), 5), (dict(ws=0xE000000 + 16), 5),
+    (dict(out=B_), 10), (dict(ws=0x9000000), 10),
+])
+def test_mha_rejects_bad_arguments(kwargs, status):
+    assert _call_mha(**kwargs) == status

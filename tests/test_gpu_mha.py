@@ -1,0 +1,54 @@
+"""Multi-head attention with projections (attn_mha_fwd) against the fp64 MultiHead oracle.
+
+Tolerance 2e-2 absolute, from the arithmetic: Q, K, V and the heads' outputs are
+rounded to bf16 (2^-9 relative each) and the attention stays within its own
+1e-2 bar; W^O is drawn with variance 1/(h*64), so the output projection carries
+the per-feature errors over with unit gain (they add in quadrature over its
+h*64 inputs), plus the output's own bf16 rounding.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import mha
+import transformer_scaled_dot_masked_gb300 as attn
+from workloads import MASK_CAUSAL, MASK_KEY_PADDING, MASK_NONE, draw_mha
+
+from gpu_helpers import as_f64, report
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.load()
+
+
+def dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+CASES = [
+    # name, B, h, m, n, d_model, mask, self-attention, lengths (lo, hi)
+    ("base_encoder_padding", 3, 8, 100, 100, 512, MASK_KEY_PADDING, True, (10, 100)),
+    ("base_decoder_causal", 2, 8, 130, 130, 512, MASK_CAUSAL, True, None),
+    ("big_cross_padding", 2, 16, 128, 160, 1024, MASK_KEY_PADDING, False, (40, 160)),
+    ("two_heads_long", 1, 2, 700, 700, 128, MASK_NONE, True, None),
+]
+
+
+@pytest.mark.parametrize("name,B,h,m,n,dm,mask,selfattn,lengths", CASES, ids=[c[0] for c in CASES])
+def test_mha_matches_oracle(orc, name, B, h, m, n, dm, mask, selfattn, lengths):
+    xq, xkv, wq, wk, wv, wo = draw_mha(B, h, m, n, dm, seed=81, self_attention=selfattn)
+    lens = np.full(B, n, dtype=np.int32)
+    if lengths is not None:
+        lens = np.random.default_rng(82).integers(lengths[0], lengths[1] + 1, size=B).astype(np.int32)
+    out = attn.attn_mha_fwd(dev(xq), dev(xkv), dev(wq), dev(wk), dev(wv), dev(wo), h,
+                            torch.from_numpy(lens).cuda(), mask, 64 ** -0.5)
+    torch.cuda.synchronize()
+    st, info = attn.device_status()
+    assert st == 0, f"device status {st} (info {info})"
+    ref = mha.mha_fwd(orc, xq, xkv, wq, wk, wv, wo, h, lens, mask, 64 ** -0.5)
+    got = as_f64(out)
+    assert np.abs(got - ref).max() <= 2e-2, report(got, ref, 2e-2)

@@ -19,7 +19,7 @@ from . import _native
 from ._native import (AttnError, KERNEL_AUTO, KERNEL_FLASH, KERNEL_SHORT, KERNEL_SIMT, MASK_CAUSAL,
                       MASK_KEY_PADDING, MASK_NONE, MASK_WINDOW, DTYPE_BF16, DTYPE_FP32)
 
-__all__ = ["attn_fwd", "attn_fwd_window", "attn_fwd_lse", "MASK_WINDOW", "attn_bwd", "bwd_workspace_size", "attn_decode", "decode_workspace_size", "AttnError", "select_kernel", "device_status", "make_workspace", "workspace_size", "MASK_NONE", "MASK_KEY_PADDING",
+__all__ = ["attn_fwd", "attn_mha_fwd", "mha_workspace_size", "attn_fwd_window", "attn_fwd_lse", "MASK_WINDOW", "attn_bwd", "bwd_workspace_size", "attn_decode", "decode_workspace_size", "AttnError", "select_kernel", "device_status", "make_workspace", "workspace_size", "MASK_NONE", "MASK_KEY_PADDING",
            "MASK_CAUSAL", "KERNEL_AUTO", "KERNEL_FLASH", "KERNEL_SHORT", "KERNEL_SIMT"]
 
 
@@ -254,6 +254,45 @@ def attn_fwd_window(q, k, v, key_lengths=None, mask_kind: int = MASK_WINDOW, win
     dims = _native.make_dims(B, h, m, n, d, _dtype_code(q))
     st = _native.fwd_window_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), _lengths_ptr(key_lengths, mask_kind, B),
                                 mask_kind, window, scale, out.data_ptr(), dims, stream.cuda_stream)
+    if st != _native.ATTN_OK:
+        raise AttnError(st)
+    return out
+
+
+def mha_workspace_size(B, h, m, n, d_model) -> int:
+    """Bytes of device workspace ``attn_mha_fwd`` needs (0: shapes not supported)."""
+    return _native.mha_workspace_size(B, h, m, n, d_model)
+
+
+def attn_mha_fwd(xq, xkv, wq, wk, wv, wo, h: int, key_lengths=None, mask_kind: int = MASK_NONE,
+                 scale: Optional[float] = None, out=None, workspace=None, stream=None):
+    """Multi-head attention with its projections (bf16, d_k = 64, no biases).
+
+    xq [B, m, d_model], xkv [B, n, d_model]; wq, wk, wv [d_model, h * 64] (head i = columns
+    64i..64i+63); wo [h * 64, d_model].  Returns out [B, m, d_model] =
+    Concat(Attention(xq wq_i, xkv wk_i, xkv wv_i)) wo.
+    """
+    import torch
+    for t in (xq, xkv, wq, wk, wv, wo):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16:
+            raise ValueError("inputs must be contiguous bf16 CUDA tensors")
+    B, m, dm = xq.shape
+    n = xkv.shape[1]
+    if xkv.shape != (B, n, dm) or wq.shape != (dm, h * 64) or wk.shape != wq.shape or wv.shape != wq.shape \
+            or wo.shape != (h * 64, dm):
+        raise ValueError("shape mismatch between inputs, projections and h")
+    scale = 64 ** -0.5 if scale is None else scale
+    if out is None:
+        out = torch.empty_like(xq)
+    need = _native.mha_workspace_size(B, h, m, n, dm)
+    if need == 0:
+        raise AttnError(2)  # ATTN_ERR_SHAPE
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=xq.device)
+    stream = torch.cuda.current_stream(xq.device) if stream is None else stream
+    st = _native.mha_raw(xq.data_ptr(), xkv.data_ptr(), wq.data_ptr(), wk.data_ptr(), wv.data_ptr(), wo.data_ptr(),
+                         _lengths_ptr(key_lengths, mask_kind, B), mask_kind, scale, out.data_ptr(), B, h, m, n, dm,
+                         workspace.data_ptr(), workspace.numel() * workspace.element_size(), stream.cuda_stream)
     if st != _native.ATTN_OK:
         raise AttnError(st)
     return out

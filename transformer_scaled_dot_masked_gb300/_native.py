@@ -29,6 +29,11 @@ KERNEL_AUTO, KERNEL_FLASH, KERNEL_SHORT, KERNEL_SIMT = 0, 1, 2, 3
 KERNEL_NAMES = {KERNEL_AUTO: "auto", KERNEL_FLASH: "flash", KERNEL_SHORT: "short", KERNEL_SIMT: "simt"}
 
 
+class MhaDims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("h", ctypes.c_int32), ("m", ctypes.c_int32),
+                ("n", ctypes.c_int32), ("d_model", ctypes.c_int32)]
+
+
 class AttnDims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("h", ctypes.c_int32), ("m", ctypes.c_int32),
                 ("n", ctypes.c_int32), ("d_k", ctypes.c_int32), ("dtype", ctypes.c_int32)]
@@ -58,6 +63,11 @@ lib.attn_bwd.restype = ctypes.c_int
 lib.attn_fwd_window.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_float, _vp,
                                 ctypes.POINTER(AttnDims), _vp]
 lib.attn_fwd_window.restype = ctypes.c_int
+lib.attn_mha_workspace_size.argtypes = [ctypes.POINTER(MhaDims)]
+lib.attn_mha_workspace_size.restype = ctypes.c_size_t
+lib.attn_mha_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_float, _vp,
+                             ctypes.POINTER(MhaDims), _vp, ctypes.c_size_t, _vp]
+lib.attn_mha_fwd.restype = ctypes.c_int
 lib.attn_decode_workspace_size.argtypes = [ctypes.POINTER(AttnDims)]
 lib.attn_decode_workspace_size.restype = ctypes.c_size_t
 lib.attn_decode.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, ctypes.POINTER(AttnDims), _vp,
@@ -158,6 +168,19 @@ def decode_raw(q_ptr, k_ptr, v_ptr, lens_ptr, scale, out_ptr, lse_ptr, dims: Att
     """attn_decode with integer device pointers; returns the status code."""
     return lib.attn_decode(q_ptr, k_ptr, v_ptr, lens_ptr, float(scale), out_ptr, lse_ptr, ctypes.byref(dims),
                            ws_ptr, int(ws_bytes), stream_ptr)
+
+
+def mha_workspace_size(B, h, m, n, d_model) -> int:
+    d = MhaDims(int(B), int(h), int(m), int(n), int(d_model))
+    return int(lib.attn_mha_workspace_size(ctypes.byref(d)))
+
+
+def mha_raw(xq, xkv, wq, wk, wv, wo, lens_ptr, mask_kind, scale, out_ptr, B, h, m, n, d_model, ws_ptr, ws_bytes,
+            stream_ptr) -> int:
+    """attn_mha_fwd with integer device pointers; returns the status code."""
+    d = MhaDims(int(B), int(h), int(m), int(n), int(d_model))
+    return lib.attn_mha_fwd(xq, xkv, wq, wk, wv, wo, lens_ptr, int(mask_kind), float(scale), out_ptr,
+                            ctypes.byref(d), ws_ptr, int(ws_bytes), stream_ptr)
 
 
 def device_status(stream_ptr=None):

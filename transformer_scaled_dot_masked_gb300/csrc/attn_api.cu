@@ -371,6 +371,106 @@ attn_status attn_decode(const void *Q, const void *K, const void *V, const int32
                                                                                                   : ATTN_ERR_CUDA;
 }
 
+namespace {
+attn_status validate_mha_dims(const attn_mha_dims *d)
+{
+    if (d == nullptr) return ATTN_ERR_NULL;
+    if (d->B < 1 || d->h < 1 || d->m < 1 || d->n < 1 || d->d_model < 1) return ATTN_ERR_SHAPE;
+    if (d->B > 65535 || d->h > 65535 || (d->h * 64) % 128 != 0 || d->d_model % 128 != 0) return ATTN_ERR_SHAPE;
+    return ATTN_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+struct MhaLayout {
+    size_t q, k, v, o, total; // byte offsets in the workspace
+};
+
+MhaLayout mha_layout(const attn_mha_dims &d)
+{
+    const size_t BH = static_cast<size_t>(d.B) * d.h;
+    MhaLayout L;
+    L.q = 0;
+    L.k = L.q + align256(BH * d.m * 64 * 2);
+    L.v = L.k + align256(BH * d.n * 64 * 2);
+    L.o = L.v + align256(BH * d.n * 64 * 2);
+    L.total = L.o + align256(BH * d.m * 64 * 2);
+    return L;
+}
+} // namespace
+
+size_t attn_mha_workspace_size(const attn_mha_dims *dims)
+{
+    if (validate_mha_dims(dims) != ATTN_OK) return 0;
+    return mha_layout(*dims).total;
+}
+
+attn_status attn_mha_fwd(const void *Xq, const void *Xkv, const void *Wq, const void *Wk, const void *Wv,
+                         const void *Wo, const int32_t *key_lengths, int mask_kind, float scale, void *out,
+                         const attn_mha_dims *dims, void *workspace, size_t workspace_bytes, void *stream)
+{
+    attn_status st = validate_mha_dims(dims);
+    if (st != ATTN_OK) return st;
+    if (!Xq || !Xkv || !Wq || !Wk || !Wv || !Wo || !out || !workspace) return ATTN_ERR_NULL;
+    if ((mask_kind & ATTN_MASK_KEY_PADDING) && key_lengths == nullptr) return ATTN_ERR_NULL;
+    if ((mask_kind & ~(ATTN_MASK_KEY_PADDING | ATTN_MASK_CAUSAL)) != 0) return ATTN_ERR_MASK;
+    const attn_mha_dims &d = *dims;
+    if ((mask_kind & ATTN_MASK_CAUSAL) && d.m != d.n) return ATTN_ERR_SHAPE;
+    if (!std::isfinite(scale) || scale < 0.f) return ATTN_ERR_VALUE;
+    const void *ptrs[8] = {Xq, Xkv, Wq, Wk, Wv, Wo, out, workspace};
+    for (const void *q : ptrs)
+        if (!aligned(q, 16)) return ATTN_ERR_ALIGN;
+    if (!aligned(workspace, 256)) return ATTN_ERR_ALIGN;
+    if ((mask_kind & ATTN_MASK_KEY_PADDING) && !aligned(key_lengths, 4)) return ATTN_ERR_ALIGN;
+    const MhaLayout L = mha_layout(d);
+    if (workspace_bytes < L.total) return ATTN_ERR_SHAPE;
+    const uint64_t dm = d.d_model, hd = static_cast<uint64_t>(d.h) * 64;
+    const uint64_t xq = static_cast<uint64_t>(d.B) * d.m * dm * 2, xkv = static_cast<uint64_t>(d.B) * d.n * dm * 2;
+    const uint64_t wb = dm * hd * 2;
+    struct Span {
+        const void *p;
+        uint64_t n;
+    };
+    const Span ins[7] = {{Xq, xq}, {Xkv, xkv}, {Wq, wb}, {Wk, wb}, {Wv, wb}, {Wo, wb},
+                         {(mask_kind & ATTN_MASK_KEY_PADDING) ? key_lengths : nullptr, 4ull * d.B}};
+    for (const Span &in : ins)
+        if (overlaps(out, xq, in.p, in.n) || overlaps(workspace, L.total, in.p, in.n)) return ATTN_ERR_ALIAS;
+    if (overlaps(out, xq, workspace, L.total)) return ATTN_ERR_ALIAS;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    void *Q = ws + L.q, *K = ws + L.k, *V = ws + L.v, *O = ws + L.o;
+    attn::ProjProblem pp;
+    pp.B = d.B;
+    pp.h = d.h;
+    pp.mode = attn::kProjIn;
+    pp.K = d.d_model;
+    pp.N = d.h * 64;
+    const struct {
+        const void *x, *w;
+        void *o;
+        int L;
+    } ins_proj[3] = {{Xq, Wq, Q, d.m}, {Xkv, Wk, K, d.n}, {Xkv, Wv, V, d.n}};
+    for (const auto &ip : ins_proj) {
+        pp.a = ip.x;
+        pp.w = ip.w;
+        pp.out = ip.o;
+        pp.L = ip.L;
+        if (attn::launch_proj(pp, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    }
+    attn_dims ad{d.B, d.h, d.m, d.n, 64, ATTN_BF16};
+    st = run(Q, K, V, key_lengths, mask_kind, scale, O, &ad, stream, ATTN_KERNEL_AUTO, nullptr);
+    if (st != ATTN_OK) return st;
+    pp.mode = attn::kProjOut;
+    pp.a = O;
+    pp.w = Wo;
+    pp.out = out;
+    pp.L = d.m;
+    pp.K = d.h * 64;
+    pp.N = d.d_model;
+    return attn::launch_proj(pp, s) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 int attn_select_kernel(const attn_dims *dims, int mask_kind)
 {
     if (validate_dims(dims, mask_kind, 1.0f) != ATTN_OK) return ATTN_KERNEL_AUTO;
@@ -384,6 +484,13 @@ attn_status attn_device_status(void *stream, int32_t *info)
         return ATTN_ERR_CUDA;
     if (attn::bwd_status_read_and_clear(static_cast<cudaStream_t>(stream), &bcode, &bwhere) != cudaSuccess)
         return ATTN_ERR_CUDA;
+    uint32_t pcode = 0, pwhere = 0;
+    if (attn::proj_status_read_and_clear(static_cast<cudaStream_t>(stream), &pcode, &pwhere) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    if (code == 0 && bcode == 0 && pcode != 0) {
+        code = pcode;
+        where = 200 + pwhere; // projection wait sites are reported as 200 + site
+    }
     if (code == 0 && bcode != 0) {
         code = bcode;
         where = 100 + bwhere; // backward wait sites are reported as 100 + site

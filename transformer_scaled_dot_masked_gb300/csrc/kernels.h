@@ -47,6 +47,10 @@ cudaError_t launch_decode(const Problem &p, void *workspace, int sms, cudaStream
 // rows x 64 columns of one (b, h), 128-byte swizzle, rows past `rows` read as 0.
 bool encode_rows_map(CUtensorMap *map, const void *base, int rows, int BH);
 
+// [outer][rows][inner] bf16 as a 3-D TMA tensor (inner a multiple of 8); box =
+// box_rows rows x 64 elements of one outer index, 128-byte swizzle.
+bool encode_bf16_3d(CUtensorMap *map, const void *base, int inner, int rows, int outer, int box_rows);
+
 // [BH][rows][64] fp32 as a 3-D tensor for TMA reductions; box = 128 rows x 32
 // columns (one 128-byte swizzle span), 128-byte swizzle.
 bool encode_rows_map_f32(CUtensorMap *map, void *base, int rows, int BH);
@@ -68,6 +72,21 @@ struct BwdProblem {
 size_t bwd_workspace_bytes(int B, int h, int m);
 cudaError_t launch_bwd(const BwdProblem &p, cudaStream_t stream);
 cudaError_t bwd_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint32_t *info);
+
+// Projection GEMM of the multi-head wrapper (tcgen05).  kIn: out[b*h + j][t][:] =
+// row t of x[b] (a [B][L][K] bf16 tensor) times columns 64j .. 64j+63 of w
+// ([K][N] bf16, N = h * 64).  kOut: out[b][t][:] = sum over heads j of row t of
+// a[b*h + j] ([B*h][L][64]) times rows 64j .. 64j+63 of w ([h * 64][N]).
+enum ProjMode : int { kProjIn = 0, kProjOut = 1 };
+struct ProjProblem {
+    ProjMode mode;
+    const void *a;   // kIn: x [B][L][K]; kOut: heads [B*h][L][64]
+    const void *w;   // [K][N], K = d_model (kIn) or h * 64 (kOut)
+    void *out;       // kIn: [B*h][L][64]; kOut: [B][L][N]
+    int B, h, L, K, N;
+};
+cudaError_t launch_proj(const ProjProblem &p, cudaStream_t stream);
+cudaError_t proj_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint32_t *info);
 
 // Device status word of the flash kernel (bounded waits that gave up).
 cudaError_t flash_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint32_t *info);

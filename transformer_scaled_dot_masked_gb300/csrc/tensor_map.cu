@@ -46,6 +46,21 @@ bool encode_rows_map(CUtensorMap *map, const void *base, int rows, int BH)
     return r == CUDA_SUCCESS;
 }
 
+bool encode_bf16_3d(CUtensorMap *map, const void *base, int inner, int rows, int outer, int box_rows)
+{
+    auto enc = get_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(outer)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * 2, static_cast<cuuint64_t>(rows) * inner * 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool encode_rows_map_f32(CUtensorMap *map, void *base, int rows, int BH)
 {
     auto enc = get_encoder();
