@@ -86,7 +86,7 @@ def row_pairs(w, lengths, rows) -> float:
 # DRAM bytes (read + write) of one flash-kernel launch on the default workload,
 # from an ncu capture (profiles/attn_flash_long_causal_8192.md), keyed by a hash of
 # the kernel source it was taken on: any later change to the kernel reports null.
-MEASURED_TRAFFIC = {"dc3744e0ad1b41f5": 852619008 + 46486528}
+MEASURED_TRAFFIC = {"aa7c31b438ba1442": 850552320 + 46595584}
 
 
 def measured_traffic():

@@ -35,6 +35,7 @@ CASES = [
     ("base_decoder_causal", 2, 8, 130, 130, 512, MASK_CAUSAL, True, None),
     ("big_cross_padding", 2, 16, 128, 160, 1024, MASK_KEY_PADDING, False, (40, 160)),
     ("two_heads_long", 1, 2, 700, 700, 128, MASK_NONE, True, None),
+    ("six_heads_odd_column_tiles", 2, 6, 300, 300, 384, MASK_CAUSAL, True, None),
 ]
 
 

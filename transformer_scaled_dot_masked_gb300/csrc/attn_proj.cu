@@ -4,19 +4,22 @@
 // MultiHead equation: head_i = Attention(Q W_i^Q, K W_i^K, V W_i^V),
 // MultiHead = Concat(head_1, ..., head_h) W^O; no bias terms).
 //
-// One CTA computes a 128 x 128 tile of D = A B with fp32 accumulation in TMEM:
+// A persistent CTA per SM walks 128 x 256 tiles of D = A B (fp32 accumulation in
+// TMEM; a last tile of 128 columns when N is an odd multiple of 128):
 //   kProjIn   A = rows t0 .. t0+127 of x[b] ([B][L][K], K = d_model), B = columns
-//             n0 .. n0+127 of W ([K][h*64]); the tile is heads n0/64 and n0/64 + 1,
-//             stored straight into the head-split layout [B*h][L][64] (the
+//             n0 .. n0+255 of W ([K][h*64]); each 64-column block of the tile is one
+//             head, stored straight into the head-split layout [B*h][L][64] (the
 //             per-head W_i are column blocks of W).
 //   kProjOut  A = the heads' outputs [B*h][L][64]: the 64-wide K step j reads head
-//             j, so Concat needs no copy; B = columns n0 .. n0+127 of W^O
+//             j, so Concat needs no copy; B = columns n0 .. n0+255 of W^O
 //             ([h*64][N]); the tile goes to out[b] ([B][L][N]).
-// A tiles are K-major (64 bf16 = one 128-byte swizzle row per tile row), B tiles
-// 64 x 64 MN-major, loaded by TMA through a 4-stage ring; each 64-wide K step is
-// 4 x 2 MMAs of M128 N64 K16 into two 64-column accumulators.  The epilogue
-// converts to bf16 through a swizzled shared-memory tile and TMA stores (rows
-// past L are clipped).
+// A tiles are K-major (64 bf16 = one 128-byte swizzle row per tile row); B tiles
+// are 64 x 64 MN-major blocks, two side by side forming each N = 128 operand (the
+// descriptor's leading offset is the distance between them).  A 3-stage TMA ring
+// feeds 4 x 2 MMAs of M128 N128 K16 per 64-wide K step.  Two 256-column TMEM
+// accumulators alternate between tiles, so the epilogue of one tile (bf16 through
+// a swizzled shared-memory tile, TMA stores, rows past L clipped) runs while the
+// next tile accumulates.
 //
 // Warps: 0 TMA producer, 1 MMA issuer (and TMEM owner), 2-5 epilogue.  Every
 // mbarrier wait is bounded and reports through this file's status word.
@@ -36,20 +39,23 @@ __device__ unsigned int g_proj_status_info;
 
 namespace {
 
-constexpr int kTM = 128, kTN = 128, kTK = 64; // output tile and K step
-constexpr int kStages = 4;
+constexpr int kTM = 128, kTN = 256, kTK = 64; // output tile and K step
+constexpr int kStages = 3;
 constexpr int kThreads = 192;
 constexpr uint32_t kATile = kTM * kTK * 2;    // 16 KiB
-constexpr uint32_t kBHalf = kTK * 64 * 2;     // 8 KiB: 64 K rows x 64 N columns
-constexpr uint32_t kTmemCols = 128;
+constexpr uint32_t kBBlock = kTK * 64 * 2;    // 8 KiB: 64 K rows x 64 N columns
+constexpr uint32_t kTmemCols = 512;           // two 256-column accumulators
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr uint32_t kIdesc = idesc_bf16_f32(kTM, 64, 0, 1); // A K-major, B MN-major, N = 64
+constexpr uint32_t kIdesc = idesc_bf16_f32(kTM, 128, 0, 1); // A K-major, B MN-major, N = 128
 
 struct alignas(1024) ProjSmem {
     uint8_t a[kStages][kATile];
-    uint8_t b[kStages][2][kBHalf];
-    uint8_t stage[2][kTM * 64 * 2]; // bf16 output halves, 128-byte swizzle
-    uint64_t full[kStages], empty[kStages], acc_full, staged[2];
+    uint8_t b[kStages][4][kBBlock];
+    uint8_t stage[4][kTM * 64 * 2]; // bf16 output blocks of 64 columns, 128-byte swizzle
+    uint64_t full[kStages], empty[kStages];
+    uint64_t acc_full[2], acc_empty[2]; // accumulator a holds a finished tile / may be overwritten
+    uint64_t stage_free, staged[4];
+    uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -81,8 +87,24 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity)
 }
 
 struct ProjParams {
-    int mode, h, K;
+    int mode, h, K, N, B, m_tiles; // m_tiles: 128-row tiles per batch entry
+    int n_tiles, tiles;
 };
+
+struct TileId {
+    int b, t0, n0, ncols; // ncols: 256, or 128 for a last half tile
+};
+
+__device__ __forceinline__ TileId tile_id(const ProjParams &p, int t)
+{
+    TileId id;
+    const int nt = t % p.n_tiles, mi = t / p.n_tiles;
+    id.b = mi / p.m_tiles;
+    id.t0 = (mi % p.m_tiles) * kTM;
+    id.n0 = nt * kTN;
+    id.ncols = min(kTN, p.N - id.n0);
+    return id;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 attn_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
@@ -92,7 +114,6 @@ attn_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
     ProjSmem &sm = *reinterpret_cast<ProjSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                  ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x / 32;
-    const int n0 = blockIdx.x * kTN, t0 = blockIdx.y * kTM, b = blockIdx.z;
     const int ksteps = p.K / kTK;
     int *ab = &sm.abort_flag;
 
@@ -101,9 +122,13 @@ attn_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], 1);
         }
-        mbar_init(&sm.acc_full, 1);
-        mbar_init(&sm.staged[0], kTM);
-        mbar_init(&sm.staged[1], kTM);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&sm.acc_full[a], 1);
+            mbar_init(&sm.acc_empty[a], kTM);
+        }
+        mbar_init(&sm.stage_free, 1);
+        for (int q = 0; q < 4; ++q) mbar_init(&sm.staged[q], kTM);
+        mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -121,93 +146,129 @@ attn_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
         if (threadIdx.x == 0) {
             tma_prefetch_map(&tm_a);
             tma_prefetch_map(&tm_w);
-            int issued = 0;
-            for (int kk = 0; kk < ksteps; ++kk) {
-                const int s = kk % kStages;
-                if (!wait_bar(&sm.empty[s], ((kk / kStages) & 1) ^ 1, ab, 1)) break;
-                mbar_arrive_expect_tx(&sm.full[s], kATile + 2 * kBHalf);
-                if (p.mode == kProjIn)
-                    tma_load_3d(sm.a[s], &tm_a, &sm.full[s], kk * kTK, t0, b);
-                else
-                    tma_load_3d(sm.a[s], &tm_a, &sm.full[s], 0, t0, b * p.h + kk);
-                // W as a 2-D tensor (the third coordinate is 0)
-                tma_load_3d(sm.b[s][0], &tm_w, &sm.full[s], n0, kk * kTK, 0);
-                tma_load_3d(sm.b[s][1], &tm_w, &sm.full[s], n0 + 64, kk * kTK, 0);
-                ++issued;
+            uint32_t kc = 0, issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
+                const TileId id = tile_id(p, t);
+                const int blocks = id.ncols / 64;
+                for (int kk = 0; kk < ksteps; ++kk, ++kc) {
+                    const uint32_t s = kc % kStages;
+                    if (!(ok = wait_bar(&sm.empty[s], ((kc / kStages) & 1) ^ 1, ab, 1))) break;
+                    mbar_arrive_expect_tx(&sm.full[s], kATile + blocks * kBBlock);
+                    if (p.mode == kProjIn)
+                        tma_load_3d(sm.a[s], &tm_a, &sm.full[s], kk * kTK, id.t0, id.b);
+                    else
+                        tma_load_3d(sm.a[s], &tm_a, &sm.full[s], 0, id.t0, id.b * p.h + kk);
+                    // W as a 3-D tensor with one outer slice
+                    for (int q = 0; q < blocks; ++q)
+                        tma_load_3d(sm.b[s][q], &tm_w, &sm.full[s], id.n0 + 64 * q, kk * kTK, 0);
+                    ++issued;
+                }
             }
-            for (int kk = issued > kStages ? issued - kStages : 0; kk < issued; ++kk)
-                drain_wait(&sm.full[kk % kStages], (kk / kStages) & 1);
+            for (uint32_t c = issued > kStages ? issued - kStages : 0; c < issued; ++c)
+                drain_wait(&sm.full[c % kStages], (c / kStages) & 1);
         }
         __syncwarp();
     } else if (warp == 1) {
         if (threadIdx.x == 32) {
             const uint32_t desc_hi = static_cast<uint32_t>(smem_desc_sw128(0, 0, 1024) >> 32);
             const uint32_t a_lo = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.a[0]), 16, 1024));
-            const uint32_t b_lo = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.b[0][0]), kBHalf, 1024));
+            // N = 128 operands: two 64-column blocks kBBlock apart (the leading offset)
+            const uint32_t b_lo = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.b[0][0]), kBBlock, 1024));
+            uint32_t kc = 0;
             bool ok = true;
-            for (int kk = 0; kk < ksteps && ok; ++kk) {
-                const int s = kk % kStages;
-                if (!(ok = wait_bar(&sm.full[s], (kk / kStages) & 1, ab, 2))) break;
+            int i = 0;
+            for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x, ++i) {
+                const TileId id = tile_id(p, t);
+                const int a = i & 1;
+                // the epilogue has read this accumulator's previous tile
+                if (!(ok = wait_bar(&sm.acc_empty[a], ((i >> 1) & 1) ^ 1, ab, 2))) break;
                 tc_fence_after();
-                const uint32_t ad = a_lo + s * (kATile >> 4);
-                const uint32_t acc = kk > 0 ? 1u : 0u;
-#pragma unroll
-                for (int nh = 0; nh < 2; ++nh) {
-                    // A: 16 bf16 of K per step = 32 bytes; B: K rows 16kk.. = 2 KiB per step
-                    const uint32_t bd = b_lo + (s * 2 + nh) * (kBHalf >> 4);
-                    const uint32_t d = tmem + 64 * nh;
-                    mma_ss_k<0, 0>(d, ad, bd, desc_hi, kIdesc, acc);
-                    mma_ss_k<2, 128>(d, ad, bd, desc_hi, kIdesc, 1u);
-                    mma_ss_k<4, 256>(d, ad, bd, desc_hi, kIdesc, 1u);
-                    mma_ss_k<6, 384>(d, ad, bd, desc_hi, kIdesc, 1u);
+                for (int kk = 0; kk < ksteps; ++kk, ++kc) {
+                    const uint32_t s = kc % kStages;
+                    if (!(ok = wait_bar(&sm.full[s], (kc / kStages) & 1, ab, 3))) break;
+                    tc_fence_after();
+                    const uint32_t ad = a_lo + s * (kATile >> 4);
+                    const uint32_t acc = kk > 0 ? 1u : 0u;
+                    for (int nq = 0; nq < id.ncols / 128; ++nq) {
+                        // A: 16 bf16 of K per step = 32 bytes; B: K rows 16kk.. = 2 KiB per step
+                        const uint32_t bd = b_lo + (s * 4 + 2 * nq) * (kBBlock >> 4);
+                        const uint32_t d = tmem + 256 * a + 128 * nq;
+                        mma_ss_k<0, 0>(d, ad, bd, desc_hi, kIdesc, acc);
+                        mma_ss_k<2, 128>(d, ad, bd, desc_hi, kIdesc, 1u);
+                        mma_ss_k<4, 256>(d, ad, bd, desc_hi, kIdesc, 1u);
+                        mma_ss_k<6, 384>(d, ad, bd, desc_hi, kIdesc, 1u);
+                    }
+                    mma_commit(&sm.empty[s]);
                 }
-                mma_commit(&sm.empty[s]);
+                if (ok) mma_commit(&sm.acc_full[a]);
             }
-            // the epilogue waits on this (also after an abort: every MMA issued is complete)
-            mma_commit(&sm.acc_full);
+            if (!ok) {
+                // make sure no MMA is still writing TMEM when the CTA frees it
+                mma_commit(&sm.drain);
+                drain_wait(&sm.drain, 0);
+            }
         }
         __syncwarp();
     } else {
-        // epilogue: thread t = output row t of the tile (TMEM lane t)
-        const int t = (warp % 4) * 32 + threadIdx.x % 32;
+        // epilogue: thread r = output row r of the tile (TMEM lane r)
+        const int r = (warp % 4) * 32 + threadIdx.x % 32;
         const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
-        const bool ok = __all_sync(0xffffffffu, wait_bar(&sm.acc_full, 0, ab, 3));
-        if (ok && !*reinterpret_cast<volatile int *>(ab)) {
+        bool ok = true;
+        int i = 0;
+        for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x, ++i) {
+            const TileId id = tile_id(p, t);
+            const int a = i & 1;
+            ok = __all_sync(0xffffffffu, wait_bar(&sm.acc_full[a], (i >> 1) & 1, ab, 4));
+            if (!ok) break;
             tc_fence_after();
-#pragma unroll 1
-            for (int nh = 0; nh < 2; ++nh) {
-                uint32_t r[64];
-                tmem_ld32(tmem + lane_base + 64 * nh, r);
-                tmem_ld32(tmem + lane_base + 64 * nh + 32, r + 32);
+            // the staging blocks are rewritten only after the previous tile's stores read them
+            if (r == 0) {
+                bulk_wait_read_all();
+                mbar_arrive(&sm.stage_free);
+            }
+            ok = __all_sync(0xffffffffu, wait_bar(&sm.stage_free, i & 1, ab, 5));
+            if (!ok) break;
+            const int blocks = id.ncols / 64;
+            for (int q = 0; q < blocks; ++q) {
+                uint32_t v[64];
+                tmem_ld32(tmem + lane_base + 256 * a + 64 * q, v);
+                tmem_ld32(tmem + lane_base + 256 * a + 64 * q + 32, v + 32);
                 tmem_wait_ld();
-                reg_fence32(r);
-                reg_fence32(r + 32);
-                const uint32_t row = smem_addr(sm.stage[nh]) + t * 128;
+                reg_fence32(v);
+                reg_fence32(v + 32);
+                const uint32_t row = smem_addr(sm.stage[q]) + r * 128;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    uint4 v;
-                    v.x = pack_bf16x2(__uint_as_float(r[8 * c + 0]), __uint_as_float(r[8 * c + 1]));
-                    v.y = pack_bf16x2(__uint_as_float(r[8 * c + 2]), __uint_as_float(r[8 * c + 3]));
-                    v.z = pack_bf16x2(__uint_as_float(r[8 * c + 4]), __uint_as_float(r[8 * c + 5]));
-                    v.w = pack_bf16x2(__uint_as_float(r[8 * c + 6]), __uint_as_float(r[8 * c + 7]));
-                    st_shared_v4(row + ((c ^ (t & 7)) << 4), v);
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(v[8 * c + 0]), __uint_as_float(v[8 * c + 1]));
+                    w.y = pack_bf16x2(__uint_as_float(v[8 * c + 2]), __uint_as_float(v[8 * c + 3]));
+                    w.z = pack_bf16x2(__uint_as_float(v[8 * c + 4]), __uint_as_float(v[8 * c + 5]));
+                    w.w = pack_bf16x2(__uint_as_float(v[8 * c + 6]), __uint_as_float(v[8 * c + 7]));
+                    st_shared_v4(row + ((c ^ (r & 7)) << 4), w);
                 }
                 fence_proxy_async_shared();
-                mbar_arrive(&sm.staged[nh]);
+                mbar_arrive(&sm.staged[q]);
             }
-            if (t == 0) {
-#pragma unroll 1
-                for (int nh = 0; nh < 2; ++nh) {
-                    if (!wait_bar(&sm.staged[nh], 0, ab, 4)) break;
+            // a half tile leaves blocks 2 and 3 unused: arrive anyway, so every staged
+            // barrier completes one phase per tile and its parity follows the tile count
+            for (int q = blocks; q < 4; ++q) mbar_arrive(&sm.staged[q]);
+            // the accumulator is free for the tile after next
+            tc_fence_before();
+            mbar_arrive(&sm.acc_empty[a]);
+            if (r == 0) {
+                for (int q = 0; q < blocks && ok; ++q) {
+                    if (!(ok = wait_bar(&sm.staged[q], i & 1, ab, 6))) break;
                     if (p.mode == kProjIn)
-                        tma_store_3d(&tm_out, sm.stage[nh], 0, t0, b * p.h + n0 / 64 + nh);
+                        tma_store_3d(&tm_out, sm.stage[q], 0, id.t0, id.b * p.h + (id.n0 + 64 * q) / 64);
                     else
-                        tma_store_3d(&tm_out, sm.stage[nh], n0 + 64 * nh, t0, b);
+                        tma_store_3d(&tm_out, sm.stage[q], id.n0 + 64 * q, id.t0, id.b);
                 }
                 bulk_commit_group();
-                bulk_wait_all();
             }
+            ok = __all_sync(0xffffffffu, ok);
         }
+        if (r == 0) bulk_wait_all();
     }
     tc_fence_before();
     __syncthreads();
@@ -238,7 +299,7 @@ cudaError_t launch_proj(const ProjProblem &pp, cudaStream_t stream)
             configured[dev] = true;
         }
     }
-    if (pp.K % kTK != 0 || pp.N % kTN != 0) return cudaErrorInvalidValue;
+    if (pp.K % kTK != 0 || pp.N % 128 != 0) return cudaErrorInvalidValue;
     CUtensorMap ta, tw, to;
     const int BH = pp.B * pp.h;
     bool enc;
@@ -254,7 +315,14 @@ cudaError_t launch_proj(const ProjProblem &pp, cudaStream_t stream)
     p.mode = pp.mode;
     p.h = pp.h;
     p.K = pp.K;
-    const dim3 grid(pp.N / kTN, (pp.L + kTM - 1) / kTM, pp.B);
+    p.N = pp.N;
+    p.B = pp.B;
+    p.m_tiles = (pp.L + kTM - 1) / kTM;
+    p.n_tiles = (pp.N + kTN - 1) / kTN;
+    p.tiles = p.n_tiles * p.m_tiles * pp.B;
+    int sms = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const int grid = p.tiles < sms ? p.tiles : sms;
     attn_proj_kernel<<<grid, kThreads, kSmemBytes, stream>>>(ta, tw, to, p);
     return cudaGetLastError();
 }
