@@ -774,6 +774,10 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
     if (row == 0) bulk_wait_all();
 }
 
+// kWindow: compiled separately for launches with a restricted-attention window, so
+// each kernel holds only the softmax variant it runs (the short workloads are
+// dominated by cold first tiles, where instruction fetch counts).
+template <bool kWindow>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_flash_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -823,10 +827,7 @@ attn_flash_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // CTA-wide barrier (every thread arrives exactly once) and returns.
     if (warp < 4 * kSlots) {
         regs_increase<kSoftmaxRegs>();
-        if (p.window >= 0)
-            softmax_role<true>(sm, p, &tm_o, tmem, warp / 4);
-        else
-            softmax_role<false>(sm, p, &tm_o, tmem, warp / 4);
+        softmax_role<kWindow>(sm, p, &tm_o, tmem, warp / 4);
         tc_fence_before();
         __syncthreads();
         return;
@@ -879,7 +880,10 @@ cudaError_t launch_flash(const Problem &pb, bool pair_mode, int *tile_counter, c
         DeviceInfo &di = infos[dev];
         if (!di.configured) {
             if ((e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-            if ((e = cudaFuncSetAttribute(attn_flash_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if ((e = cudaFuncSetAttribute(attn_flash_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>(kSmemBytes))) != cudaSuccess)
+                return e;
+            if ((e = cudaFuncSetAttribute(attn_flash_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           static_cast<int>(kSmemBytes))) != cudaSuccess)
                 return e;
             di.configured = true;
@@ -909,7 +913,10 @@ cudaError_t launch_flash(const Problem &pb, bool pair_mode, int *tile_counter, c
     p.num_tiles = pair_mode ? BH * p.q_pairs : (BH + 1) / 2;
     p.tile_counter = tile_counter;
     const int grid = p.num_tiles < sms ? p.num_tiles : sms;
-    attn_flash_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, p);
+    if (p.window >= 0)
+        attn_flash_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, p);
+    else
+        attn_flash_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, p);
     return cudaGetLastError();
 }
 
