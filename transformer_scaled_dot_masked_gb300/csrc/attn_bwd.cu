@@ -27,16 +27,19 @@
 // takes the step's queries 32g .. 32g+31):
 //   MMA:      S^T = K_j Q_i^T, dP^T = V_j dO_i^T     (4 + 4 x M128 N128 K16, K-major)
 //   compute:  P^T = exp2(S^T scale log2 e - L_i), dS^T = P^T o (dP^T - D_i), masked;
-//             P^T and dS^T overwrite S^T and dP^T in TMEM as bf16 pairs, and dS is
-//             also written to shared memory as a K-major [query][key] tile
-//   MMA:      dV_j += P^T dO_i, dK_j += dS^T Q_i       (A from TMEM, B MN-major)
-//             dQ_i  = dS K_j                           (A K-major, B MN-major)
+//             P^T goes to TMEM as bf16 pairs, dS^T to shared memory as a K-major
+//             [key][query] tile (two buffers, alternating by step)
+//   MMA:      dV_j += P^T dO_i (A from TMEM), dK_j += dS^T Q_i (A K-major),
+//             dQ_i  = dS K_j (dS^T read as an MN-major A); B operands MN-major
 //   compute:  read dQ_i from TMEM (lane = query row), stage it in shared memory
 //             and add it to the accumulator with one TMA reduction per group
+// The steps overlap: S^T and dP^T are released as soon as every compute thread has
+// read them, so step i+1's scores are computed while step i's weights are; step
+// i's dQ is read out after step i+1's weights are written.
 // The epilogue writes dV_j and scale * dK_j as bf16.
 //
-// TMEM (512 columns): S^T/P^T [0,128), dP^T/dS^T [128,256), dV [256,320),
-// dK [320,384), dQ [384,448).
+// TMEM (512 columns): S^T [0,128), dP^T [128,256), dV [256,320), dK [320,384),
+// dQ [384,448), P^T [448,512).
 //
 // Every mbarrier wait is bounded; a wait that runs out sets the CTA's abort flag
 // and this file's device status word, and every role leaves its loop.
@@ -67,14 +70,16 @@ constexpr int kLoadWarp = kGroups * 4;
 constexpr int kMmaWarp = kLoadWarp + 1;
 constexpr uint32_t kTileBytes = kBM * kD * 2;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384, kColPT = 448;
 constexpr uint64_t kWaitLimitNs = 2000000000ull; // 2 s: far beyond any legitimate wait
 constexpr uint32_t kIdescNN = idesc_bf16_f32(kBM, kBM, 0, 0); // both operands K-major, N = 128
 constexpr uint32_t kIdescN64 = idesc_bf16_f32(kBM, kD, 0, 1); // B MN-major, N = 64
+constexpr uint32_t kIdescDQ = idesc_bf16_f32(kBM, kD, 1, 1);  // A and B MN-major, N = 64
 
 enum BwdSite : uint32_t {
     kSiteLoadQEmpty = 1, kSiteMmaKvFull, kSiteMmaQFull, kSiteMmaDqFull, kSiteMmaPReady, kSiteMmaDqFree,
-    kSiteCmpQFull, kSiteCmpSdpFull, kSiteCmpDqFull, kSiteCmpSLoaded, kSiteCmpDqsFree, kSiteCmpDqsFull
+    kSiteCmpQFull, kSiteCmpSdpFull, kSiteCmpDqFull, kSiteCmpSLoaded, kSiteCmpDqsFree, kSiteCmpDqsFull,
+    kSiteMmaSLoaded
 };
 
 struct alignas(1024) BwdSmem {
@@ -82,12 +87,14 @@ struct alignas(1024) BwdSmem {
     uint8_t v[kTileBytes];
     uint8_t q[kStages][kTileBytes];
     uint8_t dout[kStages][kTileBytes];
-    uint8_t ds[2][kTileBytes]; // dS [query][key] bf16, 128-byte swizzle: keys 0-63, keys 64-127
+    // dS^T [key][query] bf16 of steps with even / odd index, 128-byte swizzle, two
+    // blocks each: queries 0-63, queries 64-127
+    uint8_t dst[2][2][kTileBytes];
     uint8_t dq_stage[2][kBM * 32 * 4]; // dQ columns 0-31 / 32-63: 128 rows x 32 fp32, 128-byte swizzle
     float2 ld[kStages][kBM];    // (lse * log2 e, D) of the step's query rows
     uint64_t kv_full, q_full[kStages], q_empty[kStages];
     uint64_t sdp_full, p_ready, dq_full, dq_free;
-    uint64_t s_loaded; // every group has read its S^T and dP^T columns out of TMEM
+    uint64_t s_loaded; // every compute thread has read its S^T and dP^T columns out of TMEM
     uint64_t dqs_free[2], dqs_full[2]; // dq_stage[g] may be written / may be reduced into the accumulator
     uint64_t drain; // abort path only: completion of every MMA this CTA issued
     uint32_t tmem_base;
@@ -187,25 +194,20 @@ __device__ __forceinline__ void mma_role(BwdSmem &sm, uint32_t tmem, int steps)
     const uint32_t v_km = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.v), 16, 1024));
     const uint32_t q_km = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.q[0]), 16, 1024));
     const uint32_t do_km = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.dout[0]), 16, 1024));
-    const uint32_t ds_km = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.ds[0]), 16, 1024));
-    // the same tiles as MN-major B operands (rows are the reduction dimension)
+    const uint32_t dst_km = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.dst[0][0]), 16, 1024));
+    // the same tiles as MN-major operands (rows are the reduction dimension); dS^T
+    // read as dS: its two 64-query blocks are the two M atoms, one tile apart
     const uint32_t k_mn = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.k), kTileBytes, 1024));
     const uint32_t q_mn = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.q[0]), kTileBytes, 1024));
     const uint32_t do_mn = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.dout[0]), kTileBytes, 1024));
+    const uint32_t dst_mn = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.dst[0][0]), kTileBytes, 1024));
     constexpr uint32_t kStageUnits = kTileBytes >> 4; // descriptor units per stage
+    const uint32_t ts = tmem + kColS, tdp = tmem + kColDP;
+    const uint32_t tdv = tmem + kColDV, tdk = tmem + kColDK, tdq = tmem + kColDQ, tpt = tmem + kColPT;
 
-    bool ok = wait_bar(&sm.kv_full, 0, ab, kSiteMmaKvFull);
-    for (int t = 0; t < steps && ok; ++t) {
-        const int s = t % kStages;
-        const uint32_t su = static_cast<uint32_t>(s) * kStageUnits;
-        if (!(ok = wait_bar(&sm.q_full[s], (t / kStages) & 1, ab, kSiteMmaQFull))) break;
-        if (t > 0) {
-            // every MMA of the previous step has completed: P^T and dS^T were consumed
-            if (!(ok = wait_bar(&sm.dq_full, (t - 1) & 1, ab, kSiteMmaDqFull))) break;
-        }
-        tc_fence_after();
-        // S^T = K Q^T and dP^T = V dO^T: 16 of the 64 columns (32 bytes) per K step
-        const uint32_t ts = tmem + kColS, tdp = tmem + kColDP;
+    // S^T = K Q^T and dP^T = V dO^T of the step in stage s: 16 of the 64 columns
+    // (32 bytes) per K step
+    auto scores = [&](uint32_t su) {
         mma_ss_k<0, 0>(ts, k_km, q_km + su, desc_hi, kIdescNN, 0u);
         mma_ss_k<2, 2>(ts, k_km, q_km + su, desc_hi, kIdescNN, 1u);
         mma_ss_k<4, 4>(ts, k_km, q_km + su, desc_hi, kIdescNN, 1u);
@@ -215,49 +217,71 @@ __device__ __forceinline__ void mma_role(BwdSmem &sm, uint32_t tmem, int steps)
         mma_ss_k<4, 4>(tdp, v_km, do_km + su, desc_hi, kIdescNN, 1u);
         mma_ss_k<6, 6>(tdp, v_km, do_km + su, desc_hi, kIdescNN, 1u);
         mma_commit(&sm.sdp_full);
+    };
 
+    bool ok = wait_bar(&sm.kv_full, 0, ab, kSiteMmaKvFull);
+    if (ok) ok = wait_bar(&sm.q_full[0], 0, ab, kSiteMmaQFull);
+    if (ok) {
+        tc_fence_after();
+        scores(0);
+    }
+    for (int t = 0; t < steps && ok; ++t) {
+        const int s = t % kStages;
+        const uint32_t su = static_cast<uint32_t>(s) * kStageUnits;
+        if (t + 1 < steps) {
+            // the next step's scores as soon as every compute thread has read this
+            // step's out of TMEM: they run while this step's weights are computed
+            const int s1 = (t + 1) % kStages;
+            ok = wait_bar(&sm.s_loaded, t & 1, ab, kSiteMmaSLoaded);
+            if (ok) ok = wait_bar(&sm.q_full[s1], ((t + 1) / kStages) & 1, ab, kSiteMmaQFull);
+            if (!ok) break;
+            tc_fence_after();
+            scores(static_cast<uint32_t>(s1) * kStageUnits);
+        }
         if (!(ok = wait_bar(&sm.p_ready, t & 1, ab, kSiteMmaPReady))) break;
         tc_fence_after();
-        // dV += P^T dO, dK += dS^T Q: queries 16kk.. are TMEM columns 8kk.. (bf16
-        // pairs) and MN-major B rows 16kk.. (2 KiB = 128 descriptor units)
+        // dV += P^T dO (P^T in TMEM: queries 16kk.. are columns 8kk.., bf16 pairs),
+        // dK += dS^T Q (dS^T K-major in shared memory: queries 0-63 in the first
+        // block, 32 bytes per K step, 64-127 in the second, 16 KiB on); B operands
+        // MN-major, rows 16kk.. at 2 KiB = 128 descriptor units per K step
         const uint32_t acc = t > 0 ? 1u : 0u;
-        const uint32_t tdv = tmem + kColDV, tdk = tmem + kColDK;
-        const uint32_t tp = tmem + kColS, tds = tmem + kColDP;
         const uint32_t dob = do_mn + su, qb = q_mn + su;
-        mma_ts_k<0, 0>(tdv, tp, dob, desc_hi, kIdescN64, acc);
-        mma_ts_k<8, 128>(tdv, tp, dob, desc_hi, kIdescN64, 1u);
-        mma_ts_k<16, 256>(tdv, tp, dob, desc_hi, kIdescN64, 1u);
-        mma_ts_k<24, 384>(tdv, tp, dob, desc_hi, kIdescN64, 1u);
-        mma_ts_k<32, 512>(tdv, tp, dob, desc_hi, kIdescN64, 1u);
-        mma_ts_k<40, 640>(tdv, tp, dob, desc_hi, kIdescN64, 1u);
-        mma_ts_k<48, 768>(tdv, tp, dob, desc_hi, kIdescN64, 1u);
-        mma_ts_k<56, 896>(tdv, tp, dob, desc_hi, kIdescN64, 1u);
-        mma_ts_k<0, 0>(tdk, tds, qb, desc_hi, kIdescN64, acc);
-        mma_ts_k<8, 128>(tdk, tds, qb, desc_hi, kIdescN64, 1u);
-        mma_ts_k<16, 256>(tdk, tds, qb, desc_hi, kIdescN64, 1u);
-        mma_ts_k<24, 384>(tdk, tds, qb, desc_hi, kIdescN64, 1u);
-        mma_ts_k<32, 512>(tdk, tds, qb, desc_hi, kIdescN64, 1u);
-        mma_ts_k<40, 640>(tdk, tds, qb, desc_hi, kIdescN64, 1u);
-        mma_ts_k<48, 768>(tdk, tds, qb, desc_hi, kIdescN64, 1u);
-        mma_ts_k<56, 896>(tdk, tds, qb, desc_hi, kIdescN64, 1u);
+        const uint32_t du = static_cast<uint32_t>(t & 1) * (2 * kStageUnits); // dS^T buffer
+        const uint32_t dsk = dst_km + du, dsm = dst_mn + du;
+        mma_ts_k<0, 0>(tdv, tpt, dob, desc_hi, kIdescN64, acc);
+        mma_ts_k<8, 128>(tdv, tpt, dob, desc_hi, kIdescN64, 1u);
+        mma_ts_k<16, 256>(tdv, tpt, dob, desc_hi, kIdescN64, 1u);
+        mma_ts_k<24, 384>(tdv, tpt, dob, desc_hi, kIdescN64, 1u);
+        mma_ts_k<32, 512>(tdv, tpt, dob, desc_hi, kIdescN64, 1u);
+        mma_ts_k<40, 640>(tdv, tpt, dob, desc_hi, kIdescN64, 1u);
+        mma_ts_k<48, 768>(tdv, tpt, dob, desc_hi, kIdescN64, 1u);
+        mma_ts_k<56, 896>(tdv, tpt, dob, desc_hi, kIdescN64, 1u);
+        mma_ss_k<0, 0>(tdk, dsk, qb, desc_hi, kIdescN64, acc);
+        mma_ss_k<2, 128>(tdk, dsk, qb, desc_hi, kIdescN64, 1u);
+        mma_ss_k<4, 256>(tdk, dsk, qb, desc_hi, kIdescN64, 1u);
+        mma_ss_k<6, 384>(tdk, dsk, qb, desc_hi, kIdescN64, 1u);
+        mma_ss_k<1024, 512>(tdk, dsk, qb, desc_hi, kIdescN64, 1u);
+        mma_ss_k<1026, 640>(tdk, dsk, qb, desc_hi, kIdescN64, 1u);
+        mma_ss_k<1028, 768>(tdk, dsk, qb, desc_hi, kIdescN64, 1u);
+        mma_ss_k<1030, 896>(tdk, dsk, qb, desc_hi, kIdescN64, 1u);
+        // Q_i and dO_i are read by nothing after dV and dK: the stage can be refilled
+        mma_commit(&sm.q_empty[s]);
         if (t > 0) {
             // the compute warps have read the previous dQ out of TMEM
             if (!(ok = wait_bar(&sm.dq_free, (t - 1) & 1, ab, kSiteMmaDqFree))) break;
             tc_fence_after();
         }
-        // dQ = dS K: keys 0-63 in the first dS atom (32 bytes per K step), keys
-        // 64-127 in the second (16 KiB on); K_j rows 16kk.. as MN-major B
-        const uint32_t tdq = tmem + kColDQ;
-        mma_ss_k<0, 0>(tdq, ds_km, k_mn, desc_hi, kIdescN64, 0u);
-        mma_ss_k<2, 128>(tdq, ds_km, k_mn, desc_hi, kIdescN64, 1u);
-        mma_ss_k<4, 256>(tdq, ds_km, k_mn, desc_hi, kIdescN64, 1u);
-        mma_ss_k<6, 384>(tdq, ds_km, k_mn, desc_hi, kIdescN64, 1u);
-        mma_ss_k<1024, 512>(tdq, ds_km, k_mn, desc_hi, kIdescN64, 1u);
-        mma_ss_k<1026, 640>(tdq, ds_km, k_mn, desc_hi, kIdescN64, 1u);
-        mma_ss_k<1028, 768>(tdq, ds_km, k_mn, desc_hi, kIdescN64, 1u);
-        mma_ss_k<1030, 896>(tdq, ds_km, k_mn, desc_hi, kIdescN64, 1u);
-        mma_commit(&sm.q_empty[s]);
-        mma_commit(&sm.dq_full);
+        // dQ = dS K: dS^T read as an MN-major A (keys 16kk.. are rows 16kk.., 2 KiB
+        // per K step), K_j rows 16kk.. as MN-major B
+        mma_ss_k<0, 0>(tdq, dsm, k_mn, desc_hi, kIdescDQ, 0u);
+        mma_ss_k<128, 128>(tdq, dsm, k_mn, desc_hi, kIdescDQ, 1u);
+        mma_ss_k<256, 256>(tdq, dsm, k_mn, desc_hi, kIdescDQ, 1u);
+        mma_ss_k<384, 384>(tdq, dsm, k_mn, desc_hi, kIdescDQ, 1u);
+        mma_ss_k<512, 512>(tdq, dsm, k_mn, desc_hi, kIdescDQ, 1u);
+        mma_ss_k<640, 640>(tdq, dsm, k_mn, desc_hi, kIdescDQ, 1u);
+        mma_ss_k<768, 768>(tdq, dsm, k_mn, desc_hi, kIdescDQ, 1u);
+        mma_ss_k<896, 896>(tdq, dsm, k_mn, desc_hi, kIdescDQ, 1u);
+        mma_commit(&sm.dq_full); // every MMA of step t: P^T and dS^T consumed, dQ complete
     }
 }
 
@@ -265,6 +289,11 @@ __device__ __forceinline__ void mma_role(BwdSmem &sm, uint32_t tmem, int steps)
 // key tile for the score work on queries 32g .. 32g+31 of each step; query row t
 // and dQ columns 16g .. 16g+15 for the dQ readout; in the epilogue, columns
 // 32(g % 2) .. +31 of dV (g < 2) or dK (g >= 2) of key row t.
+//
+// Step t: read S^T, dP^T (releasing them for step t + 1's products), compute P^T
+// and dS^T, wait for step t - 1's products to finish with the previous P^T and
+// dS^T, write the new ones, then read out step t - 1's dQ (one step late, so that
+// no thread waits for the products of the step it has just fed).
 __device__ __forceinline__ void compute_role(BwdSmem &sm, const BwdParams &p, const CUtensorMap *tm_dq,
                                              uint32_t tmem, int bh, int key0, int len, int i_begin, int steps)
 {
@@ -274,19 +303,54 @@ __device__ __forceinline__ void compute_role(BwdSmem &sm, const BwdParams &p, co
     const int half = g / 2;              // dQ staging block (columns 32 * half ..)
     const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
     const uint32_t t_s = tmem + lane_base + kColS + 32 * g, t_dp = tmem + lane_base + kColDP + 32 * g;
+    const uint32_t t_pt = tmem + lane_base + kColPT + 16 * g;
     const uint32_t t_dq = tmem + lane_base + kColDQ + 16 * g;
     const bool causal = (p.mask_kind & kMaskCausal) != 0;
     const float sl2 = p.scale_log2;
     const int k = key0 + t;         // this thread's key
     const bool key_live = k < len;  // len <= n: keys past n (zero-filled rows) are never live
-    // dS[q][k] goes to row q of the atom holding key k: chunk (k % 64) / 8 of the
-    // row, swizzled with the row's low three bits
-    const uint32_t ds_col = smem_addr(sm.ds[t / 64]) + ((t % 64) % 8) * 2;
-    const uint32_t ds_chunk = (t % 64) / 8;
+    // dS^T row t (this thread's key), queries 32g .. 32g+31: four 16-byte chunks
+    // 4(g % 2) .. of the 128-byte row in block g / 2, swizzled with t % 8
+    const uint32_t dst_row0 = smem_addr(sm.dst[0][g / 2]) + t * 128;
     const uint32_t dqs_row = smem_addr(sm.dq_stage[half]) + t * 128; // this thread's staging row
     const bool dq_issuer = t == 0 && g % 2 == 0;
     int *ab = &sm.abort_flag;
     bool ok = true;
+
+    // dQ of step r into the accumulator: groups 2h and 2h+1 stage columns 32h ..
+    // 32h+31 (row t at t * 128 bytes, 16-byte chunk c at c ^ (t % 8): conflict-free)
+    // and one thread adds the block with a TMA reduction, which skips rows past m.
+    // The block is rewritten only after the previous reduction has read it.
+    auto dq_readout = [&](int r) -> bool {
+        uint32_t qr[16];
+        tmem_ld16(t_dq, qr);
+        tmem_wait_ld();
+        reg_fence16(qr);
+        tc_fence_before();
+        mbar_arrive(&sm.dq_free);
+        if (dq_issuer) {
+            bulk_wait_read_all();
+            mbar_arrive(&sm.dqs_free[half]);
+        }
+        bool good = warp_all(wait_bar(&sm.dqs_free[half], r & 1, ab, kSiteCmpDqsFree));
+        if (!good) return false;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int c4 = 4 * (g % 2) + j;
+            st_shared_v4(dqs_row + ((c4 ^ (t & 7)) << 4),
+                         make_uint4(qr[4 * j], qr[4 * j + 1], qr[4 * j + 2], qr[4 * j + 3]));
+        }
+        fence_proxy_async_shared();
+        mbar_arrive(&sm.dqs_full[half]);
+        if (dq_issuer) {
+            good = wait_bar(&sm.dqs_full[half], r & 1, ab, kSiteCmpDqsFull);
+            if (good) {
+                tma_reduce_add_3d(tm_dq, sm.dq_stage[half], 32 * half, (i_begin + r) * kBM, bh);
+                bulk_commit_group();
+            }
+        }
+        return warp_all(good);
+    };
 
     for (int st = 0; st < steps && ok; ++st) {
         const int s = st % kStages;
@@ -301,15 +365,14 @@ __device__ __forceinline__ void compute_role(BwdSmem &sm, const BwdParams &p, co
         const bool diag = causal && i0 == key0;
         const bool plain = __all_sync(0xffffffffu, key_live) && !diag;
         const uint32_t ldv = smem_addr(sm.ld[s]) + 32 * g * 8; // float2 (L, D) per query row
-        // P^T and dS^T of queries q go back to columns q / 2 (the layout the P V and
-        // dS^T Q products read), over scores another group may not have read yet:
-        // every group reads all its columns (s_loaded) before any group writes.
-        // The chunk is read and processed in two halves of 16 queries.
-        uint32_t pp[16], pd[16];
+        const uint32_t dst_row = dst_row0 + static_cast<uint32_t>(st & 1) * (2 * kTileBytes);
+        uint32_t pp[16], pd[4];
         // (L, D) of rows qq, qq + 1 in one 16-byte load, issued two pairs ahead
         float4 ldq[3];
         ldq[0] = ld_shared_f4_ordered(ldv);
         ldq[1] = ld_shared_f4_ordered(ldv + 16);
+        // the chunk is read and processed in two halves of 16 queries; every thread
+        // has read both when it releases S^T and dP^T
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             uint32_t sr[16], dr[16];
@@ -337,61 +400,35 @@ __device__ __forceinline__ void compute_role(BwdSmem &sm, const BwdParams &p, co
                 const float d0 = e0 * (__uint_as_float(dr[2 * v]) - ld.y);
                 const float d1 = e1 * (__uint_as_float(dr[2 * v + 1]) - ld.w);
                 pp[u] = pack_bf16x2(e0, e1);
-                pd[u] = pack_bf16x2(d0, d1);
-                // dS into shared memory, one bf16 per query row (ordered after the
-                // loads above but free of them otherwise; fence_proxy_async below
-                // publishes them)
-                st_shared_u16_ordered(ds_col + qq * 128 + ((ds_chunk ^ (qq & 7)) << 4),
-                                      static_cast<uint16_t>(pd[u]));
-                st_shared_u16_ordered(ds_col + (qq + 1) * 128 + ((ds_chunk ^ ((qq + 1) & 7)) << 4),
-                                      static_cast<uint16_t>(pd[u] >> 16));
+                pd[u % 4] = pack_bf16x2(d0, d1);
+                if (u % 4 == 3) {
+                    // dS^T buffer st % 2 was last read by step st - 2's products,
+                    // which completed before this thread wrote step st - 1's P^T
+                    const int c4 = 4 * (g % 2) + u / 4;
+                    st_shared_v4_ordered(dst_row + ((c4 ^ (t & 7)) << 4), make_uint4(pd[0], pd[1], pd[2], pd[3]));
+                }
             }
         }
-        ok = warp_all(wait_bar(&sm.s_loaded, st & 1, ab, kSiteCmpSLoaded));
-        if (!ok) break;
-        tc_fence_after();
-        tmem_st16(tmem + lane_base + kColS + 16 * g, pp);
-        tmem_st16(tmem + lane_base + kColDP + 16 * g, pd);
+        if (st > 0) {
+            // step st - 1's products have finished with P^T (and its dQ is ready)
+            ok = warp_all(wait_bar(&sm.dq_full, (st - 1) & 1, ab, kSiteCmpDqFull));
+            if (!ok) break;
+            tc_fence_after();
+        }
+        tmem_st16(t_pt, pp);
         tmem_wait_st();
         tc_fence_before();
         fence_proxy_async_shared();
         mbar_arrive(&sm.p_ready);
-
-        ok = warp_all(wait_bar(&sm.dq_full, st & 1, ab, kSiteCmpDqFull));
-        if (!ok) break;
-        tc_fence_after();
-        uint32_t qr[16];
-        tmem_ld16(t_dq, qr);
-        tmem_wait_ld();
-        reg_fence16(qr);
-        tc_fence_before();
-        mbar_arrive(&sm.dq_free);
-        // dQ part into the accumulator: groups 2h and 2h+1 stage columns 32h .. 32h+31
-        // (row t at t * 128 bytes, 16-byte chunk c at c ^ (t % 8): conflict-free) and
-        // one thread adds the block with a TMA reduction, which skips rows past m.
-        // The block is rewritten only after the previous reduction has read it.
-        if (dq_issuer) {
-            bulk_wait_read_all();
-            mbar_arrive(&sm.dqs_free[half]);
+        if (st > 0) ok = dq_readout(st - 1);
+    }
+    if (ok) {
+        // the last step's dQ; its completion also covers every earlier product
+        ok = warp_all(wait_bar(&sm.dq_full, (steps - 1) & 1, ab, kSiteCmpDqFull));
+        if (ok) {
+            tc_fence_after();
+            ok = dq_readout(steps - 1);
         }
-        ok = warp_all(wait_bar(&sm.dqs_free[half], st & 1, ab, kSiteCmpDqsFree));
-        if (!ok) break;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int c4 = 4 * (g % 2) + j;
-            st_shared_v4(dqs_row + ((c4 ^ (t & 7)) << 4),
-                         make_uint4(qr[4 * j], qr[4 * j + 1], qr[4 * j + 2], qr[4 * j + 3]));
-        }
-        fence_proxy_async_shared();
-        mbar_arrive(&sm.dqs_full[half]);
-        if (dq_issuer) {
-            ok = wait_bar(&sm.dqs_full[half], st & 1, ab, kSiteCmpDqsFull);
-            if (ok) {
-                tma_reduce_add_3d(tm_dq, sm.dq_stage[half], 32 * half, i0, bh);
-                bulk_commit_group();
-            }
-        }
-        ok = warp_all(ok);
     }
     // the staging blocks must stay valid, and the sums land, before the CTA exits
     if (dq_issuer) bulk_wait_all();

@@ -171,6 +171,13 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v)
                  : "memory");
 }
 
+// As st_shared_v4, but ordered only against other volatile asm (no memory clobber),
+// so loads issued ahead through ld_shared_f4_ordered are not held back.
+__device__ __forceinline__ void st_shared_v4_ordered(uint32_t addr, uint4 v)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
+}
+
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols)
 {
