@@ -31,7 +31,8 @@
  *
  * Ownership: the caller allocates and owns every buffer.  The library keeps
  * no per-call state and allocates no device memory; the only global state is
- * a small device status word that records a kernel giving up a bounded wait.
+ * a small device status word that records a kernel giving up a bounded wait,
+ * and the streams and events attn_fwd_host makes once per device.
  * attn_fwd_ws additionally takes a caller-owned workspace (see there).
  *
  * Asynchrony: every compute entry point only enqueues work on the given
@@ -197,6 +198,49 @@ attn_status attn_fwd_ws(const void *Q, const void *K, const void *V,
 attn_status attn_fwd_noalloc(const void *Q, const void *K, const void *V,
                              const int32_t *key_lengths, int mask_kind, float scale,
                              void *out, const attn_dims *dims, void *stream);
+
+/* Bytes of device workspace attn_fwd_host needs for `dims` (host only, no CUDA
+ * call): room for Q, K, V and out on the device, the key lengths and the tile
+ * counters.  0 when dims is NULL or invalid. */
+size_t attn_fwd_host_workspace_size(const attn_dims *dims);
+
+/*
+ * attn_fwd on HOST buffers: the same operation (the attention equation of
+ * "Paper Deep Reading: Attention Is All You Need", §04, with the mask M), with Q, K, V,
+ * key_lengths (int32 [B]) and out in host memory, laid out as for attn_fwd.
+ * The call copies the inputs to the device, runs the kernels and copies the
+ * output back, overlapping the three: the problem is cut into chunks of whole
+ * (batch, head) slices (whole batches, or a range of heads of one batch);
+ * chunk c's kernel starts as soon as its inputs are in, while later chunks'
+ * inputs are still being copied, and its output is copied back as soon as the
+ * kernel is done.  Page-locked host memory (cudaHostAlloc) lets the copies run
+ * asynchronously at full speed; pageable memory works, more slowly.
+ *
+ *   dev_workspace  device memory of at least attn_fwd_host_workspace_size(dims)
+ *                  bytes, 256-byte aligned, owned by the caller; it holds the
+ *                  device copies of the tensors for the duration of the call.
+ *   stream         caller's stream: the work is ordered after everything
+ *                  already enqueued on it, and everything enqueued on it later
+ *                  waits for the call's last copy back.  Internally the call
+ *                  uses streams and events of its own (made once per device on
+ *                  first use and kept for the life of the process).
+ *
+ * Asynchronous: returns once the work is enqueued; `out` holds the result once
+ * `stream` is synchronised.  The host buffers and the workspace must stay valid
+ * (and the inputs unchanged) until then.  Calls on different caller streams
+ * must use different workspaces.
+ *
+ * Errors: as attn_fwd for dims, mask_kind and scale; NULL tensor or workspace
+ * pointer (ATTN_ERR_NULL); workspace too small (ATTN_ERR_SHAPE) or not 256-byte
+ * aligned (ATTN_ERR_ALIGN); out overlapping an input (ATTN_ERR_ALIAS); a
+ * failing CUDA call (ATTN_ERR_CUDA; work enqueued before the failure may still
+ * run, and the caller's stream still waits for it).  Host pointers need no
+ * particular alignment.
+ */
+attn_status attn_fwd_host(const void *Q, const void *K, const void *V,
+                          const int32_t *key_lengths, int mask_kind, float scale,
+                          void *out, const attn_dims *dims, void *dev_workspace,
+                          size_t dev_workspace_bytes, void *stream);
 
 /*
  * attn_fwd that also writes each query row's log-sum-exp,

@@ -115,6 +115,44 @@ def test_workspace_validation():
     assert _call_ws(q=A + 8) == 5             # tensor checks still apply
 
 
+# ---------------------------------------------------------------- host buffers
+def _host_size(B, h, m, n, d, dtype):
+    """The device workspace attn_fwd_host needs: Q, K, V, out (each rounded up to
+    256 bytes), the int32 lengths (rounded up to 256) and two 256-byte tile counters."""
+    r = lambda x: (x + 255) // 256 * 256
+    esz = 2 if dtype == 0 else 4
+    return 2 * r(B * h * m * d * esz) + 2 * r(B * h * n * d * esz) + r(4 * B) + 2 * 256
+
+
+def test_host_workspace_size():
+    for dims in [(2, 3, 300, 200, 64, 0), (1, 1, 1, 1, 1, 1), (9, 2, 100, 100, 64, 0), (3, 4, 37, 53, 3, 1)]:
+        assert N.host_workspace_size(N.make_dims(*dims)) == _host_size(*dims)
+    assert N.host_workspace_size(N.make_dims(0, 3, 300, 200, 64, 0)) == 0      # bad dims
+    assert N.host_workspace_size(N.make_dims(2, 3, 300, 200, 200, 0)) == 0     # d_k too wide
+
+
+def _call_host(ws=0x6000000, ws_bytes=None, mask=0, lens=None, **kw):
+    dims = kw.pop("dims", (2, 2, 8, 8, 64, 0))
+    d = N.make_dims(*dims)
+    ws_bytes = _host_size(*dims) if ws_bytes is None else ws_bytes
+    return N.fwd_host_raw(kw.get("q", A), B_, C, lens, mask, kw.get("scale", 0.125), kw.get("out", O), d, ws,
+                          ws_bytes, None)
+
+
+def test_host_validation():
+    assert _call_host(ws=None) == 1                       # workspace NULL
+    assert _call_host(q=None) == 1                        # tensor NULL
+    assert _call_host(mask=1) == 1                        # padding without lengths
+    assert _call_host(ws_bytes=_host_size(2, 2, 8, 8, 64, 0) - 1) == 2
+    assert _call_host(ws=0x6000000 + 16) == 5             # workspace not 256-byte aligned
+    assert _call_host(out=A + 64) == 10                   # out inside Q
+    assert _call_host(out=L - 8, mask=1, lens=L) == 10    # out over the lengths
+    assert _call_host(dims=(2, 2, 8, 9, 64, 0), mask=2) == 2   # causal with m != n
+    assert _call_host(mask=8) == 4                        # unknown mask bit
+    assert _call_host(scale=float("nan")) == 9
+    assert _call_host(dims=(2, 2, 8, 8, 64, 7)) == 3      # unknown dtype
+
+
 # ---------------------------------------------------------------- forward with lse, backward
 LSE, DO, OUT2, DQ, DK, DV, WS = 0x7000000, 0x8000000, 0x9000000, 0xA000000, 0xB000000, 0xC000000, 0xD000000
 

@@ -19,7 +19,7 @@ from . import _native
 from ._native import (AttnError, KERNEL_AUTO, KERNEL_FLASH, KERNEL_SHORT, KERNEL_SIMT, MASK_CAUSAL,
                       MASK_KEY_PADDING, MASK_NONE, MASK_WINDOW, DTYPE_BF16, DTYPE_FP32)
 
-__all__ = ["attn_fwd", "attn_mha_fwd", "mha_workspace_size", "attn_fwd_window", "attn_fwd_lse", "MASK_WINDOW", "attn_bwd", "bwd_workspace_size", "attn_decode", "decode_workspace_size", "AttnError", "select_kernel", "device_status", "make_workspace", "workspace_size", "MASK_NONE", "MASK_KEY_PADDING",
+__all__ = ["attn_fwd", "attn_fwd_host", "host_workspace_size", "attn_mha_fwd", "mha_workspace_size", "attn_fwd_window", "attn_fwd_lse", "MASK_WINDOW", "attn_bwd", "bwd_workspace_size", "attn_decode", "decode_workspace_size", "AttnError", "select_kernel", "device_status", "make_workspace", "workspace_size", "MASK_NONE", "MASK_KEY_PADDING",
            "MASK_CAUSAL", "KERNEL_AUTO", "KERNEL_FLASH", "KERNEL_SHORT", "KERNEL_SIMT"]
 
 
@@ -91,6 +91,63 @@ def attn_fwd(q, k, v, key_lengths=None, mask_kind: int = MASK_NONE, scale: Optio
     else:
         st = _native.fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), lens_ptr, mask_kind, scale,
                              out.data_ptr(), dims, stream.cuda_stream, kernel)
+    if st != _native.ATTN_OK:
+        raise AttnError(st)
+    return out
+
+
+def host_workspace_size(B, h, m, n, d, dtype: int = DTYPE_BF16) -> int:
+    """Bytes of device workspace attn_fwd_host needs (0 for invalid sizes)."""
+    return _native.host_workspace_size(_native.make_dims(B, h, m, n, d, dtype))
+
+
+def attn_fwd_host(q, k, v, key_lengths=None, mask_kind: int = MASK_NONE, scale: Optional[float] = None,
+                  out=None, workspace=None, stream=None, device=None):
+    """attn_fwd on host (CPU) tensors: the C-ABI call copies the inputs in, runs the
+    kernels and copies the output back, chunk by chunk so that the three overlap.
+
+    q: [B, h, m, d_k]; k, v: [B, h, n, d_k] contiguous CPU tensors (bf16 or fp32; pinned
+    memory for full-speed asynchronous copies).  key_lengths: int32 [B] CPU tensor
+    (needed for MASK_KEY_PADDING).  out: optional preallocated CPU tensor.  workspace:
+    optional CUDA uint8 buffer of at least host_workspace_size(...) bytes (allocated on
+    ``device`` when omitted).  Enqueued on ``stream`` (default: torch's current stream on
+    the device); ``out`` is valid after that stream is synchronised.
+    """
+    import torch
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, h, len, d_k]")
+    for t in (q, k, v):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous CPU tensors")
+    B, h, m, d = q.shape
+    n = k.shape[2]
+    if k.shape != (B, h, n, d) or v.shape != k.shape or q.dtype != k.dtype or q.dtype != v.dtype:
+        raise ValueError(f"shape/dtype mismatch: q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=q.is_pinned())
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or out.is_cuda:
+        raise ValueError("out must be a contiguous CPU tensor shaped and typed like q")
+    lens_ptr = None
+    if mask_kind & MASK_KEY_PADDING:
+        if key_lengths is None or key_lengths.dtype != torch.int32 or key_lengths.is_cuda \
+                or key_lengths.numel() != B or not key_lengths.is_contiguous():
+            raise ValueError("key padding needs key_lengths: contiguous int32 CPU tensor of B elements")
+        lens_ptr = key_lengths.data_ptr()
+    device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    dims = _native.make_dims(B, h, m, n, d, _dtype_code(q))
+    need = _native.host_workspace_size(dims)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+    elif not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    if stream is None:
+        stream = torch.cuda.current_stream(workspace.device)
+    with torch.cuda.device(workspace.device):
+        st = _native.fwd_host_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), lens_ptr, mask_kind, scale,
+                                  out.data_ptr(), dims, workspace.data_ptr(),
+                                  workspace.numel() * workspace.element_size(), stream.cuda_stream)
     if st != _native.ATTN_OK:
         raise AttnError(st)
     return out

@@ -51,6 +51,10 @@ lib.attn_workspace_size.restype = ctypes.c_size_t
 lib.attn_fwd_ws.argtypes = lib.attn_fwd.argtypes + [_vp, ctypes.c_size_t]
 lib.attn_fwd_ws.restype = ctypes.c_int
 lib.attn_fwd_noalloc.argtypes = lib.attn_fwd.argtypes
+lib.attn_fwd_host_workspace_size.argtypes = [ctypes.POINTER(AttnDims)]
+lib.attn_fwd_host_workspace_size.restype = ctypes.c_size_t
+lib.attn_fwd_host.argtypes = lib.attn_fwd.argtypes[:-1] + [_vp, ctypes.c_size_t, _vp]
+lib.attn_fwd_host.restype = ctypes.c_int
 lib.attn_fwd_noalloc.restype = ctypes.c_int
 lib.attn_fwd_lse.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_float, _vp, _vp,
                              ctypes.POINTER(AttnDims), _vp]
@@ -124,6 +128,17 @@ def fwd_ws_raw(q_ptr, k_ptr, v_ptr, lens_ptr, mask_kind, scale, out_ptr, dims: A
     """attn_fwd_ws with integer device pointers; returns the status code."""
     return lib.attn_fwd_ws(q_ptr, k_ptr, v_ptr, lens_ptr, int(mask_kind), float(scale), out_ptr,
                            ctypes.byref(dims), stream_ptr, ws_ptr, int(ws_bytes))
+
+
+def host_workspace_size(dims: AttnDims) -> int:
+    return int(lib.attn_fwd_host_workspace_size(ctypes.byref(dims)))
+
+
+def fwd_host_raw(q_ptr, k_ptr, v_ptr, lens_ptr, mask_kind, scale, out_ptr, dims: AttnDims, ws_ptr, ws_bytes,
+                 stream_ptr) -> int:
+    """attn_fwd_host with integer host pointers (device workspace); returns the status code."""
+    return lib.attn_fwd_host(q_ptr, k_ptr, v_ptr, lens_ptr, int(mask_kind), float(scale), out_ptr,
+                             ctypes.byref(dims), ws_ptr, int(ws_bytes), stream_ptr)
 
 
 def fwd_noalloc_raw(q_ptr, k_ptr, v_ptr, lens_ptr, mask_kind, scale, out_ptr, dims: AttnDims,

@@ -471,6 +471,181 @@ attn_status attn_mha_fwd(const void *Xq, const void *Xkv, const void *Wq, const 
     return attn::launch_proj(pp, s) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+} // extern "C"
+
+// ------------------------------------------------------------ host buffers
+namespace {
+
+constexpr int kHostChunksTarget = 8; // chunks per call (about: the cut follows (batch, head) slices)
+constexpr int kHostComputeStreams = 2;
+constexpr int kHostMaxChunks = 64;
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+struct HostPlan {
+    size_t q_bytes, kv_bytes, len_off, ctr_off, total;
+};
+
+HostPlan host_plan(const attn_dims &d)
+{
+    const size_t esz = d.dtype == ATTN_BF16 ? 2 : 4;
+    HostPlan p;
+    p.q_bytes = static_cast<size_t>(d.B) * d.h * d.m * d.d_k * esz;
+    p.kv_bytes = static_cast<size_t>(d.B) * d.h * d.n * d.d_k * esz;
+    // [Q][K][V][out][lengths][one tile counter per compute stream]
+    p.len_off = 2 * round256(p.q_bytes) + 2 * round256(p.kv_bytes);
+    p.ctr_off = p.len_off + round256(4ull * d.B);
+    p.total = p.ctr_off + kHostComputeStreams * attn::kWorkspaceBytes;
+    return p;
+}
+
+// A chunk: batches [b0, b0 + nb) with all heads, or heads [h0, h0 + nh) of batch b0
+// (nb == 1).  Either way its rows are contiguous in every tensor and its key
+// lengths are lengths[b0 ...].
+struct HostChunk {
+    int b0, nb, h0, nh;
+};
+
+int host_chunks(const attn_dims &d, HostChunk *c)
+{
+    int k = 0;
+    if (d.B >= kHostChunksTarget) {
+        const int nb = (d.B + kHostChunksTarget - 1) / kHostChunksTarget;
+        for (int b = 0; b < d.B; b += nb) c[k++] = {b, nb < d.B - b ? nb : d.B - b, 0, d.h};
+    } else {
+        int parts = (kHostChunksTarget + d.B - 1) / d.B;
+        if (parts > d.h) parts = d.h;
+        const int nh = (d.h + parts - 1) / parts;
+        for (int b = 0; b < d.B; ++b)
+            for (int h0 = 0; h0 < d.h; h0 += nh) c[k++] = {b, 1, h0, nh < d.h - h0 ? nh : d.h - h0};
+    }
+    return k;
+}
+
+// Streams and events of one device, made on first use and kept for the process.
+struct HostDevice {
+    std::mutex mu;
+    bool ready = false;
+    cudaStream_t in = nullptr, out = nullptr, comp[kHostComputeStreams] = {};
+    cudaEvent_t start = nullptr, done = nullptr, ev_in[kHostMaxChunks] = {}, ev_comp[kHostMaxChunks] = {};
+};
+HostDevice g_host_devices[kMaxDevices];
+
+cudaError_t host_device_setup(HostDevice &hd)
+{
+    if (hd.ready) return cudaSuccess;
+    cudaError_t e;
+    if ((e = cudaStreamCreateWithFlags(&hd.in, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithFlags(&hd.out, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    for (auto &s : hd.comp)
+        if ((e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&hd.start, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&hd.done, cudaEventDisableTiming)) != cudaSuccess) return e;
+    for (int i = 0; i < kHostMaxChunks; ++i) {
+        if ((e = cudaEventCreateWithFlags(&hd.ev_in[i], cudaEventDisableTiming)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&hd.ev_comp[i], cudaEventDisableTiming)) != cudaSuccess) return e;
+    }
+    hd.ready = true;
+    return cudaSuccess;
+}
+
+} // namespace
+
+extern "C" {
+
+size_t attn_fwd_host_workspace_size(const attn_dims *dims)
+{
+    if (validate_dims(dims, 0, 1.f) != ATTN_OK) return 0;
+    return host_plan(*dims).total;
+}
+
+attn_status attn_fwd_host(const void *Q, const void *K, const void *V, const int32_t *key_lengths, int mask_kind,
+                          float scale, void *out, const attn_dims *dims, void *dev_workspace,
+                          size_t dev_workspace_bytes, void *stream)
+{
+    if (dims == nullptr || Q == nullptr || K == nullptr || V == nullptr || out == nullptr) return ATTN_ERR_NULL;
+    if ((mask_kind & ATTN_MASK_KEY_PADDING) && key_lengths == nullptr) return ATTN_ERR_NULL;
+    attn_status st = validate_dims(dims, mask_kind, scale);
+    if (st != ATTN_OK) return st;
+    if (dev_workspace == nullptr) return ATTN_ERR_NULL;
+    const attn_dims &d = *dims;
+    const HostPlan plan = host_plan(d);
+    if (dev_workspace_bytes < plan.total) return ATTN_ERR_SHAPE;
+    if (!aligned(dev_workspace, 256)) return ATTN_ERR_ALIGN;
+    if (overlaps(out, plan.q_bytes, Q, plan.q_bytes) || overlaps(out, plan.q_bytes, K, plan.kv_bytes) ||
+        overlaps(out, plan.q_bytes, V, plan.kv_bytes))
+        return ATTN_ERR_ALIAS;
+    if ((mask_kind & ATTN_MASK_KEY_PADDING) && overlaps(out, plan.q_bytes, key_lengths, 4ull * d.B))
+        return ATTN_ERR_ALIAS;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+    HostDevice &hd = g_host_devices[dev];
+    std::lock_guard<std::mutex> lock(hd.mu); // one call enqueues at a time: the events are reused
+    if (host_device_setup(hd) != cudaSuccess) return ATTN_ERR_CUDA;
+
+    const size_t esz = d.dtype == ATTN_BF16 ? 2 : 4;
+    const size_t q_row = static_cast<size_t>(d.m) * d.d_k * esz; // bytes of one (batch, head) slice
+    const size_t kv_row = static_cast<size_t>(d.n) * d.d_k * esz;
+    HostChunk chunks[kHostMaxChunks];
+    int nchunks = 1;
+    chunks[0] = {0, d.B, 0, d.h};
+    // chunks start at slice boundaries, which keep the 16-byte alignment the kernels need
+    // only when a slice is a whole number of 16-byte units
+    if (q_row % 16 == 0 && kv_row % 16 == 0) nchunks = host_chunks(d, chunks);
+    uint8_t *ws = static_cast<uint8_t *>(dev_workspace);
+    uint8_t *dq = ws, *dk = ws + round256(plan.q_bytes), *dv = dk + round256(plan.kv_bytes);
+    uint8_t *dout = dv + round256(plan.kv_bytes);
+    int32_t *dlen = reinterpret_cast<int32_t *>(ws + plan.len_off);
+    uint8_t *ctr = ws + plan.ctr_off;
+    cudaStream_t user = static_cast<cudaStream_t>(stream);
+    const uint8_t *hq = static_cast<const uint8_t *>(Q), *hk = static_cast<const uint8_t *>(K),
+                  *hv = static_cast<const uint8_t *>(V);
+    uint8_t *ho = static_cast<uint8_t *>(out);
+
+    // everything already on the caller's stream comes first
+    bool ok = cudaEventRecord(hd.start, user) == cudaSuccess;
+    ok = ok && cudaStreamWaitEvent(hd.in, hd.start, 0) == cudaSuccess;
+    ok = ok && cudaStreamWaitEvent(hd.out, hd.start, 0) == cudaSuccess;
+    ok = ok && cudaMemsetAsync(ctr, 0, kHostComputeStreams * attn::kWorkspaceBytes, hd.in) == cudaSuccess;
+    if (mask_kind & ATTN_MASK_KEY_PADDING)
+        ok = ok && cudaMemcpyAsync(dlen, key_lengths, 4ull * d.B, cudaMemcpyHostToDevice, hd.in) == cudaSuccess;
+    for (int c = 0; c < nchunks && ok; ++c) {
+        const HostChunk &ch = chunks[c];
+        const size_t bh0 = static_cast<size_t>(ch.b0) * d.h + ch.h0;
+        const size_t units = static_cast<size_t>(ch.nb) * ch.nh;
+        // inputs of chunk c, then its kernel as soon as they are in, then its output back
+        ok = ok && cudaMemcpyAsync(dq + bh0 * q_row, hq + bh0 * q_row, units * q_row, cudaMemcpyHostToDevice,
+                                   hd.in) == cudaSuccess;
+        ok = ok && cudaMemcpyAsync(dk + bh0 * kv_row, hk + bh0 * kv_row, units * kv_row, cudaMemcpyHostToDevice,
+                                   hd.in) == cudaSuccess;
+        ok = ok && cudaMemcpyAsync(dv + bh0 * kv_row, hv + bh0 * kv_row, units * kv_row, cudaMemcpyHostToDevice,
+                                   hd.in) == cudaSuccess;
+        ok = ok && cudaEventRecord(hd.ev_in[c], hd.in) == cudaSuccess;
+        cudaStream_t cs = hd.comp[c % kHostComputeStreams];
+        ok = ok && cudaStreamWaitEvent(cs, hd.ev_in[c], 0) == cudaSuccess;
+        if (!ok) break;
+        attn_dims sub = d;
+        sub.B = ch.nb;
+        sub.h = ch.nh;
+        st = attn_fwd_ws(dq + bh0 * q_row, dk + bh0 * kv_row, dv + bh0 * kv_row,
+                         (mask_kind & ATTN_MASK_KEY_PADDING) ? dlen + ch.b0 : nullptr, mask_kind, scale,
+                         dout + bh0 * q_row, &sub, cs, ctr + (c % kHostComputeStreams) * attn::kWorkspaceBytes,
+                         attn::kWorkspaceBytes);
+        if (st != ATTN_OK) break;
+        ok = cudaEventRecord(hd.ev_comp[c], cs) == cudaSuccess;
+        ok = ok && cudaStreamWaitEvent(hd.out, hd.ev_comp[c], 0) == cudaSuccess;
+        ok = ok && cudaMemcpyAsync(ho + bh0 * q_row, dout + bh0 * q_row, units * q_row, cudaMemcpyDeviceToHost,
+                                   hd.out) == cudaSuccess;
+    }
+    // the caller's stream waits for the last copy back (which waited for every kernel)
+    const bool joined = cudaEventRecord(hd.done, hd.out) == cudaSuccess &&
+                        cudaStreamWaitEvent(user, hd.done, 0) == cudaSuccess;
+    if (st != ATTN_OK) return st;
+    return ok && joined ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 int attn_select_kernel(const attn_dims *dims, int mask_kind)
 {
     if (validate_dims(dims, mask_kind, 1.0f) != ATTN_OK) return ATTN_KERNEL_AUTO;
