@@ -68,7 +68,7 @@ __device__ __forceinline__ void merge(float (&m)[M], float (&l)[M], float (&a)[M
 
 // M: query rows handled per (b, h) (the call's m rounded up to 1, 2, 4 or 8).
 template <int M>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, M == 1 ? 4 : 1)
 attn_decode_kernel(const __nv_bfloat16 *__restrict__ Q, const __nv_bfloat16 *__restrict__ K,
                    const __nv_bfloat16 *__restrict__ V, const int32_t *__restrict__ lengths,
                    __nv_bfloat16 *__restrict__ out, float *__restrict__ lse, float *__restrict__ part, int h,
@@ -115,16 +115,21 @@ attn_decode_kernel(const __nv_bfloat16 *__restrict__ Q, const __nv_bfloat16 *__r
     const uint4 *Vh = reinterpret_cast<const uint4 *>(V + static_cast<size_t>(bh) * n * kD);
     // Passes over the warp's rows are warp-uniform (the shuffles below need all 32
     // lanes); a row past the chunk is loaded as nothing and skipped after them.
-    // The next pass's rows are requested before this pass's arithmetic.
+    // The rows of the next two passes are requested before this pass's arithmetic.
     int row = k_begin + warp * 4 + r;
     uint4 ku = make_uint4(0, 0, 0, 0), vu = make_uint4(0, 0, 0, 0);
+    uint4 ku1 = make_uint4(0, 0, 0, 0), vu1 = make_uint4(0, 0, 0, 0);
     if (row < k_end) {
         ku = __ldg(Kh + static_cast<size_t>(row) * (kD / 8) + j);
         vu = __ldg(Vh + static_cast<size_t>(row) * (kD / 8) + j);
     }
+    if (row + kRowsPerPass < k_end) {
+        ku1 = __ldg(Kh + static_cast<size_t>(row + kRowsPerPass) * (kD / 8) + j);
+        vu1 = __ldg(Vh + static_cast<size_t>(row + kRowsPerPass) * (kD / 8) + j);
+    }
     for (int base = k_begin + warp * 4; base < k_end; base += kRowsPerPass, row += kRowsPerPass) {
         const bool valid = row < k_end;
-        const int nrow = row + kRowsPerPass;
+        const int nrow = row + 2 * kRowsPerPass;
         uint4 kn = make_uint4(0, 0, 0, 0), vn = make_uint4(0, 0, 0, 0);
         if (nrow < k_end) {
             kn = __ldg(Kh + static_cast<size_t>(nrow) * (kD / 8) + j);
@@ -152,8 +157,10 @@ attn_decode_kernel(const __nv_bfloat16 *__restrict__ Q, const __nv_bfloat16 *__r
                 mx[qi] = mn;
             }
         }
-        ku = kn;
-        vu = vn;
+        ku = ku1;
+        vu = vu1;
+        ku1 = kn;
+        vu1 = vn;
     }
     // the warp's four row groups (lanes j, j + 8, j + 16, j + 24) into lanes 0-7
 #pragma unroll
@@ -244,10 +251,13 @@ __global__ void attn_decode_combine_kernel(const float *__restrict__ part, __nv_
 
 int decode_splits(int B, int h, int n, int sms)
 {
-    // enough CTAs for about four waves, each reading at least 256 keys
+    // Enough CTAs for about four waves, and no CTA reading more than 512 keys (so
+    // heads with long caches do not finish alone), each reading at least 256 keys.
     const int max_splits = (n + 255) / 256;
     const long heads = static_cast<long>(B) * h;
     long want = (4L * sms + heads - 1) / heads;
+    const long by_rows = (n + 511) / 512;
+    if (want < by_rows) want = by_rows;
     if (want < 1) want = 1;
     if (want > max_splits) want = max_splits;
     if (want > 65535) want = 65535;
