@@ -451,13 +451,16 @@ attn_status attn_mha_fwd(const void *Xq, const void *Xkv, const void *Wq, const 
         void *o;
         int L;
     } ins_proj[3] = {{Xq, Wq, Q, d.m}, {Xkv, Wk, K, d.n}, {Xkv, Wv, V, d.n}};
-    for (const auto &ip : ins_proj) {
-        pp.a = ip.x;
-        pp.w = ip.w;
-        pp.out = ip.o;
-        pp.L = ip.L;
-        if (attn::launch_proj(pp, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    attn::ProjProblem in3[3];
+    for (int i = 0; i < 3; ++i) {
+        in3[i] = pp;
+        in3[i].a = ins_proj[i].x;
+        in3[i].w = ins_proj[i].w;
+        in3[i].out = ins_proj[i].o;
+        in3[i].L = ins_proj[i].L;
     }
+    // the three input projections in one launch
+    if (attn::launch_proj_multi(in3, 3, s) != cudaSuccess) return ATTN_ERR_CUDA;
     attn_dims ad{d.B, d.h, d.m, d.n, 64, ATTN_BF16};
     st = run(Q, K, V, key_lengths, mask_kind, scale, O, &ad, stream, ATTN_KERNEL_AUTO, nullptr);
     if (st != ATTN_OK) return st;

@@ -5,7 +5,10 @@
 // MultiHead = Concat(head_1, ..., head_h) W^O; no bias terms).
 //
 // A persistent CTA per SM walks 128 x 256 tiles of D = A B (fp32 accumulation in
-// TMEM; a last tile of 128 columns when N is an odd multiple of 128):
+// TMEM; a last tile of 128 columns when N is an odd multiple of 128).  One launch
+// may hold up to three products of the same shape (the W^Q, W^K and W^V products,
+// whose row counts may differ): their tiles form one list, so the three share the
+// pipeline fill and the last wave:
 //   kProjIn   A = rows t0 .. t0+127 of x[b] ([B][L][K], K = d_model), B = columns
 //             n0 .. n0+255 of W ([K][h*64]); each 64-column block of the tile is one
 //             head, stored straight into the head-split layout [B*h][L][64] (the
@@ -15,11 +18,11 @@
 //             ([h*64][N]); the tile goes to out[b] ([B][L][N]).
 // A tiles are K-major (64 bf16 = one 128-byte swizzle row per tile row); B tiles
 // are 64 x 64 MN-major blocks, two side by side forming each N = 128 operand (the
-// descriptor's leading offset is the distance between them).  A 3-stage TMA ring
+// descriptor's leading offset is the distance between them).  A 4-stage TMA ring
 // feeds 4 x 2 MMAs of M128 N128 K16 per 64-wide K step.  Two 256-column TMEM
 // accumulators alternate between tiles, so the epilogue of one tile (bf16 through
-// a swizzled shared-memory tile, TMA stores, rows past L clipped) runs while the
-// next tile accumulates.
+// two swizzled shared-memory blocks used in turn, TMA stores, rows past L clipped)
+// runs while the next tile accumulates.
 //
 // Warps: 0 TMA producer, 1 MMA issuer (and TMEM owner), 2-5 epilogue.  Every
 // mbarrier wait is bounded and reports through this file's status word.
@@ -40,7 +43,7 @@ __device__ unsigned int g_proj_status_info;
 namespace {
 
 constexpr int kTM = 128, kTN = 256, kTK = 64; // output tile and K step
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kThreads = 192;
 constexpr uint32_t kATile = kTM * kTK * 2;    // 16 KiB
 constexpr uint32_t kBBlock = kTK * 64 * 2;    // 8 KiB: 64 K rows x 64 N columns
@@ -51,10 +54,10 @@ constexpr uint32_t kIdesc = idesc_bf16_f32(kTM, 128, 0, 1); // A K-major, B MN-m
 struct alignas(1024) ProjSmem {
     uint8_t a[kStages][kATile];
     uint8_t b[kStages][4][kBBlock];
-    uint8_t stage[4][kTM * 64 * 2]; // bf16 output blocks of 64 columns, 128-byte swizzle
+    uint8_t stage[2][kTM * 64 * 2]; // bf16 output blocks of 64 columns, 128-byte swizzle, used in turn
     uint64_t full[kStages], empty[kStages];
     uint64_t acc_full[2], acc_empty[2]; // accumulator a holds a finished tile / may be overwritten
-    uint64_t stage_free, staged[4];
+    uint64_t stage_free[2], staged[2];  // staging block j may be rewritten / holds a block to store
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -86,29 +89,54 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity)
         if (global_timer_ns() - start > kWaitLimitNs) return;
 }
 
+constexpr int kMaxProblems = 3; // the W^Q, W^K, W^V products of one layer in one launch
+
+// Tensor maps of the launch's products: A, W and the output of product i.
+struct ProjMaps {
+    CUtensorMap a[kMaxProblems], w[kMaxProblems], out[kMaxProblems];
+};
+
 struct ProjParams {
-    int mode, h, K, N, B, m_tiles; // m_tiles: 128-row tiles per batch entry
+    int mode, h, K, N, B, problems;
+    int m_tiles[kMaxProblems]; // 128-row tiles per batch entry of product i
+    int tiles_of[kMaxProblems];
     int n_tiles, tiles;
 };
 
 struct TileId {
-    int b, t0, n0, ncols; // ncols: 256, or 128 for a last half tile
+    int pi, b, t0, n0, ncols; // pi: product; ncols: 256, or 128 for a last half tile
 };
 
+// Tiles are numbered product by product; selects instead of indexing the
+// parameter arrays with a run-time value.
 __device__ __forceinline__ TileId tile_id(const ProjParams &p, int t)
 {
     TileId id;
+    id.pi = 0;
+    if (p.problems > 1 && t >= p.tiles_of[0]) {
+        t -= p.tiles_of[0];
+        id.pi = 1;
+        if (p.problems > 2 && t >= p.tiles_of[1]) {
+            t -= p.tiles_of[1];
+            id.pi = 2;
+        }
+    }
+    const int mt = id.pi == 0 ? p.m_tiles[0] : (id.pi == 1 ? p.m_tiles[1] : p.m_tiles[2]);
     const int nt = t % p.n_tiles, mi = t / p.n_tiles;
-    id.b = mi / p.m_tiles;
-    id.t0 = (mi % p.m_tiles) * kTM;
+    id.b = mi / mt;
+    id.t0 = (mi % mt) * kTM;
     id.n0 = nt * kTN;
     id.ncols = min(kTN, p.N - id.n0);
     return id;
 }
 
+__device__ __forceinline__ const CUtensorMap *pick(const CUtensorMap (&m)[kMaxProblems], int pi)
+{
+    return pi == 0 ? &m[0] : (pi == 1 ? &m[1] : &m[2]);
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-attn_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
-                 const __grid_constant__ CUtensorMap tm_out, const ProjParams p)
+attn_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     ProjSmem &sm = *reinterpret_cast<ProjSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -126,8 +154,10 @@ attn_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
             mbar_init(&sm.acc_full[a], 1);
             mbar_init(&sm.acc_empty[a], kTM);
         }
-        mbar_init(&sm.stage_free, 1);
-        for (int q = 0; q < 4; ++q) mbar_init(&sm.staged[q], kTM);
+        for (int j = 0; j < 2; ++j) {
+            mbar_init(&sm.stage_free[j], 1);
+            mbar_init(&sm.staged[j], kTM);
+        }
         mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
         fence_mbarrier_init();
@@ -144,24 +174,27 @@ attn_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
 
     if (warp == 0) {
         if (threadIdx.x == 0) {
-            tma_prefetch_map(&tm_a);
-            tma_prefetch_map(&tm_w);
+            for (int pi = 0; pi < p.problems; ++pi) {
+                tma_prefetch_map(pick(maps.a, pi));
+                tma_prefetch_map(pick(maps.w, pi));
+            }
             uint32_t kc = 0, issued = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
                 const TileId id = tile_id(p, t);
                 const int blocks = id.ncols / 64;
+                const CUtensorMap *tm_a = pick(maps.a, id.pi), *tm_w = pick(maps.w, id.pi);
                 for (int kk = 0; kk < ksteps; ++kk, ++kc) {
                     const uint32_t s = kc % kStages;
                     if (!(ok = wait_bar(&sm.empty[s], ((kc / kStages) & 1) ^ 1, ab, 1))) break;
                     mbar_arrive_expect_tx(&sm.full[s], kATile + blocks * kBBlock);
                     if (p.mode == kProjIn)
-                        tma_load_3d(sm.a[s], &tm_a, &sm.full[s], kk * kTK, id.t0, id.b);
+                        tma_load_3d(sm.a[s], tm_a, &sm.full[s], kk * kTK, id.t0, id.b);
                     else
-                        tma_load_3d(sm.a[s], &tm_a, &sm.full[s], 0, id.t0, id.b * p.h + kk);
+                        tma_load_3d(sm.a[s], tm_a, &sm.full[s], 0, id.t0, id.b * p.h + kk);
                     // W as a 3-D tensor with one outer slice
                     for (int q = 0; q < blocks; ++q)
-                        tma_load_3d(sm.b[s][q], &tm_w, &sm.full[s], id.n0 + 64 * q, kk * kTK, 0);
+                        tma_load_3d(sm.b[s][q], tm_w, &sm.full[s], id.n0 + 64 * q, kk * kTK, 0);
                     ++issued;
                 }
             }
@@ -211,33 +244,47 @@ attn_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
         }
         __syncwarp();
     } else {
-        // epilogue: thread r = output row r of the tile (TMEM lane r)
+        // epilogue: thread r = output row r of the tile (TMEM lane r).  Each 64-column
+        // block goes through one of two staging blocks in turn: block q is written
+        // once the store of the block before last has read its staging block, and
+        // stored by one thread; every use of staging block j completes one phase of
+        // stage_free[j] and of staged[j], so both follow the use count.
         const int r = (warp % 4) * 32 + threadIdx.x % 32;
         const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
         bool ok = true;
         int i = 0;
+        uint32_t uses[2] = {0, 0};
         for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x, ++i) {
             const TileId id = tile_id(p, t);
             const int a = i & 1;
             ok = __all_sync(0xffffffffu, wait_bar(&sm.acc_full[a], (i >> 1) & 1, ab, 4));
             if (!ok) break;
             tc_fence_after();
-            // the staging blocks are rewritten only after the previous tile's stores read them
-            if (r == 0) {
-                bulk_wait_read_all();
-                mbar_arrive(&sm.stage_free);
-            }
-            ok = __all_sync(0xffffffffu, wait_bar(&sm.stage_free, i & 1, ab, 5));
-            if (!ok) break;
+            const CUtensorMap *tm_out = pick(maps.out, id.pi);
             const int blocks = id.ncols / 64;
-            for (int q = 0; q < blocks; ++q) {
+            for (int q = 0; q < blocks && ok; ++q) {
+                const int j = q & 1;
+                const uint32_t u = j ? uses[1] : uses[0];
                 uint32_t v[64];
                 tmem_ld32(tmem + lane_base + 256 * a + 64 * q, v);
                 tmem_ld32(tmem + lane_base + 256 * a + 64 * q + 32, v + 32);
                 tmem_wait_ld();
                 reg_fence32(v);
                 reg_fence32(v + 32);
-                const uint32_t row = smem_addr(sm.stage[q]) + r * 128;
+                if (q == blocks - 1) {
+                    // the accumulator is free for the tile after next
+                    tc_fence_before();
+                    mbar_arrive(&sm.acc_empty[a]);
+                }
+                if (r == 0) {
+                    // each block's store is its own group: all but the last (the other
+                    // staging block's) have read their source, this block's included
+                    bulk_wait_read_1();
+                    mbar_arrive(&sm.stage_free[j]);
+                }
+                ok = __all_sync(0xffffffffu, wait_bar(&sm.stage_free[j], u & 1, ab, 5));
+                if (!ok) break;
+                const uint32_t row = smem_addr(sm.stage[j]) + r * 128;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     uint4 w;
@@ -248,25 +295,19 @@ attn_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
                     st_shared_v4(row + ((c ^ (r & 7)) << 4), w);
                 }
                 fence_proxy_async_shared();
-                mbar_arrive(&sm.staged[q]);
-            }
-            // a half tile leaves blocks 2 and 3 unused: arrive anyway, so every staged
-            // barrier completes one phase per tile and its parity follows the tile count
-            for (int q = blocks; q < 4; ++q) mbar_arrive(&sm.staged[q]);
-            // the accumulator is free for the tile after next
-            tc_fence_before();
-            mbar_arrive(&sm.acc_empty[a]);
-            if (r == 0) {
-                for (int q = 0; q < blocks && ok; ++q) {
-                    if (!(ok = wait_bar(&sm.staged[q], i & 1, ab, 6))) break;
-                    if (p.mode == kProjIn)
-                        tma_store_3d(&tm_out, sm.stage[q], 0, id.t0, id.b * p.h + (id.n0 + 64 * q) / 64);
-                    else
-                        tma_store_3d(&tm_out, sm.stage[q], id.n0 + 64 * q, id.t0, id.b);
+                mbar_arrive(&sm.staged[j]);
+                if (r == 0) {
+                    if ((ok = wait_bar(&sm.staged[j], u & 1, ab, 6))) {
+                        if (p.mode == kProjIn)
+                            tma_store_3d(tm_out, sm.stage[j], 0, id.t0, id.b * p.h + (id.n0 + 64 * q) / 64);
+                        else
+                            tma_store_3d(tm_out, sm.stage[j], id.n0 + 64 * q, id.t0, id.b);
+                        bulk_commit_group();
+                    }
                 }
-                bulk_commit_group();
+                ok = __all_sync(0xffffffffu, ok);
+                if (j) ++uses[1]; else ++uses[0];
             }
-            ok = __all_sync(0xffffffffu, ok);
         }
         if (r == 0) bulk_wait_all();
     }
@@ -282,7 +323,7 @@ constexpr size_t kSmemBytes = sizeof(ProjSmem) + 1024;
 
 } // namespace
 
-cudaError_t launch_proj(const ProjProblem &pp, cudaStream_t stream)
+cudaError_t launch_proj_multi(const ProjProblem *pps, int count, cudaStream_t stream)
 {
     static bool configured[64] = {};
     static std::mutex mu;
@@ -299,33 +340,57 @@ cudaError_t launch_proj(const ProjProblem &pp, cudaStream_t stream)
             configured[dev] = true;
         }
     }
-    if (pp.K % kTK != 0 || pp.N % 128 != 0) return cudaErrorInvalidValue;
-    CUtensorMap ta, tw, to;
-    const int BH = pp.B * pp.h;
-    bool enc;
-    if (pp.mode == kProjIn) {
-        enc = encode_bf16_3d(&ta, pp.a, pp.K, pp.L, pp.B, kTM) && encode_bf16_3d(&to, pp.out, 64, pp.L, BH, kTM);
-    } else {
-        enc = encode_bf16_3d(&ta, pp.a, 64, pp.L, BH, kTM) && encode_bf16_3d(&to, pp.out, pp.N, pp.L, pp.B, kTM);
-    }
-    // W [K][N] as a 3-D tensor with one outer slice: 64 x 64 boxes
-    enc = enc && encode_bf16_3d(&tw, pp.w, pp.N, pp.K, 1, kTK);
-    if (!enc) return cudaErrorInvalidValue;
+    if (count < 1 || count > kMaxProblems) return cudaErrorInvalidValue;
+    const ProjProblem &p0 = pps[0];
+    if (p0.K % kTK != 0 || p0.N % 128 != 0) return cudaErrorInvalidValue;
+    ProjMaps maps;
     ProjParams p;
-    p.mode = pp.mode;
-    p.h = pp.h;
-    p.K = pp.K;
-    p.N = pp.N;
-    p.B = pp.B;
-    p.m_tiles = (pp.L + kTM - 1) / kTM;
-    p.n_tiles = (pp.N + kTN - 1) / kTN;
-    p.tiles = p.n_tiles * p.m_tiles * pp.B;
+    p.mode = p0.mode;
+    p.h = p0.h;
+    p.K = p0.K;
+    p.N = p0.N;
+    p.B = p0.B;
+    p.problems = count;
+    p.n_tiles = (p0.N + kTN - 1) / kTN;
+    p.tiles = 0;
+    const int BH = p0.B * p0.h;
+    for (int i = 0; i < kMaxProblems; ++i) {
+        p.m_tiles[i] = 0;
+        p.tiles_of[i] = 0;
+    }
+    for (int i = 0; i < count; ++i) {
+        const ProjProblem &pp = pps[i];
+        // one launch runs products of one shape: only the row count may differ
+        if (pp.mode != p0.mode || pp.B != p0.B || pp.h != p0.h || pp.K != p0.K || pp.N != p0.N)
+            return cudaErrorInvalidValue;
+        bool enc;
+        if (pp.mode == kProjIn) {
+            enc = encode_bf16_3d(&maps.a[i], pp.a, pp.K, pp.L, pp.B, kTM) &&
+                  encode_bf16_3d(&maps.out[i], pp.out, 64, pp.L, BH, kTM);
+        } else {
+            enc = encode_bf16_3d(&maps.a[i], pp.a, 64, pp.L, BH, kTM) &&
+                  encode_bf16_3d(&maps.out[i], pp.out, pp.N, pp.L, pp.B, kTM);
+        }
+        // W [K][N] as a 3-D tensor with one outer slice: 64 x 64 boxes
+        enc = enc && encode_bf16_3d(&maps.w[i], pp.w, pp.N, pp.K, 1, kTK);
+        if (!enc) return cudaErrorInvalidValue;
+        p.m_tiles[i] = (pp.L + kTM - 1) / kTM;
+        p.tiles_of[i] = p.n_tiles * p.m_tiles[i] * pp.B;
+        p.tiles += p.tiles_of[i];
+    }
+    for (int i = count; i < kMaxProblems; ++i) {
+        maps.a[i] = maps.a[0];
+        maps.w[i] = maps.w[0];
+        maps.out[i] = maps.out[0];
+    }
     int sms = 0;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const int grid = p.tiles < sms ? p.tiles : sms;
-    attn_proj_kernel<<<grid, kThreads, kSmemBytes, stream>>>(ta, tw, to, p);
+    attn_proj_kernel<<<grid, kThreads, kSmemBytes, stream>>>(maps, p);
     return cudaGetLastError();
 }
+
+cudaError_t launch_proj(const ProjProblem &pp, cudaStream_t stream) { return launch_proj_multi(&pp, 1, stream); }
 
 cudaError_t proj_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint32_t *info)
 {

@@ -86,6 +86,8 @@ struct ProjProblem {
     int B, h, L, K, N;
 };
 cudaError_t launch_proj(const ProjProblem &p, cudaStream_t stream);
+// Up to three products of one shape (mode, B, h, K, N; L may differ) in one launch.
+cudaError_t launch_proj_multi(const ProjProblem *p, int count, cudaStream_t stream);
 cudaError_t proj_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint32_t *info);
 
 // Device status word of the flash kernel (bounded waits that gave up).

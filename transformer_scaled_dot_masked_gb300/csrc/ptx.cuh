@@ -129,6 +129,10 @@ __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bul
 // this thread's committed bulk stores have finished reading shared memory
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
+// Wait until at most the most recently committed bulk group may still read its
+// shared-memory source (every older one has finished reading).
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+
 // this thread's committed bulk stores are complete (written to global memory)
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
