@@ -652,10 +652,25 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
             for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(sr[c]);
             bool prescaled = boundary; // x already multiplied by scale * log2 e
             if (boundary) {
-                // scale first, then mask: a zero scale must not turn -inf into NaN
+                // Scale first, then mask: a zero scale must not turn -inf into NaN.  The
+                // allowed columns of a row are the range [cnt_lo, cnt) (cnt_lo <= 0
+                // without a window).
+                if (kWindow) {
+                    // two bounds: one bit mask per 32 columns, then one bit test per column
 #pragma unroll
-                for (int c = 0; c < kBN; ++c)
-                    x[c] = (c < cnt && (!kWindow || c >= cnt_lo)) ? x[c] * sl2 : -CUDART_INF_F;
+                    for (int ch = 0; ch < kBN / 32; ++ch) {
+                        const int hi = min(max(cnt - 32 * ch, 0), 32);
+                        const int lo = min(max(cnt_lo - 32 * ch, 0), 32);
+                        uint32_t m = hi >= 32 ? 0xffffffffu : (1u << hi) - 1u;
+                        m &= lo >= 32 ? 0u : ~((1u << lo) - 1u);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            x[32 * ch + e] = (m & (1u << e)) ? x[32 * ch + e] * sl2 : -CUDART_INF_F;
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c) x[c] = c < cnt ? x[c] * sl2 : -CUDART_INF_F;
+                }
             }
 
             // Reference for the exponentials.  The row max is taken only on the row's
