@@ -96,6 +96,12 @@ def measured_traffic():
     return MEASURED_TRAFFIC.get(key)
 
 
+def workload_config(w):
+    """The workload part of the JSON line's config, the same on both arms."""
+    return {"workload": w.description, "B": w.B, "h": w.h, "m": w.m, "n": w.n, "d_k": w.d,
+            "mask": "causal" if w.causal else ("key_padding" if w.padded else "none")}
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -466,8 +472,7 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": w.description, "B": w.B, "h": w.h, "m": w.m, "n": w.n,
-                                        "d_k": w.d, "mask": w.mask},
+        "data": "synthetic", "config": workload_config(w),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": orc.num_threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -542,8 +547,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.description, "B": w.B, "h": w.h, "m": w.m, "n": w.n, "d_k": w.d,
-                   "mask": "causal" if w.causal else ("key_padding" if w.padded else "none"),
+        "config": {**workload_config(w),
                    "kernel": attn._native.KERNEL_NAMES[kern],
                    "entry_point": "attn_fwd" if ws is None else "attn_fwd_ws (dynamic tile schedule)",
                    "l2": "inputs+output 268 MB > L2, no flush between steps",
