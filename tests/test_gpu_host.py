@@ -107,3 +107,14 @@ def test_host_repeated_calls_reuse_workspace():
     ref = as_f64(run(inp))
     for o in outs:
         np.testing.assert_array_equal(as_f64(o), ref)
+
+
+def test_host_full_size_long_causal_bitwise():
+    """The long causal workload (B4 h16 n=8192, 268 MB of tensors, eight chunks) through
+    the host-buffer path equals the device path bit for bit."""
+    from workloads import WORKLOADS
+    w = WORKLOADS[5]
+    inp = draw(w)
+    got = run_host(inp)
+    dev = run(inp)
+    assert torch.equal(got.view(torch.int16), dev.cpu().view(torch.int16))

@@ -53,3 +53,21 @@ def test_mha_matches_oracle(orc, name, B, h, m, n, dm, mask, selfattn, lengths):
     ref = mha.mha_fwd(orc, xq, xkv, wq, wk, wv, wo, h, lens, mask, 64 ** -0.5)
     got = as_f64(out)
     assert np.abs(got - ref).max() <= 2e-2, report(got, ref, 2e-2)
+
+
+def test_mha_benchmarked_size(orc):
+    """The benchmarked call at full size and with its inputs: B32 sentences of 256
+    positions, d_model 1024, h 16, key padding with lengths in [128, 256] (the same
+    seeds as the benchmark), every output element against the oracle."""
+    B, h, L, dm = 32, 16, 256, 1024
+    xq, _, wq, wk, wv, wo = draw_mha(B, h, L, L, dm, seed=1007, self_attention=True)
+    lens = np.random.default_rng(1008).integers(128, 257, size=B).astype(np.int32)
+    x = dev(xq)
+    out = attn.attn_mha_fwd(x, x, dev(wq), dev(wk), dev(wv), dev(wo), h, torch.from_numpy(lens).cuda(),
+                            MASK_KEY_PADDING, 0.125)
+    torch.cuda.synchronize()
+    st, info = attn.device_status()
+    assert st == 0, f"device status {st} (info {info})"
+    ref = mha.mha_fwd(orc, xq, xq, wq, wk, wv, wo, h, lens, MASK_KEY_PADDING, 0.125)
+    got = as_f64(out)
+    assert np.abs(got - ref).max() <= 2e-2, report(got, ref, 2e-2)

@@ -72,3 +72,20 @@ def test_window_locality_bitwise():
     moved = run_window(type(inp)(w, inp.q, k2, v2, inp.key_lengths), WIN, 100)
     np.testing.assert_array_equal(moved[:, :, :600], base[:, :, :600])
     assert not np.array_equal(moved, base)
+
+
+def test_window_benchmarked_size(orc):
+    """The benchmarked call at full size: B4 h16 n=8192, window 256, the long workload's
+    inputs; every row of two heads (first and last) and 2048 random rows elsewhere
+    against the oracle."""
+    from workloads import WORKLOADS
+    w = WORKLOADS[5]
+    inp = draw(w)
+    got = run_window(inp, WIN, 256)
+    rng = np.random.default_rng(53)
+    m = w.m
+    rows = np.concatenate([np.arange(0, m), np.arange((w.B * w.h - 1) * m, w.B * w.h * m),
+                           rng.integers(0, w.B * w.h * m, size=2048)])
+    ref = orc.attn_rows(inp.q, inp.k, inp.v, None, WIN, w.scale, rows, window=256)
+    got_rows = got.reshape(-1, w.d)[rows]
+    assert np.abs(got_rows - ref).max() <= 1e-2, report(got_rows, ref, 1e-2)
