@@ -30,6 +30,30 @@ constexpr int kD = 64;
 constexpr int kWarps = 8;
 constexpr int kRowsPerPass = kWarps * 4; // key rows the CTA reads per pass
 constexpr int kPart = kD + 2;            // floats of one partial: O[64], max, sum
+// passes of rows each warp has in flight (3 for m > 4, whose merge buffer needs the
+// room: static shared memory stays under 48 KB)
+template <int M>
+__host__ __device__ constexpr int depth_of() { return M > 4 ? 3 : 4; }
+
+// 16 bytes global -> shared without registers (zero-filled when !valid: no read).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_u4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
 
 __device__ __forceinline__ float ex2f(float x)
 {
@@ -68,13 +92,16 @@ __device__ __forceinline__ void merge(float (&m)[M], float (&l)[M], float (&a)[M
 
 // M: query rows handled per (b, h) (the call's m rounded up to 1, 2, 4 or 8).
 template <int M>
-__global__ void __launch_bounds__(kWarps * 32, M == 1 ? 4 : 1)
+__global__ void __launch_bounds__(kWarps * 32, M == 1 ? 5 : 1)
 attn_decode_kernel(const __nv_bfloat16 *__restrict__ Q, const __nv_bfloat16 *__restrict__ K,
                    const __nv_bfloat16 *__restrict__ V, const int32_t *__restrict__ lengths,
                    __nv_bfloat16 *__restrict__ out, float *__restrict__ lse, float *__restrict__ part, int h,
                    int m, int n, int chunk, int splits, float scale_log2)
 {
     __shared__ float red[kWarps][M][kPart];
+    // each lane's 16-byte slices of its K and V rows, kDepth passes deep per warp
+    constexpr int kDepth = depth_of<M>();
+    __shared__ __align__(16) uint4 ring[kWarps][kDepth][2][32];
     const int bh = blockIdx.x;
     const int split = blockIdx.y;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -115,26 +142,29 @@ attn_decode_kernel(const __nv_bfloat16 *__restrict__ Q, const __nv_bfloat16 *__r
     const uint4 *Vh = reinterpret_cast<const uint4 *>(V + static_cast<size_t>(bh) * n * kD);
     // Passes over the warp's rows are warp-uniform (the shuffles below need all 32
     // lanes); a row past the chunk is loaded as nothing and skipped after them.
-    // The rows of the next two passes are requested before this pass's arithmetic.
+    // Each lane copies its own 16-byte slices of the K and V rows of the next
+    // kDepth - 1 passes into shared memory (cp.async, no registers held) and reads
+    // back only what it copied, so its own wait_group is the only ordering needed.
     int row = k_begin + warp * 4 + r;
-    uint4 ku = make_uint4(0, 0, 0, 0), vu = make_uint4(0, 0, 0, 0);
-    uint4 ku1 = make_uint4(0, 0, 0, 0), vu1 = make_uint4(0, 0, 0, 0);
-    if (row < k_end) {
-        ku = __ldg(Kh + static_cast<size_t>(row) * (kD / 8) + j);
-        vu = __ldg(Vh + static_cast<size_t>(row) * (kD / 8) + j);
-    }
-    if (row + kRowsPerPass < k_end) {
-        ku1 = __ldg(Kh + static_cast<size_t>(row + kRowsPerPass) * (kD / 8) + j);
-        vu1 = __ldg(Vh + static_cast<size_t>(row + kRowsPerPass) * (kD / 8) + j);
-    }
+    const uint32_t my_ring = static_cast<uint32_t>(__cvta_generic_to_shared(&ring[warp][0][0][lane]));
+    auto issue = [&](int prow, int st) {
+        const bool v = prow < k_end;
+        const size_t at = static_cast<size_t>(v ? prow : 0) * (kD / 8) + j; // row 0 exists: n >= 1
+        cp_async16(my_ring + st * (2 * 32 * 16), Kh + at, v);
+        cp_async16(my_ring + st * (2 * 32 * 16) + 32 * 16, Vh + at, v);
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int st = 0; st < kDepth - 1; ++st) issue(row + st * kRowsPerPass, st);
+    int stage = 0;
     for (int base = k_begin + warp * 4; base < k_end; base += kRowsPerPass, row += kRowsPerPass) {
         const bool valid = row < k_end;
-        const int nrow = row + 2 * kRowsPerPass;
-        uint4 kn = make_uint4(0, 0, 0, 0), vn = make_uint4(0, 0, 0, 0);
-        if (nrow < k_end) {
-            kn = __ldg(Kh + static_cast<size_t>(nrow) * (kD / 8) + j);
-            vn = __ldg(Vh + static_cast<size_t>(nrow) * (kD / 8) + j);
-        }
+        // the stage read in the previous pass is refilled (an empty group past the end)
+        issue(row + (kDepth - 1) * kRowsPerPass, (stage + kDepth - 1) % kDepth);
+        cp_async_wait<kDepth - 1>();
+        const uint4 ku = ld_shared_u4(my_ring + stage * (2 * 32 * 16));
+        const uint4 vu = ld_shared_u4(my_ring + stage * (2 * 32 * 16) + 32 * 16);
+        stage = (stage + 1) % kDepth;
         float kf[8], vf[8];
         unpack8(ku, kf);
         unpack8(vu, vf);
@@ -157,11 +187,8 @@ attn_decode_kernel(const __nv_bfloat16 *__restrict__ Q, const __nv_bfloat16 *__r
                 mx[qi] = mn;
             }
         }
-        ku = ku1;
-        vu = vu1;
-        ku1 = kn;
-        vu1 = vn;
     }
+    cp_async_wait<0>(); // no copy may still target the ring when the CTA moves on
     // the warp's four row groups (lanes j, j + 8, j + 16, j + 24) into lanes 0-7
 #pragma unroll
     for (int off = 8; off <= 16; off *= 2) {
