@@ -55,7 +55,12 @@ def test_kernel_selection():
     assert attn.select_kernel(32, 16, 128, 160, 64, bf, 1) == N.KERNEL_SHORT
     assert attn.select_kernel(4, 16, 8192, 8192, 64, bf, 2) == N.KERNEL_FLASH
     assert attn.select_kernel(1, 1, 16, 16, 64, f32, 0) == N.KERNEL_SIMT
-    assert attn.select_kernel(1, 1, 16, 16, 32, bf, 0) == N.KERNEL_SIMT
+    # bf16 heads narrower than 64 (multiples of 8) run zero-padded on tensor cores
+    assert attn.select_kernel(1, 1, 16, 16, 32, bf, 0) == N.KERNEL_SHORT
+    assert attn.select_kernel(1, 1, 300, 300, 16, bf, 2) == N.KERNEL_FLASH
+    assert attn.select_kernel(1, 1, 16, 16, 8, bf, 0) == N.KERNEL_SHORT
+    assert attn.select_kernel(1, 1, 16, 16, 20, bf, 0) == N.KERNEL_SIMT    # not a multiple of 8
+    assert attn.select_kernel(1, 1, 16, 16, 128, bf, 0) == N.KERNEL_SIMT   # wider than 64
     assert attn.select_kernel(1, 1, 16, 17, 64, bf, 2) == N.KERNEL_AUTO   # causal needs m == n
     assert attn.select_kernel(1, 1, 16, 16, 65, bf, 0) == N.KERNEL_SIMT   # d_k > 64: CUDA cores
     assert attn.select_kernel(1, 1, 16, 16, 129, bf, 0) == N.KERNEL_AUTO  # d_k > 128
@@ -88,10 +93,12 @@ def test_rejects_bad_arguments(kwargs, status):
 
 
 def test_rejects_unsupported_kernel_choice():
-    # fp32 on a tensor-core kernel, SHORT with m > 128, unknown kernel id
+    # fp32 on a tensor-core kernel, SHORT with m > 128, head widths the tensor-core
+    # kernels do not take, unknown kernel id
     assert _call(dims=(2, 2, 8, 8, 64, 1), kernel=N.KERNEL_FLASH) == 6
     assert _call(dims=(2, 2, 200, 200, 64, 0), kernel=N.KERNEL_SHORT) == 6
-    assert _call(dims=(2, 2, 8, 8, 32, 0), kernel=N.KERNEL_SHORT) == 6
+    assert _call(dims=(2, 2, 8, 8, 20, 0), kernel=N.KERNEL_SHORT) == 6   # d_k not a multiple of 8
+    assert _call(dims=(2, 2, 8, 8, 128, 0), kernel=N.KERNEL_FLASH) == 6  # wider than 64
     assert _call(kernel=17) == 6
 
 

@@ -276,6 +276,45 @@ WIDTHS = [
 
 @pytest.mark.parametrize("name,dtype,B,h,m,n,d,mask,lengths", WIDTHS, ids=[c[0] for c in WIDTHS])
 def test_head_widths(orc, name, dtype, B, h, m, n, d, mask, lengths):
+    """bf16 heads narrower than 64 run zero-padded on the tensor-core kernels (and still
+    on the CUDA-core one when asked); other widths and fp32 on the CUDA cores."""
     w = Workload(name, dtype, B, h, m, n, d, mask, d ** -0.5, 61, lengths)
-    assert attn.select_kernel(B, h, m, n, d, 0 if dtype == "bf16" else 1, mask) == K_SIMT
+    auto = attn.select_kernel(B, h, m, n, d, 0 if dtype == "bf16" else 1, mask)
+    if dtype == "bf16" and d <= 64:
+        assert auto == (K_SHORT if m <= 128 else K_FLASH)
+        check_full(orc, w, K_SIMT)
+    else:
+        assert auto == K_SIMT
     check_full(orc, w, K_AUTO)
+
+
+NARROW = [
+    # tensor-core kernels with zero-padded heads: pair mode, windows, padding, ragged tails
+    ("d8_pair_causal", 1, 3, 300, 300, 8, MASK_CAUSAL, None),
+    ("d16_pair_padding", 2, 2, 400, 400, 16, MASK_KEY_PADDING, (0, 400)),
+    ("d24_cross_split", 3, 2, 100, 230, 24, MASK_KEY_PADDING, (1, 230)),
+    ("d32_long_causal", 1, 2, 2048, 2048, 32, MASK_CAUSAL, None),
+    ("d48_pair_padding_causal", 2, 2, 333, 333, 48, MASK_CAUSAL | MASK_KEY_PADDING, (0, 333)),
+    ("d56_split_causal", 4, 2, 128, 128, 56, MASK_CAUSAL, None),
+]
+
+
+@pytest.mark.parametrize("name,B,h,m,n,d,mask,lengths", NARROW, ids=[c[0] for c in NARROW])
+def test_narrow_heads_tensor_cores(orc, name, B, h, m, n, d, mask, lengths):
+    w = Workload(name, "bf16", B, h, m, n, d, mask, d ** -0.5, 62, lengths)
+    kern = K_SHORT if m <= 128 else K_FLASH
+    assert attn.select_kernel(B, h, m, n, d, 0, mask) == kern
+    check_full(orc, w, kern)
+
+
+def test_narrow_heads_output_stays_in_bounds():
+    """A d_k = 16 launch writes exactly its [B, h, m, 16] output: the TMA store clips the
+    zero-padded columns (guard regions on both sides stay untouched)."""
+    w = Workload("guard16", "bf16", 2, 3, 300, 300, 16, MASK_CAUSAL, 0.25, 63)
+    inp = draw(w)
+    n_out = w.B * w.h * w.m * w.d
+    guard = 4096
+    buf = torch.full((n_out + 2 * guard,), -7.0, dtype=torch.bfloat16, device="cuda")
+    out = buf[guard:guard + n_out].view(w.B, w.h, w.m, w.d)
+    run(inp, K_FLASH, out=out)
+    assert (buf[:guard] == -7.0).all() and (buf[guard + n_out:] == -7.0).all()

@@ -19,12 +19,16 @@ bool overlaps(const void *a, uint64_t abytes, const void *b, uint64_t bbytes)
     return a0 < b0 + bbytes && b0 < a0 + abytes;
 }
 
-// Which kernel AUTO picks: tensor cores for bf16 with d_k == 64 (two heads per
-// CTA tile when a head has at most 128 queries, two query tiles of one head
-// otherwise); CUDA cores for fp32 and for narrower bf16 heads.
+// Heads the tensor-core kernels take: bf16, d_k a multiple of 8 up to 64 (narrower
+// heads run zero-padded to 64 inside the kernel).
+bool tensor_core_head(const attn_dims &d) { return d.dtype == ATTN_BF16 && d.d_k % 8 == 0 && d.d_k <= 64; }
+
+// Which kernel AUTO picks: tensor cores for tensor_core_head (two heads per CTA tile
+// when a head has at most 128 queries, two query tiles of one head otherwise); CUDA
+// cores for fp32 and for other bf16 head widths.
 int auto_kernel(const attn_dims &d)
 {
-    if (d.dtype == ATTN_BF16 && d.d_k == 64) return d.m <= 128 ? ATTN_KERNEL_SHORT : ATTN_KERNEL_FLASH;
+    if (tensor_core_head(d)) return d.m <= 128 ? ATTN_KERNEL_SHORT : ATTN_KERNEL_FLASH;
     return ATTN_KERNEL_SIMT;
 }
 
@@ -99,11 +103,11 @@ attn_status run(const void *Q, const void *K, const void *V, const int32_t *key_
         e = attn::launch_simt(p, s);
         break;
     case ATTN_KERNEL_FLASH:
-        if (!p.bf16 || p.d != 64) return ATTN_ERR_UNSUPPORTED;
+        if (!tensor_core_head(d)) return ATTN_ERR_UNSUPPORTED;
         e = attn::launch_flash(p, /*pair_mode=*/true, tile_counter, s);
         break;
     case ATTN_KERNEL_SHORT:
-        if (!p.bf16 || p.d != 64 || p.m > 128) return ATTN_ERR_UNSUPPORTED;
+        if (!tensor_core_head(d) || p.m > 128) return ATTN_ERR_UNSUPPORTED;
         e = attn::launch_flash(p, /*pair_mode=*/false, tile_counter, s);
         break;
     default:

@@ -118,6 +118,8 @@ struct FlashParams {
     __nv_bfloat16 *out;
     float *lse; // per-row log-sum-exp of the scaled scores (natural log), or nullptr
     int window; // restricted attention: keys with |i - j| <= window stay; -1: no window
+    int d;      // head width in memory (a multiple of 8, <= 64): narrower heads enter the
+                // 64-wide tiles zero-padded by the TMA loads and leave clipped by the store
     int BH, h, m, n, mask_kind;
     float scale_log2;
     int pair_mode;
@@ -552,19 +554,23 @@ __device__ __forceinline__ void recompute_scores(const FlashParams &p, int bh, i
                                                  int cnt, float (&x)[kBN])
 {
     const bool row_in = i < p.m;
-    const __nv_bfloat16 *qr = p.q + (static_cast<size_t>(bh) * p.m + (row_in ? i : 0)) * kD;
+    const __nv_bfloat16 *qr = p.q + (static_cast<size_t>(bh) * p.m + (row_in ? i : 0)) * p.d;
     float q[kD];
 #pragma unroll
-    for (int d = 0; d < kD; ++d) q[d] = row_in ? __bfloat162float(qr[d]) : 0.f;
+    for (int d = 0; d < kD; ++d) {
+        q[d] = 0.f;
+        if (row_in && d < p.d) q[d] = __bfloat162float(qr[d]);
+    }
     float srow[kBN];
 #pragma unroll 1
     for (int c = 0; c < kBN; ++c) {
         float v = -CUDART_INF_F;
         if (c < cnt && c >= cnt_lo) {
-            const __nv_bfloat16 *kr = p.k + (static_cast<size_t>(bh) * p.n + key0 + c) * kD;
+            const __nv_bfloat16 *kr = p.k + (static_cast<size_t>(bh) * p.n + key0 + c) * p.d;
             float a = 0.f;
 #pragma unroll
-            for (int d = 0; d < kD; ++d) a = fmaf(q[d], __bfloat162float(kr[d]), a);
+            for (int d = 0; d < kD; ++d)
+                if (d < p.d) a = fmaf(q[d], __bfloat162float(kr[d]), a);
             v = a * p.scale_log2;
         }
         srow[c] = v;
@@ -608,12 +614,12 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
         const int n_kv = slot ? T.n_kv[1] : T.n_kv[0];
         const int kv_len = slot ? T.kv_len[1] : T.kv_len[0];
         const int i = q0 + row;
-        __nv_bfloat16 *orow = p.out + (static_cast<size_t>(bh) * p.m + i) * kD;
+        __nv_bfloat16 *orow = p.out + (static_cast<size_t>(bh) * p.m + i) * p.d;
         if (n_kv <= kv_lo) { // no allowed key for any row of this tile: output 0
             if (i < p.m) {
                 uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-                for (int c = 0; c < kD / 8; ++c) reinterpret_cast<uint4 *>(orow)[c] = z;
+                for (int c = 0; c < p.d / 8; ++c) reinterpret_cast<uint4 *>(orow)[c] = z;
                 if (p.lse != nullptr) p.lse[static_cast<size_t>(bh) * p.m + i] = -CUDART_INF_F;
             }
             continue;
@@ -906,9 +912,12 @@ cudaError_t launch_flash(const Problem &pb, bool pair_mode, int *tile_counter, c
     }
     const int sms = infos[dev].sms;
     const int BH = pb.B * pb.h;
+    if (pb.d % 8 != 0 || pb.d < 8 || pb.d > kD) return cudaErrorInvalidValue;
+    // rows of d elements in 64-wide, 128-row boxes: columns d .. 63 of a load read as
+    // zero, and a store writes only columns below d
     CUtensorMap tq, tk, tv, to;
-    if (!encode_rows_map(&tq, pb.q, pb.m, BH) || !encode_rows_map(&tk, pb.k, pb.n, BH) ||
-        !encode_rows_map(&tv, pb.v, pb.n, BH) || !encode_rows_map(&to, pb.out, pb.m, BH))
+    if (!encode_bf16_3d(&tq, pb.q, pb.d, pb.m, BH, kBM) || !encode_bf16_3d(&tk, pb.k, pb.d, pb.n, BH, kBN) ||
+        !encode_bf16_3d(&tv, pb.v, pb.d, pb.n, BH, kBN) || !encode_bf16_3d(&to, pb.out, pb.d, pb.m, BH, kBM))
         return cudaErrorInvalidValue;
     FlashParams p;
     p.q = static_cast<const __nv_bfloat16 *>(pb.q);
@@ -917,6 +926,7 @@ cudaError_t launch_flash(const Problem &pb, bool pair_mode, int *tile_counter, c
     p.out = static_cast<__nv_bfloat16 *>(pb.out);
     p.lse = pb.lse;
     p.window = (pb.mask_kind & kMaskWindow) ? pb.window : -1;
+    p.d = pb.d;
     p.BH = BH;
     p.h = pb.h;
     p.m = pb.m;

@@ -27,7 +27,8 @@ enum : int { kMaskKeyPadding = 1, kMaskCausal = 2, kMaskWindow = 4 };
 // CUDA-core kernel: fp32 arithmetic, d <= 64, any m, n.
 cudaError_t launch_simt(const Problem &p, cudaStream_t stream);
 
-// tcgen05/TMA kernel (bf16, d == 64).  pair_mode: each CTA tile holds two
+// tcgen05/TMA kernel (bf16, d a multiple of 8 up to 64: narrower heads enter the
+// 64-wide tiles zero-padded by the TMA loads and leave clipped by the TMA store).  pair_mode: each CTA tile holds two
 // consecutive 128-row query tiles of one head sharing K/V; otherwise each
 // CTA tile holds one 128-row query tile of each of two heads (m <= 128).
 // tile_counter: two zeroed ints in global memory for the dynamic tile
