@@ -151,18 +151,20 @@ JUMP_CASES = [
 ]
 
 
-def jump_inputs(name, B, h, m, n, mask, lengths, soft, hard):
+def jump_inputs(name, B, h, m, n, mask, lengths, soft, hard, d=64):
     """Seeded inputs in which the listed rows' scores grow sharply after their first
     key tiles: by ~20 log2 units (exponentials against the running reference stay
     finite but leave the kept range) and by > 128 (they overflow fp32).  The two
-    large keys also make most other rows peaked."""
-    w = Workload(name, "bf16", B, h, m, n, 64, mask, 0.125, 321, lengths)
+    large keys also make most other rows peaked.  Any head width d (the dot products
+    are the same: half the width carries the values)."""
+    w = Workload(name, "bf16", B, h, m, n, d, mask, 0.125, 321, lengths)
     inp = draw(w)
     bits = lambda x: np.uint16(np.array(x, dtype=np.float32).view(np.uint32) >> 16)  # exact in bf16
-    inp.q[:, :, soft, :32], inp.q[:, :, soft, 32:] = bits(1.0), bits(0.0)
-    inp.q[:, :, hard, :32], inp.q[:, :, hard, 32:] = bits(0.0), bits(1.0)
-    inp.k[:, :, 260, :32], inp.k[:, :, 260, 32:] = bits(4.0), bits(0.0)   # soft rows: S = 128
-    inp.k[:, :, 400, :32], inp.k[:, :, 400, 32:] = bits(0.0), bits(32.0)  # hard rows: S = 1024
+    hd = d // 2
+    inp.q[:, :, soft, :hd], inp.q[:, :, soft, hd:] = bits(1.0), bits(0.0)
+    inp.q[:, :, hard, :hd], inp.q[:, :, hard, hd:] = bits(0.0), bits(1.0)
+    inp.k[:, :, 260, :hd], inp.k[:, :, 260, hd:] = bits(128.0 / hd), bits(0.0)   # soft rows: q.k = 128
+    inp.k[:, :, 400, :hd], inp.k[:, :, 400, hd:] = bits(0.0), bits(1024.0 / hd)  # hard rows: q.k = 1024
     return w, inp
 
 
@@ -181,6 +183,21 @@ def test_score_jumps_between_key_tiles(orc, name, B, h, m, n, mask, lengths, sof
         got = as_f64(run(inp, kern))
         assert np.isfinite(got).all()
         assert np.abs(got - ref).max() <= 1e-2, f"kernel {kern}: " + report(got, ref, 1e-2)
+
+
+@pytest.mark.parametrize("name,B,h,m,n,mask,lengths,soft,hard", JUMP_CASES, ids=[c[0] for c in JUMP_CASES])
+def test_score_jumps_narrow_heads(orc, name, B, h, m, n, mask, lengths, soft, hard):
+    """The score jumps with d_k = 32 on the tensor-core kernels: the rescale and the
+    score recomputation (which reads Q and K rows of the true width) stay exact."""
+    w, inp = jump_inputs(name, B, h, m, n, mask, lengths, soft, hard, d=32)
+    rng = np.random.default_rng(6)
+    vals = rng.uniform(-1.0, 1.0, size=inp.v.shape).astype(np.float32)
+    inp.v[...] = (vals.view(np.uint32) >> 16).astype(np.uint16)
+    ref = orc.attn_fwd(inp.q, inp.k, inp.v, inp.key_lengths, w.mask, w.scale)
+    kern = K_SHORT if m <= 128 else K_FLASH
+    got = as_f64(run(inp, kern))
+    assert np.isfinite(got).all()
+    assert np.abs(got - ref).max() <= 1e-2, report(got, ref, 1e-2)
 
 
 @pytest.mark.parametrize("name,B,h,m,n,mask,lengths,soft,hard", JUMP_CASES, ids=[c[0] for c in JUMP_CASES])
