@@ -118,14 +118,14 @@ struct FlashParams {
     __nv_bfloat16 *out;
     float *lse; // per-row log-sum-exp of the scaled scores (natural log), or nullptr
     int window; // restricted attention: keys with |i - j| <= window stay; -1: no window
-    int d;      // head width in memory (a multiple of 8, <= 64): narrower heads enter the
-                // 64-wide tiles zero-padded by the TMA loads and leave clipped by the store
     int BH, h, m, n, mask_kind;
     float scale_log2;
     int pair_mode;
     int num_tiles;
     int q_pairs;        // pair mode: query-tile pairs per head
     int *tile_counter;  // [0] next tile to claim, [1] CTAs done; nullptr: static snake schedule
+    int d;              // head width in memory (a multiple of 8, <= 64): narrower heads enter
+                        // the 64-wide tiles zero-padded by the TMA loads and leave clipped by the store
 };
 
 struct Tile {
@@ -550,27 +550,33 @@ __device__ __forceinline__ float weights_bf16(const float (&x)[kBN], bool presca
 // is allowed iff cnt_lo <= c < cnt; allowed keys are below n).  Rows past m read as zero
 // queries, as the TMA loads fill them.  Taken only when a tile's exponentials
 // against the running reference overflowed, so it favours size over speed.
+template <bool kNarrow>
 __device__ __forceinline__ void recompute_scores(const FlashParams &p, int bh, int i, int key0, int cnt_lo,
                                                  int cnt, float (&x)[kBN])
 {
     const bool row_in = i < p.m;
-    const __nv_bfloat16 *qr = p.q + (static_cast<size_t>(bh) * p.m + (row_in ? i : 0)) * p.d;
+    const int width = kNarrow ? p.d : kD; // elements per row in memory
+    const __nv_bfloat16 *qr = p.q + (static_cast<size_t>(bh) * p.m + (row_in ? i : 0)) * width;
     float q[kD];
 #pragma unroll
     for (int d = 0; d < kD; ++d) {
-        q[d] = 0.f;
-        if (row_in && d < p.d) q[d] = __bfloat162float(qr[d]);
+        if (kNarrow) {
+            q[d] = 0.f;
+            if (row_in && d < width) q[d] = __bfloat162float(qr[d]);
+        } else {
+            q[d] = row_in ? __bfloat162float(qr[d]) : 0.f;
+        }
     }
     float srow[kBN];
 #pragma unroll 1
     for (int c = 0; c < kBN; ++c) {
         float v = -CUDART_INF_F;
         if (c < cnt && c >= cnt_lo) {
-            const __nv_bfloat16 *kr = p.k + (static_cast<size_t>(bh) * p.n + key0 + c) * p.d;
+            const __nv_bfloat16 *kr = p.k + (static_cast<size_t>(bh) * p.n + key0 + c) * width;
             float a = 0.f;
 #pragma unroll
             for (int d = 0; d < kD; ++d)
-                if (d < p.d) a = fmaf(q[d], __bfloat162float(kr[d]), a);
+                if (!kNarrow || d < width) a = fmaf(q[d], __bfloat162float(kr[d]), a);
             v = a * p.scale_log2;
         }
         srow[c] = v;
@@ -581,7 +587,7 @@ __device__ __forceinline__ void recompute_scores(const FlashParams &p, int bh, i
 
 // kWindow: the launch has a restricted-attention window (compiled separately so
 // that launches without one run none of its bound arithmetic).
-template <bool kWindow>
+template <bool kWindow, bool kNarrow>
 __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParams &p, const CUtensorMap *tm_o,
                                              uint32_t tmem, int slot)
 {
@@ -614,12 +620,13 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
         const int n_kv = slot ? T.n_kv[1] : T.n_kv[0];
         const int kv_len = slot ? T.kv_len[1] : T.kv_len[0];
         const int i = q0 + row;
-        __nv_bfloat16 *orow = p.out + (static_cast<size_t>(bh) * p.m + i) * p.d;
+        const int width = kNarrow ? p.d : kD; // elements per row in memory
+        __nv_bfloat16 *orow = p.out + (static_cast<size_t>(bh) * p.m + i) * width;
         if (n_kv <= kv_lo) { // no allowed key for any row of this tile: output 0
             if (i < p.m) {
                 uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-                for (int c = 0; c < p.d / 8; ++c) reinterpret_cast<uint4 *>(orow)[c] = z;
+                for (int c = 0; c < width / 8; ++c) reinterpret_cast<uint4 *>(orow)[c] = z;
                 if (p.lse != nullptr) p.lse[static_cast<size_t>(bh) * p.m + i] = -CUDART_INF_F;
             }
             continue;
@@ -708,7 +715,7 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
                     // units, or are not finite).  The scores have left the registers:
                     // recompute this row's from Q and K, already scaled and masked,
                     // and take their max.
-                    recompute_scores(p, bh, i, key0, cnt_lo, cnt, x);
+                    recompute_scores<kNarrow>(p, bh, i, key0, cnt_lo, cnt, x);
                     move_reference(x, true, sl2, m_run, m_use, alpha, grow);
                     tile_sum = weights_bf16(x, true, sl2, m_use, pk);
                 }
@@ -795,10 +802,11 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
     if (row == 0) bulk_wait_all();
 }
 
-// kWindow: compiled separately for launches with a restricted-attention window, so
-// each kernel holds only the softmax variant it runs (the short workloads are
-// dominated by cold first tiles, where instruction fetch counts).
-template <bool kWindow>
+// kWindow: compiled separately for launches with a restricted-attention window;
+// kNarrow: for heads narrower than 64 (row width read from the parameters).  Each
+// kernel holds only the code it runs: its speed depends on instruction fetch (the
+// short workloads are dominated by cold first tiles) and on code layout.
+template <bool kWindow, bool kNarrow>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_flash_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -848,7 +856,7 @@ attn_flash_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // CTA-wide barrier (every thread arrives exactly once) and returns.
     if (warp < 4 * kSlots) {
         regs_increase<kSoftmaxRegs>();
-        softmax_role<kWindow>(sm, p, &tm_o, tmem, warp / 4);
+        softmax_role<kWindow, kNarrow>(sm, p, &tm_o, tmem, warp / 4);
         tc_fence_before();
         __syncthreads();
         return;
@@ -901,12 +909,14 @@ cudaError_t launch_flash(const Problem &pb, bool pair_mode, int *tile_counter, c
         DeviceInfo &di = infos[dev];
         if (!di.configured) {
             if ((e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-            if ((e = cudaFuncSetAttribute(attn_flash_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          static_cast<int>(kSmemBytes))) != cudaSuccess)
-                return e;
-            if ((e = cudaFuncSetAttribute(attn_flash_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          static_cast<int>(kSmemBytes))) != cudaSuccess)
-                return e;
+            const void *kernels[4] = {reinterpret_cast<const void *>(attn_flash_kernel<false, false>),
+                                      reinterpret_cast<const void *>(attn_flash_kernel<true, false>),
+                                      reinterpret_cast<const void *>(attn_flash_kernel<false, true>),
+                                      reinterpret_cast<const void *>(attn_flash_kernel<true, true>)};
+            for (const void *k : kernels)
+                if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              static_cast<int>(kSmemBytes))) != cudaSuccess)
+                    return e;
             di.configured = true;
         }
     }
@@ -938,10 +948,19 @@ cudaError_t launch_flash(const Problem &pb, bool pair_mode, int *tile_counter, c
     p.num_tiles = pair_mode ? BH * p.q_pairs : (BH + 1) / 2;
     p.tile_counter = tile_counter;
     const int grid = p.num_tiles < sms ? p.num_tiles : sms;
-    if (p.window >= 0)
-        attn_flash_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, p);
-    else
-        attn_flash_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, p);
+    // compiled four times: with or without a window, full or narrower heads
+    const bool narrow = pb.d != kD;
+    if (p.window >= 0) {
+        if (narrow)
+            attn_flash_kernel<true, true><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, p);
+        else
+            attn_flash_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, p);
+    } else {
+        if (narrow)
+            attn_flash_kernel<false, true><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, p);
+        else
+            attn_flash_kernel<false, false><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, p);
+    }
     return cudaGetLastError();
 }
 
