@@ -72,7 +72,7 @@ namespace {
 
 attn_status run(const void *Q, const void *K, const void *V, const int32_t *key_lengths, int mask_kind, float scale,
                 void *out, const attn_dims *dims, void *stream, int kernel, int *tile_counter, float *lse = nullptr,
-                int window = -1)
+                int window = -1, bool overlap_launch = false)
 {
     // the window bit is accepted only from attn_fwd_window (window >= 0), which checks it
     const int checked = window >= 0 ? (mask_kind & ~ATTN_MASK_WINDOW) : mask_kind;
@@ -96,6 +96,7 @@ attn_status run(const void *Q, const void *K, const void *V, const int32_t *key_
     p.window = window;
     p.scale = scale;
     p.bf16 = d.dtype == ATTN_BF16;
+    p.overlap_launch = overlap_launch;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     switch (kernel) {
@@ -466,7 +467,10 @@ attn_status attn_mha_fwd(const void *Xq, const void *Xkv, const void *Wq, const 
     // the three input projections in one launch
     if (attn::launch_proj_multi(in3, 3, s) != cudaSuccess) return ATTN_ERR_CUDA;
     attn_dims ad{d.B, d.h, d.m, d.n, 64, ATTN_BF16};
-    st = run(Q, K, V, key_lengths, mask_kind, scale, O, &ad, stream, ATTN_KERNEL_AUTO, nullptr);
+    // the attention and the output projection each start as programmatic dependents of
+    // the launch before them: their set-up overlaps its tail, and each waits for it to
+    // complete before reading its output
+    st = run(Q, K, V, key_lengths, mask_kind, scale, O, &ad, stream, ATTN_KERNEL_AUTO, nullptr, nullptr, -1, true);
     if (st != ATTN_OK) return st;
     pp.mode = attn::kProjOut;
     pp.a = O;
@@ -475,6 +479,7 @@ attn_status attn_mha_fwd(const void *Xq, const void *Xkv, const void *Wq, const 
     pp.L = d.m;
     pp.K = d.h * 64;
     pp.N = d.d_model;
+    pp.overlap_launch = true;
     return attn::launch_proj(pp, s) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

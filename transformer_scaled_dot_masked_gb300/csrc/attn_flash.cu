@@ -851,6 +851,9 @@ attn_flash_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
+    // set-up above overlaps the previous kernel's tail when launched as its programmatic
+    // dependent; nothing below may read what that kernel writes before it completes
+    grid_dependency_wait();
 
     // The two register regions never rejoin: each branch ends with its own
     // CTA-wide barrier (every thread arrives exactly once) and returns.
@@ -950,18 +953,23 @@ cudaError_t launch_flash(const Problem &pb, bool pair_mode, int *tile_counter, c
     const int grid = p.num_tiles < sms ? p.num_tiles : sms;
     // compiled four times: with or without a window, full or narrower heads
     const bool narrow = pb.d != kD;
-    if (p.window >= 0) {
-        if (narrow)
-            attn_flash_kernel<true, true><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, p);
-        else
-            attn_flash_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, p);
-    } else {
-        if (narrow)
-            attn_flash_kernel<false, true><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, p);
-        else
-            attn_flash_kernel<false, false><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, p);
+    auto kernel = p.window >= 0 ? (narrow ? attn_flash_kernel<true, true> : attn_flash_kernel<true, false>)
+                                : (narrow ? attn_flash_kernel<false, true> : attn_flash_kernel<false, false>);
+    if (!pb.overlap_launch) {
+        kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, p);
+        return cudaGetLastError();
     }
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, to, p);
 }
 
 cudaError_t flash_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint32_t *info)

@@ -171,6 +171,9 @@ attn_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
+    // set-up above overlaps the previous kernel's tail when launched as its programmatic
+    // dependent; nothing below may read what that kernel writes before it completes
+    grid_dependency_wait();
 
     if (warp == 0) {
         if (threadIdx.x == 0) {
@@ -386,8 +389,21 @@ cudaError_t launch_proj_multi(const ProjProblem *pps, int count, cudaStream_t st
     int sms = 0;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const int grid = p.tiles < sms ? p.tiles : sms;
-    attn_proj_kernel<<<grid, kThreads, kSmemBytes, stream>>>(maps, p);
-    return cudaGetLastError();
+    if (!p0.overlap_launch) {
+        attn_proj_kernel<<<grid, kThreads, kSmemBytes, stream>>>(maps, p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_proj_kernel, maps, p);
 }
 
 cudaError_t launch_proj(const ProjProblem &pp, cudaStream_t stream) { return launch_proj_multi(&pp, 1, stream); }

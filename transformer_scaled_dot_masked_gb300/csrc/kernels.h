@@ -20,6 +20,8 @@ struct Problem {
     int window = -1; // window half-width when bit 2 is set (keys with |i - j| <= window stay)
     float scale;    // >= 0
     bool bf16;      // element type of q, k, v, out (fp32 otherwise)
+    bool overlap_launch = false; // tensor-core kernels: launched as a programmatic dependent of the
+                                 // previous kernel on the stream (its prologue overlaps that kernel's tail)
 };
 
 enum : int { kMaskKeyPadding = 1, kMaskCausal = 2, kMaskWindow = 4 };
@@ -85,6 +87,7 @@ struct ProjProblem {
     const void *w;   // [K][N], K = d_model (kIn) or h * 64 (kOut)
     void *out;       // kIn: [B*h][L][64]; kOut: [B][L][N]
     int B, h, L, K, N;
+    bool overlap_launch = false; // launched as a programmatic dependent of the previous kernel on the stream
 };
 cudaError_t launch_proj(const ProjProblem &p, cudaStream_t stream);
 // Up to three products of one shape (mode, B, h, K, N; L may differ) in one launch.

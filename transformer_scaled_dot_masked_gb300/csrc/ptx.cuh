@@ -182,6 +182,11 @@ __device__ __forceinline__ void st_shared_v4_ordered(uint32_t addr, uint4 v)
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
 }
 
+// Wait until the grids this launch depends on programmatically (a launch with the
+// programmatic stream serialization attribute) have completed and their writes are
+// visible; a no-op for an ordinary launch.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols)
 {
