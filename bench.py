@@ -86,7 +86,7 @@ def row_pairs(w, lengths, rows) -> float:
 # DRAM bytes (read + write) of one flash-kernel launch on the default workload,
 # from an ncu capture (profiles/attn_flash_long_causal_8192.md), keyed by a hash of
 # the kernel source it was taken on: any later change to the kernel reports null.
-MEASURED_TRAFFIC = {"9deb77ad86ab5ac3": 839793408 + 47095296}
+MEASURED_TRAFFIC = {"5762ae7212cbf6b5": 842824960 + 46914816}
 
 
 def measured_traffic():
