@@ -85,7 +85,8 @@ typedef enum {
     ATTN_KERNEL_AUTO = 0,  /* let the library choose (what attn_fwd does) */
     ATTN_KERNEL_FLASH = 1, /* tcgen05/TMA flash kernel, 256 query rows per CTA tile (bf16, d_k a multiple of 8, <= 64) */
     ATTN_KERNEL_SHORT = 2, /* same machinery, two heads per CTA tile, whole head resident (bf16, d_k as FLASH, m <= 128) */
-    ATTN_KERNEL_SIMT = 3   /* CUDA-core fp32 kernel (fp32 or bf16, d_k <= 128) */
+    ATTN_KERNEL_SIMT = 3,  /* CUDA-core fp32 kernel (fp32 or bf16, d_k <= 128) */
+    ATTN_KERNEL_WIDE = 4   /* tcgen05/TMA kernel for d_k == 128, one 128-row query tile per CTA (bf16, no window) */
 } attn_kernel;
 
 typedef struct {
@@ -120,8 +121,8 @@ typedef struct {
  * finite: non-finite values propagate through the arithmetic as IEEE rules
  * dictate.  Kernel choice: bf16 with d_k a multiple of 8 up to 64 runs on tensor
  * cores, narrower heads zero-padded to 64 inside the kernel (ATTN_KERNEL_SHORT
- * when m <= 128, else ATTN_KERNEL_FLASH); everything else
- * runs ATTN_KERNEL_SIMT.
+ * when m <= 128, else ATTN_KERNEL_FLASH); bf16 with d_k == 128 on
+ * ATTN_KERNEL_WIDE (tensor cores); everything else runs ATTN_KERNEL_SIMT.
  */
 attn_status attn_fwd(const void *Q, const void *K, const void *V,
                      const int32_t *key_lengths, int mask_kind, float scale,

@@ -60,7 +60,9 @@ def test_kernel_selection():
     assert attn.select_kernel(1, 1, 300, 300, 16, bf, 2) == N.KERNEL_FLASH
     assert attn.select_kernel(1, 1, 16, 16, 8, bf, 0) == N.KERNEL_SHORT
     assert attn.select_kernel(1, 1, 16, 16, 20, bf, 0) == N.KERNEL_SIMT    # not a multiple of 8
-    assert attn.select_kernel(1, 1, 16, 16, 128, bf, 0) == N.KERNEL_SIMT   # wider than 64
+    assert attn.select_kernel(1, 1, 16, 16, 128, bf, 0) == N.KERNEL_WIDE   # 128 wide: its own kernel
+    assert attn.select_kernel(1, 1, 16, 16, 96, bf, 0) == N.KERNEL_SIMT    # other widths above 64
+    assert attn.select_kernel(1, 1, 16, 16, 128, f32, 0) == N.KERNEL_SIMT
     assert attn.select_kernel(1, 1, 16, 17, 64, bf, 2) == N.KERNEL_AUTO   # causal needs m == n
     assert attn.select_kernel(1, 1, 16, 16, 65, bf, 0) == N.KERNEL_SIMT   # d_k > 64: CUDA cores
     assert attn.select_kernel(1, 1, 16, 16, 129, bf, 0) == N.KERNEL_AUTO  # d_k > 128
@@ -99,6 +101,8 @@ def test_rejects_unsupported_kernel_choice():
     assert _call(dims=(2, 2, 200, 200, 64, 0), kernel=N.KERNEL_SHORT) == 6
     assert _call(dims=(2, 2, 8, 8, 20, 0), kernel=N.KERNEL_SHORT) == 6   # d_k not a multiple of 8
     assert _call(dims=(2, 2, 8, 8, 128, 0), kernel=N.KERNEL_FLASH) == 6  # wider than 64
+    assert _call(dims=(2, 2, 8, 8, 64, 0), kernel=N.KERNEL_WIDE) == 6    # the wide kernel: d_k 128 only
+    assert _call(dims=(2, 2, 8, 8, 128, 1), kernel=N.KERNEL_WIDE) == 6   # and bf16 only
     assert _call(kernel=17) == 6
 
 

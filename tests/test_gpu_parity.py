@@ -16,6 +16,7 @@ from gpu_helpers import as_f64, report, run, to_device, tol_for
 pytestmark = pytest.mark.gpu
 
 K_FLASH, K_SHORT, K_SIMT, K_AUTO = attn.KERNEL_FLASH, attn.KERNEL_SHORT, attn.KERNEL_SIMT, attn.KERNEL_AUTO
+K_WIDE = attn.KERNEL_WIDE
 
 
 def kernels_for(w: Workload):
@@ -300,9 +301,55 @@ def test_head_widths(orc, name, dtype, B, h, m, n, d, mask, lengths):
     if dtype == "bf16" and d <= 64:
         assert auto == (K_SHORT if m <= 128 else K_FLASH)
         check_full(orc, w, K_SIMT)
+    elif dtype == "bf16" and d == 128:
+        assert auto == K_WIDE
+        check_full(orc, w, K_SIMT)
     else:
         assert auto == K_SIMT
     check_full(orc, w, K_AUTO)
+
+
+WIDE_CASES = [
+    # d_k = 128 on the tensor-core kernel: ragged query and key tiles, padding (with
+    # empty rows), causal, cross-attention, a long sequence, a single query
+    ("causal_ragged", 2, 3, 300, 300, MASK_CAUSAL, None),
+    ("padding_with_empty", 3, 2, 200, 200, MASK_KEY_PADDING, (0, 200)),
+    ("cross_padding", 2, 4, 100, 333, MASK_KEY_PADDING, (1, 333)),
+    ("long_causal", 1, 2, 2048, 2048, MASK_CAUSAL, None),
+    ("no_mask_long_keys", 1, 3, 128, 1000, MASK_NONE, None),
+    ("causal_padding", 2, 2, 260, 260, MASK_CAUSAL | MASK_KEY_PADDING, (0, 260)),
+    ("single_query", 4, 2, 1, 77, MASK_NONE, None),
+]
+
+
+@pytest.mark.parametrize("name,B,h,m,n,mask,lengths", WIDE_CASES, ids=[c[0] for c in WIDE_CASES])
+def test_wide_heads_tensor_cores(orc, name, B, h, m, n, mask, lengths):
+    w = Workload(name, "bf16", B, h, m, n, 128, mask, 128 ** -0.5, 64, lengths)
+    assert attn.select_kernel(B, h, m, n, 128, 0, mask) == K_WIDE
+    check_full(orc, w, K_WIDE)
+
+
+def test_wide_heads_lse_and_bounds(orc):
+    """The log-sum-exp output of the wide kernel, and that it writes exactly its output
+    (guard regions on both sides untouched)."""
+    w = Workload("wide_lse", "bf16", 2, 3, 200, 200, 128, MASK_CAUSAL | MASK_KEY_PADDING, 0.09, 65, (0, 200))
+    inp = draw(w)
+    q, k, v = (to_device(x, "bf16") for x in (inp.q, inp.k, inp.v))
+    lens = torch.from_numpy(inp.key_lengths).cuda()
+    out, lse = attn.attn_fwd_lse(q, k, v, lens, w.mask, w.scale)
+    torch.cuda.synchronize()
+    ref = orc.attn_lse(inp.q, inp.k, inp.key_lengths, w.mask, w.scale)
+    got = lse.double().cpu().numpy()
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isfinite(got), fin)
+    assert np.abs(got[fin] - ref[fin]).max() <= 2e-3
+    n_out = w.B * w.h * w.m * w.d
+    guard = 4096
+    buf = torch.full((n_out + 2 * guard,), -7.0, dtype=torch.bfloat16, device="cuda")
+    o2 = buf[guard:guard + n_out].view(w.B, w.h, w.m, w.d)
+    run(inp, K_WIDE, out=o2)
+    assert (buf[:guard] == -7.0).all() and (buf[guard + n_out:] == -7.0).all()
+    np.testing.assert_array_equal(as_f64(o2), as_f64(out))
 
 
 NARROW = [

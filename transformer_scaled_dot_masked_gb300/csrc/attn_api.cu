@@ -29,6 +29,7 @@ bool tensor_core_head(const attn_dims &d) { return d.dtype == ATTN_BF16 && d.d_k
 int auto_kernel(const attn_dims &d)
 {
     if (tensor_core_head(d)) return d.m <= 128 ? ATTN_KERNEL_SHORT : ATTN_KERNEL_FLASH;
+    if (d.dtype == ATTN_BF16 && d.d_k == 128) return ATTN_KERNEL_WIDE;
     return ATTN_KERNEL_SIMT;
 }
 
@@ -79,7 +80,10 @@ attn_status run(const void *Q, const void *K, const void *V, const int32_t *key_
     const attn_status st = validate(Q, K, V, key_lengths, checked, scale, out, dims);
     if (st != ATTN_OK) return st;
     const attn_dims &d = *dims;
-    if (kernel == ATTN_KERNEL_AUTO) kernel = auto_kernel(d);
+    if (kernel == ATTN_KERNEL_AUTO) {
+        kernel = auto_kernel(d);
+        if (kernel == ATTN_KERNEL_WIDE && window >= 0) kernel = ATTN_KERNEL_SIMT; // no window in the wide kernel
+    }
     attn::Problem p;
     p.q = Q;
     p.k = K;
@@ -106,6 +110,10 @@ attn_status run(const void *Q, const void *K, const void *V, const int32_t *key_
     case ATTN_KERNEL_FLASH:
         if (!tensor_core_head(d)) return ATTN_ERR_UNSUPPORTED;
         e = attn::launch_flash(p, /*pair_mode=*/true, tile_counter, s);
+        break;
+    case ATTN_KERNEL_WIDE:
+        if (!p.bf16 || p.d != 128 || window >= 0) return ATTN_ERR_UNSUPPORTED;
+        e = attn::launch_wide(p, s);
         break;
     case ATTN_KERNEL_SHORT:
         if (!tensor_core_head(d) || p.m > 128) return ATTN_ERR_UNSUPPORTED;
@@ -674,6 +682,13 @@ attn_status attn_device_status(void *stream, int32_t *info)
     uint32_t pcode = 0, pwhere = 0;
     if (attn::proj_status_read_and_clear(static_cast<cudaStream_t>(stream), &pcode, &pwhere) != cudaSuccess)
         return ATTN_ERR_CUDA;
+    uint32_t wcode = 0, wwhere = 0;
+    if (attn::wide_status_read_and_clear(static_cast<cudaStream_t>(stream), &wcode, &wwhere) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    if (code == 0 && wcode != 0) {
+        code = wcode;
+        where = 300 + wwhere; // wide-head wait sites are reported as 300 + site
+    }
     if (code == 0 && bcode == 0 && pcode != 0) {
         code = pcode;
         where = 200 + pwhere; // projection wait sites are reported as 200 + site
