@@ -86,7 +86,7 @@ typedef enum {
     ATTN_KERNEL_FLASH = 1, /* tcgen05/TMA flash kernel, 256 query rows per CTA tile (bf16, d_k a multiple of 8, <= 64) */
     ATTN_KERNEL_SHORT = 2, /* same machinery, two heads per CTA tile, whole head resident (bf16, d_k as FLASH, m <= 128) */
     ATTN_KERNEL_SIMT = 3,  /* CUDA-core fp32 kernel (fp32 or bf16, d_k <= 128) */
-    ATTN_KERNEL_WIDE = 4   /* tcgen05/TMA kernel for d_k == 128, one 128-row query tile per CTA (bf16, no window) */
+    ATTN_KERNEL_WIDE = 4   /* tcgen05/TMA kernel for d_k == 128, one 128-row query tile per CTA (bf16) */
 } attn_kernel;
 
 typedef struct {

@@ -47,12 +47,17 @@ CASES = [
     ("split_mode_w64_causal", "bf16", 4, 2, 128, MASK_CAUSAL, 64, None),
     ("fp32_w7", "fp32", 2, 2, 150, MASK_KEY_PADDING, 7, (1, 150)),
     ("narrow_heads_w3", "bf16_d32", 2, 2, 90, MASK_CAUSAL, 3, None),
+    ("wide_heads_w0", "bf16_d128", 2, 2, 300, 0, 0, None),
+    ("wide_heads_w127_causal", "bf16_d128", 2, 2, 700, MASK_CAUSAL, 127, None),
+    ("wide_heads_w128_padding", "bf16_d128", 3, 2, 700, MASK_KEY_PADDING, 128, (0, 700)),
+    ("wide_heads_w200_causal_padding", "bf16_d128", 2, 2, 1000, MASK_CAUSAL | MASK_KEY_PADDING, 200, (100, 1000)),
+    ("wide_heads_covering_window", "bf16_d128", 2, 2, 260, 0, 5000, None),
 ]
 
 
 @pytest.mark.parametrize("name,dtype,B,h,n,mask,window,lengths", CASES, ids=[c[0] for c in CASES])
 def test_window_matches_oracle(orc, name, dtype, B, h, n, mask, window, lengths):
-    d = 32 if dtype.endswith("d32") else 64
+    d = int(dtype.split("_d")[1]) if "_d" in dtype else 64
     w = Workload(name, dtype.split("_")[0], B, h, n, n, d, mask | WIN, d ** -0.5, 51, lengths)
     inp = draw(w)
     got = run_window(inp, mask | WIN, window)
@@ -61,9 +66,10 @@ def test_window_matches_oracle(orc, name, dtype, B, h, n, mask, window, lengths)
     assert np.abs(got - ref).max() <= tol, report(got, ref, tol)
 
 
-def test_window_locality_bitwise():
+@pytest.mark.parametrize("d", [64, 128])
+def test_window_locality_bitwise(d):
     """Row i is bitwise unchanged when keys and values further than the window from it change."""
-    w = Workload("loc", "bf16", 1, 2, 1024, 1024, 64, WIN, 0.125, 52)
+    w = Workload("loc", "bf16", 1, 2, 1024, 1024, d, WIN, d ** -0.5, 52)
     inp = draw(w)
     base = run_window(inp, WIN, 100)
     k2, v2 = inp.k.copy(), inp.v.copy()

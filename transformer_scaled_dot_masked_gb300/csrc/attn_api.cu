@@ -80,10 +80,7 @@ attn_status run(const void *Q, const void *K, const void *V, const int32_t *key_
     const attn_status st = validate(Q, K, V, key_lengths, checked, scale, out, dims);
     if (st != ATTN_OK) return st;
     const attn_dims &d = *dims;
-    if (kernel == ATTN_KERNEL_AUTO) {
-        kernel = auto_kernel(d);
-        if (kernel == ATTN_KERNEL_WIDE && window >= 0) kernel = ATTN_KERNEL_SIMT; // no window in the wide kernel
-    }
+    if (kernel == ATTN_KERNEL_AUTO) kernel = auto_kernel(d);
     attn::Problem p;
     p.q = Q;
     p.k = K;
@@ -112,7 +109,7 @@ attn_status run(const void *Q, const void *K, const void *V, const int32_t *key_
         e = attn::launch_flash(p, /*pair_mode=*/true, tile_counter, s);
         break;
     case ATTN_KERNEL_WIDE:
-        if (!p.bf16 || p.d != 128 || window >= 0) return ATTN_ERR_UNSUPPORTED;
+        if (!p.bf16 || p.d != 128) return ATTN_ERR_UNSUPPORTED;
         e = attn::launch_wide(p, s);
         break;
     case ATTN_KERNEL_SHORT:

@@ -13,7 +13,9 @@
 //   MMA:     O += P V_j                 (8 x M128 N128 K16, P from TMEM, V MN-major:
 //            its two 64-column atoms are the two halves of N)
 // The epilogue divides O by the row sum (0 for a row with no allowed key) and writes
-// bf16 rows.  TMEM (512 columns): S [0,128), P [128,192) bf16 pairs, O [256,384).
+// bf16 rows.  A restricted-attention window limits each CTA to the key tiles that
+// meet its rows' windows and masks the rest of each row's range.
+// TMEM (512 columns): S [0,128), P [128,192) bf16 pairs, O [256,384).
 //
 // Every mbarrier wait is bounded: one that runs out sets the CTA's abort flag and
 // this file's status word, every role leaves its loop, waits (bounded) for its own
@@ -69,6 +71,7 @@ struct WideParams {
     __nv_bfloat16 *out;
     float *lse;
     int BH, h, m, n, mask_kind, q_tiles;
+    int window; // restricted attention: keys with |i - j| <= window stay; -1: none
     float scale_log2;
 };
 
@@ -125,8 +128,15 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         len = __ldg(p.key_lengths + bh / p.h);
         len = len < 0 ? 0 : (len > p.n ? p.n : len);
     }
-    const int kv_end = causal ? min(len, q0 + kBM) : len;
-    const int n_kv = kv_end > 0 ? (kv_end + kBN - 1) / kBN : 0;
+    int kv_end = causal ? min(len, q0 + kBM) : len;
+    int kv_lo = 0; // first key tile
+    if (p.window >= 0) {
+        // keys within `window` of some row q0 .. min(m, q0 + 128) - 1 of the tile
+        kv_lo = max(0, q0 - p.window) / kBN;
+        kv_end = min(kv_end, min(p.m, q0 + kBM) + p.window);
+    }
+    // key tiles [kv_lo, kv_lo + n_kv); fill f of the ring holds key tile kv_lo + f
+    const int n_kv = kv_end > kv_lo * kBN ? (kv_end + kBN - 1) / kBN - kv_lo : 0;
 
     if (n_kv == 0) {
         // no allowed key for any row of this tile: output 0
@@ -181,10 +191,11 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const int st = j % kStages;
                 if (!wait_bar(&sm.kv_empty[st], ((j / kStages) & 1) ^ 1, ab, kSiteLoadKvEmpty)) break;
                 mbar_arrive_expect_tx(&sm.kv_full[st], 2 * kTileBytes);
-                tma_load_3d(sm.k[st], &tm_k, &sm.kv_full[st], 0, j * kBN, bh);
-                tma_load_3d(sm.k[st] + kAtomBytes, &tm_k, &sm.kv_full[st], 64, j * kBN, bh);
-                tma_load_3d(sm.v[st], &tm_v, &sm.kv_full[st], 0, j * kBN, bh);
-                tma_load_3d(sm.v[st] + kAtomBytes, &tm_v, &sm.kv_full[st], 64, j * kBN, bh);
+                const int key0 = (kv_lo + j) * kBN;
+                tma_load_3d(sm.k[st], &tm_k, &sm.kv_full[st], 0, key0, bh);
+                tma_load_3d(sm.k[st] + kAtomBytes, &tm_k, &sm.kv_full[st], 64, key0, bh);
+                tma_load_3d(sm.v[st], &tm_v, &sm.kv_full[st], 0, key0, bh);
+                tma_load_3d(sm.v[st] + kAtomBytes, &tm_v, &sm.kv_full[st], 64, key0, bh);
                 ++issued;
             }
             // copies still in flight must land before the CTA may exit
@@ -260,8 +271,14 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const uint32_t t_s = tmem + lane_base + kColS, t_p = tmem + lane_base + kColP;
         const uint32_t t_o = tmem + lane_base + kColO;
         const float sl2 = p.scale_log2;
-        // keys allowed for row i: [0, hi) (below the padded length, and i + 1 causal)
-        const int hi = causal ? min(len, i + 1) : len;
+        // keys allowed for row i: [lo, hi) (below the padded length, i + 1 causal, and
+        // within `window` of i)
+        int hi = causal ? min(len, i + 1) : len;
+        int lo = 0;
+        if (p.window >= 0) {
+            hi = min(hi, i + p.window + 1);
+            lo = i - p.window;
+        }
         float m_run = -CUDART_INF_F, l_run = 0.f;
         bool ok = true;
         for (int j = 0; j < n_kv && ok; ++j) {
@@ -277,12 +294,13 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             tc_fence_before();
             mbar_arrive(&sm.s_free);
             // scale first, then mask: a zero scale must not turn -inf into NaN
-            const int cnt = hi - j * kBN;
+            const int key0 = (kv_lo + j) * kBN;
+            const int cnt = hi - key0, cnt_lo = lo - key0;
             float x[kBN];
             float mt = -CUDART_INF_F;
 #pragma unroll
             for (int c = 0; c < kBN; ++c) {
-                x[c] = c < cnt ? __uint_as_float(sr[c]) * sl2 : -CUDART_INF_F;
+                x[c] = (c < cnt && c >= cnt_lo) ? __uint_as_float(sr[c]) * sl2 : -CUDART_INF_F;
                 mt = fmaxf(mt, x[c]);
             }
             const float m_new = fmaxf(m_run, mt);
@@ -382,7 +400,7 @@ cudaError_t launch_wide(const Problem &pb, cudaStream_t stream)
             configured[dev] = true;
         }
     }
-    if (!pb.bf16 || pb.d != kDW || (pb.mask_kind & kMaskWindow)) return cudaErrorInvalidValue;
+    if (!pb.bf16 || pb.d != kDW) return cudaErrorInvalidValue;
     const int BH = pb.B * pb.h;
     CUtensorMap tq, tk, tv;
     if (!encode_bf16_3d(&tq, pb.q, kDW, pb.m, BH, kBM) || !encode_bf16_3d(&tk, pb.k, kDW, pb.n, BH, kBN) ||
@@ -398,6 +416,7 @@ cudaError_t launch_wide(const Problem &pb, cudaStream_t stream)
     p.n = pb.n;
     p.mask_kind = pb.mask_kind;
     p.q_tiles = (pb.m + kBM - 1) / kBM;
+    p.window = (pb.mask_kind & kMaskWindow) ? pb.window : -1;
     p.scale_log2 = pb.scale * 1.4426950408889634f;
     const long long grid = static_cast<long long>(BH) * p.q_tiles;
     if (grid > 0x7fffffff) return cudaErrorInvalidValue;

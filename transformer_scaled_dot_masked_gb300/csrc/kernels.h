@@ -97,8 +97,7 @@ cudaError_t proj_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint
 // Device status word of the flash kernel (bounded waits that gave up).
 cudaError_t flash_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint32_t *info);
 
-// tcgen05/TMA kernel for bf16 heads of width 128 (one 128-row query tile per CTA,
-// no window).
+// tcgen05/TMA kernel for bf16 heads of width 128 (one 128-row query tile per CTA).
 cudaError_t launch_wide(const Problem &p, cudaStream_t stream);
 cudaError_t wide_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint32_t *info);
 
