@@ -202,6 +202,20 @@ def test_score_jumps_narrow_heads(orc, name, B, h, m, n, mask, lengths, soft, ha
 
 
 @pytest.mark.parametrize("name,B,h,m,n,mask,lengths,soft,hard", JUMP_CASES, ids=[c[0] for c in JUMP_CASES])
+def test_score_jumps_wide_heads(orc, name, B, h, m, n, mask, lengths, soft, hard):
+    """The score jumps with d_k = 128 on the wide kernel: its fixed per-row reference,
+    the power-of-two rescale and the score recomputation (of 128-wide rows)."""
+    w, inp = jump_inputs(name, B, h, m, n, mask, lengths, soft, hard, d=128)
+    rng = np.random.default_rng(7)
+    vals = rng.uniform(-1.0, 1.0, size=inp.v.shape).astype(np.float32)
+    inp.v[...] = (vals.view(np.uint32) >> 16).astype(np.uint16)
+    ref = orc.attn_fwd(inp.q, inp.k, inp.v, inp.key_lengths, w.mask, w.scale)
+    got = as_f64(run(inp, K_WIDE))
+    assert np.isfinite(got).all()
+    assert np.abs(got - ref).max() <= 1e-2, report(got, ref, 1e-2)
+
+
+@pytest.mark.parametrize("name,B,h,m,n,mask,lengths,soft,hard", JUMP_CASES, ids=[c[0] for c in JUMP_CASES])
 def test_peaked_rows_error_bound(orc, name, B, h, m, n, mask, lengths, soft, hard):
     """The same peaked rows with standard normal values, against the error bound of
     bf16 weights: per element |err| <= 2^-8 max|v| (weight rounding) + half an

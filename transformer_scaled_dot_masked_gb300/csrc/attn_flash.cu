@@ -51,6 +51,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "softmax_tile.cuh"
 
 namespace attn {
 
@@ -78,11 +79,6 @@ constexpr uint32_t kSlotCols = 256;
 constexpr uint32_t kColS = 0, kColP = 128, kColO = 192;
 constexpr int kTileRing = 4;              // CTA tile indices handed from the loader to the other roles
 constexpr uint32_t kTileConsumers = 2 + 2 * 128; // two MMA issuers, two softmax warpgroups
-// A key tile's exponentials are taken against the row's running reference max
-// and kept when their sum is at most 2^15 (so is every weight).  A larger finite
-// sum is brought back below 2^8 by an exact power of two; an infinite one (the
-// row's scores grew by 128 or more in log2 units) recomputes that row's scores.
-constexpr float kFastSumLimit = 32768.0f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull; // 2 s
 constexpr uint64_t kDrainLimitNs = 200000000ull; // 0.2 s
 
@@ -493,55 +489,6 @@ __device__ __forceinline__ void mma_role(SharedStorage &sm, const FlashParams &p
         mma_commit(&sm.drain[s]);
         drain_wait(&sm.drain[s], 0);
     }
-}
-
-// Row max of one key tile (x holds scores, or scores * scale * log2 e when
-// `prescaled`), in log2 units; moves the reference up to it if it is larger.
-// alpha rescales what was accumulated against the old reference (0 when there
-// was none).
-__device__ __forceinline__ void move_reference(const float (&x)[kBN], bool prescaled, float sl2, float m_run,
-                                               float &m_use, float &alpha, bool &grow)
-{
-    // four independent chains of three-input max
-    float mx[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) mx[k] = fmaxf(x[2 * k], x[2 * k + 1]);
-#pragma unroll
-    for (int c = 8; c < kBN; c += 8) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) mx[k] = max3(mx[k], x[c + 2 * k], x[c + 2 * k + 1]);
-    }
-    float row_max = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-    if (!prescaled) row_max *= sl2;
-    const float m_new = fmaxf(m_run, row_max);
-    grow = m_new > m_run;
-    m_use = grow ? m_new : m_run;
-    alpha = grow ? ex2(m_run - m_new) : 1.f;
-}
-
-// Weights exp2(x * scale * log2 e - m_use) of one key tile as bf16 pairs (column
-// 2c in the low half of pk[c]); returns their sum (before rounding).  The
-// exponent argument and the sum use packed two-lane fp32 ops.
-__device__ __forceinline__ float weights_bf16(const float (&x)[kBN], bool prescaled, float sl2, float m_use,
-                                              uint32_t (&pk)[kBN / 2])
-{
-    const float m_sub = (m_use == -CUDART_INF_F) ? 0.f : m_use;
-    const uint64_t mul2 = prescaled ? f2(1.f, 1.f) : f2(sl2, sl2);
-    const uint64_t sub2 = f2(-m_sub, -m_sub);
-    uint64_t acc2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
-#pragma unroll
-    for (int c2 = 0; c2 < kBN / 2; ++c2) {
-        const int c = 2 * c2;
-        float a0, a1;
-        unf2(fma2(f2(x[c], x[c + 1]), mul2, sub2), a0, a1);
-        const float e0 = ex2(a0), e1 = ex2(a1);
-        acc2[c2 & 1] = add2(acc2[c2 & 1], f2(e0, e1));
-        pk[c2] = pack_bf16x2(e0, e1);
-    }
-    float s0, s1, s2, s3;
-    unf2(acc2[0], s0, s1);
-    unf2(acc2[1], s2, s3);
-    return (s0 + s1) + (s2 + s3);
 }
 
 // Scores of query row i of head bh against keys key0 .. key0+127, recomputed on

@@ -3,19 +3,31 @@
 // equation of "Paper Deep Reading: Attention Is All You Need", §04, for the model
 // variants whose heads are 128 wide (the variants table of the same page).
 //
-// One CTA per (batch, head, 128-row query tile), heaviest query tiles first.  Q and
+// One CTA per (batch, head, pair of 128-row query tiles), heaviest pairs first.
+// The two tiles ("slots") share one stream of K and V tiles and take turns on the
+// tensor cores: while one slot's softmax runs, the other slot's MMAs do.  Q and
 // each 128-key tile of K and V are 128 x 128 bf16, loaded by TMA as two 64-column
 // boxes (128-byte swizzle atoms) 16 KiB apart; K and V pass through a two-stage ring.
-//   MMA:     S = Q K_j^T                (8 x M128 N128 K16: four K steps in each atom)
-//   softmax: 4 warps, thread r = row r = TMEM lane r; masked scores, online softmax
-//            (the row max of every key tile), P = exp2(S scale log2 e - max) as bf16
-//            pairs in TMEM; O is rescaled in TMEM when a row's max grows
-//   MMA:     O += P V_j                 (8 x M128 N128 K16, P from TMEM, V MN-major:
+//   MMA:     S_s = Q_s K_t^T            (8 x M128 N128 K16: four K steps in each atom)
+//   softmax: 4 warps per slot, thread r = row r = TMEM lane r; scores masked on
+//            boundary tiles only; P = exp2(S scale log2 e - r) as bf16 pairs written
+//            over the upper half of S, against a per-row reference r: the row max
+//            of the row's first key tile, moved up only when a later tile's sum
+//            exceeds 2^15 (by an exact power of two, or, when a weight
+//            overflowed, to the max of the row's recomputed scores); O is rescaled
+//            in TMEM only when r moves
+//   MMA:     O_s += P_s V_t             (8 x M128 N128 K16, P from TMEM, V MN-major:
 //            its two 64-column atoms are the two halves of N)
+// The MMA warp issues, per key tile t: O_0 += P_0 V_(t-1), S_0 = Q_0 K_t^T,
+// O_1 += P_1 V_(t-1), S_1 = Q_1 K_t^T.  The tensor cores run a thread's MMAs in
+// order, so S_s(t) overwrites P_s(t - 1) only after O_s += P_s V_(t-1) has read it,
+// and the commit that signals S_s(t) also covers that P V: once the softmax sees
+// S_s(t), O_s is free to rescale.  Each slot covers only the key tiles its rows can
+// see (causal diagonal, padded length, window); the CTA loads their union.
 // The epilogue divides O by the row sum (0 for a row with no allowed key) and writes
-// bf16 rows.  A restricted-attention window limits each CTA to the key tiles that
-// meet its rows' windows and masks the rest of each row's range.
-// TMEM (512 columns): S [0,128), P [128,192) bf16 pairs, O [256,384).
+// bf16 rows.
+// TMEM (512 columns), per slot s at column 256 s: S [0,128) with P over [64,128)
+// as bf16 pairs, O [128,256).
 //
 // Every mbarrier wait is bounded: one that runs out sets the CTA's abort flag and
 // this file's status word, every role leaves its loop, waits (bounded) for its own
@@ -29,6 +41,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "softmax_tile.cuh"
 
 namespace attn {
 
@@ -37,40 +50,50 @@ __device__ unsigned int g_wide_status_info;
 
 namespace {
 
-constexpr int kBM = 128;                              // query rows per CTA
+constexpr int kBM = 128;                              // query rows per slot
 constexpr int kBN = 128;                              // keys per key tile
 constexpr int kDW = 128;                              // head width
+constexpr int kSlots = 2;                             // query tiles per CTA
 constexpr uint32_t kAtomBytes = 128 * 64 * 2;         // one 64-column atom of a 128-row tile
 constexpr uint32_t kTileBytes = (kDW / 64) * kAtomBytes; // 32 KiB
 constexpr int kStages = 2;
-constexpr int kLoadWarp = 4, kMmaWarp = 5;
-constexpr int kThreads = 192;
+constexpr int kLoadWarp = 4 * kSlots, kMmaWarp = kLoadWarp + 1;
+// three full warpgroups: two of softmax, one of control (loader, MMA, two idle
+// warps that complete it so that setmaxnreg can move registers to the softmax)
+constexpr int kThreads = 384;
+constexpr uint32_t kSoftmaxRegs = 200; // per thread, softmax warpgroups
+constexpr uint32_t kControlRegs = 104; // per thread, control warpgroup
+static_assert(2 * kSoftmaxRegs + kControlRegs <= 3 * 168, "register split exceeds the launch allocation");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColP = 128, kColO = 256;
+constexpr uint32_t kSlotCols = 256, kColS = 0, kColP = 64, kColO = 128;
 constexpr uint64_t kWaitLimitNs = 2000000000ull; // 2 s
 constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, 0, 0);  // Q (K-major) x K (K-major)
 constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kDW, 0, 1); // P (TMEM) x V (MN-major), N = 128
 
 enum WideSite : uint32_t {
-    kSiteLoadKvEmpty = 1, kSiteMmaQFull, kSiteMmaKvFull, kSiteMmaSFree, kSiteMmaPFull, kSiteSmSFull,
-    kSiteSmPvDone
+    kSiteLoadKvEmpty = 1, kSiteMmaQFull, kSiteMmaKvFull, kSiteMmaPFull, kSiteSmSFull, kSiteSmODone
 };
 
 struct alignas(1024) WideSmem {
-    uint8_t q[kTileBytes];
+    uint8_t q[kSlots][kTileBytes];
     uint8_t k[kStages][kTileBytes];
     uint8_t v[kStages][kTileBytes];
-    uint64_t q_full, kv_full[kStages], kv_empty[kStages];
-    uint64_t s_full, s_free, p_full, pv_done, drain;
+    uint64_t q_full[kSlots], kv_full[kStages], kv_empty[kStages];
+    uint64_t s_full[kSlots], p_full[kSlots], o_done[kSlots], drain;
     uint32_t tmem_base;
     int abort_flag;
 };
 
+static_assert(kBN == kTileKeys, "the shared softmax helpers take 128-key tiles");
+static_assert(kSlots == 2, "the softmax role picks its slot's range with a two-way select");
+static_assert(sizeof(WideSmem) + 1024 <= 227 * 1024, "shared memory per CTA");
+
 struct WideParams {
+    const __nv_bfloat16 *q, *k; // read only by the rare score recomputation
     const int32_t *key_lengths; // nullptr unless key padding
     __nv_bfloat16 *out;
     float *lse;
-    int BH, h, m, n, mask_kind, q_tiles;
+    int BH, h, m, n, mask_kind, q_pairs;
     int window; // restricted attention: keys with |i - j| <= window stay; -1: none
     float scale_log2;
 };
@@ -110,6 +133,69 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity)
 
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
+// Key tiles [lo, hi) that rows q0s .. min(m, q0s + 128) - 1 can see; lo == hi when none.
+__device__ __forceinline__ void slot_range(const WideParams &p, int q0s, int len, bool causal, int &lo, int &hi)
+{
+    lo = hi = 0;
+    if (q0s >= p.m) return;
+    int kv_end = causal ? min(len, q0s + kBM) : len;
+    int first = 0;
+    if (p.window >= 0) {
+        first = max(0, q0s - p.window) / kBN;
+        kv_end = min(kv_end, min(p.m, q0s + kBM) + p.window);
+    }
+    if (kv_end <= first * kBN) return;
+    lo = first;
+    hi = (kv_end + kBN - 1) / kBN;
+}
+
+// Scores of query row i of head bh against keys key0 .. key0+127, recomputed on
+// the CUDA cores from Q and K in global memory (fp32 sums of exact bf16
+// products), multiplied by scale * log2 e, and -inf where not allowed (column c
+// is allowed iff cnt_lo <= c < cnt; allowed keys are below n).  Rows past m read
+// as zero queries, as the TMA loads fill them.  Taken only when a tile's
+// exponentials against the running reference overflowed, so it favours size
+// over speed.
+__device__ __forceinline__ void recompute_scores(const WideParams &p, int bh, int i, int key0, int cnt_lo, int cnt,
+                                                  float (&x)[kBN])
+{
+    const bool row_in = i < p.m;
+    const uint4 *qr = reinterpret_cast<const uint4 *>(p.q + (static_cast<size_t>(bh) * p.m + (row_in ? i : 0)) * kDW);
+    float srow[kBN];
+#pragma unroll 1
+    for (int c = 0; c < kBN; ++c) {
+        float v = -CUDART_INF_F;
+        if (c < cnt && c >= cnt_lo) {
+            const uint4 *kr = reinterpret_cast<const uint4 *>(p.k + (static_cast<size_t>(bh) * p.n + key0 + c) * kDW);
+            float a = 0.f;
+#pragma unroll 4
+            for (int u = 0; u < kDW / 8; ++u) {
+                const uint4 qa = row_in ? qr[u] : make_uint4(0, 0, 0, 0), ka = kr[u];
+                const uint32_t qw[4] = {qa.x, qa.y, qa.z, qa.w}, kw[4] = {ka.x, ka.y, ka.z, ka.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    a = fmaf(__uint_as_float(qw[e] << 16), __uint_as_float(kw[e] << 16), a);
+                    a = fmaf(__uint_as_float(qw[e] & 0xffff0000u), __uint_as_float(kw[e] & 0xffff0000u), a);
+                }
+            }
+            v = a * p.scale_log2;
+        }
+        srow[c] = v;
+    }
+#pragma unroll
+    for (int c = 0; c < kBN; ++c) x[c] = srow[c];
+}
+
+__device__ __forceinline__ void zero_rows(const WideParams &p, int bh, int i)
+{
+    if (i >= p.m) return;
+    uint4 *orow = reinterpret_cast<uint4 *>(p.out + (static_cast<size_t>(bh) * p.m + i) * kDW);
+    const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int c = 0; c < kDW / 8; ++c) orow[c] = z;
+    if (p.lse != nullptr) p.lse[static_cast<size_t>(bh) * p.m + i] = -CUDART_INF_F;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const WideParams p)
@@ -118,51 +204,45 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     WideSmem &sm = *reinterpret_cast<WideSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                  ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    // heaviest query tiles first: with a causal mask later query tiles see more keys
-    const int qt = p.q_tiles - 1 - static_cast<int>(blockIdx.x) / p.BH;
+    // heaviest pairs first: with a causal mask later query tiles see more keys
+    const int qp = p.q_pairs - 1 - static_cast<int>(blockIdx.x) / p.BH;
     const int bh = static_cast<int>(blockIdx.x) % p.BH;
-    const int q0 = qt * kBM;
+    const int q0 = qp * kSlots * kBM;
     const bool causal = (p.mask_kind & kMaskCausal) != 0;
     int len = p.n;
     if (p.key_lengths != nullptr) {
         len = __ldg(p.key_lengths + bh / p.h);
         len = len < 0 ? 0 : (len > p.n ? p.n : len);
     }
-    int kv_end = causal ? min(len, q0 + kBM) : len;
-    int kv_lo = 0; // first key tile
-    if (p.window >= 0) {
-        // keys within `window` of some row q0 .. min(m, q0 + 128) - 1 of the tile
-        kv_lo = max(0, q0 - p.window) / kBN;
-        kv_end = min(kv_end, min(p.m, q0 + kBM) + p.window);
-    }
-    // key tiles [kv_lo, kv_lo + n_kv); fill f of the ring holds key tile kv_lo + f
-    const int n_kv = kv_end > kv_lo * kBN ? (kv_end + kBN - 1) / kBN - kv_lo : 0;
-
-    if (n_kv == 0) {
-        // no allowed key for any row of this tile: output 0
-        if (warp < 4) {
-            const int i = q0 + warp * 32 + lane;
-            if (i < p.m) {
-                uint4 *orow = reinterpret_cast<uint4 *>(p.out + (static_cast<size_t>(bh) * p.m + i) * kDW);
-                const uint4 z = make_uint4(0, 0, 0, 0);
+    int lo[kSlots], hi[kSlots];
 #pragma unroll
-                for (int c = 0; c < kDW / 8; ++c) orow[c] = z;
-                if (p.lse != nullptr) p.lse[static_cast<size_t>(bh) * p.m + i] = -CUDART_INF_F;
-            }
+    for (int s = 0; s < kSlots; ++s) slot_range(p, q0 + s * kBM, len, causal, lo[s], hi[s]);
+    // union of the slots' key tiles; fill f of the ring holds key tile t_lo + f
+    int t_lo = 0x7fffffff, t_hi = 0;
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s)
+        if (hi[s] > lo[s]) {
+            t_lo = min(t_lo, lo[s]);
+            t_hi = max(t_hi, hi[s]);
         }
+
+    if (t_hi == 0) {
+        // no allowed key for any row of the CTA: output 0
+        if (warp < kLoadWarp) zero_rows(p, bh, q0 + (warp / 4) * kBM + (warp % 4) * 32 + lane);
         return;
     }
 
     if (threadIdx.x == 0) {
-        mbar_init(&sm.q_full, 1);
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(&sm.q_full[s], 1);
+            mbar_init(&sm.s_full[s], 1);
+            mbar_init(&sm.p_full[s], kBM);
+            mbar_init(&sm.o_done[s], 1);
+        }
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&sm.kv_full[s], 1);
             mbar_init(&sm.kv_empty[s], 1);
         }
-        mbar_init(&sm.s_full, 1);
-        mbar_init(&sm.s_free, kBM);
-        mbar_init(&sm.p_full, kBM);
-        mbar_init(&sm.pv_done, 1);
         mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
         fence_mbarrier_init();
@@ -177,152 +257,108 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
     int *ab = &sm.abort_flag;
+    const int n_fill = t_hi - t_lo;
 
-    if (warp == kLoadWarp) {
-        if (lane == 0) {
-            tma_prefetch_map(&tm_q);
-            tma_prefetch_map(&tm_k);
-            tma_prefetch_map(&tm_v);
-            mbar_arrive_expect_tx(&sm.q_full, kTileBytes);
-            tma_load_3d(sm.q, &tm_q, &sm.q_full, 0, q0, bh);
-            tma_load_3d(sm.q + kAtomBytes, &tm_q, &sm.q_full, 64, q0, bh);
-            int issued = 0;
-            for (int j = 0; j < n_kv; ++j) {
-                const int st = j % kStages;
-                if (!wait_bar(&sm.kv_empty[st], ((j / kStages) & 1) ^ 1, ab, kSiteLoadKvEmpty)) break;
-                mbar_arrive_expect_tx(&sm.kv_full[st], 2 * kTileBytes);
-                const int key0 = (kv_lo + j) * kBN;
-                tma_load_3d(sm.k[st], &tm_k, &sm.kv_full[st], 0, key0, bh);
-                tma_load_3d(sm.k[st] + kAtomBytes, &tm_k, &sm.kv_full[st], 64, key0, bh);
-                tma_load_3d(sm.v[st], &tm_v, &sm.kv_full[st], 0, key0, bh);
-                tma_load_3d(sm.v[st] + kAtomBytes, &tm_v, &sm.kv_full[st], 64, key0, bh);
-                ++issued;
+    // The two register regions never rejoin: each ends with its own CTA-wide
+    // barrier (every thread arrives exactly once).
+    if (warp < kLoadWarp) {
+        regs_increase<kSoftmaxRegs>();
+        // softmax and epilogue of slot s: thread r = row r of the tile = TMEM lane r
+        const int s = warp / 4, quad = warp % 4;
+        const int row = quad * 32 + lane;
+        const int i = q0 + s * kBM + row;
+        const int my_lo = s == 0 ? lo[0] : lo[1];
+        const int n_s = (s == 0 ? hi[0] : hi[1]) - my_lo;
+        if (n_s == 0) {
+            zero_rows(p, bh, i);
+        } else {
+            const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+            const uint32_t t_s = tmem + lane_base + s * kSlotCols + kColS;
+            const uint32_t t_p = tmem + lane_base + s * kSlotCols + kColP;
+            const uint32_t t_o = tmem + lane_base + s * kSlotCols + kColO;
+            const float sl2 = p.scale_log2;
+            // keys allowed for row i: [klo, khi) (below the padded length, i + 1 causal,
+            // and within `window` of i)
+            int khi = causal ? min(len, i + 1) : len;
+            int klo = 0;
+            if (p.window >= 0) {
+                khi = min(khi, i + p.window + 1);
+                klo = i - p.window;
             }
-            // copies still in flight must land before the CTA may exit
-            drain_wait(&sm.q_full, 0);
-            for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
-                drain_wait(&sm.kv_full[j % kStages], (j / kStages) & 1);
-        }
-        __syncwarp();
-    } else if (warp == kMmaWarp) {
-        if (lane == 0) {
-            const uint32_t desc_hi = static_cast<uint32_t>(smem_desc_sw128(0, 0, 1024) >> 32);
-            const uint32_t q_lo = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.q), 16, 1024));
-            const uint32_t k_lo = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.k[0]), 16, 1024));
-            // V as an MN-major B of N = 128: its two 64-column atoms kAtomBytes apart
-            const uint32_t v_lo = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.v[0]), kAtomBytes, 1024));
-            constexpr uint32_t kStageUnits = kTileBytes >> 4;
-            const uint32_t ts = tmem + kColS, tp = tmem + kColP, to = tmem + kColO;
-            bool ok = wait_bar(&sm.q_full, 0, ab, kSiteMmaQFull);
-            for (int j = 0; j <= n_kv && ok; ++j) {
-                if (j < n_kv) {
-                    // S(j) once K_j is in and the softmax has read S(j - 1)
-                    const int st = j % kStages;
-                    ok = wait_bar(&sm.kv_full[st], (j / kStages) & 1, ab, kSiteMmaKvFull);
-                    if (ok && j > 0) ok = wait_bar(&sm.s_free, (j - 1) & 1, ab, kSiteMmaSFree);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t kd = k_lo + st * kStageUnits;
-                    // 16 columns (32 bytes, 2 units) per K step; the second atom 16 KiB
-                    // (1024 units) on
-                    mma_ss_k<0, 0>(ts, q_lo, kd, desc_hi, kIdescS, 0u);
-                    mma_ss_k<2, 2>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
-                    mma_ss_k<4, 4>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
-                    mma_ss_k<6, 6>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
-                    mma_ss_k<1024, 1024>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
-                    mma_ss_k<1026, 1026>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
-                    mma_ss_k<1028, 1028>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
-                    mma_ss_k<1030, 1030>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
-                    mma_commit(&sm.s_full);
-                }
-                if (j >= 1) {
-                    // O += P(j - 1) V(j - 1): keys 16kk.. are P columns 8kk.. (bf16 pairs)
-                    // and V rows 16kk.. (2 KiB = 128 units per K step)
-                    const int jp = j - 1, st = jp % kStages;
-                    ok = wait_bar(&sm.p_full, jp & 1, ab, kSiteMmaPFull);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t vd = v_lo + st * kStageUnits;
-                    const uint32_t acc0 = jp > 0 ? 1u : 0u;
-                    mma_ts_k<0, 0>(to, tp, vd, desc_hi, kIdescPV, acc0);
-                    mma_ts_k<8, 128>(to, tp, vd, desc_hi, kIdescPV, 1u);
-                    mma_ts_k<16, 256>(to, tp, vd, desc_hi, kIdescPV, 1u);
-                    mma_ts_k<24, 384>(to, tp, vd, desc_hi, kIdescPV, 1u);
-                    mma_ts_k<32, 512>(to, tp, vd, desc_hi, kIdescPV, 1u);
-                    mma_ts_k<40, 640>(to, tp, vd, desc_hi, kIdescPV, 1u);
-                    mma_ts_k<48, 768>(to, tp, vd, desc_hi, kIdescPV, 1u);
-                    mma_ts_k<56, 896>(to, tp, vd, desc_hi, kIdescPV, 1u);
-                    mma_commit(&sm.pv_done);
-                    mma_commit(&sm.kv_empty[st]);
-                }
-            }
-            if (!ok) {
-                // make sure no MMA is still writing TMEM when the CTA frees it
-                mma_commit(&sm.drain);
-                drain_wait(&sm.drain, 0);
-            }
-        }
-        __syncwarp();
-    } else {
-        // softmax and epilogue: thread r = row r of the tile = TMEM lane r
-        const int row = warp * 32 + lane;
-        const int i = q0 + row;
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-        const uint32_t t_s = tmem + lane_base + kColS, t_p = tmem + lane_base + kColP;
-        const uint32_t t_o = tmem + lane_base + kColO;
-        const float sl2 = p.scale_log2;
-        // keys allowed for row i: [lo, hi) (below the padded length, i + 1 causal, and
-        // within `window` of i)
-        int hi = causal ? min(len, i + 1) : len;
-        int lo = 0;
-        if (p.window >= 0) {
-            hi = min(hi, i + p.window + 1);
-            lo = i - p.window;
-        }
-        float m_run = -CUDART_INF_F, l_run = 0.f;
-        bool ok = true;
-        for (int j = 0; j < n_kv && ok; ++j) {
-            ok = warp_all(wait_bar(&sm.s_full, j & 1, ab, kSiteSmSFull));
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t sr[kBN];
-#pragma unroll
-            for (int c = 0; c < kBN / 32; ++c) tmem_ld32(t_s + 32 * c, sr + 32 * c);
-            tmem_wait_ld();
-#pragma unroll
-            for (int c = 0; c < kBN / 32; ++c) reg_fence32(sr + 32 * c);
-            tc_fence_before();
-            mbar_arrive(&sm.s_free);
-            // scale first, then mask: a zero scale must not turn -inf into NaN
-            const int key0 = (kv_lo + j) * kBN;
-            const int cnt = hi - key0, cnt_lo = lo - key0;
-            float x[kBN];
-            float mt = -CUDART_INF_F;
-#pragma unroll
-            for (int c = 0; c < kBN; ++c) {
-                x[c] = (c < cnt && c >= cnt_lo) ? __uint_as_float(sr[c]) * sl2 : -CUDART_INF_F;
-                mt = fmaxf(mt, x[c]);
-            }
-            const float m_new = fmaxf(m_run, mt);
-            // O and l hold nothing before the row's first allowed key: no rescale then
-            const bool rescale = m_run != -CUDART_INF_F && m_new > m_run;
-            const float alpha = rescale ? ex2(m_run - m_new) : 1.f;
-            const float m_sub = m_new == -CUDART_INF_F ? 0.f : m_new;
-            uint32_t pk[kBN / 2];
-            float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-            for (int c2 = 0; c2 < kBN / 2; ++c2) {
-                const float e0 = ex2(x[2 * c2] - m_sub), e1 = ex2(x[2 * c2 + 1] - m_sub);
-                s0 += e0;
-                s1 += e1;
-                pk[c2] = pack_bf16x2(e0, e1);
-            }
-            if (j > 0) {
-                // P and O are in use by the previous P V until it completes
-                ok = warp_all(wait_bar(&sm.pv_done, (j - 1) & 1, ab, kSiteSmPvDone));
+            const int q0s = q0 + s * kBM;
+            float m_run = -CUDART_INF_F; // running reference, log2 units, as used for the exponentials
+            float l_run = 0.f;           // running sum of exponentials relative to m_run
+            bool ok = true;
+            for (int jj = 0; jj < n_s && ok; ++jj) {
+                ok = warp_all(wait_bar(&sm.s_full[s], jj & 1, ab, kSiteSmSFull));
                 if (!ok) break;
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, rescale)) {
+                uint32_t sr[kBN];
+#pragma unroll
+                for (int c = 0; c < kBN / 32; ++c) tmem_ld32(t_s + 32 * c, sr + 32 * c);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < kBN / 32; ++c) reg_fence32(sr + 32 * c);
+                const int key0 = (my_lo + jj) * kBN;
+                // column c of the tile is allowed for row i iff cnt_lo <= c < cnt; a tile
+                // is a boundary tile when that fails for some column of some row
+                const int cnt = khi - key0, cnt_lo = klo - key0;
+                const bool boundary = (key0 + kBN > len) || (causal && key0 + kBN - 1 > q0s) ||
+                                      (p.window >= 0 && (key0 < q0s + kBM - 1 - p.window ||
+                                                         key0 + kBN - 1 > q0s + p.window));
+                float x[kBN];
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(sr[c]);
+                const bool prescaled = boundary; // x already multiplied by scale * log2 e
+                if (boundary) {
+                    // scale first, then mask: a zero scale must not turn -inf into NaN; one
+                    // bit mask of allowed columns per 32 columns, one bit test per column
+#pragma unroll
+                    for (int ch = 0; ch < kBN / 32; ++ch) {
+                        const int top = min(max(cnt - 32 * ch, 0), 32);
+                        const int bot = min(max(cnt_lo - 32 * ch, 0), 32);
+                        uint32_t msk = top >= 32 ? 0xffffffffu : (1u << top) - 1u;
+                        msk &= bot >= 32 ? 0u : ~((1u << bot) - 1u);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            x[32 * ch + e] = (msk & (1u << e)) ? x[32 * ch + e] * sl2 : -CUDART_INF_F;
+                    }
+                }
+                // Reference for the exponentials: the row max of the row's first tile with
+                // an allowed key; later tiles keep it and check the tile's sum instead.
+                float m_use = m_run, alpha = 1.f;
+                bool grow = false;
+                const bool first = m_run == -CUDART_INF_F;
+                if (first) move_reference(x, prescaled, sl2, m_run, m_use, alpha, grow);
+                uint32_t pk[kBN / 2];
+                float tile_sum = weights_bf16(x, prescaled, sl2, m_use, pk);
+                if (!first && !(tile_sum <= kFastSumLimit)) {
+                    if (tile_sum < CUDART_INF_F) {
+                        // finite but large: scale the weights by 2^-k (k an integer, so the
+                        // bf16 values scale exactly) and move the reference up by k
+                        const int k = ((__float_as_int(tile_sum) >> 23) & 0xff) - 127 - 7; // 8..120
+                        const float f2k = __int_as_float((127 - k) << 23);                 // 2^-k
+#pragma unroll
+                        for (int c2 = 0; c2 < kBN / 2; ++c2) {
+                            const float lo2 = __uint_as_float(pk[c2] << 16), hi2 = __uint_as_float(pk[c2] & 0xffff0000u);
+                            pk[c2] = pack_bf16x2(lo2 * f2k, hi2 * f2k);
+                        }
+                        tile_sum *= f2k;
+                        alpha = f2k;
+                        m_use = m_run + static_cast<float>(k);
+                        grow = true;
+                    } else {
+                        // some weight overflowed (the scores grew by 128 or more in log2
+                        // units, or are not finite): recompute this row's scores from Q and
+                        // K, already scaled and masked, and take their max
+                        recompute_scores(p, bh, i, key0, cnt_lo, cnt, x);
+                        move_reference(x, true, sl2, m_run, m_use, alpha, grow);
+                        tile_sum = weights_bf16(x, true, sl2, m_use, pk);
+                    }
+                }
+                if (jj > 0 && __any_sync(0xffffffffu, grow)) {
+                    // the P V of the previous tile has completed (the commit that
+                    // signalled this S covers it): move O to the new reference
 #pragma unroll 1
                     for (int c = 0; c < kDW / 32; ++c) {
                         uint32_t orr[32];
@@ -334,42 +370,146 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         tmem_st32(t_o + 32 * c, orr);
                     }
                 }
+                tmem_st32(t_p, pk);
+                tmem_st32(t_p + 32, pk + 32);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&sm.p_full[s]);
+                l_run = l_run * alpha + tile_sum;
+                m_run = m_use;
             }
-            tmem_st32(t_p, pk);
-            tmem_st32(t_p + 32, pk + 32);
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&sm.p_full);
-            l_run = l_run * alpha + (s0 + s1);
-            m_run = m_new;
-        }
-        if (ok) ok = warp_all(wait_bar(&sm.pv_done, (n_kv - 1) & 1, ab, kSiteSmPvDone));
-        if (ok) {
-            tc_fence_after();
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-            if (p.lse != nullptr && i < p.m) // weights are exp2(x - m_run) / l: lse = (m_run + log2 l) ln 2
-                p.lse[static_cast<size_t>(bh) * p.m + i] =
-                    l_run > 0.f ? (m_run + __log2f(l_run)) * 0.6931471805599453f : -CUDART_INF_F;
-            uint4 *orow = reinterpret_cast<uint4 *>(p.out + (static_cast<size_t>(bh) * p.m + (i < p.m ? i : 0)) * kDW);
+            if (ok) ok = warp_all(wait_bar(&sm.o_done[s], 0, ab, kSiteSmODone));
+            if (ok) {
+                tc_fence_after();
+                const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+                if (p.lse != nullptr && i < p.m) // weights are exp2(x - m_run) / l: lse = (m_run + log2 l) ln 2
+                    p.lse[static_cast<size_t>(bh) * p.m + i] =
+                        l_run > 0.f ? (m_run + __log2f(l_run)) * 0.6931471805599453f : -CUDART_INF_F;
+                uint4 *orow =
+                    reinterpret_cast<uint4 *>(p.out + (static_cast<size_t>(bh) * p.m + (i < p.m ? i : 0)) * kDW);
 #pragma unroll 1
-            for (int c = 0; c < kDW / 32; ++c) {
-                uint32_t orr[32];
-                tmem_ld32(t_o + 32 * c, orr);
-                tmem_wait_ld();
-                reg_fence32(orr);
-                if (i < p.m) {
+                for (int c = 0; c < kDW / 32; ++c) {
+                    uint32_t orr[32];
+                    tmem_ld32(t_o + 32 * c, orr);
+                    tmem_wait_ld();
+                    reg_fence32(orr);
+                    if (i < p.m) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(orr[8 * q + 0]) * inv, __uint_as_float(orr[8 * q + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(orr[8 * q + 2]) * inv, __uint_as_float(orr[8 * q + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(orr[8 * q + 4]) * inv, __uint_as_float(orr[8 * q + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(orr[8 * q + 6]) * inv, __uint_as_float(orr[8 * q + 7]) * inv);
-                        orow[4 * c + q] = w;
+                        for (int q = 0; q < 4; ++q) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(orr[8 * q + 0]) * inv, __uint_as_float(orr[8 * q + 1]) * inv);
+                            w.y = pack_bf16x2(__uint_as_float(orr[8 * q + 2]) * inv, __uint_as_float(orr[8 * q + 3]) * inv);
+                            w.z = pack_bf16x2(__uint_as_float(orr[8 * q + 4]) * inv, __uint_as_float(orr[8 * q + 5]) * inv);
+                            w.w = pack_bf16x2(__uint_as_float(orr[8 * q + 6]) * inv, __uint_as_float(orr[8 * q + 7]) * inv);
+                            orow[4 * c + q] = w;
+                        }
                     }
                 }
             }
         }
+        tc_fence_before();
+        __syncthreads();
+        return;
+    }
+    regs_decrease<kControlRegs>();
+    if (warp == kLoadWarp) {
+        if (lane == 0) {
+            tma_prefetch_map(&tm_q);
+            tma_prefetch_map(&tm_k);
+            tma_prefetch_map(&tm_v);
+            for (int s = 0; s < kSlots; ++s) {
+                if (hi[s] == lo[s]) continue;
+                mbar_arrive_expect_tx(&sm.q_full[s], kTileBytes);
+                tma_load_3d(sm.q[s], &tm_q, &sm.q_full[s], 0, q0 + s * kBM, bh);
+                tma_load_3d(sm.q[s] + kAtomBytes, &tm_q, &sm.q_full[s], 64, q0 + s * kBM, bh);
+            }
+            int issued = 0;
+            for (int f = 0; f < n_fill; ++f) {
+                const int st = f % kStages;
+                if (!wait_bar(&sm.kv_empty[st], ((f / kStages) & 1) ^ 1, ab, kSiteLoadKvEmpty)) break;
+                mbar_arrive_expect_tx(&sm.kv_full[st], 2 * kTileBytes);
+                const int key0 = (t_lo + f) * kBN;
+                tma_load_3d(sm.k[st], &tm_k, &sm.kv_full[st], 0, key0, bh);
+                tma_load_3d(sm.k[st] + kAtomBytes, &tm_k, &sm.kv_full[st], 64, key0, bh);
+                tma_load_3d(sm.v[st], &tm_v, &sm.kv_full[st], 0, key0, bh);
+                tma_load_3d(sm.v[st] + kAtomBytes, &tm_v, &sm.kv_full[st], 64, key0, bh);
+                ++issued;
+            }
+            // copies still in flight must land before the CTA may exit
+            for (int s = 0; s < kSlots; ++s)
+                if (hi[s] > lo[s]) drain_wait(&sm.q_full[s], 0);
+            for (int f = issued > kStages ? issued - kStages : 0; f < issued; ++f)
+                drain_wait(&sm.kv_full[f % kStages], (f / kStages) & 1);
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            const uint32_t desc_hi = static_cast<uint32_t>(smem_desc_sw128(0, 0, 1024) >> 32);
+            const uint32_t k_lo = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.k[0]), 16, 1024));
+            // V as an MN-major B of N = 128: its two 64-column atoms kAtomBytes apart
+            const uint32_t v_lo = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.v[0]), kAtomBytes, 1024));
+            constexpr uint32_t kStageUnits = kTileBytes >> 4;
+            bool ok = true;
+            bool q_in[kSlots] = {};
+            for (int t = t_lo; t <= t_hi && ok; ++t) {
+                const int f = t - t_lo, st = f % kStages;
+                if (t < t_hi) ok = wait_bar(&sm.kv_full[st], (f / kStages) & 1, ab, kSiteMmaKvFull);
+#pragma unroll
+                for (int s = 0; s < kSlots; ++s) {
+                    const uint32_t ts = tmem + s * kSlotCols + kColS;
+                    if (ok && t - 1 >= lo[s] && t - 1 < hi[s]) {
+                        // O_s += P_s(t - 1) V(t - 1): keys 16kk.. are P columns 8kk..
+                        // (bf16 pairs) and V rows 16kk.. (2 KiB = 128 units per K step)
+                        const int jj = t - 1 - lo[s];
+                        ok = wait_bar(&sm.p_full[s], jj & 1, ab, kSiteMmaPFull);
+                        if (!ok) continue;
+                        tc_fence_after();
+                        const uint32_t vd = v_lo + ((f + kStages - 1) % kStages) * kStageUnits;
+                        const uint32_t tp = tmem + s * kSlotCols + kColP, to = tmem + s * kSlotCols + kColO;
+                        const uint32_t acc0 = jj > 0 ? 1u : 0u;
+                        mma_ts_k<0, 0>(to, tp, vd, desc_hi, kIdescPV, acc0);
+                        mma_ts_k<8, 128>(to, tp, vd, desc_hi, kIdescPV, 1u);
+                        mma_ts_k<16, 256>(to, tp, vd, desc_hi, kIdescPV, 1u);
+                        mma_ts_k<24, 384>(to, tp, vd, desc_hi, kIdescPV, 1u);
+                        mma_ts_k<32, 512>(to, tp, vd, desc_hi, kIdescPV, 1u);
+                        mma_ts_k<40, 640>(to, tp, vd, desc_hi, kIdescPV, 1u);
+                        mma_ts_k<48, 768>(to, tp, vd, desc_hi, kIdescPV, 1u);
+                        mma_ts_k<56, 896>(to, tp, vd, desc_hi, kIdescPV, 1u);
+                        if (t == hi[s]) mma_commit(&sm.o_done[s]);
+                    }
+                    if (ok && t < hi[s] && t >= lo[s]) {
+                        // S_s(t) = Q_s K_t^T, after the P V above in the tensor pipe
+                        if (!q_in[s]) {
+                            ok = wait_bar(&sm.q_full[s], 0, ab, kSiteMmaQFull);
+                            if (!ok) continue;
+                            q_in[s] = true;
+                        }
+                        tc_fence_after();
+                        const uint32_t q_lo = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.q[s]), 16, 1024));
+                        const uint32_t kd = k_lo + st * kStageUnits;
+                        // 16 columns (32 bytes, 2 units) per K step; the second atom 16 KiB
+                        // (1024 units) on
+                        mma_ss_k<0, 0>(ts, q_lo, kd, desc_hi, kIdescS, 0u);
+                        mma_ss_k<2, 2>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
+                        mma_ss_k<4, 4>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
+                        mma_ss_k<6, 6>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
+                        mma_ss_k<1024, 1024>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
+                        mma_ss_k<1026, 1026>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
+                        mma_ss_k<1028, 1028>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
+                        mma_ss_k<1030, 1030>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
+                        mma_commit(&sm.s_full[s]);
+                    }
+                }
+                // every MMA that reads fill f - 1 has been issued: free its stage once they end
+                if (ok && t > t_lo) mma_commit(&sm.kv_empty[(f + kStages - 1) % kStages]);
+            }
+            if (!ok) {
+                // make sure no MMA is still writing TMEM when the CTA frees it
+                mma_commit(&sm.drain);
+                drain_wait(&sm.drain, 0);
+            }
+        }
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -407,6 +547,8 @@ cudaError_t launch_wide(const Problem &pb, cudaStream_t stream)
         !encode_bf16_3d(&tv, pb.v, kDW, pb.n, BH, kBN))
         return cudaErrorInvalidValue;
     WideParams p;
+    p.q = static_cast<const __nv_bfloat16 *>(pb.q);
+    p.k = static_cast<const __nv_bfloat16 *>(pb.k);
     p.key_lengths = (pb.mask_kind & kMaskKeyPadding) ? pb.key_lengths : nullptr;
     p.out = static_cast<__nv_bfloat16 *>(pb.out);
     p.lse = pb.lse;
@@ -415,10 +557,10 @@ cudaError_t launch_wide(const Problem &pb, cudaStream_t stream)
     p.m = pb.m;
     p.n = pb.n;
     p.mask_kind = pb.mask_kind;
-    p.q_tiles = (pb.m + kBM - 1) / kBM;
+    p.q_pairs = (pb.m + kSlots * kBM - 1) / (kSlots * kBM);
     p.window = (pb.mask_kind & kMaskWindow) ? pb.window : -1;
     p.scale_log2 = pb.scale * 1.4426950408889634f;
-    const long long grid = static_cast<long long>(BH) * p.q_tiles;
+    const long long grid = static_cast<long long>(BH) * p.q_pairs;
     if (grid > 0x7fffffff) return cudaErrorInvalidValue;
     attn_wide_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
