@@ -7,7 +7,8 @@
 // The two tiles ("slots") share one stream of K and V tiles and take turns on the
 // tensor cores: while one slot's softmax runs, the other slot's MMAs do.  Q and
 // each 128-key tile of K and V are 128 x 128 bf16, loaded by TMA as two 64-column
-// boxes (128-byte swizzle atoms) 16 KiB apart; K and V pass through a two-stage ring.
+// boxes (128-byte swizzle atoms) 16 KiB apart; K and V pass through two-stage rings
+// of their own (a K tile is free a tile before its V tile is).
 //   MMA:     S_s = Q_s K_t^T            (8 x M128 N128 K16: four K steps in each atom)
 //   softmax: 4 warps per slot, thread r = row r = TMEM lane r; scores masked on
 //            boundary tiles only; P = exp2(S scale log2 e - r) as bf16 pairs written
@@ -71,14 +72,15 @@ constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, 0, 0);  // Q (K-major) x K
 constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kDW, 0, 1); // P (TMEM) x V (MN-major), N = 128
 
 enum WideSite : uint32_t {
-    kSiteLoadKvEmpty = 1, kSiteMmaQFull, kSiteMmaKvFull, kSiteMmaPFull, kSiteSmSFull, kSiteSmODone
+    kSiteLoadKEmpty = 1, kSiteLoadVEmpty, kSiteMmaQFull, kSiteMmaKFull, kSiteMmaVFull, kSiteMmaPFull,
+    kSiteSmSFull, kSiteSmODone
 };
 
 struct alignas(1024) WideSmem {
     uint8_t q[kSlots][kTileBytes];
     uint8_t k[kStages][kTileBytes];
     uint8_t v[kStages][kTileBytes];
-    uint64_t q_full[kSlots], kv_full[kStages], kv_empty[kStages];
+    uint64_t q_full[kSlots], k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
     uint64_t s_full[kSlots], p_full[kSlots], o_done[kSlots], drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -240,8 +242,10 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             mbar_init(&sm.o_done[s], 1);
         }
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&sm.kv_full[s], 1);
-            mbar_init(&sm.kv_empty[s], 1);
+            mbar_init(&sm.k_full[s], 1);
+            mbar_init(&sm.k_empty[s], 1);
+            mbar_init(&sm.v_full[s], 1);
+            mbar_init(&sm.v_empty[s], 1);
         }
         mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
@@ -423,23 +427,31 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 tma_load_3d(sm.q[s], &tm_q, &sm.q_full[s], 0, q0 + s * kBM, bh);
                 tma_load_3d(sm.q[s] + kAtomBytes, &tm_q, &sm.q_full[s], 64, q0 + s * kBM, bh);
             }
-            int issued = 0;
+            // K and V in rings of their own: K_t is free once both slots' S(t) have
+            // read it, V_t only after both P V(t), a tile later
+            int k_issued = 0, v_issued = 0;
             for (int f = 0; f < n_fill; ++f) {
                 const int st = f % kStages;
-                if (!wait_bar(&sm.kv_empty[st], ((f / kStages) & 1) ^ 1, ab, kSiteLoadKvEmpty)) break;
-                mbar_arrive_expect_tx(&sm.kv_full[st], 2 * kTileBytes);
+                const uint32_t par = ((f / kStages) & 1) ^ 1;
                 const int key0 = (t_lo + f) * kBN;
-                tma_load_3d(sm.k[st], &tm_k, &sm.kv_full[st], 0, key0, bh);
-                tma_load_3d(sm.k[st] + kAtomBytes, &tm_k, &sm.kv_full[st], 64, key0, bh);
-                tma_load_3d(sm.v[st], &tm_v, &sm.kv_full[st], 0, key0, bh);
-                tma_load_3d(sm.v[st] + kAtomBytes, &tm_v, &sm.kv_full[st], 64, key0, bh);
-                ++issued;
+                if (!wait_bar(&sm.k_empty[st], par, ab, kSiteLoadKEmpty)) break;
+                mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
+                tma_load_3d(sm.k[st], &tm_k, &sm.k_full[st], 0, key0, bh);
+                tma_load_3d(sm.k[st] + kAtomBytes, &tm_k, &sm.k_full[st], 64, key0, bh);
+                ++k_issued;
+                if (!wait_bar(&sm.v_empty[st], par, ab, kSiteLoadVEmpty)) break;
+                mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
+                tma_load_3d(sm.v[st], &tm_v, &sm.v_full[st], 0, key0, bh);
+                tma_load_3d(sm.v[st] + kAtomBytes, &tm_v, &sm.v_full[st], 64, key0, bh);
+                ++v_issued;
             }
             // copies still in flight must land before the CTA may exit
             for (int s = 0; s < kSlots; ++s)
                 if (hi[s] > lo[s]) drain_wait(&sm.q_full[s], 0);
-            for (int f = issued > kStages ? issued - kStages : 0; f < issued; ++f)
-                drain_wait(&sm.kv_full[f % kStages], (f / kStages) & 1);
+            for (int f = k_issued > kStages ? k_issued - kStages : 0; f < k_issued; ++f)
+                drain_wait(&sm.k_full[f % kStages], (f / kStages) & 1);
+            for (int f = v_issued > kStages ? v_issued - kStages : 0; f < v_issued; ++f)
+                drain_wait(&sm.v_full[f % kStages], (f / kStages) & 1);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -452,8 +464,9 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             bool ok = true;
             bool q_in[kSlots] = {};
             for (int t = t_lo; t <= t_hi && ok; ++t) {
-                const int f = t - t_lo, st = f % kStages;
-                if (t < t_hi) ok = wait_bar(&sm.kv_full[st], (f / kStages) & 1, ab, kSiteMmaKvFull);
+                // fill f of the rings holds key tile t; V(t - 1) is fill f - 1
+                const int f = t - t_lo, st = f % kStages, pst = (f + kStages - 1) % kStages;
+                bool k_in = false, v_in = false; // K_t / V_(t-1) known to have landed
 #pragma unroll
                 for (int s = 0; s < kSlots; ++s) {
                     const uint32_t ts = tmem + s * kSlotCols + kColS;
@@ -461,10 +474,15 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         // O_s += P_s(t - 1) V(t - 1): keys 16kk.. are P columns 8kk..
                         // (bf16 pairs) and V rows 16kk.. (2 KiB = 128 units per K step)
                         const int jj = t - 1 - lo[s];
+                        if (!v_in) {
+                            ok = wait_bar(&sm.v_full[pst], ((f - 1) / kStages) & 1, ab, kSiteMmaVFull);
+                            if (!ok) continue;
+                            v_in = true;
+                        }
                         ok = wait_bar(&sm.p_full[s], jj & 1, ab, kSiteMmaPFull);
                         if (!ok) continue;
                         tc_fence_after();
-                        const uint32_t vd = v_lo + ((f + kStages - 1) % kStages) * kStageUnits;
+                        const uint32_t vd = v_lo + pst * kStageUnits;
                         const uint32_t tp = tmem + s * kSlotCols + kColP, to = tmem + s * kSlotCols + kColO;
                         const uint32_t acc0 = jj > 0 ? 1u : 0u;
                         mma_ts_k<0, 0>(to, tp, vd, desc_hi, kIdescPV, acc0);
@@ -477,8 +495,20 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         mma_ts_k<56, 896>(to, tp, vd, desc_hi, kIdescPV, 1u);
                         if (t == hi[s]) mma_commit(&sm.o_done[s]);
                     }
+                    if (s == kSlots - 1 && ok && t > t_lo) {
+                        // every P V that reads V(t - 1) has been issued: free its stage
+                        // once they end (a fill no slot read is waited for all the same,
+                        // so that no copy is still landing when the stage is refilled)
+                        if (!v_in) ok = wait_bar(&sm.v_full[pst], ((f - 1) / kStages) & 1, ab, kSiteMmaVFull);
+                        if (ok) mma_commit(&sm.v_empty[pst]);
+                    }
                     if (ok && t < hi[s] && t >= lo[s]) {
                         // S_s(t) = Q_s K_t^T, after the P V above in the tensor pipe
+                        if (!k_in) {
+                            ok = wait_bar(&sm.k_full[st], (f / kStages) & 1, ab, kSiteMmaKFull);
+                            if (!ok) continue;
+                            k_in = true;
+                        }
                         if (!q_in[s]) {
                             ok = wait_bar(&sm.q_full[s], 0, ab, kSiteMmaQFull);
                             if (!ok) continue;
@@ -499,9 +529,12 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         mma_ss_k<1030, 1030>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
                         mma_commit(&sm.s_full[s]);
                     }
+                    if (s == kSlots - 1 && ok && t < t_hi) {
+                        // both S(t) issued: free K_t's stage once they end
+                        if (!k_in) ok = wait_bar(&sm.k_full[st], (f / kStages) & 1, ab, kSiteMmaKFull);
+                        if (ok) mma_commit(&sm.k_empty[st]);
+                    }
                 }
-                // every MMA that reads fill f - 1 has been issued: free its stage once they end
-                if (ok && t > t_lo) mma_commit(&sm.kv_empty[(f + kStages - 1) % kStages]);
             }
             if (!ok) {
                 // make sure no MMA is still writing TMEM when the CTA frees it
