@@ -330,7 +330,8 @@ def mha_workload(torch, attn, device, peak_tf, steps=50):
 def head_width_workloads(torch, attn, device, steps=50):
     """The model variants that trade heads for head width at h * d_k = 512 (h=4 d_k=128,
     h=16 d_k=32, h=32 d_k=16) on the encoder workload's shape (B64, n=m=100, key padding),
-    next to the base h=8 d_k=64.  Widths other than 64 run on the CUDA-core kernel."""
+    next to the base h=8 d_k=64.  All run on tensor cores: widths 16 and 32 zero-padded
+    on the d_k = 64 kernels, width 128 on its own kernel."""
     base = WORKLOADS[2]
     res = {}
     for h, d in ((8, 64), (4, 128), (16, 32), (32, 16)):
@@ -352,6 +353,34 @@ def head_width_workloads(torch, attn, device, steps=50):
         res[w.name] = {"kernel": attn._native.KERNEL_NAMES[kern], "us_per_launch": ms * 1e3,
                        "tflops_useful": useful_flops(w, inp.key_lengths) / (ms * 1e-3) / 1e12}
     return res
+
+
+def wide_workload(torch, attn, device, peak_tf, steps=50):
+    """Heads of width 128 on the long causal sequences: workload 5 with h=8, d_k=128
+    (B4 n=m=8192, the same d_model of 1024), inputs 268 MB in all (> L2).  Useful work:
+    4*d_k FLOPs per allowed (query, key) pair."""
+    w = WORKLOADS[5].with_(h=8, d=128, scale=128 ** -0.5, name="long_causal_h8_d128")
+    inp = draw(w)
+    q, k, v = (to_device(x, w.dtype, torch, device) for x in (inp.q, inp.k, inp.v))
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        attn.attn_fwd(q, k, v, None, w.mask, w.scale, out=out, stream=stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    ms = time_launches(step, steps, torch, stream)
+    st, info = attn.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} (info {info}) after the wide-head loop")
+    flops = useful_flops(w, inp.key_lengths)
+    kern = attn.select_kernel(w.B, w.h, w.m, w.n, w.d, 0, w.mask)
+    return {"workload": f"causal self-attention, bf16, B={w.B} h={w.h} n=m={w.n} d_k={w.d}",
+            "entry_point": "attn_fwd", "kernel": attn._native.KERNEL_NAMES[kern], "us_per_call": ms * 1e3,
+            "tflops_useful": flops / (ms * 1e-3) / 1e12, "frac_of_peak": flops / (ms * 1e-3) / 1e12 / peak_tf,
+            "calls_timed": steps, "algorithmic": "4*d_k FLOPs per allowed (query, key) pair"}
 
 
 def window_workload(torch, attn, device, peak_tf, steps=50, window=256):
@@ -588,6 +617,7 @@ def main():
         result["decode"] = decode_workload(torch, attn, device, peak_hbm)
         result["window"] = window_workload(torch, attn, device, peak_tf)
         result["head_widths"] = head_width_workloads(torch, attn, device)
+        result["wide_heads"] = wide_workload(torch, attn, device, peak_tf)
         result["mha"] = mha_workload(torch, attn, device, peak_tf)
         if rank == 0:
             cb, _ = cpu_oracle_sample(w, inp, args.cpu_seconds)

@@ -19,11 +19,11 @@
 //            in TMEM only when r moves
 //   MMA:     O_s += P_s V_t             (8 x M128 N128 K16, P from TMEM, V MN-major:
 //            its two 64-column atoms are the two halves of N)
-// The MMA warp issues, per key tile t: O_0 += P_0 V_(t-1), S_0 = Q_0 K_t^T,
-// O_1 += P_1 V_(t-1), S_1 = Q_1 K_t^T.  The tensor cores run a thread's MMAs in
-// order, so S_s(t) overwrites P_s(t - 1) only after O_s += P_s V_(t-1) has read it,
-// and the commit that signals S_s(t) also covers that P V: once the softmax sees
-// S_s(t), O_s is free to rescale.  Each slot covers only the key tiles its rows can
+// Each slot has an MMA issuer; per key tile t the two issue, taking turns, O_0 +=
+// P_0 V_(t-1), S_0 = Q_0 K_t^T, then O_1 += P_1 V_(t-1), S_1 = Q_1 K_t^T.  The tensor
+// cores run a thread's MMAs in order, so S_s(t) overwrites P_s(t - 1) only after
+// O_s += P_s V_(t-1) has read it, and the commit that signals S_s(t) also covers
+// that P V: once the softmax sees S_s(t), O_s is free to rescale.  Each slot covers only the key tiles its rows can
 // see (causal diagonal, padded length, window); the CTA loads their union.
 // The epilogue divides O by the row sum (0 for a row with no allowed key) and writes
 // bf16 rows.
@@ -58,9 +58,11 @@ constexpr int kSlots = 2;                             // query tiles per CTA
 constexpr uint32_t kAtomBytes = 128 * 64 * 2;         // one 64-column atom of a 128-row tile
 constexpr uint32_t kTileBytes = (kDW / 64) * kAtomBytes; // 32 KiB
 constexpr int kStages = 2;
-constexpr int kLoadWarp = 4 * kSlots, kMmaWarp = kLoadWarp + 1;
-// three full warpgroups: two of softmax, one of control (loader, MMA, two idle
-// warps that complete it so that setmaxnreg can move registers to the softmax)
+constexpr int kLoadWarp = 4 * kSlots;
+constexpr int kMmaWarp = kLoadWarp + 1; // MMA issuer of slot 0 (slot s: kMmaWarp + s); allocates TMEM
+// three full warpgroups: two of softmax, one of control (loader, the two MMA
+// issuers and an idle warp that completes it so that setmaxnreg can move
+// registers to the softmax)
 constexpr int kThreads = 384;
 constexpr uint32_t kSoftmaxRegs = 200; // per thread, softmax warpgroups
 constexpr uint32_t kControlRegs = 104; // per thread, control warpgroup
@@ -73,7 +75,7 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kDW, 0, 1); // P (TMEM) x V (M
 
 enum WideSite : uint32_t {
     kSiteLoadKEmpty = 1, kSiteLoadVEmpty, kSiteMmaQFull, kSiteMmaKFull, kSiteMmaVFull, kSiteMmaPFull,
-    kSiteSmSFull, kSiteSmODone
+    kSiteSmSFull, kSiteSmODone, kSiteMmaTurn
 };
 
 struct alignas(1024) WideSmem {
@@ -81,7 +83,8 @@ struct alignas(1024) WideSmem {
     uint8_t k[kStages][kTileBytes];
     uint8_t v[kStages][kTileBytes];
     uint64_t q_full[kSlots], k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
-    uint64_t s_full[kSlots], p_full[kSlots], o_done[kSlots], drain;
+    uint64_t s_full[kSlots], p_full[kSlots], o_done[kSlots], drain[kSlots];
+    uint64_t turn[kSlots]; // turn[s]: the other issuer has issued its group, slot s may go
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -243,11 +246,14 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&sm.k_full[s], 1);
-            mbar_init(&sm.k_empty[s], 1);
+            mbar_init(&sm.k_empty[s], kSlots); // one commit from each MMA issuer
             mbar_init(&sm.v_full[s], 1);
-            mbar_init(&sm.v_empty[s], 1);
+            mbar_init(&sm.v_empty[s], kSlots);
         }
-        mbar_init(&sm.drain, 1);
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(&sm.drain[s], 1);
+            mbar_init(&sm.turn[s], 1);
+        }
         sm.abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -454,92 +460,80 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 drain_wait(&sm.v_full[f % kStages], (f / kStages) & 1);
         }
         __syncwarp();
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+        // One issuer per slot; per key tile t each issues O_s += P_s V(t - 1), then
+        // S_s = Q_s K_t^T.  The two take turns (slot 0, slot 1, slot 0, ...), passing
+        // a token through turn[], so the tensor cores receive the groups in that order
+        // and the slots stay half an iteration apart, while each issuer's waits
+        // overlap the other's MMAs.  Every issuer commits once per fill of each ring,
+        // whether its slot read the fill or not, after waiting for that fill to land.
         if (lane == 0) {
+            const int s = warp - kMmaWarp;
+            const int my_lo = s == 0 ? lo[0] : lo[1];
+            const int my_hi = s == 0 ? hi[0] : hi[1];
             const uint32_t desc_hi = static_cast<uint32_t>(smem_desc_sw128(0, 0, 1024) >> 32);
+            const uint32_t q_lo = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.q[s]), 16, 1024));
             const uint32_t k_lo = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.k[0]), 16, 1024));
             // V as an MN-major B of N = 128: its two 64-column atoms kAtomBytes apart
             const uint32_t v_lo = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.v[0]), kAtomBytes, 1024));
             constexpr uint32_t kStageUnits = kTileBytes >> 4;
-            bool ok = true;
-            bool q_in[kSlots] = {};
+            const uint32_t ts = tmem + s * kSlotCols + kColS, tp = tmem + s * kSlotCols + kColP;
+            const uint32_t to = tmem + s * kSlotCols + kColO;
+            bool ok = true, q_in = false;
             for (int t = t_lo; t <= t_hi && ok; ++t) {
                 // fill f of the rings holds key tile t; V(t - 1) is fill f - 1
                 const int f = t - t_lo, st = f % kStages, pst = (f + kStages - 1) % kStages;
-                bool k_in = false, v_in = false; // K_t / V_(t-1) known to have landed
-#pragma unroll
-                for (int s = 0; s < kSlots; ++s) {
-                    const uint32_t ts = tmem + s * kSlotCols + kColS;
-                    if (ok && t - 1 >= lo[s] && t - 1 < hi[s]) {
-                        // O_s += P_s(t - 1) V(t - 1): keys 16kk.. are P columns 8kk..
-                        // (bf16 pairs) and V rows 16kk.. (2 KiB = 128 units per K step)
-                        const int jj = t - 1 - lo[s];
-                        if (!v_in) {
-                            ok = wait_bar(&sm.v_full[pst], ((f - 1) / kStages) & 1, ab, kSiteMmaVFull);
-                            if (!ok) continue;
-                            v_in = true;
-                        }
-                        ok = wait_bar(&sm.p_full[s], jj & 1, ab, kSiteMmaPFull);
-                        if (!ok) continue;
-                        tc_fence_after();
-                        const uint32_t vd = v_lo + pst * kStageUnits;
-                        const uint32_t tp = tmem + s * kSlotCols + kColP, to = tmem + s * kSlotCols + kColO;
-                        const uint32_t acc0 = jj > 0 ? 1u : 0u;
-                        mma_ts_k<0, 0>(to, tp, vd, desc_hi, kIdescPV, acc0);
-                        mma_ts_k<8, 128>(to, tp, vd, desc_hi, kIdescPV, 1u);
-                        mma_ts_k<16, 256>(to, tp, vd, desc_hi, kIdescPV, 1u);
-                        mma_ts_k<24, 384>(to, tp, vd, desc_hi, kIdescPV, 1u);
-                        mma_ts_k<32, 512>(to, tp, vd, desc_hi, kIdescPV, 1u);
-                        mma_ts_k<40, 640>(to, tp, vd, desc_hi, kIdescPV, 1u);
-                        mma_ts_k<48, 768>(to, tp, vd, desc_hi, kIdescPV, 1u);
-                        mma_ts_k<56, 896>(to, tp, vd, desc_hi, kIdescPV, 1u);
-                        if (t == hi[s]) mma_commit(&sm.o_done[s]);
-                    }
-                    if (s == kSlots - 1 && ok && t > t_lo) {
-                        // every P V that reads V(t - 1) has been issued: free its stage
-                        // once they end (a fill no slot read is waited for all the same,
-                        // so that no copy is still landing when the stage is refilled)
-                        if (!v_in) ok = wait_bar(&sm.v_full[pst], ((f - 1) / kStages) & 1, ab, kSiteMmaVFull);
-                        if (ok) mma_commit(&sm.v_empty[pst]);
-                    }
-                    if (ok && t < hi[s] && t >= lo[s]) {
-                        // S_s(t) = Q_s K_t^T, after the P V above in the tensor pipe
-                        if (!k_in) {
-                            ok = wait_bar(&sm.k_full[st], (f / kStages) & 1, ab, kSiteMmaKFull);
-                            if (!ok) continue;
-                            k_in = true;
-                        }
-                        if (!q_in[s]) {
-                            ok = wait_bar(&sm.q_full[s], 0, ab, kSiteMmaQFull);
-                            if (!ok) continue;
-                            q_in[s] = true;
-                        }
-                        tc_fence_after();
-                        const uint32_t q_lo = static_cast<uint32_t>(smem_desc_sw128(smem_addr(sm.q[s]), 16, 1024));
-                        const uint32_t kd = k_lo + st * kStageUnits;
-                        // 16 columns (32 bytes, 2 units) per K step; the second atom 16 KiB
-                        // (1024 units) on
-                        mma_ss_k<0, 0>(ts, q_lo, kd, desc_hi, kIdescS, 0u);
-                        mma_ss_k<2, 2>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
-                        mma_ss_k<4, 4>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
-                        mma_ss_k<6, 6>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
-                        mma_ss_k<1024, 1024>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
-                        mma_ss_k<1026, 1026>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
-                        mma_ss_k<1028, 1028>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
-                        mma_ss_k<1030, 1030>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
-                        mma_commit(&sm.s_full[s]);
-                    }
-                    if (s == kSlots - 1 && ok && t < t_hi) {
-                        // both S(t) issued: free K_t's stage once they end
-                        if (!k_in) ok = wait_bar(&sm.k_full[st], (f / kStages) & 1, ab, kSiteMmaKFull);
-                        if (ok) mma_commit(&sm.k_empty[st]);
-                    }
+                const bool do_pv = t - 1 >= my_lo && t - 1 < my_hi, do_s = t >= my_lo && t < my_hi;
+                // this slot's own inputs first, while the other issuer may still be issuing
+                if (t > t_lo) ok = wait_bar(&sm.v_full[pst], ((f - 1) / kStages) & 1, ab, kSiteMmaVFull);
+                if (ok && do_pv) ok = wait_bar(&sm.p_full[s], (t - 1 - my_lo) & 1, ab, kSiteMmaPFull);
+                if (ok && t < t_hi) ok = wait_bar(&sm.k_full[st], (f / kStages) & 1, ab, kSiteMmaKFull);
+                if (ok && do_s && !q_in) ok = q_in = wait_bar(&sm.q_full[s], 0, ab, kSiteMmaQFull);
+                // then the turn: slot 1 after slot 0 of the same tile, slot 0 after slot 1
+                // of the previous one
+                if (ok && (s == 1 || t > t_lo))
+                    ok = wait_bar(&sm.turn[s], (s == 1 ? f : f - 1) & 1, ab, kSiteMmaTurn);
+                if (!ok) break;
+                tc_fence_after();
+                if (do_pv) {
+                    // O_s += P_s(t - 1) V(t - 1): keys 16kk.. are P columns 8kk..
+                    // (bf16 pairs) and V rows 16kk.. (2 KiB = 128 units per K step)
+                    const uint32_t vd = v_lo + pst * kStageUnits;
+                    const uint32_t acc0 = t - 1 > my_lo ? 1u : 0u;
+                    mma_ts_k<0, 0>(to, tp, vd, desc_hi, kIdescPV, acc0);
+                    mma_ts_k<8, 128>(to, tp, vd, desc_hi, kIdescPV, 1u);
+                    mma_ts_k<16, 256>(to, tp, vd, desc_hi, kIdescPV, 1u);
+                    mma_ts_k<24, 384>(to, tp, vd, desc_hi, kIdescPV, 1u);
+                    mma_ts_k<32, 512>(to, tp, vd, desc_hi, kIdescPV, 1u);
+                    mma_ts_k<40, 640>(to, tp, vd, desc_hi, kIdescPV, 1u);
+                    mma_ts_k<48, 768>(to, tp, vd, desc_hi, kIdescPV, 1u);
+                    mma_ts_k<56, 896>(to, tp, vd, desc_hi, kIdescPV, 1u);
+                    if (t == my_hi) mma_commit(&sm.o_done[s]);
                 }
+                // this issuer is done with V(t - 1): its share of freeing the stage
+                if (t > t_lo) mma_commit(&sm.v_empty[pst]);
+                if (do_s) {
+                    // S_s(t) = Q_s K_t^T, after the P V above in the tensor pipe; 16
+                    // columns (32 bytes, 2 units) per K step, the second atom 16 KiB
+                    // (1024 units) on
+                    const uint32_t kd = k_lo + st * kStageUnits;
+                    mma_ss_k<0, 0>(ts, q_lo, kd, desc_hi, kIdescS, 0u);
+                    mma_ss_k<2, 2>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
+                    mma_ss_k<4, 4>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
+                    mma_ss_k<6, 6>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
+                    mma_ss_k<1024, 1024>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
+                    mma_ss_k<1026, 1026>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
+                    mma_ss_k<1028, 1028>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
+                    mma_ss_k<1030, 1030>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
+                    mma_commit(&sm.s_full[s]);
+                }
+                if (t < t_hi) mma_commit(&sm.k_empty[st]);
+                mbar_arrive(&sm.turn[1 - s]); // the other slot's turn
             }
             if (!ok) {
-                // make sure no MMA is still writing TMEM when the CTA frees it
-                mma_commit(&sm.drain);
-                drain_wait(&sm.drain, 0);
+                // make sure no MMA of this issuer is still writing TMEM when the CTA frees it
+                mma_commit(&sm.drain[s]);
+                drain_wait(&sm.drain[s], 0);
             }
         }
         __syncwarp();
