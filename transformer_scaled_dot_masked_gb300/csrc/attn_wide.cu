@@ -136,6 +136,56 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity)
         if (global_timer_ns() - start > kWaitLimitNs) return;
 }
 
+// mbarrier try_wait without a suspend-time hint (the hardware's own time limit).
+__device__ __forceinline__ bool mbar_try_wait_nohint(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+    return done != 0;
+}
+
+// Bounded wait of the softmax warps for their scores: try_wait without the
+// 20 us suspend hint, which resumes the warps sooner after the MMAs complete
+// (a test_wait spin would take issue slots from the other slot's softmax).
+__device__ __forceinline__ bool wait_scores(uint64_t *bar, uint32_t parity, int *abort_flag, uint32_t site)
+{
+    const uint32_t a = smem_addr(bar);
+    const uint64_t start = global_timer_ns();
+    while (true) {
+        for (int k = 0; k < 64; ++k)
+            if (mbar_try_wait_nohint(a, parity)) return true;
+        if (*reinterpret_cast<volatile int *>(abort_flag)) return false;
+        if (global_timer_ns() - start > kWaitLimitNs) {
+            *reinterpret_cast<volatile int *>(abort_flag) = 1;
+            atomicOr(&g_wide_status_code, 1u);
+            atomicCAS(&g_wide_status_info, 0u, site);
+            return false;
+        }
+    }
+}
+
+// Bounded wait that polls (test_wait) instead of suspending: a thread suspended in
+// try_wait resumes a few hundred cycles after the phase completes, which the MMA
+// issuers cannot afford (the tensor cores drain meanwhile).
+__device__ __forceinline__ bool wait_poll(uint64_t *bar, uint32_t parity, int *abort_flag, uint32_t site)
+{
+    const uint32_t a = smem_addr(bar);
+    if (mbar_test_wait(a, parity)) return true;
+    const uint64_t start = global_timer_ns();
+    while (true) {
+        for (int k = 0; k < 256; ++k)
+            if (mbar_test_wait(a, parity)) return true;
+        if (*reinterpret_cast<volatile int *>(abort_flag)) return false;
+        if (global_timer_ns() - start > kWaitLimitNs) {
+            *reinterpret_cast<volatile int *>(abort_flag) = 1;
+            atomicOr(&g_wide_status_code, 1u);
+            atomicCAS(&g_wide_status_info, 0u, site);
+            return false;
+        }
+    }
+}
+
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
 // Key tiles [lo, hi) that rows q0s .. min(m, q0s + 128) - 1 can see; lo == hi when none.
@@ -300,7 +350,7 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             float l_run = 0.f;           // running sum of exponentials relative to m_run
             bool ok = true;
             for (int jj = 0; jj < n_s && ok; ++jj) {
-                ok = warp_all(wait_bar(&sm.s_full[s], jj & 1, ab, kSiteSmSFull));
+                ok = warp_all(wait_scores(&sm.s_full[s], jj & 1, ab, kSiteSmSFull));
                 if (!ok) break;
                 tc_fence_after();
                 uint32_t sr[kBN];
@@ -485,14 +535,14 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const int f = t - t_lo, st = f % kStages, pst = (f + kStages - 1) % kStages;
                 const bool do_pv = t - 1 >= my_lo && t - 1 < my_hi, do_s = t >= my_lo && t < my_hi;
                 // this slot's own inputs first, while the other issuer may still be issuing
-                if (t > t_lo) ok = wait_bar(&sm.v_full[pst], ((f - 1) / kStages) & 1, ab, kSiteMmaVFull);
-                if (ok && do_pv) ok = wait_bar(&sm.p_full[s], (t - 1 - my_lo) & 1, ab, kSiteMmaPFull);
-                if (ok && t < t_hi) ok = wait_bar(&sm.k_full[st], (f / kStages) & 1, ab, kSiteMmaKFull);
+                if (t > t_lo) ok = wait_poll(&sm.v_full[pst], ((f - 1) / kStages) & 1, ab, kSiteMmaVFull);
+                if (ok && do_pv) ok = wait_poll(&sm.p_full[s], (t - 1 - my_lo) & 1, ab, kSiteMmaPFull);
+                if (ok && t < t_hi) ok = wait_poll(&sm.k_full[st], (f / kStages) & 1, ab, kSiteMmaKFull);
                 if (ok && do_s && !q_in) ok = q_in = wait_bar(&sm.q_full[s], 0, ab, kSiteMmaQFull);
                 // then the turn: slot 1 after slot 0 of the same tile, slot 0 after slot 1
                 // of the previous one
                 if (ok && (s == 1 || t > t_lo))
-                    ok = wait_bar(&sm.turn[s], (s == 1 ? f : f - 1) & 1, ab, kSiteMmaTurn);
+                    ok = wait_poll(&sm.turn[s], (s == 1 ? f : f - 1) & 1, ab, kSiteMmaTurn);
                 if (!ok) break;
                 tc_fence_after();
                 if (do_pv) {
