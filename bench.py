@@ -85,15 +85,21 @@ def row_pairs(w, lengths, rows) -> float:
 
 # DRAM bytes (read + write) of one flash-kernel launch on the default workload,
 # from an ncu capture (profiles/attn_flash_long_causal_8192.md), keyed by a hash of
-# the kernel source it was taken on: any later change to the kernel reports null.
-MEASURED_TRAFFIC = {"5762ae7212cbf6b5": 842824960 + 46914816}
+# the sources the kernel is compiled from: any later change to them reports null.
+MEASURED_TRAFFIC = {"733f78500373ad62": 847713536 + 46592000}
+FLASH_SOURCES = ("attn_flash.cu", "softmax_tile.cuh", "ptx.cuh")
+
+
+def flash_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for name in FLASH_SOURCES:
+        h.update(open(os.path.join(ROOT, "transformer_scaled_dot_masked_gb300", "csrc", name), "rb").read())
+    return h.hexdigest()[:16]
 
 
 def measured_traffic():
-    import hashlib
-    path = os.path.join(ROOT, "transformer_scaled_dot_masked_gb300", "csrc", "attn_flash.cu")
-    key = hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
-    return MEASURED_TRAFFIC.get(key)
+    return MEASURED_TRAFFIC.get(flash_source_hash())
 
 
 def workload_config(w):
@@ -584,6 +590,7 @@ def main():
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": achieved / peak_tf,
                      "traffic": measured_traffic() if args.workload == 5 else None,
+                     "source_hash": flash_source_hash(),
                      "peak_source": f"{peak_src} bf16 dense burst",
                      "algorithmic": "4*d_k FLOPs per allowed (query, key) pair per launch"},
         "gpu_launches": args.steps,
