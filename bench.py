@@ -361,32 +361,53 @@ def head_width_workloads(torch, attn, device, steps=50):
     return res
 
 
-def wide_workload(torch, attn, device, peak_tf, steps=50):
+def wide_workload(torch, attn, device, peak_tf, steps=50, extra=True):
     """Heads of width 128 on the long causal sequences: workload 5 with h=8, d_k=128
     (B4 n=m=8192, the same d_model of 1024), inputs 268 MB in all (> L2).  Useful work:
-    4*d_k FLOPs per allowed (query, key) pair."""
+    4*d_k FLOPs per allowed (query, key) pair.  With `extra`, the same kernel also on
+    the unmasked B4 h8 n=4096 case and on restricted attention with windows 256 and
+    1024 over the n=8192 inputs (through attn_fwd_window)."""
     w = WORKLOADS[5].with_(h=8, d=128, scale=128 ** -0.5, name="long_causal_h8_d128")
     inp = draw(w)
     q, k, v = (to_device(x, w.dtype, torch, device) for x in (inp.q, inp.k, inp.v))
     out = torch.empty_like(q)
     stream = torch.cuda.current_stream(device)
 
-    def step():
-        attn.attn_fwd(q, k, v, None, w.mask, w.scale, out=out, stream=stream)
+    def timed(step, what):
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        ms = time_launches(step, steps, torch, stream)
+        st, info = attn.device_status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} (info {info}) after the wide-head loop ({what})")
+        return ms
 
-    for _ in range(3):
-        step()
-    torch.cuda.synchronize()
-    ms = time_launches(step, steps, torch, stream)
-    st, info = attn.device_status()
-    if st != 0:
-        raise RuntimeError(f"device status {st} (info {info}) after the wide-head loop")
+    ms = timed(lambda: attn.attn_fwd(q, k, v, None, w.mask, w.scale, out=out, stream=stream), "causal")
     flops = useful_flops(w, inp.key_lengths)
     kern = attn.select_kernel(w.B, w.h, w.m, w.n, w.d, 0, w.mask)
-    return {"workload": f"causal self-attention, bf16, B={w.B} h={w.h} n=m={w.n} d_k={w.d}",
-            "entry_point": "attn_fwd", "kernel": attn._native.KERNEL_NAMES[kern], "us_per_call": ms * 1e3,
-            "tflops_useful": flops / (ms * 1e-3) / 1e12, "frac_of_peak": flops / (ms * 1e-3) / 1e12 / peak_tf,
-            "calls_timed": steps, "algorithmic": "4*d_k FLOPs per allowed (query, key) pair"}
+    res = {"workload": f"causal self-attention, bf16, B={w.B} h={w.h} n=m={w.n} d_k={w.d}",
+           "entry_point": "attn_fwd", "kernel": attn._native.KERNEL_NAMES[kern], "us_per_call": ms * 1e3,
+           "tflops_useful": flops / (ms * 1e-3) / 1e12, "frac_of_peak": flops / (ms * 1e-3) / 1e12 / peak_tf,
+           "calls_timed": steps, "algorithmic": "4*d_k FLOPs per allowed (query, key) pair"}
+    if not extra:
+        return res
+    half = w.n // 2
+    qh, kh, vh = (x[:, :, :half].contiguous() for x in (q, k, v))
+    oh = torch.empty_like(qh)
+    ms = timed(lambda: attn.attn_fwd(qh, kh, vh, None, attn.MASK_NONE, w.scale, out=oh, stream=stream), "no mask")
+    fl = 4.0 * w.d * w.B * w.h * half * half
+    res["no_mask_n4096"] = {"us_per_call": ms * 1e3, "tflops_useful": fl / (ms * 1e-3) / 1e12,
+                            "frac_of_peak": fl / (ms * 1e-3) / 1e12 / peak_tf}
+    i = np.arange(w.n)
+    for win in (256, 1024):
+        ms = timed(lambda: attn.attn_fwd_window(q, k, v, None, attn.MASK_WINDOW, win, w.scale, out=out,
+                                                stream=stream), f"window {win}")
+        pairs = float((np.minimum(i + win, w.n - 1) - np.maximum(i - win, 0) + 1).sum()) * w.B * w.h
+        fl = 4.0 * w.d * pairs
+        res[f"window_{win}"] = {"us_per_call": ms * 1e3, "tflops_useful": fl / (ms * 1e-3) / 1e12,
+                                "frac_of_peak": fl / (ms * 1e-3) / 1e12 / peak_tf}
+    return res
 
 
 def window_workload(torch, attn, device, peak_tf, steps=50, window=256):
