@@ -333,6 +333,11 @@ WIDE_CASES = [
     ("no_mask_long_keys", 1, 3, 128, 1000, MASK_NONE, None),
     ("causal_padding", 2, 2, 260, 260, MASK_CAUSAL | MASK_KEY_PADDING, (0, 260)),
     ("single_query", 4, 2, 1, 77, MASK_NONE, None),
+    # m, n <= 128: two heads per CTA; an odd head count leaves the last CTA's second
+    # slot without a head, and zero key lengths leave whole slots without keys
+    ("head_pairs_odd_padding", 3, 1, 100, 100, MASK_KEY_PADDING, (0, 100)),
+    ("head_pairs_causal", 2, 3, 128, 128, MASK_CAUSAL, None),
+    ("head_pairs_cross", 5, 3, 37, 128, MASK_KEY_PADDING, (1, 128)),
 ]
 
 
@@ -343,10 +348,12 @@ def test_wide_heads_tensor_cores(orc, name, B, h, m, n, mask, lengths):
     check_full(orc, w, K_WIDE)
 
 
-def test_wide_heads_lse_and_bounds(orc):
+@pytest.mark.parametrize("B,h,m", [(2, 3, 200), (3, 1, 100)], ids=["query_tile_pairs", "head_pairs_odd"])
+def test_wide_heads_lse_and_bounds(orc, B, h, m):
     """The log-sum-exp output of the wide kernel, and that it writes exactly its output
-    (guard regions on both sides untouched)."""
-    w = Workload("wide_lse", "bf16", 2, 3, 200, 200, 128, MASK_CAUSAL | MASK_KEY_PADDING, 0.09, 65, (0, 200))
+    (guard regions on both sides untouched), with two query tiles per CTA and with two
+    heads per CTA (an odd head count: the last CTA's second slot has no head)."""
+    w = Workload("wide_lse", "bf16", B, h, m, m, 128, MASK_CAUSAL | MASK_KEY_PADDING, 0.09, 65, (0, m))
     inp = draw(w)
     q, k, v = (to_device(x, "bf16") for x in (inp.q, inp.k, inp.v))
     lens = torch.from_numpy(inp.key_lengths).cuda()

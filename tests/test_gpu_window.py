@@ -52,6 +52,7 @@ CASES = [
     ("wide_heads_w128_padding", "bf16_d128", 3, 2, 700, MASK_KEY_PADDING, 128, (0, 700)),
     ("wide_heads_w200_causal_padding", "bf16_d128", 2, 2, 1000, MASK_CAUSAL | MASK_KEY_PADDING, 200, (100, 1000)),
     ("wide_heads_covering_window", "bf16_d128", 2, 2, 260, 0, 5000, None),
+    ("wide_heads_pairs_w5", "bf16_d128", 3, 1, 100, MASK_KEY_PADDING, 5, (0, 100)),
 ]
 
 

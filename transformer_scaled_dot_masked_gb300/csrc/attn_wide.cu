@@ -99,7 +99,9 @@ struct WideParams {
     __nv_bfloat16 *out;
     float *lse;
     int BH, h, m, n, mask_kind, q_pairs;
-    int window; // restricted attention: keys with |i - j| <= window stay; -1: none
+    int window;     // restricted attention: keys with |i - j| <= window stay; -1: none
+    int head_pairs; // 1: m, n <= 128, and slot s of CTA c takes (batch, head) 2c + s (host side;
+                    // the kernel is instantiated for each mode)
     float scale_log2;
 };
 
@@ -251,6 +253,10 @@ __device__ __forceinline__ void zero_rows(const WideParams &p, int bh, int i)
     if (p.lse != nullptr) p.lse[static_cast<size_t>(bh) * p.m + i] = -CUDART_INF_F;
 }
 
+// kHeadPairs: the launch has one query tile and one key tile per head, and each
+// CTA takes two heads (compiled separately so that the other launches carry none
+// of it).
+template <bool kHeadPairs>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const WideParams p)
@@ -259,19 +265,35 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     WideSmem &sm = *reinterpret_cast<WideSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                  ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    // heaviest pairs first: with a causal mask later query tiles see more keys
-    const int qp = p.q_pairs - 1 - static_cast<int>(blockIdx.x) / p.BH;
-    const int bh = static_cast<int>(blockIdx.x) % p.BH;
-    const int q0 = qp * kSlots * kBM;
+    constexpr bool hp = kHeadPairs;
     const bool causal = (p.mask_kind & kMaskCausal) != 0;
-    int len = p.n;
-    if (p.key_lengths != nullptr) {
-        len = __ldg(p.key_lengths + bh / p.h);
-        len = len < 0 ? 0 : (len > p.n ? p.n : len);
-    }
-    int lo[kSlots], hi[kSlots];
+    // Slot s works on query rows q0s[s] .. q0s[s] + 127 of head bhs[s].  Query-tile
+    // pairs: one head, two consecutive query tiles, heaviest pairs first (with a causal
+    // mask later query tiles see more keys).  Head pairs: two heads, query tile 0; a
+    // slot past the last head has no rows.
+    int bhs[kSlots], q0s[kSlots], lens[kSlots], lo[kSlots], hi[kSlots];
 #pragma unroll
-    for (int s = 0; s < kSlots; ++s) slot_range(p, q0 + s * kBM, len, causal, lo[s], hi[s]);
+    for (int s = 0; s < kSlots; ++s) {
+        if (hp) {
+            bhs[s] = kSlots * static_cast<int>(blockIdx.x) + s;
+            q0s[s] = 0;
+        } else {
+            bhs[s] = static_cast<int>(blockIdx.x) % p.BH;
+            q0s[s] = ((p.q_pairs - 1 - static_cast<int>(blockIdx.x) / p.BH) * kSlots + s) * kBM;
+        }
+        int len = 0;
+        if (bhs[s] < p.BH) {
+            len = p.n;
+            if (p.key_lengths != nullptr) {
+                len = __ldg(p.key_lengths + bhs[s] / p.h);
+                len = len < 0 ? 0 : (len > p.n ? p.n : len);
+            }
+            slot_range(p, q0s[s], len, causal, lo[s], hi[s]);
+        } else {
+            lo[s] = hi[s] = 0;
+        }
+        lens[s] = len;
+    }
     // union of the slots' key tiles; fill f of the ring holds key tile t_lo + f
     int t_lo = 0x7fffffff, t_hi = 0;
 #pragma unroll
@@ -283,7 +305,11 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
     if (t_hi == 0) {
         // no allowed key for any row of the CTA: output 0
-        if (warp < kLoadWarp) zero_rows(p, bh, q0 + (warp / 4) * kBM + (warp % 4) * 32 + lane);
+        if (warp < kLoadWarp) {
+            const int s = warp / 4;
+            const int bh = s == 0 ? bhs[0] : bhs[1];
+            if (bh < p.BH) zero_rows(p, bh, (s == 0 ? q0s[0] : q0s[1]) + (warp % 4) * 32 + lane);
+        }
         return;
     }
 
@@ -326,11 +352,13 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // softmax and epilogue of slot s: thread r = row r of the tile = TMEM lane r
         const int s = warp / 4, quad = warp % 4;
         const int row = quad * 32 + lane;
-        const int i = q0 + s * kBM + row;
+        const int bh = s == 0 ? bhs[0] : bhs[1], len = s == 0 ? lens[0] : lens[1];
+        const int q0s_ = s == 0 ? q0s[0] : q0s[1];
+        const int i = q0s_ + row;
         const int my_lo = s == 0 ? lo[0] : lo[1];
         const int n_s = (s == 0 ? hi[0] : hi[1]) - my_lo;
         if (n_s == 0) {
-            zero_rows(p, bh, i);
+            if (bh < p.BH) zero_rows(p, bh, i);
         } else {
             const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
             const uint32_t t_s = tmem + lane_base + s * kSlotCols + kColS;
@@ -345,7 +373,6 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 khi = min(khi, i + p.window + 1);
                 klo = i - p.window;
             }
-            const int q0s = q0 + s * kBM;
             float m_run = -CUDART_INF_F; // running reference, log2 units, as used for the exponentials
             float l_run = 0.f;           // running sum of exponentials relative to m_run
             bool ok = true;
@@ -363,9 +390,9 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 // column c of the tile is allowed for row i iff cnt_lo <= c < cnt; a tile
                 // is a boundary tile when that fails for some column of some row
                 const int cnt = khi - key0, cnt_lo = klo - key0;
-                const bool boundary = (key0 + kBN > len) || (causal && key0 + kBN - 1 > q0s) ||
-                                      (p.window >= 0 && (key0 < q0s + kBM - 1 - p.window ||
-                                                         key0 + kBN - 1 > q0s + p.window));
+                const bool boundary = (key0 + kBN > len) || (causal && key0 + kBN - 1 > q0s_) ||
+                                      (p.window >= 0 && (key0 < q0s_ + kBM - 1 - p.window ||
+                                                         key0 + kBN - 1 > q0s_ + p.window));
                 float x[kBN];
 #pragma unroll
                 for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(sr[c]);
@@ -480,13 +507,23 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             for (int s = 0; s < kSlots; ++s) {
                 if (hi[s] == lo[s]) continue;
                 mbar_arrive_expect_tx(&sm.q_full[s], kTileBytes);
-                tma_load_3d(sm.q[s], &tm_q, &sm.q_full[s], 0, q0 + s * kBM, bh);
-                tma_load_3d(sm.q[s] + kAtomBytes, &tm_q, &sm.q_full[s], 64, q0 + s * kBM, bh);
+                tma_load_3d(sm.q[s], &tm_q, &sm.q_full[s], 0, q0s[s], bhs[s]);
+                tma_load_3d(sm.q[s] + kAtomBytes, &tm_q, &sm.q_full[s], 64, q0s[s], bhs[s]);
+                if (hp) {
+                    // head pairs: the slot's one key tile of K and V, in stage s of each ring
+                    mbar_arrive_expect_tx(&sm.k_full[s], kTileBytes);
+                    tma_load_3d(sm.k[s], &tm_k, &sm.k_full[s], 0, 0, bhs[s]);
+                    tma_load_3d(sm.k[s] + kAtomBytes, &tm_k, &sm.k_full[s], 64, 0, bhs[s]);
+                    mbar_arrive_expect_tx(&sm.v_full[s], kTileBytes);
+                    tma_load_3d(sm.v[s], &tm_v, &sm.v_full[s], 0, 0, bhs[s]);
+                    tma_load_3d(sm.v[s] + kAtomBytes, &tm_v, &sm.v_full[s], 64, 0, bhs[s]);
+                }
             }
             // K and V in rings of their own: K_t is free once both slots' S(t) have
             // read it, V_t only after both P V(t), a tile later
+            const int bh = bhs[0];
             int k_issued = 0, v_issued = 0;
-            for (int f = 0; f < n_fill; ++f) {
+            for (int f = 0; f < (hp ? 0 : n_fill); ++f) {
                 const int st = f % kStages;
                 const uint32_t par = ((f / kStages) & 1) ^ 1;
                 const int key0 = (t_lo + f) * kBN;
@@ -503,7 +540,13 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             // copies still in flight must land before the CTA may exit
             for (int s = 0; s < kSlots; ++s)
-                if (hi[s] > lo[s]) drain_wait(&sm.q_full[s], 0);
+                if (hi[s] > lo[s]) {
+                    drain_wait(&sm.q_full[s], 0);
+                    if (hp) {
+                        drain_wait(&sm.k_full[s], 0);
+                        drain_wait(&sm.v_full[s], 0);
+                    }
+                }
             for (int f = k_issued > kStages ? k_issued - kStages : 0; f < k_issued; ++f)
                 drain_wait(&sm.k_full[f % kStages], (f / kStages) & 1);
             for (int f = v_issued > kStages ? v_issued - kStages : 0; f < v_issued; ++f)
@@ -517,6 +560,8 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // and the slots stay half an iteration apart, while each issuer's waits
         // overlap the other's MMAs.  Every issuer commits once per fill of each ring,
         // whether its slot read the fill or not, after waiting for that fill to land.
+        // Head pairs: one key tile per slot, in stage s, loaded once; each issuer waits
+        // only for its own and frees nothing.
         if (lane == 0) {
             const int s = warp - kMmaWarp;
             const int my_lo = s == 0 ? lo[0] : lo[1];
@@ -532,12 +577,14 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             bool ok = true, q_in = false;
             for (int t = t_lo; t <= t_hi && ok; ++t) {
                 // fill f of the rings holds key tile t; V(t - 1) is fill f - 1
-                const int f = t - t_lo, st = f % kStages, pst = (f + kStages - 1) % kStages;
+                const int f = t - t_lo;
+                const int st = hp ? s : f % kStages, pst = hp ? s : (f + kStages - 1) % kStages;
+                const uint32_t k_par = hp ? 0u : (f / kStages) & 1, v_par = hp ? 0u : ((f - 1) / kStages) & 1;
                 const bool do_pv = t - 1 >= my_lo && t - 1 < my_hi, do_s = t >= my_lo && t < my_hi;
                 // this slot's own inputs first, while the other issuer may still be issuing
-                if (t > t_lo) ok = wait_poll(&sm.v_full[pst], ((f - 1) / kStages) & 1, ab, kSiteMmaVFull);
+                if (t > t_lo && (!hp || do_pv)) ok = wait_poll(&sm.v_full[pst], v_par, ab, kSiteMmaVFull);
                 if (ok && do_pv) ok = wait_poll(&sm.p_full[s], (t - 1 - my_lo) & 1, ab, kSiteMmaPFull);
-                if (ok && t < t_hi) ok = wait_poll(&sm.k_full[st], (f / kStages) & 1, ab, kSiteMmaKFull);
+                if (ok && t < t_hi && (!hp || do_s)) ok = wait_poll(&sm.k_full[st], k_par, ab, kSiteMmaKFull);
                 if (ok && do_s && !q_in) ok = q_in = wait_bar(&sm.q_full[s], 0, ab, kSiteMmaQFull);
                 // then the turn: slot 1 after slot 0 of the same tile, slot 0 after slot 1
                 // of the previous one
@@ -561,7 +608,7 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     if (t == my_hi) mma_commit(&sm.o_done[s]);
                 }
                 // this issuer is done with V(t - 1): its share of freeing the stage
-                if (t > t_lo) mma_commit(&sm.v_empty[pst]);
+                if (t > t_lo && !hp) mma_commit(&sm.v_empty[pst]);
                 if (do_s) {
                     // S_s(t) = Q_s K_t^T, after the P V above in the tensor pipe; 16
                     // columns (32 bytes, 2 units) per K step, the second atom 16 KiB
@@ -577,7 +624,7 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     mma_ss_k<1030, 1030>(ts, q_lo, kd, desc_hi, kIdescS, 1u);
                     mma_commit(&sm.s_full[s]);
                 }
-                if (t < t_hi) mma_commit(&sm.k_empty[st]);
+                if (t < t_hi && !hp) mma_commit(&sm.k_empty[st]);
                 mbar_arrive(&sm.turn[1 - s]); // the other slot's turn
             }
             if (!ok) {
@@ -611,7 +658,9 @@ cudaError_t launch_wide(const Problem &pb, cudaStream_t stream)
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!configured[dev]) {
-            if ((e = cudaFuncSetAttribute(attn_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if ((e = cudaFuncSetAttribute(attn_wide_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>(kSmemBytes))) != cudaSuccess ||
+                (e = cudaFuncSetAttribute(attn_wide_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           static_cast<int>(kSmemBytes))) != cudaSuccess)
                 return e;
             configured[dev] = true;
@@ -635,11 +684,17 @@ cudaError_t launch_wide(const Problem &pb, cudaStream_t stream)
     p.n = pb.n;
     p.mask_kind = pb.mask_kind;
     p.q_pairs = (pb.m + kSlots * kBM - 1) / (kSlots * kBM);
+    // one query tile and one key tile per head: two heads per CTA, so that the
+    // second slot has rows (and the grid halves)
+    p.head_pairs = (pb.m <= kBM && pb.n <= kBN && BH > 1) ? 1 : 0;
     p.window = (pb.mask_kind & kMaskWindow) ? pb.window : -1;
     p.scale_log2 = pb.scale * 1.4426950408889634f;
-    const long long grid = static_cast<long long>(BH) * p.q_pairs;
+    const long long grid = p.head_pairs ? (BH + kSlots - 1) / kSlots : static_cast<long long>(BH) * p.q_pairs;
     if (grid > 0x7fffffff) return cudaErrorInvalidValue;
-    attn_wide_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+    if (p.head_pairs)
+        attn_wide_kernel<true><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+    else
+        attn_wide_kernel<false><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
