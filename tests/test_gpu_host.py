@@ -5,8 +5,9 @@ bitwise against attn_fwd on device copies of the same inputs: every (batch, head
 slice is computed by the same kernel either way, so cutting the problem into chunks
 must not change a single bit.  The cases cover both ways of cutting (whole batches
 when B >= 8, head ranges within a batch otherwise, with a ragged last range), the
-single-chunk path (fp32 rows that are not whole 16-byte units), pageable memory and
-the ordering on the caller's stream.
+single-chunk path (fp32 rows that are not whole 16-byte units), heads of width 128
+(whose short-row launches pair heads, which a one-head chunk cannot), pageable
+memory and the ordering on the caller's stream.
 """
 import numpy as np
 import pytest
@@ -55,6 +56,10 @@ CASES = [
     ("fp32_odd_width_single_chunk", "fp32", 3, 4, 37, 53, 3, MASK_KEY_PADDING, (0, 53)),
     ("fp32_whole_rows", "fp32", 2, 5, 64, 64, 16, MASK_CAUSAL, None),
     ("narrow_heads_bf16", "bf16", 4, 3, 90, 90, 32, 0, None),
+    # heads of width 128: long rows (query-tile pairs), and short rows, where the
+    # whole problem runs as head pairs but a one-head chunk cannot
+    ("wide_heads_causal", "bf16", 2, 3, 300, 300, 128, MASK_CAUSAL, None),
+    ("wide_heads_short_padding", "bf16", 3, 3, 100, 100, 128, MASK_KEY_PADDING, (0, 100)),
 ]
 
 
