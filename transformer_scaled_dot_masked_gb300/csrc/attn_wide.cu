@@ -25,8 +25,8 @@
 // O_s += P_s V_(t-1) has read it, and the commit that signals S_s(t) also covers
 // that P V: once the softmax sees S_s(t), O_s is free to rescale.  Each slot covers only the key tiles its rows can
 // see (causal diagonal, padded length, window); the CTA loads their union.
-// The epilogue divides O by the row sum (0 for a row with no allowed key) and writes
-// bf16 rows.
+// The epilogue divides O by the row sum (0 for a row with no allowed key) and stores
+// the bf16 tile through the slot's Q buffer with TMA.
 // TMEM (512 columns), per slot s at column 256 s: S [0,128) with P over [64,128)
 // as bf16 pairs, O [128,256).
 //
@@ -75,7 +75,7 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kDW, 0, 1); // P (TMEM) x V (M
 
 enum WideSite : uint32_t {
     kSiteLoadKEmpty = 1, kSiteLoadVEmpty, kSiteMmaQFull, kSiteMmaKFull, kSiteMmaVFull, kSiteMmaPFull,
-    kSiteSmSFull, kSiteSmODone, kSiteMmaTurn
+    kSiteSmSFull, kSiteSmODone, kSiteMmaTurn, kSiteSmStaged
 };
 
 struct alignas(1024) WideSmem {
@@ -85,6 +85,7 @@ struct alignas(1024) WideSmem {
     uint64_t q_full[kSlots], k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
     uint64_t s_full[kSlots], p_full[kSlots], o_done[kSlots], drain[kSlots];
     uint64_t turn[kSlots]; // turn[s]: the other issuer has issued its group, slot s may go
+    uint64_t staged[kSlots]; // slot s's output tile is in q[s], ready for the TMA store
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -259,7 +260,8 @@ __device__ __forceinline__ void zero_rows(const WideParams &p, int bh, int i)
 template <bool kHeadPairs>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, const WideParams p)
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                 const WideParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     WideSmem &sm = *reinterpret_cast<WideSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -329,6 +331,7 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(&sm.drain[s], 1);
             mbar_init(&sm.turn[s], 1);
+            mbar_init(&sm.staged[s], kBM);
         }
         sm.abort_flag = 0;
         fence_mbarrier_init();
@@ -472,24 +475,38 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (p.lse != nullptr && i < p.m) // weights are exp2(x - m_run) / l: lse = (m_run + log2 l) ln 2
                     p.lse[static_cast<size_t>(bh) * p.m + i] =
                         l_run > 0.f ? (m_run + __log2f(l_run)) * 0.6931471805599453f : -CUDART_INF_F;
-                uint4 *orow =
-                    reinterpret_cast<uint4 *>(p.out + (static_cast<size_t>(bh) * p.m + (i < p.m ? i : 0)) * kDW);
+                // Output: each thread writes its row of O / l into the slot's Q tile, free
+                // now that every MMA of the slot has completed, in the 128-byte-swizzled
+                // layout of the Q boxes (16-byte chunk c of row r at chunk c ^ (r % 8) of
+                // its 64-column atom); then one thread stores the tile with two TMA boxes,
+                // which clip rows past m.
+                const uint32_t stage = smem_addr(sm.q[s]) + row * 128;
 #pragma unroll 1
                 for (int c = 0; c < kDW / 32; ++c) {
                     uint32_t orr[32];
                     tmem_ld32(t_o + 32 * c, orr);
                     tmem_wait_ld();
                     reg_fence32(orr);
-                    if (i < p.m) {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint4 w;
-                            w.x = pack_bf16x2(__uint_as_float(orr[8 * q + 0]) * inv, __uint_as_float(orr[8 * q + 1]) * inv);
-                            w.y = pack_bf16x2(__uint_as_float(orr[8 * q + 2]) * inv, __uint_as_float(orr[8 * q + 3]) * inv);
-                            w.z = pack_bf16x2(__uint_as_float(orr[8 * q + 4]) * inv, __uint_as_float(orr[8 * q + 5]) * inv);
-                            w.w = pack_bf16x2(__uint_as_float(orr[8 * q + 6]) * inv, __uint_as_float(orr[8 * q + 7]) * inv);
-                            orow[4 * c + q] = w;
-                        }
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(orr[8 * q + 0]) * inv, __uint_as_float(orr[8 * q + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(orr[8 * q + 2]) * inv, __uint_as_float(orr[8 * q + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(orr[8 * q + 4]) * inv, __uint_as_float(orr[8 * q + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(orr[8 * q + 6]) * inv, __uint_as_float(orr[8 * q + 7]) * inv);
+                        const int chunk = (c & 1) * 4 + q; // 16-byte chunk within the 64-column atom
+                        st_shared_v4(stage + (c >> 1) * kAtomBytes + ((chunk ^ (row & 7)) << 4), w);
+                    }
+                }
+                fence_proxy_async_shared();
+                mbar_arrive(&sm.staged[s]);
+                if (row == 0) {
+                    if (wait_bar(&sm.staged[s], 0, ab, kSiteSmStaged)) {
+                        tma_store_3d(&tm_o, sm.q[s], 0, q0s_, bh);
+                        tma_store_3d(&tm_o, sm.q[s] + kAtomBytes, 64, q0s_, bh);
+                        bulk_commit_group();
+                        // the tile must stay in shared memory until the stores have read it
+                        bulk_wait_all();
                     }
                 }
             }
@@ -668,9 +685,9 @@ cudaError_t launch_wide(const Problem &pb, cudaStream_t stream)
     }
     if (!pb.bf16 || pb.d != kDW) return cudaErrorInvalidValue;
     const int BH = pb.B * pb.h;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if (!encode_bf16_3d(&tq, pb.q, kDW, pb.m, BH, kBM) || !encode_bf16_3d(&tk, pb.k, kDW, pb.n, BH, kBN) ||
-        !encode_bf16_3d(&tv, pb.v, kDW, pb.n, BH, kBN))
+        !encode_bf16_3d(&tv, pb.v, kDW, pb.n, BH, kBN) || !encode_bf16_3d(&to, pb.out, kDW, pb.m, BH, kBM))
         return cudaErrorInvalidValue;
     WideParams p;
     p.q = static_cast<const __nv_bfloat16 *>(pb.q);
@@ -692,9 +709,9 @@ cudaError_t launch_wide(const Problem &pb, cudaStream_t stream)
     const long long grid = p.head_pairs ? (BH + kSlots - 1) / kSlots : static_cast<long long>(BH) * p.q_pairs;
     if (grid > 0x7fffffff) return cudaErrorInvalidValue;
     if (p.head_pairs)
-        attn_wide_kernel<true><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+        attn_wide_kernel<true><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, p);
     else
-        attn_wide_kernel<false><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+        attn_wide_kernel<false><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, p);
     return cudaGetLastError();
 }
 
