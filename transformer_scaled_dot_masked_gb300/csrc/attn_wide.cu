@@ -3,9 +3,11 @@
 // equation of "Paper Deep Reading: Attention Is All You Need", §04, for the model
 // variants whose heads are 128 wide (the variants table of the same page).
 //
-// One CTA per (batch, head, pair of 128-row query tiles), heaviest pairs first.
-// The two tiles ("slots") share one stream of K and V tiles and take turns on the
-// tensor cores: while one slot's softmax runs, the other slot's MMAs do.  Q and
+// One CTA per (batch, head, pair of 128-row query tiles), heaviest pairs first;
+// for heads of a single query and key tile, one CTA per pair of heads instead
+// (attn_wide_kernel<true>).  The two tiles ("slots") share one stream of K and V
+// tiles (head pairs: one K and V tile each) and take turns on the tensor cores:
+// while one slot's softmax runs, the other slot's MMAs do.  Q and
 // each 128-key tile of K and V are 128 x 128 bf16, loaded by TMA as two 64-column
 // boxes (128-byte swizzle atoms) 16 KiB apart; K and V pass through two-stage rings
 // of their own (a K tile is free a tile before its V tile is).
@@ -23,8 +25,9 @@
 // P_0 V_(t-1), S_0 = Q_0 K_t^T, then O_1 += P_1 V_(t-1), S_1 = Q_1 K_t^T.  The tensor
 // cores run a thread's MMAs in order, so S_s(t) overwrites P_s(t - 1) only after
 // O_s += P_s V_(t-1) has read it, and the commit that signals S_s(t) also covers
-// that P V: once the softmax sees S_s(t), O_s is free to rescale.  Each slot covers only the key tiles its rows can
-// see (causal diagonal, padded length, window); the CTA loads their union.
+// that P V: once the softmax sees S_s(t), O_s is free to rescale.  Each slot covers
+// only the key tiles its rows can see (causal diagonal, padded length, window); the
+// CTA loads their union.
 // The epilogue divides O by the row sum (0 for a row with no allowed key) and stores
 // the bf16 tile through the slot's Q buffer with TMA.
 // TMEM (512 columns), per slot s at column 256 s: S [0,128) with P over [64,128)
@@ -54,7 +57,7 @@ namespace {
 constexpr int kBM = 128;                              // query rows per slot
 constexpr int kBN = 128;                              // keys per key tile
 constexpr int kDW = 128;                              // head width
-constexpr int kSlots = 2;                             // query tiles per CTA
+constexpr int kSlots = 2;                             // query tiles (or heads) per CTA
 constexpr uint32_t kAtomBytes = 128 * 64 * 2;         // one 64-column atom of a 128-row tile
 constexpr uint32_t kTileBytes = (kDW / 64) * kAtomBytes; // 32 KiB
 constexpr int kStages = 2;
