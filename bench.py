@@ -13,6 +13,14 @@ Prints ONE JSON line (rank 0).  Under torchrun each rank runs its own full
 batch (independent (batch, head) work, no collective on the data path) and
 the time is the max over ranks: weak scaling.
 
+Besides the contract's keys, the line carries (unless --kernel-only):
+other_workloads (the four short configurations), backward, decode, window
+(d_k = 64), head_widths (the encoder shape at d_k 16, 32, 64, 128), wide_heads
+(d_k = 128 on the long sequences: causal, unmasked, windows 256 and 1024), mha
+(projections + attention) and cpu_baseline.  roofline.traffic is the DRAM bytes
+of one launch from the committed ncu capture, reported while roofline.source_hash
+(the flash kernel's sources) matches it.
+
 --impl reference times the fp64 CPU oracle on the host cores instead, on a
 bounded sample of query rows of the same workload per step (the pages have no
 GPU implementation to compare against).
