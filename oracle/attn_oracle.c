@@ -17,7 +17,7 @@
  * the CUDA library; the mask flag values below mirror the library's public
  * enum because both describe the same caller-visible argument.
  *
- * Readings of the pages taken here (each one is listed in the design doc):
+ * Readings of the pages taken here:
  *  - key padding is trailing: key j of batch b is masked iff j >= len_b, the
  *    same for every head; len_b is clamped to [0, n]; query rows are never
  *    masked by padding;
