@@ -359,8 +359,8 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const int s = warp / 4, quad = warp % 4;
         const int row = quad * 32 + lane;
         const int bh = s == 0 ? bhs[0] : bhs[1], len = s == 0 ? lens[0] : lens[1];
-        const int q0s_ = s == 0 ? q0s[0] : q0s[1];
-        const int i = q0s_ + row;
+        const int q0_slot = s == 0 ? q0s[0] : q0s[1];
+        const int i = q0_slot + row;
         const int my_lo = s == 0 ? lo[0] : lo[1];
         const int n_s = (s == 0 ? hi[0] : hi[1]) - my_lo;
         if (n_s == 0) {
@@ -396,9 +396,9 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 // column c of the tile is allowed for row i iff cnt_lo <= c < cnt; a tile
                 // is a boundary tile when that fails for some column of some row
                 const int cnt = khi - key0, cnt_lo = klo - key0;
-                const bool boundary = (key0 + kBN > len) || (causal && key0 + kBN - 1 > q0s_) ||
-                                      (p.window >= 0 && (key0 < q0s_ + kBM - 1 - p.window ||
-                                                         key0 + kBN - 1 > q0s_ + p.window));
+                const bool boundary = (key0 + kBN > len) || (causal && key0 + kBN - 1 > q0_slot) ||
+                                      (p.window >= 0 && (key0 < q0_slot + kBM - 1 - p.window ||
+                                                         key0 + kBN - 1 > q0_slot + p.window));
                 float x[kBN];
 #pragma unroll
                 for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(sr[c]);
@@ -505,8 +505,8 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 mbar_arrive(&sm.staged[s]);
                 if (row == 0) {
                     if (wait_bar(&sm.staged[s], 0, ab, kSiteSmStaged)) {
-                        tma_store_3d(&tm_o, sm.q[s], 0, q0s_, bh);
-                        tma_store_3d(&tm_o, sm.q[s] + kAtomBytes, 64, q0s_, bh);
+                        tma_store_3d(&tm_o, sm.q[s], 0, q0_slot, bh);
+                        tma_store_3d(&tm_o, sm.q[s] + kAtomBytes, 64, q0_slot, bh);
                         bulk_commit_group();
                         // the tile must stay in shared memory until the stores have read it
                         bulk_wait_all();
