@@ -86,7 +86,8 @@ typedef enum {
     ATTN_KERNEL_FLASH = 1, /* tcgen05/TMA flash kernel, 256 query rows per CTA tile (bf16, d_k a multiple of 8, <= 64) */
     ATTN_KERNEL_SHORT = 2, /* same machinery, two heads per CTA tile, whole head resident (bf16, d_k as FLASH, m <= 128) */
     ATTN_KERNEL_SIMT = 3,  /* CUDA-core fp32 kernel (fp32 or bf16, d_k <= 128) */
-    ATTN_KERNEL_WIDE = 4   /* tcgen05/TMA kernel for d_k == 128, one 128-row query tile per CTA (bf16) */
+    ATTN_KERNEL_WIDE = 4   /* tcgen05/TMA kernel for d_k == 128 (bf16): two 128-row query tiles of one
+                              head per CTA, or two heads per CTA when m <= 128 and n <= 128 */
 } attn_kernel;
 
 typedef struct {
@@ -94,7 +95,8 @@ typedef struct {
     int32_t h;     /* heads, >= 1 */
     int32_t m;     /* query rows per (batch, head), >= 1 */
     int32_t n;     /* key/value rows per (batch, head), >= 1 */
-    int32_t d_k;   /* head width (d_v == d_k), 1..128; the tensor-core kernels need 64 */
+    int32_t d_k;   /* head width (d_v == d_k), 1..128; tensor cores take bf16 heads of a
+                      multiple of 8 up to 64, or of 128 */
     int32_t dtype; /* attn_dtype */
 } attn_dims;
 
