@@ -211,9 +211,10 @@ def pin_lengths_indexed_by_batch(o):
 
 
 def pin_brute_force(o):
-    """The full-matrix formula (oracle/brute.py) on every tiny shape and mask kind."""
+    """The full-matrix formula (oracle/brute.py) on every tiny shape and mask kind, at
+    the head widths the kernels take (16, 32, 64, 128) and odd ones."""
     rng = np.random.default_rng(19)
-    for d in (1, 2, 3, 64):
+    for d in (1, 2, 3, 16, 32, 64, 128):
         for m in range(1, 8):
             for n in range(1, 8):
                 B, h = 2, 2
@@ -351,23 +352,30 @@ def pin_lse(o):
     """lse against the full-matrix formula: exp(scale*QK^T + M - lse) has unit row sums,
     and uniform scores give log(len)."""
     rng = np.random.default_rng(35)
-    B, h, m, n, d = 2, 2, 7, 7, 3
+    for d in (3, 128):
+        _lse_unit_row_sums(o, rng, d)
+    zero = np.zeros((1, 1, 5, 3))
+    K = _rand(rng, 1, 1, 5, 3)
+    np.testing.assert_allclose(o.attn_lse(zero, K, None, CAUSAL, 1.0)[0, 0],
+                               np.log(np.arange(1, 6)), atol=1e-14)
+
+
+def _lse_unit_row_sums(o, rng, d):
+    B, h, m, n = 2, 2, 7, 7
     Q, K = _rand(rng, B, h, m, d), _rand(rng, B, h, n, d)
     lens = np.array([0, 5], dtype=np.int32)
+    scale = 0.7 / math.sqrt(d / 3.0)
     for mk in (0, PAD, CAUSAL, PAD | CAUSAL):
-        lse = o.attn_lse(Q, K, lens, mk, 0.7)
+        lse = o.attn_lse(Q, K, lens, mk, scale)
         for b in range(B):
             M = brute.additive_mask(m, n, mk, int(lens[b]))
             for head in range(h):
-                S = Q[b, head] @ K[b, head].T * 0.7 + M
+                S = Q[b, head] @ K[b, head].T * scale + M
                 for i in range(m):
                     if np.isfinite(S[i]).any():
                         assert abs(np.exp(S[i] - lse[b, head, i]).sum() - 1.0) <= 1e-13
                     else:
                         assert lse[b, head, i] == -np.inf
-    zero = np.zeros((1, 1, 5, 3))
-    np.testing.assert_allclose(o.attn_lse(zero, K[:1, :1, :5], None, CAUSAL, 1.0)[0, 0],
-                               np.log(np.arange(1, 6)), atol=1e-14)
 
 
 def pin_bwd_torch_autograd(o):
