@@ -408,17 +408,21 @@ WIN = 4
 
 
 def pin_window_brute_force(o):
-    """The full-matrix formula with the banded mask, every tiny shape, window and mask."""
+    """The full-matrix formula with the banded mask, every tiny shape, window and mask,
+    at head widths 3 and 128 (the widths windows run at on tensor cores include 128)."""
     rng = np.random.default_rng(41)
-    for n in range(1, 8):
-        for w in (0, 1, 2, 3, 9):
-            B, h, d = 2, 2, 3
-            Q, K, V = _rand(rng, B, h, n, d), _rand(rng, B, h, n, d), _rand(rng, B, h, n, d)
-            lens = rng.integers(0, n + 1, size=B).astype(np.int32)
-            for mk in (WIN, WIN | PAD, WIN | CAUSAL, WIN | PAD | CAUSAL):
-                got = o.attn_fwd(Q, K, V, lens, mk, 0.7, window=w)
-                ref = brute.attention(Q, K, V, lens, mk, 0.7, window=w)
-                np.testing.assert_allclose(got, ref, rtol=0, atol=1e-13, err_msg=f"n={n} w={w} mask={mk}")
+    for d in (3, 128):
+        scale = 0.7 / math.sqrt(d / 3.0)
+        for n in range(1, 8):
+            for w in (0, 1, 2, 3, 9):
+                B, h = 2, 2
+                Q, K, V = _rand(rng, B, h, n, d), _rand(rng, B, h, n, d), _rand(rng, B, h, n, d)
+                lens = rng.integers(0, n + 1, size=B).astype(np.int32)
+                for mk in (WIN, WIN | PAD, WIN | CAUSAL, WIN | PAD | CAUSAL):
+                    got = o.attn_fwd(Q, K, V, lens, mk, scale, window=w)
+                    ref = brute.attention(Q, K, V, lens, mk, scale, window=w)
+                    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-13,
+                                               err_msg=f"d={d} n={n} w={w} mask={mk}")
 
 
 def pin_window_zero_copies_values(o):
