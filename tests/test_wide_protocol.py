@@ -11,8 +11,9 @@ thread's tcgen05 operations execute in order), the two issuers' streams interlea
 at random.  The model checks that no role waits forever, that every MMA reads the
 K or V tile it should from its stage (a refill clears the stage while it is in
 flight), that each P V reads the P of its own tile and each S overwrites P only
-after that P V, and that O holds exactly the finished tiles when the softmax sees
-the next S (so it may rescale) and when the epilogue reads it.  A mutant with
+after that P V, that O holds exactly the finished tiles when the softmax sees the
+next S (so it may rescale) and when the epilogue reads it, and that no S MMA is
+left to read the slot's Q buffer when the epilogue stages its output tile there.  A mutant with
 stage-release barriers that expect one commit instead of two must be caught.
 """
 import random
@@ -157,6 +158,9 @@ def simulate(ranges, head_pairs, rng, release_count=2):
             while not bar[f"o{s}"].done(0):
                 yield
             assert tmem["O"][s] == list(range(lo[s], hi[s]))
+            # the epilogue stages the output tile in the slot's Q buffer: no S MMA of
+            # the slot may still be waiting to read Q
+            assert not any(op[0] == "s" and op[1] == s for op in pipes[0] + pipes[1])
 
     def execute(op):
         if op[0] == "commit":
