@@ -13,8 +13,9 @@ K or V tile it should from its stage (a refill clears the stage while it is in
 flight), that each P V reads the P of its own tile and each S overwrites P only
 after that P V, that O holds exactly the finished tiles when the softmax sees the
 next S (so it may rescale) and when the epilogue reads it, and that no S MMA is
-left to read the slot's Q buffer when the epilogue stages its output tile there.  A mutant with
-stage-release barriers that expect one commit instead of two must be caught.
+left to read the slot's Q buffer when the epilogue stages its output tile there.
+A mutant with stage-release barriers that expect one commit instead of two must be
+caught.
 """
 import random
 
