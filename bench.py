@@ -92,7 +92,7 @@ def row_pairs(w, lengths, rows) -> float:
 
 
 # DRAM bytes (read + write) of one flash-kernel launch on the default workload,
-# from an ncu capture (profiles/attn_flash_long_causal_8192.md), keyed by a hash of
+# from one ncu capture of that launch (dram__bytes_read.sum + dram__bytes_write.sum), keyed by a hash of
 # the sources the kernel is compiled from: any later change to them reports null.
 MEASURED_TRAFFIC = {"733f78500373ad62": 847713536 + 46592000}
 FLASH_SOURCES = ("attn_flash.cu", "softmax_tile.cuh", "ptx.cuh")

@@ -64,7 +64,7 @@ typedef enum {
     ATTN_ERR_UNSUPPORTED = 6,    /* the kernel asked for cannot run this call */
     ATTN_ERR_CUDA = 7,           /* a CUDA runtime call failed (device query, launch) */
     ATTN_ERR_DEVICE_TIMEOUT = 8, /* a kernel gave up a bounded wait (see attn_device_status) */
-    ATTN_ERR_VALUE = 9,          /* scale is negative or not finite */
+    ATTN_ERR_VALUE = 9,          /* scale is negative (other than ATTN_SCALE_DEFAULT) or not finite */
     ATTN_ERR_ALIAS = 10,         /* out overlaps Q, K, V or key_lengths */
     ATTN_ERR_SCRATCH = 11        /* the call needs more scratch than attn_fwd_noalloc holds */
 } attn_status;
@@ -75,6 +75,14 @@ typedef enum {
     ATTN_MASK_CAUSAL = 2,
     ATTN_MASK_WINDOW = 4 /* restricted self-attention; attn_fwd_window only */
 } attn_mask_kind; /* bit flags: 3 = key padding and causal */
+
+/*
+ * Passing ATTN_SCALE_DEFAULT as `scale` asks the library for the formula's own
+ * scale, 1/sqrt(d_k) ("Paper Deep Reading", §04: the dot products are divided by
+ * sqrt(d_k) so that their variance stays near 1), computed on the host in double
+ * and rounded to float.  Any other negative or non-finite scale is rejected.
+ */
+#define ATTN_SCALE_DEFAULT (-1.0f)
 
 typedef enum {
     ATTN_BF16 = 0, /* bf16 in and out; fp32 accumulation and softmax state */
@@ -109,7 +117,8 @@ typedef struct {
  *                KEY_PADDING (may be NULL otherwise).  Values are clamped to [0, n]
  *                on the device.
  *   mask_kind    attn_mask_kind bits
- *   scale        multiplies Q K^T; 1/sqrt(d_k) in the formula.  Must be finite and >= 0.
+ *   scale        multiplies Q K^T; 1/sqrt(d_k) in the formula.  Must be finite and >= 0,
+ *                or ATTN_SCALE_DEFAULT for 1/sqrt(d_k).
  *   out          device tensor [B][h][m][d_k] of dims->dtype; 16-byte aligned
  *   dims         shapes and dtype (host pointer)
  *   stream       cudaStream_t to enqueue on (NULL = legacy default stream)
@@ -160,8 +169,8 @@ size_t attn_workspace_size(void);
  * workspaces; calls ordered on one stream may share one.
  *
  * Errors as attn_fwd, plus: workspace NULL (ATTN_ERR_NULL), too small
- * (ATTN_ERR_SHAPE), unaligned (ATTN_ERR_ALIGN), overlapping a tensor
- * (ATTN_ERR_ALIAS).
+ * (ATTN_ERR_SHAPE), unaligned (ATTN_ERR_ALIGN), overlapping a tensor or, with
+ * KEY_PADDING, key_lengths (ATTN_ERR_ALIAS).
  */
 attn_status attn_fwd_ws(const void *Q, const void *K, const void *V,
                         const int32_t *key_lengths, int mask_kind, float scale,
@@ -189,8 +198,11 @@ attn_status attn_fwd_ws(const void *Q, const void *K, const void *V,
  * that loads the library holds that array until the process exits.  The
  * first call on a device looks up the array's device address with that
  * device current (one-time set-up); make that first call before any stream
- * capture on that device.  Each call zeroes the counters it needs on
- * `stream` before its kernel.  All calls on a device share the one array:
+ * capture on that device.  The address is kept for the life of the process
+ * (a failed lookup is retried by the next call): calls after a device reset
+ * (cudaDeviceReset, or a new primary context) are not supported.  Calls whose
+ * kernel uses the array (bf16 heads of width up to 64) zero its counters on
+ * `stream` before their kernel.  All calls on a device share the one array:
  * calls that may run at the same time on the GPU (different streams) race
  * on it and must not be made; calls ordered on one stream are safe.
  *

@@ -481,6 +481,49 @@ def pin_window_torch_sdpa(o):
         np.testing.assert_allclose(got[live], ref[live], rtol=0, atol=1e-12)
 
 
+
+def pin_window_rows(o):
+    """Selected rows through the windowed row entry point equal the same rows of the
+    full-matrix formula with the banded mask, for every mask kind and w in {0, 2, 9}."""
+    rng = np.random.default_rng(46)
+    B, h, n, d = 2, 2, 12, 5
+    Q, K, V = _rand(rng, B, h, n, d), _rand(rng, B, h, n, d), _rand(rng, B, h, n, d)
+    lens = np.array([7, 12], dtype=np.int32)
+    rows = rng.choice(B * h * n, size=17, replace=False).astype(np.int64)
+    for w in (0, 2, 9):
+        for mk in (WIN, WIN | PAD, WIN | CAUSAL, WIN | PAD | CAUSAL):
+            ref = brute.attention(Q, K, V, lens, mk, 0.6, window=w).reshape(B * h * n, d)[rows]
+            got = o.attn_rows(Q, K, V, lens, mk, 0.6, rows, window=w)
+            np.testing.assert_allclose(got, ref, rtol=0, atol=1e-13, err_msg=f"w={w} mask={mk}")
+
+
+def pin_window_lse(o):
+    """Windowed log-sum-exp against the banded full-matrix formula: exp(scale*QK^T + M - lse)
+    has unit row sums; with Q = 0 every allowed key scores 0, so lse = log(number of keys
+    in the row's window)."""
+    rng = np.random.default_rng(47)
+    B, h, n, d = 2, 2, 9, 4
+    Q, K = _rand(rng, B, h, n, d), _rand(rng, B, h, n, d)
+    lens = np.array([0, 6], dtype=np.int32)
+    for w in (0, 2, 9):
+        for mk in (WIN, WIN | PAD, WIN | CAUSAL, WIN | PAD | CAUSAL):
+            lse = o.attn_lse(Q, K, lens, mk, 0.7, window=w)
+            for b in range(B):
+                M = brute.additive_mask(n, n, mk, int(lens[b]), w)
+                for head in range(h):
+                    S = Q[b, head] @ K[b, head].T * 0.7 + M
+                    for i in range(n):
+                        if np.isfinite(S[i]).any():
+                            assert abs(np.exp(S[i] - lse[b, head, i]).sum() - 1.0) <= 1e-13
+                        else:
+                            assert lse[b, head, i] == -np.inf
+    zero = np.zeros((1, 1, n, d))
+    for w in (0, 1, 3):
+        got = o.attn_lse(zero, K[:1, :1], None, WIN, 1.0, window=w)[0, 0]
+        count = np.array([min(n - 1, i + w) - max(0, i - w) + 1 for i in range(n)], dtype=np.float64)
+        np.testing.assert_allclose(got, np.log(count), rtol=0, atol=1e-14)
+
+
 # ---------------------------------------------------------------- multi-head projections
 def pin_mha_two_head_example(o):
     """The primer's two-head example through the projections: X_q = X_kv = I, head 1's
@@ -570,6 +613,8 @@ ALL_PINS = [
     pin_window_wide_equals_full,
     pin_window_locality,
     pin_window_torch_sdpa,
+    pin_window_rows,
+    pin_window_lse,
     pin_mha_two_head_example,
     pin_mha_torch,
     pin_mha_identity_projections,

@@ -88,6 +88,7 @@ def _call(q=A, k=B_, v=C, lens=L, mask=0, scale=0.125, out=O, dims=(2, 2, 8, 8, 
     (dict(mask=4), 4), (dict(mask=-1), 4),
     (dict(q=A + 8), 5), (dict(out=O + 4), 5), (dict(lens=L + 2, mask=1), 5),
     (dict(scale=float("nan")), 9), (dict(scale=float("inf")), 9), (dict(scale=-0.5), 9),
+    (dict(scale=-1.0001), 9), (dict(scale=N.SCALE_DEFAULT, q=A + 8), 5),  # the sentinel passes the scale check
     (dict(out=A), 10), (dict(out=B_ + 64), 10), (dict(out=L - 16, mask=1), 10),
 ])
 def test_rejects_bad_arguments(kwargs, status):
@@ -113,7 +114,8 @@ def test_null_dims():
 def _call_ws(ws=0x6000000, ws_bytes=None, **kw):
     d = N.make_dims(*(kw.pop("dims", (2, 2, 8, 8, 64, 0))))
     ws_bytes = N.workspace_size() if ws_bytes is None else ws_bytes
-    return N.fwd_ws_raw(kw.get("q", A), B_, C, L, 0, 0.125, kw.get("out", O), d, None, ws, ws_bytes)
+    return N.fwd_ws_raw(kw.get("q", A), B_, C, L, kw.get("mask", 0), 0.125, kw.get("out", O), d, None, ws,
+                        ws_bytes)
 
 
 def test_workspace_validation():
@@ -124,6 +126,8 @@ def test_workspace_validation():
     assert _call_ws(ws=O + 64) == 10          # inside out
     assert _call_ws(ws=A) == 10               # inside Q
     assert _call_ws(q=A + 8) == 5             # tensor checks still apply
+    assert _call_ws(ws=L, mask=1) == 10       # over the key lengths the kernel reads
+    assert _call_ws(ws=L - 16, mask=1) == 10
 
 
 # ---------------------------------------------------------------- host buffers

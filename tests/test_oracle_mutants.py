@@ -41,6 +41,10 @@ MUTANTS = {
     # restricted attention
     "window_off_by_one": ("(i - j > g_window || j - i > g_window)", "(i - j >= g_window || j - i > g_window)"),
     "window_one_sided": ("(i - j > g_window || j - i > g_window)", "(i - j > g_window)"),
+    "window_rows_ignores_window": ("g_window = window;\n    int rc = oracle_attn_rows(",
+                                   "int rc = oracle_attn_rows("),
+    "window_lse_ignores_window": ("g_window = window;\n    int rc = oracle_attn_lse(",
+                                  "int rc = oracle_attn_lse("),
 }
 
 

@@ -5,9 +5,14 @@ framework that owns all device memory).  It takes no workspace and uses the
 library's own statically allocated device array instead.
 
 Called through the C ABI and compared with attn_fwd on the same inputs, on two
-calls in a row (the array keeps the previous call's contents, so the second
-call checks that each call starts from cleared counters).  This file is named
-to be collected last; it passes alone and after the other tests.
+calls in a row: the array keeps the previous call's contents, and the second
+call runs on what the first left there.  (A kernel that finishes normally leaves
+its tile counters at zero itself; the zeroing each call does first matters only
+after a kernel that gave up a bounded wait, which these calls do not provoke.)
+The cases cover both tensor-core kernels that read the array (pair mode and
+split mode), the d_k = 128 kernel and the CUDA-core kernel (which use none of
+it), and key lengths of 0, 1 and n.  This file is named to be collected last;
+it passes alone and after the other tests.
 """
 import numpy as np
 import pytest
@@ -33,10 +38,14 @@ def _noalloc(q, k, v, lens, w, out):
     (5, dict(B=1, h=4, m=1024, n=1024)),   # long causal, pair mode
     (4, dict(B=6)),                        # cross-attention with padding, split mode
     (1, dict()),                           # fp32 (CUDA-core kernel, no scratch needed)
+    (5, dict(B=1, h=2, m=384, n=384, d=128, scale=128 ** -0.5)),  # d_k = 128 kernel, no scratch needed
+    (2, dict(B=3, h=2)),                   # encoder padding with lengths 0, 1 and n (below)
 ])
 def test_noalloc_matches_attn_fwd_twice(cfg, shape):
     w = WORKLOADS[cfg].with_(**shape)
     inp = draw(w)
+    if cfg == 2:
+        inp.key_lengths[:] = [0, 1, w.n]
     q, k, v = (to_device(x, w.dtype) for x in (inp.q, inp.k, inp.v))
     lens = torch.from_numpy(inp.key_lengths).cuda()
     ref = attn.attn_fwd(q, k, v, lens, w.mask, w.scale)

@@ -17,7 +17,7 @@ from typing import Optional
 
 from . import _native
 from ._native import (AttnError, KERNEL_AUTO, KERNEL_FLASH, KERNEL_SHORT, KERNEL_SIMT, KERNEL_WIDE, MASK_CAUSAL,
-                      MASK_KEY_PADDING, MASK_NONE, MASK_WINDOW, DTYPE_BF16, DTYPE_FP32)
+                      MASK_KEY_PADDING, MASK_NONE, MASK_WINDOW, DTYPE_BF16, DTYPE_FP32, SCALE_DEFAULT)
 
 __all__ = ["attn_fwd", "attn_fwd_host", "host_workspace_size", "attn_mha_fwd", "mha_workspace_size", "attn_fwd_window", "attn_fwd_lse", "MASK_WINDOW", "attn_bwd", "bwd_workspace_size", "attn_decode", "decode_workspace_size", "AttnError", "select_kernel", "device_status", "make_workspace", "workspace_size", "MASK_NONE", "MASK_KEY_PADDING",
            "MASK_CAUSAL", "KERNEL_AUTO", "KERNEL_FLASH", "KERNEL_SHORT", "KERNEL_SIMT", "KERNEL_WIDE"]
@@ -49,7 +49,7 @@ def attn_fwd(q, k, v, key_lengths=None, mask_kind: int = MASK_NONE, scale: Optio
 
     q: [B, h, m, d_k]; k, v: [B, h, n, d_k]; same dtype (bf16 or fp32), contiguous,
     on the current CUDA device.  key_lengths: int32 [B] CUDA tensor (needed for
-    MASK_KEY_PADDING).  scale defaults to 1/sqrt(d_k).  out: optional preallocated
+    MASK_KEY_PADDING).  scale defaults to 1/sqrt(d_k), which the library computes (ATTN_SCALE_DEFAULT).  out: optional preallocated
     [B, h, m, d_k] tensor.  Enqueued on ``stream`` (default: torch's current stream).
     workspace: optional zero-filled CUDA buffer from ``make_workspace`` (selects the
     dynamic tile schedule, attn_fwd_ws; not combinable with an explicit kernel).
@@ -66,7 +66,7 @@ def attn_fwd(q, k, v, key_lengths=None, mask_kind: int = MASK_NONE, scale: Optio
     if k.shape != (B, h, n, d) or v.shape != k.shape or q.dtype != k.dtype or q.dtype != v.dtype:
         raise ValueError(f"shape/dtype mismatch: q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
     if scale is None:
-        scale = d ** -0.5
+        scale = SCALE_DEFAULT
     if out is None:
         out = torch.empty_like(q)
     elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
@@ -124,7 +124,7 @@ def attn_fwd_host(q, k, v, key_lengths=None, mask_kind: int = MASK_NONE, scale: 
     if k.shape != (B, h, n, d) or v.shape != k.shape or q.dtype != k.dtype or q.dtype != v.dtype:
         raise ValueError(f"shape/dtype mismatch: q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
     if scale is None:
-        scale = d ** -0.5
+        scale = SCALE_DEFAULT
     if out is None:
         out = torch.empty(q.shape, dtype=q.dtype, pin_memory=q.is_pinned())
     elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or out.is_cuda:
@@ -196,7 +196,7 @@ def attn_fwd_lse(q, k, v, key_lengths=None, mask_kind: int = MASK_NONE, scale: O
     the statistic ``attn_bwd`` needs.  Returns (out, lse)."""
     import torch
     B, h, m, n, d = _check_qkv(q, k, v)
-    scale = d ** -0.5 if scale is None else scale
+    scale = SCALE_DEFAULT if scale is None else scale
     if out is None:
         out = torch.empty_like(q)
     _like(out, q, "out")
@@ -228,7 +228,7 @@ def attn_bwd(q, k, v, out, dout, lse, key_lengths=None, mask_kind: int = MASK_NO
     """
     import torch
     B, h, m, n, d = _check_qkv(q, k, v)
-    scale = d ** -0.5 if scale is None else scale
+    scale = SCALE_DEFAULT if scale is None else scale
     _like(out, q, "out")
     _like(dout, q, "dout")
     if lse.shape != (B, h, m) or lse.dtype != torch.float32 or not lse.is_contiguous() or not lse.is_cuda:
@@ -272,7 +272,7 @@ def attn_decode(q, k_cache, v_cache, cache_lengths=None, scale: Optional[float] 
     """
     import torch
     B, h, m, n, d = _check_qkv(q, k_cache, v_cache)
-    scale = d ** -0.5 if scale is None else scale
+    scale = SCALE_DEFAULT if scale is None else scale
     if out is None:
         out = torch.empty_like(q)
     _like(out, q, "out")
@@ -303,7 +303,7 @@ def attn_fwd_window(q, k, v, key_lengths=None, mask_kind: int = MASK_WINDOW, win
     the keys j with |i - j| <= window (combinable with MASK_CAUSAL and MASK_KEY_PADDING)."""
     import torch
     B, h, m, n, d = _check_qkv(q, k, v)
-    scale = d ** -0.5 if scale is None else scale
+    scale = SCALE_DEFAULT if scale is None else scale
     if out is None:
         out = torch.empty_like(q)
     _like(out, q, "out")
@@ -338,7 +338,7 @@ def attn_mha_fwd(xq, xkv, wq, wk, wv, wo, h: int, key_lengths=None, mask_kind: i
     if xkv.shape != (B, n, dm) or wq.shape != (dm, h * 64) or wk.shape != wq.shape or wv.shape != wq.shape \
             or wo.shape != (h * 64, dm):
         raise ValueError("shape mismatch between inputs, projections and h")
-    scale = 64 ** -0.5 if scale is None else scale
+    scale = SCALE_DEFAULT if scale is None else scale
     if out is None:
         out = torch.empty_like(xq)
     need = _native.mha_workspace_size(B, h, m, n, dm)

@@ -25,6 +25,8 @@ ATTN_OK = 0
 ATTN_ERR_DEVICE_TIMEOUT = 8
 MASK_NONE, MASK_KEY_PADDING, MASK_CAUSAL, MASK_WINDOW = 0, 1, 2, 4
 DTYPE_BF16, DTYPE_FP32 = 0, 1
+# ATTN_SCALE_DEFAULT: the library substitutes the formula's scale, 1/sqrt(d_k)
+SCALE_DEFAULT = -1.0
 KERNEL_AUTO, KERNEL_FLASH, KERNEL_SHORT, KERNEL_SIMT, KERNEL_WIDE = 0, 1, 2, 3, 4
 KERNEL_NAMES = {KERNEL_AUTO: "auto", KERNEL_FLASH: "flash", KERNEL_SHORT: "short", KERNEL_SIMT: "simt",
                 KERNEL_WIDE: "wide"}

@@ -33,6 +33,15 @@ int auto_kernel(const attn_dims &d)
     return ATTN_KERNEL_SIMT;
 }
 
+bool scale_ok(float scale) { return scale == ATTN_SCALE_DEFAULT || (std::isfinite(scale) && scale >= 0.f); }
+
+// The scale a kernel multiplies the scores by: the caller's, or 1/sqrt(d_k) for
+// ATTN_SCALE_DEFAULT (the formula's scale).
+float resolve_scale(float scale, int d_k)
+{
+    return scale == ATTN_SCALE_DEFAULT ? static_cast<float>(1.0 / std::sqrt(static_cast<double>(d_k))) : scale;
+}
+
 attn_status validate_dims(const attn_dims *dims, int mask_kind, float scale)
 {
     if (dims == nullptr) return ATTN_ERR_NULL;
@@ -43,7 +52,7 @@ attn_status validate_dims(const attn_dims *dims, int mask_kind, float scale)
     if (d.B < 1 || d.h < 1 || d.m < 1 || d.n < 1) return ATTN_ERR_SHAPE;
     if (d.B > 65535 || d.h > 65535) return ATTN_ERR_SHAPE;                  // grid limits
     if ((mask_kind & ATTN_MASK_CAUSAL) && d.m != d.n) return ATTN_ERR_SHAPE; // queries and keys share positions
-    if (!std::isfinite(scale) || scale < 0.f) return ATTN_ERR_VALUE;
+    if (!scale_ok(scale)) return ATTN_ERR_VALUE;
     return ATTN_OK;
 }
 
@@ -95,7 +104,7 @@ attn_status run(const void *Q, const void *K, const void *V, const int32_t *key_
     p.d = d.d_k;
     p.mask_kind = mask_kind;
     p.window = window;
-    p.scale = scale;
+    p.scale = resolve_scale(scale, d.d_k);
     p.bf16 = d.dtype == ATTN_BF16;
     p.overlap_launch = overlap_launch;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -129,14 +138,14 @@ attn_status run(const void *Q, const void *K, const void *V, const int32_t *key_
 static __device__ __align__(256) unsigned char g_noalloc_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
 
 struct NoAllocDevice {
-    std::once_flag once;
-    void *ptr = nullptr;
-    cudaError_t err = cudaSuccess;
+    std::mutex lock;
+    void *ptr = nullptr; // set once a lookup has succeeded; kept for the life of the process
 };
 constexpr int kMaxDevices = 64;
 NoAllocDevice g_noalloc_devices[kMaxDevices];
 
-// Device address of g_noalloc_scratch on the current device (set up on first use).
+// Device address of g_noalloc_scratch on the current device.  The first successful
+// lookup is kept; a failed one is not, so the next call tries again.
 cudaError_t noalloc_scratch(void **ptr)
 {
     int dev = 0;
@@ -144,8 +153,13 @@ cudaError_t noalloc_scratch(void **ptr)
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     NoAllocDevice &d = g_noalloc_devices[dev];
-    std::call_once(d.once, [&d] { d.err = cudaGetSymbolAddress(&d.ptr, g_noalloc_scratch); });
-    if (d.err != cudaSuccess) return d.err;
+    std::lock_guard<std::mutex> guard(d.lock);
+    if (d.ptr == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        d.ptr = p;
+    }
     *ptr = d.ptr;
     return cudaSuccess;
 }
@@ -162,8 +176,12 @@ attn_status attn_fwd_noalloc(const void *Q, const void *K, const void *V, const 
     if (attn::kWorkspaceBytes > ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_SCRATCH;
     void *scratch = nullptr;
     if (noalloc_scratch(&scratch) != cudaSuccess) return ATTN_ERR_CUDA;
-    // the array keeps the previous call's contents: the tile counters must start at zero
-    if (cudaMemsetAsync(scratch, 0, attn::kWorkspaceBytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    // The array keeps the previous call's contents.  Only the d_k <= 64 tensor-core
+    // kernels read it (their tile counters); they leave it zeroed when they finish,
+    // but not after an earlier call gave up a bounded wait, so it is cleared here.
+    const int kernel = auto_kernel(*dims);
+    if ((kernel == ATTN_KERNEL_FLASH || kernel == ATTN_KERNEL_SHORT) &&
+        cudaMemsetAsync(scratch, 0, attn::kWorkspaceBytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;
     return run(Q, K, V, key_lengths, mask_kind, scale, out, dims, stream, ATTN_KERNEL_AUTO,
                static_cast<int *>(scratch));
@@ -194,6 +212,8 @@ attn_status attn_fwd_ws(const void *Q, const void *K, const void *V, const int32
     const uint64_t kbytes = static_cast<uint64_t>(d.B) * d.h * d.n * d.d_k * esz;
     if (overlaps(workspace, workspace_bytes, out, qbytes) || overlaps(workspace, workspace_bytes, Q, qbytes) ||
         overlaps(workspace, workspace_bytes, K, kbytes) || overlaps(workspace, workspace_bytes, V, kbytes))
+        return ATTN_ERR_ALIAS;
+    if ((mask_kind & ATTN_MASK_KEY_PADDING) && overlaps(workspace, workspace_bytes, key_lengths, 4ull * d.B))
         return ATTN_ERR_ALIAS;
     return run(Q, K, V, key_lengths, mask_kind, scale, out, dims, stream, ATTN_KERNEL_AUTO,
                static_cast<int *>(workspace));
@@ -297,7 +317,7 @@ attn_status attn_bwd(const void *Q, const void *K, const void *V, const void *ou
     p.m = d.m;
     p.n = d.n;
     p.mask_kind = mask_kind;
-    p.scale = scale;
+    p.scale = resolve_scale(scale, d.d_k);
     return attn::launch_bwd(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -375,7 +395,7 @@ attn_status attn_decode(const void *Q, const void *K, const void *V, const int32
     p.n = d.n;
     p.d = 64;
     p.mask_kind = mask;
-    p.scale = scale;
+    p.scale = resolve_scale(scale, d.d_k);
     p.bf16 = true;
     return attn::launch_decode(p, workspace, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK
                                                                                                   : ATTN_ERR_CUDA;
@@ -426,7 +446,7 @@ attn_status attn_mha_fwd(const void *Xq, const void *Xkv, const void *Wq, const 
     if ((mask_kind & ~(ATTN_MASK_KEY_PADDING | ATTN_MASK_CAUSAL)) != 0) return ATTN_ERR_MASK;
     const attn_mha_dims &d = *dims;
     if ((mask_kind & ATTN_MASK_CAUSAL) && d.m != d.n) return ATTN_ERR_SHAPE;
-    if (!std::isfinite(scale) || scale < 0.f) return ATTN_ERR_VALUE;
+    if (!scale_ok(scale)) return ATTN_ERR_VALUE;
     const void *ptrs[8] = {Xq, Xkv, Wq, Wk, Wv, Wo, out, workspace};
     for (const void *q : ptrs)
         if (!aligned(q, 16)) return ATTN_ERR_ALIGN;
@@ -710,7 +730,7 @@ const char *attn_status_string(int status)
     case ATTN_ERR_UNSUPPORTED: return "the requested kernel cannot run this call";
     case ATTN_ERR_CUDA: return "CUDA runtime error";
     case ATTN_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait; its output is incomplete";
-    case ATTN_ERR_VALUE: return "scale must be finite and >= 0";
+    case ATTN_ERR_VALUE: return "scale must be finite and >= 0, or ATTN_SCALE_DEFAULT";
     case ATTN_ERR_ALIAS: return "out overlaps an input";
     case ATTN_ERR_SCRATCH: return "the call needs more scratch than attn_fwd_noalloc holds";
     default: return "unknown status";
