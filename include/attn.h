@@ -94,8 +94,11 @@ typedef enum {
     ATTN_KERNEL_FLASH = 1, /* tcgen05/TMA flash kernel, 256 query rows per CTA tile (bf16, d_k a multiple of 8, <= 64) */
     ATTN_KERNEL_SHORT = 2, /* same machinery, two heads per CTA tile, whole head resident (bf16, d_k as FLASH, m <= 128) */
     ATTN_KERNEL_SIMT = 3,  /* CUDA-core fp32 kernel (fp32 or bf16, d_k <= 128) */
-    ATTN_KERNEL_WIDE = 4   /* tcgen05/TMA kernel for d_k == 128 (bf16): two 128-row query tiles of one
+    ATTN_KERNEL_WIDE = 4,  /* tcgen05/TMA kernel for d_k == 128 (bf16): two 128-row query tiles of one
                               head per CTA, or two heads per CTA when m <= 128 and n <= 128 */
+    ATTN_KERNEL_RESIDENT = 5 /* tcgen05/TMA kernel for short sequences: one head per CTA with its Q, K
+                                and V resident, exact two-pass softmax per row (bf16, d_k as FLASH,
+                                m <= 128, n <= 192) */
 } attn_kernel;
 
 typedef struct {
@@ -131,9 +134,13 @@ typedef struct {
  * an input (ATTN_ERR_ALIAS), CUDA failures (ATTN_ERR_CUDA).  Inputs must be
  * finite: non-finite values propagate through the arithmetic as IEEE rules
  * dictate.  Kernel choice: bf16 with d_k a multiple of 8 up to 64 runs on tensor
- * cores, narrower heads zero-padded to 64 inside the kernel (ATTN_KERNEL_SHORT
- * when m <= 128, else ATTN_KERNEL_FLASH); bf16 with d_k == 128 on
- * ATTN_KERNEL_WIDE (tensor cores); everything else runs ATTN_KERNEL_SIMT.
+ * cores, narrower heads zero-padded to 64 inside the kernel (ATTN_KERNEL_RESIDENT
+ * when m <= 128 and n <= 192, ATTN_KERNEL_SHORT when m <= 128 and n > 192, else
+ * ATTN_KERNEL_FLASH); bf16 with d_k == 128 on ATTN_KERNEL_WIDE (tensor cores);
+ * everything else runs ATTN_KERNEL_SIMT.  The resident kernel is launched as a
+ * programmatic dependent of the kernel before it on the stream: its launch and
+ * set-up overlap that kernel's tail, and it reads and writes memory only after
+ * that kernel has completed (stream order is kept).
  */
 attn_status attn_fwd(const void *Q, const void *K, const void *V,
                      const int32_t *key_lengths, int mask_kind, float scale,
@@ -427,6 +434,26 @@ int attn_select_kernel(const attn_dims *dims, int mask_kind);
  * leaves its output incomplete, but leaves the CUDA context usable.
  */
 attn_status attn_device_status(void *stream, int32_t *info);
+
+/*
+ * Test hook of the failure detection (not part of the operation; no page of the
+ * method has a counterpart).  Runs the whole-head-resident kernel of attn_fwd on
+ * these arguments with every bounded wait limited to wait_ns nanoseconds and with
+ * one row thread withholding its report that its first chunk of weights is stored,
+ * so the MMA-issuing thread's wait for that chunk runs out: the kernel records the
+ * time-out (attn_device_status then returns ATTN_ERR_DEVICE_TIMEOUT with info 403,
+ * the weights wait of that kernel), waits for its own copies and MMAs, frees its
+ * TMEM and exits without writing `out`.  The CUDA context stays usable.  It lets a
+ * test check the abort path without any fault on the GPU.
+ *
+ * Arguments as attn_fwd; the dims must be ones the resident kernel runs (bf16, d_k a
+ * multiple of 8 up to 64, m <= 128, n <= 192; ATTN_ERR_UNSUPPORTED otherwise);
+ * wait_ns in [100000, 2000000000] (ATTN_ERR_VALUE otherwise).
+ */
+attn_status attn_test_withheld_arrival(const void *Q, const void *K, const void *V,
+                                       const int32_t *key_lengths, int mask_kind, float scale,
+                                       void *out, const attn_dims *dims, uint64_t wait_ns,
+                                       void *stream);
 
 /* Static description of a status code (never NULL). */
 const char *attn_status_string(int status);

@@ -34,6 +34,14 @@ def tol_for(w):
     return BF16_TOL if w.dtype == "bf16" else FP32_TOL
 
 
+def rounding_bound(ref, tol=BF16_TOL):
+    """Per-element bound for bf16 outputs: tol, plus the output's own half-ulp where
+    |ref| >= 4 (the spacing of bf16 there is 2^-5, so a correctly rounded output can be
+    up to 0.0156 from the exact value, beyond 1e-2 by its rounding alone)."""
+    half_ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -126))) - 8)
+    return tol + np.where(np.abs(ref) >= 4.0, half_ulp, 0.0)
+
+
 def report(got, ref, tol):
     err = np.abs(got - ref)
     worst = np.unravel_index(int(err.argmax()), err.shape)

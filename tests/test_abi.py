@@ -34,8 +34,9 @@ def test_python_constants_match_header():
     assert N.ATTN_ERR_DEVICE_TIMEOUT == _enum("ATTN_ERR_DEVICE_TIMEOUT")
     assert (N.MASK_KEY_PADDING, N.MASK_CAUSAL) == (_enum("ATTN_MASK_KEY_PADDING"), _enum("ATTN_MASK_CAUSAL"))
     assert (N.DTYPE_BF16, N.DTYPE_FP32) == (_enum("ATTN_BF16"), _enum("ATTN_FP32"))
-    assert (N.KERNEL_FLASH, N.KERNEL_SHORT, N.KERNEL_SIMT) == (
-        _enum("ATTN_KERNEL_FLASH"), _enum("ATTN_KERNEL_SHORT"), _enum("ATTN_KERNEL_SIMT"))
+    assert (N.KERNEL_FLASH, N.KERNEL_SHORT, N.KERNEL_SIMT, N.KERNEL_WIDE, N.KERNEL_RESIDENT) == (
+        _enum("ATTN_KERNEL_FLASH"), _enum("ATTN_KERNEL_SHORT"), _enum("ATTN_KERNEL_SIMT"),
+        _enum("ATTN_KERNEL_WIDE"), _enum("ATTN_KERNEL_RESIDENT"))
     # the dims struct is six int32 fields in this order
     fields = re.search(r"typedef struct \{(.*?)\} attn_dims;", HEADER_TEXT, re.S).group(1)
     assert re.findall(r"int32_t (\w+);", fields) == [f for f, _ in N.AttnDims._fields_]
@@ -51,14 +52,18 @@ def test_status_strings_and_version():
 
 def test_kernel_selection():
     bf, f32 = N.DTYPE_BF16, N.DTYPE_FP32
-    assert attn.select_kernel(64, 8, 100, 100, 64, bf, 1) == N.KERNEL_SHORT
-    assert attn.select_kernel(32, 16, 128, 160, 64, bf, 1) == N.KERNEL_SHORT
+    assert attn.select_kernel(64, 8, 100, 100, 64, bf, 1) == N.KERNEL_RESIDENT
+    assert attn.select_kernel(32, 16, 128, 160, 64, bf, 1) == N.KERNEL_RESIDENT
+    assert attn.select_kernel(32, 8, 128, 128, 64, bf, 2) == N.KERNEL_RESIDENT
+    assert attn.select_kernel(2, 2, 128, 192, 64, bf, 0) == N.KERNEL_RESIDENT  # the most keys it holds
+    assert attn.select_kernel(2, 2, 128, 193, 64, bf, 0) == N.KERNEL_SHORT
+    assert attn.select_kernel(2, 2, 129, 100, 64, bf, 0) == N.KERNEL_FLASH
     assert attn.select_kernel(4, 16, 8192, 8192, 64, bf, 2) == N.KERNEL_FLASH
     assert attn.select_kernel(1, 1, 16, 16, 64, f32, 0) == N.KERNEL_SIMT
     # bf16 heads narrower than 64 (multiples of 8) run zero-padded on tensor cores
-    assert attn.select_kernel(1, 1, 16, 16, 32, bf, 0) == N.KERNEL_SHORT
+    assert attn.select_kernel(1, 1, 16, 16, 32, bf, 0) == N.KERNEL_RESIDENT
     assert attn.select_kernel(1, 1, 300, 300, 16, bf, 2) == N.KERNEL_FLASH
-    assert attn.select_kernel(1, 1, 16, 16, 8, bf, 0) == N.KERNEL_SHORT
+    assert attn.select_kernel(1, 1, 16, 16, 8, bf, 0) == N.KERNEL_RESIDENT
     assert attn.select_kernel(1, 1, 16, 16, 20, bf, 0) == N.KERNEL_SIMT    # not a multiple of 8
     assert attn.select_kernel(1, 1, 16, 16, 128, bf, 0) == N.KERNEL_WIDE   # 128 wide: its own kernel
     assert attn.select_kernel(1, 1, 16, 16, 96, bf, 0) == N.KERNEL_SIMT    # other widths above 64
@@ -104,6 +109,10 @@ def test_rejects_unsupported_kernel_choice():
     assert _call(dims=(2, 2, 8, 8, 128, 0), kernel=N.KERNEL_FLASH) == 6  # wider than 64
     assert _call(dims=(2, 2, 8, 8, 64, 0), kernel=N.KERNEL_WIDE) == 6    # the wide kernel: d_k 128 only
     assert _call(dims=(2, 2, 8, 8, 128, 1), kernel=N.KERNEL_WIDE) == 6   # and bf16 only
+    assert _call(dims=(2, 2, 8, 193, 64, 0), kernel=N.KERNEL_RESIDENT) == 6  # more keys than it holds
+    assert _call(dims=(2, 2, 129, 8, 64, 0), kernel=N.KERNEL_RESIDENT) == 6  # more than 128 queries
+    assert _call(dims=(2, 2, 8, 8, 64, 1), kernel=N.KERNEL_RESIDENT) == 6    # fp32
+    assert _call(dims=(2, 2, 8, 8, 20, 0), kernel=N.KERNEL_RESIDENT) == 6    # d_k not a multiple of 8
     assert _call(kernel=17) == 6
 
 

@@ -11,12 +11,21 @@ import oracle
 import transformer_scaled_dot_masked_gb300 as attn
 from workloads import WORKLOADS, MASK_CAUSAL, MASK_KEY_PADDING, MASK_NONE, Workload, draw, sample_rows
 
-from gpu_helpers import as_f64, report, run, to_device, tol_for
+from gpu_helpers import as_f64, report, rounding_bound, run, to_device, tol_for
 
 pytestmark = pytest.mark.gpu
 
 K_FLASH, K_SHORT, K_SIMT, K_AUTO = attn.KERNEL_FLASH, attn.KERNEL_SHORT, attn.KERNEL_SIMT, attn.KERNEL_AUTO
-K_WIDE = attn.KERNEL_WIDE
+K_WIDE, K_RESIDENT = attn.KERNEL_WIDE, attn.KERNEL_RESIDENT
+
+
+def resident_fits(m, n, d=64, dtype="bf16"):
+    return dtype == "bf16" and d % 8 == 0 and d <= 64 and m <= 128 and n <= 192
+
+
+def auto_for(m, n):
+    """The tensor-core kernel the library picks for bf16 heads of width <= 64."""
+    return K_RESIDENT if resident_fits(m, n) else (K_SHORT if m <= 128 else K_FLASH)
 
 
 def kernels_for(w: Workload):
@@ -25,6 +34,8 @@ def kernels_for(w: Workload):
         ks.append(K_FLASH)
         if w.m <= 128:
             ks.append(K_SHORT)
+        if resident_fits(w.m, w.n):
+            ks.append(K_RESIDENT)
     return ks
 
 
@@ -84,6 +95,13 @@ EDGE = [
     ("single_query", 2, 2, 1, 500, MASK_KEY_PADDING, (1, 500)),
     ("one_by_one_causal", 1, 1, 1, 1, MASK_CAUSAL, None),
     ("exact_tiles_no_mask", 1, 2, 256, 256, MASK_NONE, None),
+    # the whole-head-resident kernel at the edges of its range: the most keys it holds,
+    # one key box short of that, one query, lengths 0 .. n with causal, 17 keys
+    ("resident_max_keys", 2, 3, 100, 192, MASK_KEY_PADDING, (0, 192)),
+    ("resident_cross_191", 2, 2, 128, 191, MASK_NONE, None),
+    ("resident_single_query", 3, 2, 1, 192, MASK_KEY_PADDING, (0, 192)),
+    ("resident_causal_padding", 3, 2, 128, 128, MASK_CAUSAL | MASK_KEY_PADDING, (0, 128)),
+    ("resident_17_keys", 2, 3, 33, 17, MASK_NONE, None),
 ]
 
 
@@ -129,7 +147,7 @@ def test_worked_example_on_every_kernel():
     columns leave every score unchanged.  bf16 holds 1, -1, 5 exactly."""
     import json, os
     g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "worked_sdpa_2x2.json")))
-    for dtype, kernels in (("bf16", [K_FLASH, K_SHORT, K_SIMT]), ("fp32", [K_SIMT])):
+    for dtype, kernels in (("bf16", [K_FLASH, K_SHORT, K_RESIDENT, K_SIMT]), ("fp32", [K_SIMT])):
         tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
         q = torch.zeros(1, 1, 2, 64, dtype=tdt, device="cuda")
         k, v = torch.zeros_like(q), torch.zeros_like(q)
@@ -313,7 +331,7 @@ def test_head_widths(orc, name, dtype, B, h, m, n, d, mask, lengths):
     w = Workload(name, dtype, B, h, m, n, d, mask, d ** -0.5, 61, lengths)
     auto = attn.select_kernel(B, h, m, n, d, 0 if dtype == "bf16" else 1, mask)
     if dtype == "bf16" and d <= 64:
-        assert auto == (K_SHORT if m <= 128 else K_FLASH)
+        assert auto == auto_for(m, n)
         check_full(orc, w, K_SIMT)
     elif dtype == "bf16" and d == 128:
         assert auto == K_WIDE
@@ -387,9 +405,11 @@ NARROW = [
 @pytest.mark.parametrize("name,B,h,m,n,d,mask,lengths", NARROW, ids=[c[0] for c in NARROW])
 def test_narrow_heads_tensor_cores(orc, name, B, h, m, n, d, mask, lengths):
     w = Workload(name, "bf16", B, h, m, n, d, mask, d ** -0.5, 62, lengths)
-    kern = K_SHORT if m <= 128 else K_FLASH
+    kern = auto_for(m, n)
     assert attn.select_kernel(B, h, m, n, d, 0, mask) == kern
     check_full(orc, w, kern)
+    if kern == K_RESIDENT:
+        check_full(orc, w, K_SHORT)
 
 
 def test_narrow_heads_output_stays_in_bounds():
@@ -403,3 +423,73 @@ def test_narrow_heads_output_stays_in_bounds():
     out = buf[guard:guard + n_out].view(w.B, w.h, w.m, w.d)
     run(inp, K_FLASH, out=out)
     assert (buf[:guard] == -7.0).all() and (buf[guard + n_out:] == -7.0).all()
+
+
+# ---------------------------------------------------------------- whole-head-resident kernel
+@pytest.mark.parametrize("scale", [0.0, 1.0, 0.01, 0.35])
+def test_resident_other_scales(orc, scale):
+    """Scale 1 with d_k = 64 makes most rows peaked (score spread ~8): there the bound
+    adds the output's own half-ulp where |out| >= 4."""
+    w = Workload("resident_scales", "bf16", 2, 2, 128, 128, 64, MASK_CAUSAL, scale, 99)
+    inp = draw(w)
+    got = as_f64(run(inp, K_RESIDENT))
+    ref = orc.attn_fwd(inp.q, inp.k, inp.v, inp.key_lengths, w.mask, w.scale)
+    assert (np.abs(got - ref) - rounding_bound(ref)).max() <= 0, report(got, ref, 1e-2)
+
+
+def test_resident_rows_sum_to_one():
+    """With V = 1 everywhere every output is exactly 1: the row sum adds the same
+    rounded weights the P V product applies."""
+    w = WORKLOADS[4].with_(B=4)
+    inp = draw(w)
+    inp.v[...] = np.uint16(0x3F80)  # bf16 1.0
+    got = as_f64(run(inp, K_RESIDENT))
+    assert np.abs(got - 1.0).max() <= 2.0 ** -8
+
+
+def test_resident_peaked_rows_standard_values(orc):
+    """Rows whose scores jump far above the rest (by ~20 and by > 128 in log2 units),
+    with standard normal values.  The resident kernel takes each row's exact maximum
+    and sums the rounded weights, so the output is a weighted mean with the weights
+    applied: 1e-2, plus the output's own half-ulp where |out| >= 4 (bf16 spacing)."""
+    B, h, m, n, d = 3, 2, 128, 160, 64
+    w = Workload("resident_peaked", "bf16", B, h, m, n, d, MASK_KEY_PADDING, 0.125, 322, (100, 160))
+    inp = draw(w)
+    bits = lambda x: np.uint16(np.array(x, dtype=np.float32).view(np.uint32) >> 16)
+    soft, hard = [5, 77, 127], [6, 100]
+    inp.q[:, :, soft, :32], inp.q[:, :, soft, 32:] = bits(1.0), bits(0.0)
+    inp.q[:, :, hard, :32], inp.q[:, :, hard, 32:] = bits(0.0), bits(1.0)
+    inp.k[:, :, 60, :32], inp.k[:, :, 60, 32:] = bits(4.0), bits(0.0)    # soft rows: q.k = 128
+    inp.k[:, :, 90, :32], inp.k[:, :, 90, 32:] = bits(0.0), bits(32.0)   # hard rows: q.k = 1024
+    ref = orc.attn_fwd(inp.q, inp.k, inp.v, inp.key_lengths, w.mask, w.scale)
+    got = as_f64(run(inp, K_RESIDENT))
+    assert np.isfinite(got).all()
+    assert (np.abs(got - ref) - rounding_bound(ref)).max() <= 0, report(got, ref, 1e-2)
+
+
+@pytest.mark.parametrize("mask", [MASK_KEY_PADDING, MASK_CAUSAL | MASK_KEY_PADDING], ids=["padding", "causal_padding"])
+def test_resident_lse_and_bounds(orc, mask):
+    """The log-sum-exp output of the resident kernel (rows with no allowed key: -inf),
+    and that it writes exactly its output (guard regions on both sides untouched)."""
+    B, h, m = 3, 3, 100 if mask == MASK_KEY_PADDING else 128
+    n = 150 if mask == MASK_KEY_PADDING else m
+    w = Workload("resident_lse", "bf16", B, h, m, n, 64, mask, 0.125, 66, (0, n))
+    inp = draw(w)
+    inp.key_lengths[0] = 0
+    q, k, v = (to_device(x, "bf16") for x in (inp.q, inp.k, inp.v))
+    lens = torch.from_numpy(inp.key_lengths).cuda()
+    assert attn.select_kernel(B, h, m, n, 64, 0, mask) == K_RESIDENT
+    out, lse = attn.attn_fwd_lse(q, k, v, lens, w.mask, w.scale)
+    torch.cuda.synchronize()
+    ref = orc.attn_lse(inp.q, inp.k, inp.key_lengths, w.mask, w.scale)
+    got = lse.double().cpu().numpy()
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isfinite(got), fin)
+    assert np.abs(got[fin] - ref[fin]).max() <= 2e-3
+    n_out = w.B * w.h * w.m * w.d
+    guard = 4096
+    buf = torch.full((n_out + 2 * guard,), -7.0, dtype=torch.bfloat16, device="cuda")
+    o2 = buf[guard:guard + n_out].view(w.B, w.h, w.m, w.d)
+    run(inp, K_RESIDENT, out=o2)
+    assert (buf[:guard] == -7.0).all() and (buf[guard + n_out:] == -7.0).all()
+    np.testing.assert_array_equal(as_f64(o2), as_f64(out))

@@ -43,10 +43,13 @@ CASES = [
     ("pair_mode_w200_causal_padding", "bf16", 2, 2, 1000, MASK_CAUSAL | MASK_KEY_PADDING, 200, (100, 1000)),
     ("pair_mode_long_w300", "bf16", 1, 4, 4096, 0, 300, None),
     ("pair_mode_covering_window", "bf16", 2, 2, 260, MASK_CAUSAL, 5000, None),
-    ("split_mode_w10", "bf16", 3, 3, 100, MASK_KEY_PADDING, 10, (0, 100)),
-    ("split_mode_w64_causal", "bf16", 4, 2, 128, MASK_CAUSAL, 64, None),
+    ("resident_w10", "bf16", 3, 3, 100, MASK_KEY_PADDING, 10, (0, 100)),
+    ("resident_w64_causal", "bf16", 4, 2, 128, MASK_CAUSAL, 64, None),
+    ("resident_w0_causal_padding", "bf16", 3, 2, 128, MASK_CAUSAL | MASK_KEY_PADDING, 0, (0, 128)),
+    ("resident_w40_m33", "bf16", 2, 3, 33, 0, 40, None),
     ("fp32_w7", "fp32", 2, 2, 150, MASK_KEY_PADDING, 7, (1, 150)),
     ("narrow_heads_w3", "bf16_d32", 2, 2, 90, MASK_CAUSAL, 3, None),
+    ("narrow_heads_pair_mode_w17", "bf16_d16", 2, 2, 300, MASK_KEY_PADDING, 17, (0, 300)),
     ("wide_heads_w0", "bf16_d128", 2, 2, 300, 0, 0, None),
     ("wide_heads_w127_causal", "bf16_d128", 2, 2, 700, MASK_CAUSAL, 127, None),
     ("wide_heads_w128_padding", "bf16_d128", 3, 2, 700, MASK_KEY_PADDING, 128, (0, 700)),

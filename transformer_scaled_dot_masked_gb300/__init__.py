@@ -16,11 +16,11 @@ from __future__ import annotations
 from typing import Optional
 
 from . import _native
-from ._native import (AttnError, KERNEL_AUTO, KERNEL_FLASH, KERNEL_SHORT, KERNEL_SIMT, KERNEL_WIDE, MASK_CAUSAL,
+from ._native import (AttnError, KERNEL_AUTO, KERNEL_FLASH, KERNEL_SHORT, KERNEL_SIMT, KERNEL_WIDE, KERNEL_RESIDENT, MASK_CAUSAL,
                       MASK_KEY_PADDING, MASK_NONE, MASK_WINDOW, DTYPE_BF16, DTYPE_FP32, SCALE_DEFAULT)
 
 __all__ = ["attn_fwd", "attn_fwd_host", "host_workspace_size", "attn_mha_fwd", "mha_workspace_size", "attn_fwd_window", "attn_fwd_lse", "MASK_WINDOW", "attn_bwd", "bwd_workspace_size", "attn_decode", "decode_workspace_size", "AttnError", "select_kernel", "device_status", "make_workspace", "workspace_size", "MASK_NONE", "MASK_KEY_PADDING",
-           "MASK_CAUSAL", "KERNEL_AUTO", "KERNEL_FLASH", "KERNEL_SHORT", "KERNEL_SIMT", "KERNEL_WIDE"]
+           "MASK_CAUSAL", "KERNEL_AUTO", "KERNEL_FLASH", "KERNEL_SHORT", "KERNEL_SIMT", "KERNEL_WIDE", "KERNEL_RESIDENT"]
 
 
 def _dtype_code(t) -> int:

@@ -27,9 +27,9 @@ MASK_NONE, MASK_KEY_PADDING, MASK_CAUSAL, MASK_WINDOW = 0, 1, 2, 4
 DTYPE_BF16, DTYPE_FP32 = 0, 1
 # ATTN_SCALE_DEFAULT: the library substitutes the formula's scale, 1/sqrt(d_k)
 SCALE_DEFAULT = -1.0
-KERNEL_AUTO, KERNEL_FLASH, KERNEL_SHORT, KERNEL_SIMT, KERNEL_WIDE = 0, 1, 2, 3, 4
+KERNEL_AUTO, KERNEL_FLASH, KERNEL_SHORT, KERNEL_SIMT, KERNEL_WIDE, KERNEL_RESIDENT = 0, 1, 2, 3, 4, 5
 KERNEL_NAMES = {KERNEL_AUTO: "auto", KERNEL_FLASH: "flash", KERNEL_SHORT: "short", KERNEL_SIMT: "simt",
-                KERNEL_WIDE: "wide"}
+                KERNEL_WIDE: "wide", KERNEL_RESIDENT: "resident"}
 
 
 class MhaDims(ctypes.Structure):
@@ -59,6 +59,8 @@ lib.attn_fwd_host_workspace_size.restype = ctypes.c_size_t
 lib.attn_fwd_host.argtypes = lib.attn_fwd.argtypes[:-1] + [_vp, ctypes.c_size_t, _vp]
 lib.attn_fwd_host.restype = ctypes.c_int
 lib.attn_fwd_noalloc.restype = ctypes.c_int
+lib.attn_test_withheld_arrival.argtypes = lib.attn_fwd.argtypes[:-1] + [ctypes.c_uint64, _vp]
+lib.attn_test_withheld_arrival.restype = ctypes.c_int
 lib.attn_fwd_lse.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_float, _vp, _vp,
                              ctypes.POINTER(AttnDims), _vp]
 lib.attn_fwd_lse.restype = ctypes.c_int
@@ -142,6 +144,13 @@ def fwd_host_raw(q_ptr, k_ptr, v_ptr, lens_ptr, mask_kind, scale, out_ptr, dims:
     """attn_fwd_host with integer host pointers (device workspace); returns the status code."""
     return lib.attn_fwd_host(q_ptr, k_ptr, v_ptr, lens_ptr, int(mask_kind), float(scale), out_ptr,
                              ctypes.byref(dims), ws_ptr, int(ws_bytes), stream_ptr)
+
+
+def test_withheld_arrival_raw(q_ptr, k_ptr, v_ptr, lens_ptr, mask_kind, scale, out_ptr, dims: AttnDims,
+                              wait_ns: int, stream_ptr) -> int:
+    """attn_test_withheld_arrival (failure-detection test hook); returns the status code."""
+    return lib.attn_test_withheld_arrival(q_ptr, k_ptr, v_ptr, lens_ptr, int(mask_kind), float(scale), out_ptr,
+                                          ctypes.byref(dims), int(wait_ns), stream_ptr)
 
 
 def fwd_noalloc_raw(q_ptr, k_ptr, v_ptr, lens_ptr, mask_kind, scale, out_ptr, dims: AttnDims,

@@ -23,11 +23,13 @@ bool overlaps(const void *a, uint64_t abytes, const void *b, uint64_t bbytes)
 // heads run zero-padded to 64 inside the kernel).
 bool tensor_core_head(const attn_dims &d) { return d.dtype == ATTN_BF16 && d.d_k % 8 == 0 && d.d_k <= 64; }
 
-// Which kernel AUTO picks: tensor cores for tensor_core_head (two heads per CTA tile
-// when a head has at most 128 queries, two query tiles of one head otherwise); CUDA
+// Which kernel AUTO picks: tensor cores for tensor_core_head (one head per CTA, whole
+// head resident, when a head has at most 128 queries and 192 keys; two heads per CTA
+// tile when it has at most 128 queries; two query tiles of one head otherwise); CUDA
 // cores for fp32 and for other bf16 head widths.
 int auto_kernel(const attn_dims &d)
 {
+    if (tensor_core_head(d) && attn::resident_fits(d.m, d.n, d.d_k)) return ATTN_KERNEL_RESIDENT;
     if (tensor_core_head(d)) return d.m <= 128 ? ATTN_KERNEL_SHORT : ATTN_KERNEL_FLASH;
     if (d.dtype == ATTN_BF16 && d.d_k == 128) return ATTN_KERNEL_WIDE;
     return ATTN_KERNEL_SIMT;
@@ -124,6 +126,11 @@ attn_status run(const void *Q, const void *K, const void *V, const int32_t *key_
     case ATTN_KERNEL_SHORT:
         if (!tensor_core_head(d) || p.m > 128) return ATTN_ERR_UNSUPPORTED;
         e = attn::launch_flash(p, /*pair_mode=*/false, tile_counter, s);
+        break;
+    case ATTN_KERNEL_RESIDENT:
+        if (!tensor_core_head(d) || !attn::resident_fits(d.m, d.n, d.d_k)) return ATTN_ERR_UNSUPPORTED;
+        p.overlap_launch = true; // every access of the kernel follows its dependency wait
+        e = attn::launch_resident(p, s);
         break;
     default:
         return ATTN_ERR_UNSUPPORTED;
@@ -683,6 +690,35 @@ attn_status attn_fwd_host(const void *Q, const void *K, const void *V, const int
     return ok && joined ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+attn_status attn_test_withheld_arrival(const void *Q, const void *K, const void *V, const int32_t *key_lengths,
+                                       int mask_kind, float scale, void *out, const attn_dims *dims,
+                                       uint64_t wait_ns, void *stream)
+{
+    const attn_status st = validate(Q, K, V, key_lengths, mask_kind, scale, out, dims);
+    if (st != ATTN_OK) return st;
+    const attn_dims &d = *dims;
+    if (!tensor_core_head(d) || !attn::resident_fits(d.m, d.n, d.d_k)) return ATTN_ERR_UNSUPPORTED;
+    if (wait_ns < 100000ull || wait_ns > 2000000000ull) return ATTN_ERR_VALUE;
+    attn::Problem p;
+    p.q = Q;
+    p.k = K;
+    p.v = V;
+    p.key_lengths = (mask_kind & ATTN_MASK_KEY_PADDING) ? key_lengths : nullptr;
+    p.out = out;
+    p.lse = nullptr;
+    p.B = d.B;
+    p.h = d.h;
+    p.m = d.m;
+    p.n = d.n;
+    p.d = d.d_k;
+    p.mask_kind = mask_kind;
+    p.scale = resolve_scale(scale, d.d_k);
+    p.bf16 = true;
+    attn::ResidentTestHook hook{wait_ns, 1};
+    return attn::launch_resident(p, static_cast<cudaStream_t>(stream), &hook) == cudaSuccess ? ATTN_OK
+                                                                                                 : ATTN_ERR_CUDA;
+}
+
 int attn_select_kernel(const attn_dims *dims, int mask_kind)
 {
     if (validate_dims(dims, mask_kind, 1.0f) != ATTN_OK) return ATTN_KERNEL_AUTO;
@@ -702,6 +738,13 @@ attn_status attn_device_status(void *stream, int32_t *info)
     uint32_t wcode = 0, wwhere = 0;
     if (attn::wide_status_read_and_clear(static_cast<cudaStream_t>(stream), &wcode, &wwhere) != cudaSuccess)
         return ATTN_ERR_CUDA;
+    uint32_t rcode = 0, rwhere = 0;
+    if (attn::resident_status_read_and_clear(static_cast<cudaStream_t>(stream), &rcode, &rwhere) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    if (code == 0 && rcode != 0) {
+        code = rcode;
+        where = 400 + rwhere; // resident-kernel wait sites are reported as 400 + site
+    }
     if (code == 0 && wcode != 0) {
         code = wcode;
         where = 300 + wwhere; // wide-head wait sites are reported as 300 + site

@@ -790,6 +790,11 @@ attn_flash_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         fence_mbarrier_init();
     }
     __syncwarp();
+    // Set-up above overlaps the previous kernel's tail when launched as its programmatic
+    // dependent.  Nothing below may read what that kernel writes before it completes,
+    // and TMEM is allocated only after it has completed: a kernel that let this one
+    // launch early may still have CTAs waiting for columns.
+    grid_dependency_wait();
     if (warp == kMmaWarp) {
         tmem_alloc(&sm.tmem_base, kTmemCols);
         tmem_relinquish();
@@ -798,9 +803,6 @@ attn_flash_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
-    // set-up above overlaps the previous kernel's tail when launched as its programmatic
-    // dependent; nothing below may read what that kernel writes before it completes
-    grid_dependency_wait();
 
     // The two register regions never rejoin: each branch ends with its own
     // CTA-wide barrier (every thread arrives exactly once) and returns.

@@ -163,6 +163,11 @@ attn_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
         fence_mbarrier_init();
     }
     __syncwarp();
+    // Set-up above overlaps the previous kernel's tail when launched as its programmatic
+    // dependent.  Nothing below may read what that kernel writes before it completes,
+    // and TMEM is allocated only after it has completed: a kernel that let this one
+    // launch early may still have CTAs waiting for columns.
+    grid_dependency_wait();
     if (warp == 1) {
         tmem_alloc(&sm.tmem_base, kTmemCols);
         tmem_relinquish();
@@ -171,9 +176,6 @@ attn_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
-    // set-up above overlaps the previous kernel's tail when launched as its programmatic
-    // dependent; nothing below may read what that kernel writes before it completes
-    grid_dependency_wait();
 
     if (warp == 0) {
         if (threadIdx.x == 0) {

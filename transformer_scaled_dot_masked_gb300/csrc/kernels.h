@@ -97,6 +97,21 @@ cudaError_t proj_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint
 // Device status word of the flash kernel (bounded waits that gave up).
 cudaError_t flash_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint32_t *info);
 
+// Whole-head-resident tcgen05/TMA kernel for short sequences (bf16, d a multiple of 8
+// up to 64, m <= 128, n <= kResidentMaxKeys): one head per CTA, exact two-pass softmax
+// per row.  Launched as a programmatic dependent of the previous kernel when
+// p.overlap_launch is set (everything it reads or writes follows the dependency wait).
+constexpr int kResidentMaxKeys = 192;
+bool resident_fits(int m, int n, int d);
+// Test hook of the bounded waits: a short wait limit, and the last thread withholding
+// its arrival on the weights barrier, so that the MMA issuer's wait runs out.
+struct ResidentTestHook {
+    uint64_t wait_ns;
+    int withhold_p_arrival;
+};
+cudaError_t launch_resident(const Problem &p, cudaStream_t stream, const ResidentTestHook *hook = nullptr);
+cudaError_t resident_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint32_t *info);
+
 // tcgen05/TMA kernel for bf16 heads of width 128 (one 128-row query tile per CTA).
 cudaError_t launch_wide(const Problem &p, cudaStream_t stream);
 cudaError_t wide_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint32_t *info);
