@@ -502,6 +502,31 @@ def cpu_oracle_sample(w, inp, target_s, seed=3):
                       f"{flops / 1e9:.1f} GFLOP useful)", "seconds": el}, (orc, qd, kd, vd)
 
 
+def cpu_per_config(all_cores_c5):
+    """The oracle on workloads 1-4 in full, on one core and on all of them, and on
+    workload 5's row sample on all cores: useful TFLOPS and seconds per run."""
+    import oracle
+    orc = oracle.load()
+    cores = orc.num_threads()
+    res = {"nproc": os.cpu_count(), "threads_all": cores}
+    for cfg in (1, 2, 3, 4):
+        w = WORKLOADS[cfg]
+        inp = draw(w)
+        flops = useful_flops(w, inp.key_lengths)
+        entry = {}
+        for label, threads in (("one_core", 1), ("all_cores", cores)):
+            orc.set_num_threads(threads)
+            t0 = time.perf_counter()
+            orc.attn_fwd(inp.q, inp.k, inp.v, inp.key_lengths, w.mask, w.scale)
+            el = time.perf_counter() - t0
+            entry[label] = {"tflops_useful": flops / el / 1e12, "seconds": el, "threads": threads}
+        res[w.name] = entry
+    orc.set_num_threads(cores)
+    res[WORKLOADS[5].name] = {"all_cores": all_cores_c5,
+                              "one_core": "not timed (all cores on a row sample take ~15 s)"}
+    return res
+
+
 def run_reference(args, w):
     """--impl reference: the fp64 CPU oracle, one bounded row sample per step."""
     rank = int(os.environ.get("RANK", "0"))
@@ -657,7 +682,9 @@ def main():
         result["mha"] = mha_workload(torch, attn, device, peak_tf)
         if rank == 0:
             cb, _ = cpu_oracle_sample(w, inp, args.cpu_seconds)
-            cb.pop("seconds", None)
+            seconds = cb.pop("seconds", None)
+            cb["per_config"] = cpu_per_config({"tflops_useful": cb["value"], "seconds": seconds,
+                                               "threads": cb["cores"], "sample": cb["sample"]})
             result["cpu_baseline"] = cb
 
     if rank == 0:

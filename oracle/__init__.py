@@ -83,6 +83,8 @@ class Oracle:
         lib.oracle_attn_bwd.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+        lib.oracle_set_num_threads.restype = None
         self._lib = lib
 
     # -- input widening ---------------------------------------------------
@@ -105,6 +107,10 @@ class Oracle:
 
     def num_threads(self) -> int:
         return int(self._lib.oracle_num_threads())
+
+    def set_num_threads(self, n: int) -> None:
+        """Threads the row loops use from now on (timing only; results do not depend on it)."""
+        self._lib.oracle_set_num_threads(int(n))
 
     @staticmethod
     def _dims(q, k, v):

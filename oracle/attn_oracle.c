@@ -72,6 +72,16 @@ int oracle_num_threads(void)
 #endif
 }
 
+/* Threads the row loops use from now on (for timing the oracle on one core or all). */
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* Half-width of the restricted-attention window for the current call (set by the
  * _w entry points for the duration of one call; 0 otherwise). */
 static int64_t g_window = 0;
