@@ -329,7 +329,8 @@ size_t attn_bwd_workspace_size(const attn_dims *dims);
  *                  the same time on the GPU need different workspaces
  *   dims, stream   as for the forward
  *
- * Supported: bf16 with d_k == 64 (ATTN_ERR_DTYPE otherwise).  All tensors
+ * Supported: bf16 with d_k a multiple of 8 up to 64 (narrower heads run zero-padded
+ * to 64 inside the kernels; ATTN_ERR_DTYPE otherwise).  All tensors
  * 16-byte aligned, lse 4-byte aligned (ATTN_ERR_ALIGN).  dQ, dK, dV and the
  * workspace must not overlap each other or any input (ATTN_ERR_ALIAS).  A
  * workspace that is too small is ATTN_ERR_SHAPE.  Other errors as attn_fwd.
@@ -355,11 +356,12 @@ size_t attn_decode_workspace_size(const attn_dims *dims);
  * exactly attn_fwd with ATTN_MASK_KEY_PADDING and key_lengths = cache_lengths
  * (a row with no cached key is 0).
  *
- *   Q              device bf16 [B][h][m][64], 1 <= m <= 8
- *   K, V           device bf16 [B][h][n][64]: the caches, n = their capacity
+ *   Q              device bf16 [B][h][m][d_k], 1 <= m <= 8, d_k in {16, 32, 64, 128} (the
+ *                  head widths of the model-variant table)
+ *   K, V           device bf16 [B][h][n][d_k]: the caches, n = their capacity
  *   cache_lengths  device int32 [B], clamped to [0, n]; NULL: every row holds n keys
  *   scale          as for attn_fwd
- *   out            device bf16 [B][h][m][64]
+ *   out            device bf16 [B][h][m][d_k]
  *   lse            NULL, or device float [B][h][m]: each row's log-sum-exp (natural log)
  *   workspace      attn_decode_workspace_size(dims) bytes, 16-byte aligned, any
  *                  contents (may be NULL when that size is 0); calls that may run
@@ -368,7 +370,7 @@ size_t attn_decode_workspace_size(const attn_dims *dims);
  * The keys of each (batch, head) are split over several CTAs on the CUDA cores
  * (the work is memory-bound: each cached row is read once per call), then one
  * pass merges the splits.  Errors as attn_fwd, plus: dtype other than bf16 or
- * d_k != 64 (ATTN_ERR_DTYPE), m > 8 (ATTN_ERR_SHAPE), workspace NULL or too small
+ * another d_k (ATTN_ERR_DTYPE), m > 8 (ATTN_ERR_SHAPE), workspace NULL or too small
  * when one is needed (ATTN_ERR_NULL / ATTN_ERR_SHAPE), lse or the workspace
  * unaligned (ATTN_ERR_ALIGN) or overlapping a tensor (ATTN_ERR_ALIAS).
  */

@@ -83,6 +83,45 @@ def test_bwd_matches_oracle(orc, name, B, h, m, n, mask, lengths):
     assert np.abs(got_lse[live] - ref_lse[live]).max() <= 1e-3
 
 
+NARROW_BWD = [
+    # heads narrower than 64 (the model-variant table's d_k = 32 and 16, and other
+    # multiples of 8): zero-padded to 64 inside the kernels, only d_k columns written
+    ("d16_causal_ragged", 2, 2, 300, 300, 16, MASK_CAUSAL, None),
+    ("d32_cross_padding", 3, 2, 200, 333, 32, MASK_KEY_PADDING, (0, 333)),
+    ("d8_padding_causal", 2, 3, 130, 130, 8, MASK_KEY_PADDING | MASK_CAUSAL, (1, 130)),
+    ("d48_short_heads", 4, 2, 100, 150, 48, MASK_KEY_PADDING, (0, 150)),
+]
+
+
+@pytest.mark.parametrize("name,B,h,m,n,d,mask,lengths", NARROW_BWD, ids=[c[0] for c in NARROW_BWD])
+def test_bwd_narrow_heads(orc, name, B, h, m, n, d, mask, lengths):
+    """Gradients of narrower heads against the oracle, written exactly into their
+    [B, h, len, d_k] outputs (guard regions on both sides of each stay untouched)."""
+    w = Workload(name, "bf16", B, h, m, n, d, mask, d ** -0.5, 78, lengths)
+    inp = draw(w)
+    dout = draw_dout(w)
+    q, k, v = (to_device(x, w.dtype) for x in (inp.q, inp.k, inp.v))
+    do = to_device(dout, w.dtype)
+    lens = torch.from_numpy(inp.key_lengths).cuda()
+    out, lse = attn.attn_fwd_lse(q, k, v, lens, w.mask, w.scale)
+    guard = 4096
+    bufs, grads = [], []
+    for like in (q, k, v):
+        buf = torch.full((like.numel() + 2 * guard,), -7.0, dtype=torch.bfloat16, device="cuda")
+        bufs.append(buf)
+        grads.append(buf[guard:guard + like.numel()].view(like.shape))
+    attn.attn_bwd(q, k, v, out, do, lse, lens, w.mask, w.scale, dq=grads[0], dk=grads[1], dv=grads[2])
+    torch.cuda.synchronize()
+    st, info = attn.device_status()
+    assert st == 0, f"device status {st} (info {info})"
+    for buf in bufs:
+        assert (buf[:guard] == -7.0).all() and (buf[-guard:] == -7.0).all()
+    rq, rk, rv = orc.attn_bwd(inp.q, inp.k, inp.v, dout, inp.key_lengths, w.mask, w.scale)
+    check_grad("dV", grads[2], rv)
+    check_grad("dK", grads[1], rk)
+    check_grad("dQ", grads[0], rq)
+
+
 @pytest.mark.parametrize("cfg", [2, 3, 4])
 def test_bwd_workloads(orc, cfg):
     w = WORKLOADS[cfg]

@@ -91,3 +91,32 @@ def test_decode_matches_forward_kernels():
     fwd = attn.attn_fwd(q, k, v, torch.from_numpy(inp.key_lengths).cuda(), MASK_KEY_PADDING, w.scale)
     torch.cuda.synchronize()
     assert (out.float() - fwd.float()).abs().max().item() <= 1.6e-2
+
+
+WIDTH_CASES = [
+    # the model-variant table's other head widths: d_k = 16 (h 32), 32 (h 16), 128 (h 4);
+    # m from 1 to 8, ragged caches, one split and many
+    ("d16_one_query", 16, 8, 4, 1, 700, (0, 700)),
+    ("d16_eight_queries", 16, 2, 3, 8, 3000, (1, 3000)),
+    ("d32_two_queries", 32, 4, 4, 2, 1500, (0, 1500)),
+    ("d32_many_heads_one_split", 32, 64, 16, 1, 64, (1, 64)),
+    ("d128_one_query_long", 128, 2, 2, 1, 9000, (8000, 9000)),
+    ("d128_eight_queries", 128, 3, 2, 8, 600, (0, 600)),
+    ("d128_five_queries", 128, 2, 2, 5, 333, (300, 333)),
+]
+
+
+@pytest.mark.parametrize("name,d,B,h,m,n,lengths", WIDTH_CASES, ids=[c[0] for c in WIDTH_CASES])
+def test_decode_other_head_widths(orc, name, d, B, h, m, n, lengths):
+    w = Workload(name, "bf16", B, h, m, n, d, MASK_KEY_PADDING, d ** -0.5, 34, lengths)
+    inp = draw(w)
+    inp.key_lengths[0] = lengths[0]
+    out, lse = run_decode(inp, lse=True)
+    got = as_f64(out)
+    ref = orc.attn_fwd(inp.q, inp.k, inp.v, inp.key_lengths, MASK_KEY_PADDING, w.scale)
+    assert np.abs(got - ref).max() <= 1e-2, report(got, ref, 1e-2)
+    ref_lse = orc.attn_lse(inp.q, inp.k, inp.key_lengths, MASK_KEY_PADDING, w.scale)
+    g = lse.cpu().numpy().astype(np.float64)
+    live = np.isfinite(ref_lse)
+    assert (g[~live] == -np.inf).all()
+    assert np.abs(g[live] - ref_lse[live]).max() <= 1e-3

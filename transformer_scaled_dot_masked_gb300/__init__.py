@@ -220,7 +220,8 @@ def bwd_workspace_size(B, h, m, n, d, dtype: int = DTYPE_BF16) -> int:
 
 def attn_bwd(q, k, v, out, dout, lse, key_lengths=None, mask_kind: int = MASK_NONE,
              scale: Optional[float] = None, dq=None, dk=None, dv=None, workspace=None, stream=None):
-    """Gradients (dq, dk, dv) of sum(dout * out) for out = attention(q, k, v), bf16 with d_k = 64.
+    """Gradients (dq, dk, dv) of sum(dout * out) for out = attention(q, k, v), bf16 with d_k a
+    multiple of 8 up to 64.
 
     out and lse come from ``attn_fwd_lse`` on the same inputs, mask and scale.
     workspace: optional CUDA uint8 buffer of at least ``bwd_workspace_size(...)`` bytes
@@ -242,7 +243,7 @@ def attn_bwd(q, k, v, out, dout, lse, key_lengths=None, mask_kind: int = MASK_NO
     dims = _native.make_dims(B, h, m, n, d, _dtype_code(q))
     need = _native.bwd_workspace_size(dims)
     if need == 0:
-        raise AttnError(3)  # ATTN_ERR_DTYPE: the backward runs bf16 with d_k = 64
+        raise AttnError(3)  # ATTN_ERR_DTYPE: the backward runs bf16 with d_k a multiple of 8 up to 64
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     if not workspace.is_cuda or not workspace.is_contiguous():
@@ -264,9 +265,10 @@ def decode_workspace_size(B, h, m, n, d=64, dtype: int = DTYPE_BF16) -> int:
 
 def attn_decode(q, k_cache, v_cache, cache_lengths=None, scale: Optional[float] = None, out=None, lse=None,
                 workspace=None, stream=None):
-    """m (1..8) new query rows per (batch, head) against cached keys/values (bf16, d_k = 64).
+    """m (1..8) new query rows per (batch, head) against cached keys/values (bf16, d_k 16, 32,
+    64 or 128).
 
-    q: [B, h, m, 64]; k_cache, v_cache: [B, h, n, 64] (n = capacity); cache_lengths: int32 [B]
+    q: [B, h, m, d_k]; k_cache, v_cache: [B, h, n, d_k] (n = capacity); cache_lengths: int32 [B]
     CUDA tensor of valid cached rows per batch entry (None: all n).  Same result as
     ``attn_fwd`` with MASK_KEY_PADDING.  lse: optional float32 [B, h, m] output.
     """

@@ -269,7 +269,7 @@ attn_status attn_fwd_lse(const void *Q, const void *K, const void *V, const int3
 
 size_t attn_bwd_workspace_size(const attn_dims *dims)
 {
-    if (validate_dims(dims, 0, 1.0f) != ATTN_OK || dims->dtype != ATTN_BF16 || dims->d_k != 64) return 0;
+    if (validate_dims(dims, 0, 1.0f) != ATTN_OK || !tensor_core_head(*dims)) return 0;
     return attn::bwd_workspace_bytes(dims->B, dims->h, dims->m);
 }
 
@@ -284,7 +284,7 @@ attn_status attn_bwd(const void *Q, const void *K, const void *V, const void *ou
     const attn_status st = validate(Q, K, V, key_lengths, mask_kind, scale, dQ, dims);
     if (st != ATTN_OK) return st;
     const attn_dims &d = *dims;
-    if (d.dtype != ATTN_BF16 || d.d_k != 64) return ATTN_ERR_DTYPE;
+    if (!tensor_core_head(d)) return ATTN_ERR_DTYPE; // bf16, d_k a multiple of 8 up to 64
     if (!aligned(out, 16) || !aligned(dout, 16) || !aligned(dK, 16) || !aligned(dV, 16) || !aligned(lse, 4) ||
         !aligned(workspace, 256))
         return ATTN_ERR_ALIGN;
@@ -318,6 +318,7 @@ attn_status attn_bwd(const void *Q, const void *K, const void *V, const void *ou
     p.dq = dQ;
     p.dk = dK;
     p.dv = dV;
+    p.d = d.d_k;
     p.workspace = workspace;
     p.B = d.B;
     p.h = d.h;
@@ -343,7 +344,7 @@ attn_status validate_decode_dims(const attn_dims *dims)
     if (dims == nullptr) return ATTN_ERR_NULL;
     const attn_status st = validate_dims(dims, ATTN_MASK_KEY_PADDING, 1.0f);
     if (st != ATTN_OK) return st;
-    if (dims->dtype != ATTN_BF16 || dims->d_k != 64) return ATTN_ERR_DTYPE;
+    if (dims->dtype != ATTN_BF16 || !attn::decode_width_supported(dims->d_k)) return ATTN_ERR_DTYPE;
     if (dims->m > 8) return ATTN_ERR_SHAPE;
     return ATTN_OK;
 }
@@ -354,7 +355,7 @@ size_t attn_decode_workspace_size(const attn_dims *dims)
     if (validate_decode_dims(dims) != ATTN_OK) return 0;
     const int sms = current_sms();
     if (sms <= 0) return 0;
-    return attn::decode_workspace_bytes(dims->B, dims->h, dims->m, dims->n, sms);
+    return attn::decode_workspace_bytes(dims->B, dims->h, dims->m, dims->n, dims->d_k, sms);
 }
 
 attn_status attn_decode(const void *Q, const void *K, const void *V, const int32_t *cache_lengths, float scale,
@@ -367,8 +368,8 @@ attn_status attn_decode(const void *Q, const void *K, const void *V, const int32
     st = validate(Q, K, V, cache_lengths, mask, scale, out, dims);
     if (st != ATTN_OK) return st;
     const attn_dims &d = *dims;
-    const uint64_t qbytes = static_cast<uint64_t>(d.B) * d.h * d.m * 64 * 2;
-    const uint64_t kbytes = static_cast<uint64_t>(d.B) * d.h * d.n * 64 * 2;
+    const uint64_t qbytes = static_cast<uint64_t>(d.B) * d.h * d.m * d.d_k * 2;
+    const uint64_t kbytes = static_cast<uint64_t>(d.B) * d.h * d.n * d.d_k * 2;
     const uint64_t lbytes = static_cast<uint64_t>(d.B) * d.h * d.m * 4;
     if (lse != nullptr) {
         if (!aligned(lse, 4)) return ATTN_ERR_ALIGN;
@@ -379,7 +380,7 @@ attn_status attn_decode(const void *Q, const void *K, const void *V, const int32
     }
     const int sms = current_sms();
     if (sms <= 0) return ATTN_ERR_CUDA;
-    const size_t need = attn::decode_workspace_bytes(d.B, d.h, d.m, d.n, sms);
+    const size_t need = attn::decode_workspace_bytes(d.B, d.h, d.m, d.n, d.d_k, sms);
     if (need > 0) {
         if (workspace == nullptr) return ATTN_ERR_NULL;
         if (workspace_bytes < need) return ATTN_ERR_SHAPE;
@@ -400,7 +401,7 @@ attn_status attn_decode(const void *Q, const void *K, const void *V, const int32
     p.h = d.h;
     p.m = d.m;
     p.n = d.n;
-    p.d = 64;
+    p.d = d.d_k;
     p.mask_kind = mask;
     p.scale = resolve_scale(scale, d.d_k);
     p.bf16 = true;

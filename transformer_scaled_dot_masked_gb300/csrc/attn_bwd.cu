@@ -104,9 +104,10 @@ struct alignas(1024) BwdSmem {
 struct BwdParams {
     const float2 *ld;        // [BH][m_pad] (lse * log2 e, D); padding rows (+inf, 0)
     float *dq_acc;           // [BH][m][64] fp32, zeroed by the pre kernel
-    __nv_bfloat16 *dk, *dv;  // [BH][n][64]
+    __nv_bfloat16 *dk, *dv;  // [BH][n][d]
     const int32_t *key_lengths;
     int BH, h, m, n, m_pad, mask_kind, q_tiles;
+    int d;                   // head width in memory (a multiple of 8, <= 64); the tiles are 64 wide
     float scale_log2;        // scale * log2 e
     float scale;
 };
@@ -442,10 +443,11 @@ __device__ __forceinline__ void compute_role(BwdSmem &sm, const BwdParams &p, co
     reg_fence32(r);
     if (k < p.n) {
         const float f = g < 2 ? 1.f : p.scale;
-        uint4 *dst = reinterpret_cast<uint4 *>((g < 2 ? p.dv : p.dk) + (static_cast<size_t>(bh) * p.n + k) * kD +
+        uint4 *dst = reinterpret_cast<uint4 *>((g < 2 ? p.dv : p.dk) + (static_cast<size_t>(bh) * p.n + k) * p.d +
                                                32 * (g % 2));
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
+            if (32 * (g % 2) + 8 * c >= p.d) break; // narrower heads: only the first d columns exist
             uint4 a;
             a.x = pack_bf16x2(__uint_as_float(r[8 * c + 0]) * f, __uint_as_float(r[8 * c + 1]) * f);
             a.y = pack_bf16x2(__uint_as_float(r[8 * c + 2]) * f, __uint_as_float(r[8 * c + 3]) * f);
@@ -477,10 +479,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (steps <= 0) {
         // no query sees any key of this tile: its gradients are 0
         const uint4 z = make_uint4(0, 0, 0, 0);
-        for (int r = threadIdx.x; r < kBM * (kD / 8); r += blockDim.x) {
-            const int kk = key0 + r / (kD / 8);
+        const int row8 = p.d / 8; // 16-byte chunks per row
+        for (int r = threadIdx.x; r < kBM * row8; r += blockDim.x) {
+            const int kk = key0 + r / row8;
             if (kk >= p.n) continue;
-            const size_t off = (static_cast<size_t>(bh) * p.n + kk) * kD / 8 + r % (kD / 8);
+            const size_t off = (static_cast<size_t>(bh) * p.n + kk) * row8 + r % row8;
             reinterpret_cast<uint4 *>(p.dv)[off] = z;
             reinterpret_cast<uint4 *>(p.dk)[off] = z;
         }
@@ -541,10 +544,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 }
 
 // D_i = sum_c dO_ic O_ic and (lse_i log2 e, D_i) per query row, padded to whole
-// tiles; zeroes the dQ accumulator.  One thread per (head, padded row).
+// tiles; zeroes the dQ accumulator (64 columns per row whatever the head width).  One
+// thread per (head, padded row); rows of out and dout hold d elements.
 __global__ void attn_bwd_pre_kernel(const __nv_bfloat16 *__restrict__ out, const __nv_bfloat16 *__restrict__ dout,
                                     const float *__restrict__ lse, float2 *__restrict__ ld,
-                                    float *__restrict__ dq_acc, int BH, int m, int m_pad)
+                                    float *__restrict__ dq_acc, int BH, int m, int m_pad, int d)
 {
     const size_t r = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (r >= static_cast<size_t>(BH) * m_pad) return;
@@ -554,11 +558,12 @@ __global__ void attn_bwd_pre_kernel(const __nv_bfloat16 *__restrict__ out, const
         return;
     }
     const size_t row = static_cast<size_t>(bh) * m + q;
-    const uint4 *o = reinterpret_cast<const uint4 *>(out + row * kD);
-    const uint4 *g = reinterpret_cast<const uint4 *>(dout + row * kD);
+    const uint4 *o = reinterpret_cast<const uint4 *>(out + row * d);
+    const uint4 *g = reinterpret_cast<const uint4 *>(dout + row * d);
     float dsum = 0.f;
 #pragma unroll
     for (int c = 0; c < kD / 8; ++c) {
+        if (8 * c >= d) break;
         const uint4 a = o[c], b = g[c];
         const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
@@ -573,14 +578,17 @@ __global__ void attn_bwd_pre_kernel(const __nv_bfloat16 *__restrict__ out, const
     for (int c = 0; c < kD / 4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// dQ = bf16(scale * accumulator), eight elements per thread.
+// dQ = bf16(scale * accumulator), eight elements per thread: chunk r is columns
+// 8 (r % (d / 8)) .. of row r / (d / 8); the accumulator's rows are 64 wide.
 __global__ void attn_bwd_post_kernel(const float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dq,
-                                     size_t count8, float scale)
+                                     size_t count8, float scale, int d)
 {
     const size_t r = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (r >= count8) return;
-    const float4 a = reinterpret_cast<const float4 *>(dq_acc)[2 * r];
-    const float4 b = reinterpret_cast<const float4 *>(dq_acc)[2 * r + 1];
+    const size_t row = r / (d / 8), c8 = r % (d / 8);
+    const float4 *src = reinterpret_cast<const float4 *>(dq_acc + row * kD + 8 * c8);
+    const float4 a = src[0];
+    const float4 b = src[1];
     uint4 o;
     o.x = pack_bf16x2(a.x * scale, a.y * scale);
     o.y = pack_bf16x2(a.z * scale, a.w * scale);
@@ -624,16 +632,18 @@ cudaError_t launch_bwd(const BwdProblem &pb, cudaStream_t stream)
     float *dq_acc = static_cast<float *>(pb.workspace);
     float2 *ld = reinterpret_cast<float2 *>(static_cast<uint8_t *>(pb.workspace) +
                                             align_up(static_cast<size_t>(BH) * pb.m * kD * sizeof(float), 256));
+    if (pb.d % 8 != 0 || pb.d < 8 || pb.d > kD) return cudaErrorInvalidValue;
+    // rows of d elements in 64-wide, 128-row boxes: columns d .. 63 of a load read as zero
     CUtensorMap tq, tk, tv, tdo, tdq;
-    if (!encode_rows_map(&tq, pb.q, pb.m, BH) || !encode_rows_map(&tk, pb.k, pb.n, BH) ||
-        !encode_rows_map(&tv, pb.v, pb.n, BH) || !encode_rows_map(&tdo, pb.dout, pb.m, BH) ||
+    if (!encode_bf16_3d(&tq, pb.q, pb.d, pb.m, BH, kBM) || !encode_bf16_3d(&tk, pb.k, pb.d, pb.n, BH, kBM) ||
+        !encode_bf16_3d(&tv, pb.v, pb.d, pb.n, BH, kBM) || !encode_bf16_3d(&tdo, pb.dout, pb.d, pb.m, BH, kBM) ||
         !encode_rows_map_f32(&tdq, dq_acc, pb.m, BH))
         return cudaErrorInvalidValue;
 
     const size_t pre_rows = static_cast<size_t>(BH) * m_pad;
     attn_bwd_pre_kernel<<<static_cast<unsigned>((pre_rows + 255) / 256), 256, 0, stream>>>(
         static_cast<const __nv_bfloat16 *>(pb.out), static_cast<const __nv_bfloat16 *>(pb.dout), pb.lse, ld,
-        dq_acc, BH, pb.m, m_pad);
+        dq_acc, BH, pb.m, m_pad, pb.d);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     BwdParams p;
@@ -649,15 +659,16 @@ cudaError_t launch_bwd(const BwdProblem &pb, cudaStream_t stream)
     p.m_pad = m_pad;
     p.mask_kind = pb.mask_kind;
     p.q_tiles = m_pad / kBM;
+    p.d = pb.d;
     p.scale_log2 = pb.scale * 1.4426950408889634f;
     p.scale = pb.scale;
     const int k_tiles = (pb.n + kBM - 1) / kBM;
     attn_bwd_kernel<<<k_tiles * BH, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-    const size_t count8 = static_cast<size_t>(BH) * pb.m * kD / 8;
+    const size_t count8 = static_cast<size_t>(BH) * pb.m * (pb.d / 8);
     attn_bwd_post_kernel<<<static_cast<unsigned>((count8 + 255) / 256), 256, 0, stream>>>(
-        dq_acc, static_cast<__nv_bfloat16 *>(pb.dq), count8, pb.scale);
+        dq_acc, static_cast<__nv_bfloat16 *>(pb.dq), count8, pb.scale, pb.d);
     return cudaGetLastError();
 }
 

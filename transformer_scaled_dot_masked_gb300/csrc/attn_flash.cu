@@ -119,6 +119,7 @@ struct FlashParams {
     int pair_mode;
     int num_tiles;
     int q_pairs;        // pair mode: query-tile pairs per head
+    int group_heads;    // pair mode: heads per group of the tile order (their K and V share L2)
     int *tile_counter;  // [0] next tile to claim, [1] CTAs done; nullptr: static snake schedule
     int d;              // head width in memory (a multiple of 8, <= 64): narrower heads enter
                         // the 64-wide tiles zero-padded by the TMA loads and leave clipped by the store
@@ -161,9 +162,14 @@ __device__ __forceinline__ Tile decode_tile(const FlashParams &p, int t)
 {
     Tile T;
     if (p.pair_mode) {
-        // heaviest pair first: with a causal mask later query tiles see more keys
-        const int pair = p.q_pairs - 1 - t / p.BH;
-        const int bh = t % p.BH;
+        // Heads are taken in groups whose keys and values fit in L2 together; within a
+        // group, heaviest pair first (with a causal mask later query tiles see more keys),
+        // so the CTAs working at one time share a group's K and V through L2.
+        const int per_group = p.group_heads * p.q_pairs;
+        const int g = t / per_group, r = t - g * per_group;
+        const int heads = min(p.group_heads, p.BH - g * p.group_heads); // the last group may be short
+        const int pair = p.q_pairs - 1 - r / heads;
+        const int bh = g * p.group_heads + r % heads;
         T.bh[0] = T.bh[1] = bh;
         T.q0[0] = pair * 2 * kBM;
         T.q0[1] = pair * 2 * kBM + kBM;
@@ -897,6 +903,13 @@ cudaError_t launch_flash(const Problem &pb, bool pair_mode, int *tile_counter, c
     p.scale_log2 = pb.scale * 1.4426950408889634f;
     p.pair_mode = pair_mode ? 1 : 0;
     p.q_pairs = (pb.m + 2 * kBM - 1) / (2 * kBM);
+    {
+        // about 32 MB of keys and values per group: a quarter of L2, leaving room for the
+        // query tiles and output tiles streaming through it
+        const size_t kv_head = 2ull * pb.n * 64 * 2;
+        const size_t g = (32ull << 20) / (kv_head > 0 ? kv_head : 1);
+        p.group_heads = static_cast<int>(g < 1 ? 1 : (g > static_cast<size_t>(BH) ? BH : g));
+    }
     p.num_tiles = pair_mode ? BH * p.q_pairs : (BH + 1) / 2;
     p.tile_counter = tile_counter;
     const int grid = p.num_tiles < sms ? p.num_tiles : sms;

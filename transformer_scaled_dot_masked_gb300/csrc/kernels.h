@@ -40,10 +40,11 @@ cudaError_t launch_flash(const Problem &p, bool pair_mode, int *tile_counter, cu
 // Bytes of workspace the dynamic tile schedule needs.
 constexpr size_t kWorkspaceBytes = 256;
 
-// Incremental decoding (bf16, d == 64, m <= 8 queries per head, every query sees
-// keys 0 .. len_b - 1): split-KV CUDA-core kernel plus a combine pass.
+// Incremental decoding (bf16, d in {16, 32, 64, 128}, m <= 8 queries per head, every
+// query sees keys 0 .. len_b - 1): split-KV CUDA-core kernel plus a combine pass.
 int decode_splits(int B, int h, int n, int sms);
-size_t decode_workspace_bytes(int B, int h, int m, int n, int sms);
+bool decode_width_supported(int d);
+size_t decode_workspace_bytes(int B, int h, int m, int n, int d, int sms);
 cudaError_t launch_decode(const Problem &p, void *workspace, int sms, cudaStream_t stream);
 
 // [BH][rows][64] bf16 viewed as a 3-D tensor (64, rows, BH) for TMA; box = 128
@@ -58,15 +59,17 @@ bool encode_bf16_3d(CUtensorMap *map, const void *base, int inner, int rows, int
 // columns (one 128-byte swizzle span), 128-byte swizzle.
 bool encode_rows_map_f32(CUtensorMap *map, void *base, int rows, int BH);
 
-// Backward: dQ, dK, dV (bf16, d == 64) from Q, K, V, the forward's output and
-// per-row log-sum-exp, and the output gradient.
+// Backward: dQ, dK, dV (bf16, d a multiple of 8 up to 64) from Q, K, V, the forward's
+// output and per-row log-sum-exp, and the output gradient.
 struct BwdProblem {
-    const void *q, *k, *v, *out, *dout; // bf16 [B][h][rows][64]
+    const void *q, *k, *v, *out, *dout; // bf16 [B][h][rows][d]
     const float *lse;                   // [B][h][m], natural log
     const int32_t *key_lengths;         // device [B]; nullptr unless key padding
     void *dq, *dk, *dv;                 // bf16, shaped like q, k, v
     void *workspace;                    // bwd_workspace_bytes(B, h, m), 256-byte aligned
     int B, h, m, n;
+    int d = 64;                         // head width: a multiple of 8 up to 64 (narrower heads
+                                        // enter the 64-wide tiles zero-padded)
     int mask_kind;
     float scale;
 };
