@@ -108,6 +108,8 @@ struct BwdParams {
     const int32_t *key_lengths;
     int BH, h, m, n, m_pad, mask_kind, q_tiles;
     int d;                   // head width in memory (a multiple of 8, <= 64); the tiles are 64 wide
+    int group_heads;         // heads per group of the CTA order (their Q and dO share L2)
+    int k_tiles;             // key tiles per head
     float scale_log2;        // scale * log2 e
     float scale;
 };
@@ -467,9 +469,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     BwdSmem &sm = *reinterpret_cast<BwdSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x / 32;
-    // key tile j ascending first: with a causal mask the low key tiles see the most queries
-    const int j = blockIdx.x / p.BH;
-    const int bh = blockIdx.x % p.BH;
+    // Heads in groups whose Q and dO fit in L2 together, so the CTAs running at one time
+    // share them; within a group, key tile j ascending first (with a causal mask the low
+    // key tiles see the most queries).
+    const int per_group = p.group_heads * p.k_tiles;
+    const int grp = static_cast<int>(blockIdx.x) / per_group, r_in = static_cast<int>(blockIdx.x) - grp * per_group;
+    const int heads = min(p.group_heads, p.BH - grp * p.group_heads); // the last group may be short
+    const int j = r_in / heads;
+    const int bh = grp * p.group_heads + r_in % heads;
     const int key0 = j * kBM;
     const int len = key_len(p, bh);
     const bool causal = (p.mask_kind & kMaskCausal) != 0;
@@ -663,6 +670,13 @@ cudaError_t launch_bwd(const BwdProblem &pb, cudaStream_t stream)
     p.scale_log2 = pb.scale * 1.4426950408889634f;
     p.scale = pb.scale;
     const int k_tiles = (pb.n + kBM - 1) / kBM;
+    p.k_tiles = k_tiles;
+    {
+        // about 32 MB of Q and dO per group (a quarter of L2)
+        const size_t qdo_head = 2ull * pb.m * kD * 2;
+        const size_t g = (32ull << 20) / (qdo_head > 0 ? qdo_head : 1);
+        p.group_heads = static_cast<int>(g < 1 ? 1 : (g > static_cast<size_t>(BH) ? BH : g));
+    }
     attn_bwd_kernel<<<k_tiles * BH, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
