@@ -378,13 +378,14 @@ attn_status attn_decode(const void *Q, const void *K, const void *V, const int32
                         float scale, void *out, float *lse, const attn_dims *dims,
                         void *workspace, size_t workspace_bytes, void *stream);
 
-/* Shapes of a multi-head attention call with its projections (d_k = d_v = 64). */
+/* Shapes of a multi-head attention call with its projections (d_v = d_k). */
 typedef struct {
     int32_t B;       /* batch */
-    int32_t h;       /* heads; h * 64 must be a multiple of 128 */
+    int32_t h;       /* heads; h * d_k must be a multiple of 128 */
     int32_t m;       /* query positions */
     int32_t n;       /* key/value positions */
     int32_t d_model; /* model width, a multiple of 128 */
+    int32_t d_k;     /* head width: 64 or 128 (0 is read as 64); the pages' d_model / h */
 } attn_mha_dims;
 
 /* Bytes of device workspace attn_mha_fwd needs (host only, no CUDA call); 0 if
@@ -393,27 +394,30 @@ size_t attn_mha_workspace_size(const attn_mha_dims *dims);
 
 /*
  * Multi-head attention with its projections ("Paper Deep Reading", §04; the
- * slide deck's "Multi-Head Attention" slide):
+ * slide deck's "Multi-Head Attention" slide; heads of width 64, as in the base and
+ * big models, or 128, the model-variant table's h = 4 row):
  *
  *     head_i = Attention(Xq W_i^Q, Xkv W_i^K, Xkv W_i^V),
  *     out    = Concat(head_1, ..., head_h) W^O,
  *
- * with d_k = d_v = 64 and no bias terms (the formula has none); Attention is
- * attn_fwd's (mask and scale as there).  All tensors bf16, row-major, in device
- * memory of the current device, 16-byte aligned:
+ * with d_k = d_v = dims->d_k and no bias terms (the formula has none); Attention
+ * is attn_fwd's (mask and scale as there; ATTN_SCALE_DEFAULT gives 1/sqrt(d_k)).
+ * All tensors bf16, row-major, in device memory of the current device, 16-byte
+ * aligned:
  *   Xq   [B][m][d_model], Xkv [B][n][d_model] (pass Xq for self-attention)
- *   Wq, Wk, Wv  [d_model][h * 64]: head i uses columns 64i .. 64i+63
- *   Wo   [h * 64][d_model]: head i's output multiplies rows 64i .. 64i+63
+ *   Wq, Wk, Wv  [d_model][h * d_k]: head i uses columns i d_k .. (i + 1) d_k - 1
+ *   Wo   [h * d_k][d_model]: head i's output multiplies rows i d_k .. (i + 1) d_k - 1
  *   out  [B][m][d_model]
  *   workspace  attn_mha_workspace_size(dims) bytes (Q, K, V and the heads'
- *              outputs in [B][h][len][64]), 256-byte aligned, any contents
+ *              outputs in [B][h][len][d_k]), 256-byte aligned, any contents
  * Five kernels are enqueued: three projections into the head-split layout
  * (tcgen05 GEMMs whose epilogues write each 64-column block as one head), the
  * attention, and the output projection, which reads the heads' outputs as its K
  * dimension directly (the concatenation costs no copy).
  *
- * Errors: NULL pointers (ATTN_ERR_NULL), bad shapes or h * 64 or d_model not
- * multiples of 128, causal with m != n (ATTN_ERR_SHAPE), mask bits other than
+ * Errors: NULL pointers (ATTN_ERR_NULL), bad shapes or h * d_k or d_model not
+ * multiples of 128, causal with m != n (ATTN_ERR_SHAPE), d_k other than 64 or 128
+ * (ATTN_ERR_DTYPE), mask bits other than
  * KEY_PADDING and CAUSAL (ATTN_ERR_MASK), unaligned pointers (ATTN_ERR_ALIGN),
  * bad scale (ATTN_ERR_VALUE), a workspace too small (ATTN_ERR_SHAPE), out or the
  * workspace overlapping an input or each other (ATTN_ERR_ALIAS), CUDA errors.

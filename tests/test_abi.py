@@ -269,3 +269,16 @@ def _call_mha(dims=(2, 2, 8, 8, 128), mask=0, lens=None, ws=0xE000000, ws_bytes=
 ])
 def test_mha_rejects_bad_arguments(kwargs, status):
     assert _call_mha(**kwargs) == status
+
+
+def test_mha_head_width():
+    # the dims struct is six int32 fields in this order
+    fields = re.search(r"typedef struct \{([^}]*)\} attn_mha_dims;", HEADER_TEXT).group(1)
+    assert re.findall(r"int32_t (\w+);", fields) == [f for f, _ in N.MhaDims._fields_]
+    assert N.mha_workspace_size(2, 2, 8, 8, 128, 128) == 2 * N.mha_workspace_size(2, 2, 8, 8, 128, 64)
+    assert N.mha_workspace_size(2, 2, 8, 8, 128, 0) == N.mha_workspace_size(2, 2, 8, 8, 128, 64)  # 0 reads as 64
+    assert N.mha_workspace_size(2, 2, 8, 8, 128, 32) == 0                                        # not built
+    assert N.mha_workspace_size(2, 1, 8, 8, 128, 128) > 0                                        # h * 128
+    d = N.MhaDims(2, 2, 8, 8, 128, 96)
+    assert N.lib.attn_mha_fwd(A, B_, C, 0x7000000, 0x8000000, 0x9000000, None, 0, ctypes.c_float(0.125), O,
+                              ctypes.byref(d), 0xE000000, 1 << 20, None) == 3                   # ATTN_ERR_DTYPE

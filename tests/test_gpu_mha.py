@@ -55,6 +55,33 @@ def test_mha_matches_oracle(orc, name, B, h, m, n, dm, mask, selfattn, lengths):
     assert np.abs(got - ref).max() <= 2e-2, report(got, ref, 2e-2)
 
 
+WIDE_CASES = [
+    # heads of width 128: the model-variant table's h = 4 row (d_model 512) and a wider
+    # model; the attention runs on the d_k = 128 kernel, each head spans two 64-column
+    # blocks of the projections
+    ("h4_d128_encoder_padding", 3, 4, 100, 100, 512, MASK_KEY_PADDING, True, (10, 100)),
+    ("h4_d128_decoder_causal", 2, 4, 300, 300, 512, MASK_CAUSAL, True, None),
+    ("h8_d128_cross_padding", 2, 8, 128, 200, 1024, MASK_KEY_PADDING, False, (40, 200)),
+    ("h1_d128_long", 1, 1, 700, 700, 256, MASK_NONE, True, None),
+]
+
+
+@pytest.mark.parametrize("name,B,h,m,n,dm,mask,selfattn,lengths", WIDE_CASES, ids=[c[0] for c in WIDE_CASES])
+def test_mha_wide_heads(orc, name, B, h, m, n, dm, mask, selfattn, lengths):
+    xq, xkv, wq, wk, wv, wo = draw_mha(B, h, m, n, dm, seed=83, self_attention=selfattn, d_k=128)
+    lens = np.full(B, n, dtype=np.int32)
+    if lengths is not None:
+        lens = np.random.default_rng(84).integers(lengths[0], lengths[1] + 1, size=B).astype(np.int32)
+    out = attn.attn_mha_fwd(dev(xq), dev(xkv), dev(wq), dev(wk), dev(wv), dev(wo), h,
+                            torch.from_numpy(lens).cuda(), mask)  # default scale: 1/sqrt(128)
+    torch.cuda.synchronize()
+    st, info = attn.device_status()
+    assert st == 0, f"device status {st} (info {info})"
+    ref = mha.mha_fwd(orc, xq, xkv, wq, wk, wv, wo, h, lens, mask, 128 ** -0.5)
+    got = as_f64(out)
+    assert np.abs(got - ref).max() <= 2e-2, report(got, ref, 2e-2)
+
+
 def test_mha_benchmarked_size(orc):
     """The benchmarked call at full size and with its inputs: B32 sentences of 256
     positions, d_model 1024, h 16, key padding with lengths in [128, 256] (the same

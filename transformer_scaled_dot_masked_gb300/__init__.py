@@ -325,11 +325,11 @@ def mha_workspace_size(B, h, m, n, d_model) -> int:
 
 def attn_mha_fwd(xq, xkv, wq, wk, wv, wo, h: int, key_lengths=None, mask_kind: int = MASK_NONE,
                  scale: Optional[float] = None, out=None, workspace=None, stream=None):
-    """Multi-head attention with its projections (bf16, d_k = 64, no biases).
+    """Multi-head attention with its projections (bf16, d_k = 64 or 128, no biases).
 
-    xq [B, m, d_model], xkv [B, n, d_model]; wq, wk, wv [d_model, h * 64] (head i = columns
-    64i..64i+63); wo [h * 64, d_model].  Returns out [B, m, d_model] =
-    Concat(Attention(xq wq_i, xkv wk_i, xkv wv_i)) wo.
+    xq [B, m, d_model], xkv [B, n, d_model]; wq, wk, wv [d_model, h * d_k] (head i = columns
+    i*d_k .. (i+1)*d_k - 1); wo [h * d_k, d_model]; d_k is read from the shape of wq.
+    Returns out [B, m, d_model] = Concat(Attention(xq wq_i, xkv wk_i, xkv wv_i)) wo.
     """
     import torch
     for t in (xq, xkv, wq, wk, wv, wo):
@@ -337,21 +337,25 @@ def attn_mha_fwd(xq, xkv, wq, wk, wv, wo, h: int, key_lengths=None, mask_kind: i
             raise ValueError("inputs must be contiguous bf16 CUDA tensors")
     B, m, dm = xq.shape
     n = xkv.shape[1]
-    if xkv.shape != (B, n, dm) or wq.shape != (dm, h * 64) or wk.shape != wq.shape or wv.shape != wq.shape \
-            or wo.shape != (h * 64, dm):
+    if wq.dim() != 2 or wq.shape[1] % h:
+        raise ValueError("wq must be [d_model, h * d_k]")
+    dk = wq.shape[1] // h
+    if xkv.shape != (B, n, dm) or wq.shape != (dm, h * dk) or wk.shape != wq.shape or wv.shape != wq.shape \
+            or wo.shape != (h * dk, dm):
         raise ValueError("shape mismatch between inputs, projections and h")
     scale = SCALE_DEFAULT if scale is None else scale
     if out is None:
         out = torch.empty_like(xq)
-    need = _native.mha_workspace_size(B, h, m, n, dm)
+    need = _native.mha_workspace_size(B, h, m, n, dm, dk)
     if need == 0:
-        raise AttnError(2)  # ATTN_ERR_SHAPE
+        raise AttnError(2)  # ATTN_ERR_SHAPE (or a head width other than 64 and 128)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=xq.device)
     stream = torch.cuda.current_stream(xq.device) if stream is None else stream
     st = _native.mha_raw(xq.data_ptr(), xkv.data_ptr(), wq.data_ptr(), wk.data_ptr(), wv.data_ptr(), wo.data_ptr(),
                          _lengths_ptr(key_lengths, mask_kind, B), mask_kind, scale, out.data_ptr(), B, h, m, n, dm,
-                         workspace.data_ptr(), workspace.numel() * workspace.element_size(), stream.cuda_stream)
+                         workspace.data_ptr(), workspace.numel() * workspace.element_size(), stream.cuda_stream,
+                         dk)
     if st != _native.ATTN_OK:
         raise AttnError(st)
     return out

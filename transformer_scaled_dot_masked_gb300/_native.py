@@ -34,7 +34,7 @@ KERNEL_NAMES = {KERNEL_AUTO: "auto", KERNEL_FLASH: "flash", KERNEL_SHORT: "short
 
 class MhaDims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("h", ctypes.c_int32), ("m", ctypes.c_int32),
-                ("n", ctypes.c_int32), ("d_model", ctypes.c_int32)]
+                ("n", ctypes.c_int32), ("d_model", ctypes.c_int32), ("d_k", ctypes.c_int32)]
 
 
 class AttnDims(ctypes.Structure):
@@ -197,15 +197,15 @@ def decode_raw(q_ptr, k_ptr, v_ptr, lens_ptr, scale, out_ptr, lse_ptr, dims: Att
                            ws_ptr, int(ws_bytes), stream_ptr)
 
 
-def mha_workspace_size(B, h, m, n, d_model) -> int:
-    d = MhaDims(int(B), int(h), int(m), int(n), int(d_model))
+def mha_workspace_size(B, h, m, n, d_model, d_k=64) -> int:
+    d = MhaDims(int(B), int(h), int(m), int(n), int(d_model), int(d_k))
     return int(lib.attn_mha_workspace_size(ctypes.byref(d)))
 
 
 def mha_raw(xq, xkv, wq, wk, wv, wo, lens_ptr, mask_kind, scale, out_ptr, B, h, m, n, d_model, ws_ptr, ws_bytes,
-            stream_ptr) -> int:
+            stream_ptr, d_k=64) -> int:
     """attn_mha_fwd with integer device pointers; returns the status code."""
-    d = MhaDims(int(B), int(h), int(m), int(n), int(d_model))
+    d = MhaDims(int(B), int(h), int(m), int(n), int(d_model), int(d_k))
     return lib.attn_mha_fwd(xq, xkv, wq, wk, wv, wo, lens_ptr, int(mask_kind), float(scale), out_ptr,
                             ctypes.byref(d), ws_ptr, int(ws_bytes), stream_ptr)
 

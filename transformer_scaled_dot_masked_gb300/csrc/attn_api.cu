@@ -410,11 +410,16 @@ attn_status attn_decode(const void *Q, const void *K, const void *V, const int32
 }
 
 namespace {
+int mha_dk(const attn_mha_dims &d) { return d.d_k == 0 ? 64 : d.d_k; }
+
 attn_status validate_mha_dims(const attn_mha_dims *d)
 {
     if (d == nullptr) return ATTN_ERR_NULL;
+    if (d->d_k != 0 && d->d_k != 64 && d->d_k != 128) return ATTN_ERR_DTYPE;
     if (d->B < 1 || d->h < 1 || d->m < 1 || d->n < 1 || d->d_model < 1) return ATTN_ERR_SHAPE;
-    if (d->B > 65535 || d->h > 65535 || (d->h * 64) % 128 != 0 || d->d_model % 128 != 0) return ATTN_ERR_SHAPE;
+    if (d->B > 65535 || d->h > 65535 || (static_cast<int64_t>(d->h) * mha_dk(*d)) % 128 != 0 ||
+        d->d_model % 128 != 0)
+        return ATTN_ERR_SHAPE;
     return ATTN_OK;
 }
 
@@ -427,12 +432,13 @@ struct MhaLayout {
 MhaLayout mha_layout(const attn_mha_dims &d)
 {
     const size_t BH = static_cast<size_t>(d.B) * d.h;
+    const size_t dk = static_cast<size_t>(mha_dk(d));
     MhaLayout L;
     L.q = 0;
-    L.k = L.q + align256(BH * d.m * 64 * 2);
-    L.v = L.k + align256(BH * d.n * 64 * 2);
-    L.o = L.v + align256(BH * d.n * 64 * 2);
-    L.total = L.o + align256(BH * d.m * 64 * 2);
+    L.k = L.q + align256(BH * d.m * dk * 2);
+    L.v = L.k + align256(BH * d.n * dk * 2);
+    L.o = L.v + align256(BH * d.n * dk * 2);
+    L.total = L.o + align256(BH * d.m * dk * 2);
     return L;
 }
 } // namespace
@@ -462,7 +468,8 @@ attn_status attn_mha_fwd(const void *Xq, const void *Xkv, const void *Wq, const 
     if ((mask_kind & ATTN_MASK_KEY_PADDING) && !aligned(key_lengths, 4)) return ATTN_ERR_ALIGN;
     const MhaLayout L = mha_layout(d);
     if (workspace_bytes < L.total) return ATTN_ERR_SHAPE;
-    const uint64_t dm = d.d_model, hd = static_cast<uint64_t>(d.h) * 64;
+    const int dk = mha_dk(d);
+    const uint64_t dm = d.d_model, hd = static_cast<uint64_t>(d.h) * dk;
     const uint64_t xq = static_cast<uint64_t>(d.B) * d.m * dm * 2, xkv = static_cast<uint64_t>(d.B) * d.n * dm * 2;
     const uint64_t wb = dm * hd * 2;
     struct Span {
@@ -483,7 +490,8 @@ attn_status attn_mha_fwd(const void *Xq, const void *Xkv, const void *Wq, const 
     pp.h = d.h;
     pp.mode = attn::kProjIn;
     pp.K = d.d_model;
-    pp.N = d.h * 64;
+    pp.N = d.h * dk;
+    pp.dk = dk;
     const struct {
         const void *x, *w;
         void *o;
@@ -499,7 +507,7 @@ attn_status attn_mha_fwd(const void *Xq, const void *Xkv, const void *Wq, const 
     }
     // the three input projections in one launch
     if (attn::launch_proj_multi(in3, 3, s) != cudaSuccess) return ATTN_ERR_CUDA;
-    attn_dims ad{d.B, d.h, d.m, d.n, 64, ATTN_BF16};
+    attn_dims ad{d.B, d.h, d.m, d.n, dk, ATTN_BF16};
     // the attention and the output projection each start as programmatic dependents of
     // the launch before them: their set-up overlaps its tail, and each waits for it to
     // complete before reading its output
@@ -510,7 +518,7 @@ attn_status attn_mha_fwd(const void *Xq, const void *Xkv, const void *Wq, const 
     pp.w = Wo;
     pp.out = out;
     pp.L = d.m;
-    pp.K = d.h * 64;
+    pp.K = d.h * dk;
     pp.N = d.d_model;
     pp.overlap_launch = true;
     return attn::launch_proj(pp, s) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
@@ -781,6 +789,6 @@ const char *attn_status_string(int status)
     }
 }
 
-int32_t attn_version(void) { return (1 << 16) | 1; }
+int32_t attn_version(void) { return (1 << 16) | 2; }
 
 } // extern "C"

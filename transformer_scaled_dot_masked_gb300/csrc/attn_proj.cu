@@ -98,6 +98,7 @@ struct ProjMaps {
 
 struct ProjParams {
     int mode, h, K, N, B, problems;
+    int dk; // head width: a head is dk / 64 blocks of 64 columns
     int m_tiles[kMaxProblems]; // 128-row tiles per batch entry of product i
     int tiles_of[kMaxProblems];
     int n_tiles, tiles;
@@ -195,8 +196,9 @@ attn_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
                     mbar_arrive_expect_tx(&sm.full[s], kATile + blocks * kBBlock);
                     if (p.mode == kProjIn)
                         tma_load_3d(sm.a[s], tm_a, &sm.full[s], kk * kTK, id.t0, id.b);
-                    else
-                        tma_load_3d(sm.a[s], tm_a, &sm.full[s], 0, id.t0, id.b * p.h + kk);
+                    else // K step kk: columns 64 (kk % (dk / 64)) .. of head kk / (dk / 64)
+                        tma_load_3d(sm.a[s], tm_a, &sm.full[s], (kk % (p.dk / 64)) * 64, id.t0,
+                                    id.b * p.h + kk / (p.dk / 64));
                     // W as a 3-D tensor with one outer slice
                     for (int q = 0; q < blocks; ++q)
                         tma_load_3d(sm.b[s][q], tm_w, &sm.full[s], id.n0 + 64 * q, kk * kTK, 0);
@@ -303,8 +305,9 @@ attn_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
                 mbar_arrive(&sm.staged[j]);
                 if (r == 0) {
                     if ((ok = wait_bar(&sm.staged[j], u & 1, ab, 6))) {
-                        if (p.mode == kProjIn)
-                            tma_store_3d(tm_out, sm.stage[j], 0, id.t0, id.b * p.h + (id.n0 + 64 * q) / 64);
+                        if (p.mode == kProjIn) // column c of the product: head c / dk, column c % dk of it
+                            tma_store_3d(tm_out, sm.stage[j], (id.n0 + 64 * q) % p.dk, id.t0,
+                                         id.b * p.h + (id.n0 + 64 * q) / p.dk);
                         else
                             tma_store_3d(tm_out, sm.stage[j], id.n0 + 64 * q, id.t0, id.b);
                         bulk_commit_group();
@@ -352,9 +355,11 @@ cudaError_t launch_proj_multi(const ProjProblem *pps, int count, cudaStream_t st
     ProjParams p;
     p.mode = p0.mode;
     p.h = p0.h;
+    if (p0.dk != 64 && p0.dk != 128) return cudaErrorInvalidValue;
     p.K = p0.K;
     p.N = p0.N;
     p.B = p0.B;
+    p.dk = p0.dk;
     p.problems = count;
     p.n_tiles = (p0.N + kTN - 1) / kTN;
     p.tiles = 0;
@@ -366,14 +371,14 @@ cudaError_t launch_proj_multi(const ProjProblem *pps, int count, cudaStream_t st
     for (int i = 0; i < count; ++i) {
         const ProjProblem &pp = pps[i];
         // one launch runs products of one shape: only the row count may differ
-        if (pp.mode != p0.mode || pp.B != p0.B || pp.h != p0.h || pp.K != p0.K || pp.N != p0.N)
+        if (pp.mode != p0.mode || pp.B != p0.B || pp.h != p0.h || pp.K != p0.K || pp.N != p0.N || pp.dk != p0.dk)
             return cudaErrorInvalidValue;
         bool enc;
         if (pp.mode == kProjIn) {
             enc = encode_bf16_3d(&maps.a[i], pp.a, pp.K, pp.L, pp.B, kTM) &&
-                  encode_bf16_3d(&maps.out[i], pp.out, 64, pp.L, BH, kTM);
+                  encode_bf16_3d(&maps.out[i], pp.out, pp.dk, pp.L, BH, kTM);
         } else {
-            enc = encode_bf16_3d(&maps.a[i], pp.a, 64, pp.L, BH, kTM) &&
+            enc = encode_bf16_3d(&maps.a[i], pp.a, pp.dk, pp.L, BH, kTM) &&
                   encode_bf16_3d(&maps.out[i], pp.out, pp.N, pp.L, pp.B, kTM);
         }
         // W [K][N] as a 3-D tensor with one outer slice: 64 x 64 boxes

@@ -103,6 +103,7 @@ struct WideParams {
     __nv_bfloat16 *out;
     float *lse;
     int BH, h, m, n, mask_kind, q_pairs;
+    int group_heads; // query-tile pairs: heads per group of the CTA order (their K and V share L2)
     int window;     // restricted attention: keys with |i - j| <= window stay; -1: none
     int head_pairs; // 1: m, n <= 128, and slot s of CTA c takes (batch, head) 2c + s (host side;
                     // the kernel is instantiated for each mode)
@@ -273,9 +274,13 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     constexpr bool hp = kHeadPairs;
     const bool causal = (p.mask_kind & kMaskCausal) != 0;
     // Slot s works on query rows q0s[s] .. q0s[s] + 127 of head bhs[s].  Query-tile
-    // pairs: one head, two consecutive query tiles, heaviest pairs first (with a causal
-    // mask later query tiles see more keys).  Head pairs: two heads, query tile 0; a
-    // slot past the last head has no rows.
+    // pairs: one head, two consecutive query tiles; heads in groups whose keys and values
+    // fit in L2 together (the CTAs running at one time share them), heaviest pairs first
+    // within a group (with a causal mask later query tiles see more keys).  Head pairs:
+    // two heads, query tile 0; a slot past the last head has no rows.
+    const int per_group = p.group_heads * p.q_pairs;
+    const int grp = static_cast<int>(blockIdx.x) / per_group, r_in = static_cast<int>(blockIdx.x) - grp * per_group;
+    const int g_heads = min(p.group_heads, p.BH - grp * p.group_heads); // the last group may be short
     int bhs[kSlots], q0s[kSlots], lens[kSlots], lo[kSlots], hi[kSlots];
 #pragma unroll
     for (int s = 0; s < kSlots; ++s) {
@@ -283,8 +288,8 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             bhs[s] = kSlots * static_cast<int>(blockIdx.x) + s;
             q0s[s] = 0;
         } else {
-            bhs[s] = static_cast<int>(blockIdx.x) % p.BH;
-            q0s[s] = ((p.q_pairs - 1 - static_cast<int>(blockIdx.x) / p.BH) * kSlots + s) * kBM;
+            bhs[s] = grp * p.group_heads + r_in % g_heads;
+            q0s[s] = ((p.q_pairs - 1 - r_in / g_heads) * kSlots + s) * kBM;
         }
         int len = 0;
         if (bhs[s] < p.BH) {
@@ -704,6 +709,12 @@ cudaError_t launch_wide(const Problem &pb, cudaStream_t stream)
     p.n = pb.n;
     p.mask_kind = pb.mask_kind;
     p.q_pairs = (pb.m + kSlots * kBM - 1) / (kSlots * kBM);
+    {
+        // about 32 MB of keys and values per group (a quarter of L2)
+        const size_t kv_head = 2ull * pb.n * kDW * 2;
+        const size_t g = (32ull << 20) / (kv_head > 0 ? kv_head : 1);
+        p.group_heads = static_cast<int>(g < 1 ? 1 : (g > static_cast<size_t>(BH) ? BH : g));
+    }
     // one query tile and one key tile per head: two heads per CTA, so that the
     // second slot has rows (and the grid halves)
     p.head_pairs = (pb.m <= kBM && pb.n <= kBN && BH > 1) ? 1 : 0;

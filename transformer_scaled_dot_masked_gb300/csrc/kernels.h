@@ -80,16 +80,17 @@ cudaError_t launch_bwd(const BwdProblem &p, cudaStream_t stream);
 cudaError_t bwd_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint32_t *info);
 
 // Projection GEMM of the multi-head wrapper (tcgen05).  kIn: out[b*h + j][t][:] =
-// row t of x[b] (a [B][L][K] bf16 tensor) times columns 64j .. 64j+63 of w
-// ([K][N] bf16, N = h * 64).  kOut: out[b][t][:] = sum over heads j of row t of
-// a[b*h + j] ([B*h][L][64]) times rows 64j .. 64j+63 of w ([h * 64][N]).
+// row t of x[b] (a [B][L][K] bf16 tensor) times columns dk j .. dk (j+1) - 1 of w
+// ([K][N] bf16, N = h * dk).  kOut: out[b][t][:] = sum over heads j of row t of
+// a[b*h + j] ([B*h][L][dk]) times rows dk j .. dk (j+1) - 1 of w ([h * dk][N]).
 enum ProjMode : int { kProjIn = 0, kProjOut = 1 };
 struct ProjProblem {
     ProjMode mode;
-    const void *a;   // kIn: x [B][L][K]; kOut: heads [B*h][L][64]
-    const void *w;   // [K][N], K = d_model (kIn) or h * 64 (kOut)
-    void *out;       // kIn: [B*h][L][64]; kOut: [B][L][N]
+    const void *a;   // kIn: x [B][L][K]; kOut: heads [B*h][L][dk]
+    const void *w;   // [K][N], K = d_model (kIn) or h * dk (kOut)
+    void *out;       // kIn: [B*h][L][dk]; kOut: [B][L][N]
     int B, h, L, K, N;
+    int dk = 64;     // head width (64 or 128): a head is dk / 64 blocks of 64 columns
     bool overlap_launch = false; // launched as a programmatic dependent of the previous kernel on the stream
 };
 cudaError_t launch_proj(const ProjProblem &p, cudaStream_t stream);

@@ -153,17 +153,17 @@ def draw_dout(w: Workload, seed: Optional[int] = None) -> np.ndarray:
     return round_to_bf16_bits(g) if w.dtype == "bf16" else g
 
 
-def draw_mha(B: int, h: int, m: int, n: int, d_model: int, seed: int, self_attention: bool):
+def draw_mha(B: int, h: int, m: int, n: int, d_model: int, seed: int, self_attention: bool, d_k: int = 64):
     """Inputs of one multi-head call: Xq [B, m, d_model], Xkv [B, n, d_model] (Xq itself for
-    self-attention) standard normal, and W^Q, W^K, W^V [d_model, h*64], W^O [h*64, d_model]
+    self-attention) standard normal, and W^Q, W^K, W^V [d_model, h*d_k], W^O [h*d_k, d_model]
     normal with variance 1/fan_in (so projected values stay of order one); all rounded to
     bf16, drawn in that order from default_rng(seed)."""
     rng = np.random.default_rng(seed)
     xq = rng.standard_normal((B, m, d_model), dtype=np.float32)
     xkv = xq if self_attention else rng.standard_normal((B, n, d_model), dtype=np.float32)
-    ws = [rng.standard_normal((d_model, h * 64), dtype=np.float32) / np.float32(np.sqrt(d_model))
+    ws = [rng.standard_normal((d_model, h * d_k), dtype=np.float32) / np.float32(np.sqrt(d_model))
           for _ in range(3)]
-    wo = rng.standard_normal((h * 64, d_model), dtype=np.float32) / np.float32(np.sqrt(h * 64))
+    wo = rng.standard_normal((h * d_k, d_model), dtype=np.float32) / np.float32(np.sqrt(h * d_k))
     r = round_to_bf16_bits
     return r(xq), r(xkv), r(ws[0]), r(ws[1]), r(ws[2]), r(wo)
 
