@@ -493,3 +493,34 @@ def test_resident_lse_and_bounds(orc, mask):
     run(inp, K_RESIDENT, out=o2)
     assert (buf[:guard] == -7.0).all() and (buf[guard + n_out:] == -7.0).all()
     np.testing.assert_array_equal(as_f64(o2), as_f64(out))
+
+
+@pytest.mark.parametrize("d", [8, 16, 24, 32, 40, 48, 56])
+def test_resident_narrow_heads(orc, d):
+    """Every narrower head width on the resident kernel (zero-padded 64-wide tiles,
+    d_k-column stores): padding with empty rows, causal with padding, and the
+    log-sum-exp; guard regions around the output stay untouched."""
+    for name, m, n, mask in (("pad", 100, 170, MASK_KEY_PADDING), ("causal_pad", 128, 128, MASK_CAUSAL | MASK_KEY_PADDING)):
+        w = Workload(f"resident_d{d}_{name}", "bf16", 3, 2, m, n, d, mask, d ** -0.5, 70 + d, (0, n))
+        inp = draw(w)
+        inp.key_lengths[0] = 0
+        assert attn.select_kernel(w.B, w.h, m, n, d, 0, mask) == K_RESIDENT
+        q, k, v = (to_device(x, "bf16") for x in (inp.q, inp.k, inp.v))
+        lens = torch.from_numpy(inp.key_lengths).cuda()
+        n_out = w.B * w.h * m * d
+        guard = 4096
+        buf = torch.full((n_out + 2 * guard,), -7.0, dtype=torch.bfloat16, device="cuda")
+        out = buf[guard:guard + n_out].view(w.B, w.h, m, d)
+        lse = torch.empty((w.B, w.h, m), dtype=torch.float32, device="cuda")
+        attn.attn_fwd_lse(q, k, v, lens, mask, w.scale, out=out, lse=lse)
+        torch.cuda.synchronize()
+        assert attn.device_status() == (0, 0)
+        assert (buf[:guard] == -7.0).all() and (buf[guard + n_out:] == -7.0).all()
+        ref = orc.attn_fwd(inp.q, inp.k, inp.v, inp.key_lengths, mask, w.scale)
+        got = as_f64(out)
+        assert np.abs(got - ref).max() <= 1e-2, report(got, ref, 1e-2)
+        ref_lse = orc.attn_lse(inp.q, inp.k, inp.key_lengths, mask, w.scale)
+        g = lse.double().cpu().numpy()
+        fin = np.isfinite(ref_lse)
+        assert np.array_equal(np.isfinite(g), fin)
+        assert np.abs(g[fin] - ref_lse[fin]).max() <= 2e-3
