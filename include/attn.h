@@ -329,13 +329,15 @@ size_t attn_bwd_workspace_size(const attn_dims *dims);
  *                  the same time on the GPU need different workspaces
  *   dims, stream   as for the forward
  *
- * Supported: bf16 with d_k a multiple of 8 up to 64 (narrower heads run zero-padded
- * to 64 inside the kernels; ATTN_ERR_DTYPE otherwise).  All tensors
+ * Supported: every dtype and head width attn_fwd takes.  bf16 with d_k a multiple of
+ * 8 up to 64 runs on tensor cores (narrower heads zero-padded to 64 inside the
+ * kernels; three kernels: a row pass for D and the padded per-row table that zeroes
+ * the dQ accumulator, the tensor-core pass, the dQ conversion); fp32 and the other
+ * bf16 widths up to 128 run on the CUDA cores with fp32 arithmetic (two kernels: a
+ * rows pass for D and dQ, a keys pass for dK and dV).  All tensors
  * 16-byte aligned, lse 4-byte aligned (ATTN_ERR_ALIGN).  dQ, dK, dV and the
  * workspace must not overlap each other or any input (ATTN_ERR_ALIAS).  A
  * workspace that is too small is ATTN_ERR_SHAPE.  Other errors as attn_fwd.
- * Three kernels are enqueued: a row pass (D and the padded per-row table; zeroes
- * the dQ accumulator), the tensor-core pass, and the dQ conversion.
  */
 attn_status attn_bwd(const void *Q, const void *K, const void *V, const void *out,
                      const void *dout, const float *lse, const int32_t *key_lengths,

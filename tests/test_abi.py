@@ -192,10 +192,12 @@ def test_fwd_lse_validation():
 
 def test_bwd_workspace_size():
     assert N.bwd_workspace_size(N.make_dims(2, 3, 300, 200, 64, 0)) >= 2 * 3 * 300 * 64 * 4
-    assert N.bwd_workspace_size(N.make_dims(2, 3, 300, 200, 64, 1)) == 0   # fp32: no backward
     assert N.bwd_workspace_size(N.make_dims(2, 3, 300, 200, 32, 0)) >= 2 * 3 * 300 * 64 * 4  # zero-padded
-    assert N.bwd_workspace_size(N.make_dims(2, 3, 300, 200, 20, 0)) == 0   # not a multiple of 8
-    assert N.bwd_workspace_size(N.make_dims(2, 3, 300, 200, 128, 0)) == 0  # wider than 64
+    # CUDA-core backward (fp32, other bf16 widths up to 128): D, one float per query row
+    assert N.bwd_workspace_size(N.make_dims(2, 3, 300, 200, 64, 1)) == 2 * 3 * 300 * 4
+    assert N.bwd_workspace_size(N.make_dims(2, 3, 300, 200, 20, 0)) == 2 * 3 * 300 * 4
+    assert N.bwd_workspace_size(N.make_dims(2, 3, 300, 200, 128, 0)) == 2 * 3 * 300 * 4
+    assert N.bwd_workspace_size(N.make_dims(2, 3, 300, 200, 129, 0)) == 0  # wider than any kernel
     assert N.bwd_workspace_size(N.make_dims(0, 3, 300, 200, 64, 0)) == 0   # bad dims
 
 
@@ -211,7 +213,7 @@ def _call_bwd(dims=(2, 2, 8, 8, 64, 0), mask=0, lens=None, ws_bytes=None, **kw):
 @pytest.mark.parametrize("kwargs,status", [
     (dict(out=None), 1), (dict(dout=None), 1), (dict(lse=None), 1), (dict(dq=None), 1), (dict(dk=None), 1),
     (dict(dv=None), 1), (dict(ws=None), 1), (dict(q=None), 1), (dict(mask=1), 1),
-    (dict(dims=(2, 2, 8, 8, 64, 1)), 3), (dict(dims=(2, 2, 8, 8, 20, 0)), 3), (dict(dims=(2, 2, 8, 8, 128, 0)), 3),
+    (dict(dims=(2, 2, 8, 8, 129, 0)), 3), (dict(dims=(2, 2, 8, 8, 64, 7)), 3),
     (dict(dims=(2, 2, 8, 9, 64, 0), mask=2), 2), (dict(ws_bytes=64), 2),
     (dict(dout=DO + 8), 5), (dict(dk=DK + 2), 5), (dict(lse=LSE + 1), 5), (dict(ws=WS + 16), 5),
     (dict(dq=A), 10), (dict(dk=DQ + 32), 10), (dict(dv=DO), 10), (dict(ws=LSE), 10), (dict(dv=OUT2 + 16), 10),

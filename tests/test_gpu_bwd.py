@@ -180,3 +180,31 @@ def test_bwd_masked_keys_get_zero_and_dkdv_reproducible():
     assert (dk1[0] == 0).all() and (dv1[0] == 0).all() and (dq1[0] == 0).all()
     assert (dk1[1, :, 129:] == 0).all() and (dv1[1, :, 129:] == 0).all()
     assert torch.allclose(dq1.float(), dq2.float(), atol=1e-2)
+
+
+SIMT_BWD = [
+    # the CUDA-core backward: heads of width 128 (the model-variant table's h = 4 row),
+    # other bf16 widths, and fp32 (true fp32: its bound is far tighter than bf16's)
+    ("d128_causal_ragged", "bf16", 2, 2, 300, 300, 128, MASK_CAUSAL, None),
+    ("d128_cross_padding", "bf16", 3, 2, 100, 250, 128, MASK_KEY_PADDING, (0, 250)),
+    ("d100_padding_causal", "bf16", 2, 2, 130, 130, 100, MASK_KEY_PADDING | MASK_CAUSAL, (1, 130)),
+    ("fp32_d64_causal", "fp32", 2, 2, 200, 200, 64, MASK_CAUSAL, None),
+    ("fp32_d33_cross_padding", "fp32", 2, 3, 50, 70, 33, MASK_KEY_PADDING, (0, 70)),
+]
+
+
+@pytest.mark.parametrize("name,dtype,B,h,m,n,d,mask,lengths", SIMT_BWD, ids=[c[0] for c in SIMT_BWD])
+def test_bwd_cuda_cores(orc, name, dtype, B, h, m, n, d, mask, lengths):
+    w = Workload(name, dtype, B, h, m, n, d, mask, d ** -0.5, 79, lengths)
+    inp = draw(w)
+    dout = draw_dout(w)
+    _, lse, dq, dk, dv = gpu_grads(inp, dout)
+    rq, rk, rv = orc.attn_bwd(inp.q, inp.k, inp.v, dout, inp.key_lengths, w.mask, w.scale)
+    if dtype == "fp32":
+        for name_, g, r in (("dV", dv, rv), ("dK", dk, rk), ("dQ", dq, rq)):
+            err = np.abs(as_f64(g) - r).max()
+            assert err <= 1e-4 * max(1.0, np.abs(r).max()), f"{name_}: max err {err:.3e}"
+    else:
+        check_grad("dV", dv, rv)
+        check_grad("dK", dk, rk)
+        check_grad("dQ", dq, rq)

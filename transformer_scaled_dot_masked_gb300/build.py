@@ -20,7 +20,8 @@ LIBRARY = os.path.join(PKG, "libattn_gb300.so")
 BUILD_DIR = os.path.join(PKG, "_build")
 
 SOURCES = ["attn_api.cu", "attn_simt.cu", "attn_flash.cu", "attn_bwd.cu", "attn_decode.cu", "attn_proj.cu", "attn_wide.cu",
-           "attn_resident.cu", "tensor_map.cu"]
+           "attn_resident.cu", "attn_bwd_simt.cu",
+           "tensor_map.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

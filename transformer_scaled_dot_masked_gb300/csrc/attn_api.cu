@@ -267,10 +267,17 @@ attn_status attn_fwd_lse(const void *Q, const void *K, const void *V, const int3
     return run(Q, K, V, key_lengths, mask_kind, scale, out, dims, stream, ATTN_KERNEL_AUTO, nullptr, lse);
 }
 
+// Workspace of the backward for these dims: the tensor-core backward's (bf16 heads of a
+// multiple of 8 up to 64) or the CUDA-core backward's (everything else up to 128 wide).
+size_t bwd_need(const attn_dims &d)
+{
+    return tensor_core_head(d) ? attn::bwd_workspace_bytes(d.B, d.h, d.m) : attn::bwd_simt_workspace_bytes(d.B, d.h, d.m);
+}
+
 size_t attn_bwd_workspace_size(const attn_dims *dims)
 {
-    if (validate_dims(dims, 0, 1.0f) != ATTN_OK || !tensor_core_head(*dims)) return 0;
-    return attn::bwd_workspace_bytes(dims->B, dims->h, dims->m);
+    if (validate_dims(dims, 0, 1.0f) != ATTN_OK) return 0;
+    return bwd_need(*dims);
 }
 
 attn_status attn_bwd(const void *Q, const void *K, const void *V, const void *out, const void *dout, const float *lse,
@@ -284,14 +291,14 @@ attn_status attn_bwd(const void *Q, const void *K, const void *V, const void *ou
     const attn_status st = validate(Q, K, V, key_lengths, mask_kind, scale, dQ, dims);
     if (st != ATTN_OK) return st;
     const attn_dims &d = *dims;
-    if (!tensor_core_head(d)) return ATTN_ERR_DTYPE; // bf16, d_k a multiple of 8 up to 64
     if (!aligned(out, 16) || !aligned(dout, 16) || !aligned(dK, 16) || !aligned(dV, 16) || !aligned(lse, 4) ||
         !aligned(workspace, 256))
         return ATTN_ERR_ALIGN;
-    const size_t need = attn::bwd_workspace_bytes(d.B, d.h, d.m);
+    const size_t need = bwd_need(d);
     if (workspace_bytes < need) return ATTN_ERR_SHAPE;
-    const uint64_t qbytes = static_cast<uint64_t>(d.B) * d.h * d.m * d.d_k * 2;
-    const uint64_t kbytes = static_cast<uint64_t>(d.B) * d.h * d.n * d.d_k * 2;
+    const uint64_t esz = d.dtype == ATTN_BF16 ? 2 : 4;
+    const uint64_t qbytes = static_cast<uint64_t>(d.B) * d.h * d.m * d.d_k * esz;
+    const uint64_t kbytes = static_cast<uint64_t>(d.B) * d.h * d.n * d.d_k * esz;
     const uint64_t lbytes = static_cast<uint64_t>(d.B) * d.h * d.m * 4;
     struct Span {
         const void *p;
@@ -306,6 +313,30 @@ attn_status attn_bwd(const void *Q, const void *K, const void *V, const void *ou
             if (overlaps(outs[a].p, outs[a].n, outs[b].p, outs[b].n)) return ATTN_ERR_ALIAS;
         for (int b = 0; b < 7; ++b)
             if (overlaps(outs[a].p, outs[a].n, ins[b].p, ins[b].n)) return ATTN_ERR_ALIAS;
+    }
+    if (!tensor_core_head(d)) {
+        // fp32, and bf16 heads the tensor-core backward does not take: the CUDA cores
+        attn::BwdSimtProblem p;
+        p.q = Q;
+        p.k = K;
+        p.v = V;
+        p.out = out;
+        p.dout = dout;
+        p.lse = lse;
+        p.key_lengths = (mask_kind & ATTN_MASK_KEY_PADDING) ? key_lengths : nullptr;
+        p.dq = dQ;
+        p.dk = dK;
+        p.dv = dV;
+        p.workspace = workspace;
+        p.B = d.B;
+        p.h = d.h;
+        p.m = d.m;
+        p.n = d.n;
+        p.d = d.d_k;
+        p.mask_kind = mask_kind;
+        p.scale = resolve_scale(scale, d.d_k);
+        p.bf16 = d.dtype == ATTN_BF16;
+        return attn::launch_bwd_simt(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
     }
     attn::BwdProblem p;
     p.q = Q;

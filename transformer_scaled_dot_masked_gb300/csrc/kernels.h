@@ -74,6 +74,22 @@ struct BwdProblem {
     float scale;
 };
 
+// CUDA-core backward (fp32 arithmetic; bf16 or fp32 tensors; any d up to 128): a rows
+// pass (D and dQ) and a keys pass (dK and dV).  Workspace: D, B * h * m floats.
+struct BwdSimtProblem {
+    const void *q, *k, *v, *out, *dout; // [B][h][rows][d]
+    const float *lse;                   // [B][h][m], natural log
+    const int32_t *key_lengths;         // device [B]; nullptr unless key padding
+    void *dq, *dk, *dv;
+    void *workspace;                    // bwd_simt_workspace_bytes(B, h, m), 4-byte aligned
+    int B, h, m, n, d;
+    int mask_kind;
+    float scale;
+    bool bf16;
+};
+size_t bwd_simt_workspace_bytes(int B, int h, int m);
+cudaError_t launch_bwd_simt(const BwdSimtProblem &p, cudaStream_t stream);
+
 // Workspace of the backward: the fp32 dQ accumulator and the per-row table.
 size_t bwd_workspace_bytes(int B, int h, int m);
 cudaError_t launch_bwd(const BwdProblem &p, cudaStream_t stream);
