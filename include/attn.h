@@ -387,7 +387,8 @@ typedef struct {
     int32_t m;       /* query positions */
     int32_t n;       /* key/value positions */
     int32_t d_model; /* model width, a multiple of 128 */
-    int32_t d_k;     /* head width: 64 or 128 (0 is read as 64); the pages' d_model / h */
+    int32_t d_k;     /* head width: a multiple of 8 up to 64, or 128 (0 is read as 64); the
+                        pages' d_model / h */
 } attn_mha_dims;
 
 /* Bytes of device workspace attn_mha_fwd needs (host only, no CUDA call); 0 if
@@ -411,15 +412,19 @@ size_t attn_mha_workspace_size(const attn_mha_dims *dims);
  *   Wo   [h * d_k][d_model]: head i's output multiplies rows i d_k .. (i + 1) d_k - 1
  *   out  [B][m][d_model]
  *   workspace  attn_mha_workspace_size(dims) bytes (Q, K, V and the heads'
- *              outputs in [B][h][len][d_k]), 256-byte aligned, any contents
- * Five kernels are enqueued: three projections into the head-split layout
- * (tcgen05 GEMMs whose epilogues write each 64-column block as one head), the
- * attention, and the output projection, which reads the heads' outputs as its K
- * dimension directly (the concatenation costs no copy).
+ *              outputs in [B][h][len][d_k], and for narrow heads the concatenated
+ *              projections), 256-byte aligned, any contents
+ * With d_k 64 or 128, three kernels are enqueued: the three projections into the
+ * head-split layout (one tcgen05 GEMM launch whose epilogue writes each 64-column
+ * block into its head), the attention, and the output projection, which reads the
+ * heads' outputs as its K dimension directly (the concatenation costs no copy).
+ * Narrower heads (the model-variant table's 16 and 32) take the projections into
+ * the concatenated layout [B][len][h * d_k], copy them into heads and the heads'
+ * outputs back (memory-bound copies), with the attention in between.
  *
  * Errors: NULL pointers (ATTN_ERR_NULL), bad shapes or h * d_k or d_model not
- * multiples of 128, causal with m != n (ATTN_ERR_SHAPE), d_k other than 64 or 128
- * (ATTN_ERR_DTYPE), mask bits other than
+ * multiples of 128, causal with m != n (ATTN_ERR_SHAPE), d_k not a multiple of 8 up
+ * to 64 and not 128 (ATTN_ERR_DTYPE), mask bits other than
  * KEY_PADDING and CAUSAL (ATTN_ERR_MASK), unaligned pointers (ATTN_ERR_ALIGN),
  * bad scale (ATTN_ERR_VALUE), a workspace too small (ATTN_ERR_SHAPE), out or the
  * workspace overlapping an input or each other (ATTN_ERR_ALIAS), CUDA errors.

@@ -279,7 +279,10 @@ def test_mha_head_width():
     assert re.findall(r"int32_t (\w+);", fields) == [f for f, _ in N.MhaDims._fields_]
     assert N.mha_workspace_size(2, 2, 8, 8, 128, 128) == 2 * N.mha_workspace_size(2, 2, 8, 8, 128, 64)
     assert N.mha_workspace_size(2, 2, 8, 8, 128, 0) == N.mha_workspace_size(2, 2, 8, 8, 128, 64)  # 0 reads as 64
-    assert N.mha_workspace_size(2, 2, 8, 8, 128, 32) == 0                                        # not built
+    # narrow heads: Q, K, V, O split plus the three concatenated products (O merges into Q's)
+    assert N.mha_workspace_size(2, 4, 8, 8, 128, 32) == 7 * N.mha_workspace_size(2, 2, 8, 8, 128, 64) // 4
+    assert N.mha_workspace_size(2, 2, 8, 8, 128, 32) == 0                                        # h * d_k = 64
+    assert N.mha_workspace_size(2, 8, 8, 8, 128, 20) == 0                                        # not a multiple of 8
     assert N.mha_workspace_size(2, 1, 8, 8, 128, 128) > 0                                        # h * 128
     d = N.MhaDims(2, 2, 8, 8, 128, 96)
     assert N.lib.attn_mha_fwd(A, B_, C, 0x7000000, 0x8000000, 0x9000000, None, 0, ctypes.c_float(0.125), O,

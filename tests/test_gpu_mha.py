@@ -82,6 +82,33 @@ def test_mha_wide_heads(orc, name, B, h, m, n, dm, mask, selfattn, lengths):
     assert np.abs(got - ref).max() <= 2e-2, report(got, ref, 2e-2)
 
 
+NARROW_CASES = [
+    # the model-variant table's narrower heads at d_model 512: h = 16 with d_k = 32 and
+    # h = 32 with d_k = 16 (projections through the concatenated layout), and d_k = 48
+    ("h16_d32_encoder_padding", 2, 16, 100, 100, 512, MASK_KEY_PADDING, True, (10, 100)),
+    ("h32_d16_decoder_causal", 2, 32, 130, 130, 512, MASK_CAUSAL, True, None),
+    ("h16_d32_cross_padding", 2, 16, 128, 200, 512, MASK_KEY_PADDING, False, (40, 200)),
+    ("h8_d48_long", 1, 8, 300, 300, 384, MASK_NONE, True, None),
+]
+
+
+@pytest.mark.parametrize("name,B,h,m,n,dm,mask,selfattn,lengths", NARROW_CASES, ids=[c[0] for c in NARROW_CASES])
+def test_mha_narrow_heads(orc, name, B, h, m, n, dm, mask, selfattn, lengths):
+    dk = int(name.split("_d")[1].split("_")[0])
+    xq, xkv, wq, wk, wv, wo = draw_mha(B, h, m, n, dm, seed=85, self_attention=selfattn, d_k=dk)
+    lens = np.full(B, n, dtype=np.int32)
+    if lengths is not None:
+        lens = np.random.default_rng(86).integers(lengths[0], lengths[1] + 1, size=B).astype(np.int32)
+    out = attn.attn_mha_fwd(dev(xq), dev(xkv), dev(wq), dev(wk), dev(wv), dev(wo), h,
+                            torch.from_numpy(lens).cuda(), mask)  # default scale: 1/sqrt(d_k)
+    torch.cuda.synchronize()
+    st, info = attn.device_status()
+    assert st == 0, f"device status {st} (info {info})"
+    ref = mha.mha_fwd(orc, xq, xkv, wq, wk, wv, wo, h, lens, mask, dk ** -0.5)
+    got = as_f64(out)
+    assert np.abs(got - ref).max() <= 2e-2, report(got, ref, 2e-2)
+
+
 def test_mha_benchmarked_size(orc):
     """The benchmarked call at full size and with its inputs: B32 sentences of 256
     positions, d_model 1024, h 16, key padding with lengths in [128, 256] (the same

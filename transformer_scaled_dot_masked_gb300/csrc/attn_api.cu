@@ -446,7 +446,9 @@ int mha_dk(const attn_mha_dims &d) { return d.d_k == 0 ? 64 : d.d_k; }
 attn_status validate_mha_dims(const attn_mha_dims *d)
 {
     if (d == nullptr) return ATTN_ERR_NULL;
-    if (d->d_k != 0 && d->d_k != 64 && d->d_k != 128) return ATTN_ERR_DTYPE;
+    // 64 and 128 wide heads are whole 64-column blocks of the projections; narrower
+    // ones (a multiple of 8 below 64) go through the concatenated layout
+    if (d->d_k != 0 && d->d_k != 128 && !(d->d_k % 8 == 0 && d->d_k >= 8 && d->d_k <= 64)) return ATTN_ERR_DTYPE;
     if (d->B < 1 || d->h < 1 || d->m < 1 || d->n < 1 || d->d_model < 1) return ATTN_ERR_SHAPE;
     if (d->B > 65535 || d->h > 65535 || (static_cast<int64_t>(d->h) * mha_dk(*d)) % 128 != 0 ||
         d->d_model % 128 != 0)
@@ -457,8 +459,15 @@ attn_status validate_mha_dims(const attn_mha_dims *d)
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct MhaLayout {
-    size_t q, k, v, o, total; // byte offsets in the workspace
+    size_t q, k, v, o;    // byte offsets in the workspace: the head-split Q, K, V, O
+    size_t qc, kc, vc;    // narrow heads: the concatenated projections (the heads' output reuses qc)
+    size_t total;
 };
+
+// Heads whose width is a whole number of 64-column blocks go straight from the
+// projections' epilogues into the head-split layout; narrower heads go through the
+// concatenated layout [B][len][h * d_k] and a copy.
+bool mha_direct(const attn_mha_dims &d) { return mha_dk(d) % 64 == 0; }
 
 MhaLayout mha_layout(const attn_mha_dims &d)
 {
@@ -470,6 +479,13 @@ MhaLayout mha_layout(const attn_mha_dims &d)
     L.v = L.k + align256(BH * d.n * dk * 2);
     L.o = L.v + align256(BH * d.n * dk * 2);
     L.total = L.o + align256(BH * d.m * dk * 2);
+    L.qc = L.kc = L.vc = 0;
+    if (!mha_direct(d)) {
+        L.qc = L.total;
+        L.kc = L.qc + align256(BH * d.m * dk * 2);
+        L.vc = L.kc + align256(BH * d.n * dk * 2);
+        L.total = L.vc + align256(BH * d.n * dk * 2);
+    }
     return L;
 }
 } // namespace
@@ -516,6 +532,51 @@ attn_status attn_mha_fwd(const void *Xq, const void *Xkv, const void *Wq, const 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     void *Q = ws + L.q, *K = ws + L.k, *V = ws + L.v, *O = ws + L.o;
+    if (!mha_direct(d)) {
+        // Narrow heads: the projections as plain products into [B][len][h * d_k] (one
+        // "head" as wide as the product), split into heads, attention, heads merged
+        // back (into the Q product's space, free by then), the output projection.
+        void *Qc = ws + L.qc, *Kc = ws + L.kc, *Vc = ws + L.vc;
+        attn::ProjProblem in3[3];
+        const struct {
+            const void *x, *w;
+            void *o;
+            int L;
+        } prods[3] = {{Xq, Wq, Qc, d.m}, {Xkv, Wk, Kc, d.n}, {Xkv, Wv, Vc, d.n}};
+        for (int i = 0; i < 3; ++i) {
+            in3[i].mode = attn::kProjIn;
+            in3[i].a = prods[i].x;
+            in3[i].w = prods[i].w;
+            in3[i].out = prods[i].o;
+            in3[i].B = d.B;
+            in3[i].h = 1;
+            in3[i].L = prods[i].L;
+            in3[i].K = d.d_model;
+            in3[i].N = d.h * dk;
+            in3[i].dk = d.h * dk;
+        }
+        if (attn::launch_proj_multi(in3, 3, s) != cudaSuccess) return ATTN_ERR_CUDA;
+        if (attn::launch_heads_copy(Qc, Q, d.B, d.m, d.h, dk, true, s) != cudaSuccess ||
+            attn::launch_heads_copy(Kc, K, d.B, d.n, d.h, dk, true, s) != cudaSuccess ||
+            attn::launch_heads_copy(Vc, V, d.B, d.n, d.h, dk, true, s) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        attn_dims ad{d.B, d.h, d.m, d.n, dk, ATTN_BF16};
+        st = run(Q, K, V, key_lengths, mask_kind, scale, O, &ad, stream, ATTN_KERNEL_AUTO, nullptr);
+        if (st != ATTN_OK) return st;
+        if (attn::launch_heads_copy(O, Qc, d.B, d.m, d.h, dk, false, s) != cudaSuccess) return ATTN_ERR_CUDA;
+        attn::ProjProblem po;
+        po.mode = attn::kProjIn;
+        po.a = Qc;
+        po.w = Wo;
+        po.out = out;
+        po.B = d.B;
+        po.h = 1;
+        po.L = d.m;
+        po.K = d.h * dk;
+        po.N = d.d_model;
+        po.dk = d.d_model;
+        return attn::launch_proj(po, s) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    }
     attn::ProjProblem pp;
     pp.B = d.B;
     pp.h = d.h;

@@ -355,7 +355,8 @@ cudaError_t launch_proj_multi(const ProjProblem *pps, int count, cudaStream_t st
     ProjParams p;
     p.mode = p0.mode;
     p.h = p0.h;
-    if (p0.dk != 64 && p0.dk != 128) return cudaErrorInvalidValue;
+    // dk: the head width, or for a plain product (h = 1) the whole output width
+    if (p0.dk % 64 != 0 || p0.dk <= 0 || (p0.mode == kProjIn ? p0.N : p0.K) % p0.dk != 0) return cudaErrorInvalidValue;
     p.K = p0.K;
     p.N = p0.N;
     p.B = p0.B;
@@ -414,6 +415,39 @@ cudaError_t launch_proj_multi(const ProjProblem *pps, int count, cudaStream_t st
 }
 
 cudaError_t launch_proj(const ProjProblem &pp, cudaStream_t stream) { return launch_proj_multi(&pp, 1, stream); }
+
+namespace {
+
+// Between the concatenated layout [B][L][h][dk] and the head-split layout [B][h][L][dk],
+// 16 bytes per thread (dk a multiple of 8): chunk c of head hh of row t of batch b.
+__global__ void attn_heads_copy_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst, int L, int h,
+                                       int dk8, size_t total, int split)
+{
+    const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= total) return;
+    const size_t c = idx % dk8;
+    size_t rest = idx / dk8;
+    const size_t hh = rest % h;
+    rest /= h;
+    const size_t t = rest % L, b = rest / L;
+    const size_t heads = ((b * h + hh) * L + t) * dk8 + c; // idx is the concatenated position
+    if (split) dst[heads] = src[idx];
+    else dst[idx] = src[heads];
+}
+
+} // namespace
+
+cudaError_t launch_heads_copy(const void *src, void *dst, int B, int L, int h, int dk, bool split,
+                              cudaStream_t stream)
+{
+    if (dk % 8 != 0 || dk <= 0) return cudaErrorInvalidValue;
+    const size_t total = static_cast<size_t>(B) * L * h * (dk / 8);
+    if (total == 0) return cudaSuccess;
+    const unsigned blocks = static_cast<unsigned>((total + 255) / 256);
+    attn_heads_copy_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), L,
+                                                        h, dk / 8, total, split ? 1 : 0);
+    return cudaGetLastError();
+}
 
 cudaError_t proj_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint32_t *info)
 {

@@ -113,6 +113,9 @@ cudaError_t launch_proj(const ProjProblem &p, cudaStream_t stream);
 // Up to three products of one shape (mode, B, h, K, N; L may differ) in one launch.
 cudaError_t launch_proj_multi(const ProjProblem *p, int count, cudaStream_t stream);
 cudaError_t proj_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint32_t *info);
+// bf16 [B][L][h][dk] (concatenated heads) to [B][h][L][dk] (split) or back; dk a multiple of 8.
+cudaError_t launch_heads_copy(const void *src, void *dst, int B, int L, int h, int dk, bool split,
+                              cudaStream_t stream);
 
 // Device status word of the flash kernel (bounded waits that gave up).
 cudaError_t flash_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint32_t *info);
