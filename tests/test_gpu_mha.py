@@ -1,7 +1,7 @@
 """Multi-head attention with projections (attn_mha_fwd) against the fp64 MultiHead oracle.
 
 Tolerance 2e-2 absolute, from the arithmetic: Q, K, V and the heads' outputs are
-rounded to bf16 (2^-9 relative each) and the attention stays within its own
+rounded to bf16 (2^-8 relative each) and the attention stays within its own
 1e-2 bar; W^O is drawn with variance 1/(h*64), so the output projection carries
 the per-feature errors over with unit gain (they add in quadrature over its
 h*64 inputs), plus the output's own bf16 rounding.

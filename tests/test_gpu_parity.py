@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import transformer_scaled_dot_masked_gb300 as attn
-from workloads import WORKLOADS, MASK_CAUSAL, MASK_KEY_PADDING, MASK_NONE, Workload, draw, sample_rows
+from workloads import WORKLOADS, MASK_CAUSAL, MASK_KEY_PADDING, MASK_NONE, Workload, draw, round_to_bf16_bits, sample_rows
 
 from gpu_helpers import as_f64, report, rounding_bound, run, to_device, tol_for
 
@@ -222,15 +222,22 @@ def test_score_jumps_narrow_heads(orc, name, B, h, m, n, mask, lengths, soft, ha
 @pytest.mark.parametrize("name,B,h,m,n,mask,lengths,soft,hard", JUMP_CASES, ids=[c[0] for c in JUMP_CASES])
 def test_score_jumps_wide_heads(orc, name, B, h, m, n, mask, lengths, soft, hard):
     """The score jumps with d_k = 128 on the wide kernel: its fixed per-row reference,
-    the power-of-two rescale and the score recomputation (of 128-wide rows)."""
+    the power-of-two rescale and the score recomputation (of 128-wide rows).  Its row
+    sum adds the weights as rounded, so every output is a weighted mean of exactly
+    the weights applied.  Standard normal values: 1e-2 plus only the output's own
+    half-ulp where |out| >= 4, on every row.  Values of standard deviation 4: the
+    same bound on the rows dominated by one key (the jumped rows); on rows that two
+    or three keys share, each weight's own bf16 rounding (2^-8 relative) moves the
+    mean by up to 2^-8 times the spread of their values, which wider values push
+    past 1e-2."""
     w, inp = jump_inputs(name, B, h, m, n, mask, lengths, soft, hard, d=128)
-    rng = np.random.default_rng(7)
-    vals = rng.uniform(-1.0, 1.0, size=inp.v.shape).astype(np.float32)
-    inp.v[...] = (vals.view(np.uint32) >> 16).astype(np.uint16)
-    ref = orc.attn_fwd(inp.q, inp.k, inp.v, inp.key_lengths, w.mask, w.scale)
-    got = as_f64(run(inp, K_WIDE))
-    assert np.isfinite(got).all()
-    assert np.abs(got - ref).max() <= 1e-2, report(got, ref, 1e-2)
+    for sigma, rows in ((1.0, slice(None)), (4.0, soft + hard)):
+        v = sigma * np.random.default_rng(7).standard_normal(inp.v.shape).astype(np.float32)
+        inp.v[...] = round_to_bf16_bits(v)
+        ref = orc.attn_fwd(inp.q, inp.k, inp.v, inp.key_lengths, w.mask, w.scale)[:, :, rows]
+        got = as_f64(run(inp, K_WIDE))[:, :, rows]
+        assert np.isfinite(got).all()
+        assert (np.abs(got - ref) - rounding_bound(ref)).max() <= 0, f"sd {sigma}: " + report(got, ref, 1e-2)
 
 
 @pytest.mark.parametrize("name,B,h,m,n,mask,lengths,soft,hard", JUMP_CASES, ids=[c[0] for c in JUMP_CASES])
@@ -248,6 +255,24 @@ def test_peaked_rows_error_bound(orc, name, B, h, m, n, mask, lengths, soft, har
         assert np.isfinite(got).all()
         excess = np.abs(got - ref) - bound
         assert excess.max() <= 0, f"kernel {kern}: " + report(got, ref, float(bound.max()))
+
+
+@pytest.mark.parametrize("name,B,h,m,n,mask,lengths,soft,hard", JUMP_CASES, ids=[c[0] for c in JUMP_CASES])
+def test_jumped_rows_are_weighted_means(orc, name, B, h, m, n, mask, lengths, soft, hard):
+    """The rows whose scores jump, each dominated by one key of a later tile, with
+    values of standard deviation 4: the tile that rescales (or recomputes) its
+    weights adds them to the row sum as rounded, so these outputs are weighted means
+    of exactly the weights applied (had the sum missed the dominant weight's
+    rounding, the error would reach 2^-8 * 16 = 0.06): 1e-2 plus the output's own
+    half-ulp where |out| >= 4."""
+    w, inp = jump_inputs(name, B, h, m, n, mask, lengths, soft, hard)
+    v = 4.0 * np.random.default_rng(8).standard_normal(inp.v.shape).astype(np.float32)
+    inp.v[...] = round_to_bf16_bits(v)
+    ref = orc.attn_fwd(inp.q, inp.k, inp.v, inp.key_lengths, w.mask, w.scale)[:, :, soft + hard]
+    for kern in kernels_for(w):
+        got = as_f64(run(inp, kern))[:, :, soft + hard]
+        assert np.isfinite(got).all()
+        assert (np.abs(got - ref) - rounding_bound(ref)).max() <= 0, f"kernel {kern}: " + report(got, ref, 1e-2)
 
 
 # ---------------------------------------------------------------- invariants

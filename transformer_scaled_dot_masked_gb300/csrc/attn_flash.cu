@@ -585,7 +585,7 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
             continue;
         }
         float m_run = -CUDART_INF_F; // running max, log2 units, as used for the exponentials
-        float l_run = 0.f;           // running sum of exponentials relative to m_run
+        float l_run = 0.f;           // running sum of the weights relative to m_run
         for (int j = kv_lo; j < n_kv; ++j) {
             ok = warp_all(wait_bar(&sm.s_full[slot], s_cnt & 1, ab, kSiteSmSFull));
             if (!ok) break;
@@ -649,17 +649,12 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
             uint32_t pk[kBN / 2];
             float tile_sum = weights_bf16(x, prescaled, sl2, m_use, pk);
             if (!first && !(tile_sum <= kFastSumLimit)) {
+                float f = 1.f;
                 if (tile_sum < CUDART_INF_F) {
-                    // Finite but large: scale the weights by 2^-k (k an integer, so the
-                    // bf16 values scale exactly) and move the reference up by k.
+                    // Finite but large: scale the weights by f = 2^-k (k an integer, so
+                    // the bf16 values scale exactly) and move the reference up by k.
                     const int k = ((__float_as_int(tile_sum) >> 23) & 0xff) - 127 - 7; // 8..120
-                    const float f = __int_as_float((127 - k) << 23);                   // 2^-k
-#pragma unroll
-                    for (int c2 = 0; c2 < kBN / 2; ++c2) {
-                        const float lo = __uint_as_float(pk[c2] << 16), hi = __uint_as_float(pk[c2] & 0xffff0000u);
-                        pk[c2] = pack_bf16x2(lo * f, hi * f);
-                    }
-                    tile_sum *= f;
+                    f = __int_as_float((127 - k) << 23);                               // 2^-k
                     alpha = f;
                     m_use = m_run + static_cast<float>(k);
                     grow = true;
@@ -670,8 +665,13 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
                     // and take their max.
                     recompute_scores<kNarrow>(p, bh, i, key0, cnt_lo, cnt, x);
                     move_reference(x, true, sl2, m_run, m_use, alpha, grow);
-                    tile_sum = weights_bf16(x, true, sl2, m_use, pk);
+                    weights_bf16(x, true, sl2, m_use, pk);
                 }
+                // Such a tile holds a key far above the row's reference, likely the
+                // row's dominant one: its weights enter the row sum as rounded, the
+                // values P V applies (the log-sum-exp then carries their rounding,
+                // at most 2^-8 relative, on these rows alone).
+                tile_sum = scale_and_sum(pk, f);
             }
             if (j > kv_lo) {
                 // P and O are still in use by the previous P V until it completes;
@@ -716,7 +716,7 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
         tc_fence_before();
         mbar_arrive(&sm.o_free[slot]);
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        if (p.lse != nullptr && i < p.m) // weights are exp2(x - m_run) / l_run: lse = (m_run + log2 l_run) ln 2
+        if (p.lse != nullptr && i < p.m) // weights are exp2(x - m_run) / l: lse = (m_run + log2 l) ln 2
             p.lse[static_cast<size_t>(bh) * p.m + i] =
                 l_run > 0.f ? (m_run + __log2f(l_run)) * 0.6931471805599453f : -CUDART_INF_F;
         // Output: each thread writes its row of O / l into this slot's staging tile in

@@ -385,7 +385,7 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 klo = i - p.window;
             }
             float m_run = -CUDART_INF_F; // running reference, log2 units, as used for the exponentials
-            float l_run = 0.f;           // running sum of exponentials relative to m_run
+            float l_run = 0.f;           // running sum of the rounded weights relative to m_run
             bool ok = true;
             for (int jj = 0; jj < n_s && ok; ++jj) {
                 ok = warp_all(wait_scores(&sm.s_full[s], jj & 1, ab, kSiteSmSFull));
@@ -429,7 +429,9 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const bool first = m_run == -CUDART_INF_F;
                 if (first) move_reference(x, prescaled, sl2, m_run, m_use, alpha, grow);
                 uint32_t pk[kBN / 2];
-                float tile_sum = weights_bf16(x, prescaled, sl2, m_use, pk);
+                // the sum of the weights as rounded: the output is a weighted mean of
+                // exactly the weights P V applies
+                float tile_sum = weights_bf16_rounded(x, prescaled, sl2, m_use, pk);
                 if (!first && !(tile_sum <= kFastSumLimit)) {
                     if (tile_sum < CUDART_INF_F) {
                         // finite but large: scale the weights by 2^-k (k an integer, so the
@@ -451,7 +453,7 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         // K, already scaled and masked, and take their max
                         recompute_scores(p, bh, i, key0, cnt_lo, cnt, x);
                         move_reference(x, true, sl2, m_run, m_use, alpha, grow);
-                        tile_sum = weights_bf16(x, true, sl2, m_use, pk);
+                        tile_sum = weights_bf16_rounded(x, true, sl2, m_use, pk);
                     }
                 }
                 if (jj > 0 && __any_sync(0xffffffffu, grow)) {
@@ -480,7 +482,9 @@ attn_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             if (ok) {
                 tc_fence_after();
                 const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-                if (p.lse != nullptr && i < p.m) // weights are exp2(x - m_run) / l: lse = (m_run + log2 l) ln 2
+                // weights are exp2(x - m_run) / l: lse = (m_run + log2 l) ln 2 (l sums the
+                // rounded weights: within 2^-8 relative of the sum before rounding)
+                if (p.lse != nullptr && i < p.m)
                     p.lse[static_cast<size_t>(bh) * p.m + i] =
                         l_run > 0.f ? (m_run + __log2f(l_run)) * 0.6931471805599453f : -CUDART_INF_F;
                 // Output: each thread writes its row of O / l into the slot's Q tile, free

@@ -69,4 +69,51 @@ __device__ __forceinline__ float weights_bf16(const float (&x)[kTileKeys], bool 
     return (s0 + s1) + (s2 + s3);
 }
 
+// acc0 += the bf16 in the low half of pk, acc1 += the one in the high half (exact
+// bf16 values widened to fp32 inside the add).
+__device__ __forceinline__ void add_bf16_pair(float &acc0, float &acc1, uint32_t pk)
+{
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+        : "+f"(acc0), "+f"(acc1) : "r"(pk));
+}
+
+// The same weights, returning the sum of the weights as rounded: the values the
+// P V product applies, so that dividing by it makes the output a weighted mean of
+// exactly those.
+__device__ __forceinline__ float weights_bf16_rounded(const float (&x)[kTileKeys], bool prescaled, float sl2,
+                                                      float m_use, uint32_t (&pk)[kTileKeys / 2])
+{
+    const float m_sub = (m_use == -CUDART_INF_F) ? 0.f : m_use;
+    const uint64_t mul2 = prescaled ? f2(1.f, 1.f) : f2(sl2, sl2);
+    const uint64_t sub2 = f2(-m_sub, -m_sub);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int c2 = 0; c2 < kTileKeys / 2; ++c2) {
+        const int c = 2 * c2;
+        float a0, a1;
+        unf2(fma2(f2(x[c], x[c + 1]), mul2, sub2), a0, a1);
+        const float e0 = ex2(a0), e1 = ex2(a1);
+        pk[c2] = pack_bf16x2(e0, e1);
+        add_bf16_pair(acc[(2 * c2) & 3], acc[(2 * c2 + 1) & 3], pk[c2]);
+    }
+    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+}
+
+// Scales one key tile's packed bf16 weights by f (a power of two, so exactly) and
+// returns the sum of the scaled weights as rounded.
+__device__ __forceinline__ float scale_and_sum(uint32_t (&pk)[kTileKeys / 2], float f)
+{
+    uint64_t acc2 = f2(0.f, 0.f);
+#pragma unroll
+    for (int c2 = 0; c2 < kTileKeys / 2; ++c2) {
+        const float lo = __uint_as_float(pk[c2] << 16) * f, hi = __uint_as_float(pk[c2] & 0xffff0000u) * f;
+        pk[c2] = pack_bf16x2(lo, hi);
+        acc2 = add2(acc2, f2(lo, hi));
+    }
+    float s0, s1;
+    unf2(acc2, s0, s1);
+    return s0 + s1;
+}
+
 } // namespace attn
