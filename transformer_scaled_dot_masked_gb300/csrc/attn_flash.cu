@@ -593,7 +593,7 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
             tc_fence_after();
             uint32_t sr[kBN];
 #pragma unroll
-            for (int c = 0; c < kBN / 32; ++c) tmem_ld32(t_s + c * 32, sr + c * 32);
+            tmem_ld128(t_s, sr);
             tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < kBN / 32; ++c) reg_fence32(sr + c * 32);
@@ -708,8 +708,7 @@ __device__ __forceinline__ void softmax_role(SharedStorage &sm, const FlashParam
         ++pv_cnt;
         tc_fence_after();
         uint32_t orr[kD];
-        tmem_ld32(t_o, orr);
-        tmem_ld32(t_o + 32, orr + 32);
+        tmem_ld64(t_o, orr);
         tmem_wait_ld();
         reg_fence32(orr);
         reg_fence32(orr + 32);

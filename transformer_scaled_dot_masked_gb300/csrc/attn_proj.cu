@@ -291,8 +291,7 @@ attn_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
             const int blocks = id.ncols / 64;
             for (int q = 0; q < blocks; ++q, ++stored) {
                 uint32_t v[64];
-                tmem_ld32(tmem + lane_base + 256 * a + 64 * q, v);
-                tmem_ld32(tmem + lane_base + 256 * a + 64 * q + 32, v + 32);
+                tmem_ld64(tmem + lane_base + 256 * a + 64 * q, v);
                 tmem_wait_ld();
                 reg_fence32(v);
                 reg_fence32(v + 32);
