@@ -96,9 +96,9 @@ typedef enum {
     ATTN_KERNEL_SIMT = 3,  /* CUDA-core fp32 kernel (fp32 or bf16, d_k <= 128) */
     ATTN_KERNEL_WIDE = 4,  /* tcgen05/TMA kernel for d_k == 128 (bf16): two 128-row query tiles of one
                               head per CTA, or two heads per CTA when m <= 128 and n <= 128 */
-    ATTN_KERNEL_RESIDENT = 5 /* tcgen05/TMA kernel for short sequences: one head per CTA with its Q, K
-                                and V resident, exact two-pass softmax per row (bf16, d_k as FLASH,
-                                m <= 128, n <= 192) */
+    ATTN_KERNEL_RESIDENT = 5 /* tcgen05/TMA kernel for short key sequences: one 128-row query tile of
+                                one head per CTA with its Q, K and V resident, exact two-pass softmax
+                                per row (bf16, d_k as FLASH, n <= 256, any m) */
 } attn_kernel;
 
 typedef struct {
@@ -135,7 +135,7 @@ typedef struct {
  * finite: non-finite values propagate through the arithmetic as IEEE rules
  * dictate.  Kernel choice: bf16 with d_k a multiple of 8 up to 64 runs on tensor
  * cores, narrower heads zero-padded to 64 inside the kernel (ATTN_KERNEL_RESIDENT
- * when m <= 128 and n <= 192, ATTN_KERNEL_SHORT when m <= 128 and n > 192, else
+ * when n <= 256, ATTN_KERNEL_SHORT when m <= 128 and n > 256, else
  * ATTN_KERNEL_FLASH); bf16 with d_k == 128 on ATTN_KERNEL_WIDE (tensor cores);
  * everything else runs ATTN_KERNEL_SIMT.  The resident kernel is launched as a
  * programmatic dependent of the kernel before it on the stream: its launch and
@@ -460,7 +460,7 @@ attn_status attn_device_status(void *stream, int32_t *info);
  * test check the abort path without any fault on the GPU.
  *
  * Arguments as attn_fwd; the dims must be ones the resident kernel runs (bf16, d_k a
- * multiple of 8 up to 64, m <= 128, n <= 192; ATTN_ERR_UNSUPPORTED otherwise);
+ * multiple of 8 up to 64, n <= 256; ATTN_ERR_UNSUPPORTED otherwise);
  * wait_ns in [100000, 2000000000] (ATTN_ERR_VALUE otherwise).
  */
 attn_status attn_test_withheld_arrival(const void *Q, const void *K, const void *V,

@@ -55,9 +55,12 @@ def test_kernel_selection():
     assert attn.select_kernel(64, 8, 100, 100, 64, bf, 1) == N.KERNEL_RESIDENT
     assert attn.select_kernel(32, 16, 128, 160, 64, bf, 1) == N.KERNEL_RESIDENT
     assert attn.select_kernel(32, 8, 128, 128, 64, bf, 2) == N.KERNEL_RESIDENT
-    assert attn.select_kernel(2, 2, 128, 192, 64, bf, 0) == N.KERNEL_RESIDENT  # the most keys it holds
-    assert attn.select_kernel(2, 2, 128, 193, 64, bf, 0) == N.KERNEL_SHORT
-    assert attn.select_kernel(2, 2, 129, 100, 64, bf, 0) == N.KERNEL_FLASH
+    assert attn.select_kernel(2, 2, 128, 192, 64, bf, 0) == N.KERNEL_RESIDENT
+    assert attn.select_kernel(2, 2, 128, 256, 64, bf, 0) == N.KERNEL_RESIDENT  # the most keys it holds
+    assert attn.select_kernel(2, 2, 128, 257, 64, bf, 0) == N.KERNEL_SHORT
+    assert attn.select_kernel(2, 2, 129, 100, 64, bf, 0) == N.KERNEL_RESIDENT  # one CTA per query tile
+    assert attn.select_kernel(32, 16, 256, 256, 64, bf, 1) == N.KERNEL_RESIDENT
+    assert attn.select_kernel(2, 2, 300, 257, 64, bf, 0) == N.KERNEL_FLASH
     assert attn.select_kernel(4, 16, 8192, 8192, 64, bf, 2) == N.KERNEL_FLASH
     assert attn.select_kernel(1, 1, 16, 16, 64, f32, 0) == N.KERNEL_SIMT
     # bf16 heads narrower than 64 (multiples of 8) run zero-padded on tensor cores
@@ -109,8 +112,7 @@ def test_rejects_unsupported_kernel_choice():
     assert _call(dims=(2, 2, 8, 8, 128, 0), kernel=N.KERNEL_FLASH) == 6  # wider than 64
     assert _call(dims=(2, 2, 8, 8, 64, 0), kernel=N.KERNEL_WIDE) == 6    # the wide kernel: d_k 128 only
     assert _call(dims=(2, 2, 8, 8, 128, 1), kernel=N.KERNEL_WIDE) == 6   # and bf16 only
-    assert _call(dims=(2, 2, 8, 193, 64, 0), kernel=N.KERNEL_RESIDENT) == 6  # more keys than it holds
-    assert _call(dims=(2, 2, 129, 8, 64, 0), kernel=N.KERNEL_RESIDENT) == 6  # more than 128 queries
+    assert _call(dims=(2, 2, 8, 257, 64, 0), kernel=N.KERNEL_RESIDENT) == 6  # more keys than it holds
     assert _call(dims=(2, 2, 8, 8, 64, 1), kernel=N.KERNEL_RESIDENT) == 6    # fp32
     assert _call(dims=(2, 2, 8, 8, 20, 0), kernel=N.KERNEL_RESIDENT) == 6    # d_k not a multiple of 8
     assert _call(kernel=17) == 6

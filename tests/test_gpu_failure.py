@@ -55,7 +55,7 @@ def test_wait_runs_out_and_context_survives(cfg, shape):
 
 
 def test_hook_rejects_what_it_cannot_run():
-    w = WORKLOADS[5].with_(B=1, h=1, m=256, n=256)  # more than 128 queries: not the resident kernel
+    w = WORKLOADS[5].with_(B=1, h=1, m=300, n=300)  # more than 256 keys: not the resident kernel
     inp = draw(w)
     out = torch.empty((w.B, w.h, w.m, w.d), dtype=torch.bfloat16, device="cuda")
     assert _withheld(inp, out, 20_000_000) == 6  # ATTN_ERR_UNSUPPORTED

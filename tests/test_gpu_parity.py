@@ -20,7 +20,7 @@ K_WIDE, K_RESIDENT = attn.KERNEL_WIDE, attn.KERNEL_RESIDENT
 
 
 def resident_fits(m, n, d=64, dtype="bf16"):
-    return dtype == "bf16" and d % 8 == 0 and d <= 64 and m <= 128 and n <= 192
+    return dtype == "bf16" and d % 8 == 0 and d <= 64 and n <= 256
 
 
 def auto_for(m, n):
@@ -102,6 +102,15 @@ EDGE = [
     ("resident_single_query", 3, 2, 1, 192, MASK_KEY_PADDING, (0, 192)),
     ("resident_causal_padding", 3, 2, 128, 128, MASK_CAUSAL | MASK_KEY_PADDING, (0, 128)),
     ("resident_17_keys", 2, 3, 33, 17, MASK_NONE, None),
+    # above 192 keys (O over the last two chunks of S, their weights held first): the
+    # most keys it holds, one chunk past 192 (one held chunk), a ragged box
+    ("resident_256_keys", 2, 3, 100, 256, MASK_KEY_PADDING, (0, 256)),
+    ("resident_208_keys", 2, 2, 128, 208, MASK_NONE, None),
+    ("resident_250_keys_one_query", 3, 2, 1, 250, MASK_KEY_PADDING, (180, 250)),
+    # several query tiles per head (one CTA each), causal and padded, ragged last tile
+    ("resident_query_tiles_causal", 2, 3, 256, 256, MASK_CAUSAL, None),
+    ("resident_query_tiles_ragged", 2, 2, 300, 230, MASK_KEY_PADDING, (0, 230)),
+    ("resident_long_queries_short_keys", 1, 2, 1000, 60, MASK_KEY_PADDING, (1, 60)),
 ]
 
 
@@ -492,12 +501,14 @@ def test_resident_peaked_rows_standard_values(orc):
     assert (np.abs(got - ref) - rounding_bound(ref)).max() <= 0, report(got, ref, 1e-2)
 
 
-@pytest.mark.parametrize("mask", [MASK_KEY_PADDING, MASK_CAUSAL | MASK_KEY_PADDING], ids=["padding", "causal_padding"])
-def test_resident_lse_and_bounds(orc, mask):
+@pytest.mark.parametrize("mask,m,n", [(MASK_KEY_PADDING, 100, 150), (MASK_CAUSAL | MASK_KEY_PADDING, 128, 128),
+                                      (MASK_KEY_PADDING, 200, 256), (MASK_CAUSAL | MASK_KEY_PADDING, 250, 250)],
+                         ids=["padding", "causal_padding", "padding_256_keys_two_tiles", "causal_250"])
+def test_resident_lse_and_bounds(orc, mask, m, n):
     """The log-sum-exp output of the resident kernel (rows with no allowed key: -inf),
-    and that it writes exactly its output (guard regions on both sides untouched)."""
-    B, h, m = 3, 3, 100 if mask == MASK_KEY_PADDING else 128
-    n = 150 if mask == MASK_KEY_PADDING else m
+    and that it writes exactly its output (guard regions on both sides untouched), with
+    one and two query tiles per head and up to 256 keys."""
+    B, h = 3, 3
     w = Workload("resident_lse", "bf16", B, h, m, n, 64, mask, 0.125, 66, (0, n))
     inp = draw(w)
     inp.key_lengths[0] = 0

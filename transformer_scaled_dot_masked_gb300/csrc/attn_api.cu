@@ -23,10 +23,10 @@ bool overlaps(const void *a, uint64_t abytes, const void *b, uint64_t bbytes)
 // heads run zero-padded to 64 inside the kernel).
 bool tensor_core_head(const attn_dims &d) { return d.dtype == ATTN_BF16 && d.d_k % 8 == 0 && d.d_k <= 64; }
 
-// Which kernel AUTO picks: tensor cores for tensor_core_head (one head per CTA, whole
-// head resident, when a head has at most 128 queries and 192 keys; two heads per CTA
-// tile when it has at most 128 queries; two query tiles of one head otherwise); CUDA
-// cores for fp32 and for other bf16 head widths.
+// Which kernel AUTO picks: tensor cores for tensor_core_head (one query tile per CTA
+// with the head's keys and values resident, when a head has at most 256 keys; two
+// heads per CTA tile when it has at most 128 queries; two query tiles of one head
+// otherwise); CUDA cores for fp32 and for other bf16 head widths.
 int auto_kernel(const attn_dims &d)
 {
     if (tensor_core_head(d) && attn::resident_fits(d.m, d.n, d.d_k)) return ATTN_KERNEL_RESIDENT;

@@ -1,17 +1,18 @@
 // Whole-head-resident masked attention for short sequences on sm_103a (TMA + tcgen05 + TMEM).
 //
-// softmax(scale * Q K^T + M) V for one (batch, head) per CTA ("Paper Deep Reading:
-// Attention Is All You Need", §04 attention equation with the mask M; the slide
-// deck's "Three Applications of Attention": encoder self-attention with key
-// padding, decoder self-attention with a causal mask, encoder-decoder attention).
-// A head with at most 128 queries and 192 keys fits in shared memory and TMEM at
-// once, so each row's softmax is taken over the whole row: the exact row maximum
-// first, then the exponentials, with no running rescale.  This path is bound by
-// HBM bandwidth (every byte of Q, K, V and O is moved once), so the kernel is
+// softmax(scale * Q K^T + M) V for one 128-row query tile of one (batch, head) per
+// CTA ("Paper Deep Reading: Attention Is All You Need", §04 attention equation with
+// the mask M; the slide deck's "Three Applications of Attention": encoder
+// self-attention with key padding, decoder self-attention with a causal mask,
+// encoder-decoder attention).  A query tile with up to 256 keys fits in shared
+// memory and TMEM at once, so each row's softmax is taken over the whole row: the
+// exact row maximum first, then the exponentials, with no running rescale.  This
+// path is bound by HBM bandwidth (every byte of Q, K, V and O is moved once; the
+// query tiles of a head read its K and V from L2 after the first), so the kernel is
 // built for many small CTAs in flight rather than for tensor-pipe throughput.
 //
-// One CTA of 160 threads per head: warps 0-3 own one query row per thread (TMEM
-// lane t = row t), warp 4 issues the copies and the MMAs.
+// One CTA of 160 threads per query tile: warps 0-3 own one query row per thread
+// (TMEM lane t = row q0 + t), warp 4 issues the copies and the MMAs.
 //   1. warp 4 issues the TMA loads, one copy per lane: Q (one 128-row box; rows past
 //      m read as 0), then K, then V, in 64-row and 16-row boxes only up to the keys
 //      some row may see (the padded length, or m under a causal mask, rounded up to
@@ -24,7 +25,9 @@
 //      with exactly the weights the MMA applies (the log-sum-exp output uses the sum
 //      before rounding, the exact statistic);
 //   4. O = P V after S in TMEM                       (kv_rows / 16 x M128 N64 K16, P from TMEM),
-//      issued 32 keys at a time as soon as every row has stored that chunk of P;
+//      issued 32 keys at a time as soon as every row has stored that chunk of P
+//      (above 192 keys O lies over the last two chunks of S, whose weights each row
+//      takes first and holds in registers: kernel variant kLong);
 //   5. epilogue: O / sum in bf16; each warp stages its 32 rows in the (now free) Q
 //      buffer with the 128-byte swizzle and stores them with one TMA copy, which clips
 //      rows past m (and columns past d_k for narrow heads).
@@ -66,7 +69,10 @@ constexpr uint32_t kRowBytes = kD * 2;            // one key row in shared memor
 constexpr uint32_t kIdescPV = idesc_bf16_f32(kRows, kD, 0, 1); // P (TMEM) x V (MN-major)
 constexpr uint64_t kDefaultWaitNs = 2000000000ull; // 2 s
 constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s
-static_assert(kResidentMaxKeys % 32 == 0 && kResidentMaxKeys <= 192, "S, then P and O, must fit 256 columns");
+// S takes up to 256 TMEM columns and O 64: above 192 keys O lies over the last two
+// chunks of S, whose weights are taken first and held in registers (see pass 2)
+static_assert(kResidentMaxKeys % 32 == 0 && kResidentMaxKeys <= 256, "S must fit 256 columns");
+constexpr int kShortKeys = 192; // up to this many keys S and O never overlap
 
 // where a wait gave up (the status word's info)
 enum Site : uint32_t { kSiteQK = 1, kSiteS = 2, kSiteP = 3, kSiteV = 4, kSiteO = 5 };
@@ -82,6 +88,7 @@ struct ResidentParams {
     const int32_t *key_lengths; // [B] or nullptr
     float *lse;                 // [B][h][m] natural log, or nullptr
     int h, m, n, mask_kind;
+    int q_tiles;                // 128-row query tiles per head (one CTA each)
     int window;                 // restricted attention: keys with |i - j| <= window stay; -1: none
     int kv_cap;                 // key rows the K and V buffers hold: n rounded up to kKeyBox
     float scale_log2;
@@ -212,7 +219,10 @@ constexpr int kThreads = kRows + 32;
 constexpr int kCtlWarp = 4;
 constexpr int kMaxChunks = kResidentMaxKeys / 32;
 
-__global__ void __launch_bounds__(kThreads, 4)
+// kLong: heads with more than 192 keys (S and O overlap in TMEM; two CTAs per SM at
+// most by their 256 columns, so the row threads may hold two chunks of weights)
+template <bool kLong>
+__global__ void __launch_bounds__(kThreads, kLong ? 2 : 4)
 attn_resident_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k64,
                      const __grid_constant__ CUtensorMap tm_k16, const __grid_constant__ CUtensorMap tm_v64,
                      const __grid_constant__ CUtensorMap tm_v16, const __grid_constant__ CUtensorMap tm_o32,
@@ -225,7 +235,10 @@ attn_resident_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     uint8_t *v_s = k_s + p.kv_cap * kRowBytes;
     Ctl &c = *reinterpret_cast<Ctl *>(v_s + p.kv_cap * kRowBytes);
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int bh = blockIdx.x;
+    // the query tiles of one head are neighbours in the grid (they read the same K, V)
+    const int bh = blockIdx.x / p.q_tiles;
+    const int q0 = (blockIdx.x % p.q_tiles) * kRows;
+    const int rows = min(kRows, p.m - q0); // query rows of this tile
     int *ab = &c.abort_flag;
 
     if (tid == kCtlWarp * 32) {
@@ -262,8 +275,8 @@ attn_resident_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         len = len < 0 ? 0 : (len > p.n ? p.n : len);
     }
     const bool causal = (p.mask_kind & kMaskCausal) != 0;
-    int need = causal ? min(len, p.m) : len; // keys some row of the head may see
-    if (p.window >= 0) need = min(need, p.m + p.window);
+    int need = causal ? min(len, q0 + rows) : len; // keys some row of the tile may see
+    if (p.window >= 0) need = min(need, q0 + rows + p.window);
     // key rows loaded and multiplied: whole 16-row boxes, at least one (an empty head
     // still runs the same steps on a box of real, finite keys and writes zeros)
     const int kv_rows = max(kKeyBox, (need + kKeyBox - 1) / kKeyBox * kKeyBox);
@@ -271,8 +284,10 @@ attn_resident_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     // TMEM: S in [0, kv_rows); P (bf16 pairs) over [0, kv_rows / 2), chunk by chunk as
     // S is read; O after S, so that P V starts on the first chunks while later ones are
     // still being read.  Up to 64 keys: 128 columns (four CTAs compute per SM), else 256.
+    // Above 192 keys O lies over S chunks 6 and 7: pass 2 takes their weights first.
     const uint32_t tmem_cols = kv_rows <= 64 ? 128u : 256u;
     const uint32_t col_o = kv_rows <= 64 ? 64u : 192u;
+    const int held_lo = kLong && kv_rows > kShortKeys ? kShortKeys / 32 : nch; // first chunk under O
     const uint64_t lim = p.wait_ns;
 
     if (warp == kCtlWarp) {
@@ -288,7 +303,7 @@ attn_resident_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         const int r0 = lane < big ? lane * kKeyBoxBig : big * kKeyBoxBig + (lane - big) * kKeyBox;
         if (lane < big) tma_load_3d(k_s + r0 * kRowBytes, &tm_k64, &c.qk_full, 0, r0, bh);
         else if (lane < big + small) tma_load_3d(k_s + r0 * kRowBytes, &tm_k16, &c.qk_full, 0, r0, bh);
-        if (lane == 31) tma_load_3d(q_s, &tm_q, &c.qk_full, 0, 0, bh);
+        if (lane == 31) tma_load_3d(q_s, &tm_q, &c.qk_full, 0, q0, bh);
         __syncwarp();
         if (lane < big) tma_load_3d(v_s + r0 * kRowBytes, &tm_v64, &c.v_full, 0, r0, bh);
         else if (lane < big + small) tma_load_3d(v_s + r0 * kRowBytes, &tm_v16, &c.v_full, 0, r0, bh);
@@ -338,8 +353,8 @@ attn_resident_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         }
         __syncwarp();
     } else {
-        // ---- softmax of row `row` over keys [lo, hi)
-        const int row = tid;
+        // ---- softmax of query row `row` (TMEM lane tid) over keys [lo, hi)
+        const int row = q0 + tid;
         const uint32_t t_row = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         int hi = causal ? min(len, row + 1) : len;
         int lo = 0;
@@ -348,7 +363,7 @@ attn_resident_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             lo = row - p.window;
         }
         const float sl2 = p.scale_log2;
-        const bool warp_live = warp * 32 < p.m; // rows past m are never stored
+        const bool warp_live = warp * 32 < rows; // rows past m are never stored
         // the row threads' waits depend on the MMA issuer's, so they get twice its limit:
         // when something stalls, the first wait to run out is the one that names it
         ok = wait_poll(&c.s_full, 0, ab, 2 * lim, kSiteS);
@@ -382,19 +397,37 @@ attn_resident_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         // pass 2: bf16 pairs over the start of S (chunk ch to columns [16 ch, 16 ch + 16),
         // which only chunks this thread has already read occupied); each chunk is handed to
         // the MMA issuer as soon as every row has stored it
+        auto weights_of = [&](int ch, uint32_t (&pk)[16]) {
+            if (ch >= c_lo && ch < c_hi) {
+                uint32_t r[32];
+                tmem_ld32(t_row + 32 * ch, r);
+                tmem_wait_ld();
+                reg_fence32(r);
+                const bool mk = !(32 * ch >= lo_max && 32 * ch + 32 <= hi_min);
+                chunk_weights_any(mk, want_lse, r, lo - 32 * ch, hi - 32 * ch, mul2, sub2, pk, acc, accx);
+            } else {
+#pragma unroll
+                for (int e2 = 0; e2 < 16; ++e2) pk[e2] = 0u;
+            }
+        };
+        // Above 192 keys O lies over S chunks 6 and 7: their weights are taken first and
+        // held in registers.  They are stored after the other chunks, into the columns of
+        // S chunk 3, which this thread has read by then.  The first P V, which writes O,
+        // follows chunk 0, which every row hands over only after reading chunks 6 and 7.
+        uint32_t held[2][16];
+        if (kLong && ok) {
+#pragma unroll
+            for (int hc = 0; hc < 2; ++hc)
+                if (held_lo + hc < nch) weights_of(held_lo + hc, held[hc]);
+        }
         for (int ch = 0; ch < nch; ++ch) {
             if (ok) {
                 uint32_t pk[16];
-                if (ch >= c_lo && ch < c_hi) {
-                    uint32_t r[32];
-                    tmem_ld32(t_row + 32 * ch, r);
-                    tmem_wait_ld();
-                    reg_fence32(r);
-                    const bool mk = !(32 * ch >= lo_max && 32 * ch + 32 <= hi_min);
-                    chunk_weights_any(mk, want_lse, r, lo - 32 * ch, hi - 32 * ch, mul2, sub2, pk, acc, accx);
-                } else {
+                if (kLong && ch >= held_lo) {
 #pragma unroll
-                    for (int e2 = 0; e2 < 16; ++e2) pk[e2] = 0u;
+                    for (int e2 = 0; e2 < 16; ++e2) pk[e2] = ch == held_lo ? held[0][e2] : held[1][e2];
+                } else {
+                    weights_of(ch, pk);
                 }
                 tmem_st16(t_row + 16 * ch, pk);
                 tmem_wait_st();
@@ -427,7 +460,7 @@ attn_resident_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 p.lse[static_cast<size_t>(bh) * p.m + row] =
                     lx > 0.f ? (mx + __log2f(lx)) * 0.6931471805599453f : -CUDART_INF_F;
             // 128-byte swizzle: 16-byte chunk k of row r at chunk k ^ (r % 8) (conflict-free)
-            const uint32_t stage_row = smem_addr(q_s) + row * kRowBytes;
+            const uint32_t stage_row = smem_addr(q_s) + tid * kRowBytes;
 #pragma unroll
             for (int k8 = 0; k8 < kD / 8; ++k8) {
                 uint4 v;
@@ -435,13 +468,13 @@ attn_resident_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 v.y = pack_bf16x2(__uint_as_float(o[8 * k8 + 2]) * inv, __uint_as_float(o[8 * k8 + 3]) * inv);
                 v.z = pack_bf16x2(__uint_as_float(o[8 * k8 + 4]) * inv, __uint_as_float(o[8 * k8 + 5]) * inv);
                 v.w = pack_bf16x2(__uint_as_float(o[8 * k8 + 6]) * inv, __uint_as_float(o[8 * k8 + 7]) * inv);
-                st_shared_v4(stage_row + ((k8 ^ (row & 7)) << 4), v);
+                st_shared_v4(stage_row + ((k8 ^ (tid & 7)) << 4), v);
             }
             fence_proxy_async_shared();
             __syncwarp();
             if (lane == 0) {
                 // rows past m and columns past d are clipped by the copy
-                tma_store_3d(&tm_o32, q_s + warp * 32 * kRowBytes, 0, warp * 32, bh);
+                tma_store_3d(&tm_o32, q_s + warp * 32 * kRowBytes, 0, q0 + warp * 32, bh);
                 bulk_commit_group();
                 bulk_wait_read_all(); // the staging rows must stay valid until the copy has read them
             }
@@ -470,7 +503,7 @@ size_t smem_bytes(int kv_cap) { return 1024 + kQBytes + 2u * kv_cap * (kD * 2) +
 
 } // namespace
 
-bool resident_fits(int m, int n, int d) { return m <= kRows && n <= kResidentMaxKeys && d % 8 == 0 && d <= kD; }
+bool resident_fits(int m, int n, int d) { return m >= 1 && n <= kResidentMaxKeys && d % 8 == 0 && d <= kD; }
 
 cudaError_t launch_resident(const Problem &pb, cudaStream_t stream, const ResidentTestHook *hook)
 {
@@ -485,7 +518,10 @@ cudaError_t launch_resident(const Problem &pb, cudaStream_t stream, const Reside
         std::lock_guard<std::mutex> lock(mu);
         DeviceInfo &di = infos[dev];
         if (!di.configured) {
-            if ((e = cudaFuncSetAttribute(reinterpret_cast<const void *>(attn_resident_kernel),
+            if ((e = cudaFuncSetAttribute(reinterpret_cast<const void *>(attn_resident_kernel<false>),
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>(smem_bytes(kShortKeys)))) != cudaSuccess ||
+                (e = cudaFuncSetAttribute(reinterpret_cast<const void *>(attn_resident_kernel<true>),
                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           static_cast<int>(smem_bytes(kResidentMaxKeys)))) != cudaSuccess)
                 return e;
@@ -507,6 +543,7 @@ cudaError_t launch_resident(const Problem &pb, cudaStream_t stream, const Reside
     p.lse = pb.lse;
     p.h = pb.h;
     p.m = pb.m;
+    p.q_tiles = (pb.m + kRows - 1) / kRows;
     p.n = pb.n;
     p.mask_kind = pb.mask_kind;
     p.window = (pb.mask_kind & kMaskWindow) ? pb.window : -1;
@@ -515,7 +552,9 @@ cudaError_t launch_resident(const Problem &pb, cudaStream_t stream, const Reside
     p.wait_ns = hook != nullptr ? hook->wait_ns : kDefaultWaitNs;
     p.withhold_p_arrival = hook != nullptr ? hook->withhold_p_arrival : 0;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(BH);
+    const long long ctas = static_cast<long long>(BH) * p.q_tiles;
+    if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem_bytes(kv_cap);
     cfg.stream = stream;
@@ -524,7 +563,9 @@ cudaError_t launch_resident(const Problem &pb, cudaStream_t stream, const Reside
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pb.overlap_launch ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, attn_resident_kernel, tq, tk64, tk16, tv64, tv16, to32, p);
+    if (kv_cap > kShortKeys)
+        return cudaLaunchKernelEx(&cfg, attn_resident_kernel<true>, tq, tk64, tk16, tv64, tv16, to32, p);
+    return cudaLaunchKernelEx(&cfg, attn_resident_kernel<false>, tq, tk64, tk16, tv64, tv16, to32, p);
 }
 
 cudaError_t resident_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint32_t *info)

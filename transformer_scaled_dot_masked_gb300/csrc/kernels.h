@@ -120,11 +120,12 @@ cudaError_t launch_heads_copy(const void *src, void *dst, int B, int L, int h, i
 // Device status word of the flash kernel (bounded waits that gave up).
 cudaError_t flash_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint32_t *info);
 
-// Whole-head-resident tcgen05/TMA kernel for short sequences (bf16, d a multiple of 8
-// up to 64, m <= 128, n <= kResidentMaxKeys): one head per CTA, exact two-pass softmax
-// per row.  Launched as a programmatic dependent of the previous kernel when
-// p.overlap_launch is set (everything it reads or writes follows the dependency wait).
-constexpr int kResidentMaxKeys = 192;
+// Whole-head-resident tcgen05/TMA kernel for short key sequences (bf16, d a multiple
+// of 8 up to 64, n <= kResidentMaxKeys, any m): one 128-row query tile of one head per
+// CTA with all of the head's keys, exact two-pass softmax per row.  Launched as a
+// programmatic dependent of the previous kernel when p.overlap_launch is set
+// (everything it reads or writes follows the dependency wait).
+constexpr int kResidentMaxKeys = 256;
 bool resident_fits(int m, int n, int d);
 // Test hook of the bounded waits: a short wait limit, and the last thread withholding
 // its arrival on the weights barrier, so that the MMA issuer's wait runs out.
