@@ -596,6 +596,9 @@ attn_status attn_mha_fwd(const void *Xq, const void *Xkv, const void *Wq, const 
         in3[i].w = ins_proj[i].w;
         in3[i].out = ins_proj[i].o;
         in3[i].L = ins_proj[i].L;
+        // a programmatic dependent of whatever ran before on the stream: only its
+        // barrier set-up runs before that kernel completes
+        in3[i].overlap_launch = true;
     }
     // the three input projections in one launch
     if (attn::launch_proj_multi(in3, 3, s) != cudaSuccess) return ATTN_ERR_CUDA;

@@ -179,7 +179,10 @@ attn_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
     // Set-up above overlaps the previous kernel's tail when launched as its programmatic
     // dependent.  Nothing below may read what that kernel writes before it completes,
     // and TMEM is allocated only after it has completed: a kernel that let this one
-    // launch early may still have CTAs waiting for columns.
+    // launch early may still have CTAs waiting for columns.  Every CTA of this
+    // (persistent) grid is resident, so the next grid may launch now: its CTAs take SMs
+    // as this grid's leave and wait for it to complete.
+    grid_launch_dependents();
     grid_dependency_wait();
     if (warp == 1) {
         tmem_alloc_pair(&sm.tmem_base, kTmemCols); // one warp of each CTA of the pair, together

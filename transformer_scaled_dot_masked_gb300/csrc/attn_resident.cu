@@ -133,11 +133,6 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity)
         if (global_timer_ns() - start > kDrainLimitNs) return;
 }
 
-__device__ __forceinline__ void grid_launch_dependents()
-{
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 // Row maximum of one 32-key chunk of raw scores.  kMask: only columns e of the chunk
 // with lo_rel <= e < hi_rel count (a chunk that is allowed whole for every row of the
 // warp skips the test).

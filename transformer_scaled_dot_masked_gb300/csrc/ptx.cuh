@@ -187,6 +187,13 @@ __device__ __forceinline__ void st_shared_v4_ordered(uint32_t addr, uint4 v)
 // visible; a no-op for an ordinary launch.
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Lets the next grid on the stream (a programmatic dependent) launch once every CTA of
+// this grid has executed this or exited; its CTAs then wait in grid_dependency_wait.
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols)
 {
