@@ -4,8 +4,9 @@ Every mbarrier wait of the tensor-core kernels gives up after a time limit, reco
 the time-out in a device status word, lets the kernel drain its own copies and MMAs,
 free its TMEM and exit, and leaves the CUDA context usable.  The test hook
 attn_test_withheld_arrival runs the whole-head-resident kernel with a 20 ms limit and
-one row thread that never reports its first chunk of weights, so the MMA issuer's
-wait for that chunk runs out (no other wait can: each completes in microseconds).
+one row thread that never reports its chunks of weights, so the MMA issuer's wait for
+the first chunk runs out (no other wait can: each completes in microseconds).  Its
+long-key variant (above 192 keys, the held chunks) and query tiles are covered too.
 """
 import numpy as np
 import pytest
@@ -34,7 +35,9 @@ def _withheld(inp, out, wait_ns):
     return st
 
 
-@pytest.mark.parametrize("cfg,shape", [(3, dict(B=1, h=1)), (4, dict(B=2, h=2))], ids=["causal_128", "cross_160"])
+@pytest.mark.parametrize("cfg,shape", [(3, dict(B=1, h=1)), (4, dict(B=2, h=2)),
+                                       (4, dict(B=2, h=2, m=200, n=256, lengths=(200, 256)))],
+                         ids=["causal_128", "cross_160", "two_query_tiles_256_keys"])
 def test_wait_runs_out_and_context_survives(cfg, shape):
     w = WORKLOADS[cfg].with_(**shape)
     inp = draw(w)
