@@ -36,6 +36,10 @@ CASES = [
     ("big_cross_padding", 2, 16, 128, 160, 1024, MASK_KEY_PADDING, False, (40, 160)),
     ("two_heads_long", 1, 2, 700, 700, 128, MASK_NONE, True, None),
     ("six_heads_odd_column_tiles", 2, 6, 300, 300, 384, MASK_CAUSAL, True, None),
+    # the projections' CTA pairs on tiny and ragged row counts: a pair tile of 256 rows
+    # with one valid row (the second CTA's rows all past L, never stored), and 17 / 33
+    ("one_position", 1, 2, 1, 1, 128, MASK_NONE, True, None),
+    ("ragged_cross_17_33", 3, 2, 17, 33, 128, MASK_KEY_PADDING, False, (1, 33)),
 ]
 
 
@@ -89,6 +93,7 @@ NARROW_CASES = [
     ("h32_d16_decoder_causal", 2, 32, 130, 130, 512, MASK_CAUSAL, True, None),
     ("h16_d32_cross_padding", 2, 16, 128, 200, 512, MASK_KEY_PADDING, False, (40, 200)),
     ("h8_d48_long", 1, 8, 300, 300, 384, MASK_NONE, True, None),
+    ("h4_d32_five_causal", 1, 4, 5, 5, 128, MASK_CAUSAL, True, None),
 ]
 
 
