@@ -550,28 +550,25 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
 }
 
-// D_i = sum_c dO_ic O_ic and (lse_i log2 e, D_i) per query row, padded to whole
-// tiles; zeroes the dQ accumulator (64 columns per row whatever the head width).  One
-// thread per (head, padded row); rows of out and dout hold d elements.
+// D_i = sum_c dO_ic O_ic and (lse_i * log2 e, D_i) per query row (padding rows of
+// the last tile: (+inf, 0)), and the row's 64 accumulator columns zeroed.  Eight
+// threads per row, each with 16 bytes of O and dO and 32 bytes of the accumulator,
+// so a warp's loads and stores cover whole consecutive rows; the eight partial dot
+// products are summed with three shuffles.
 __global__ void attn_bwd_pre_kernel(const __nv_bfloat16 *__restrict__ out, const __nv_bfloat16 *__restrict__ dout,
                                     const float *__restrict__ lse, float2 *__restrict__ ld,
                                     float *__restrict__ dq_acc, int BH, int m, int m_pad, int d)
 {
-    const size_t r = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (r >= static_cast<size_t>(BH) * m_pad) return;
+    const size_t t = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const size_t r = t / 8; // query row (BH * m_pad * 8 threads: a whole number of warps)
+    const int part = static_cast<int>(t % 8);
+    if (r >= static_cast<size_t>(BH) * m_pad) return; // whole warps only
     const int bh = static_cast<int>(r / m_pad), q = static_cast<int>(r % m_pad);
-    if (q >= m) {
-        ld[r] = make_float2(CUDART_INF_F, 0.f);
-        return;
-    }
     const size_t row = static_cast<size_t>(bh) * m + q;
-    const uint4 *o = reinterpret_cast<const uint4 *>(out + row * d);
-    const uint4 *g = reinterpret_cast<const uint4 *>(dout + row * d);
     float dsum = 0.f;
-#pragma unroll
-    for (int c = 0; c < kD / 8; ++c) {
-        if (8 * c >= d) break;
-        const uint4 a = o[c], b = g[c];
+    if (q < m && 8 * part < d) {
+        const uint4 a = reinterpret_cast<const uint4 *>(out + row * d)[part];
+        const uint4 b = reinterpret_cast<const uint4 *>(dout + row * d)[part];
         const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -579,10 +576,17 @@ __global__ void attn_bwd_pre_kernel(const __nv_bfloat16 *__restrict__ out, const
             dsum = fmaf(__uint_as_float(av[u] & 0xffff0000u), __uint_as_float(bv[u] & 0xffff0000u), dsum);
         }
     }
-    ld[r] = make_float2(lse[row] * 1.4426950408889634f, dsum);
+    dsum += __shfl_xor_sync(0xffffffffu, dsum, 4);
+    dsum += __shfl_xor_sync(0xffffffffu, dsum, 2);
+    dsum += __shfl_xor_sync(0xffffffffu, dsum, 1);
+    if (q >= m) {
+        if (part == 0) ld[r] = make_float2(CUDART_INF_F, 0.f);
+        return;
+    }
+    if (part == 0) ld[r] = make_float2(lse[row] * 1.4426950408889634f, dsum);
     float4 *acc = reinterpret_cast<float4 *>(dq_acc + row * kD);
-#pragma unroll
-    for (int c = 0; c < kD / 4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    acc[part] = make_float4(0.f, 0.f, 0.f, 0.f);
+    acc[part + 8] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // dQ = bf16(scale * accumulator), eight elements per thread: chunk r is columns
@@ -647,8 +651,8 @@ cudaError_t launch_bwd(const BwdProblem &pb, cudaStream_t stream)
         !encode_rows_map_f32(&tdq, dq_acc, pb.m, BH))
         return cudaErrorInvalidValue;
 
-    const size_t pre_rows = static_cast<size_t>(BH) * m_pad;
-    attn_bwd_pre_kernel<<<static_cast<unsigned>((pre_rows + 255) / 256), 256, 0, stream>>>(
+    const size_t pre_threads = static_cast<size_t>(BH) * m_pad * 8;
+    attn_bwd_pre_kernel<<<static_cast<unsigned>((pre_threads + 255) / 256), 256, 0, stream>>>(
         static_cast<const __nv_bfloat16 *>(pb.out), static_cast<const __nv_bfloat16 *>(pb.dout), pb.lse, ld,
         dq_acc, BH, pb.m, m_pad, pb.d);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
