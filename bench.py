@@ -19,7 +19,11 @@ other_workloads (the four short configurations), backward, decode, window
 (d_k = 128 on the long sequences: causal, unmasked, windows 256 and 1024), mha
 (projections + attention) and cpu_baseline.  roofline.traffic is the DRAM bytes
 of one launch from the committed ncu capture, reported while roofline.source_hash
-(the flash kernel's sources) matches it.
+(the flash kernel's sources) matches it.  parity holds the check of the buffers
+that were timed against the fp64 oracle the cpu_baseline leg runs anyway: the
+sampled rows of the main workload in the output of its last timed step, and
+workloads 1-4 element by element in the outputs of their timed launches (1e-2
+absolute for bf16, 1e-4 for fp32); a miss ends the run with an error.
 
 --impl reference times the fp64 CPU oracle on the host cores instead, on a
 bounded sample of query rows of the same workload per step (the pages have no
@@ -214,10 +218,12 @@ def time_launches(fn, steps, torch, stream):
 def short_workloads(torch, attn, device, peak_hbm):
     """Per-launch time of the memory-bound workloads (and the fp32 one) with
     input sets rotated so their total exceeds twice the L2 size; launches are
-    captured in a CUDA graph so the figure is device time, not launch latency."""
+    captured in a CUDA graph so the figure is device time, not launch latency.
+    Also returns, by workload name, the output the timed launches wrote into the
+    first input set's buffer (float64 on the host), for the parity check."""
     props = torch.cuda.get_device_properties(device)
     l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
-    res = {}
+    res, outputs = {}, {}
     for cfg in (1, 2, 3, 4):
         w = WORKLOADS[cfg]
         inp = draw(w)
@@ -252,6 +258,7 @@ def short_workloads(torch, attn, device, peak_hbm):
                 t1.synchronize()
                 times.append(t0.elapsed_time(t1) / (reps * copies))
         ms = statistics.median(times)
+        outputs[w.name] = sets[0][4].double().cpu().numpy()
         nb = algorithmic_bytes(w, inp.key_lengths)
         res[w.name] = {
             "kernel": attn._native.KERNEL_NAMES[kern], "us_per_launch": ms * 1e3,
@@ -263,7 +270,7 @@ def short_workloads(torch, attn, device, peak_hbm):
         }
         del sets, g
         torch.cuda.empty_cache()
-    return res
+    return res, outputs
 
 
 def backward_workload(torch, attn, device, peak_tf, steps=20):
@@ -479,6 +486,11 @@ def decode_workload(torch, attn, device, peak_hbm, steps=50):
             "algorithmic": "each live cached K and V row once, plus Q and O (bf16)"}
 
 
+def parity_tol(w):
+    """The bar of the parity tests: 1e-2 absolute for bf16 outputs, 1e-4 for fp32."""
+    return 1e-2 if w.dtype == "bf16" else 1e-4
+
+
 def cpu_oracle_sample(w, inp, target_s, seed=3):
     """Time the fp64 oracle on random query rows of w for about target_s seconds."""
     import oracle
@@ -494,17 +506,19 @@ def cpu_oracle_sample(w, inp, target_s, seed=3):
     count = int(np.clip(16 * target_s / dt, 16, total_rows))
     rows = rng.integers(0, total_rows, size=count)
     t0 = time.perf_counter()
-    orc.attn_rows(qd, kd, vd, inp.key_lengths, w.mask, w.scale, rows, widened=True)
+    ref = orc.attn_rows(qd, kd, vd, inp.key_lengths, w.mask, w.scale, rows, widened=True)
     el = time.perf_counter() - t0
     flops = 4.0 * w.d * row_pairs(w, inp.key_lengths, rows)
     return {"value": flops / el / 1e12, "unit": UNIT, "cores": orc.num_threads(), "kind": "oracle",
             "sample": f"{count} random query rows of {w.description} ({el:.1f} s, fp64, "
-                      f"{flops / 1e9:.1f} GFLOP useful)", "seconds": el}, (orc, qd, kd, vd)
+                      f"{flops / 1e9:.1f} GFLOP useful)", "seconds": el}, (rows, ref)
 
 
-def cpu_per_config(all_cores_c5):
+def cpu_per_config(all_cores_c5, timed_outputs, parity):
     """The oracle on workloads 1-4 in full, on one core and on all of them, and on
-    workload 5's row sample on all cores: useful TFLOPS and seconds per run."""
+    workload 5's row sample on all cores: useful TFLOPS and seconds per run.  The
+    full outputs also check, element by element, the outputs the GPU wrote in the
+    timed launches of workloads 1-4 (timed_outputs, by workload name), into parity."""
     import oracle
     orc = oracle.load()
     cores = orc.num_threads()
@@ -517,10 +531,14 @@ def cpu_per_config(all_cores_c5):
         for label, threads in (("one_core", 1), ("all_cores", cores)):
             orc.set_num_threads(threads)
             t0 = time.perf_counter()
-            orc.attn_fwd(inp.q, inp.k, inp.v, inp.key_lengths, w.mask, w.scale)
+            ref = orc.attn_fwd(inp.q, inp.k, inp.v, inp.key_lengths, w.mask, w.scale)
             el = time.perf_counter() - t0
             entry[label] = {"tflops_useful": flops / el / 1e12, "seconds": el, "threads": threads}
         res[w.name] = entry
+        if w.name in timed_outputs:
+            err = float(np.abs(timed_outputs[w.name] - ref).max())
+            parity[w.name] = {"elements": int(ref.size), "max_abs_err": err, "tol": parity_tol(w),
+                              "ok": err <= parity_tol(w)}
     # workload 5 (5.5e11 useful FLOP, minutes on one core): one core on a random row sample
     w = WORKLOADS[5]
     inp = draw(w)
@@ -679,7 +697,7 @@ def main():
                          "ms_per_step": ems, "steps": e2e_steps,
                          "entry_point": "attn_fwd_host (host buffers; copies in, kernels and copies out overlapped)"}
         result["gpu_launches"] = args.steps  # e2e launches are outside the device-timed region
-        result["other_workloads"] = short_workloads(torch, attn, device, peak_hbm)
+        result["other_workloads"], timed_outputs = short_workloads(torch, attn, device, peak_hbm)
         result["backward"] = backward_workload(torch, attn, device, peak_tf)
         result["decode"] = decode_workload(torch, attn, device, peak_hbm)
         result["window"] = window_workload(torch, attn, device, peak_tf)
@@ -687,11 +705,24 @@ def main():
         result["wide_heads"] = wide_workload(torch, attn, device, peak_tf)
         result["mha"] = mha_workload(torch, attn, device, peak_tf)
         if rank == 0:
-            cb, _ = cpu_oracle_sample(w, inp, args.cpu_seconds)
+            cb, (rows, ref) = cpu_oracle_sample(w, inp, args.cpu_seconds)
             seconds = cb.pop("seconds", None)
+            # parity on the buffers that were timed: the oracle rows of the sample against
+            # the same rows of the output the last timed step wrote, and workloads 1-4 in
+            # full against their timed outputs
+            got = out.reshape(-1, w.d)[torch.from_numpy(rows).to(device)].double().cpu().numpy()
+            err = float(np.abs(got - ref).max())
+            parity = {w.name: {"elements": int(ref.size), "rows": int(rows.size), "max_abs_err": err,
+                               "tol": parity_tol(w), "ok": err <= parity_tol(w)}}
             cb["per_config"] = cpu_per_config({"tflops_useful": cb["value"], "seconds": seconds,
-                                               "threads": cb["cores"], "sample": cb["sample"]})
+                                               "threads": cb["cores"], "sample": cb["sample"]},
+                                              timed_outputs, parity)
             result["cpu_baseline"] = cb
+            result["parity"] = parity
+            bad = [k for k, v in parity.items() if not v["ok"]]
+            if bad:
+                print(json.dumps(result))
+                raise RuntimeError(f"timed outputs differ from the oracle beyond the tolerance: {bad}")
 
     if rank == 0:
         print(json.dumps(result))
