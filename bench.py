@@ -215,6 +215,9 @@ def time_launches(fn, steps, torch, stream):
     return start.elapsed_time(end) / steps
 
 
+SHORT_REPLAYS = 10  # graph replays per short workload; the figure is their median
+
+
 def short_workloads(torch, attn, device, peak_hbm):
     """Per-launch time of the memory-bound workloads (and the fp32 one) with
     input sets rotated so their total exceeds twice the L2 size; launches are
@@ -250,7 +253,7 @@ def short_workloads(torch, attn, device, peak_hbm):
             g.replay()
             stream.synchronize()
             times = []
-            for _ in range(5):
+            for _ in range(SHORT_REPLAYS):
                 t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 t0.record(stream)
                 g.replay()
@@ -266,7 +269,7 @@ def short_workloads(torch, attn, device, peak_hbm):
             "tflops_useful": useful_flops(w, inp.key_lengths) / (ms * 1e-3) / 1e12,
             "hbm_gbs_algorithmic": nb / (ms * 1e-3) / 1e9,
             "hbm_frac": nb / (ms * 1e-3) / 1e9 / peak_hbm,
-            "input_sets": copies, "launches_timed": reps * copies * 5,
+            "input_sets": copies, "launches_timed": reps * copies * SHORT_REPLAYS,
         }
         del sets, g
         torch.cuda.empty_cache()
