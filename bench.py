@@ -120,6 +120,15 @@ def workload_config(w):
             "mask": "causal" if w.causal else ("key_padding" if w.padded else "none")}
 
 
+def load_sustained_peak():
+    """The bf16 dense rate measured over seconds under the power cap (None if absent)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"])
+    except Exception:
+        return None
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -673,6 +682,8 @@ def main():
                      "traffic": measured_traffic() if args.workload == 5 else None,
                      "source_hash": flash_source_hash(),
                      "peak_source": f"{peak_src} bf16 dense burst",
+                     "peak_sustained": load_sustained_peak(),
+                     "frac_sustained": (achieved / load_sustained_peak()) if load_sustained_peak() else None,
                      "algorithmic": "4*d_k FLOPs per allowed (query, key) pair per launch"},
         "gpu_launches": args.steps,
     }
