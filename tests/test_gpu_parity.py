@@ -66,12 +66,17 @@ def test_workload_full(orc, cfg):
 
 def test_long_causal_sampled_rows(orc):
     """n = m = 8192 causal at full size, in the launch configuration the benchmark times;
-    checked on sampled rows (tile edges of the first and last head plus random rows)."""
+    checked on every row of the first and the last head ((b, h) = (0, 0) and (3, 15)),
+    the first and last row of every 128-row query tile of every head, and random rows."""
     w = WORKLOADS[5]
     inp = draw(w)
     assert attn.select_kernel(w.B, w.h, w.m, w.n, w.d, 0, w.mask) == K_FLASH
     got = as_f64(run(inp, K_AUTO)).reshape(-1, w.d)
-    rows = sample_rows(w, 1536)
+    heads = np.concatenate([np.arange(w.m), (w.B * w.h - 1) * w.m + np.arange(w.m)])
+    edges = (np.arange(w.B * w.h)[:, None] * w.m + np.array([0, 127])[None, :]
+             + np.arange(0, w.m, 128)[:, None, None]).reshape(-1)
+    rows = np.unique(np.concatenate([heads, edges, sample_rows(w, 1536)]))
+    assert rows.size > 2 * w.m + w.B * w.h * (w.m // 128)
     ref = orc.attn_rows(inp.q, inp.k, inp.v, inp.key_lengths, w.mask, w.scale, rows)
     assert np.abs(got[rows] - ref).max() <= 1e-2, report(got[rows], ref, 1e-2)
     assert np.isfinite(got).all()
