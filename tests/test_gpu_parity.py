@@ -64,6 +64,18 @@ def test_workload_full(orc, cfg):
         assert np.abs(got - ref).max() <= tol_for(w), f"kernel {kern}: " + report(got, ref, tol_for(w))
 
 
+def full_size_rows(w, m, extra):
+    """Linear output-row ids ((b*h + head)*m + i) of a full-size check: every row of the
+    first and the last head, the first and last row of every 128-row query tile of
+    every head, and the rows in `extra`."""
+    heads = np.concatenate([np.arange(m), (w.B * w.h - 1) * m + np.arange(m)])
+    edges = (np.arange(w.B * w.h)[:, None] * m + np.array([0, 127])[None, :]
+             + np.arange(0, m, 128)[:, None, None]).reshape(-1)
+    rows = np.unique(np.concatenate([heads, edges, extra]))
+    assert rows.size > 2 * m + w.B * w.h * (m // 128) and rows.max() < w.B * w.h * m
+    return rows
+
+
 def test_long_causal_sampled_rows(orc):
     """n = m = 8192 causal at full size, in the launch configuration the benchmark times;
     checked on every row of the first and the last head ((b, h) = (0, 0) and (3, 15)),
@@ -72,16 +84,43 @@ def test_long_causal_sampled_rows(orc):
     inp = draw(w)
     assert attn.select_kernel(w.B, w.h, w.m, w.n, w.d, 0, w.mask) == K_FLASH
     got = as_f64(run(inp, K_AUTO)).reshape(-1, w.d)
-    heads = np.concatenate([np.arange(w.m), (w.B * w.h - 1) * w.m + np.arange(w.m)])
-    edges = (np.arange(w.B * w.h)[:, None] * w.m + np.array([0, 127])[None, :]
-             + np.arange(0, w.m, 128)[:, None, None]).reshape(-1)
-    rows = np.unique(np.concatenate([heads, edges, sample_rows(w, 1536)]))
-    assert rows.size > 2 * w.m + w.B * w.h * (w.m // 128)
+    rows = full_size_rows(w, w.m, sample_rows(w, 1536))
     ref = orc.attn_rows(inp.q, inp.k, inp.v, inp.key_lengths, w.mask, w.scale, rows)
     assert np.abs(got[rows] - ref).max() <= 1e-2, report(got[rows], ref, 1e-2)
     assert np.isfinite(got).all()
     # every row of a softmax-weighted mean lies inside the hull of the value rows it averages
     assert np.abs(got).max() <= 5.5
+
+
+def test_wide_heads_benchmarked_sizes(orc):
+    """The d_k = 128 calls the benchmark times, at full size on its inputs (the long
+    workload with h = 8 and d_k = 128): causal n = 8192 through attn_fwd, no mask on the
+    first 4096 positions, and windows of 256 and 1024 through attn_fwd_window; each
+    checked on every row of the first and the last head, both edge rows of every
+    query tile of every head, and random rows."""
+    w = WORKLOADS[5].with_(h=8, d=128, scale=128 ** -0.5, name="long_causal_h8_d128")
+    inp = draw(w)
+    assert attn.select_kernel(w.B, w.h, w.m, w.n, w.d, 0, w.mask) == K_WIDE
+    q, k, v = (to_device(x, "bf16") for x in (inp.q, inp.k, inp.v))
+    half = w.n // 2
+    qh, kh, vh = (x[:, :, :half].contiguous() for x in (q, k, v))
+    host_half = tuple(np.ascontiguousarray(x[:, :, :half]) for x in (inp.q, inp.k, inp.v))
+    full = (inp.q, inp.k, inp.v)
+    cases = [
+        ("causal", lambda: attn.attn_fwd(q, k, v, None, w.mask, w.scale), w.m, full, w.mask, None),
+        ("no_mask_4096", lambda: attn.attn_fwd(qh, kh, vh, None, MASK_NONE, w.scale), half, host_half,
+         MASK_NONE, None),
+    ] + [(f"window_{win}", lambda win=win: attn.attn_fwd_window(q, k, v, None, attn.MASK_WINDOW, win, w.scale),
+          w.m, full, attn.MASK_WINDOW, win) for win in (256, 1024)]
+    rng = np.random.default_rng(61)
+    for name, call, m, ins, mask, win in cases:
+        got = as_f64(call()).reshape(-1, w.d)
+        torch.cuda.synchronize()
+        rows = full_size_rows(w, m, rng.integers(0, w.B * w.h * m, size=1024))
+        ref = orc.attn_rows(*ins, None, mask, w.scale, rows, window=win)
+        assert np.abs(got[rows] - ref).max() <= 1e-2, f"{name}: " + report(got[rows], ref, 1e-2)
+        assert np.isfinite(got).all(), name
+    assert attn.device_status() == (0, 0)
 
 
 # ---------------------------------------------------------------- ragged and edge shapes
