@@ -19,7 +19,8 @@
 //      16), so padded keys cost almost no HBM traffic;
 //   2. S = Q K^T into TMEM columns [0, kv_rows)      (4 x tcgen05.mma M128 N=kv_rows K16)
 //   3. each row thread: pass 1 takes the row maximum over its allowed keys (32-column
-//      TMEM loads; chunks allowed whole for the warp skip the mask arithmetic), pass 2
+//      TMEM loads that also return the chunk's maximum, taken as is for a chunk allowed
+//      whole for the warp, over the allowed columns otherwise), pass 2
 //      takes P = exp2(S * scale * log2 e - max), rounds it to bf16 pairs written over
 //      the start of S, and sums the ROUNDED weights, so the output is a weighted mean
 //      with exactly the weights the MMA applies (the log-sum-exp output uses the sum
@@ -133,6 +134,23 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity)
         if (global_timer_ns() - start > kDrainLimitNs) return;
 }
 
+// 32 consecutive TMEM columns of this warp's 32 lanes, as tmem_ld32, and their
+// maximum, taken by the load itself (sm_103a): as fmaxf, a NaN column is passed
+// over.  Both are valid after tmem_wait_ld.
+__device__ __forceinline__ void tmem_ld32_max(uint32_t taddr, uint32_t (&r)[32], float &mx)
+{
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, %32, [%33];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+          "=f"(mx)
+        : "r"(taddr));
+}
+
 // Row maximum of one 32-key chunk of raw scores.  kMask: only columns e of the chunk
 // with lo_rel <= e < hi_rel count (a chunk that is allowed whole for every row of the
 // warp skips the test).
@@ -200,11 +218,6 @@ __device__ __forceinline__ void chunk_weights_any(bool mask, bool lse, const uin
         if (lse) chunk_weights<false, true>(r, lo_rel, hi_rel, mul2, sub2, pk, acc, accx);
         else chunk_weights<false, false>(r, lo_rel, hi_rel, mul2, sub2, pk, acc, accx);
     }
-}
-
-__device__ __forceinline__ float chunk_max_any(bool mask, const uint32_t (&r)[32], int lo_rel, int hi_rel)
-{
-    return mask ? chunk_max<true>(r, lo_rel, hi_rel) : chunk_max<false>(r, lo_rel, hi_rel);
 }
 
 // 160 threads: warps 0-3 own one query row each per thread (TMEM lane = row); warp 4
@@ -376,14 +389,19 @@ attn_resident_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tc_fence_after();
             // pass 1: row maximum of the raw scores over the allowed columns (scaled after:
             // scaling by a non-negative number keeps the order, and a zero scale must not
-            // meet a masked -inf)
+            // meet a masked -inf).  A chunk allowed whole for the warp takes the maximum
+            // the load computes; a masked one takes it over its allowed columns.
             for (int ch = c_lo; ch < c_hi; ++ch) {
                 uint32_t r[32];
-                tmem_ld32(t_row + 32 * ch, r);
+                float cm;
+                tmem_ld32_max(t_row + 32 * ch, r, cm);
                 tmem_wait_ld();
-                reg_fence32(r);
-                const bool mk = !(32 * ch >= lo_max && 32 * ch + 32 <= hi_min);
-                mraw = fmaxf(mraw, chunk_max_any(mk, r, lo - 32 * ch, hi - 32 * ch));
+                asm volatile("" : "+f"(cm)::"memory"); // cm is read after the wait
+                if (!(32 * ch >= lo_max && 32 * ch + 32 <= hi_min)) {
+                    reg_fence32(r);
+                    cm = chunk_max<true>(r, lo - 32 * ch, hi - 32 * ch);
+                }
+                mraw = fmaxf(mraw, cm);
             }
         }
         const float mx = mraw == -CUDART_INF_F ? -CUDART_INF_F : mraw * sl2;
