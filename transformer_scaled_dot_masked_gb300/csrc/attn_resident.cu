@@ -207,19 +207,6 @@ __device__ __forceinline__ void chunk_weights(const uint32_t (&r)[32], int lo_re
     }
 }
 
-__device__ __forceinline__ void chunk_weights_any(bool mask, bool lse, const uint32_t (&r)[32], int lo_rel, int hi_rel,
-                                                  uint64_t mul2, uint64_t sub2, uint32_t (&pk)[16], float (&acc)[4],
-                                                  uint64_t &accx)
-{
-    if (mask) {
-        if (lse) chunk_weights<true, true>(r, lo_rel, hi_rel, mul2, sub2, pk, acc, accx);
-        else chunk_weights<true, false>(r, lo_rel, hi_rel, mul2, sub2, pk, acc, accx);
-    } else {
-        if (lse) chunk_weights<false, true>(r, lo_rel, hi_rel, mul2, sub2, pk, acc, accx);
-        else chunk_weights<false, false>(r, lo_rel, hi_rel, mul2, sub2, pk, acc, accx);
-    }
-}
-
 // 160 threads: warps 0-3 own one query row each per thread (TMEM lane = row); warp 4
 // issues the copies, allocates TMEM and issues the MMAs.
 constexpr int kRowThreads = kRows;
@@ -228,8 +215,10 @@ constexpr int kCtlWarp = 4;
 constexpr int kMaxChunks = kResidentMaxKeys / 32;
 
 // kLong: heads with more than 192 keys (S and O overlap in TMEM; two CTAs per SM at
-// most by their 256 columns, so the row threads may hold two chunks of weights)
-template <bool kLong>
+// most by their 256 columns, so the row threads may hold two chunks of weights).
+// kLse: the launch writes each row's log-sum-exp (compiled apart, so that the
+// launches without it carry none of its arithmetic).
+template <bool kLong, bool kLse>
 __global__ void __launch_bounds__(kThreads, kLong ? 2 : 4)
 attn_resident_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k64,
                      const __grid_constant__ CUtensorMap tm_k16, const __grid_constant__ CUtensorMap tm_v64,
@@ -381,7 +370,7 @@ attn_resident_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         const int c_hi = warp_live ? (__reduce_max_sync(0xffffffffu, hi) + 31) / 32 : 0;
         const int c_lo = warp_live ? max(0, __reduce_min_sync(0xffffffffu, lo)) / 32 : 0;
         const int hi_min = __reduce_min_sync(0xffffffffu, hi), lo_max = __reduce_max_sync(0xffffffffu, lo);
-        const bool want_lse = p.lse != nullptr;
+        constexpr bool want_lse = kLse;
         float mraw = -CUDART_INF_F;
         float acc[4] = {0.f, 0.f, 0.f, 0.f}; // rounded weights: the output's divisor
         uint64_t accx = f2(0.f, 0.f);        // weights before rounding: the log-sum-exp
@@ -417,7 +406,8 @@ attn_resident_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 tmem_wait_ld();
                 reg_fence32(r);
                 const bool mk = !(32 * ch >= lo_max && 32 * ch + 32 <= hi_min);
-                chunk_weights_any(mk, want_lse, r, lo - 32 * ch, hi - 32 * ch, mul2, sub2, pk, acc, accx);
+                if (mk) chunk_weights<true, kLse>(r, lo - 32 * ch, hi - 32 * ch, mul2, sub2, pk, acc, accx);
+                else chunk_weights<false, kLse>(r, lo - 32 * ch, hi - 32 * ch, mul2, sub2, pk, acc, accx);
             } else {
 #pragma unroll
                 for (int e2 = 0; e2 < 16; ++e2) pk[e2] = 0u;
@@ -531,13 +521,17 @@ cudaError_t launch_resident(const Problem &pb, cudaStream_t stream, const Reside
         std::lock_guard<std::mutex> lock(mu);
         DeviceInfo &di = infos[dev];
         if (!di.configured) {
-            if ((e = cudaFuncSetAttribute(reinterpret_cast<const void *>(attn_resident_kernel<false>),
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          static_cast<int>(smem_bytes(kShortKeys)))) != cudaSuccess ||
-                (e = cudaFuncSetAttribute(reinterpret_cast<const void *>(attn_resident_kernel<true>),
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          static_cast<int>(smem_bytes(kResidentMaxKeys)))) != cudaSuccess)
-                return e;
+            const struct {
+                const void *fn;
+                size_t bytes;
+            } fns[4] = {{reinterpret_cast<const void *>(attn_resident_kernel<false, false>), smem_bytes(kShortKeys)},
+                        {reinterpret_cast<const void *>(attn_resident_kernel<false, true>), smem_bytes(kShortKeys)},
+                        {reinterpret_cast<const void *>(attn_resident_kernel<true, false>), smem_bytes(kResidentMaxKeys)},
+                        {reinterpret_cast<const void *>(attn_resident_kernel<true, true>), smem_bytes(kResidentMaxKeys)}};
+            for (const auto &f : fns)
+                if ((e = cudaFuncSetAttribute(f.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              static_cast<int>(f.bytes))) != cudaSuccess)
+                    return e;
             di.configured = true;
         }
     }
@@ -577,8 +571,10 @@ cudaError_t launch_resident(const Problem &pb, cudaStream_t stream, const Reside
     cfg.attrs = attr;
     cfg.numAttrs = pb.overlap_launch ? 1 : 0;
     if (kv_cap > kShortKeys)
-        return cudaLaunchKernelEx(&cfg, attn_resident_kernel<true>, tq, tk64, tk16, tv64, tv16, to32, p);
-    return cudaLaunchKernelEx(&cfg, attn_resident_kernel<false>, tq, tk64, tk16, tv64, tv16, to32, p);
+        return p.lse ? cudaLaunchKernelEx(&cfg, attn_resident_kernel<true, true>, tq, tk64, tk16, tv64, tv16, to32, p)
+                     : cudaLaunchKernelEx(&cfg, attn_resident_kernel<true, false>, tq, tk64, tk16, tv64, tv16, to32, p);
+    return p.lse ? cudaLaunchKernelEx(&cfg, attn_resident_kernel<false, true>, tq, tk64, tk16, tv64, tv16, to32, p)
+                 : cudaLaunchKernelEx(&cfg, attn_resident_kernel<false, false>, tq, tk64, tk16, tv64, tv16, to32, p);
 }
 
 cudaError_t resident_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint32_t *info)
