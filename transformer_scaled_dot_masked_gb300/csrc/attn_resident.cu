@@ -153,8 +153,8 @@ __device__ __forceinline__ void tmem_ld32_max(uint32_t taddr, uint32_t (&r)[32],
 
 // Row maximum of one 32-key chunk of raw scores.  kMask: only columns e of the chunk
 // with lo_rel <= e < hi_rel count (a chunk that is allowed whole for every row of the
-// warp skips the test).
-template <bool kMask>
+// warp skips the test); kLo: the lower bound applies (a window), else lo_rel <= 0.
+template <bool kMask, bool kLo>
 __device__ __forceinline__ float chunk_max(const uint32_t (&r)[32], int lo_rel, int hi_rel)
 {
     if (!kMask) {
@@ -170,7 +170,7 @@ __device__ __forceinline__ float chunk_max(const uint32_t (&r)[32], int lo_rel, 
     float m4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
-        const float y = e < hi_rel && e >= lo_rel ? __uint_as_float(r[e]) : -CUDART_INF_F;
+        const float y = e < hi_rel && (!kLo || e >= lo_rel) ? __uint_as_float(r[e]) : -CUDART_INF_F;
         m4[e & 3] = fmaxf(m4[e & 3], y);
     }
     return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
@@ -186,9 +186,9 @@ __device__ __forceinline__ void add_bf16_pair(float &acc0, float &acc1, uint32_t
 }
 
 // Weights exp2(S * scale * log2 e - mx) of one 32-key chunk as bf16 pairs (zero outside
-// [lo_rel, hi_rel) when kMask); adds the rounded weights to acc and, when kLse, the
-// unrounded ones to accx.
-template <bool kMask, bool kLse>
+// [lo_rel, hi_rel) when kMask; kLo as for chunk_max); adds the rounded weights to acc
+// and, when kLse, the unrounded ones to accx.
+template <bool kMask, bool kLse, bool kLo>
 __device__ __forceinline__ void chunk_weights(const uint32_t (&r)[32], int lo_rel, int hi_rel, uint64_t mul2,
                                               uint64_t sub2, uint32_t (&pk)[16], float (&acc)[4], uint64_t &accx)
 {
@@ -197,8 +197,8 @@ __device__ __forceinline__ void chunk_weights(const uint32_t (&r)[32], int lo_re
         float a0, a1;
         unf2(fma2(f2(__uint_as_float(r[2 * e2]), __uint_as_float(r[2 * e2 + 1])), mul2, sub2), a0, a1);
         if (kMask) {
-            a0 = 2 * e2 < hi_rel && 2 * e2 >= lo_rel ? a0 : -CUDART_INF_F;
-            a1 = 2 * e2 + 1 < hi_rel && 2 * e2 + 1 >= lo_rel ? a1 : -CUDART_INF_F;
+            a0 = 2 * e2 < hi_rel && (!kLo || 2 * e2 >= lo_rel) ? a0 : -CUDART_INF_F;
+            a1 = 2 * e2 + 1 < hi_rel && (!kLo || 2 * e2 + 1 >= lo_rel) ? a1 : -CUDART_INF_F;
         }
         const float e0 = ex2(a0), e1 = ex2(a1);
         if (kLse) accx = add2(accx, f2(e0, e1));
@@ -216,9 +216,10 @@ constexpr int kMaxChunks = kResidentMaxKeys / 32;
 
 // kLong: heads with more than 192 keys (S and O overlap in TMEM; two CTAs per SM at
 // most by their 256 columns, so the row threads may hold two chunks of weights).
-// kLse: the launch writes each row's log-sum-exp (compiled apart, so that the
-// launches without it carry none of its arithmetic).
-template <bool kLong, bool kLse>
+// kLse: the launch writes each row's log-sum-exp; kWin: the launch has a restricted-
+// attention window (each compiled apart, so that the launches without them carry none
+// of their arithmetic).
+template <bool kLong, bool kLse, bool kWin>
 __global__ void __launch_bounds__(kThreads, kLong ? 2 : 4)
 attn_resident_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k64,
                      const __grid_constant__ CUtensorMap tm_k16, const __grid_constant__ CUtensorMap tm_v64,
@@ -273,7 +274,7 @@ attn_resident_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     }
     const bool causal = (p.mask_kind & kMaskCausal) != 0;
     int need = causal ? min(len, q0 + rows) : len; // keys some row of the tile may see
-    if (p.window >= 0) need = min(need, q0 + rows + p.window);
+    if (kWin) need = min(need, q0 + rows + p.window);
     // key rows loaded and multiplied: whole 16-row boxes, at least one (an empty head
     // still runs the same steps on a box of real, finite keys and writes zeros)
     const int kv_rows = max(kKeyBox, (need + kKeyBox - 1) / kKeyBox * kKeyBox);
@@ -355,7 +356,7 @@ attn_resident_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         const uint32_t t_row = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         int hi = causal ? min(len, row + 1) : len;
         int lo = 0;
-        if (p.window >= 0) {
+        if (kWin) {
             hi = min(hi, row + p.window + 1);
             lo = row - p.window;
         }
@@ -368,8 +369,8 @@ attn_resident_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         // chunks [c_lo, c_hi) hold an allowed key of some row of this warp; a chunk inside
         // [lo_max, hi_min) is allowed whole for every row of it (no mask arithmetic)
         const int c_hi = warp_live ? (__reduce_max_sync(0xffffffffu, hi) + 31) / 32 : 0;
-        const int c_lo = warp_live ? max(0, __reduce_min_sync(0xffffffffu, lo)) / 32 : 0;
-        const int hi_min = __reduce_min_sync(0xffffffffu, hi), lo_max = __reduce_max_sync(0xffffffffu, lo);
+        const int c_lo = kWin && warp_live ? max(0, __reduce_min_sync(0xffffffffu, lo)) / 32 : 0;
+        const int hi_min = __reduce_min_sync(0xffffffffu, hi), lo_max = kWin ? __reduce_max_sync(0xffffffffu, lo) : 0;
         constexpr bool want_lse = kLse;
         float mraw = -CUDART_INF_F;
         float acc[4] = {0.f, 0.f, 0.f, 0.f}; // rounded weights: the output's divisor
@@ -388,7 +389,7 @@ attn_resident_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 asm volatile("" : "+f"(cm)::"memory"); // cm is read after the wait
                 if (!(32 * ch >= lo_max && 32 * ch + 32 <= hi_min)) {
                     reg_fence32(r);
-                    cm = chunk_max<true>(r, lo - 32 * ch, hi - 32 * ch);
+                    cm = chunk_max<true, kWin>(r, lo - 32 * ch, hi - 32 * ch);
                 }
                 mraw = fmaxf(mraw, cm);
             }
@@ -406,8 +407,8 @@ attn_resident_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 tmem_wait_ld();
                 reg_fence32(r);
                 const bool mk = !(32 * ch >= lo_max && 32 * ch + 32 <= hi_min);
-                if (mk) chunk_weights<true, kLse>(r, lo - 32 * ch, hi - 32 * ch, mul2, sub2, pk, acc, accx);
-                else chunk_weights<false, kLse>(r, lo - 32 * ch, hi - 32 * ch, mul2, sub2, pk, acc, accx);
+                if (mk) chunk_weights<true, kLse, kWin>(r, lo - 32 * ch, hi - 32 * ch, mul2, sub2, pk, acc, accx);
+                else chunk_weights<false, kLse, kWin>(r, lo - 32 * ch, hi - 32 * ch, mul2, sub2, pk, acc, accx);
             } else {
 #pragma unroll
                 for (int e2 = 0; e2 < 16; ++e2) pk[e2] = 0u;
@@ -502,6 +503,12 @@ struct DeviceInfo {
     bool configured = false;
 };
 
+template <bool kLong, bool kLse, bool kWin>
+const void *variant_fn()
+{
+    return reinterpret_cast<const void *>(attn_resident_kernel<kLong, kLse, kWin>);
+}
+
 size_t smem_bytes(int kv_cap) { return 1024 + kQBytes + 2u * kv_cap * (kD * 2) + sizeof(Ctl); }
 
 } // namespace
@@ -524,10 +531,14 @@ cudaError_t launch_resident(const Problem &pb, cudaStream_t stream, const Reside
             const struct {
                 const void *fn;
                 size_t bytes;
-            } fns[4] = {{reinterpret_cast<const void *>(attn_resident_kernel<false, false>), smem_bytes(kShortKeys)},
-                        {reinterpret_cast<const void *>(attn_resident_kernel<false, true>), smem_bytes(kShortKeys)},
-                        {reinterpret_cast<const void *>(attn_resident_kernel<true, false>), smem_bytes(kResidentMaxKeys)},
-                        {reinterpret_cast<const void *>(attn_resident_kernel<true, true>), smem_bytes(kResidentMaxKeys)}};
+            } fns[8] = {{variant_fn<false, false, false>(), smem_bytes(kShortKeys)},
+                        {variant_fn<false, false, true>(), smem_bytes(kShortKeys)},
+                        {variant_fn<false, true, false>(), smem_bytes(kShortKeys)},
+                        {variant_fn<false, true, true>(), smem_bytes(kShortKeys)},
+                        {variant_fn<true, false, false>(), smem_bytes(kResidentMaxKeys)},
+                        {variant_fn<true, false, true>(), smem_bytes(kResidentMaxKeys)},
+                        {variant_fn<true, true, false>(), smem_bytes(kResidentMaxKeys)},
+                        {variant_fn<true, true, true>(), smem_bytes(kResidentMaxKeys)}};
             for (const auto &f : fns)
                 if ((e = cudaFuncSetAttribute(f.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               static_cast<int>(f.bytes))) != cudaSuccess)
@@ -570,11 +581,12 @@ cudaError_t launch_resident(const Problem &pb, cudaStream_t stream, const Reside
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pb.overlap_launch ? 1 : 0;
-    if (kv_cap > kShortKeys)
-        return p.lse ? cudaLaunchKernelEx(&cfg, attn_resident_kernel<true, true>, tq, tk64, tk16, tv64, tv16, to32, p)
-                     : cudaLaunchKernelEx(&cfg, attn_resident_kernel<true, false>, tq, tk64, tk16, tv64, tv16, to32, p);
-    return p.lse ? cudaLaunchKernelEx(&cfg, attn_resident_kernel<false, true>, tq, tk64, tk16, tv64, tv16, to32, p)
-                 : cudaLaunchKernelEx(&cfg, attn_resident_kernel<false, false>, tq, tk64, tk16, tv64, tv16, to32, p);
+    const void *fn = kv_cap > kShortKeys ? (p.lse ? (p.window >= 0 ? variant_fn<true, true, true>() : variant_fn<true, true, false>())
+                                                  : (p.window >= 0 ? variant_fn<true, false, true>() : variant_fn<true, false, false>()))
+                                         : (p.lse ? (p.window >= 0 ? variant_fn<false, true, true>() : variant_fn<false, true, false>())
+                                                  : (p.window >= 0 ? variant_fn<false, false, true>() : variant_fn<false, false, false>()));
+    void *args[] = {&tq, &tk64, &tk16, &tv64, &tv16, &to32, &p};
+    return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 cudaError_t resident_status_read_and_clear(cudaStream_t stream, uint32_t *code, uint32_t *info)
