@@ -452,8 +452,9 @@ attn_status attn_device_status(void *stream, int32_t *info);
  * Test hook of the failure detection (not part of the operation; no page of the
  * method has a counterpart).  Runs the whole-head-resident kernel of attn_fwd on
  * these arguments with every bounded wait limited to wait_ns nanoseconds and with
- * one row thread withholding its report that its first chunk of weights is stored,
- * so the MMA-issuing thread's wait for that chunk runs out: the kernel records the
+ * the barrier on which the rows report their first chunk of weights stored waiting
+ * for one report more than they make (one arrival withheld), so the MMA-issuing
+ * thread's wait for that chunk runs out: the kernel records the
  * time-out (attn_device_status then returns ATTN_ERR_DEVICE_TIMEOUT with info 403,
  * the weights wait of that kernel), waits for its own copies and MMAs, frees its
  * TMEM and exits without writing `out`.  The CUDA context stays usable.  It lets a

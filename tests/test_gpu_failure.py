@@ -4,8 +4,9 @@ Every mbarrier wait of the tensor-core kernels gives up after a time limit, reco
 the time-out in a device status word, lets the kernel drain its own copies and MMAs,
 free its TMEM and exit, and leaves the CUDA context usable.  The test hook
 attn_test_withheld_arrival runs the whole-head-resident kernel with a 20 ms limit and
-one row thread that never reports its chunks of weights, so the MMA issuer's wait for
-the first chunk runs out (no other wait can: each completes in microseconds).  Its
+the barrier of the first chunk of weights waiting for one arrival more than the row
+threads make, so the MMA issuer's wait for that chunk runs out (no other wait can:
+each completes in microseconds).  Its
 long-key variant (above 192 keys, the held chunks) and query tiles are covered too.
 """
 import numpy as np

@@ -94,7 +94,8 @@ struct ResidentParams {
     int kv_cap;                 // key rows the K and V buffers hold: n rounded up to kKeyBox
     float scale_log2;
     uint64_t wait_ns;           // limit of every bounded wait
-    int withhold_p_arrival;     // test hook: the last row thread does not report its first chunk
+    int withhold_p_arrival;     // test hook: the first chunk's barrier waits for one arrival more
+                                // than the row threads make, so the MMA issuer's wait runs out
 };
 
 __device__ __forceinline__ bool give_up(int *abort_flag, uint64_t start, uint64_t limit_ns, uint32_t site)
@@ -243,7 +244,8 @@ attn_resident_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         mbar_init(&c.qk_full, 1);
         mbar_init(&c.v_full, 1);
         mbar_init(&c.s_full, 1);
-        for (int ch = 0; ch < kMaxChunks; ++ch) mbar_init(&c.p_full[ch], kRowThreads);
+        for (int ch = 0; ch < kMaxChunks; ++ch)
+            mbar_init(&c.p_full[ch], kRowThreads + (ch == 0 && p.withhold_p_arrival ? 1 : 0));
         mbar_init(&c.o_full, 1);
         mbar_init(&c.drain, 1);
         c.abort_flag = 0;
@@ -437,7 +439,7 @@ attn_resident_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 tmem_wait_st();
             }
             tc_fence_before();
-            if (!(p.withhold_p_arrival && tid == kRowThreads - 1)) mbar_arrive(&c.p_full[ch]);
+            mbar_arrive(&c.p_full[ch]);
         }
         const float l = (acc[0] + acc[1]) + (acc[2] + acc[3]);
         float s0, s1;

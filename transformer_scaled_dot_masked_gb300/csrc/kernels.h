@@ -127,8 +127,9 @@ cudaError_t flash_status_read_and_clear(cudaStream_t stream, uint32_t *code, uin
 // (everything it reads or writes follows the dependency wait).
 constexpr int kResidentMaxKeys = 256;
 bool resident_fits(int m, int n, int d);
-// Test hook of the bounded waits: a short wait limit, and the last thread withholding
-// its arrival on the weights barrier, so that the MMA issuer's wait runs out.
+// Test hook of the bounded waits: a short wait limit, and the barrier on which the rows
+// hand over their first chunk of weights waiting for one arrival more than they make,
+// so that the MMA issuer's wait runs out.
 struct ResidentTestHook {
     uint64_t wait_ns;
     int withhold_p_arrival;
