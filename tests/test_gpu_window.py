@@ -47,6 +47,11 @@ CASES = [
     ("resident_w64_causal", "bf16", 4, 2, 128, MASK_CAUSAL, 64, None),
     ("resident_w0_causal_padding", "bf16", 3, 2, 128, MASK_CAUSAL | MASK_KEY_PADDING, 0, (0, 128)),
     ("resident_w40_m33", "bf16", 2, 3, 33, 0, 40, None),
+    # the resident kernel's variant above 192 keys (O over the last S chunks, held
+    # weights) with a window: two query tiles per head
+    ("resident_long_w50_padding", "bf16", 2, 3, 256, MASK_KEY_PADDING, 50, (100, 256)),
+    ("resident_long_w0_causal", "bf16", 2, 2, 224, MASK_CAUSAL, 0, None),
+    ("resident_long_w130", "bf16", 2, 2, 250, 0, 130, None),
     ("fp32_w7", "fp32", 2, 2, 150, MASK_KEY_PADDING, 7, (1, 150)),
     ("narrow_heads_w3", "bf16_d32", 2, 2, 90, MASK_CAUSAL, 3, None),
     ("narrow_heads_pair_mode_w17", "bf16_d16", 2, 2, 300, MASK_KEY_PADDING, 17, (0, 300)),
